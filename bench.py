@@ -1,0 +1,466 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized decode GEMV/GEMM: achieved GB/s and fraction of the HBM roofline.
+
+Default workload (one "step" = one decode token through every linear of an 8B-shaped decoder):
+32 layers x {q 4096x4096, k 1024x4096, v 1024x4096, o 4096x4096, gate 14336x4096,
+up 14336x4096, down 4096x14336}, M = 1, asymmetric INT4 (uint4 codes, fp16 scale, 4-bit
+zero, group 128).  Weights are drawn N(0, 0.02) with 0.1 % outliers x20 on the GPU (seeded),
+quantized by the library's GPU quantizer and packed once (untimed); x is bf16 N(0, 1), a fresh
+row per linear.  The 224 uq_gemm calls of a step are captured in one CUDA graph.  The packed
+weights (3.6 GB) exceed L2 (~129 MB), so no flush is needed between steps.
+
+Metric: algorithmic bytes (packed codes + scales + zeros + x + y, each once) per second.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl uq|reference] [--workload NAME] [--m M]
+
+Under torchrun each rank runs an independent replica on its own GPU (the path has no
+exchange step); value = bytes of all ranks / max-over-ranks time ("weak" scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "quantized decode GEMV/GEMM GB/s and % of HBM roofline vs M (1 GB300)"
+FALLBACK_HBM_GBS = 6800.0
+
+# (fmt, group, sigma, outlier_p, layers, linears, default M)
+_L8 = [("q", 4096, 4096), ("k", 1024, 4096), ("v", 1024, 4096), ("o", 4096, 4096),
+       ("gate", 14336, 4096), ("up", 14336, 4096), ("down", 4096, 14336)]
+_L70 = [("q", 8192, 8192), ("k", 1024, 8192), ("v", 1024, 8192), ("o", 8192, 8192),
+        ("gate", 28672, 8192), ("up", 28672, 8192), ("down", 8192, 28672)]
+WORKLOADS = {
+    "llama8b-int4a-decode": dict(fmt="INT4_ASYM", group=128, sigma=0.02, outlier_p=0.001, layers=32,
+                                 linears=_L8, m=1,
+                                 title="8B-shaped decode linears (32 layers x q,k,v,o,gate,up,down), "
+                                       "INT4 asym g128, 0.1% outliers x20"),
+    "sweep-int4a": dict(fmt="INT4_ASYM", group=128, sigma=0.02, outlier_p=0.0, layers=48,
+                        linears=[("gate", 14336, 4096), ("down", 4096, 14336)], m=1,
+                        title="batched decode sweep: 14336x4096 and 4096x14336, INT4 asym g128"),
+    "int8s-8192": dict(fmt="INT8_SYM", group=128, sigma=0.02, outlier_p=0.0, layers=40,
+                       linears=[("w", 8192, 8192)], m=1, title="8192x8192 INT8 sym g128"),
+    "int2a-8192": dict(fmt="INT2_ASYM", group=64, sigma=0.02, outlier_p=0.0, layers=100,
+                       linears=[("w", 8192, 8192)], m=1, title="8192x8192 INT2 asym g64"),
+    "nf4-8192": dict(fmt="NF4", group=64, sigma=0.02, outlier_p=0.0, layers=60,
+                     linears=[("w", 8192, 8192)], m=1, title="8192x8192 NF4 g64"),
+    "k4-70b-stack": dict(fmt="K4", group=256, sigma=0.015, outlier_p=0.0, layers=8, linears=_L70, m=1,
+                         title="70B-shaped decode linear stack (8 layers x 7), two-level INT4"),
+}
+BITS = {"INT4_SYM": 4, "INT4_ASYM": 4, "INT8_SYM": 8, "INT2_ASYM": 2, "NF4": 4, "K4": 4}
+
+
+def alg_bytes(fmt, group, N, K, M):
+    """Algorithmic bytes of one linear: codes + metadata + x + y, each moved once."""
+    codes = N * K * BITS[fmt] // 8
+    if fmt == "K4":
+        meta = N * (K // 256) * 16
+    else:
+        G = K // group
+        meta = N * G * 2
+        if fmt == "INT4_ASYM":
+            meta += N * ((G + 1) // 2)
+        elif fmt == "INT2_ASYM":
+            meta += N * G * 2
+        elif fmt == "NF4":
+            meta += 64
+    return codes + meta + 2 * M * K + 2 * M * N
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "gemm_uq_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        if name.startswith("uq_gemv") or name == "uq_common.cuh":
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel."""
+    path = os.path.join(ROOT, "profiles", f"gemv_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            for key in ("hbm_gbs", "hbm_GBs", "hbm"):
+                if key in d:
+                    return float(d[key]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            self.proc.wait(timeout=5)
+
+    def summary(self):
+        self.f.flush()
+        rows = []
+        with open(self.f.name) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------------------------
+def build_weights(spec, m, dev, seed_base=12345):
+    """Quantize and pack every linear of the workload on the GPU; returns per-linear records."""
+    import torch
+    import gemm_uq_gb300 as uq
+    fmt, group = spec["fmt"], spec["group"]
+    gen = torch.Generator(device=dev)
+    recs = []
+    cb = None
+    if fmt == "NF4":
+        import numpy as np
+        cb = torch.from_numpy(np.loadtxt(os.path.join(ROOT, "tests", "golden", "nf4_codebook.txt"),
+                                         dtype=np.float64).astype(np.float32)).to(dev)
+    idx = 0
+    for layer in range(spec["layers"]):
+        for name, N, K in spec["linears"]:
+            gen.manual_seed(seed_base + idx)
+            w = torch.randn((N, K), generator=gen, device=dev, dtype=torch.float32) * spec["sigma"]
+            if spec["outlier_p"] > 0:
+                mask = torch.rand((N, K), generator=gen, device=dev) < spec["outlier_p"]
+                w = torch.where(mask, w * 20.0, w)
+                del mask
+            if fmt == "K4":
+                codes, d, dmin, sc, mm = uq.quantize_k4(w)
+                scales = uq.pack_kmeta(d, dmin, sc, mm)
+                zc = None
+                del d, dmin, sc, mm
+            else:
+                codes, scales, zeros = uq.quantize(w, group, fmt, codebook=cb)
+                zc = uq.pack_zeros(zeros) if fmt == "INT4_ASYM" else (zeros if fmt == "INT2_ASYM" else cb)
+            del w
+            wq = uq.pack_layout(codes, group, fmt)
+            del codes
+            recs.append(dict(name=f"L{layer}.{name}", N=N, K=K, wq=wq, scales=scales, zc=zc))
+            idx += 1
+    torch.cuda.synchronize()
+    return recs
+
+
+def run_uq(args, rank, world, dist):
+    import torch
+    import gemm_uq_gb300 as uq
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    spec = WORKLOADS[args.workload]
+    fmt, group = spec["fmt"], spec["group"]
+    M = args.m if args.m else spec["m"]
+    recs = build_weights(spec, M, dev)
+
+    # x for every linear lives in one device buffer (so the e2e leg copies it with one memcpy)
+    x_sizes = [M * r["K"] for r in recs]
+    y_sizes = [M * r["N"] for r in recs]
+    xbuf = torch.empty(sum(x_sizes), dtype=torch.bfloat16, device=dev)
+    ybuf = torch.empty(sum(y_sizes), dtype=torch.bfloat16, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(777 + rank)
+    xbuf.copy_(torch.randn(xbuf.numel(), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16))
+    ox = oy = 0
+    for r, xs, ys in zip(recs, x_sizes, y_sizes):
+        r["x"], r["y"] = xbuf[ox:ox + xs], ybuf[oy:oy + ys]
+        ox += xs
+        oy += ys
+    step_bytes = sum(alg_bytes(fmt, group, r["N"], r["K"], M) for r in recs)
+
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+
+    def issue(events=None):
+        for i, r in enumerate(recs):
+            if events is not None:
+                events[i][0].record(stream)
+            uq.gemm_ptrs(r["x"].data_ptr(), r["wq"].data_ptr(), r["scales"].data_ptr(),
+                         r["zc"].data_ptr() if r["zc"] is not None else 0, r["y"].data_ptr(),
+                         M, r["N"], r["K"], group, fmt, sh)
+            if events is not None:
+                events[i][1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            issue()                        # grows the per-stream workspace outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        issue()
+    torch.cuda.synchronize()
+
+    def replay(n):
+        with torch.cuda.stream(stream):
+            for _ in range(n):
+                graph.replay()
+
+    replay(args.warmup)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        t_start.record(stream)
+        replay(args.steps)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = t_start.elapsed_time(t_end)
+    clocks = clk.summary()
+
+    # end to end through the public API: H2D of every x, the step, D2H of every y, each step
+    xh = torch.empty(xbuf.numel(), dtype=torch.bfloat16, pin_memory=True)
+    yh = torch.empty(ybuf.numel(), dtype=torch.bfloat16, pin_memory=True)
+    xh.copy_(xbuf.cpu())
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            xbuf.copy_(xh, non_blocking=True)
+            graph.replay()
+            yh.copy_(ybuf, non_blocking=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            xbuf.copy_(xh, non_blocking=True)
+            graph.replay()
+            yh.copy_(ybuf, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+
+    # per-kernel durations: a second graph with an event pair around every launch
+    kern_ms = None
+    try:
+        evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in recs]
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=stream):
+            issue(evs)
+        totals = []
+        for _ in range(3):
+            with torch.cuda.stream(stream):
+                g2.replay()
+            torch.cuda.synchronize()
+            totals.append(sum(a.elapsed_time(b) for a, b in evs))
+        kern_ms = statistics.median(totals)
+        kern_src = "events around each launch inside a replayed graph"
+    except Exception:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in recs]
+        totals = []
+        for _ in range(3):
+            with torch.cuda.stream(stream):
+                issue(evs)
+            torch.cuda.synchronize()
+            totals.append(sum(a.elapsed_time(b) for a, b in evs))
+        kern_ms = statistics.median(totals)
+        kern_src = "events around each eager launch"
+
+    if dist:
+        t = torch.tensor([ms, e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        return
+
+    launches = len(recs)
+    total_bytes = step_bytes * args.steps * world
+    value = total_bytes / (ms * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+    achieved = step_bytes / (kern_ms * 1e-3) / 1e9
+    traffic = read_traffic(args.workload) if M == spec["m"] else None
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x int4 -> fp32 acc" if BITS[fmt] == 4 else
+        f"bf16 x {fmt.lower()} -> fp32 acc",
+        "data": "synthetic (seeded N(0,sigma) weights quantized on the GPU; bf16 N(0,1) x)",
+        "config": {"workload": args.workload, "description": spec["title"], "fmt": fmt, "group": group, "M": M,
+                   "linears_per_step": launches, "bytes_per_step": step_bytes,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "no flush: packed weights per step exceed L2 (%.2f GB)" % (step_bytes / 1e9),
+                   "launch": "one CUDA graph per step"},
+        "gpu_launches": launches * args.steps,
+        "e2e": {"value": round(step_bytes * args.steps * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": xbuf.numel() * 2, "d2h_bytes_per_step": ybuf.numel() * 2},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} HBM copy bandwidth",
+                     "traffic": traffic, "kernel": f"gemv_kernel<{fmt},{min(M, 8)}>",
+                     "kernel_ms_per_step": round(kern_ms, 4), "timing": kern_src},
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(spec, M)
+    print(json.dumps(out), flush=True)
+
+
+# ---------------------------------------------------------------------------------------------
+def _oracle_sample(spec, M, rows_per_linear):
+    """Oracle inputs for a bounded sample: the first rows of one layer's linears (quantized untimed)."""
+    import numpy as np
+    from oracle import quant as oquant
+    from oracle.nf4 import nf4_codebook
+    from synth import activations, normal_weights
+    cb = nf4_codebook() if spec["fmt"] == "NF4" else None
+    items = []
+    for i, (name, N, K) in enumerate(spec["linears"]):
+        n = min(N, rows_per_linear)
+        w = normal_weights(9000 + i, n, K, spec["sigma"], outlier_p=spec["outlier_p"], outlier_mult=20.0)
+        qz = oquant.quantize(w, spec["fmt"], spec["group"], codebook=cb)
+        x = activations(9000 + i, M, K)
+        items.append((qz, x, alg_bytes(spec["fmt"], spec["group"], n, K, M)))
+    return items
+
+
+def _oracle_pass(items):
+    from oracle import gemm as ogemm
+    for qz, x, _ in items:
+        ogemm.quantized_gemm(x, qz)
+
+
+def cpu_baseline(spec, M, target_s=10.0, rows_per_linear=512):
+    items = _oracle_sample(spec, M, rows_per_linear)
+    nbytes = sum(b for _, _, b in items)
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        _oracle_pass(items)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= target_s or el > 30.0:
+            break
+    return {"value": round(nbytes * passes / el / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"first {rows_per_linear} rows of each of the {len(items)} linears of one layer, M={M}, "
+                      f"{passes} passes of the float64 dequantize-then-matmul ({el:.1f} s)"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    spec = WORKLOADS[args.workload]
+    M = args.m if args.m else spec["m"]
+    items = _oracle_sample(spec, M, rows_per_linear=256)
+    nbytes = sum(b for _, _, b in items)
+    for _ in range(args.warmup):
+        _oracle_pass(items)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_pass(items)
+    el = time.perf_counter() - t0
+    value = nbytes * args.steps / el / 1e9
+    sample = f"first 256 rows of each of the {len(items)} linears of one layer, M={M} (float64 oracle)"
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "config": {"workload": args.workload, "description": spec["title"],
+                                           "fmt": spec["fmt"], "group": spec["group"], "M": M},
+           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["uq", "reference"], default="uq")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama8b-int4a-decode")
+    ap.add_argument("--m", type=int, default=0, help="override the batch rows M")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    try:
+        run_uq(args, rank, world, dist)
+    finally:
+        if dist:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

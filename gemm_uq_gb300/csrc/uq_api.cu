@@ -1,0 +1,381 @@
+// uq_api.cu -- the C ABI (include/uq.h): argument validation, path choice, workspace, launches.
+//
+// Host-side only.  Every entry point validates its arguments and returns a status; nothing
+// throws across the ABI and nothing falls back to another implementation: a request the
+// kernels do not implement is refused with UQ_ERR_UNSUPPORTED.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+
+#include "uq_kernels.h"
+
+namespace {
+
+thread_local std::string g_last_error = "";
+
+uq_status fail(uq_status s, const char* fmt_msg, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt_msg);
+    vsnprintf(buf, sizeof buf, fmt_msg, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+uq_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(UQ_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_fmt(int fmt) { return fmt >= UQ_INT4_SYM && fmt <= UQ_K4; }
+
+// shape rules shared by every call that takes (N, K, group, fmt)
+uq_status check_shape(int N, int K, int group, int fmt) {
+    if (!valid_fmt(fmt)) return fail(UQ_ERR_INVALID, "unknown format %d", fmt);
+    if (N < 0 || K < 0) return fail(UQ_ERR_INVALID, "negative size N=%d K=%d", N, K);
+    if (fmt == UQ_K4) {
+        if (group != 256) return fail(UQ_ERR_UNSUPPORTED, "UQ_K4 needs group 256 (got %d)", group);
+        if (K % 256) return fail(UQ_ERR_INVALID, "UQ_K4 needs K %% 256 == 0 (K=%d)", K);
+        return UQ_OK;
+    }
+    if (group != 32 && group != 64 && group != 128)
+        return fail(UQ_ERR_UNSUPPORTED, "group must be 32, 64 or 128 (got %d)", group);
+    if (K % group) return fail(UQ_ERR_INVALID, "K=%d is not a multiple of group %d", K, group);
+    if (fmt == UQ_INT2_ASYM && (K % 64))
+        return fail(UQ_ERR_UNSUPPORTED, "UQ_INT2_ASYM needs K %% 64 == 0 (K=%d)", K);
+    return UQ_OK;
+}
+
+size_t meta_scales_bytes(int N, int K, int group, int fmt) {
+    if (fmt == UQ_K4) return (size_t)N * (K / 256) * 16;
+    return (size_t)N * (K / group) * 2;
+}
+size_t meta_zeros_bytes(int N, int K, int group, int fmt) {
+    if (fmt == UQ_INT4_ASYM) return (size_t)N * ((K / group + 1) / 2);
+    if (fmt == UQ_INT2_ASYM) return (size_t)N * (K / group) * 2;
+    if (fmt == UQ_NF4) return 64;
+    return 0;
+}
+bool needs_zc(int fmt) { return fmt == UQ_INT4_ASYM || fmt == UQ_INT2_ASYM || fmt == UQ_NF4; }
+
+// ---------------------------------------------------------------------------------------------
+// per-device state: SM count and two device words (fault flag, pack range violations)
+struct DeviceState {
+    int sms = 0;
+    unsigned int* words = nullptr;   // [0] fault, [1] bad-code counter
+};
+std::mutex g_mu;
+std::map<int, DeviceState> g_dev;
+
+// per (device, stream) workspace for the split-K partial sums and the row-block tickets
+struct Workspace {
+    float* partials = nullptr;
+    size_t partial_bytes = 0;
+    unsigned int* tickets = nullptr;   // zero between calls (the kernels reset what they use)
+    size_t ticket_bytes = 0;
+};
+std::map<std::pair<int, void*>, Workspace> g_ws;
+
+uq_status device_state(DeviceState** out, int* dev_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.words) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (major != 10 || minor != 3)
+            return fail(UQ_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev,
+                        major, minor);
+        e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        e = cudaMalloc(&d.words, 256);
+        if (e != cudaSuccess) return fail(UQ_ERR_NOMEM, "cudaMalloc of device words failed");
+        e = cudaMemset(d.words, 0, 256);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+    }
+    *out = &d;
+    if (dev_out) *dev_out = dev;
+    return UQ_OK;
+}
+
+uq_status grow(void** ptr, size_t* have, size_t need, bool zero, cudaStream_t st) {
+    if (*have >= need) return UQ_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    if (cs != cudaStreamCaptureStatusNone)
+        return fail(UQ_ERR_NOMEM, "workspace must grow to %zu bytes but the stream is being captured; "
+                                  "make one call of this size before capturing", need);
+    size_t bytes = *have ? *have : 4096;
+    while (bytes < need) bytes *= 2;
+    if (*ptr) {
+        e = cudaStreamSynchronize(st);     // in-flight kernels of this stream may still use the old buffer
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+        cudaFree(*ptr);
+        *ptr = nullptr;
+        *have = 0;
+    }
+    e = cudaMalloc(ptr, bytes);
+    if (e != cudaSuccess) { *ptr = nullptr; return fail(UQ_ERR_NOMEM, "cudaMalloc(%zu) failed", bytes); }
+    if (zero) {
+        e = cudaMemsetAsync(*ptr, 0, bytes, st);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    }
+    *have = bytes;
+    return UQ_OK;
+}
+
+uq_status workspace(int dev, cudaStream_t st, size_t partial_bytes, size_t ticket_bytes, Workspace** out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    Workspace& w = g_ws[{dev, (void*)st}];
+    uq_status s = grow(reinterpret_cast<void**>(&w.partials), &w.partial_bytes, partial_bytes, false, st);
+    if (s != UQ_OK) return s;
+    s = grow(reinterpret_cast<void**>(&w.tickets), &w.ticket_bytes, ticket_bytes, true, st);
+    if (s != UQ_OK) return s;
+    *out = &w;
+    return UQ_OK;
+}
+
+// one GEMV launch for Mb <= 8 rows of x
+uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const void* zc, uint16_t* y,
+                   int Mb, int N, int K, int ldx, int ldy, int group, int fmt, cudaStream_t st,
+                   const DeviceState& ds, int dev) {
+    const uq::Layout L(N, K, fmt);
+    const long long T = (long long)L.NB * L.KB;
+    long long P = (long long)ds.sms * uq::GEMV_WARPS;
+    if (P > T) P = T;
+    Workspace* ws = nullptr;
+    uq_status s = workspace(dev, st, uq::gemv_partials_floats((int)P, Mb) * sizeof(float),
+                            (size_t)L.NB * sizeof(unsigned int), &ws);
+    if (s != UQ_OK) return s;
+    uq::GemvArgs a;
+    a.x = x;
+    a.wq = static_cast<const uint8_t*>(wq);
+    a.scales = static_cast<const uint8_t*>(scales);
+    a.zc = static_cast<const uint8_t*>(zc);
+    a.y = y;
+    a.M = Mb; a.N = N; a.K = K; a.group = group; a.ldx = ldx; a.ldy = ldy;
+    a.NB = L.NB; a.KB = L.KB; a.T = T; a.P = (int)P;
+    a.partials = ws->partials;
+    a.tickets = ws->tickets;
+    a.fault = ds.words;
+    const int grid = (int)((P + uq::GEMV_WARPS - 1) / uq::GEMV_WARPS);
+    cudaError_t e = uq::launch_gemv(fmt, a, grid, st);
+    if (e != cudaSuccess) return cuda_fail(e, "GEMV launch");
+    return UQ_OK;
+}
+
+}  // namespace
+
+// =============================================================================================
+extern "C" {
+
+const char* uq_status_string(uq_status s) {
+    switch (s) {
+        case UQ_OK: return "UQ_OK";
+        case UQ_ERR_INVALID: return "UQ_ERR_INVALID";
+        case UQ_ERR_UNSUPPORTED: return "UQ_ERR_UNSUPPORTED";
+        case UQ_ERR_ALIGN: return "UQ_ERR_ALIGN";
+        case UQ_ERR_CUDA: return "UQ_ERR_CUDA";
+        case UQ_ERR_NOMEM: return "UQ_ERR_NOMEM";
+        default: return "UQ_ERR_UNKNOWN";
+    }
+}
+
+const char* uq_last_error(void) { return g_last_error.c_str(); }
+
+uq_status uq_packed_size(int N, int K, int group, uq_fmt fmt, size_t* wq_bytes, size_t* scales_bytes,
+                         size_t* zeros_bytes) {
+    uq_status s = check_shape(N, K, group, fmt);
+    if (s != UQ_OK) return s;
+    if (wq_bytes) *wq_bytes = (size_t)N * K * uq::fmt_bits(fmt) / 8;
+    if (scales_bytes) *scales_bytes = meta_scales_bytes(N, K, group, fmt);
+    if (zeros_bytes) *zeros_bytes = meta_zeros_bytes(N, K, group, fmt);
+    return UQ_OK;
+}
+
+uq_status uq_pack_layout(const int8_t* codes, void* wq, int N, int K, int group, uq_fmt fmt, void* stream) {
+    uq_status s = check_shape(N, K, group, fmt);
+    if (s != UQ_OK) return s;
+    if ((long long)N * K == 0) return UQ_OK;
+    if (!codes || !wq) return fail(UQ_ERR_INVALID, "null pointer");
+    if (!aligned16(codes) || !aligned16(wq)) return fail(UQ_ERR_ALIGN, "codes and wq must be 16-byte aligned");
+    DeviceState* ds = nullptr;
+    if ((s = device_state(&ds, nullptr)) != UQ_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(ds->words + 1, 0, sizeof(unsigned int), st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    e = uq::launch_pack(fmt, codes, static_cast<uint8_t*>(wq), N, K, ds->words + 1, st);
+    if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+    unsigned int bad = 0;
+    e = cudaMemcpyAsync(&bad, ds->words + 1, sizeof bad, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "pack check");
+    if (bad) return fail(UQ_ERR_INVALID, "%u code words hold a code outside the format's range", bad);
+    return UQ_OK;
+}
+
+uq_status uq_pack_kmeta(const uint16_t* d, const uint16_t* dmin, const uint8_t* sc, const uint8_t* m, void* meta,
+                        int N, int K, void* stream) {
+    uq_status s = check_shape(N, K, 256, UQ_K4);
+    if (s != UQ_OK) return s;
+    const long long count = (long long)N * (K / 256);
+    if (count == 0) return UQ_OK;
+    if (!d || !dmin || !sc || !m || !meta) return fail(UQ_ERR_INVALID, "null pointer");
+    if (!aligned16(d) || !aligned16(dmin) || !aligned16(sc) || !aligned16(m) || !aligned16(meta))
+        return fail(UQ_ERR_ALIGN, "K4 metadata pointers must be 16-byte aligned");
+    DeviceState* ds = nullptr;
+    if ((s = device_state(&ds, nullptr)) != UQ_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(ds->words + 1, 0, sizeof(unsigned int), st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    e = uq::launch_pack_kmeta(d, dmin, sc, m, static_cast<uint8_t*>(meta), count, ds->words + 1, st);
+    if (e != cudaSuccess) return cuda_fail(e, "kmeta launch");
+    unsigned int bad = 0;
+    e = cudaMemcpyAsync(&bad, ds->words + 1, sizeof bad, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "kmeta check");
+    if (bad) return fail(UQ_ERR_INVALID, "%u K4 records hold a 6-bit code above 63", bad);
+    return UQ_OK;
+}
+
+uq_status uq_pack_zeros(const uint8_t* zeros, uint8_t* packed, int N, int G, void* stream) {
+    if (N < 0 || G < 0) return fail(UQ_ERR_INVALID, "negative size");
+    if ((long long)N * G == 0) return UQ_OK;
+    if (!zeros || !packed) return fail(UQ_ERR_INVALID, "null pointer");
+    if (!aligned16(zeros) || !aligned16(packed)) return fail(UQ_ERR_ALIGN, "pointers must be 16-byte aligned");
+    cudaError_t e = uq::launch_pack_zeros(zeros, packed, N, G, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pack_zeros launch");
+    return UQ_OK;
+}
+
+static uq_status check_meta_ptrs(const void* scales, const void* zc, int fmt) {
+    if (!scales) return fail(UQ_ERR_INVALID, "scales is NULL");
+    if (needs_zc(fmt) && !zc) return fail(UQ_ERR_INVALID, "this format needs zeros_or_codebook");
+    if (!needs_zc(fmt) && zc) return fail(UQ_ERR_INVALID, "zeros_or_codebook must be NULL for this format");
+    if (!aligned16(scales) || (zc && !aligned16(zc)))
+        return fail(UQ_ERR_ALIGN, "scales / zeros_or_codebook must be 16-byte aligned");
+    return UQ_OK;
+}
+
+uq_status uq_gemm(const uint16_t* x, const void* wq, const void* scales, const void* zeros_or_codebook,
+                  uint16_t* y, int M, int N, int K, int group, uq_fmt fmt, void* stream) {
+    uq_status s = check_shape(N, K, group, fmt);
+    if (s != UQ_OK) return s;
+    if (M < 0) return fail(UQ_ERR_INVALID, "negative M");
+    if (M == 0 || N == 0) return UQ_OK;
+    if (!y) return fail(UQ_ERR_INVALID, "y is NULL");
+    if (!aligned16(y)) return fail(UQ_ERR_ALIGN, "y must be 16-byte aligned");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        cudaError_t e = cudaMemsetAsync(y, 0, (size_t)M * N * 2, st);
+        return e == cudaSuccess ? UQ_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    if (!x || !wq) return fail(UQ_ERR_INVALID, "x or wq is NULL");
+    if (!aligned16(x) || !aligned16(wq)) return fail(UQ_ERR_ALIGN, "x and wq must be 16-byte aligned");
+    if ((s = check_meta_ptrs(scales, zeros_or_codebook, fmt)) != UQ_OK) return s;
+    DeviceState* ds = nullptr;
+    int dev = 0;
+    if ((s = device_state(&ds, &dev)) != UQ_OK) return s;
+    for (int m0 = 0; m0 < M; m0 += 8) {
+        const int mb = (M - m0) < 8 ? (M - m0) : 8;
+        s = run_gemv(x + (long long)m0 * K, wq, scales, zeros_or_codebook, y + (long long)m0 * N, mb, N, K, K, N,
+                     group, fmt, st, *ds, dev);
+        if (s != UQ_OK) return s;
+    }
+    return UQ_OK;
+}
+
+uq_status uq_unpack_codes(const void* wq, int8_t* codes, int N, int K, int group, uq_fmt fmt, void* stream) {
+    uq_status s = check_shape(N, K, group, fmt);
+    if (s != UQ_OK) return s;
+    if ((long long)N * K == 0) return UQ_OK;
+    if (!wq || !codes) return fail(UQ_ERR_INVALID, "null pointer");
+    if (!aligned16(wq) || !aligned16(codes)) return fail(UQ_ERR_ALIGN, "pointers must be 16-byte aligned");
+    cudaError_t e = uq::launch_unpack(fmt, static_cast<const uint8_t*>(wq), codes, N, K,
+                                      static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "unpack launch");
+    return UQ_OK;
+}
+
+uq_status uq_dequant(const void* wq, const void* scales, const void* zeros_or_codebook, float* w, int N, int K,
+                     int group, uq_fmt fmt, void* stream) {
+    uq_status s = check_shape(N, K, group, fmt);
+    if (s != UQ_OK) return s;
+    if ((long long)N * K == 0) return UQ_OK;
+    if (!wq || !w) return fail(UQ_ERR_INVALID, "null pointer");
+    if (!aligned16(wq) || !aligned16(w)) return fail(UQ_ERR_ALIGN, "pointers must be 16-byte aligned");
+    if ((s = check_meta_ptrs(scales, zeros_or_codebook, fmt)) != UQ_OK) return s;
+    cudaError_t e = uq::launch_dequant(fmt, static_cast<const uint8_t*>(wq), static_cast<const uint8_t*>(scales),
+                                       static_cast<const uint8_t*>(zeros_or_codebook), w, N, K, group,
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "dequant launch");
+    return UQ_OK;
+}
+
+uq_status uq_quantize(const float* w, int8_t* codes, uint16_t* scales, void* zeros, const float* codebook, int N,
+                      int K, int group, uq_fmt fmt, void* stream) {
+    if (fmt == UQ_K4) return fail(UQ_ERR_INVALID, "use uq_quantize_k4 for UQ_K4");
+    uq_status s = check_shape(N, K, group, fmt);
+    if (s != UQ_OK) return s;
+    if ((long long)N * K == 0) return UQ_OK;
+    if (!w || !codes || !scales) return fail(UQ_ERR_INVALID, "null pointer");
+    const bool wants_z = (fmt == UQ_INT4_ASYM || fmt == UQ_INT2_ASYM);
+    if (wants_z != (zeros != nullptr)) return fail(UQ_ERR_INVALID, "zeros must be given exactly for the ASYM formats");
+    if ((fmt == UQ_NF4) != (codebook != nullptr)) return fail(UQ_ERR_INVALID, "codebook must be given exactly for UQ_NF4");
+    if (!aligned16(w) || !aligned16(codes) || !aligned16(scales) || (zeros && !aligned16(zeros)) ||
+        (codebook && !aligned16(codebook)))
+        return fail(UQ_ERR_ALIGN, "pointers must be 16-byte aligned");
+    cudaError_t e = uq::launch_quantize(fmt, w, codes, scales, zeros, codebook, N, K, group,
+                                        static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    return UQ_OK;
+}
+
+uq_status uq_quantize_k4(const float* w, int8_t* codes, uint16_t* d, uint16_t* dmin, uint8_t* sc, uint8_t* m,
+                         int N, int K, void* stream) {
+    uq_status s = check_shape(N, K, 256, UQ_K4);
+    if (s != UQ_OK) return s;
+    if ((long long)N * K == 0) return UQ_OK;
+    if (!w || !codes || !d || !dmin || !sc || !m) return fail(UQ_ERR_INVALID, "null pointer");
+    if (!aligned16(w) || !aligned16(codes) || !aligned16(d) || !aligned16(dmin) || !aligned16(sc) || !aligned16(m))
+        return fail(UQ_ERR_ALIGN, "pointers must be 16-byte aligned");
+    cudaError_t e = uq::launch_quantize_k4(w, codes, d, dmin, sc, m, N, K, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "quantize_k4 launch");
+    return UQ_OK;
+}
+
+uq_status uq_device_fault(unsigned int* flag) {
+    if (!flag) return fail(UQ_ERR_INVALID, "null pointer");
+    DeviceState* ds = nullptr;
+    int dev = 0;
+    uq_status s = device_state(&ds, &dev);
+    if (s != UQ_OK) return s;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    unsigned int v = 0;
+    e = cudaMemcpy(&v, ds->words, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy");
+    *flag = v;
+    if (v) {
+        // a kernel returned early: its tickets may be left non-zero; clear this device's workspaces
+        cudaMemset(ds->words, 0, sizeof v);
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (auto& kv : g_ws)
+            if (kv.first.first == dev && kv.second.tickets)
+                cudaMemset(kv.second.tickets, 0, kv.second.ticket_bytes);
+        cudaDeviceSynchronize();
+    }
+    return UQ_OK;
+}
+
+}  // extern "C"

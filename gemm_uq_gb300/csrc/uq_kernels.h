@@ -1,0 +1,44 @@
+// uq_kernels.h -- internal declarations shared by the uq CUDA sources and the C-ABI host code.
+#pragma once
+
+#include "uq_common.cuh"
+
+namespace uq {
+
+// offline kernels (uq_pack.cu)
+cudaError_t launch_pack(int fmt, const int8_t* codes, uint8_t* wq, int N, int K, unsigned int* bad,
+                        cudaStream_t st);
+cudaError_t launch_unpack(int fmt, const uint8_t* wq, int8_t* codes, int N, int K, cudaStream_t st);
+cudaError_t launch_dequant(int fmt, const uint8_t* wq, const uint8_t* scales, const uint8_t* zc, float* w,
+                           int N, int K, int group, cudaStream_t st);
+cudaError_t launch_pack_kmeta(const uint16_t* d, const uint16_t* dmin, const uint8_t* sc, const uint8_t* m,
+                              uint8_t* meta, long long count, unsigned int* bad, cudaStream_t st);
+cudaError_t launch_pack_zeros(const uint8_t* z, uint8_t* out, int N, int G, cudaStream_t st);
+cudaError_t launch_quantize(int fmt, const float* w, int8_t* codes, uint16_t* scales, void* zeros,
+                            const float* codebook, int N, int K, int group, cudaStream_t st);
+cudaError_t launch_quantize_k4(const float* w, int8_t* codes, uint16_t* d, uint16_t* dmin, uint8_t* sc,
+                               uint8_t* m, int N, int K, cudaStream_t st);
+
+// small-M GEMV (uq_gemv.cu)
+struct GemvArgs {
+    const uint16_t* x;        // bf16 [M][ldx]
+    const uint8_t* wq;        // packed codes
+    const uint8_t* scales;    // fp16 [N][K/group] or K4 records
+    const uint8_t* zc;        // zeros / codebook / NULL
+    uint16_t* y;              // bf16 [M][ldy]
+    int M, N, K, group, ldx, ldy;
+    int NB, KB;               // row blocks, k tiles
+    long long T;              // tiles = NB * KB
+    int P;                    // workers (warps), P <= T
+    float* partials;          // [2P][RB][M] fp32 split-K partial sums
+    unsigned int* tickets;    // [NB], zero between calls
+    unsigned int* fault;      // device fault word
+};
+constexpr int GEMV_WARPS = 8;     // worker warps per CTA
+constexpr int GEMV_STAGES = 4;    // tiles in flight per warp
+size_t gemv_smem_bytes();
+size_t gemv_partials_floats(int P, int M);
+cudaError_t launch_gemv(int fmt, const GemvArgs& a, int grid, cudaStream_t st);
+
+
+}  // namespace uq

@@ -1,0 +1,186 @@
+/*
+ * uq.h -- C ABI of the group-wise weight-only quantized decode GEMV/GEMM library (sm_103a).
+ *
+ * What the library computes ("Ultra LLM Engine", section "Fused Kernels": a
+ * dequantized-weight GEMV for single-token decode and a dequantized-weight GEMM
+ * for batched decode; section "Quantization": group-wise INT-N and NormalFloat4
+ * weights that are packed into bytes and dequantized by the fused kernels):
+ *
+ *     y[m][n] = bf16_RNE( sum_k x[m][k] * W_hat[n][k] ),   fp32 accumulation,
+ *
+ * where x is M x K bf16, W_hat is the N x K dequantized weight (a linear layer's
+ * weight, K contiguous) and y is M x N bf16.  W_hat is never materialised: the
+ * kernels stream packed codes from HBM and dequantize them in registers (M <= 15,
+ * CUDA cores) or in shared memory feeding tcgen05 tensor cores (M >= 16).
+ *
+ * Weight formats (g = group size along K):
+ *   UQ_INT4_SYM   codes q in [-8, 7],  fp16 scale s per group        W_hat = s*q
+ *   UQ_INT4_ASYM  codes q in [0, 15],  fp16 s + 4-bit zero z         W_hat = s*(q - z)
+ *   UQ_INT8_SYM   codes q in [-128,127] fp16 s per group             W_hat = s*q
+ *   UQ_INT2_ASYM  codes q in [0, 3],   fp16 s + fp16 z (integer)     W_hat = s*(q - z)
+ *   UQ_NF4        codes q in [0, 15],  fp16 absmax a, fp32 c[16]     W_hat = RN32(a*c[q])
+ *   UQ_K4         codes q in [0, 15],  256-weight super-blocks of 8 x 32: fp16 d, dmin,
+ *                 6-bit sc_j, m_j per 32-weight sub-block             W_hat = RN32(d*sc_j*q - dmin*m_j)
+ *
+ * Conventions for every call:
+ *   - Pointers marked (device) are CUDA device memory owned by the caller; the
+ *     library never frees or retains them.  Pointers must be 16-byte aligned
+ *     (else UQ_ERR_ALIGN).  bf16 and fp16 arrays are passed as uint16_t bit patterns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Calls are asynchronous and stream-ordered unless stated otherwise.
+ *   - Errors are returned, never raised: no exception crosses the ABI, no kernel
+ *     traps or asserts, and there is no silent fallback to another implementation.
+ *   - The library runs on the device that is current on the calling thread.
+ */
+#ifndef UQ_H
+#define UQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum uq_status {
+    UQ_OK = 0,
+    UQ_ERR_INVALID = 1,      /* bad argument: size, null pointer, code out of range, metadata mismatch */
+    UQ_ERR_UNSUPPORTED = 2,  /* valid request outside what the kernels implement (group, K multiple, arch) */
+    UQ_ERR_ALIGN = 3,        /* a pointer is not 16-byte aligned */
+    UQ_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+    UQ_ERR_NOMEM = 5         /* library-owned workspace could not be allocated (or not during capture) */
+} uq_status;
+
+typedef enum uq_fmt {
+    UQ_INT4_SYM = 0,
+    UQ_INT4_ASYM = 1,
+    UQ_INT8_SYM = 2,
+    UQ_INT2_ASYM = 3,
+    UQ_NF4 = 4,
+    UQ_K4 = 5
+} uq_fmt;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* uq_status_string(uq_status s);
+
+/* Message of the last error raised on the calling thread (static per thread, never NULL). */
+const char* uq_last_error(void);
+
+/*
+ * uq_packed_size -- bytes of every buffer a (N, K, group, fmt) weight needs.
+ *   wq_bytes     packed code plane written by uq_pack_layout      (N*K*bits/8)
+ *   scales_bytes `scales` argument of uq_gemm: fp16 [N][K/group]; UQ_K4: 16-byte
+ *                records [N][K/256] written by uq_pack_kmeta
+ *   zeros_bytes  `zeros_or_codebook` argument: UQ_INT4_ASYM uint8 [N][ceil(K/group/2)]
+ *                (two 4-bit zeros per byte, low nibble = even group); UQ_INT2_ASYM fp16
+ *                [N][K/group]; UQ_NF4 64 (fp32 c[16]); others 0 (pass NULL)
+ * Host-only; any output pointer may be NULL.  Returns UQ_ERR_INVALID / UQ_ERR_UNSUPPORTED
+ * under the same rules as uq_gemm.
+ */
+uq_status uq_packed_size(int N, int K, int group, uq_fmt fmt,
+                         size_t* wq_bytes, size_t* scales_bytes, size_t* zeros_bytes);
+
+/*
+ * uq_pack_layout -- codes -> the kernels' packed code plane ("pack multiple low-bit
+ * values into bytes", section "Quantization").
+ *   codes (device)  int8 [N][K] row-major: the signed code for the SYM formats, the
+ *                   unsigned code (stored in int8) otherwise.
+ *   wq    (device)  uq_packed_size(...).wq_bytes bytes, written.
+ * Layout (library-defined): tiles of 8 rows x 512 bytes of codes (the last tile of a
+ * row is narrower, the last row block shorter), each tile contiguous; inside a
+ * 16-byte lane chunk the codes are ordered per 32-bit word so that in-register
+ * unpacking yields k-consecutive pairs.  Offline call: it SYNCHRONIZES `stream`
+ * and returns UQ_ERR_INVALID if any code is outside the format's range (wq is then
+ * unspecified).
+ */
+uq_status uq_pack_layout(const int8_t* codes, void* wq, int N, int K, int group, uq_fmt fmt,
+                         void* stream);
+
+/*
+ * uq_pack_kmeta -- UQ_K4 metadata -> 16-byte records [N][K/256] (the `scales` argument).
+ *   d, dmin (device) fp16 [N][K/256];  sc, m (device) uint8 [N][K/256][8], values 0..63.
+ *   meta    (device) 16*N*(K/256) bytes, written.  Record: fp16 d, fp16 dmin, then 8
+ *           6-bit sc codes (bytes 4..9) and 8 6-bit m codes (bytes 10..15), little-endian
+ *           bit order.  Offline call: synchronizes `stream`; UQ_ERR_INVALID if a code > 63.
+ */
+uq_status uq_pack_kmeta(const uint16_t* d, const uint16_t* dmin, const uint8_t* sc,
+                        const uint8_t* m, void* meta, int N, int K, void* stream);
+
+/*
+ * uq_gemm -- y = x . W_hat^T with W_hat dequantized on the fly (the decode hot path).
+ *   x      (device) bf16 [M][K] row-major
+ *   wq     (device) packed codes from uq_pack_layout
+ *   scales (device) fp16 [N][K/group] (s, or a for UQ_NF4); UQ_K4: records from uq_pack_kmeta
+ *   zeros_or_codebook (device) see uq_packed_size; must be NULL for INT4_SYM, INT8_SYM, K4
+ *   y      (device) bf16 [M][N] row-major, written (round to nearest even)
+ *   M >= 0, N >= 0, K >= 0; M == 0 or N == 0 is a no-op; K == 0 writes zeros.
+ *   group: 32, 64 or 128 for the flat formats (K % group == 0; UQ_INT2_ASYM also needs
+ *   K % 64 == 0); 256 for UQ_K4 (K % 256 == 0).
+ * Paths: M <= 8 one CUDA-core GEMV launch (split-K over the GPU's SMs, the partial
+ * sums reduced in a fixed order, so repeated calls are bit-identical);
+ * 9 <= M <= 15 the GEMV over row blocks of at most 8; M >= 16 the tcgen05 path.
+ * Scratch: a library-owned workspace per (device, stream), grown on the first call
+ * that needs more; that growth is refused (UQ_ERR_NOMEM) while `stream` is being
+ * captured, so make one call of the largest size before capturing.  Calls on the
+ * same stream are serialised by the stream; concurrent streams use separate workspaces.
+ */
+uq_status uq_gemm(const uint16_t* x, const void* wq, const void* scales,
+                  const void* zeros_or_codebook, uint16_t* y,
+                  int M, int N, int K, int group, uq_fmt fmt, void* stream);
+
+/*
+ * uq_unpack_codes -- debug: packed plane -> int8 codes [N][K] (device), bit-exact
+ * inverse of uq_pack_layout, using the same unpacking as the GEMV kernels.
+ */
+uq_status uq_unpack_codes(const void* wq, int8_t* codes, int N, int K, int group, uq_fmt fmt,
+                          void* stream);
+
+/*
+ * uq_dequant -- debug: W_hat as fp32 [N][K] (device), the correctly rounded value of the
+ * format's reconstruction formula (bit-exact against an exact evaluation).
+ */
+uq_status uq_dequant(const void* wq, const void* scales, const void* zeros_or_codebook,
+                     float* w, int N, int K, int group, uq_fmt fmt, void* stream);
+
+/*
+ * uq_quantize -- GPU quantizer for the flat formats (INT4_SYM, INT4_ASYM, INT8_SYM,
+ * INT2_ASYM, NF4): fp32 W [N][K] (device) -> int8 codes [N][K], fp16 scales
+ * [N][K/group], zeros (INT4_ASYM: uint8 [N][K/group], one zero per byte, NOT the
+ * nibble-packed uq_gemm layout -- use uq_pack_zeros; INT2_ASYM: fp16 [N][K/group];
+ * else NULL) and, for NF4, the input codebook fp32 c[16] (ascending).
+ * Rules (scales in float64 then fp16): symmetric s = fp16_RNE(absmax/qmax),
+ * q = clamp(rint(w/s)); asymmetric s = fp16 toward +inf of (max(w,0)-min(w,0))/L,
+ * z = rint(-min/s), q = clamp(rint(w/s)+z, 0, L); NF4 a = fp16_RNE(absmax),
+ * q = first index minimising |w/a - c[i]|.  Offline; asynchronous.
+ */
+uq_status uq_quantize(const float* w, int8_t* codes, uint16_t* scales, void* zeros,
+                      const float* codebook, int N, int K, int group, uq_fmt fmt, void* stream);
+
+/*
+ * uq_quantize_k4 -- GPU quantizer for UQ_K4: fp32 W [N][K] -> codes int8 [N][K],
+ * fp16 d, dmin [N][K/256], uint8 sc, m [N][K/256][8] (min/max quantizer with
+ * ceilings: dmin = fp16 up of max(-lo_j)/63, m_j = ceil(-lo_j/dmin),
+ * d = fp16 up of max(hi_j + dmin*m_j)/945, sc_j = ceil(r_j/(15d)),
+ * q = clamp(rint((w + dmin*m_j)/(d*sc_j)), 0, 15)).  Offline; asynchronous.
+ */
+uq_status uq_quantize_k4(const float* w, int8_t* codes, uint16_t* d, uint16_t* dmin,
+                         uint8_t* sc, uint8_t* m, int N, int K, void* stream);
+
+/*
+ * uq_pack_zeros -- INT4_ASYM zeros, one per byte [N][G] (device) -> the uq_gemm layout
+ * [N][ceil(G/2)] (two per byte, low nibble = even group).  Asynchronous.
+ */
+uq_status uq_pack_zeros(const uint8_t* zeros, uint8_t* packed, int N, int G, void* stream);
+
+/*
+ * uq_device_fault -- reads and clears the device-side fault word of the current device
+ * (set when a kernel's bounded wait on an mbarrier ran out and the kernel returned
+ * early instead of hanging).  Synchronizes the device.  *flag = 0 when no fault.
+ */
+uq_status uq_device_fault(unsigned int* flag);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UQ_H */
