@@ -210,7 +210,9 @@ def run_uq(args, rank, world, dist):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    spec = WORKLOADS[args.workload]
+    spec = dict(WORKLOADS[args.workload])
+    if args.layers:
+        spec["layers"] = args.layers
     fmt, group = spec["fmt"], spec["group"]
     M = args.m if args.m else spec["m"]
     recs = build_weights(spec, M, dev)
@@ -337,7 +339,7 @@ def run_uq(args, rank, world, dist):
     value = total_bytes / (ms * 1e-3) / 1e9
     peak, peak_src = measured_peak()
     achieved = step_bytes / (kern_ms * 1e-3) / 1e9
-    traffic = read_traffic(args.workload) if M == spec["m"] else None
+    traffic = read_traffic(args.workload) if (M == WORKLOADS[args.workload]["m"] and not args.layers) else None
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
@@ -345,6 +347,7 @@ def run_uq(args, rank, world, dist):
         f"bf16 x {fmt.lower()} -> fp32 acc",
         "data": "synthetic (seeded N(0,sigma) weights quantized on the GPU; bf16 N(0,1) x)",
         "config": {"workload": args.workload, "description": spec["title"], "fmt": fmt, "group": group, "M": M,
+                   "layers": spec["layers"],
                    "linears_per_step": launches, "bytes_per_step": step_bytes,
                    "parallelism": f"replicas x{world}",
                    "l2": "no flush: packed weights per step exceed L2 (%.2f GB)" % (step_bytes / 1e9),
@@ -439,6 +442,7 @@ def main():
     ap.add_argument("--impl", choices=["uq", "reference"], default="uq")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama8b-int4a-decode")
     ap.add_argument("--m", type=int, default=0, help="override the batch rows M")
+    ap.add_argument("--layers", type=int, default=0, help="override the number of layers (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

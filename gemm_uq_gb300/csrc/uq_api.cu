@@ -77,6 +77,8 @@ std::map<int, DeviceState> g_dev;
 struct Workspace {
     float* partials = nullptr;
     size_t partial_bytes = 0;
+    float* aux = nullptr;              // K4 column sums for the tensor-core path
+    size_t aux_bytes = 0;
     unsigned int* tickets = nullptr;   // zero between calls (the kernels reset what they use)
     size_t ticket_bytes = 0;
 };
@@ -134,11 +136,16 @@ uq_status grow(void** ptr, size_t* have, size_t need, bool zero, cudaStream_t st
     return UQ_OK;
 }
 
-uq_status workspace(int dev, cudaStream_t st, size_t partial_bytes, size_t ticket_bytes, Workspace** out) {
+uq_status workspace(int dev, cudaStream_t st, size_t partial_bytes, size_t ticket_bytes, Workspace** out,
+                    size_t aux_bytes = 0) {
     std::lock_guard<std::mutex> lk(g_mu);
     Workspace& w = g_ws[{dev, (void*)st}];
     uq_status s = grow(reinterpret_cast<void**>(&w.partials), &w.partial_bytes, partial_bytes, false, st);
     if (s != UQ_OK) return s;
+    if (aux_bytes) {
+        s = grow(reinterpret_cast<void**>(&w.aux), &w.aux_bytes, aux_bytes, false, st);
+        if (s != UQ_OK) return s;
+    }
     s = grow(reinterpret_cast<void**>(&w.tickets), &w.ticket_bytes, ticket_bytes, true, st);
     if (s != UQ_OK) return s;
     *out = &w;
@@ -171,6 +178,47 @@ uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const 
     const int grid = (int)((P + uq::GEMV_WARPS - 1) / uq::GEMV_WARPS);
     cudaError_t e = uq::launch_gemv(fmt, a, grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "GEMV launch");
+    return UQ_OK;
+}
+
+
+// one tensor-core launch for 16 <= Mb <= 64 rows of x
+uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const void* zc, uint16_t* y, int Mb, int N,
+                 int K, int ldx, int ldy, int group, int fmt, cudaStream_t st, const DeviceState& ds, int dev) {
+    const int mpad = (Mb + 15) / 16 * 16;
+    int stages = 0, dslots = 0;
+    size_t smem = 0;
+    if (uq::tc_plan(fmt, mpad, &stages, &dslots, &smem) != 0)
+        return fail(UQ_ERR_UNSUPPORTED, "no tensor-core plan for M=%d", Mb);
+    const int kc = (fmt == UQ_INT8_SYM) ? 128 : 256;
+    const int nblk = (N + 127) / 128;
+    const int CH = K / kc;
+    const long long U = (long long)nblk * CH;
+    long long P = ds.sms;
+    if (P > U) P = U;
+    Workspace* ws = nullptr;
+    const size_t aux = (fmt == UQ_K4) ? (size_t)(K / 32) * mpad * sizeof(float) : 0;
+    uq_status s = workspace(dev, st, (size_t)2 * P * 128 * mpad * sizeof(float), (size_t)nblk * sizeof(unsigned int),
+                            &ws, aux);
+    if (s != UQ_OK) return s;
+    cudaError_t e;
+    if (fmt == UQ_K4) {
+        e = uq::launch_colsum32(x, ws->aux, Mb, mpad, K, ldx, st);
+        if (e != cudaSuccess) return cuda_fail(e, "column-sum launch");
+    }
+    uq::TcArgs a;
+    a.scales = static_cast<const uint8_t*>(scales);
+    a.zc = static_cast<const uint8_t*>(zc);
+    a.y = y;
+    a.sx = ws->aux;
+    a.M = Mb; a.Mpad = mpad; a.N = N; a.K = K; a.group = group; a.ldx = ldx; a.ldy = ldy;
+    a.CH = CH; a.U = U; a.P = (int)P;
+    a.stages = stages; a.dslots = dslots;
+    a.partials = ws->partials;
+    a.tickets = ws->tickets;
+    a.fault = ds.words;
+    e = uq::launch_tc(fmt, x, static_cast<const uint8_t*>(wq), a, smem, (int)P, st);
+    if (e != cudaSuccess) return cuda_fail(e, "tensor-core launch");
     return UQ_OK;
 }
 
@@ -286,6 +334,17 @@ uq_status uq_gemm(const uint16_t* x, const void* wq, const void* scales, const v
     DeviceState* ds = nullptr;
     int dev = 0;
     if ((s = device_state(&ds, &dev)) != UQ_OK) return s;
+    if (M >= 16 && uq::tc_supported(fmt, N, K)) {
+        // tensor cores, in blocks of at most 64 activation rows (the last block at least 16 rows
+        // wide is padded to a multiple of 16 with zero rows by the TMA bounds)
+        for (int m0 = 0; m0 < M; m0 += 64) {
+            const int mb = (M - m0) < 64 ? (M - m0) : 64;
+            s = run_tc(x + (long long)m0 * K, wq, scales, zeros_or_codebook, y + (long long)m0 * N, mb, N, K, K, N,
+                       group, fmt, st, *ds, dev);
+            if (s != UQ_OK) return s;
+        }
+        return UQ_OK;
+    }
     for (int m0 = 0; m0 < M; m0 += 8) {
         const int mb = (M - m0) < 8 ? (M - m0) : 8;
         s = run_gemv(x + (long long)m0 * K, wq, scales, zeros_or_codebook, y + (long long)m0 * N, mb, N, K, K, N,

@@ -1,0 +1,574 @@
+// uq_tc.cu -- tensor-core fused dequantize + GEMM for M >= 16 (tcgen05, sm_103a).
+//
+// "Ultra LLM Engine", section "Fused Kernels": the dequantized-weight GEMM of batched decode.
+// With 16..64 activation rows the product is a dense contraction, so it runs on the 5th-gen
+// tensor cores; the kernel still streams each packed weight byte from HBM exactly once.
+//
+// Operands (swap-AB: the 128 weight rows are the MMA's M dimension, the activation rows its N):
+//   A  = the integer part of the weights, (q - z) for INT4/INT8 and q for K4, exact in bf16,
+//        written by the dequant warpgroup straight into TENSOR MEMORY (tcgen05.st), so the
+//        dequantized operand never crosses shared memory;
+//   B  = x, a [Mpad x 64] bf16 tile per 64-k step, loaded by TMA with the 128-byte swizzle
+//        (the canonical K-major layout the MMA reads through a shared-memory descriptor);
+//   D  = one fp32 accumulator slot in tensor memory per quantization group (128 lanes x Mpad
+//        columns); the epilogue warpgroup reads it back (tcgen05.ld) and applies the group's
+//        scale in fp32: y += s_g * sum_k (q - z) x  (K4: d*sc_j * sum q x - dmin*m_j * sum x).
+// So the products and the per-group sums are exact up to fp32 accumulation, as in the GEMV.
+//
+// Roles (384 threads, one CTA per SM, persistent over an equal contiguous range of units):
+//   warp 0       TMA producer: per unit one 4-D box of codes (16 tiles x 8 rows x 128 bytes,
+//                128-byte swizzle) and kc/64 boxes of x, counted on full[stage];
+//   warp 1       MMA issuer (one thread): per group g/16 tcgen05.mma (M=128, N=Mpad, K=16);
+//   warps 4..7   dequant: thread = weight row; reads its 128 code bytes, writes kc/2 columns;
+//   warps 8..11  epilogue: thread = weight row; scales, accumulates over the row block's units,
+//                then stores y, or a partial sum plus a ticket (the last contributor reduces
+//                the partials in CTA order, so results are deterministic and nobody waits).
+// Unit = (128-row block, chunk of 128 code bytes per row = kc codes).  Every wait is bounded
+// (mbar_wait_bounded); on a timeout the roles stop, the CTA frees its tensor memory and leaves.
+#include <cuda.h>
+
+#include "uq_kernels.h"
+
+namespace uq {
+
+namespace {
+
+constexpr int TC_THREADS = 384;
+constexpr int TC_ROWS = 128;
+constexpr int TC_STAGE_CODES = TC_ROWS * 128;     // bytes of codes per stage
+constexpr int TMEM_COLS = 512;
+
+__device__ __forceinline__ long long trange_begin(int c, long long U, int P) { return (long long)c * U / P; }
+__device__ __forceinline__ int tworker_of(long long u, long long U, int P) {
+    return (int)(((u + 1) * (long long)P - 1) / U);
+}
+
+// ---- tcgen05 / TMA wrappers ------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_u32(dst_smem)), "r"(ncols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(smem_u32(bar)) : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc]
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+                 :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                    "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
+                    "r"(v[14]), "r"(v[15]) : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                   "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr) : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar) {
+    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4, %5}], [%6];"
+                 :: "r"(smem_u32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];"
+                 :: "r"(smem_u32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar)) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row core groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(const void* p) {
+    const uint64_t addr = smem_u32(p);
+    return ((addr & 0x3FFFFull) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M = 128, N = mpad.
+__host__ __device__ constexpr uint32_t idesc_bf16(int mpad) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(mpad >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+template <int FMT> struct TcFmt {
+    static constexpr int KC = (FMT == UQ_INT8_SYM) ? 128 : 256;   // codes per row per unit
+    static constexpr int ACOLS = KC / 2;                           // tensor-memory columns of A per unit
+};
+
+}  // namespace
+
+struct TcSmem {
+    // barriers live after the stage buffers; offsets computed on the host and device alike
+    static __host__ __device__ constexpr int x_bytes(int kc, int mpad) { return kc * mpad * 2; }
+    static __host__ __device__ constexpr int stage_bytes(int kc, int mpad) {
+        return TC_STAGE_CODES + x_bytes(kc, mpad);
+    }
+};
+
+template <int FMT, int MPAD>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_constant__ CUtensorMap tmap_x,
+          const TcArgs a) {
+    constexpr int KC = TcFmt<FMT>::KC;
+    constexpr int ACOLS = TcFmt<FMT>::ACOLS;
+    constexpr int XB = TcSmem::x_bytes(KC, MPAD);
+    constexpr int SB = TcSmem::stage_bytes(KC, MPAD);
+    constexpr uint32_t IDESC = idesc_bf16(MPAD);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int S = a.stages, DS = a.dslots;
+    const int G = (FMT == UQ_K4) ? 32 : a.group;   // scaling granularity (K4: the 32-weight sub-block)
+    const int GPC = KC / G;                         // groups (K4: sub-blocks) per unit
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * SB);
+    uint64_t* full = bars;                          // [S]
+    uint64_t* empty = full + S;                     // [S]
+    uint64_t* afull = empty + S;                    // [2]
+    uint64_t* aempty = afull + 2;                   // [2]
+    uint64_t* dfull = aempty + 2;                   // [DS]
+    uint64_t* dempty = dfull + DS;                  // [DS]
+    uint64_t* ebar = dempty + DS;                   // epilogue warpgroup rendezvous (128 arrivals)
+    uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(ebar + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_smem + 1);
+    unsigned int* ticket_smem = reinterpret_cast<unsigned int*>(tmem_base_smem + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const long long u0 = trange_begin(cta, a.U, a.P), u1 = trange_begin(cta + 1, a.U, a.P);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 5); }
+        for (int i = 0; i < 2; ++i) { mbar_init(&afull[i], 4); mbar_init(&aempty[i], 1); }
+        for (int d = 0; d < DS; ++d) { mbar_init(&dfull[d], 1); mbar_init(&dempty[d], 4); }
+        mbar_init(ebar, 128);
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0) tmem_alloc(tmem_base_smem, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_base_smem;
+    const uint32_t A_COL0 = 0;                      // A buffers: columns [0, 2*ACOLS)
+    const uint32_t D_COL0 = 2 * ACOLS;              // D slots: columns [2*ACOLS, 2*ACOLS + DS*MPAD)
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            for (long long u = u0; u < u1 && !*abort_flag; ++u, ++issued) {
+                const int i = (int)(u - u0), s = i % S;
+                if (!mbar_wait_bounded(&empty[s], (uint32_t)(((i / S) & 1) ^ 1), a.fault, FAULT_TC_WAIT)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                const int rb = (int)(u / a.CH), c = (int)(u % a.CH);
+                uint8_t* st = smem + s * SB;
+                mbar_arrive_expect_tx(&full[s], (uint32_t)SB);
+                // codes: byte (c % 4) * 128 of the tile row, rows 0..7, k tile c / 4, 16 row blocks of 8
+                tma_load_4d(st, &tmap_codes, (c & 3) * 128, 0, c >> 2, rb * 16, &full[s]);
+#pragma unroll
+                for (int q = 0; q < KC / 64; ++q)
+                    tma_load_2d(st + TC_STAGE_CODES + q * (MPAD * 128), &tmap_x, c * KC + q * 64, 0, &full[s]);
+            }
+            // let the last copies land before the CTA can leave
+            for (int j = issued - 1; j >= 0 && j >= issued - S; --j)
+                mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1), a.fault, FAULT_TC_WAIT);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            long long dctr = 0;
+            for (long long u = u0; u < u1 && !*abort_flag; ++u) {
+                const int i = (int)(u - u0), s = i % S, ab = i & 1;
+                bool ok = mbar_wait_bounded(&full[s], (uint32_t)((i / S) & 1), a.fault, FAULT_TC_WAIT) &&
+                          mbar_wait_bounded(&afull[ab], (uint32_t)((i >> 1) & 1), a.fault, FAULT_TC_WAIT);
+                if (!ok) { *abort_flag = 1; break; }
+                tc_fence_after();
+                const uint8_t* xs = smem + s * SB + TC_STAGE_CODES;
+                for (int j = 0; j < GPC && ok; ++j, ++dctr) {
+                    const int d = (int)(dctr % DS);
+                    if (!mbar_wait_bounded(&dempty[d], (uint32_t)(((dctr / DS) & 1) ^ 1), a.fault, FAULT_TC_WAIT)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int ks_per_group = G / 16;
+                    for (int t = 0; t < ks_per_group; ++t) {
+                        const int ks = j * ks_per_group + t;                 // 16-k slice within the unit
+                        const uint64_t bdesc = sw128_desc(xs + (ks >> 2) * (MPAD * 128) + (ks & 3) * 32);
+                        mma_ts(tmem + D_COL0 + d * MPAD, tmem + A_COL0 + ab * ACOLS + ks * 8, bdesc, IDESC,
+                               t > 0 ? 1u : 0u);
+                    }
+                    tc_commit(&dfull[d]);
+                }
+                if (!ok) { *abort_flag = 1; break; }
+                tc_commit(&aempty[ab]);
+                tc_commit(&empty[s]);
+            }
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ---------------------------------------------------------------- dequant warpgroup
+        const int wq = warp - 4;
+        const int r = wq * 32 + lane;                   // row within the 128-row block
+        const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+        for (long long u = u0; u < u1 && !*abort_flag; ++u) {
+            const int i = (int)(u - u0), s = i % S, ab = i & 1;
+            const int rb = (int)(u / a.CH), c = (int)(u % a.CH);
+            const int n = rb * TC_ROWS + r;
+            // subtrahend per group as a bf16 pair (128 + z, or 128 + 8 for INT4_SYM, 128 for K4)
+            uint32_t zsub[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) zsub[j] = 0x43004300u;
+            if constexpr (FMT == UQ_INT4_SYM) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) zsub[j] = 0x43084308u;
+            } else if constexpr (FMT == UQ_INT4_ASYM) {
+                if (n < a.N) {
+                    const int Gn = a.K / G;
+                    const uint8_t* zr = a.zc + (long long)n * ((Gn + 1) >> 1);
+                    for (int j = 0; j < GPC; ++j) {
+                        const int gi = (c * KC) / G + j;
+                        const uint8_t b = __ldg(zr + (gi >> 1));
+                        const uint32_t z = (gi & 1) ? (b >> 4) : (b & 15u);
+                        zsub[j] = 0x43004300u | z | (z << 16);
+                    }
+                }
+            }
+            bool ok = mbar_wait_bounded(&full[s], (uint32_t)((i / S) & 1), a.fault, FAULT_TC_WAIT) &&
+                      mbar_wait_bounded(&aempty[ab], (uint32_t)(((i >> 1) & 1) ^ 1), a.fault, FAULT_TC_WAIT);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) { *abort_flag = 1; break; }
+            tc_fence_after();
+            const uint8_t* crow = smem + s * SB + (r >> 3) * 1024 + (r & 7) * 128;
+            const uint32_t acol = lane_addr + A_COL0 + ab * ACOLS;
+            if constexpr (FMT == UQ_INT8_SYM) {
+                // 128 codes = 8 chunks of 16 bytes -> 64 columns; each chunk gives 8 columns
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t v[16];
+#pragma unroll
+                    for (int cc2 = 0; cc2 < 2; ++cc2) {
+                        const int cc = h * 2 + cc2;
+                        const uint4 q = *reinterpret_cast<const uint4*>(crow + ((cc ^ (r & 7)) << 4));
+                        const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float f0 = byte_magic_f32(wv[e], 0) - 8388736.0f;
+                            const float f1 = byte_magic_f32(wv[e], 1) - 8388736.0f;
+                            const float f2 = byte_magic_f32(wv[e], 2) - 8388736.0f;
+                            const float f3 = byte_magic_f32(wv[e], 3) - 8388736.0f;
+                            v[cc2 * 8 + 2 * e] = f32x2_to_bf16x2(f0, f1);
+                            v[cc2 * 8 + 2 * e + 1] = f32x2_to_bf16x2(f2, f3);
+                        }
+                    }
+                    tmem_st16(acol + h * 16, v);
+                }
+            } else {
+                // 256 codes = 8 chunks of 16 bytes (32 codes) -> 128 columns; one chunk = 16 columns
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    const uint4 q = *reinterpret_cast<const uint4*>(crow + ((cc ^ (r & 7)) << 4));
+                    const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+                    const uint32_t zs = zsub[(cc * 32) / G];
+                    uint32_t v[16];
+#pragma unroll
+                    for (int w = 0; w < 4; ++w)
+#pragma unroll
+                        for (int p = 0; p < 4; ++p) v[w * 4 + p] = bf16x2_sub(nib_pair_bf16(wv[w], p), zs);
+                    tmem_st16(acol + cc * 16, v);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) { mbar_arrive(&afull[ab]); mbar_arrive(&empty[s]); }
+        }
+    } else if (warp >= 8) {
+        // ---------------------------------------------------------------- epilogue warpgroup
+        const int we = warp - 8;
+        const int r = we * 32 + lane;
+        const uint32_t lane_addr = tmem + ((uint32_t)(we * 32) << 16);
+        float acc[MPAD];
+#pragma unroll
+        for (int m = 0; m < MPAD; ++m) acc[m] = 0.f;
+        long long dctr = 0;
+        uint32_t ephase = 0;
+        // all 128 epilogue threads meet here (bounded: returns false after the time limit)
+        auto epi_sync = [&]() -> bool {
+            mbar_arrive(ebar);
+            const bool r_ok = mbar_wait_bounded(ebar, ephase, a.fault, FAULT_TC_WAIT);
+            ephase ^= 1u;
+            return r_ok;
+        };
+        const int first_rb = (int)(u0 / a.CH);
+        for (long long u = u0; u < u1 && !*abort_flag; ++u) {
+            const int rb = (int)(u / a.CH), c = (int)(u % a.CH);
+            const int n = rb * TC_ROWS + r;
+            const bool live = n < a.N;
+            bool ok = true;
+            for (int j = 0; j < GPC; ++j, ++dctr) {
+                float s1 = 0.f, s2 = 0.f;
+                if (live) {
+                    if constexpr (FMT == UQ_K4) {
+                        const int kk = c * KC + j * 32;
+                        const uint4 rec = *reinterpret_cast<const uint4*>(
+                            a.scales + ((long long)n * (a.K >> 8) + (kk >> 8)) * 16);
+                        const int sj = (kk & 255) >> 5;
+                        const uint64_t sc48 = (uint64_t)rec.y | ((uint64_t)(rec.z & 0xFFFFu) << 32);
+                        const uint64_t m48 = (uint64_t)(rec.z >> 16) | ((uint64_t)rec.w << 16);
+                        s1 = half_bits_f32((uint16_t)(rec.x & 0xFFFF)) * (float)((sc48 >> (6 * sj)) & 63);
+                        s2 = half_bits_f32((uint16_t)(rec.x >> 16)) * (float)((m48 >> (6 * sj)) & 63);
+                    } else {
+                        const int gi = (c * KC) / G + j;
+                        s1 = half_bits_f32(__ldg(reinterpret_cast<const uint16_t*>(a.scales) +
+                                                 (long long)n * (a.K / G) + gi));
+                    }
+                }
+                const int d = (int)(dctr % DS);
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait_bounded(&dfull[d], (uint32_t)((dctr / DS) & 1), a.fault, FAULT_TC_WAIT));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int q = 0; q < MPAD / 16; ++q) {
+                    float v[16];
+                    tmem_ld16(lane_addr + D_COL0 + d * MPAD + q * 16, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) acc[q * 16 + e] = fmaf(s1, v[e], acc[q * 16 + e]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&dempty[d]);
+                if constexpr (FMT == UQ_K4) {
+                    const float* sx = a.sx + (long long)((c * KC + j * 32) >> 5) * MPAD;
+#pragma unroll
+                    for (int m = 0; m < MPAD; ++m) acc[m] = fmaf(-s2, __ldg(sx + m), acc[m]);
+                }
+            }
+            if (!ok) { *abort_flag = 1; break; }
+            if (c == a.CH - 1 || u == u1 - 1) {
+                // row block finished for this CTA: store y, or a partial and a ticket
+                const bool fullcov = (c == a.CH - 1) && (rb != first_rb || (u0 % a.CH) == 0);
+                if (fullcov) {
+                    if (live)
+#pragma unroll
+                        for (int m = 0; m < MPAD; ++m)
+                            if (m < a.M)
+                                a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+                } else {
+                    const int slot = 2 * cta + (rb == first_rb ? 0 : 1);
+                    float* part = a.partials + ((long long)slot * TC_ROWS + r) * MPAD;
+#pragma unroll
+                    for (int m = 0; m < MPAD; ++m) part[m] = acc[m];
+                    __threadfence();
+                    if (!epi_sync()) { *abort_flag = 1; break; }
+                    if (r == 0) *ticket_smem = atomicAdd(a.tickets + rb, 1u);
+                    if (!epi_sync()) { *abort_flag = 1; break; }
+                    const unsigned int old = *ticket_smem;
+                    const long long uf = (long long)rb * a.CH;
+                    const int cf = tworker_of(uf, a.U, a.P), cl = tworker_of(uf + a.CH - 1, a.U, a.P);
+                    if (old == (unsigned int)(cl - cf)) {
+                        __threadfence();
+                        float sum[MPAD];
+#pragma unroll
+                        for (int m = 0; m < MPAD; ++m) sum[m] = 0.f;
+                        for (int c2 = cf; c2 <= cl; ++c2) {
+                            const int rb2 = (int)(trange_begin(c2, a.U, a.P) / a.CH);
+                            const int slot2 = 2 * c2 + (rb == rb2 ? 0 : 1);
+                            const float* p2 = a.partials + ((long long)slot2 * TC_ROWS + r) * MPAD;
+#pragma unroll
+                            for (int m = 0; m < MPAD; ++m) sum[m] += __ldcg(p2 + m);
+                        }
+                        if (live)
+#pragma unroll
+                            for (int m = 0; m < MPAD; ++m)
+                                if (m < a.M)
+                                    a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum[m]));
+                        if (r == 0) a.tickets[rb] = 0u;
+                    }
+                    if (!epi_sync()) { *abort_flag = 1; break; }
+                }
+#pragma unroll
+                for (int m = 0; m < MPAD; ++m) acc[m] = 0.f;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------------------------
+// column sums of x per 32-k block, for the K4 min term: sx[j][m] = sum_{k in block j} x[m][k]
+__global__ void colsum32_kernel(const uint16_t* __restrict__ x, float* __restrict__ sx, int M, int mpad, int K,
+                                int ldx) {
+    const int J = K / 32;
+    const long long total = (long long)J * mpad;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int j = (int)(i / mpad), m = (int)(i % mpad);
+        float s0 = 0.f, s1 = 0.f;
+        if (m < M) {
+            const uint32_t* p = reinterpret_cast<const uint32_t*>(x + (long long)m * ldx + j * 32);
+#pragma unroll
+            for (int v = 0; v < 16; ++v) {
+                const uint32_t w = p[v];
+                const float t = bf16lo_f32(w) + bf16hi_f32(w);
+                if (v < 8) s0 += t; else s1 += t;
+            }
+        }
+        sx[i] = s0 + s1;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// host side
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+template <int FMT, int MPAD>
+cudaError_t launch_tc_t(const CUtensorMap& mc, const CUtensorMap& mx, const TcArgs& a, size_t smem, int grid,
+                        cudaStream_t st) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(tc_kernel<FMT, MPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    tc_kernel<FMT, MPAD><<<grid, TC_THREADS, smem, st>>>(mc, mx, a);
+    return cudaGetLastError();
+}
+
+template <int FMT>
+cudaError_t launch_tc_m(int mpad, const CUtensorMap& mc, const CUtensorMap& mx, const TcArgs& a, size_t smem,
+                        int grid, cudaStream_t st) {
+    switch (mpad) {
+        case 16: return launch_tc_t<FMT, 16>(mc, mx, a, smem, grid, st);
+        case 32: return launch_tc_t<FMT, 32>(mc, mx, a, smem, grid, st);
+        case 48: return launch_tc_t<FMT, 48>(mc, mx, a, smem, grid, st);
+        case 64: return launch_tc_t<FMT, 64>(mc, mx, a, smem, grid, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+}  // namespace
+
+bool tc_supported(int fmt, int N, int K) {
+    if (fmt != UQ_INT4_SYM && fmt != UQ_INT4_ASYM && fmt != UQ_INT8_SYM && fmt != UQ_K4) return false;
+    if (N % 8) return false;
+    if (K % fmt_kt(fmt)) return false;
+    return encode_fn() != nullptr;
+}
+
+int tc_plan(int fmt, int mpad, int* stages, int* dslots, size_t* smem) {
+    const int kc = (fmt == UQ_INT8_SYM) ? 128 : 256;
+    const int sb = TcSmem::stage_bytes(kc, mpad);
+    int s = (200 * 1024) / sb;
+    if (s > 6) s = 6;
+    if (s < 2) return -1;
+    int ds = (TMEM_COLS - kc) / mpad;       // A takes 2 * kc/2 columns
+    if (ds > 8) ds = 8;
+    *stages = s;
+    *dslots = ds;
+    *smem = 1024 + (size_t)s * sb + (size_t)(2 * s + 4 + 2 * ds + 1) * 8 + 64;
+    return 0;
+}
+
+cudaError_t launch_colsum32(const uint16_t* x, float* sx, int M, int mpad, int K, int ldx, cudaStream_t st) {
+    const long long total = (long long)(K / 32) * mpad;
+    int g = (int)((total + 255) / 256);
+    if (g > 4096) g = 4096;
+    colsum32_kernel<<<g < 1 ? 1 : g, 256, 0, st>>>(x, sx, M, mpad, K, ldx);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tc(int fmt, const uint16_t* x, const uint8_t* wq, const TcArgs& a, size_t smem, int grid,
+                      cudaStream_t st) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int kt = fmt_kt(fmt);
+    const int KB = a.K / kt, NBt = a.N / 8;
+    CUtensorMap mc, mx;
+    {
+        cuuint64_t dims[4] = {512, 8, (cuuint64_t)KB, (cuuint64_t)NBt};
+        cuuint64_t strides[3] = {512, 4096, (cuuint64_t)KB * 4096};
+        cuuint32_t box[4] = {128, 8, 1, 16};
+        cuuint32_t es[4] = {1, 1, 1, 1};
+        if (enc(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(wq), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
+        cuuint64_t strides[1] = {(cuuint64_t)a.ldx * 2};
+        cuuint32_t box[2] = {64, (cuuint32_t)a.Mpad};
+        cuuint32_t es[2] = {1, 1};
+        if (enc(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    switch (fmt) {
+        case UQ_INT4_SYM: return launch_tc_m<UQ_INT4_SYM>(a.Mpad, mc, mx, a, smem, grid, st);
+        case UQ_INT4_ASYM: return launch_tc_m<UQ_INT4_ASYM>(a.Mpad, mc, mx, a, smem, grid, st);
+        case UQ_INT8_SYM: return launch_tc_m<UQ_INT8_SYM>(a.Mpad, mc, mx, a, smem, grid, st);
+        case UQ_K4: return launch_tc_m<UQ_K4>(a.Mpad, mc, mx, a, smem, grid, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace uq
