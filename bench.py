@@ -164,6 +164,16 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of per-rank timings (identity without a process group)."""
+    if not dist:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
 # ---------------------------------------------------------------------------------------------
 def build_weights(spec, m, dev, seed_base=12345):
     """Quantize and pack every linear of the workload on the GPU; returns per-linear records."""
@@ -327,10 +337,7 @@ def run_uq(args, rank, world, dist):
         kern_ms = statistics.median(totals)
         kern_src = "events around each eager launch"
 
-    if dist:
-        t = torch.tensor([ms, e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], dist, dev)
     if rank != 0:
         return
 

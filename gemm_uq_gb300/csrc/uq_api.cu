@@ -157,6 +157,8 @@ uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const 
                    int Mb, int N, int K, int ldx, int ldy, int group, int fmt, cudaStream_t st,
                    const DeviceState& ds, int dev) {
     const uq::Layout L(N, K, fmt);
+    if (uq::gemv_smem_bytes(fmt, K, Mb) > 227 * 1024)
+        return fail(UQ_ERR_UNSUPPORTED, "K=%d is too long for the GEMV's shared-memory x-sum table at M=%d", K, Mb);
     const long long T = (long long)L.NB * L.KB;
     long long P = (long long)ds.sms * uq::GEMV_WARPS;
     if (P > T) P = T;

@@ -69,8 +69,9 @@ __device__ __forceinline__ RowMeta load_meta(const GemvArgs& a, int n, int k0) {
         if constexpr (FMT == UQ_INT4_SYM) {
             r.zc = 136.0f;
         } else if constexpr (FMT == UQ_INT4_ASYM) {
-            uint8_t b = __ldg(a.zc + (long long)n * ((G + 1) >> 1) + (gi >> 1));
-            r.zc = 128.0f + (float)((gi & 1) ? (b >> 4) : (b & 15));
+            const uint32_t b = __ldg(a.zc + (long long)n * ((G + 1) >> 1) + (gi >> 1));
+            // fp32 with exponent 134 and z at mantissa bits 16..19 is exactly 128 + z
+            r.zc = __uint_as_float(0x43000000u | (((gi & 1) ? (b >> 4) : (b & 15u)) << 16));
         } else if constexpr (FMT == UQ_INT2_ASYM) {
             const uint16_t* zp = reinterpret_cast<const uint16_t*>(a.zc) + (long long)n * G;
             r.zc = 128.0f + half_bits_f32(__ldg(zp + gi));
@@ -88,7 +89,8 @@ template <int FMT, int M, int M0, int MP>
 __device__ __forceinline__ void tile_pass(const uint8_t* __restrict__ tile, int slice_bytes, int rows,
                                           int lane, const uint16_t* __restrict__ xg, int ldx,
                                           const RowMeta (&meta)[RB], float (&acc)[RB][M],
-                                          const float* __restrict__ lut, bool two_groups) {
+                                          const float* __restrict__ lut, bool two_groups,
+                                          const float* __restrict__ sxt) {
     constexpr int CPL = fmt_cpl(FMT);
     if constexpr (FMT == UQ_INT4_SYM || FMT == UQ_INT4_ASYM || FMT == UQ_K4 || FMT == UQ_INT2_ASYM) {
         // x as bf16 pairs: CPL/2 registers per row of x
@@ -103,15 +105,13 @@ __device__ __forceinline__ void tile_pass(const uint8_t* __restrict__ tile, int 
                 uint4 q = ldg_nc_v4(xp + 8 * v);
                 xr[i][4 * v] = q.x; xr[i][4 * v + 1] = q.y; xr[i][4 * v + 2] = q.z; xr[i][4 * v + 3] = q.w;
             }
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int v = 0; v < XR; ++v) {
-                float t = bf16lo_f32(xr[i][v]) + bf16hi_f32(xr[i][v]);
-                if (v < XR / 2) s0 += t; else s1 += t;
+            // sum of x over the lane's chunk (first / second half for INT2 with group 32),
+            // precomputed per k tile into shared memory at kernel start
+            sx[i] = sxt[(M0 + i) * 32 + lane];
+            sx2[i] = 0.f;
+            if constexpr (FMT == UQ_INT2_ASYM) {
+                if (two_groups) sx2[i] = sxt[(M + M0 + i) * 32 + lane];
             }
-            sx[i] = s0 + s1;
-            sx2[i] = s1;
-            if constexpr (FMT == UQ_INT2_ASYM) { if (two_groups) sx[i] = s0; }
         }
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
@@ -230,20 +230,45 @@ template <int FMT> struct PassPlan {
 template <int FMT, int M, int M0>
 __device__ __forceinline__ void tile_all_passes(const uint8_t* tile, int slice_bytes, int rows, int lane,
                                                 const uint16_t* xg, int ldx, const RowMeta (&meta)[RB],
-                                                float (&acc)[RB][M], const float* lut, bool two_groups) {
+                                                float (&acc)[RB][M], const float* lut, bool two_groups,
+                                                const float* sxt) {
     if constexpr (M0 < M) {
         constexpr int REM = M - M0;
         constexpr int MP = REM < PassPlan<FMT>::MAXP ? REM : PassPlan<FMT>::MAXP;
         tile_pass<FMT, M, M0, MP>(tile, slice_bytes, rows, lane, xg + (long long)M0 * ldx, ldx, meta, acc,
-                                  lut, two_groups);
-        tile_all_passes<FMT, M, M0 + MP>(tile, slice_bytes, rows, lane, xg, ldx, meta, acc, lut, two_groups);
+                                  lut, two_groups, sxt);
+        tile_all_passes<FMT, M, M0 + MP>(tile, slice_bytes, rows, lane, xg, ldx, meta, acc, lut, two_groups, sxt);
     }
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
+// Transposing butterfly: reduces CNT values per lane over the warp.  At each level a lane keeps
+// half of its values and sends the other half to its xor partner, so every sum is formed once, in
+// a fixed order; when one value is left the remaining levels are plain xor sums (commutative, so
+// both partners hold identical bits).  Afterwards lane l holds the totals of value indices
+// idx_out + j for j < max(1, CNT / 32) in v[j].
+template <int CNT>
+__device__ __forceinline__ void warp_reduce_transposed(float (&v)[CNT], int lane, int& idx_out) {
+    int idx = 0;
+    int half = CNT / 2;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+    for (int o = 16; o >= 1; o >>= 1) {
+        if (half >= 1) {
+            const bool up = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < CNT / 2; ++i) {
+                if (i < half) {
+                    const float keep = up ? v[i + half] : v[i];
+                    const float send = up ? v[i] : v[i + half];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+            if (up) idx += half;
+            half >>= 1;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+        }
+    }
+    idx_out = idx;
 }
 
 }  // namespace
@@ -252,12 +277,45 @@ template <int FMT, int M>
 __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int KT = fmt_kt(FMT), CPL = fmt_cpl(FMT);
+    constexpr bool NEEDS_SX = (FMT != UQ_INT8_SYM && FMT != UQ_NF4);
     uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + GEMV_WARPS * GEMV_STAGES * TILE_BYTES);
     float* lut = reinterpret_cast<float*>(bars_all + GEMV_WARPS * GEMV_STAGES);
+    // sx table [kb][h][m][lane]: sum of x[m] over lane chunk (half h of it for INT2 group 32)
+    float* sx_tab = lut + 16;
+    const int KBt = (a.K + KT - 1) / KT;
+    constexpr int HALVES = (FMT == UQ_INT2_ASYM) ? 2 : 1;
     if constexpr (FMT == UQ_NF4) {
         if (threadIdx.x < 16) lut[threadIdx.x] = reinterpret_cast<const float*>(a.zc)[threadIdx.x];
-        __syncthreads();
     }
+    if constexpr (NEEDS_SX) {
+        const bool split = (FMT == UQ_INT2_ASYM) && (a.group == 32);
+        for (int e = threadIdx.x; e < KBt * M * 32; e += blockDim.x) {
+            const int kb = e / (M * 32), m = (e / 32) % M, l = e % 32;
+            const int k0 = kb * KT + l * CPL;
+            float s0 = 0.f, s1 = 0.f;
+            if (k0 < a.K) {
+                const uint16_t* xp = a.x + (long long)m * a.ldx + k0;
+#pragma unroll
+                for (int v = 0; v < CPL / 8; ++v) {
+                    const uint4 q = ldg_nc_v4(xp + 8 * v);
+                    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float t = bf16lo_f32(u[j]) + bf16hi_f32(u[j]);
+                        if (4 * v + j < CPL / 4) s0 += t; else s1 += t;
+                    }
+                }
+            }
+            float* row = sx_tab + (long long)kb * HALVES * M * 32;
+            if (split) {
+                row[m * 32 + l] = s0;
+                row[(M + m) * 32 + l] = s1;
+            } else {
+                row[m * 32 + l] = s0 + s1;
+            }
+        }
+    }
+    if constexpr (FMT == UQ_NF4 || NEEDS_SX) __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int w = blockIdx.x * GEMV_WARPS + warp;
     if (w >= a.P) return;
@@ -318,7 +376,8 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
         }
         if (active)
             tile_all_passes<FMT, M, 0>(ring + s * TILE_BYTES, L.slice_bytes(kb), rows, lane,
-                                       a.x + k0, a.ldx, meta, acc, lut, two_groups);
+                                       a.x + k0, a.ldx, meta, acc, lut, two_groups,
+                                       sx_tab + (long long)kb * HALVES * M * 32);
         __syncwarp();
         if (lane == 0 && t + GEMV_STAGES < t1) {
             fence_proxy_async_smem();
@@ -332,25 +391,37 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
         if (kb == L.KB - 1 || t == t1 - 1) {
             // row block done (for this worker): reduce over lanes, then write y or a partial
             const bool full = (kb == L.KB - 1) && (nb != first_nb || (t0 % L.KB) == 0);
+            // values padded to a power of two (8 rows x M, M <= 8)
+            constexpr int CNT = RB * (M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8);
+            float v[CNT];
+#pragma unroll
+            for (int i = 0; i < CNT; ++i) v[i] = 0.f;
 #pragma unroll
             for (int r = 0; r < RB; ++r)
 #pragma unroll
-                for (int m = 0; m < M; ++m) acc[r][m] = warp_sum(acc[r][m]);
+                for (int m = 0; m < M; ++m) v[r * (CNT / RB) + m] = acc[r][m];
+            int idx = 0;
+            warp_reduce_transposed<CNT>(v, lane, idx);
+            // lane holds the totals of indices idx .. idx + RES - 1; with CNT < 32 several lanes
+            // hold the same total and only the first of them writes it
+            constexpr int RES = CNT >= 32 ? CNT / 32 : 1;
+            constexpr int OWN = CNT >= 32 ? 1 : 32 / CNT;
+            const bool owner = (lane % OWN) == 0;
             if (full) {
 #pragma unroll
-                for (int r = 0; r < RB; ++r)
-#pragma unroll
-                    for (int m = 0; m < M; ++m)
-                        if (r < rows && lane == ((r * M + m) & 31))
-                            a.y[(long long)m * a.ldy + n0 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[r][m]));
+                for (int j = 0; j < RES; ++j) {
+                    const int vr = (idx + j) / (CNT / RB), vm = (idx + j) % (CNT / RB);
+                    if (owner && vr < rows && vm < M)
+                        a.y[(long long)vm * a.ldy + n0 + vr] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+                }
             } else {
                 const int slot = 2 * w + (nb == first_nb ? 0 : 1);
                 float* part = a.partials + (long long)slot * RB * M;
 #pragma unroll
-                for (int r = 0; r < RB; ++r)
-#pragma unroll
-                    for (int m = 0; m < M; ++m)
-                        if (lane == ((r * M + m) & 31)) part[r * M + m] = acc[r][m];
+                for (int j = 0; j < RES; ++j) {
+                    const int vr = (idx + j) / (CNT / RB), vm = (idx + j) % (CNT / RB);
+                    if (owner && vr < rows && vm < M) part[vr * M + vm] = v[j];
+                }
                 __threadfence();
                 __syncwarp();
                 unsigned int old = 0;
@@ -360,14 +431,14 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
                 const int wf = worker_of(tf, a.T, a.P), wl = worker_of(tf + L.KB - 1, a.T, a.P);
                 if (old == (unsigned int)(wl - wf)) {
                     __threadfence();
-                    for (int idx = lane; idx < rows * M; idx += 32) {
+                    for (int e = lane; e < rows * M; e += 32) {
                         float sum = 0.f;
                         for (int w2 = wf; w2 <= wl; ++w2) {
                             const int nb2 = (int)(range_begin(w2, a.T, a.P) / L.KB);
                             const int slot2 = 2 * w2 + (nb == nb2 ? 0 : 1);
-                            sum += __ldcg(a.partials + (long long)slot2 * RB * M + idx);
+                            sum += __ldcg(a.partials + (long long)slot2 * RB * M + e);
                         }
-                        const int r = idx / M, m = idx % M;
+                        const int r = e / M, m = e % M;
                         a.y[(long long)m * a.ldy + n0 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
                     }
                     if (lane == 0) a.tickets[nb] = 0u;
@@ -381,8 +452,10 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
     }
 }
 
-inline size_t gemv_smem_bytes_impl() {
-    return (size_t)GEMV_WARPS * GEMV_STAGES * TILE_BYTES + (size_t)GEMV_WARPS * GEMV_STAGES * 8 + 64;
+inline size_t gemv_smem_bytes_impl(int fmt, int K, int M) {
+    const size_t kbt = (size_t)(K + fmt_kt(fmt) - 1) / fmt_kt(fmt);
+    const size_t sx = (fmt == UQ_INT8_SYM || fmt == UQ_NF4) ? 0 : kbt * (fmt == UQ_INT2_ASYM ? 2 : 1) * M * 32 * 4;
+    return (size_t)GEMV_WARPS * GEMV_STAGES * TILE_BYTES + (size_t)GEMV_WARPS * GEMV_STAGES * 8 + 64 + sx;
 }
 inline size_t gemv_partials_floats_impl(int P, int M) { return (size_t)2 * P * RB * M; }
 
@@ -390,13 +463,13 @@ namespace gemv_detail {
 template <int FMT, int M>
 cudaError_t launch_one(const GemvArgs& a, int grid, cudaStream_t st) {
     static bool configured[64] = {};   // the shared-memory opt-in, once per device
-    const size_t smem = gemv_smem_bytes_impl();
+    const size_t smem = gemv_smem_bytes_impl(FMT, a.K, a.M);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(gemv_kernel<FMT, M>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(gemv_kernel<FMT, M>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }

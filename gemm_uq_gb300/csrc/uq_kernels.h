@@ -36,7 +36,7 @@ struct GemvArgs {
 };
 constexpr int GEMV_WARPS = 8;     // worker warps per CTA
 constexpr int GEMV_STAGES = 4;    // tiles in flight per warp
-size_t gemv_smem_bytes();
+size_t gemv_smem_bytes(int fmt, int K, int M);
 size_t gemv_partials_floats(int P, int M);
 cudaError_t launch_gemv(int fmt, const GemvArgs& a, int grid, cudaStream_t st);
 
