@@ -226,6 +226,10 @@ uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const vo
 
 }  // namespace
 
+namespace uq {
+void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+}  // namespace uq
+
 // =============================================================================================
 extern "C" {
 

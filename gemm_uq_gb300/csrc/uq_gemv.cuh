@@ -6,17 +6,21 @@
 //
 //  * Work is the list of tiles (8 rows x 512 bytes of codes) in row-block-major order.
 //    Every warp is an independent worker that owns a contiguous, equal share of that list
-//    (a "stream-K" split: perfectly balanced over 152 SMs x 8 warps whatever N and K are).
-//  * Each warp keeps GEMV_STAGES tiles in flight: lane 0 issues one 1-D bulk async copy
-//    (cp.async.bulk, completion counted in bytes on an mbarrier) per tile into a
-//    warp-private ring in shared memory; there is no block-level synchronisation.
-//  * Lane l owns the 16-byte column chunk l of every tile row (32 INT4 codes).  Its slice
-//    of x stays in registers while it walks the 8 rows; codes are unpacked with the
-//    magic-exponent trick (bf16 0x4300 | code = 128 + code) and multiplied-accumulated with
-//    fma.rn.f32.bf16 (fp32 accumulate of exact bf16 products).  The +128 offset and the
-//    zero point are removed once per group: sum x*(q - z) = sum x*(128 + q) - (128 + z)*sum x.
-//  * Group scales are applied once per lane chunk (a chunk never spans two groups except
-//    INT2 with group 32, handled as two halves).
+//    (a "stream-K" split: balanced over 152 SMs x 8 warps whatever N and K are).
+//  * Each warp keeps GEMV_STAGES tiles in flight in a warp-private ring in shared memory.
+//    One stage holds a tile's codes (one 1-D bulk async copy, cp.async.bulk, issued by lane 0)
+//    AND the tile's scales / zero points / K4 records (4- or 16-byte cp.async copies issued by
+//    all lanes); both complete on the stage's mbarrier (expect_tx for the bulk bytes, one
+//    cp.async.mbarrier.arrive.noinc per lane), so a tile's metadata is prefetched as deep
+//    as its weights and the consumer never waits on a global load.
+//  * x is copied once per CTA into shared memory (in lane-chunk order, so the per-tile reads
+//    are conflict-free 16-byte loads) together with the per-chunk sums of x; the prologue
+//    runs while the first weight tiles are already in flight.
+//  * Lane l owns the 16-byte column chunk l of every tile row (32 INT4 codes).  Codes are
+//    unpacked with the magic-exponent trick (bf16 0x4300 | code = 128 + code) and multiplied-
+//    accumulated with fma.rn.f32.bf16 (fp32 accumulate of exact bf16 products).  The +128
+//    offset and the zero point are removed once per group:
+//        sum x*(q - z) = sum x*(128 + q) - (128 + z) * sum x.
 //  * A row block whose k range is split between workers is finished by a deterministic
 //    second pass: each contributor stores its fp32 partial sums, takes a ticket, and the
 //    last one sums the partials in worker order (fixed, so results are bit-reproducible)
@@ -25,6 +29,49 @@
 #include "uq_kernels.h"
 
 namespace uq {
+
+// per-format staging constants
+template <int FMT> struct GemvFmt {
+    static constexpr int KT = fmt_kt(FMT);
+    static constexpr int CPL = fmt_cpl(FMT);
+    static constexpr int GT_MAX = KT / 32;                         // groups per tile row at group 32
+    // 32-bit words of metadata staged per tile row: scales (+1 for a misaligned start), zeros
+    static constexpr int SW = (FMT == UQ_K4) ? 16 : GT_MAX / 2 + 1;
+    static constexpr int ZW = (FMT == UQ_INT4_ASYM) ? GT_MAX / 8 + 1 : (FMT == UQ_INT2_ASYM ? GT_MAX / 2 + 1 : 0);
+    static constexpr int MW = SW + ZW;
+    static constexpr int META_BYTES = (RB * MW * 4 + 15) / 16 * 16;
+    static constexpr int STAGE_BYTES = TILE_BYTES + META_BYTES;
+    static constexpr int STAGES = (FMT == UQ_INT2_ASYM) ? 3 : 4;
+    static constexpr bool NEEDS_SX = (FMT != UQ_INT8_SYM && FMT != UQ_NF4);
+    static constexpr int HALVES = (FMT == UQ_INT2_ASYM) ? 2 : 1;
+};
+
+// shared-memory plan; identical on host and device
+struct GemvSmem {
+    size_t ring, bars, lut, sx, x, total;
+};
+__host__ __device__ inline GemvSmem gemv_smem_plan(int fmt, int K, int M, bool x_in_smem) {
+    int stage = 0, stages = 0, cpl = fmt_cpl(fmt), kt = fmt_kt(fmt);
+    switch (fmt) {
+        case UQ_INT4_SYM: stage = GemvFmt<UQ_INT4_SYM>::STAGE_BYTES; stages = GemvFmt<UQ_INT4_SYM>::STAGES; break;
+        case UQ_INT4_ASYM: stage = GemvFmt<UQ_INT4_ASYM>::STAGE_BYTES; stages = GemvFmt<UQ_INT4_ASYM>::STAGES; break;
+        case UQ_INT8_SYM: stage = GemvFmt<UQ_INT8_SYM>::STAGE_BYTES; stages = GemvFmt<UQ_INT8_SYM>::STAGES; break;
+        case UQ_INT2_ASYM: stage = GemvFmt<UQ_INT2_ASYM>::STAGE_BYTES; stages = GemvFmt<UQ_INT2_ASYM>::STAGES; break;
+        case UQ_NF4: stage = GemvFmt<UQ_NF4>::STAGE_BYTES; stages = GemvFmt<UQ_NF4>::STAGES; break;
+        default: stage = GemvFmt<UQ_K4>::STAGE_BYTES; stages = GemvFmt<UQ_K4>::STAGES; break;
+    }
+    const size_t kbt = (size_t)(K + kt - 1) / kt;
+    const bool needs_sx = (fmt != UQ_INT8_SYM && fmt != UQ_NF4);
+    GemvSmem p;
+    p.ring = 0;
+    p.bars = (size_t)GEMV_WARPS * stages * stage;
+    p.lut = p.bars + (size_t)GEMV_WARPS * stages * 8;
+    p.sx = p.lut + 64;
+    p.x = p.sx + (needs_sx ? kbt * (fmt == UQ_INT2_ASYM ? 2 : 1) * M * 32 * 4 : 0);
+    p.x = (p.x + 15) / 16 * 16;
+    p.total = p.x + (x_in_smem ? kbt * M * (cpl / 8) * 32 * 16 : 0);
+    return p;
+}
 
 namespace {
 
@@ -39,6 +86,78 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
 }
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(bar)) : "memory");
+}
+
+// Copy the 4-byte-aligned words covering bytes [lo, lo + len) of `base` into dst (word 0 holds
+// byte lo & ~3).  A word that would reach past `end` (the array's end) is assembled from plain
+// byte loads instead, so nothing outside the caller's buffer is read.
+__device__ __forceinline__ void stage_words(uint32_t* dst, const uint8_t* base, long long lo, int len,
+                                            long long end, int j) {
+    const long long w0 = lo & ~3ll;
+    const long long src = w0 + 4ll * j;
+    if (src >= lo + len) return;
+    if (src + 4 <= end) {
+        cp_async4(dst + j, base + src);
+    } else {
+        uint32_t v = 0;
+        for (int b = 0; b < 4; ++b)
+            if (src + b < end) v |= (uint32_t)__ldg(base + src + b) << (8 * b);
+        dst[j] = v;
+    }
+}
+
+// Issue the copies of tile t into stage buffer `st` (all lanes take part).
+template <int FMT>
+__device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, long long t, uint8_t* st,
+                                           uint64_t* bar, int lane) {
+    using F = GemvFmt<FMT>;
+    const int nb = (int)(t / L.KB), kb = (int)(t % L.KB);
+    const int rows = L.rows(nb), n0 = nb * RB;
+    uint32_t* md = reinterpret_cast<uint32_t*>(st + TILE_BYTES);
+    if constexpr (FMT == UQ_K4) {
+        // 16-byte records: width/256 per row, 16-byte aligned
+        const int recs = L.width(kb) / 256;
+        for (int e = lane; e < rows * recs; e += 32) {
+            const int r = e / recs, j = e % recs;
+            const uint8_t* src = a.scales + ((long long)(n0 + r) * (a.K / 256) + (long long)kb * 4 + j) * 16;
+            cp_async16(md + r * F::MW + 4 * j, src);
+        }
+    } else {
+        const int G = a.K / a.group;
+        const int GT = L.KT / a.group;                 // groups per full tile row
+        const int gc = L.width(kb) / a.group;          // groups in this tile row
+        const long long send = (long long)a.N * G * 2;
+        for (int e = lane; e < rows * F::MW; e += 32) {
+            const int r = e / F::MW, j = e % F::MW;
+            const long long n = n0 + r;
+            if (j < F::SW) {
+                stage_words(md + r * F::MW, a.scales, (n * G + (long long)kb * GT) * 2, gc * 2, send, j);
+            } else if constexpr (FMT == UQ_INT4_ASYM) {
+                const long long ZB = (G + 1) >> 1;
+                stage_words(md + r * F::MW + F::SW, a.zc, n * ZB + (long long)kb * (GT >> 1), (gc + 1) >> 1,
+                            (long long)a.N * ZB, j - F::SW);
+            } else if constexpr (FMT == UQ_INT2_ASYM) {
+                stage_words(md + r * F::MW + F::SW, a.zc, (n * G + (long long)kb * GT) * 2, gc * 2, send, j - F::SW);
+            }
+        }
+    }
+    cp_async_arrive_noinc(bar);
+    __syncwarp();
+    if (lane == 0) {
+        const uint32_t bytes = (uint32_t)(rows * L.slice_bytes(kb));
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(st, a.wq + L.tile_offset(nb, kb), bytes, bar);
+    }
+}
 
 // per-row metadata of the lane's chunk, converted to what the accumulate step needs
 struct RowMeta {
@@ -48,65 +167,74 @@ struct RowMeta {
     float zc2;   // INT2 group-32 second half: 128 + z
 };
 
+// Read row r's metadata for lane chunk starting at k0 from the staged words of tile (nb, kb).
 template <int FMT>
-__device__ __forceinline__ RowMeta load_meta(const GemvArgs& a, int n, int k0) {
-    RowMeta r{0.f, 0.f, 0.f, 0.f};
+__device__ __forceinline__ RowMeta stage_meta(const GemvArgs& a, const Layout& L, const uint8_t* st, int r, int n,
+                                              int kb, int lane) {
+    using F = GemvFmt<FMT>;
+    const uint8_t* row = st + TILE_BYTES + r * F::MW * 4;
+    RowMeta m{0.f, 0.f, 0.f, 0.f};
     if constexpr (FMT == UQ_K4) {
-        const int sb = k0 >> 8, j = (k0 & 255) >> 5;
-        uint4 rec = ldg_nc_v4(a.scales + ((long long)n * (a.K >> 8) + sb) * 16);
-        float d = half_bits_f32((uint16_t)(rec.x & 0xFFFF));
-        float dmin = half_bits_f32((uint16_t)(rec.x >> 16));
-        uint64_t sc48 = (uint64_t)rec.y | ((uint64_t)(rec.z & 0xFFFFu) << 32);
-        uint64_t m48 = (uint64_t)(rec.z >> 16) | ((uint64_t)rec.w << 16);
-        r.s = d * (float)((sc48 >> (6 * j)) & 63);
-        r.s2 = dmin * (float)((m48 >> (6 * j)) & 63);
-        r.zc = 128.0f;
+        const int li = lane >> 3;                  // super-block within the tile row
+        const int j = lane & 7;                    // sub-block
+        const uint4 rec = *reinterpret_cast<const uint4*>(row + 16 * li);
+        const float d = half_bits_f32((uint16_t)(rec.x & 0xFFFF));
+        const float dmin = half_bits_f32((uint16_t)(rec.x >> 16));
+        const uint64_t sc48 = (uint64_t)rec.y | ((uint64_t)(rec.z & 0xFFFFu) << 32);
+        const uint64_t m48 = (uint64_t)(rec.z >> 16) | ((uint64_t)rec.w << 16);
+        m.s = d * (float)((sc48 >> (6 * j)) & 63);
+        m.s2 = dmin * (float)((m48 >> (6 * j)) & 63);
+        m.zc = 128.0f;
     } else {
-        const int G = a.K / a.group;
-        const int gi = k0 / a.group;
-        const uint16_t* sp = reinterpret_cast<const uint16_t*>(a.scales) + (long long)n * G;
-        r.s = half_bits_f32(__ldg(sp + gi));
+        const int G = a.K / a.group, GT = L.KT / a.group;
+        const int li = (lane * F::CPL) / a.group;  // first group of the chunk within the tile row
+        const long long sbyte = ((long long)n * G + (long long)kb * GT) * 2;
+        const uint16_t* sp = reinterpret_cast<const uint16_t*>(row + (sbyte & 3)) + li;
+        m.s = half_bits_f32(sp[0]);
         if constexpr (FMT == UQ_INT4_SYM) {
-            r.zc = 136.0f;
+            m.zc = 136.0f;
         } else if constexpr (FMT == UQ_INT4_ASYM) {
-            const uint32_t b = __ldg(a.zc + (long long)n * ((G + 1) >> 1) + (gi >> 1));
+            const long long ZB = (G + 1) >> 1;
+            const long long zbyte = (long long)n * ZB + (long long)kb * (GT >> 1);
+            const uint32_t b = row[F::SW * 4 + (zbyte & 3) + (li >> 1)];
             // fp32 with exponent 134 and z at mantissa bits 16..19 is exactly 128 + z
-            r.zc = __uint_as_float(0x43000000u | (((gi & 1) ? (b >> 4) : (b & 15u)) << 16));
+            m.zc = __uint_as_float(0x43000000u | (((li & 1) ? (b >> 4) : (b & 15u)) << 16));
         } else if constexpr (FMT == UQ_INT2_ASYM) {
-            const uint16_t* zp = reinterpret_cast<const uint16_t*>(a.zc) + (long long)n * G;
-            r.zc = 128.0f + half_bits_f32(__ldg(zp + gi));
+            const uint16_t* zp = reinterpret_cast<const uint16_t*>(row + F::SW * 4 + (sbyte & 3)) + li;
+            m.zc = 128.0f + half_bits_f32(zp[0]);
             if (a.group == 32) {
-                r.s2 = half_bits_f32(__ldg(sp + gi + 1));
-                r.zc2 = 128.0f + half_bits_f32(__ldg(zp + gi + 1));
+                m.s2 = half_bits_f32(sp[1]);
+                m.zc2 = 128.0f + half_bits_f32(zp[1]);
             }
         }
     }
-    return r;
+    return m;
 }
 
-// One pass over the tile's rows for x rows M0 .. M0+MP-1.  xg points at x[M0][k0].
-template <int FMT, int M, int M0, int MP>
-__device__ __forceinline__ void tile_pass(const uint8_t* __restrict__ tile, int slice_bytes, int rows,
-                                          int lane, const uint16_t* __restrict__ xg, int ldx,
+// One pass over the tile's rows for x rows M0 .. M0+MP-1.
+template <int FMT, int M, int M0, int MP, bool XS>
+__device__ __forceinline__ void tile_pass(const uint8_t* __restrict__ tile, int slice_bytes, int rows, int lane,
+                                          const uint16_t* __restrict__ xg, int ldx, const uint4* __restrict__ xs,
                                           const RowMeta (&meta)[RB], float (&acc)[RB][M],
                                           const float* __restrict__ lut, bool two_groups,
                                           const float* __restrict__ sxt) {
     constexpr int CPL = fmt_cpl(FMT);
+    constexpr int XU = CPL / 8;                    // 16-byte units of x per lane chunk
+    auto load_x = [&](int i, int v) -> uint4 {
+        if constexpr (XS) return xs[((M0 + i) * XU + v) * 32 + lane];
+        else return ldg_nc_v4(xg + (long long)(M0 + i) * ldx + 8 * v);
+    };
     if constexpr (FMT == UQ_INT4_SYM || FMT == UQ_INT4_ASYM || FMT == UQ_K4 || FMT == UQ_INT2_ASYM) {
-        // x as bf16 pairs: CPL/2 registers per row of x
-        constexpr int XR = CPL / 2;
+        constexpr int XR = CPL / 2;                // bf16 pairs of x per lane chunk
         uint32_t xr[MP][XR];
         float sx[MP], sx2[MP];
 #pragma unroll
         for (int i = 0; i < MP; ++i) {
-            const uint16_t* xp = xg + (long long)i * ldx;
 #pragma unroll
-            for (int v = 0; v < XR / 4; ++v) {
-                uint4 q = ldg_nc_v4(xp + 8 * v);
+            for (int v = 0; v < XU; ++v) {
+                const uint4 q = load_x(i, v);
                 xr[i][4 * v] = q.x; xr[i][4 * v + 1] = q.y; xr[i][4 * v + 2] = q.z; xr[i][4 * v + 3] = q.w;
             }
-            // sum of x over the lane's chunk (first / second half for INT2 with group 32),
-            // precomputed per k tile into shared memory at kernel start
             sx[i] = sxt[(M0 + i) * 32 + lane];
             sx2[i] = 0.f;
             if constexpr (FMT == UQ_INT2_ASYM) {
@@ -169,10 +297,9 @@ __device__ __forceinline__ void tile_pass(const uint8_t* __restrict__ tile, int 
         float xf[MP][CPL];
 #pragma unroll
         for (int i = 0; i < MP; ++i) {
-            const uint16_t* xp = xg + (long long)i * ldx;
 #pragma unroll
-            for (int v = 0; v < CPL / 8; ++v) {
-                uint4 q = ldg_nc_v4(xp + 8 * v);
+            for (int v = 0; v < XU; ++v) {
+                const uint4 q = load_x(i, v);
                 const uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -227,17 +354,17 @@ template <int FMT> struct PassPlan {
     static constexpr int MAXP = (FMT == UQ_INT2_ASYM || FMT == UQ_NF4) ? 2 : 4;
 };
 
-template <int FMT, int M, int M0>
+template <int FMT, int M, int M0, bool XS>
 __device__ __forceinline__ void tile_all_passes(const uint8_t* tile, int slice_bytes, int rows, int lane,
-                                                const uint16_t* xg, int ldx, const RowMeta (&meta)[RB],
-                                                float (&acc)[RB][M], const float* lut, bool two_groups,
-                                                const float* sxt) {
+                                                const uint16_t* xg, int ldx, const uint4* xs,
+                                                const RowMeta (&meta)[RB], float (&acc)[RB][M], const float* lut,
+                                                bool two_groups, const float* sxt) {
     if constexpr (M0 < M) {
         constexpr int REM = M - M0;
         constexpr int MP = REM < PassPlan<FMT>::MAXP ? REM : PassPlan<FMT>::MAXP;
-        tile_pass<FMT, M, M0, MP>(tile, slice_bytes, rows, lane, xg + (long long)M0 * ldx, ldx, meta, acc,
-                                  lut, two_groups, sxt);
-        tile_all_passes<FMT, M, M0 + MP>(tile, slice_bytes, rows, lane, xg, ldx, meta, acc, lut, two_groups, sxt);
+        tile_pass<FMT, M, M0, MP, XS>(tile, slice_bytes, rows, lane, xg, ldx, xs, meta, acc, lut, two_groups, sxt);
+        tile_all_passes<FMT, M, M0 + MP, XS>(tile, slice_bytes, rows, lane, xg, ldx, xs, meta, acc, lut, two_groups,
+                                             sxt);
     }
 }
 
@@ -273,31 +400,55 @@ __device__ __forceinline__ void warp_reduce_transposed(float (&v)[CNT], int lane
 
 }  // namespace
 
-template <int FMT, int M>
+template <int FMT, int M, bool XS>
 __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs a) {
+    using F = GemvFmt<FMT>;
+    constexpr int KT = F::KT, CPL = F::CPL, S = F::STAGES;
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int KT = fmt_kt(FMT), CPL = fmt_cpl(FMT);
-    constexpr bool NEEDS_SX = (FMT != UQ_INT8_SYM && FMT != UQ_NF4);
-    uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + GEMV_WARPS * GEMV_STAGES * TILE_BYTES);
-    float* lut = reinterpret_cast<float*>(bars_all + GEMV_WARPS * GEMV_STAGES);
-    // sx table [kb][h][m][lane]: sum of x[m] over lane chunk (half h of it for INT2 group 32)
-    float* sx_tab = lut + 16;
-    const int KBt = (a.K + KT - 1) / KT;
-    constexpr int HALVES = (FMT == UQ_INT2_ASYM) ? 2 : 1;
+    const GemvSmem plan = gemv_smem_plan(FMT, a.K, M, XS);
+    uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + plan.bars);
+    float* lut = reinterpret_cast<float*>(smem + plan.lut);
+    float* sx_tab = reinterpret_cast<float*>(smem + plan.sx);
+    uint4* x_tab = reinterpret_cast<uint4*>(smem + plan.x);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int w = blockIdx.x * GEMV_WARPS + warp;
+    const bool has_work = w < a.P;
+    const Layout L(a.N, a.K, FMT);
+    uint8_t* ring = smem + (size_t)warp * S * F::STAGE_BYTES;
+    uint64_t* bars = bars_all + warp * S;
+    const long long t0 = has_work ? range_begin(w, a.T, a.P) : 0;
+    const long long t1 = has_work ? range_begin(w + 1, a.T, a.P) : 0;
+
+    // 1. start the weight stream before anything else
+    if (has_work) {
+        if (lane == 0) {
+#pragma unroll
+            for (int s = 0; s < S; ++s) mbar_init(&bars[s], 33);   // lane 0's expect_tx + 32 cp.async arrivals
+            fence_barrier_init();
+        }
+        __syncwarp();
+        for (int s = 0; s < S && t0 + s < t1; ++s) issue_tile<FMT>(a, L, t0 + s, ring + s * F::STAGE_BYTES, &bars[s], lane);
+    }
+
+    // 2. CTA prologue: codebook, x in lane-chunk order, per-chunk sums of x
     if constexpr (FMT == UQ_NF4) {
         if (threadIdx.x < 16) lut[threadIdx.x] = reinterpret_cast<const float*>(a.zc)[threadIdx.x];
     }
-    if constexpr (NEEDS_SX) {
+    if constexpr (F::NEEDS_SX || XS) {
+        const int KBt = L.KB;
         const bool split = (FMT == UQ_INT2_ASYM) && (a.group == 32);
         for (int e = threadIdx.x; e < KBt * M * 32; e += blockDim.x) {
             const int kb = e / (M * 32), m = (e / 32) % M, l = e % 32;
             const int k0 = kb * KT + l * CPL;
             float s0 = 0.f, s1 = 0.f;
-            if (k0 < a.K) {
-                const uint16_t* xp = a.x + (long long)m * a.ldx + k0;
+            const bool in = k0 < a.K;
+            const uint16_t* xp = a.x + (long long)m * a.ldx + k0;
 #pragma unroll
-                for (int v = 0; v < CPL / 8; ++v) {
-                    const uint4 q = ldg_nc_v4(xp + 8 * v);
+            for (int v = 0; v < CPL / 8; ++v) {
+                const uint4 q = in ? ldg_nc_v4(xp + 8 * v) : make_uint4(0, 0, 0, 0);
+                if constexpr (XS) x_tab[((kb * M + m) * (CPL / 8) + v) * 32 + l] = q;
+                if constexpr (F::NEEDS_SX) {
                     const uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -306,42 +457,22 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
                     }
                 }
             }
-            float* row = sx_tab + (long long)kb * HALVES * M * 32;
-            if (split) {
-                row[m * 32 + l] = s0;
-                row[(M + m) * 32 + l] = s1;
-            } else {
-                row[m * 32 + l] = s0 + s1;
+            if constexpr (F::NEEDS_SX) {
+                float* row = sx_tab + (long long)kb * F::HALVES * M * 32;
+                if (split) {
+                    row[m * 32 + l] = s0;
+                    row[(M + m) * 32 + l] = s1;
+                } else {
+                    row[m * 32 + l] = s0 + s1;
+                }
             }
         }
     }
-    if constexpr (FMT == UQ_NF4 || NEEDS_SX) __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int w = blockIdx.x * GEMV_WARPS + warp;
-    if (w >= a.P) return;
+    __syncthreads();
+    if (!has_work) return;
 
-    const Layout L(a.N, a.K, FMT);
-    uint8_t* ring = smem + warp * GEMV_STAGES * TILE_BYTES;
-    uint64_t* bars = bars_all + warp * GEMV_STAGES;
-    const long long t0 = range_begin(w, a.T, a.P), t1 = range_begin(w + 1, a.T, a.P);
     const int first_nb = (int)(t0 / L.KB);
     const bool two_groups = (FMT == UQ_INT2_ASYM) && (a.group == 32);
-
-    if (lane == 0) {
-#pragma unroll
-        for (int s = 0; s < GEMV_STAGES; ++s) mbar_init(&bars[s], 1);
-        fence_barrier_init();
-        fence_proxy_async_smem();
-        for (int s = 0; s < GEMV_STAGES && t0 + s < t1; ++s) {
-            const long long t = t0 + s;
-            const int nb = (int)(t / L.KB), kb = (int)(t % L.KB);
-            const uint32_t bytes = (uint32_t)(L.rows(nb) * L.slice_bytes(kb));
-            mbar_arrive_expect_tx(&bars[s], bytes);
-            bulk_g2s(ring + s * TILE_BYTES, a.wq + L.tile_offset(nb, kb), bytes, &bars[s]);
-        }
-    }
-    __syncwarp();
-
     float acc[RB][M];
 #pragma unroll
     for (int r = 0; r < RB; ++r)
@@ -350,43 +481,36 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
 
     for (long long t = t0; t < t1; ++t) {
         const int it = (int)(t - t0);
-        const int s = it % GEMV_STAGES;
-        const uint32_t parity = (uint32_t)((it / GEMV_STAGES) & 1);
+        const int s = it % S;
+        const uint32_t parity = (uint32_t)((it / S) & 1);
         const int nb = (int)(t / L.KB), kb = (int)(t % L.KB);
         const int rows = L.rows(nb);
         const int n0 = nb * RB;
-        const int width = L.width(kb);
-        const bool active = lane * CPL < width;
+        const bool active = lane * CPL < L.width(kb);
         const int k0 = kb * KT + lane * CPL;
+        uint8_t* st = ring + s * F::STAGE_BYTES;
 
-        RowMeta meta[RB];
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            meta[r] = RowMeta{0.f, 0.f, 0.f, 0.f};
-            if (active && r < rows) meta[r] = load_meta<FMT>(a, n0 + r, k0);
-        }
-
-        if (!mbar_wait_bounded(&bars[s], parity, a.fault, FAULT_GEMV_WAIT)) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], parity, a.fault, FAULT_GEMV_WAIT))) {
             // give the copies still in flight a bounded chance to land, then leave
-            for (int j = 1; j < GEMV_STAGES && t + j < t1; ++j) {
-                const int sj = (it + j) % GEMV_STAGES;
-                mbar_wait_bounded(&bars[sj], (uint32_t)(((it + j) / GEMV_STAGES) & 1), a.fault, FAULT_GEMV_WAIT);
+            for (int j = 1; j < S && t + j < t1; ++j) {
+                const int sj = (it + j) % S;
+                mbar_wait_bounded(&bars[sj], (uint32_t)(((it + j) / S) & 1), a.fault, FAULT_GEMV_WAIT);
             }
             return;
         }
-        if (active)
-            tile_all_passes<FMT, M, 0>(ring + s * TILE_BYTES, L.slice_bytes(kb), rows, lane,
-                                       a.x + k0, a.ldx, meta, acc, lut, two_groups,
-                                       sx_tab + (long long)kb * HALVES * M * 32);
-        __syncwarp();
-        if (lane == 0 && t + GEMV_STAGES < t1) {
-            fence_proxy_async_smem();
-            const long long tn = t + GEMV_STAGES;
-            const int nbn = (int)(tn / L.KB), kbn = (int)(tn % L.KB);
-            const uint32_t bytes = (uint32_t)(L.rows(nbn) * L.slice_bytes(kbn));
-            mbar_arrive_expect_tx(&bars[s], bytes);
-            bulk_g2s(ring + s * TILE_BYTES, a.wq + L.tile_offset(nbn, kbn), bytes, &bars[s]);
+        if (active) {
+            RowMeta meta[RB];
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                meta[r] = RowMeta{0.f, 0.f, 0.f, 0.f};
+                if (r < rows) meta[r] = stage_meta<FMT>(a, L, st, r, n0 + r, kb, lane);
+            }
+            tile_all_passes<FMT, M, 0, XS>(st, L.slice_bytes(kb), rows, lane, a.x + k0, a.ldx,
+                                           x_tab + (long long)kb * M * (CPL / 8) * 32, meta, acc, lut, two_groups,
+                                           sx_tab + (long long)kb * F::HALVES * M * 32);
         }
+        __syncwarp();
+        if (t + S < t1) issue_tile<FMT>(a, L, t + S, st, &bars[s], lane);
 
         if (kb == L.KB - 1 || t == t1 - 1) {
             // row block done (for this worker): reduce over lanes, then write y or a partial
@@ -452,44 +576,49 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
     }
 }
 
+inline bool gemv_x_in_smem(int fmt, int K, int M) {
+    return gemv_smem_plan(fmt, K, M, true).total <= 227 * 1024;
+}
 inline size_t gemv_smem_bytes_impl(int fmt, int K, int M) {
-    const size_t kbt = (size_t)(K + fmt_kt(fmt) - 1) / fmt_kt(fmt);
-    const size_t sx = (fmt == UQ_INT8_SYM || fmt == UQ_NF4) ? 0 : kbt * (fmt == UQ_INT2_ASYM ? 2 : 1) * M * 32 * 4;
-    return (size_t)GEMV_WARPS * GEMV_STAGES * TILE_BYTES + (size_t)GEMV_WARPS * GEMV_STAGES * 8 + 64 + sx;
+    return gemv_smem_plan(fmt, K, M, gemv_x_in_smem(fmt, K, M)).total;
 }
 inline size_t gemv_partials_floats_impl(int P, int M) { return (size_t)2 * P * RB * M; }
 
 namespace gemv_detail {
-template <int FMT, int M>
+template <int FMT, int M, bool XS>
 cudaError_t launch_one(const GemvArgs& a, int grid, cudaStream_t st) {
     static bool configured[64] = {};   // the shared-memory opt-in, once per device
-    const size_t smem = gemv_smem_bytes_impl(FMT, a.K, a.M);
+    const size_t smem = gemv_smem_plan(FMT, a.K, M, XS).total;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(gemv_kernel<FMT, M>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        e = cudaFuncSetAttribute(gemv_kernel<FMT, M, XS>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    gemv_kernel<FMT, M><<<grid, GEMV_WARPS * 32, smem, st>>>(a);
+    gemv_kernel<FMT, M, XS><<<grid, GEMV_WARPS * 32, smem, st>>>(a);
     return cudaGetLastError();
 }
-
+template <int FMT, int M>
+cudaError_t launch_xs(const GemvArgs& a, int grid, cudaStream_t st) {
+    if (gemv_x_in_smem(FMT, a.K, M)) return launch_one<FMT, M, true>(a, grid, st);
+    return launch_one<FMT, M, false>(a, grid, st);
+}
 }  // namespace gemv_detail
 
 template <int FMT>
 cudaError_t launch_gemv_fmt(const GemvArgs& a, int grid, cudaStream_t st) {
     switch (a.M) {
-        case 1: return gemv_detail::launch_one<FMT, 1>(a, grid, st);
-        case 2: return gemv_detail::launch_one<FMT, 2>(a, grid, st);
-        case 3: return gemv_detail::launch_one<FMT, 3>(a, grid, st);
-        case 4: return gemv_detail::launch_one<FMT, 4>(a, grid, st);
-        case 5: return gemv_detail::launch_one<FMT, 5>(a, grid, st);
-        case 6: return gemv_detail::launch_one<FMT, 6>(a, grid, st);
-        case 7: return gemv_detail::launch_one<FMT, 7>(a, grid, st);
-        case 8: return gemv_detail::launch_one<FMT, 8>(a, grid, st);
+        case 1: return gemv_detail::launch_xs<FMT, 1>(a, grid, st);
+        case 2: return gemv_detail::launch_xs<FMT, 2>(a, grid, st);
+        case 3: return gemv_detail::launch_xs<FMT, 3>(a, grid, st);
+        case 4: return gemv_detail::launch_xs<FMT, 4>(a, grid, st);
+        case 5: return gemv_detail::launch_xs<FMT, 5>(a, grid, st);
+        case 6: return gemv_detail::launch_xs<FMT, 6>(a, grid, st);
+        case 7: return gemv_detail::launch_xs<FMT, 7>(a, grid, st);
+        case 8: return gemv_detail::launch_xs<FMT, 8>(a, grid, st);
         default: return cudaErrorInvalidValue;
     }
 }

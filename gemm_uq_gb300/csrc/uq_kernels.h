@@ -5,6 +5,9 @@
 
 namespace uq {
 
+// records the message uq_last_error() returns on the calling thread (uq_api.cu)
+void set_last_error(const char* msg);
+
 // offline kernels (uq_pack.cu)
 cudaError_t launch_pack(int fmt, const int8_t* codes, uint8_t* wq, int N, int K, unsigned int* bad,
                         cudaStream_t st);
