@@ -33,6 +33,7 @@ SIGNATURES = {
     "uq_quantize_k4": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P]),
     "uq_pack_zeros": (_I, [_P, _P, _I, _I, _P]),
     "uq_device_fault": (_I, [ctypes.POINTER(ctypes.c_uint)]),
+    "uq_gemm_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
 }
 
 _lib = None
@@ -122,6 +123,15 @@ def gemm(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, zc, N: int, gr
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     _check(lib().uq_gemm(_ptr(x), _ptr(wq), _ptr(scales), _ptr(zc), _ptr(y), M, N, K, group, FORMATS[fmt],
                          _stream(stream)), "uq_gemm")
+    return y
+
+
+def gemm_noalloc(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, zc, N: int, group: int, fmt: str,
+                 y: torch.Tensor, stream=None) -> torch.Tensor:
+    """uq_gemm_noalloc: the GEMV with the library's static scratch (y must be given: nothing is allocated)."""
+    M, K = x.shape
+    _check(lib().uq_gemm_noalloc(_ptr(x), _ptr(wq), _ptr(scales), _ptr(zc), _ptr(y), M, N, K, group, FORMATS[fmt],
+                                 _stream(stream)), "uq_gemm_noalloc")
     return y
 
 

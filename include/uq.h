@@ -179,6 +179,28 @@ uq_status uq_pack_zeros(const uint8_t* zeros, uint8_t* packed, int N, int G, voi
  */
 uq_status uq_device_fault(unsigned int* flag);
 
+/*
+ * uq_gemm_noalloc -- uq_gemm's small-M GEMV for callers that cannot let a library allocate device
+ * memory.  The reference pages have no counterpart: it exists for integration, not for the method.
+ * Such callers include serving runtimes that reserve all device memory at start-up and forbid
+ * later allocation (where cudaMalloc fails or steals memory promised elsewhere), and latency-
+ * critical loops that cannot take the implicit device synchronisation of cudaMalloc/cudaFree.
+ * Same arguments, layouts and result as uq_gemm (x, wq, scales, zeros_or_codebook, y are caller-
+ * owned device buffers), computed with the same GEMV kernel for every M (row blocks of 8; no
+ * tensor-core path), so the output equals uq_gemm's for M <= 15.
+ * Scratch: a 1 MiB static device array inside the library (every GPU that loads the library holds
+ * it until the process exits): room for N <= 524288 and for the split-K partial sums of one row
+ * block of x; larger requests return UQ_ERR_NOMEM with the limit in uq_last_error().  K == 0 returns
+ * UQ_ERR_UNSUPPORTED.  Calls no cudaMalloc, cudaFree or other allocating routine.
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  Every call shares the one
+ * array and clears the part that must start at zero; calls whose kernels overlap on the GPU (for
+ * example on two streams at once) race on it and must be serialised by the caller.
+ */
+uq_status uq_gemm_noalloc(const uint16_t* x, const void* wq, const void* scales,
+                          const void* zeros_or_codebook, uint16_t* y,
+                          int M, int N, int K, int group, uq_fmt fmt, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
