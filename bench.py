@@ -87,8 +87,10 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def read_traffic(workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel."""
+def read_traffic(workload, avg_alg_bytes):
+    """DRAM bytes per launch, from the committed ncu summary when it was taken on the current kernel
+    sources: the captured launch's DRAM/algorithmic byte ratio times this run's average algorithmic
+    bytes per launch (traffic scales with the bytes a launch streams)."""
     path = os.path.join(ROOT, "profiles", f"gemv_{workload}.md")
     if not os.path.exists(path):
         return None
@@ -100,7 +102,7 @@ def read_traffic(workload):
     if vals.get("kernel_source_sha") != kernel_source_hash():
         return None
     try:
-        return float(vals["dram_bytes_per_launch"])
+        return round(float(vals["dram_over_algorithmic"]) * avg_alg_bytes)
     except (KeyError, ValueError):
         return None
 
@@ -244,6 +246,9 @@ def run_uq(args, rank, world, dist):
 
     stream = torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
+    # consecutive linears of a decode step read fixed weights: let each launch stream its weights
+    # while the previous one drains (uq_set_launch_overlap)
+    uq.set_launch_overlap(not args.no_overlap)
 
     def issue(events=None):
         for i, r in enumerate(recs):
@@ -346,7 +351,7 @@ def run_uq(args, rank, world, dist):
     value = total_bytes / (ms * 1e-3) / 1e9
     peak, peak_src = measured_peak()
     achieved = step_bytes / (kern_ms * 1e-3) / 1e9
-    traffic = read_traffic(args.workload) if (M == WORKLOADS[args.workload]["m"] and not args.layers) else None
+    traffic = read_traffic(args.workload, step_bytes / launches) if M == WORKLOADS[args.workload]["m"] else None
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
@@ -358,7 +363,8 @@ def run_uq(args, rank, world, dist):
                    "linears_per_step": launches, "bytes_per_step": step_bytes,
                    "parallelism": f"replicas x{world}",
                    "l2": "no flush: packed weights per step exceed L2 (%.2f GB)" % (step_bytes / 1e9),
-                   "launch": "one CUDA graph per step"},
+                   "launch": "one CUDA graph per step",
+                   "launch_overlap": not args.no_overlap},
         "gpu_launches": launches * args.steps,
         "e2e": {"value": round(step_bytes * args.steps * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": xbuf.numel() * 2, "d2h_bytes_per_step": ybuf.numel() * 2},
@@ -451,6 +457,7 @@ def main():
     ap.add_argument("--m", type=int, default=0, help="override the batch rows M")
     ap.add_argument("--layers", type=int, default=0, help="override the number of layers (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true", help="launch without programmatic dependent launch")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -34,6 +34,7 @@ SIGNATURES = {
     "uq_pack_zeros": (_I, [_P, _P, _I, _I, _P]),
     "uq_device_fault": (_I, [ctypes.POINTER(ctypes.c_uint)]),
     "uq_gemm_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "uq_set_launch_overlap": (_I, [_I]),
 }
 
 _lib = None
@@ -187,6 +188,11 @@ def quantize_k4(w: torch.Tensor, stream=None):
     _check(lib().uq_quantize_k4(_ptr(w), _ptr(codes), _ptr(d), _ptr(dmin), _ptr(sc), _ptr(m), N, K,
                                 _stream(stream)), "uq_quantize_k4")
     return codes, d, dmin, sc, m
+
+
+def set_launch_overlap(enable: bool) -> None:
+    """uq_set_launch_overlap: let GEMV launches prefetch their (constant) weights early."""
+    _check(lib().uq_set_launch_overlap(1 if enable else 0), "uq_set_launch_overlap")
 
 
 def device_fault() -> int:

@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <string>
@@ -157,7 +158,7 @@ uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const 
                    int Mb, int N, int K, int ldx, int ldy, int group, int fmt, cudaStream_t st,
                    const DeviceState& ds, int dev) {
     const uq::Layout L(N, K, fmt);
-    if (uq::gemv_smem_bytes(fmt, K, Mb) > 227 * 1024)
+    if (uq::gemv_smem_bytes(fmt, K, group, Mb) > 227 * 1024)
         return fail(UQ_ERR_UNSUPPORTED, "K=%d is too long for the GEMV's shared-memory x-sum table at M=%d", K, Mb);
     const long long T = (long long)L.NB * L.KB;
     long long P = (long long)ds.sms * uq::GEMV_WARPS;
@@ -209,6 +210,10 @@ uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const vo
         if (e != cudaSuccess) return cuda_fail(e, "column-sum launch");
     }
     uq::TcArgs a;
+    const uq::Layout L(N, K, fmt);
+    a.wq = static_cast<const uint8_t*>(wq);
+    a.rowbytes = L.rowbytes;
+    a.NB = L.NB;
     a.scales = static_cast<const uint8_t*>(scales);
     a.zc = static_cast<const uint8_t*>(zc);
     a.y = y;
@@ -219,7 +224,7 @@ uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const vo
     a.partials = ws->partials;
     a.tickets = ws->tickets;
     a.fault = ds.words;
-    e = uq::launch_tc(fmt, x, static_cast<const uint8_t*>(wq), a, smem, (int)P, st);
+    e = uq::launch_tc(fmt, x, a, smem, (int)P, st);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core launch");
     return UQ_OK;
 }
@@ -228,6 +233,8 @@ uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const vo
 
 namespace uq {
 void set_last_error(const char* msg) { g_last_error = msg ? msg : ""; }
+static std::atomic<int> g_overlap{0};
+bool launch_overlap() { return g_overlap.load(std::memory_order_relaxed) != 0; }
 }  // namespace uq
 
 // =============================================================================================
@@ -251,7 +258,7 @@ uq_status uq_packed_size(int N, int K, int group, uq_fmt fmt, size_t* wq_bytes, 
                          size_t* zeros_bytes) {
     uq_status s = check_shape(N, K, group, fmt);
     if (s != UQ_OK) return s;
-    if (wq_bytes) *wq_bytes = (size_t)N * K * uq::fmt_bits(fmt) / 8;
+    if (wq_bytes) *wq_bytes = (size_t)uq::Layout(N, K, fmt).bytes();
     if (scales_bytes) *scales_bytes = meta_scales_bytes(N, K, group, fmt);
     if (zeros_bytes) *zeros_bytes = meta_zeros_bytes(N, K, group, fmt);
     return UQ_OK;
@@ -416,6 +423,11 @@ uq_status uq_quantize_k4(const float* w, int8_t* codes, uint16_t* d, uint16_t* d
         return fail(UQ_ERR_ALIGN, "pointers must be 16-byte aligned");
     cudaError_t e = uq::launch_quantize_k4(w, codes, d, dmin, sc, m, N, K, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "quantize_k4 launch");
+    return UQ_OK;
+}
+
+uq_status uq_set_launch_overlap(int enable) {
+    uq::g_overlap.store(enable ? 1 : 0);
     return UQ_OK;
 }
 

@@ -1,21 +1,24 @@
 // uq_common.cuh -- packed layout, format traits and PTX helpers shared by the uq kernels (sm_103a).
 //
-// Packed code plane ("pack multiple low-bit values into bytes", "Ultra LLM Engine",
-// section "Quantization"): the N x K code matrix is cut into tiles of RB = 8 rows by
-// 512 bytes of codes (KT = 4096 / bits codes).  The last tile of each row block is
-// narrower when K is not a multiple of KT, the last row block shorter when N is not
-// a multiple of 8.  Each tile is stored contiguously (row-major inside), the tiles
-// of a row block one after another in k order, the row blocks one after another:
+// Packed code plane ("pack multiple low-bit values into bytes", "Ultra LLM Engine", section
+// "Quantization"), laid out for the warp-level tensor-core instruction mma.m16n8k16:
 //
-//     tile(nb, kb) = nb * 8 * rowbytes + rows(nb) * kb * 512,   rowbytes = K * bits / 8
-//
-// so one bulk copy fetches one tile.  Inside a tile row, 32-bit words are in natural
-// k order; inside a word the codes are permuted so that a shift and a mask put two
-// k-consecutive codes into the two halves of a register:
-//     4-bit: code 2p at bits [4p, 4p+4), code 2p+1 at bits [16+4p, 16+4p+4)   (p = 0..3)
-//     2-bit: code 2p at bits [2p, 2p+2), code 2p+1 at bits [16+2p, 16+2p+2)   (p = 0..7)
-//     8-bit: code i at bits [8i, 8i+8)
-// Signed formats are stored biased: INT4_SYM as q + 8, INT8_SYM as q + 128.
+//  * Rows are taken in blocks of 16 (N is padded to Np = a multiple of 16), k in chunks of
+//    kc codes (kc = 64 for 4-bit, 128 for 2-bit, 32 for 8-bit; K is padded to Kp, a multiple
+//    of kc).  A chunk of one row block is 512 bytes: 32 lanes x 16 bytes.
+//  * A tile is 16 rows x KT codes (KT = 1024 / 2048 / 512 codes = 16 chunks = 8 KB); the last
+//    tile of a row block is narrower when Kp is not a multiple of KT.  Tiles of a row block
+//    follow each other in k order, row blocks follow each other:
+//        tile(nb, kb) = nb * 16 * Kp * bits/8 + kb * 8192.
+//  * Inside a chunk, lane L = 4g + c (g = 0..7, c = 0..3) holds, for every 16-wide k block,
+//    the codes of rows g and g + 8 at k = 16b + 4c .. 16b + 4c + 3 -- exactly the A-operand
+//    fragment that thread L feeds to mma.m16n8k16 (with the k slots of the instruction mapped
+//    to 4c..4c+3, a permutation the B operand repeats).  For 4-bit codes one 32-bit word is
+//    one k block: pair p (p = 0..3) sits at bits [4p, 4p+4) (even k) and [16+4p, 20+4p) (odd k),
+//    with p = h + 2*(j >> 1) for row g + 8h and k = 16b + 4c + j: a shift and a mask give the
+//    bf16 pair of register a_p.  2-bit words hold two k blocks (pairs 0..3 and 4..7 at 2-bit
+//    fields); 8-bit words hold the 4 codes of one row (word 2*b' + h of the chunk, b' = block).
+//  * Signed formats are stored biased: INT4_SYM as q + 8, INT8_SYM as q + 128.
 #pragma once
 
 #include <cstdint>
@@ -27,49 +30,74 @@
 
 namespace uq {
 
-constexpr int RB = 8;            // rows per tile
-constexpr int SLICE = 512;       // bytes of codes per row of a full tile
-constexpr int TILE_BYTES = RB * SLICE;
+constexpr int RB = 16;           // rows per row block (the M of mma.m16n8k16)
+constexpr int CHUNK = 512;       // bytes of one k chunk of a row block
+constexpr int TILE_BYTES = 8192; // a full tile: 16 chunks
 
 __host__ __device__ constexpr int fmt_bits(int fmt) {
     return fmt == UQ_INT8_SYM ? 8 : (fmt == UQ_INT2_ASYM ? 2 : 4);
 }
-__host__ __device__ constexpr int fmt_kt(int fmt) { return 4096 / fmt_bits(fmt); }     // codes per tile row
-__host__ __device__ constexpr int fmt_cpl(int fmt) { return 128 / fmt_bits(fmt); }     // codes per 16-byte lane chunk
-__host__ __device__ constexpr int fmt_cpw(int fmt) { return 32 / fmt_bits(fmt); }      // codes per 32-bit word
+__host__ __device__ constexpr int fmt_kt(int fmt) { return 4096 / fmt_bits(fmt); }        // codes per tile row
+__host__ __device__ constexpr int fmt_kc(int fmt) { return CHUNK * 8 / fmt_bits(fmt) / RB; }   // codes per chunk row
+__host__ __device__ constexpr int fmt_cpw(int fmt) { return 32 / fmt_bits(fmt); }            // codes per 32-bit word
 __host__ __device__ constexpr int fmt_bias(int fmt) {
     return fmt == UQ_INT4_SYM ? 8 : (fmt == UQ_INT8_SYM ? 128 : 0);
 }
 
-// Bit position of code i (0 <= i < codes per word) inside its 32-bit word.
-__host__ __device__ inline int code_bitpos(int bits, int i) {
-    if (bits == 8) return 8 * i;
-    return (i & 1) ? 16 + bits * (i >> 1) : bits * (i >> 1);
-}
-
 // Geometry of one weight matrix in the packed layout.
 struct Layout {
-    int N, K, bits, KT;
-    int NB, KB;              // row blocks, k tiles
-    long long rowbytes;      // K * bits / 8
+    int N, K, bits, KT, kc, Np, Kp, NB, KB;
+    long long rowbytes;      // Kp * bits / 8
 
     __host__ __device__ Layout(int n, int k, int fmt)
-        : N(n), K(k), bits(fmt_bits(fmt)), KT(fmt_kt(fmt)),
-          NB((n + RB - 1) / RB), KB((k + fmt_kt(fmt) - 1) / fmt_kt(fmt)),
-          rowbytes((long long)k * fmt_bits(fmt) / 8) {}
-
-    __host__ __device__ int rows(int nb) const { int r = N - nb * RB; return r < RB ? r : RB; }
-    __host__ __device__ int width(int kb) const { int w = K - kb * KT; return w < KT ? w : KT; }
-    __host__ __device__ int slice_bytes(int kb) const { return width(kb) * bits / 8; }
-    __host__ __device__ long long tile_offset(int nb, int kb) const {
-        return (long long)nb * RB * rowbytes + (long long)rows(nb) * kb * SLICE;
+        : N(n), K(k), bits(fmt_bits(fmt)), KT(fmt_kt(fmt)), kc(fmt_kc(fmt)),
+          Np((n + RB - 1) / RB * RB), Kp((k + fmt_kc(fmt) - 1) / fmt_kc(fmt) * fmt_kc(fmt)),
+          NB((n + RB - 1) / RB), KB(0), rowbytes(0) {
+        KB = (Kp + KT - 1) / KT;
+        rowbytes = (long long)Kp * bits / 8;
     }
-    // byte offset of the 32-bit word holding code k of row n
-    __host__ __device__ long long word_offset(int n, int k) const {
-        int nb = n / RB, r = n % RB, kb = k / KT, kk = k % KT;
-        return tile_offset(nb, kb) + (long long)r * slice_bytes(kb) + (long long)(kk / (32 / bits)) * 4;
+    __host__ __device__ long long bytes() const { return (long long)Np * rowbytes; }
+    __host__ __device__ int width(int kb) const { int w = Kp - kb * KT; return w < KT ? w : KT; }
+    __host__ __device__ int chunks(int kb) const { return width(kb) / kc; }
+    __host__ __device__ int tile_bytes(int kb) const { return chunks(kb) * CHUNK; }
+    __host__ __device__ long long tile_offset(int nb, int kb) const {
+        return (long long)nb * RB * rowbytes + (long long)kb * TILE_BYTES;
+    }
+    // Row and k of code slot `s` of the 32-bit word at byte offset `off` (a multiple of 4).
+    // Slots: 4-bit s = 2p + hi (p = pair 0..3), 2-bit s = 2p + hi (p = 0..7), 8-bit s = byte.
+    __host__ __device__ void slot_nk(long long off, int s, int* n, int* k) const {
+        const long long rbb = (long long)RB * rowbytes;
+        const int nb = (int)(off / rbb);
+        const long long rem = off % rbb;
+        const int kb = (int)(rem / TILE_BYTES);
+        const int rem2 = (int)(rem % TILE_BYTES);
+        const int q = rem2 / CHUNK, L = (rem2 % CHUNK) / 16, i = (rem2 % 16) / 4;
+        const int g = L >> 2, c = L & 3;
+        const int k0 = kb * KT + q * kc;
+        int r = 0, kk = 0;
+        if (bits == 4) {
+            const int p = s >> 1, hi = s & 1;
+            r = 8 * (p & 1) + g;
+            kk = i * 16 + 4 * c + 2 * (p >> 1) + hi;
+        } else if (bits == 2) {
+            const int p = s >> 1, hi = s & 1, bb = p >> 2, pp = p & 3;
+            r = 8 * (pp & 1) + g;
+            kk = (2 * i + bb) * 16 + 4 * c + 2 * (pp >> 1) + hi;
+        } else {
+            r = 8 * (i & 1) + g;
+            kk = (i >> 1) * 16 + 4 * c + s;
+        }
+        *n = nb * RB + r;
+        *k = k0 + kk;
     }
 };
+
+// bit position of code slot s inside its word (see Layout::slot_nk)
+__host__ __device__ inline int slot_bitpos(int bits, int s) {
+    if (bits == 8) return 8 * s;
+    const int p = s >> 1, hi = s & 1;
+    return bits * p + 16 * hi;
+}
 
 // ---------------------------------------------------------------------------------------------
 // Unpacking (shared by the debug exports and the GEMV/GEMM kernels).

@@ -1,76 +1,90 @@
-// uq_gemv.cuh -- small-M (M <= 8) fused dequantize + GEMV/GEMM on CUDA cores, sm_103a.
+// uq_gemv.cuh -- small-M (M <= 8) fused dequantize + GEMV/GEMM, sm_103a.
 //
 // "Ultra LLM Engine", section "Fused Kernels": dequantized-weight GEMV for single-token
-// decode and GEMM for batched decode.  Decode is bound by streaming the packed weights
-// from HBM once, so the kernel is organised around that stream:
+// decode and GEMM for batched decode.  Decode is bound by streaming the packed weights from
+// HBM once; on this GPU the arithmetic of a CUDA-core dot product (unpack, widen, FMA: about
+// three issue slots per 4-bit weight) cannot keep up with HBM, so the kernel is organised to
+// spend as few instructions per weight as possible:
 //
-//  * Work is the list of tiles (8 rows x 512 bytes of codes) in row-block-major order.
-//    Every warp is an independent worker that owns a contiguous, equal share of that list
-//    (a "stream-K" split: balanced over 152 SMs x 8 warps whatever N and K are).
-//  * Each warp keeps GEMV_STAGES tiles in flight in a warp-private ring in shared memory.
-//    One stage holds a tile's codes (one 1-D bulk async copy, cp.async.bulk, issued by lane 0)
-//    AND the tile's scales / zero points / K4 records (4- or 16-byte cp.async copies issued by
-//    all lanes); both complete on the stage's mbarrier (expect_tx for the bulk bytes, one
-//    cp.async.mbarrier.arrive.noinc per lane), so a tile's metadata is prefetched as deep
-//    as its weights and the consumer never waits on a global load.
-//  * x is copied once per CTA into shared memory (in lane-chunk order, so the per-tile reads
-//    are conflict-free 16-byte loads) together with the per-chunk sums of x; the prologue
-//    runs while the first weight tiles are already in flight.
-//  * Lane l owns the 16-byte column chunk l of every tile row (32 INT4 codes).  Codes are
-//    unpacked with the magic-exponent trick (bf16 0x4300 | code = 128 + code) and multiplied-
-//    accumulated with fma.rn.f32.bf16 (fp32 accumulate of exact bf16 products).  The +128
-//    offset and the zero point are removed once per group:
-//        sum x*(q - z) = sum x*(128 + q) - (128 + z) * sum x.
-//  * A row block whose k range is split between workers is finished by a deterministic
-//    second pass: each contributor stores its fp32 partial sums, takes a ticket, and the
-//    last one sums the partials in worker order (fixed, so results are bit-reproducible)
-//    and writes y.  No worker ever waits for another.
+//  * Work is the list of tiles (16 rows x 8 KB of codes) in row-block-major order.  Every warp
+//    is an independent worker that owns a contiguous, equal share of that list (a "stream-K"
+//    split: balanced over all SMs whatever N and K are).
+//  * Each warp keeps a ring of stages in shared memory.  A stage holds a tile's codes (one
+//    1-D bulk async copy, cp.async.bulk, issued by lane 0) and the tile's scales / zero points /
+//    K4 records (4- or 16-byte cp.async copies issued by all lanes); both complete on the
+//    stage's mbarrier (expect_tx for the bulk bytes, one cp.async.mbarrier.arrive.noinc per
+//    lane), so metadata is prefetched as deep as the weights.
+//  * x is copied once per CTA into shared memory (one bulk copy per row, rows padded so the
+//    rows of a B fragment hit different banks), then the per-group sums of x are formed from it;
+//    the prologue runs while the first weight tiles are in flight.
+//  * 4-bit and 2-bit codes: the packed plane is in mma.m16n8k16 A-fragment order, so one
+//    16-byte load per lane, a shift and a lop3 per register (magic exponent: bf16 0x4300 | code
+//    = 128 + code) give four A fragments, and the warp-wide mma.sync (bf16 x bf16 -> fp32)
+//    does the multiply-accumulate and the reduction over the 16-wide k block in one
+//    instruction; the M <= 8 activation rows are the N = 8 side of the instruction, so every
+//    M <= 8 costs the same.  Per quantization group the fp32 accumulators are scaled:
+//        y += s * (sum x*(128 + q) - (128 + z) * sum x).
+//  * INT8 and NF4 (whose codes do not map onto bf16 exactly by bit tricks) use CUDA-core FMAs
+//    on the same layout; the four lanes sharing a row are reduced with warp shuffles.
+//  * A row block whose k range is split between workers is finished by a deterministic second
+//    pass: each contributor stores its fp32 partial sums, takes a ticket, and the last one sums
+//    the partials in worker order (fixed, so results are bit-reproducible) and writes y.  No
+//    worker ever waits for another.
 #pragma once
 #include "uq_kernels.h"
 
 namespace uq {
 
-// per-format staging constants
 template <int FMT> struct GemvFmt {
+    static constexpr int BITS = fmt_bits(FMT);
     static constexpr int KT = fmt_kt(FMT);
-    static constexpr int CPL = fmt_cpl(FMT);
+    static constexpr int KC = fmt_kc(FMT);
+    static constexpr int BPC = KC / 16;                            // 16-wide k blocks per chunk
+    static constexpr bool MMA = (FMT == UQ_INT4_SYM || FMT == UQ_INT4_ASYM || FMT == UQ_K4 || FMT == UQ_INT2_ASYM);
     static constexpr int GT_MAX = KT / 32;                         // groups per tile row at group 32
     // 32-bit words of metadata staged per tile row: scales (+1 for a misaligned start), zeros
-    static constexpr int SW = (FMT == UQ_K4) ? 16 : GT_MAX / 2 + 1;
-    static constexpr int ZW = (FMT == UQ_INT4_ASYM) ? GT_MAX / 8 + 1 : (FMT == UQ_INT2_ASYM ? GT_MAX / 2 + 1 : 0);
+    // (rounded up to 4 words so 16-byte copies land 16-byte aligned)
+    static constexpr int SW = (FMT == UQ_K4) ? 16 : (GT_MAX / 2 + 1 + 3) / 4 * 4;
+    static constexpr int ZW = (FMT == UQ_INT4_ASYM) ? (GT_MAX / 8 + 1 + 3) / 4 * 4
+                            : (FMT == UQ_INT2_ASYM ? (GT_MAX / 2 + 1 + 3) / 4 * 4 : 0);
     static constexpr int MW = SW + ZW;
     static constexpr int META_BYTES = (RB * MW * 4 + 15) / 16 * 16;
     static constexpr int STAGE_BYTES = TILE_BYTES + META_BYTES;
     static constexpr int STAGES = (FMT == UQ_INT2_ASYM) ? 3 : 4;
-    static constexpr bool NEEDS_SX = (FMT != UQ_INT8_SYM && FMT != UQ_NF4);
-    static constexpr int HALVES = (FMT == UQ_INT2_ASYM) ? 2 : 1;
+    static constexpr bool NEEDS_SX = MMA;                          // per-group sums of x
 };
+
+// bytes per row of x in shared memory: the row zero-padded to Kp plus 32 bytes, so the rows of a
+// B fragment (one 8-byte load per row) fall into different banks
+__host__ __device__ inline size_t gemv_x_stride(int Kp) { return (size_t)Kp * 2 + 32; }
 
 // shared-memory plan; identical on host and device
 struct GemvSmem {
-    size_t ring, bars, lut, sx, x, total;
+    size_t bars, lut, sx, x, total;
 };
-__host__ __device__ inline GemvSmem gemv_smem_plan(int fmt, int K, int M, bool x_in_smem) {
-    int stage = 0, stages = 0, cpl = fmt_cpl(fmt), kt = fmt_kt(fmt);
-    switch (fmt) {
-        case UQ_INT4_SYM: stage = GemvFmt<UQ_INT4_SYM>::STAGE_BYTES; stages = GemvFmt<UQ_INT4_SYM>::STAGES; break;
-        case UQ_INT4_ASYM: stage = GemvFmt<UQ_INT4_ASYM>::STAGE_BYTES; stages = GemvFmt<UQ_INT4_ASYM>::STAGES; break;
-        case UQ_INT8_SYM: stage = GemvFmt<UQ_INT8_SYM>::STAGE_BYTES; stages = GemvFmt<UQ_INT8_SYM>::STAGES; break;
-        case UQ_INT2_ASYM: stage = GemvFmt<UQ_INT2_ASYM>::STAGE_BYTES; stages = GemvFmt<UQ_INT2_ASYM>::STAGES; break;
-        case UQ_NF4: stage = GemvFmt<UQ_NF4>::STAGE_BYTES; stages = GemvFmt<UQ_NF4>::STAGES; break;
-        default: stage = GemvFmt<UQ_K4>::STAGE_BYTES; stages = GemvFmt<UQ_K4>::STAGES; break;
-    }
-    const size_t kbt = (size_t)(K + kt - 1) / kt;
-    const bool needs_sx = (fmt != UQ_INT8_SYM && fmt != UQ_NF4);
+template <int FMT>
+__host__ __device__ inline GemvSmem gemv_smem_plan_t(int K, int group, int M, bool x_in_smem) {
+    using F = GemvFmt<FMT>;
+    const int Kp = (K + F::KC - 1) / F::KC * F::KC;
+    const int gs = (FMT == UQ_K4) ? 32 : group;
     GemvSmem p;
-    p.ring = 0;
-    p.bars = (size_t)GEMV_WARPS * stages * stage;
-    p.lut = p.bars + (size_t)GEMV_WARPS * stages * 8;
+    p.bars = (size_t)GEMV_WARPS * F::STAGES * F::STAGE_BYTES;
+    p.lut = p.bars + (size_t)(GEMV_WARPS * F::STAGES + 1) * 8;     // + the x mbarrier
     p.sx = p.lut + 64;
-    p.x = p.sx + (needs_sx ? kbt * (fmt == UQ_INT2_ASYM ? 2 : 1) * M * 32 * 4 : 0);
-    p.x = (p.x + 15) / 16 * 16;
-    p.total = p.x + (x_in_smem ? kbt * M * (cpl / 8) * 32 * 16 : 0);
+    p.x = p.sx + (F::NEEDS_SX ? (size_t)((Kp + gs - 1) / gs) * 8 * 4 : 0);   // sums padded to 8 columns
+    p.x = (p.x + 127) / 128 * 128;
+    p.total = p.x + (x_in_smem ? (size_t)M * gemv_x_stride(Kp) : 0);
     return p;
+}
+__host__ __device__ inline GemvSmem gemv_smem_plan(int fmt, int K, int group, int M, bool x_in_smem) {
+    switch (fmt) {
+        case UQ_INT4_SYM: return gemv_smem_plan_t<UQ_INT4_SYM>(K, group, M, x_in_smem);
+        case UQ_INT4_ASYM: return gemv_smem_plan_t<UQ_INT4_ASYM>(K, group, M, x_in_smem);
+        case UQ_INT8_SYM: return gemv_smem_plan_t<UQ_INT8_SYM>(K, group, M, x_in_smem);
+        case UQ_INT2_ASYM: return gemv_smem_plan_t<UQ_INT2_ASYM>(K, group, M, x_in_smem);
+        case UQ_NF4: return gemv_smem_plan_t<UQ_NF4>(K, group, M, x_in_smem);
+        default: return gemv_smem_plan_t<UQ_K4>(K, group, M, x_in_smem);
+    }
 }
 
 namespace {
@@ -86,6 +100,11 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
 }
+__device__ __forceinline__ uint2 ldg_nc_v2(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
 }
@@ -96,6 +115,25 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(bar)) : "memory");
 }
 
+// D += A * B for one 16 x 8 x 16 block (bf16 inputs, fp32 accumulate)
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D = A * B (accumulator input zero)
+__device__ __forceinline__ void mma_bf16_zero(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+    const float z = 0.f;
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
+}
+
 // Copy the 4-byte-aligned words covering bytes [lo, lo + len) of `base` into dst (word 0 holds
 // byte lo & ~3).  A word that would reach past `end` (the array's end) is assembled from plain
 // byte loads instead, so nothing outside the caller's buffer is read.
@@ -103,7 +141,7 @@ __device__ __forceinline__ void stage_words(uint32_t* dst, const uint8_t* base, 
                                             long long end, int j) {
     const long long w0 = lo & ~3ll;
     const long long src = w0 + 4ll * j;
-    if (src >= lo + len) return;
+    if (len <= 0 || src >= lo + len) return;
     if (src + 4 <= end) {
         cp_async4(dst + j, base + src);
     } else {
@@ -114,288 +152,129 @@ __device__ __forceinline__ void stage_words(uint32_t* dst, const uint8_t* base, 
     }
 }
 
+// Per-kernel constants of the metadata layout (divisions done once).
+struct MetaConst {
+    int G;            // scale groups per row (flat formats)
+    int GT;           // groups per full tile row
+    int ZB;           // bytes of INT4 zero nibbles per row
+    int S4;           // K4 super-blocks per row
+    bool aligned;     // every tile row's scale slice is 16-byte aligned and a multiple of 16 bytes
+};
+
 // Issue the copies of tile t into stage buffer `st` (all lanes take part).
 template <int FMT>
-__device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, long long t, uint8_t* st,
-                                           uint64_t* bar, int lane) {
+__device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, const MetaConst& mc, int nb, int kb,
+                                           uint8_t* st, uint64_t* bar, int lane) {
     using F = GemvFmt<FMT>;
-    const int nb = (int)(t / L.KB), kb = (int)(t % L.KB);
-    const int rows = L.rows(nb), n0 = nb * RB;
+    const int n0 = nb * RB;
+    const int rows = (a.N - n0) < RB ? (a.N - n0) : RB;            // rows with metadata
     uint32_t* md = reinterpret_cast<uint32_t*>(st + TILE_BYTES);
     if constexpr (FMT == UQ_K4) {
-        // 16-byte records: width/256 per row, 16-byte aligned
-        const int recs = L.width(kb) / 256;
+        // 16-byte records: one per 256 k of the tile row that lies inside K
+        const int sb0 = kb * (F::KT / 256);
+        int recs = mc.S4 - sb0;
+        if (recs > F::KT / 256) recs = F::KT / 256;
         for (int e = lane; e < rows * recs; e += 32) {
             const int r = e / recs, j = e % recs;
-            const uint8_t* src = a.scales + ((long long)(n0 + r) * (a.K / 256) + (long long)kb * 4 + j) * 16;
-            cp_async16(md + r * F::MW + 4 * j, src);
+            cp_async16(md + r * F::MW + 4 * j, a.scales + ((long long)(n0 + r) * mc.S4 + sb0 + j) * 16);
+        }
+    } else if (mc.aligned) {
+        // scale slices of GT halves (16-byte multiples, 16-byte aligned): 16-byte copies; INT4
+        // zero slices of GT/2 bytes: 4-byte copies; INT2 zero slices like the scales
+        const int sv = mc.GT / 8;                       // 16-byte vectors of scales per row
+        const int zv = (FMT == UQ_INT4_ASYM) ? mc.GT / 8 : ((FMT == UQ_INT2_ASYM) ? sv : 0);
+        const int per = sv + zv;
+        for (int e = lane; e < rows * per; e += 32) {
+            const int r = e / per, j = e % per;
+            const long long n = n0 + r;
+            if (j < sv) {
+                cp_async16(md + r * F::MW + 4 * j, a.scales + (n * mc.G + (long long)kb * mc.GT) * 2 + 16 * j);
+            } else if constexpr (FMT == UQ_INT4_ASYM) {
+                cp_async4(md + r * F::MW + F::SW + (j - sv),
+                          a.zc + n * mc.ZB + (long long)kb * (mc.GT >> 1) + 4 * (j - sv));
+            } else if constexpr (FMT == UQ_INT2_ASYM) {
+                cp_async16(md + r * F::MW + F::SW + 4 * (j - sv), a.zc + (n * mc.G + (long long)kb * mc.GT) * 2 + 16 * (j - sv));
+            }
         }
     } else {
-        const int G = a.K / a.group;
-        const int GT = L.KT / a.group;                 // groups per full tile row
-        const int gc = L.width(kb) / a.group;          // groups in this tile row
-        const long long send = (long long)a.N * G * 2;
+        int gc = mc.G - kb * mc.GT;                     // groups of this tile row inside K
+        if (gc > mc.GT) gc = mc.GT;
+        const long long send = (long long)a.N * mc.G * 2;
         for (int e = lane; e < rows * F::MW; e += 32) {
             const int r = e / F::MW, j = e % F::MW;
             const long long n = n0 + r;
             if (j < F::SW) {
-                stage_words(md + r * F::MW, a.scales, (n * G + (long long)kb * GT) * 2, gc * 2, send, j);
+                stage_words(md + r * F::MW, a.scales, (n * mc.G + (long long)kb * mc.GT) * 2, gc * 2, send, j);
             } else if constexpr (FMT == UQ_INT4_ASYM) {
-                const long long ZB = (G + 1) >> 1;
-                stage_words(md + r * F::MW + F::SW, a.zc, n * ZB + (long long)kb * (GT >> 1), (gc + 1) >> 1,
-                            (long long)a.N * ZB, j - F::SW);
+                stage_words(md + r * F::MW + F::SW, a.zc, n * mc.ZB + (long long)kb * (mc.GT >> 1), (gc + 1) >> 1,
+                            (long long)a.N * mc.ZB, j - F::SW);
             } else if constexpr (FMT == UQ_INT2_ASYM) {
-                stage_words(md + r * F::MW + F::SW, a.zc, (n * G + (long long)kb * GT) * 2, gc * 2, send, j - F::SW);
+                stage_words(md + r * F::MW + F::SW, a.zc, (n * mc.G + (long long)kb * mc.GT) * 2, gc * 2, send,
+                            j - F::SW);
             }
         }
     }
     cp_async_arrive_noinc(bar);
     __syncwarp();
     if (lane == 0) {
-        const uint32_t bytes = (uint32_t)(rows * L.slice_bytes(kb));
+        const uint32_t bytes = (uint32_t)L.tile_bytes(kb);
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, bytes);
         bulk_g2s(st, a.wq + L.tile_offset(nb, kb), bytes, bar);
     }
 }
 
-// per-row metadata of the lane's chunk, converted to what the accumulate step needs
-struct RowMeta {
-    float s;     // scale (s, a, or d*sc for K4)
-    float zc;    // value subtracted per unit of sum(x): 128 + z (INT*), 136 (INT4_SYM), 128 (K4)
-    float s2;    // INT2 group-32 second half: scale;  K4: dmin*m
-    float zc2;   // INT2 group-32 second half: 128 + z
-};
-
-// Read row r's metadata for lane chunk starting at k0 from the staged words of tile (nb, kb).
+// Pointers to row r's staged scales (fp16) and zero points for tile kb: the staged words start
+// at the word holding the row's first group, so only the parity / low bits of its offset matter.
 template <int FMT>
-__device__ __forceinline__ RowMeta stage_meta(const GemvArgs& a, const Layout& L, const uint8_t* st, int r, int n,
-                                              int kb, int lane) {
+struct RowPtrs {
+    const uint16_t* s;
+    const uint8_t* z;
+};
+template <int FMT>
+__device__ __forceinline__ RowPtrs<FMT> row_ptrs(const uint8_t* st, const MetaConst& mc, int r, int n, int kb) {
     using F = GemvFmt<FMT>;
     const uint8_t* row = st + TILE_BYTES + r * F::MW * 4;
-    RowMeta m{0.f, 0.f, 0.f, 0.f};
-    if constexpr (FMT == UQ_K4) {
-        const int li = lane >> 3;                  // super-block within the tile row
-        const int j = lane & 7;                    // sub-block
-        const uint4 rec = *reinterpret_cast<const uint4*>(row + 16 * li);
-        const float d = half_bits_f32((uint16_t)(rec.x & 0xFFFF));
-        const float dmin = half_bits_f32((uint16_t)(rec.x >> 16));
-        const uint64_t sc48 = (uint64_t)rec.y | ((uint64_t)(rec.z & 0xFFFFu) << 32);
-        const uint64_t m48 = (uint64_t)(rec.z >> 16) | ((uint64_t)rec.w << 16);
-        m.s = d * (float)((sc48 >> (6 * j)) & 63);
-        m.s2 = dmin * (float)((m48 >> (6 * j)) & 63);
-        m.zc = 128.0f;
+    const unsigned first = (unsigned)n * (unsigned)mc.G + (unsigned)kb * (unsigned)mc.GT;   // low bits only
+    RowPtrs<FMT> p;
+    p.s = reinterpret_cast<const uint16_t*>(row + 2 * (first & 1u));
+    if constexpr (FMT == UQ_INT4_ASYM) {
+        const unsigned zfirst = (unsigned)n * (unsigned)mc.ZB + (unsigned)kb * (unsigned)(mc.GT >> 1);
+        p.z = row + F::SW * 4 + (zfirst & 3u);
+    } else if constexpr (FMT == UQ_INT2_ASYM) {
+        p.z = row + F::SW * 4 + 2 * (first & 1u);
     } else {
-        const int G = a.K / a.group, GT = L.KT / a.group;
-        const int li = (lane * F::CPL) / a.group;  // first group of the chunk within the tile row
-        const long long sbyte = ((long long)n * G + (long long)kb * GT) * 2;
-        const uint16_t* sp = reinterpret_cast<const uint16_t*>(row + (sbyte & 3)) + li;
-        m.s = half_bits_f32(sp[0]);
-        if constexpr (FMT == UQ_INT4_SYM) {
-            m.zc = 136.0f;
-        } else if constexpr (FMT == UQ_INT4_ASYM) {
-            const long long ZB = (G + 1) >> 1;
-            const long long zbyte = (long long)n * ZB + (long long)kb * (GT >> 1);
-            const uint32_t b = row[F::SW * 4 + (zbyte & 3) + (li >> 1)];
-            // fp32 with exponent 134 and z at mantissa bits 16..19 is exactly 128 + z
-            m.zc = __uint_as_float(0x43000000u | (((li & 1) ? (b >> 4) : (b & 15u)) << 16));
-        } else if constexpr (FMT == UQ_INT2_ASYM) {
-            const uint16_t* zp = reinterpret_cast<const uint16_t*>(row + F::SW * 4 + (sbyte & 3)) + li;
-            m.zc = 128.0f + half_bits_f32(zp[0]);
-            if (a.group == 32) {
-                m.s2 = half_bits_f32(sp[1]);
-                m.zc2 = 128.0f + half_bits_f32(zp[1]);
-            }
-        }
+        p.z = row;
     }
-    return m;
+    return p;
 }
 
-// One pass over the tile's rows for x rows M0 .. M0+MP-1.
-template <int FMT, int M, int M0, int MP, bool XS>
-__device__ __forceinline__ void tile_pass(const uint8_t* __restrict__ tile, int slice_bytes, int rows, int lane,
-                                          const uint16_t* __restrict__ xg, int ldx, const uint4* __restrict__ xs,
-                                          const RowMeta (&meta)[RB], float (&acc)[RB][M],
-                                          const float* __restrict__ lut, bool two_groups,
-                                          const float* __restrict__ sxt) {
-    constexpr int CPL = fmt_cpl(FMT);
-    constexpr int XU = CPL / 8;                    // 16-byte units of x per lane chunk
-    auto load_x = [&](int i, int v) -> uint4 {
-        if constexpr (XS) return xs[((M0 + i) * XU + v) * 32 + lane];
-        else return ldg_nc_v4(xg + (long long)(M0 + i) * ldx + 8 * v);
-    };
-    if constexpr (FMT == UQ_INT4_SYM || FMT == UQ_INT4_ASYM || FMT == UQ_K4 || FMT == UQ_INT2_ASYM) {
-        constexpr int XR = CPL / 2;                // bf16 pairs of x per lane chunk
-        uint32_t xr[MP][XR];
-        float sx[MP], sx2[MP];
-#pragma unroll
-        for (int i = 0; i < MP; ++i) {
-#pragma unroll
-            for (int v = 0; v < XU; ++v) {
-                const uint4 q = load_x(i, v);
-                xr[i][4 * v] = q.x; xr[i][4 * v + 1] = q.y; xr[i][4 * v + 2] = q.z; xr[i][4 * v + 3] = q.w;
-            }
-            sx[i] = sxt[(M0 + i) * 32 + lane];
-            sx2[i] = 0.f;
-            if constexpr (FMT == UQ_INT2_ASYM) {
-                if (two_groups) sx2[i] = sxt[(M + M0 + i) * 32 + lane];
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            if (r < rows) {
-                const uint4 c = *reinterpret_cast<const uint4*>(tile + r * slice_bytes + lane * 16);
-                const uint32_t wv[4] = {c.x, c.y, c.z, c.w};
-                float p0[MP], p1[MP];
-#pragma unroll
-                for (int i = 0; i < MP; ++i) { p0[i] = 0.f; p1[i] = 0.f; }
-                if constexpr (FMT == UQ_INT2_ASYM) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-#pragma unroll
-                        for (int p = 0; p < 8; ++p) {
-                            const uint32_t t = crumb_pair_bf16(wv[j], p);
-#pragma unroll
-                            for (int i = 0; i < MP; ++i) {
-                                if (j < 2) p0[i] = fma2_bf16(t, xr[i][8 * j + p], p0[i]);
-                                else p1[i] = fma2_bf16(t, xr[i][8 * j + p], p1[i]);
-                            }
-                        }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-#pragma unroll
-                        for (int p = 0; p < 4; ++p) {
-                            const uint32_t t = nib_pair_bf16(wv[j], p);
-#pragma unroll
-                            for (int i = 0; i < MP; ++i) {
-                                if (j < 2) p0[i] = fma2_bf16(t, xr[i][4 * j + p], p0[i]);
-                                else p1[i] = fma2_bf16(t, xr[i][4 * j + p], p1[i]);
-                            }
-                        }
-                }
-                const RowMeta& mt = meta[r];
-#pragma unroll
-                for (int i = 0; i < MP; ++i) {
-                    float& A = acc[r][M0 + i];
-                    if constexpr (FMT == UQ_INT2_ASYM) {
-                        if (two_groups) {
-                            A = fmaf(mt.s, fmaf(-mt.zc, sx[i], p0[i]), A);
-                            A = fmaf(mt.s2, fmaf(-mt.zc2, sx2[i], p1[i]), A);
-                        } else {
-                            A = fmaf(mt.s, fmaf(-mt.zc, sx[i], p0[i] + p1[i]), A);
-                        }
-                    } else {
-                        A = fmaf(mt.s, fmaf(-mt.zc, sx[i], p0[i] + p1[i]), A);
-                        if constexpr (FMT == UQ_K4) A = fmaf(-mt.s2, sx[i], A);
-                    }
-                }
-            }
-        }
+// scale and (128 + z) of a row for the tile's local group li (flat formats)
+template <int FMT>
+__device__ __forceinline__ void row_meta(const RowPtrs<FMT>& p, int li, float& s, float& zc) {
+    s = half_bits_f32(p.s[li]);
+    if constexpr (FMT == UQ_INT4_SYM) {
+        zc = 136.0f;
+    } else if constexpr (FMT == UQ_INT4_ASYM) {
+        const uint32_t b = p.z[li >> 1];
+        // fp32 with exponent 134 and z at mantissa bits 16..19 is exactly 128 + z
+        zc = __uint_as_float(0x43000000u | (((li & 1) ? (b >> 4) : (b & 15u)) << 16));
+    } else if constexpr (FMT == UQ_INT2_ASYM) {
+        zc = 128.0f + half_bits_f32(reinterpret_cast<const uint16_t*>(p.z)[li]);
     } else {
-        // INT8_SYM and NF4: x in fp32 registers, codes to fp32 per element
-        float xf[MP][CPL];
-#pragma unroll
-        for (int i = 0; i < MP; ++i) {
-#pragma unroll
-            for (int v = 0; v < XU; ++v) {
-                const uint4 q = load_x(i, v);
-                const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    xf[i][8 * v + 2 * e] = bf16lo_f32(u[e]);
-                    xf[i][8 * v + 2 * e + 1] = bf16hi_f32(u[e]);
-                }
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            if (r < rows) {
-                const uint4 c = *reinterpret_cast<const uint4*>(tile + r * slice_bytes + lane * 16);
-                const uint32_t wv[4] = {c.x, c.y, c.z, c.w};
-                float p0[MP], p1[MP];
-#pragma unroll
-                for (int i = 0; i < MP; ++i) { p0[i] = 0.f; p1[i] = 0.f; }
-                if constexpr (FMT == UQ_INT8_SYM) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float q = byte_magic_f32(wv[j], e) - 8388736.0f;   // 2^23 + 128
-#pragma unroll
-                            for (int i = 0; i < MP; ++i) {
-                                if (e & 1) p1[i] = fmaf(xf[i][4 * j + e], q, p1[i]);
-                                else p0[i] = fmaf(xf[i][4 * j + e], q, p0[i]);
-                            }
-                        }
-                } else {  // NF4: code = index into the 16-entry codebook held in shared memory
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int pos = code_bitpos(4, e);
-                            const float cv = lut[(wv[j] >> pos) & 15u];
-#pragma unroll
-                            for (int i = 0; i < MP; ++i) {
-                                if (e & 1) p1[i] = fmaf(xf[i][8 * j + e], cv, p1[i]);
-                                else p0[i] = fmaf(xf[i][8 * j + e], cv, p0[i]);
-                            }
-                        }
-                }
-#pragma unroll
-                for (int i = 0; i < MP; ++i) acc[r][M0 + i] = fmaf(meta[r].s, p0[i] + p1[i], acc[r][M0 + i]);
-            }
-        }
+        zc = 0.0f;
     }
 }
 
-template <int FMT> struct PassPlan {
-    // rows of x handled per pass (register budget): INT2 and the fp32-x formats take fewer
-    static constexpr int MAXP = (FMT == UQ_INT2_ASYM || FMT == UQ_NF4) ? 2 : 4;
-};
-
-template <int FMT, int M, int M0, bool XS>
-__device__ __forceinline__ void tile_all_passes(const uint8_t* tile, int slice_bytes, int rows, int lane,
-                                                const uint16_t* xg, int ldx, const uint4* xs,
-                                                const RowMeta (&meta)[RB], float (&acc)[RB][M], const float* lut,
-                                                bool two_groups, const float* sxt) {
-    if constexpr (M0 < M) {
-        constexpr int REM = M - M0;
-        constexpr int MP = REM < PassPlan<FMT>::MAXP ? REM : PassPlan<FMT>::MAXP;
-        tile_pass<FMT, M, M0, MP, XS>(tile, slice_bytes, rows, lane, xg, ldx, xs, meta, acc, lut, two_groups, sxt);
-        tile_all_passes<FMT, M, M0 + MP, XS>(tile, slice_bytes, rows, lane, xg, ldx, xs, meta, acc, lut, two_groups,
-                                             sxt);
-    }
-}
-
-// Transposing butterfly: reduces CNT values per lane over the warp.  At each level a lane keeps
-// half of its values and sends the other half to its xor partner, so every sum is formed once, in
-// a fixed order; when one value is left the remaining levels are plain xor sums (commutative, so
-// both partners hold identical bits).  Afterwards lane l holds the totals of value indices
-// idx_out + j for j < max(1, CNT / 32) in v[j].
-template <int CNT>
-__device__ __forceinline__ void warp_reduce_transposed(float (&v)[CNT], int lane, int& idx_out) {
-    int idx = 0;
-    int half = CNT / 2;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        if (half >= 1) {
-            const bool up = (lane & o) != 0;
-#pragma unroll
-            for (int i = 0; i < CNT / 2; ++i) {
-                if (i < half) {
-                    const float keep = up ? v[i + half] : v[i];
-                    const float send = up ? v[i] : v[i + half];
-                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-                }
-            }
-            if (up) idx += half;
-            half >>= 1;
-        } else {
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
-        }
-    }
-    idx_out = idx;
+// K4: d*sc and dmin*m of row r for the tile's local 32-k sub-block li
+__device__ __forceinline__ void row_meta_k4(const uint8_t* st, int r, int li, float& dsc, float& dmm) {
+    const uint8_t* row = st + TILE_BYTES + r * GemvFmt<UQ_K4>::MW * 4;
+    const uint4 rec = *reinterpret_cast<const uint4*>(row + 16 * (li >> 3));
+    const int j = li & 7;
+    const uint64_t sc48 = (uint64_t)rec.y | ((uint64_t)(rec.z & 0xFFFFu) << 32);
+    const uint64_t m48 = (uint64_t)(rec.z >> 16) | ((uint64_t)rec.w << 16);
+    dsc = half_bits_f32((uint16_t)(rec.x & 0xFFFF)) * (float)((sc48 >> (6 * j)) & 63);
+    dmm = half_bits_f32((uint16_t)(rec.x >> 16)) * (float)((m48 >> (6 * j)) & 63);
 }
 
 }  // namespace
@@ -403,24 +282,41 @@ __device__ __forceinline__ void warp_reduce_transposed(float (&v)[CNT], int lane
 template <int FMT, int M, bool XS>
 __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs a) {
     using F = GemvFmt<FMT>;
-    constexpr int KT = F::KT, CPL = F::CPL, S = F::STAGES;
+    constexpr int KT = F::KT, S = F::STAGES, BPC = F::BPC;
     extern __shared__ __align__(128) uint8_t smem[];
-    const GemvSmem plan = gemv_smem_plan(FMT, a.K, M, XS);
+    const GemvSmem plan = gemv_smem_plan_t<FMT>(a.K, a.group, M, XS);
     uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + plan.bars);
     float* lut = reinterpret_cast<float*>(smem + plan.lut);
-    float* sx_tab = reinterpret_cast<float*>(smem + plan.sx);
-    uint4* x_tab = reinterpret_cast<uint4*>(smem + plan.x);
+    float* sxg = reinterpret_cast<float*>(smem + plan.sx);
+    uint8_t* xs = smem + plan.x;                                   // x rows (+ a zero row), stride xstride
+    uint64_t* xbar = bars_all + GEMV_WARPS * S;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
     const int w = blockIdx.x * GEMV_WARPS + warp;
     const bool has_work = w < a.P;
     const Layout L(a.N, a.K, FMT);
+    const int gs = (FMT == UQ_K4) ? 32 : a.group;                 // scaling granularity along k
+    MetaConst mc;
+    mc.G = a.K / a.group;
+    mc.GT = KT / a.group;
+    mc.ZB = (mc.G + 1) >> 1;
+    mc.S4 = a.K / 256;
+    const int bpg = gs / 16;                                       // 16-k blocks per group: 2, 4 or 8
+    const int bpg_log = bpg == 2 ? 1 : (bpg == 4 ? 2 : 3);
+    const size_t xstride = gemv_x_stride(L.Kp);
+    // 16-byte metadata copies: row slices 16-byte aligned and a multiple of 16 bytes long
+    mc.aligned = (a.K % (8 * a.group)) == 0 && (mc.GT % 8) == 0;
     uint8_t* ring = smem + (size_t)warp * S * F::STAGE_BYTES;
     uint64_t* bars = bars_all + warp * S;
     const long long t0 = has_work ? range_begin(w, a.T, a.P) : 0;
     const long long t1 = has_work ? range_begin(w + 1, a.T, a.P) : 0;
 
-    // 1. start the weight stream before anything else
+    // 0. let the next kernel on the stream start launching (it only prefetches its own weights
+    //    before it waits for this grid; no effect unless launched with launch overlap)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    // 1. start the weight stream before anything else (weights and metadata are constant)
     if (has_work) {
         if (lane == 0) {
 #pragma unroll
@@ -428,67 +324,85 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
             fence_barrier_init();
         }
         __syncwarp();
-        for (int s = 0; s < S && t0 + s < t1; ++s) issue_tile<FMT>(a, L, t0 + s, ring + s * F::STAGE_BYTES, &bars[s], lane);
+        int inb = (int)(t0 / L.KB), ikb = (int)(t0 % L.KB);
+        for (int s = 0; s < S && t0 + s < t1; ++s) {
+            issue_tile<FMT>(a, L, mc, inb, ikb, ring + s * F::STAGE_BYTES, &bars[s], lane);
+            if (++ikb == L.KB) { ikb = 0; ++inb; }
+        }
     }
 
-    // 2. CTA prologue: codebook, x in lane-chunk order, per-chunk sums of x
+    // 2. everything below may depend on the previous kernel on the stream (x, the split-K
+    //    workspace, y): wait for it to complete (returns at once when not launched overlapped)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // CTA prologue: codebook, x rows, per-group sums of x
     if constexpr (FMT == UQ_NF4) {
         if (threadIdx.x < 16) lut[threadIdx.x] = reinterpret_cast<const float*>(a.zc)[threadIdx.x];
     }
-    if constexpr (F::NEEDS_SX || XS) {
-        const int KBt = L.KB;
-        const bool split = (FMT == UQ_INT2_ASYM) && (a.group == 32);
-        for (int e = threadIdx.x; e < KBt * M * 32; e += blockDim.x) {
-            const int kb = e / (M * 32), m = (e / 32) % M, l = e % 32;
-            const int k0 = kb * KT + l * CPL;
-            float s0 = 0.f, s1 = 0.f;
-            const bool in = k0 < a.K;
-            const uint16_t* xp = a.x + (long long)m * a.ldx + k0;
+    if constexpr (XS) {
+        // one bulk copy per row of x into shared memory (rows are K * 2 bytes, a multiple of 16);
+        // the pad [K, Kp) of every row is zero
+        if (threadIdx.x == 0) {
+            mbar_init(xbar, 1);
+            fence_barrier_init();
+            mbar_arrive_expect_tx(xbar, (uint32_t)(M * a.K * 2));
 #pragma unroll
-            for (int v = 0; v < CPL / 8; ++v) {
-                const uint4 q = in ? ldg_nc_v4(xp + 8 * v) : make_uint4(0, 0, 0, 0);
-                if constexpr (XS) x_tab[((kb * M + m) * (CPL / 8) + v) * 32 + l] = q;
-                if constexpr (F::NEEDS_SX) {
+            for (int m = 0; m < M; ++m) bulk_g2s(xs + m * xstride, a.x + (long long)m * a.ldx, (uint32_t)(a.K * 2), xbar);
+        }
+        const int padw = (L.Kp - a.K) / 2;                          // 32-bit words of pad per row
+        for (int e = threadIdx.x; e < M * padw; e += blockDim.x)
+            reinterpret_cast<uint32_t*>(xs + (e / padw) * xstride + a.K * 2)[e % padw] = 0u;
+        __syncthreads();
+        // on a timeout the fault word is set and the kernel goes on (its results are then
+        // meaningless) so the ring's copies in flight are still drained below
+        mbar_wait_bounded(xbar, 0, a.fault, FAULT_GEMV_WAIT);
+    }
+    if constexpr (F::NEEDS_SX) {
+        // sxg[gi * 8 + m] = sum of x[m][k] over group gi (k < K), in k order; 0 for m >= M
+        const int gp = (L.Kp + gs - 1) / gs;
+        for (int e = threadIdx.x; e < gp * 8; e += blockDim.x) {
+            const int gi = e >> 3, m = e & 7;
+            float s0 = 0.f;
+            if (m < M) {
+                const int kend = (gi * gs + gs) < a.K ? (gi * gs + gs) : a.K;
+                for (int k = gi * gs; k < kend; k += 8) {
+                    uint4 q;
+                    if constexpr (XS) q = *reinterpret_cast<const uint4*>(xs + m * xstride + k * 2);
+                    else q = ldg_nc_v4(a.x + (long long)m * a.ldx + k);
                     const uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float t = bf16lo_f32(u[j]) + bf16hi_f32(u[j]);
-                        if (4 * v + j < CPL / 4) s0 += t; else s1 += t;
-                    }
+                    for (int j = 0; j < 4; ++j) s0 += bf16lo_f32(u[j]) + bf16hi_f32(u[j]);
                 }
             }
-            if constexpr (F::NEEDS_SX) {
-                float* row = sx_tab + (long long)kb * F::HALVES * M * 32;
-                if (split) {
-                    row[m * 32 + l] = s0;
-                    row[(M + m) * 32 + l] = s1;
-                } else {
-                    row[m * 32 + l] = s0 + s1;
-                }
-            }
+            sxg[e] = s0;
         }
     }
     __syncthreads();
     if (!has_work) return;
 
     const int first_nb = (int)(t0 / L.KB);
-    const bool two_groups = (FMT == UQ_INT2_ASYM) && (a.group == 32);
-    float acc[RB][M];
+    // MMA path: acc[j*2 + e] = row g + 8j, column 2c + e.  FFMA path: accf[j][m] = row g + 8j.
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float accf[2][M];
 #pragma unroll
-    for (int r = 0; r < RB; ++r)
+    for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int m = 0; m < M; ++m) acc[r][m] = 0.f;
+        for (int m = 0; m < M; ++m) accf[j][m] = 0.f;
 
+    // (row block, k tile) of the tile being consumed and of the next one to prefetch, advanced
+    // incrementally (no 64-bit division per tile)
+    int nb = (int)(t0 / L.KB), kb = (int)(t0 % L.KB);
+    int pnb = nb, pkb = kb;
+    for (int s = 0; s < S; ++s)
+        if (++pkb == L.KB) { pkb = 0; ++pnb; }
     for (long long t = t0; t < t1; ++t) {
         const int it = (int)(t - t0);
         const int s = it % S;
         const uint32_t parity = (uint32_t)((it / S) & 1);
-        const int nb = (int)(t / L.KB), kb = (int)(t % L.KB);
-        const int rows = L.rows(nb);
         const int n0 = nb * RB;
-        const bool active = lane * CPL < L.width(kb);
-        const int k0 = kb * KT + lane * CPL;
         uint8_t* st = ring + s * F::STAGE_BYTES;
+        const int nchunks = L.chunks(kb);
+        const int blk0 = (kb * KT) / 16;                           // first global 16-k block of the tile
 
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], parity, a.fault, FAULT_GEMV_WAIT))) {
             // give the copies still in flight a bounded chance to land, then leave
@@ -498,54 +412,196 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
             }
             return;
         }
-        if (active) {
-            RowMeta meta[RB];
-#pragma unroll
-            for (int r = 0; r < RB; ++r) {
-                meta[r] = RowMeta{0.f, 0.f, 0.f, 0.f};
-                if (r < rows) meta[r] = stage_meta<FMT>(a, L, st, r, n0 + r, kb, lane);
+
+        if constexpr (F::MMA) {
+            const int G_all = (FMT == UQ_K4) ? a.K / 32 : mc.G;
+            const int gi0 = (kb * KT) / gs;                        // first global group of the tile
+            RowPtrs<FMT> rp[2];
+            if constexpr (FMT != UQ_K4) {
+                rp[0] = row_ptrs<FMT>(st, mc, g, n0 + g, kb);
+                rp[1] = row_ptrs<FMT>(st, mc, g + 8, n0 + g + 8, kb);
             }
-            tile_all_passes<FMT, M, 0, XS>(st, L.slice_bytes(kb), rows, lane, a.x + k0, a.ldx,
-                                           x_tab + (long long)kb * M * (CPL / 8) * 32, meta, acc, lut, two_groups,
-                                           sx_tab + (long long)kb * F::HALVES * M * 32);
+            // B fragment source: x row min(g, M - 1) (columns >= M of D are never used), k = 4c..
+            const uint8_t* xrow = xs + (g < M ? g : M - 1) * xstride + 8 * c;
+            const uint16_t* xgrow = a.x + (long long)(g < M ? g : M - 1) * a.ldx + 4 * c;
+            // two accumulator chains (k block parity); each group starts them from zero
+            float dd[2][4];
+            for (int q = 0; q < nchunks; ++q) {
+                const uint4 cw = *reinterpret_cast<const uint4*>(st + q * CHUNK + lane * 16);
+                const uint32_t wv[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+                for (int bi = 0; bi < BPC; ++bi) {
+                    const int lb = q * BPC + bi;                   // block within the tile
+                    const int blk = blk0 + lb;
+                    uint2 b;
+                    if constexpr (XS) b = *reinterpret_cast<const uint2*>(xrow + blk * 32);
+                    else b = (blk * 16 + 4 * c < a.K) ? ldg_nc_v2(xgrow + blk * 16) : make_uint2(0, 0);
+                    uint32_t a0, a1, a2, a3;
+                    if constexpr (FMT == UQ_INT2_ASYM) {
+                        const uint32_t wd = wv[bi >> 1];
+                        const int pb = (bi & 1) * 4;
+                        a0 = crumb_pair_bf16(wd, pb + 0); a1 = crumb_pair_bf16(wd, pb + 1);
+                        a2 = crumb_pair_bf16(wd, pb + 2); a3 = crumb_pair_bf16(wd, pb + 3);
+                    } else {
+                        const uint32_t wd = wv[bi];
+                        a0 = nib_pair_bf16(wd, 0); a1 = nib_pair_bf16(wd, 1);
+                        a2 = nib_pair_bf16(wd, 2); a3 = nib_pair_bf16(wd, 3);
+                    }
+                    const int pos = lb & (bpg - 1);                // position inside the group
+                    if (pos < 2) mma_bf16_zero(dd[bi & 1], a0, a1, a2, a3, b.x, b.y);
+                    else mma_bf16(dd[bi & 1], a0, a1, a2, a3, b.x, b.y);
+                    if (pos == bpg - 1) {
+                        // end of a scaling group: fold it into the row sums
+                        const int li = lb >> bpg_log;              // group within the tile row
+                        const int gi = gi0 + li;                   // global group
+                        if (gi < G_all) {
+                            const float2 sxv = *reinterpret_cast<const float2*>(sxg + gi * 8 + 2 * c);
+                            float d[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) d[e] = dd[0][e] + dd[1][e];
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                if constexpr (FMT == UQ_K4) {
+                                    float dsc, dmm;
+                                    row_meta_k4(st, g + 8 * j, li, dsc, dmm);
+                                    const float off = fmaf(128.0f, dsc, dmm);   // (128 dsc + dmin m) per unit of sum x
+                                    acc[2 * j] = fmaf(dsc, d[2 * j], fmaf(-off, sxv.x, acc[2 * j]));
+                                    acc[2 * j + 1] = fmaf(dsc, d[2 * j + 1], fmaf(-off, sxv.y, acc[2 * j + 1]));
+                                } else {
+                                    float sc, zc;
+                                    row_meta<FMT>(rp[j], li, sc, zc);
+                                    const float szc = sc * zc;
+                                    acc[2 * j] = fmaf(sc, d[2 * j], fmaf(-szc, sxv.x, acc[2 * j]));
+                                    acc[2 * j + 1] = fmaf(sc, d[2 * j + 1], fmaf(-szc, sxv.y, acc[2 * j + 1]));
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+        } else {
+            // CUDA-core path (INT8_SYM, NF4): lane holds rows g and g + 8 at k = 16 blk + 4c .. +3
+            const int G_all = mc.G;
+            RowPtrs<FMT> rp[2];
+            rp[0] = row_ptrs<FMT>(st, mc, g, n0 + g, kb);
+            rp[1] = row_ptrs<FMT>(st, mc, g + 8, n0 + g + 8, kb);
+            float p[2][M];
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int m = 0; m < M; ++m) p[j][m] = 0.f;
+            for (int q = 0; q < nchunks; ++q) {
+                const uint4 cw = *reinterpret_cast<const uint4*>(st + q * CHUNK + lane * 16);
+                const uint32_t wv[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+                for (int bi = 0; bi < BPC; ++bi) {
+                    const int lb = q * BPC + bi;
+                    const int blk = blk0 + lb;
+                    float cv[2][4];
+                    if constexpr (FMT == UQ_INT8_SYM) {
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) cv[j][e] = byte_magic_f32(wv[2 * bi + j], e) - 8388736.0f;
+                    } else {
+                        const uint32_t wd = wv[bi];
+#pragma unroll
+                        for (int pp = 0; pp < 4; ++pp) {
+                            // pair pp: row g + 8 (pp & 1), k = 4c + 2 (pp >> 1) + {0, 1}
+                            cv[pp & 1][2 * (pp >> 1)] = lut[(wd >> (4 * pp)) & 15u];
+                            cv[pp & 1][2 * (pp >> 1) + 1] = lut[(wd >> (16 + 4 * pp)) & 15u];
+                        }
+                    }
+#pragma unroll
+                    for (int m = 0; m < M; ++m) {
+                        uint2 xb;
+                        xb = make_uint2(0, 0);
+                        if (blk * 16 + 4 * c < a.K) {
+                            if constexpr (XS) xb = *reinterpret_cast<const uint2*>(xs + m * xstride + (blk * 16 + 4 * c) * 2);
+                            else xb = ldg_nc_v2(a.x + (long long)m * a.ldx + blk * 16 + 4 * c);
+                        }
+                        const float x0 = bf16lo_f32(xb.x), x1 = bf16hi_f32(xb.x);
+                        const float x2 = bf16lo_f32(xb.y), x3 = bf16hi_f32(xb.y);
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            p[j][m] = fmaf(x0, cv[j][0], p[j][m]);
+                            p[j][m] = fmaf(x1, cv[j][1], p[j][m]);
+                            p[j][m] = fmaf(x2, cv[j][2], p[j][m]);
+                            p[j][m] = fmaf(x3, cv[j][3], p[j][m]);
+                        }
+                    }
+                    if (((lb + 1) & (bpg - 1)) == 0) {
+                        const int li = lb >> bpg_log;
+                        if (kb * mc.GT + li < G_all) {
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                float sc, zc;
+                                row_meta<FMT>(rp[j], li, sc, zc);
+#pragma unroll
+                                for (int m = 0; m < M; ++m) accf[j][m] = fmaf(sc, p[j][m], accf[j][m]);
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+#pragma unroll
+                            for (int m = 0; m < M; ++m) p[j][m] = 0.f;
+                    }
+                }
+            }
         }
         __syncwarp();
-        if (t + S < t1) issue_tile<FMT>(a, L, t + S, st, &bars[s], lane);
+        if (t + S < t1) {
+            issue_tile<FMT>(a, L, mc, pnb, pkb, st, &bars[s], lane);
+            if (++pkb == L.KB) { pkb = 0; ++pnb; }
+        }
 
         if (kb == L.KB - 1 || t == t1 - 1) {
-            // row block done (for this worker): reduce over lanes, then write y or a partial
+            // row block done (for this worker): write y or a partial
             const bool full = (kb == L.KB - 1) && (nb != first_nb || (t0 % L.KB) == 0);
-            // values padded to a power of two (8 rows x M, M <= 8)
-            constexpr int CNT = RB * (M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8);
-            float v[CNT];
+            // this thread's results: rows g + 8j, columns 2c + e (MMA) or all columns (FFMA, lane c == 0)
+            float out[2][M];
+            bool mine[2][M];
 #pragma unroll
-            for (int i = 0; i < CNT; ++i) v[i] = 0.f;
+            for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int r = 0; r < RB; ++r)
+                for (int m = 0; m < M; ++m) { out[j][m] = 0.f; mine[j][m] = false; }
+            if constexpr (F::MMA) {
 #pragma unroll
-                for (int m = 0; m < M; ++m) v[r * (CNT / RB) + m] = acc[r][m];
-            int idx = 0;
-            warp_reduce_transposed<CNT>(v, lane, idx);
-            // lane holds the totals of indices idx .. idx + RES - 1; with CNT < 32 several lanes
-            // hold the same total and only the first of them writes it
-            constexpr int RES = CNT >= 32 ? CNT / 32 : 1;
-            constexpr int OWN = CNT >= 32 ? 1 : 32 / CNT;
-            const bool owner = (lane % OWN) == 0;
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+#pragma unroll
+                        for (int m = 0; m < M; ++m)
+                            if (m == 2 * c + e) { out[j][m] = acc[2 * j + e]; mine[j][m] = true; }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int m = 0; m < M; ++m) {
+                        float v = accf[j][m];
+                        v += __shfl_xor_sync(0xffffffffu, v, 1);
+                        v += __shfl_xor_sync(0xffffffffu, v, 2);
+                        out[j][m] = v;
+                        mine[j][m] = (c == 0);
+                    }
+            }
             if (full) {
 #pragma unroll
-                for (int j = 0; j < RES; ++j) {
-                    const int vr = (idx + j) / (CNT / RB), vm = (idx + j) % (CNT / RB);
-                    if (owner && vr < rows && vm < M)
-                        a.y[(long long)vm * a.ldy + n0 + vr] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
-                }
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int m = 0; m < M; ++m) {
+                        const int n = n0 + g + 8 * j;
+                        if (mine[j][m] && n < a.N)
+                            a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(out[j][m]));
+                    }
             } else {
                 const int slot = 2 * w + (nb == first_nb ? 0 : 1);
                 float* part = a.partials + (long long)slot * RB * M;
 #pragma unroll
-                for (int j = 0; j < RES; ++j) {
-                    const int vr = (idx + j) / (CNT / RB), vm = (idx + j) % (CNT / RB);
-                    if (owner && vr < rows && vm < M) part[vr * M + vm] = v[j];
-                }
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int m = 0; m < M; ++m)
+                        if (mine[j][m]) part[(g + 8 * j) * M + m] = out[j][m];
                 __threadfence();
                 __syncwarp();
                 unsigned int old = 0;
@@ -555,32 +611,35 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
                 const int wf = worker_of(tf, a.T, a.P), wl = worker_of(tf + L.KB - 1, a.T, a.P);
                 if (old == (unsigned int)(wl - wf)) {
                     __threadfence();
-                    for (int e = lane; e < rows * M; e += 32) {
+                    for (int e = lane; e < RB * M; e += 32) {
+                        const int r = e / M, m = e % M;
+                        if (n0 + r >= a.N) continue;
                         float sum = 0.f;
                         for (int w2 = wf; w2 <= wl; ++w2) {
                             const int nb2 = (int)(range_begin(w2, a.T, a.P) / L.KB);
                             const int slot2 = 2 * w2 + (nb == nb2 ? 0 : 1);
                             sum += __ldcg(a.partials + (long long)slot2 * RB * M + e);
                         }
-                        const int r = e / M, m = e % M;
                         a.y[(long long)m * a.ldy + n0 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
                     }
                     if (lane == 0) a.tickets[nb] = 0u;
                 }
             }
+            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
 #pragma unroll
-            for (int r = 0; r < RB; ++r)
+            for (int j = 0; j < 2; ++j)
 #pragma unroll
-                for (int m = 0; m < M; ++m) acc[r][m] = 0.f;
+                for (int m = 0; m < M; ++m) accf[j][m] = 0.f;
         }
+        if (++kb == L.KB) { kb = 0; ++nb; }
     }
 }
 
-inline bool gemv_x_in_smem(int fmt, int K, int M) {
-    return gemv_smem_plan(fmt, K, M, true).total <= 227 * 1024;
+inline bool gemv_x_in_smem(int fmt, int K, int group, int M) {
+    return gemv_smem_plan(fmt, K, group, M, true).total <= 227 * 1024;
 }
-inline size_t gemv_smem_bytes_impl(int fmt, int K, int M) {
-    return gemv_smem_plan(fmt, K, M, gemv_x_in_smem(fmt, K, M)).total;
+inline size_t gemv_smem_bytes_impl(int fmt, int K, int group, int M) {
+    return gemv_smem_plan(fmt, K, group, M, gemv_x_in_smem(fmt, K, group, M)).total;
 }
 inline size_t gemv_partials_floats_impl(int P, int M) { return (size_t)2 * P * RB * M; }
 
@@ -588,7 +647,7 @@ namespace gemv_detail {
 template <int FMT, int M, bool XS>
 cudaError_t launch_one(const GemvArgs& a, int grid, cudaStream_t st) {
     static bool configured[64] = {};   // the shared-memory opt-in, once per device
-    const size_t smem = gemv_smem_plan(FMT, a.K, M, XS).total;
+    const size_t smem = gemv_smem_plan_t<FMT>(a.K, a.group, M, XS).total;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -598,12 +657,27 @@ cudaError_t launch_one(const GemvArgs& a, int grid, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    gemv_kernel<FMT, M, XS><<<grid, GEMV_WARPS * 32, smem, st>>>(a);
+    if (launch_overlap()) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(GEMV_WARPS * 32);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, gemv_kernel<FMT, M, XS>, a);
+        if (e != cudaSuccess) return e;
+    } else {
+        gemv_kernel<FMT, M, XS><<<grid, GEMV_WARPS * 32, smem, st>>>(a);
+    }
     return cudaGetLastError();
 }
 template <int FMT, int M>
 cudaError_t launch_xs(const GemvArgs& a, int grid, cudaStream_t st) {
-    if (gemv_x_in_smem(FMT, a.K, M)) return launch_one<FMT, M, true>(a, grid, st);
+    if (gemv_x_in_smem(FMT, a.K, a.group, M)) return launch_one<FMT, M, true>(a, grid, st);
     return launch_one<FMT, M, false>(a, grid, st);
 }
 }  // namespace gemv_detail

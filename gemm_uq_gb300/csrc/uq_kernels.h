@@ -7,6 +7,8 @@ namespace uq {
 
 // records the message uq_last_error() returns on the calling thread (uq_api.cu)
 void set_last_error(const char* msg);
+// whether GEMV kernels are launched with programmatic dependent launch (uq_set_launch_overlap)
+bool launch_overlap();
 
 // offline kernels (uq_pack.cu)
 cudaError_t launch_pack(int fmt, const int8_t* codes, uint8_t* wq, int N, int K, unsigned int* bad,
@@ -33,19 +35,21 @@ struct GemvArgs {
     int NB, KB;               // row blocks, k tiles
     long long T;              // tiles = NB * KB
     int P;                    // workers (warps), P <= T
-    float* partials;          // [2P][RB][M] fp32 split-K partial sums
+    float* partials;          // [2P][16][M] fp32 split-K partial sums
     unsigned int* tickets;    // [NB], zero between calls
     unsigned int* fault;      // device fault word
 };
-constexpr int GEMV_WARPS = 8;     // worker warps per CTA
-constexpr int GEMV_STAGES = 4;    // tiles in flight per warp
-size_t gemv_smem_bytes(int fmt, int K, int M);
+constexpr int GEMV_WARPS = 4;     // worker warps per CTA
+size_t gemv_smem_bytes(int fmt, int K, int group, int M);
 size_t gemv_partials_floats(int P, int M);
 cudaError_t launch_gemv(int fmt, const GemvArgs& a, int grid, cudaStream_t st);
 
 
 // tensor-core GEMM for M >= 16 (uq_tc.cu)
 struct TcArgs {
+    const uint8_t* wq;        // packed codes
+    long long rowbytes;       // bytes of one padded row of codes
+    int NB;                   // row blocks of 16
     const uint8_t* scales;    // fp16 [N][K/group] or K4 records
     const uint8_t* zc;        // INT4_ASYM zero nibbles, else NULL
     uint16_t* y;              // bf16 [M][ldy]
@@ -62,7 +66,6 @@ struct TcArgs {
 bool tc_supported(int fmt, int N, int K);
 int tc_plan(int fmt, int mpad, int* stages, int* dslots, size_t* smem);
 cudaError_t launch_colsum32(const uint16_t* x, float* sx, int M, int mpad, int K, int ldx, cudaStream_t st);
-cudaError_t launch_tc(int fmt, const uint16_t* x, const uint8_t* wq, const TcArgs& a, size_t smem, int grid,
-                      cudaStream_t st);
+cudaError_t launch_tc(int fmt, const uint16_t* x, const TcArgs& a, size_t smem, int grid, cudaStream_t st);
 
 }  // namespace uq

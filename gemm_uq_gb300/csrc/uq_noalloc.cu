@@ -17,7 +17,7 @@ namespace {
 // Scratch layout (bytes): [0, 256) fault word; [256, 256 + TICKET_BYTES) row-block tickets;
 // then the fp32 partial sums.  Every GPU that loads the library holds this array until exit.
 constexpr size_t SCRATCH_BYTES = 1u << 20;                 // 1 MiB
-constexpr size_t TICKET_BYTES = 256u << 10;                // 65536 row blocks = N <= 524288
+constexpr size_t TICKET_BYTES = 256u << 10;                // 65536 row blocks of 16 = N <= 1048576
 constexpr size_t PARTIAL_OFFSET = 256 + TICKET_BYTES;
 constexpr size_t PARTIAL_BYTES = SCRATCH_BYTES - PARTIAL_OFFSET;
 
@@ -121,11 +121,11 @@ uq_status uq_gemm_noalloc(const uint16_t* x, const void* wq, const void* scales,
     if ((size_t)L.NB * sizeof(unsigned int) > TICKET_BYTES ||
         uq::gemv_partials_floats((int)P, mb_max) * sizeof(float) > PARTIAL_BYTES) {
         snprintf(g_err, sizeof g_err,
-                 "N=%d, M=%d needs more than the %zu-byte static scratch (at most %zu row blocks of 8 and "
+                 "N=%d, M=%d needs more than the %zu-byte static scratch (at most %zu row blocks of 16 and "
                  "%zu bytes of partial sums)", N, M, SCRATCH_BYTES, TICKET_BYTES / 4, PARTIAL_BYTES);
         return err(UQ_ERR_NOMEM);
     }
-    if (uq::gemv_smem_bytes(fmt, K, mb_max) > 227 * 1024) {
+    if (uq::gemv_smem_bytes(fmt, K, group, mb_max) > 227 * 1024) {
         snprintf(g_err, sizeof g_err, "K=%d is too long for the GEMV at M=%d", K, mb_max);
         return err(UQ_ERR_UNSUPPORTED);
     }

@@ -6,66 +6,67 @@
 namespace uq {
 
 // ----------------------------------------------------------------------------------------------
-// pack: one thread per 32-bit output word (codes k = wi*cpw .. wi*cpw + cpw - 1 of row n)
+// pack / unpack / dequant: one thread per 32-bit word of the packed plane; each code slot of the
+// word is mapped to its (row, k) by Layout::slot_nk.  Slots outside [N) x [K) are padding and
+// hold the stored form of code 0.
+
+// value (code + bias, as stored) of slot s of word w, through the same register unpacking the
+// GEMV and GEMM kernels use
+template <int FMT>
+__device__ __forceinline__ int stored_code(uint32_t w, int s) {
+    if constexpr (FMT == UQ_INT8_SYM) {
+        return (int)(byte_magic_f32(w, s) - 8388608.0f);
+    } else if constexpr (FMT == UQ_INT2_ASYM) {
+        const uint32_t t = crumb_pair_bf16(w, s >> 1);
+        return (int)((s & 1) ? bf16hi_f32(t) : bf16lo_f32(t)) - 128;
+    } else {
+        const uint32_t t = nib_pair_bf16(w, s >> 1);
+        return (int)((s & 1) ? bf16hi_f32(t) : bf16lo_f32(t)) - 128;
+    }
+}
+
 template <int FMT>
 __global__ void pack_kernel(const int8_t* __restrict__ codes, uint8_t* __restrict__ wq, int N, int K,
                             unsigned int* __restrict__ bad) {
     constexpr int BITS = fmt_bits(FMT), CPW = fmt_cpw(FMT), BIAS = fmt_bias(FMT);
     constexpr int LO = (FMT == UQ_INT4_SYM) ? -8 : (FMT == UQ_INT8_SYM ? -128 : 0);
     constexpr int HI = (FMT == UQ_INT4_SYM) ? 7 : (FMT == UQ_INT8_SYM ? 127 : (FMT == UQ_INT2_ASYM ? 3 : 15));
-    const long long words_per_row = K / CPW;
-    const long long total = (long long)N * words_per_row;
     const Layout L(N, K, FMT);
-    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
-         idx += (long long)gridDim.x * blockDim.x) {
-        int n = (int)(idx / words_per_row);
-        int k = (int)(idx % words_per_row) * CPW;
-        const int8_t* src = codes + (long long)n * K + k;
+    const long long words = L.bytes() / 4;
+    for (long long wi = blockIdx.x * (long long)blockDim.x + threadIdx.x; wi < words;
+         wi += (long long)gridDim.x * blockDim.x) {
         uint32_t word = 0;
         bool ok = true;
 #pragma unroll
-        for (int i = 0; i < CPW; ++i) {
-            int c = src[i];
-            ok &= (c >= LO) && (c <= HI);
-            uint32_t u = (uint32_t)(c + BIAS) & ((1u << BITS) - 1u);
-            word |= u << code_bitpos(BITS, i);
+        for (int s = 0; s < CPW; ++s) {
+            int n, k;
+            L.slot_nk(wi * 4, s, &n, &k);
+            int c = 0;
+            if (n < N && k < K) {
+                c = codes[(long long)n * K + k];
+                ok &= (c >= LO) && (c <= HI);
+            }
+            const uint32_t u = (uint32_t)(c + BIAS) & ((1u << BITS) - 1u);
+            word |= u << slot_bitpos(BITS, s);
         }
         if (!ok) atomicAdd(bad, 1u);
-        *reinterpret_cast<uint32_t*>(wq + L.word_offset(n, k)) = word;
+        reinterpret_cast<uint32_t*>(wq)[wi] = word;
     }
 }
 
-// unpack: inverse of pack, through the same register unpacking the GEMV uses
 template <int FMT>
 __global__ void unpack_kernel(const uint8_t* __restrict__ wq, int8_t* __restrict__ codes, int N, int K) {
     constexpr int CPW = fmt_cpw(FMT), BIAS = fmt_bias(FMT);
-    const long long words_per_row = K / CPW;
-    const long long total = (long long)N * words_per_row;
     const Layout L(N, K, FMT);
-    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
-         idx += (long long)gridDim.x * blockDim.x) {
-        int n = (int)(idx / words_per_row);
-        int k = (int)(idx % words_per_row) * CPW;
-        uint32_t word = *reinterpret_cast<const uint32_t*>(wq + L.word_offset(n, k));
-        int8_t* dst = codes + (long long)n * K + k;
-        if constexpr (FMT == UQ_INT8_SYM) {
+    const long long words = L.bytes() / 4;
+    for (long long wi = blockIdx.x * (long long)blockDim.x + threadIdx.x; wi < words;
+         wi += (long long)gridDim.x * blockDim.x) {
+        const uint32_t word = reinterpret_cast<const uint32_t*>(wq)[wi];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                dst[i] = (int8_t)((int)(byte_magic_f32(word, i) - 8388608.0f) - BIAS);
-        } else if constexpr (FMT == UQ_INT2_ASYM) {
-#pragma unroll
-            for (int p = 0; p < 8; ++p) {
-                uint32_t t = crumb_pair_bf16(word, p);
-                dst[2 * p] = (int8_t)((int)bf16lo_f32(t) - 128);
-                dst[2 * p + 1] = (int8_t)((int)bf16hi_f32(t) - 128);
-            }
-        } else {
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                uint32_t t = nib_pair_bf16(word, p);
-                dst[2 * p] = (int8_t)((int)bf16lo_f32(t) - 128 - BIAS);
-                dst[2 * p + 1] = (int8_t)((int)bf16hi_f32(t) - 128 - BIAS);
-            }
+        for (int s = 0; s < CPW; ++s) {
+            int n, k;
+            L.slot_nk(wi * 4, s, &n, &k);
+            if (n < N && k < K) codes[(long long)n * K + k] = (int8_t)(stored_code<FMT>(word, s) - BIAS);
         }
     }
 }
@@ -76,65 +77,46 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ wq, const uint8_t* __
                                const uint8_t* __restrict__ zc, float* __restrict__ w, int N, int K,
                                int group) {
     constexpr int CPW = fmt_cpw(FMT), BIAS = fmt_bias(FMT);
-    const long long words_per_row = K / CPW;
-    const long long total = (long long)N * words_per_row;
     const Layout L(N, K, FMT);
+    const long long words = L.bytes() / 4;
     const int G = K / group;
-    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
-         idx += (long long)gridDim.x * blockDim.x) {
-        int n = (int)(idx / words_per_row);
-        int k = (int)(idx % words_per_row) * CPW;
-        uint32_t word = *reinterpret_cast<const uint32_t*>(wq + L.word_offset(n, k));
-        float q[CPW];
-        if constexpr (FMT == UQ_INT8_SYM) {
+    for (long long wi = blockIdx.x * (long long)blockDim.x + threadIdx.x; wi < words;
+         wi += (long long)gridDim.x * blockDim.x) {
+        const uint32_t word = reinterpret_cast<const uint32_t*>(wq)[wi];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) q[i] = byte_magic_f32(word, i) - 8388736.0f;   // 2^23 + 128
-        } else if constexpr (FMT == UQ_INT2_ASYM) {
-#pragma unroll
-            for (int p = 0; p < 8; ++p) {
-                uint32_t t = crumb_pair_bf16(word, p);
-                q[2 * p] = bf16lo_f32(t) - 128.0f;
-                q[2 * p + 1] = bf16hi_f32(t) - 128.0f;
-            }
-        } else {
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                uint32_t t = nib_pair_bf16(word, p);
-                q[2 * p] = bf16lo_f32(t) - (float)(128 + BIAS);
-                q[2 * p + 1] = bf16hi_f32(t) - (float)(128 + BIAS);
-            }
-        }
-        float* dst = w + (long long)n * K + k;
-        if constexpr (FMT == UQ_K4) {
-            int sb = k / 256, j = (k % 256) / 32;
-            uint4 rec = *reinterpret_cast<const uint4*>(scales + ((long long)n * (K / 256) + sb) * 16);
-            float d = half_bits_f32((uint16_t)(rec.x & 0xFFFF));
-            float dmin = half_bits_f32((uint16_t)(rec.x >> 16));
-            uint64_t sc48 = (uint64_t)rec.y | ((uint64_t)(rec.z & 0xFFFFu) << 32);
-            uint64_t m48 = (uint64_t)(rec.z >> 16) | ((uint64_t)rec.w << 16);
-            float dsc = d * (float)((sc48 >> (6 * j)) & 63);          // exact: 11 x 6 bits
-            float dmm = dmin * (float)((m48 >> (6 * j)) & 63);        // exact
-#pragma unroll
-            for (int i = 0; i < CPW; ++i) dst[i] = fmaf(dsc, q[i], -dmm);   // one rounding
-        } else {
-            int gi = k / group;                     // a word never straddles a group (group >= 32)
-            const uint16_t* sp = reinterpret_cast<const uint16_t*>(scales);
-            float s = half_bits_f32(sp[(long long)n * G + gi]);
-            if constexpr (FMT == UQ_NF4) {
-                const float* c = reinterpret_cast<const float*>(zc);
-#pragma unroll
-                for (int i = 0; i < CPW; ++i) dst[i] = __fmul_rn(s, __ldg(&c[(int)q[i]]));
+        for (int s = 0; s < CPW; ++s) {
+            int n, k;
+            L.slot_nk(wi * 4, s, &n, &k);
+            if (n >= N || k >= K) continue;
+            const float q = (float)(stored_code<FMT>(word, s) - BIAS);
+            float out;
+            if constexpr (FMT == UQ_K4) {
+                const int sb = k / 256, j = (k % 256) / 32;
+                const uint4 rec = *reinterpret_cast<const uint4*>(scales + ((long long)n * (K / 256) + sb) * 16);
+                const float d = half_bits_f32((uint16_t)(rec.x & 0xFFFF));
+                const float dmin = half_bits_f32((uint16_t)(rec.x >> 16));
+                const uint64_t sc48 = (uint64_t)rec.y | ((uint64_t)(rec.z & 0xFFFFu) << 32);
+                const uint64_t m48 = (uint64_t)(rec.z >> 16) | ((uint64_t)rec.w << 16);
+                const float dsc = d * (float)((sc48 >> (6 * j)) & 63);          // exact: 11 x 6 bits
+                const float dmm = dmin * (float)((m48 >> (6 * j)) & 63);        // exact
+                out = fmaf(dsc, q, -dmm);                                      // one rounding
             } else {
-                float z = 0.0f;
-                if constexpr (FMT == UQ_INT4_ASYM) {
-                    uint8_t b = zc[(long long)n * ((G + 1) / 2) + gi / 2];
-                    z = (float)((gi & 1) ? (b >> 4) : (b & 15));
-                } else if constexpr (FMT == UQ_INT2_ASYM) {
-                    z = half_bits_f32(reinterpret_cast<const uint16_t*>(zc)[(long long)n * G + gi]);
+                const int gi = k / group;
+                const float sv = half_bits_f32(reinterpret_cast<const uint16_t*>(scales)[(long long)n * G + gi]);
+                if constexpr (FMT == UQ_NF4) {
+                    out = __fmul_rn(sv, __ldg(reinterpret_cast<const float*>(zc) + (int)q));
+                } else {
+                    float z = 0.0f;
+                    if constexpr (FMT == UQ_INT4_ASYM) {
+                        const uint8_t b = zc[(long long)n * ((G + 1) / 2) + gi / 2];
+                        z = (float)((gi & 1) ? (b >> 4) : (b & 15));
+                    } else if constexpr (FMT == UQ_INT2_ASYM) {
+                        z = half_bits_f32(reinterpret_cast<const uint16_t*>(zc)[(long long)n * G + gi]);
+                    }
+                    out = __fmul_rn(sv, q - z);
                 }
-#pragma unroll
-                for (int i = 0; i < CPW; ++i) dst[i] = __fmul_rn(s, q[i] - z);
             }
+            w[(long long)n * K + k] = out;
         }
     }
 }
@@ -344,7 +326,7 @@ static int grid_for(long long work, int block) {
 
 cudaError_t launch_pack(int fmt, const int8_t* codes, uint8_t* wq, int N, int K, unsigned int* bad,
                         cudaStream_t st) {
-    long long words = (long long)N * K / fmt_cpw(fmt);
+    long long words = Layout(N, K, fmt).bytes() / 4;
     int g = grid_for(words, 256);
     switch (fmt) {
         case UQ_INT4_SYM: pack_kernel<UQ_INT4_SYM><<<g, 256, 0, st>>>(codes, wq, N, K, bad); break;
@@ -359,7 +341,7 @@ cudaError_t launch_pack(int fmt, const int8_t* codes, uint8_t* wq, int N, int K,
 }
 
 cudaError_t launch_unpack(int fmt, const uint8_t* wq, int8_t* codes, int N, int K, cudaStream_t st) {
-    long long words = (long long)N * K / fmt_cpw(fmt);
+    long long words = Layout(N, K, fmt).bytes() / 4;
     int g = grid_for(words, 256);
     switch (fmt) {
         case UQ_INT4_SYM: unpack_kernel<UQ_INT4_SYM><<<g, 256, 0, st>>>(wq, codes, N, K); break;
@@ -375,7 +357,7 @@ cudaError_t launch_unpack(int fmt, const uint8_t* wq, int8_t* codes, int N, int 
 
 cudaError_t launch_dequant(int fmt, const uint8_t* wq, const uint8_t* scales, const uint8_t* zc, float* w,
                            int N, int K, int group, cudaStream_t st) {
-    long long words = (long long)N * K / fmt_cpw(fmt);
+    long long words = Layout(N, K, fmt).bytes() / 4;
     int g = grid_for(words, 256);
     switch (fmt) {
         case UQ_INT4_SYM: dequant_kernel<UQ_INT4_SYM><<<g, 256, 0, st>>>(wq, scales, zc, w, N, K, group); break;

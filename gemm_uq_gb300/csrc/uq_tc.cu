@@ -16,10 +16,11 @@
 // So the products and the per-group sums are exact up to fp32 accumulation, as in the GEMV.
 //
 // Roles (384 threads, one CTA per SM, persistent over an equal contiguous range of units):
-//   warp 0       TMA producer: per unit one 4-D box of codes (16 tiles x 8 rows x 128 bytes,
-//                128-byte swizzle) and kc/64 boxes of x, counted on full[stage];
+//   warp 0       producer: per unit eight 2 KB bulk copies of codes (one per 16-row block of the
+//                fragment-order plane) and kc/64 TMA boxes of x, counted on full[stage];
 //   warp 1       MMA issuer (one thread): per group g/16 tcgen05.mma (M=128, N=Mpad, K=16);
-//   warps 4..7   dequant: thread = weight row; reads its 128 code bytes, writes kc/2 columns;
+//   warps 4..7   dequant: thread = weight row; reads its codes from the fragment-order chunks,
+//                writes kc/2 columns of (q - z) into tensor memory;
 //   warps 8..11  epilogue: thread = weight row; scales, accumulates over the row block's units,
 //                then stores y, or a partial sum plus a ticket (the last contributor reduces
 //                the partials in CTA order, so results are deterministic and nobody waits).
@@ -87,13 +88,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
-                                            uint64_t* bar) {
-    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
-                 " [%0], [%1, {%2, %3, %4, %5}], [%6];"
-                 :: "r"(smem_u32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
-                 : "memory");
-}
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
     asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
                  " [%0], [%1, {%2, %3}], [%4];"
@@ -138,8 +132,7 @@ struct TcSmem {
 
 template <int FMT, int MPAD>
 __global__ void __launch_bounds__(TC_THREADS, 1)
-tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_constant__ CUtensorMap tmap_x,
-          const TcArgs a) {
+tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
     constexpr int KC = TcFmt<FMT>::KC;
     constexpr int ACOLS = TcFmt<FMT>::ACOLS;
     constexpr int XB = TcSmem::x_bytes(KC, MPAD);
@@ -167,6 +160,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_constant_
     const int cta = blockIdx.x;
     const long long u0 = trange_begin(cta, a.U, a.P), u1 = trange_begin(cta + 1, a.U, a.P);
 
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 5); }
         for (int i = 0; i < 2; ++i) { mbar_init(&afull[i], 4); mbar_init(&aempty[i], 1); }
@@ -188,20 +182,40 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_constant_
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
             int issued = 0;
-            for (long long u = u0; u < u1 && !*abort_flag; ++u, ++issued) {
+            auto issue_codes = [&](long long u, int s) {
+                const int rb = (int)(u / a.CH), c = (int)(u % a.CH);
+                uint8_t* st = smem + s * SB;
+                // for each of the 8 row blocks of 16, the unit's 4 chunks (2 KB, contiguous)
+                const int nb0 = rb * 8;
+                const int nbs = (a.NB - nb0) < 8 ? (a.NB - nb0) : 8;
+                mbar_arrive_expect_tx(&full[s], (uint32_t)(nbs * 2048 + XB));
+                const int kb = c >> 2, q0 = (c & 3) * 4;
+                for (int j = 0; j < nbs; ++j)
+                    bulk_g2s(st + j * 2048, a.wq + (long long)(nb0 + j) * 16 * a.rowbytes + (long long)kb * 8192 + q0 * 512,
+                             2048u, &full[s]);
+            };
+            auto issue_x = [&](long long u, int s) {
+                const int c = (int)(u % a.CH);
+                uint8_t* st = smem + s * SB;
+#pragma unroll
+                for (int q = 0; q < KC / 64; ++q)
+                    tma_load_2d(st + TC_STAGE_CODES + q * (MPAD * 128), &tmap_x, c * KC + q * 64, 0, &full[s]);
+            };
+            // the first stages' weights are constant: stream them before waiting for the previous
+            // kernel on the stream (launch overlap); x is loaded only after that wait
+            const int pre = (u1 - u0) < S ? (int)(u1 - u0) : S;
+            for (int j = 0; j < pre; ++j) issue_codes(u0 + j, j);
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            for (int j = 0; j < pre; ++j) issue_x(u0 + j, j);
+            issued = pre;
+            for (long long u = u0 + pre; u < u1 && !*abort_flag; ++u, ++issued) {
                 const int i = (int)(u - u0), s = i % S;
                 if (!mbar_wait_bounded(&empty[s], (uint32_t)(((i / S) & 1) ^ 1), a.fault, FAULT_TC_WAIT)) {
                     *abort_flag = 1;
                     break;
                 }
-                const int rb = (int)(u / a.CH), c = (int)(u % a.CH);
-                uint8_t* st = smem + s * SB;
-                mbar_arrive_expect_tx(&full[s], (uint32_t)SB);
-                // codes: byte (c % 4) * 128 of the tile row, rows 0..7, k tile c / 4, 16 row blocks of 8
-                tma_load_4d(st, &tmap_codes, (c & 3) * 128, 0, c >> 2, rb * 16, &full[s]);
-#pragma unroll
-                for (int q = 0; q < KC / 64; ++q)
-                    tma_load_2d(st + TC_STAGE_CODES + q * (MPAD * 128), &tmap_x, c * KC + q * 64, 0, &full[s]);
+                issue_codes(u, s);
+                issue_x(u, s);
             }
             // let the last copies land before the CTA can leave
             for (int j = issued - 1; j >= 0 && j >= issued - S; --j)
@@ -272,43 +286,56 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_constant_
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) { *abort_flag = 1; break; }
             tc_fence_after();
-            const uint8_t* crow = smem + s * SB + (r >> 3) * 1024 + (r & 7) * 128;
+            // row r = 16 rbl + 8 h + g sits in lane chunks 4g .. 4g + 3 of its row block (fragment
+            // order); read them rotated by g / 2 so a quarter warp touches 8 distinct 16-byte slots
+            const int rbl = r >> 4, hh = (r >> 3) & 1, gg = r & 7;
+            const uint8_t* rbase = smem + s * SB + rbl * 2048 + gg * 64;
             const uint32_t acol = lane_addr + A_COL0 + ab * ACOLS;
             if constexpr (FMT == UQ_INT8_SYM) {
-                // 128 codes = 8 chunks of 16 bytes -> 64 columns; each chunk gives 8 columns
+                // chunk q = 32 k: words h (block 0) and 2 + h (block 1), 4 bytes each -> 16 columns
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
+                for (int q = 0; q < 4; ++q) {
                     uint32_t v[16];
 #pragma unroll
-                    for (int cc2 = 0; cc2 < 2; ++cc2) {
-                        const int cc = h * 2 + cc2;
-                        const uint4 q = *reinterpret_cast<const uint4*>(crow + ((cc ^ (r & 7)) << 4));
-                        const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int cc = (jj + (gg >> 1)) & 3;
+                        const uint4 w4 = *reinterpret_cast<const uint4*>(rbase + q * 512 + cc * 16);
+                        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float f0 = byte_magic_f32(wv[e], 0) - 8388736.0f;
-                            const float f1 = byte_magic_f32(wv[e], 1) - 8388736.0f;
-                            const float f2 = byte_magic_f32(wv[e], 2) - 8388736.0f;
-                            const float f3 = byte_magic_f32(wv[e], 3) - 8388736.0f;
-                            v[cc2 * 8 + 2 * e] = f32x2_to_bf16x2(f0, f1);
-                            v[cc2 * 8 + 2 * e + 1] = f32x2_to_bf16x2(f2, f3);
+                        for (int b2 = 0; b2 < 2; ++b2) {
+                            const uint32_t wd = wv[2 * b2 + hh];
+                            const float f0 = byte_magic_f32(wd, 0) - 8388736.0f;
+                            const float f1 = byte_magic_f32(wd, 1) - 8388736.0f;
+                            const float f2 = byte_magic_f32(wd, 2) - 8388736.0f;
+                            const float f3 = byte_magic_f32(wd, 3) - 8388736.0f;
+                            v[b2 * 8 + 2 * cc] = f32x2_to_bf16x2(f0, f1);
+                            v[b2 * 8 + 2 * cc + 1] = f32x2_to_bf16x2(f2, f3);
                         }
                     }
-                    tmem_st16(acol + h * 16, v);
+                    tmem_st16(acol + q * 16, v);
                 }
             } else {
-                // 256 codes = 8 chunks of 16 bytes (32 codes) -> 128 columns; one chunk = 16 columns
+                // chunk q = 64 k: words i = 16-k blocks; pairs hh (k 4c, 4c+1) and hh + 2 (k 4c+2, 4c+3)
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const uint4 q = *reinterpret_cast<const uint4*>(crow + ((cc ^ (r & 7)) << 4));
-                    const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
-                    const uint32_t zs = zsub[(cc * 32) / G];
-                    uint32_t v[16];
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t v[32];
 #pragma unroll
-                    for (int w = 0; w < 4; ++w)
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int cc = (jj + (gg >> 1)) & 3;
+                        const uint4 w4 = *reinterpret_cast<const uint4*>(rbase + q * 512 + cc * 16);
+                        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-                        for (int p = 0; p < 4; ++p) v[w * 4 + p] = bf16x2_sub(nib_pair_bf16(wv[w], p), zs);
-                    tmem_st16(acol + cc * 16, v);
+                        for (int i = 0; i < 4; ++i) {
+                            const uint32_t zs = zsub[(q * 64 + i * 16) / G];
+                            v[i * 8 + 2 * cc] = bf16x2_sub(nib_pair_bf16(wv[i], hh), zs);
+                            v[i * 8 + 2 * cc + 1] = bf16x2_sub(nib_pair_bf16(wv[i], hh + 2), zs);
+                        }
+                    }
+                    uint32_t lo[16], hi[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) { lo[e] = v[e]; hi[e] = v[16 + e]; }
+                    tmem_st16(acol + q * 32, lo);
+                    tmem_st16(acol + q * 32 + 16, hi);
                 }
             }
             tmem_st_wait();
@@ -318,6 +345,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const __grid_constant_
         }
     } else if (warp >= 8) {
         // ---------------------------------------------------------------- epilogue warpgroup
+        asm volatile("griddepcontrol.wait;" ::: "memory");   // sx, workspace and y follow earlier work
         const int we = warp - 8;
         const int r = we * 32 + lane;
         const uint32_t lane_addr = tmem + ((uint32_t)(we * 32) << 16);
@@ -477,8 +505,7 @@ EncodeTiledFn encode_fn() {
 }
 
 template <int FMT, int MPAD>
-cudaError_t launch_tc_t(const CUtensorMap& mc, const CUtensorMap& mx, const TcArgs& a, size_t smem, int grid,
-                        cudaStream_t st) {
+cudaError_t launch_tc_t(const CUtensorMap& mx, const TcArgs& a, size_t smem, int grid, cudaStream_t st) {
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -489,18 +516,33 @@ cudaError_t launch_tc_t(const CUtensorMap& mc, const CUtensorMap& mx, const TcAr
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    tc_kernel<FMT, MPAD><<<grid, TC_THREADS, smem, st>>>(mc, mx, a);
+    if (launch_overlap()) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(TC_THREADS);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, tc_kernel<FMT, MPAD>, mx, a);
+        if (e != cudaSuccess) return e;
+    } else {
+        tc_kernel<FMT, MPAD><<<grid, TC_THREADS, smem, st>>>(mx, a);
+    }
     return cudaGetLastError();
 }
 
 template <int FMT>
-cudaError_t launch_tc_m(int mpad, const CUtensorMap& mc, const CUtensorMap& mx, const TcArgs& a, size_t smem,
-                        int grid, cudaStream_t st) {
+cudaError_t launch_tc_m(int mpad, const CUtensorMap& mx, const TcArgs& a, size_t smem, int grid,
+                        cudaStream_t st) {
     switch (mpad) {
-        case 16: return launch_tc_t<FMT, 16>(mc, mx, a, smem, grid, st);
-        case 32: return launch_tc_t<FMT, 32>(mc, mx, a, smem, grid, st);
-        case 48: return launch_tc_t<FMT, 48>(mc, mx, a, smem, grid, st);
-        case 64: return launch_tc_t<FMT, 64>(mc, mx, a, smem, grid, st);
+        case 16: return launch_tc_t<FMT, 16>(mx, a, smem, grid, st);
+        case 32: return launch_tc_t<FMT, 32>(mx, a, smem, grid, st);
+        case 48: return launch_tc_t<FMT, 48>(mx, a, smem, grid, st);
+        case 64: return launch_tc_t<FMT, 64>(mx, a, smem, grid, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -508,8 +550,7 @@ cudaError_t launch_tc_m(int mpad, const CUtensorMap& mc, const CUtensorMap& mx, 
 
 bool tc_supported(int fmt, int N, int K) {
     if (fmt != UQ_INT4_SYM && fmt != UQ_INT4_ASYM && fmt != UQ_INT8_SYM && fmt != UQ_K4) return false;
-    if (N % 8) return false;
-    if (K % fmt_kt(fmt)) return false;
+    if (N < 1 || K % fmt_kt(fmt)) return false;
     return encode_fn() != nullptr;
 }
 
@@ -535,23 +576,10 @@ cudaError_t launch_colsum32(const uint16_t* x, float* sx, int M, int mpad, int K
     return cudaGetLastError();
 }
 
-cudaError_t launch_tc(int fmt, const uint16_t* x, const uint8_t* wq, const TcArgs& a, size_t smem, int grid,
-                      cudaStream_t st) {
+cudaError_t launch_tc(int fmt, const uint16_t* x, const TcArgs& a, size_t smem, int grid, cudaStream_t st) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    const int kt = fmt_kt(fmt);
-    const int KB = a.K / kt, NBt = a.N / 8;
-    CUtensorMap mc, mx;
-    {
-        cuuint64_t dims[4] = {512, 8, (cuuint64_t)KB, (cuuint64_t)NBt};
-        cuuint64_t strides[3] = {512, 4096, (cuuint64_t)KB * 4096};
-        cuuint32_t box[4] = {128, 8, 1, 16};
-        cuuint32_t es[4] = {1, 1, 1, 1};
-        if (enc(&mc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(wq), dims, strides, box, es,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
+    CUtensorMap mx;
     {
         cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
         cuuint64_t strides[1] = {(cuuint64_t)a.ldx * 2};
@@ -563,10 +591,10 @@ cudaError_t launch_tc(int fmt, const uint16_t* x, const uint8_t* wq, const TcArg
             return cudaErrorInvalidValue;
     }
     switch (fmt) {
-        case UQ_INT4_SYM: return launch_tc_m<UQ_INT4_SYM>(a.Mpad, mc, mx, a, smem, grid, st);
-        case UQ_INT4_ASYM: return launch_tc_m<UQ_INT4_ASYM>(a.Mpad, mc, mx, a, smem, grid, st);
-        case UQ_INT8_SYM: return launch_tc_m<UQ_INT8_SYM>(a.Mpad, mc, mx, a, smem, grid, st);
-        case UQ_K4: return launch_tc_m<UQ_K4>(a.Mpad, mc, mx, a, smem, grid, st);
+        case UQ_INT4_SYM: return launch_tc_m<UQ_INT4_SYM>(a.Mpad, mx, a, smem, grid, st);
+        case UQ_INT4_ASYM: return launch_tc_m<UQ_INT4_ASYM>(a.Mpad, mx, a, smem, grid, st);
+        case UQ_INT8_SYM: return launch_tc_m<UQ_INT8_SYM>(a.Mpad, mx, a, smem, grid, st);
+        case UQ_K4: return launch_tc_m<UQ_K4>(a.Mpad, mx, a, smem, grid, st);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -173,6 +173,17 @@ uq_status uq_quantize_k4(const float* w, int8_t* codes, uint16_t* d, uint16_t* d
 uq_status uq_pack_zeros(const uint8_t* zeros, uint8_t* packed, int N, int G, void* stream);
 
 /*
+ * uq_set_launch_overlap -- process-wide switch (default 0 = off) for how uq_gemm launches its
+ * GEMV and tensor-core kernels.  When on, each launch uses programmatic dependent launch: the kernel may
+ * begin while the previous kernel on the same stream is still finishing, and streams its packed
+ * weights, scales and zero points from HBM during that time; it waits for the previous kernel to
+ * complete before it reads x, touches the split-K workspace or writes y.  Turn it on only when
+ * wq / scales / zeros_or_codebook are not written by the work that immediately precedes the
+ * call on the stream (true for a decode loop over fixed weights).  Host-only; always UQ_OK.
+ */
+uq_status uq_set_launch_overlap(int enable);
+
+/*
  * uq_device_fault -- reads and clears the device-side fault word of the current device
  * (set when a kernel's bounded wait on an mbarrier ran out and the kernel returned
  * early instead of hanging).  Synchronizes the device.  *flag = 0 when no fault.
@@ -189,8 +200,8 @@ uq_status uq_device_fault(unsigned int* flag);
  * owned device buffers), computed with the same GEMV kernel for every M (row blocks of 8; no
  * tensor-core path), so the output equals uq_gemm's for M <= 15.
  * Scratch: a 1 MiB static device array inside the library (every GPU that loads the library holds
- * it until the process exits): room for N <= 524288 and for the split-K partial sums of one row
- * block of x; larger requests return UQ_ERR_NOMEM with the limit in uq_last_error().  K == 0 returns
+ * it until the process exits): room for N <= 1048576 and for the split-K partial sums of one
+ * 8-row block of x; larger requests return UQ_ERR_NOMEM with the limit in uq_last_error().  K == 0 returns
  * UQ_ERR_UNSUPPORTED.  Calls no cudaMalloc, cudaFree or other allocating routine.
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress) with
  * that device current; make that first call before any stream capture.  Every call shares the one

@@ -47,10 +47,14 @@ def test_noalloc_matches_uq_gemm_on_two_calls_in_a_row():
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch():
-    xd = torch.zeros((1, 256), dtype=torch.bfloat16, device=DEV)
-    wq = torch.zeros(16, dtype=torch.uint8, device=DEV)
-    sc = torch.zeros(16, dtype=torch.int16, device=DEV)
-    y = torch.zeros((1, 16), dtype=torch.bfloat16, device=DEV)
+    """N one row block past the static ticket area.  Every buffer is sized for the request, so
+    the call would only read valid memory even if the size check did not fire."""
+    N, K, group, fmt = 1048576 + 16, 32, 32, "INT4_SYM"
+    wq_bytes, sc_bytes, _ = uq.packed_size(N, K, group, fmt)
+    xd = torch.zeros((1, K), dtype=torch.bfloat16, device=DEV)
+    wq = torch.zeros(wq_bytes, dtype=torch.uint8, device=DEV)
+    sc = torch.zeros(sc_bytes // 2, dtype=torch.int16, device=DEV)
+    y = torch.zeros((1, N), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(uq.UqError) as e:
-        uq.gemm_noalloc(xd, wq, sc, None, 600000, 32, "INT4_SYM", y=y)   # N beyond the ticket area
+        uq.gemm_noalloc(xd, wq, sc, None, N, group, fmt, y=y)
     assert e.value.status == 5
