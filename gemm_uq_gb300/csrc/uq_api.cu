@@ -161,7 +161,8 @@ uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const 
     if (uq::gemv_smem_bytes(fmt, K, group, Mb) > 227 * 1024)
         return fail(UQ_ERR_UNSUPPORTED, "K=%d is too long for the GEMV's shared-memory x-sum table at M=%d", K, Mb);
     const long long T = (long long)L.NB * L.KB;
-    long long P = (long long)ds.sms * uq::GEMV_WARPS;
+    const int warps = uq::gemv_warps(fmt);
+    long long P = (long long)ds.sms * warps;
     if (P > T) P = T;
     Workspace* ws = nullptr;
     uq_status s = workspace(dev, st, uq::gemv_partials_floats((int)P, Mb) * sizeof(float),
@@ -178,7 +179,7 @@ uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const 
     a.partials = ws->partials;
     a.tickets = ws->tickets;
     a.fault = ds.words;
-    const int grid = (int)((P + uq::GEMV_WARPS - 1) / uq::GEMV_WARPS);
+    const int grid = (int)((P + warps - 1) / warps);
     cudaError_t e = uq::launch_gemv(fmt, a, grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "GEMV launch");
     return UQ_OK;

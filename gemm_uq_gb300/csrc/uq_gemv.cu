@@ -11,6 +11,7 @@ extern template cudaError_t launch_gemv_fmt<UQ_NF4>(const GemvArgs&, int, cudaSt
 extern template cudaError_t launch_gemv_fmt<UQ_K4>(const GemvArgs&, int, cudaStream_t);
 
 size_t gemv_smem_bytes(int fmt, int K, int group, int M) { return gemv_smem_bytes_impl(fmt, K, group, M); }
+int gemv_warps(int fmt) { return gemv_warps_impl(fmt); }
 size_t gemv_partials_floats(int P, int M) { return gemv_partials_floats_impl(P, M); }
 
 cudaError_t launch_gemv(int fmt, const GemvArgs& a, int grid, cudaStream_t st) {

@@ -635,11 +635,301 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
     }
 }
 
+
+// ------------------------------------------------------------------------------------------------
+// 4-bit and 2-bit formats: the GEMV on mma.sync.  GB = 16-k blocks per scaling group (2, 4 or 8;
+// K4 uses its 32-weight sub-blocks, GB = 2).  M (1..8) is a runtime value: the instruction always
+// computes 8 columns, so the work per weight does not depend on it.
+template <int FMT> struct MmaCfg {
+    static constexpr int WARPS = (FMT == UQ_INT2_ASYM) ? 6 : 8;    // workers per CTA
+    static constexpr int STAGES = 2;                               // tiles in flight per worker
+};
+
+__host__ __device__ inline GemvSmem gemv_mma_smem_plan(int fmt, int K, int group, int M, bool x_in_smem) {
+    int stage = 0, warps = 0, kc = fmt_kc(fmt);
+    switch (fmt) {
+        case UQ_INT4_SYM: stage = GemvFmt<UQ_INT4_SYM>::STAGE_BYTES; warps = MmaCfg<UQ_INT4_SYM>::WARPS; break;
+        case UQ_INT4_ASYM: stage = GemvFmt<UQ_INT4_ASYM>::STAGE_BYTES; warps = MmaCfg<UQ_INT4_ASYM>::WARPS; break;
+        case UQ_INT2_ASYM: stage = GemvFmt<UQ_INT2_ASYM>::STAGE_BYTES; warps = MmaCfg<UQ_INT2_ASYM>::WARPS; break;
+        default: stage = GemvFmt<UQ_K4>::STAGE_BYTES; warps = MmaCfg<UQ_K4>::WARPS; break;
+    }
+    const int stages = 2;
+    const int Kp = (K + kc - 1) / kc * kc;
+    const int gs = (fmt == UQ_K4) ? 32 : group;
+    GemvSmem p;
+    p.bars = (size_t)warps * stages * stage;
+    p.lut = p.bars + (size_t)(warps * stages + 1) * 8;
+    p.sx = p.lut + 64;
+    p.x = p.sx + (size_t)((Kp + gs - 1) / gs) * 8 * 4;
+    p.x = (p.x + 127) / 128 * 128;
+    p.total = p.x + (x_in_smem ? (size_t)M * gemv_x_stride(Kp) : 0);
+    return p;
+}
+
+template <int FMT, int GB, bool XS>
+__global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(const GemvArgs a) {
+    using F = GemvFmt<FMT>;
+    constexpr int KT = F::KT, S = MmaCfg<FMT>::STAGES, W = MmaCfg<FMT>::WARPS;
+    constexpr int GS = GB * 16;                                     // k per scaling group
+    constexpr int GPT = KT / GS;                                    // groups per full tile row
+    constexpr int WPG = (FMT == UQ_INT2_ASYM) ? GB / 2 : GB;        // code words per lane per group
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int M = a.M;
+    const GemvSmem plan = gemv_mma_smem_plan(FMT, a.K, a.group, M, XS);
+    uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + plan.bars);
+    float* sxg = reinterpret_cast<float*>(smem + plan.sx);
+    uint8_t* xs = smem + plan.x;
+    uint64_t* xbar = bars_all + W * S;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const int w = blockIdx.x * W + warp;
+    const bool has_work = w < a.P;
+    const Layout L(a.N, a.K, FMT);
+    uint8_t* ring = smem + (size_t)warp * S * F::STAGE_BYTES;
+    uint64_t* bars = bars_all + warp * S;
+    const long long t0 = has_work ? range_begin(w, a.T, a.P) : 0;
+    const long long t1 = has_work ? range_begin(w + 1, a.T, a.P) : 0;
+    MetaConst mc;
+    mc.G = a.K / a.group;
+    mc.GT = KT / a.group;
+    mc.ZB = (mc.G + 1) >> 1;
+    mc.S4 = a.K / 256;
+    mc.aligned = (a.K % (8 * a.group)) == 0 && (mc.GT % 8) == 0;
+    const int G_all = a.K / GS;                                     // real scaling groups per row
+    const size_t xstride = gemv_x_stride(L.Kp);
+
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (has_work) {
+        if (lane == 0) {
+#pragma unroll
+            for (int s = 0; s < S; ++s) mbar_init(&bars[s], 33);
+            fence_barrier_init();
+        }
+        __syncwarp();
+        int inb = (int)(t0 / L.KB), ikb = (int)(t0 % L.KB);
+        for (int s = 0; s < S && t0 + s < t1; ++s) {
+            issue_tile<FMT>(a, L, mc, inb, ikb, ring + s * F::STAGE_BYTES, &bars[s], lane);
+            if (++ikb == L.KB) { ikb = 0; ++inb; }
+        }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if constexpr (XS) {
+        if (threadIdx.x == 0) {
+            mbar_init(xbar, 1);
+            fence_barrier_init();
+            mbar_arrive_expect_tx(xbar, (uint32_t)(M * a.K * 2));
+            for (int m = 0; m < M; ++m) bulk_g2s(xs + m * xstride, a.x + (long long)m * a.ldx, (uint32_t)(a.K * 2), xbar);
+        }
+        const int padw = (L.Kp - a.K) / 2;
+        for (int e = threadIdx.x; e < M * padw; e += blockDim.x)
+            reinterpret_cast<uint32_t*>(xs + (e / padw) * xstride + a.K * 2)[e % padw] = 0u;
+        __syncthreads();
+        mbar_wait_bounded(xbar, 0, a.fault, FAULT_GEMV_WAIT);
+    }
+    {
+        // sxg[gi * 8 + m] = sum of x[m][k] over group gi, in k order; 0 for m >= M
+        for (int e = threadIdx.x; e < G_all * 8; e += blockDim.x) {
+            const int gi = e >> 3, m = e & 7;
+            float s0 = 0.f;
+            if (m < M) {
+#pragma unroll
+                for (int k = 0; k < GS; k += 8) {
+                    uint4 q;
+                    if constexpr (XS) q = *reinterpret_cast<const uint4*>(xs + m * xstride + (gi * GS + k) * 2);
+                    else q = ldg_nc_v4(a.x + (long long)m * a.ldx + gi * GS + k);
+                    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) s0 += bf16lo_f32(u[j]) + bf16hi_f32(u[j]);
+                }
+            }
+            sxg[e] = s0;
+        }
+    }
+    __syncthreads();
+    if (!has_work) return;
+
+    const int first_nb = (int)(t0 / L.KB);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};        // rows g + 8j, columns 2c + e
+    const int mrow = g < M ? g : M - 1;          // B rows beyond M repeat a real row; their D columns are unused
+    const uint8_t* xrow = xs + mrow * xstride + 8 * c;
+    const uint16_t* xgrow = a.x + (long long)mrow * a.ldx + 4 * c;
+    int nb = (int)(t0 / L.KB), kb = (int)(t0 % L.KB);
+    int pnb = nb, pkb = kb;
+    for (int s = 0; s < S; ++s)
+        if (++pkb == L.KB) { pkb = 0; ++pnb; }
+
+    for (long long t = t0; t < t1; ++t) {
+        const int it = (int)(t - t0);
+        const int s = it % S;
+        const uint32_t parity = (uint32_t)((it / S) & 1);
+        const int n0 = nb * RB;
+        uint8_t* st = ring + s * F::STAGE_BYTES;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], parity, a.fault, FAULT_GEMV_WAIT))) {
+            for (int j = 1; j < S && t + j < t1; ++j) {
+                const int sj = (it + j) % S;
+                mbar_wait_bounded(&bars[sj], (uint32_t)(((it + j) / S) & 1), a.fault, FAULT_GEMV_WAIT);
+            }
+            return;
+        }
+        const int gi0 = kb * GPT;
+        const int ng = (G_all - gi0) < GPT ? (G_all - gi0) : GPT;   // groups of the tile inside K
+        RowPtrs<FMT> rp[2];
+        if constexpr (FMT != UQ_K4) {
+            rp[0] = row_ptrs<FMT>(st, mc, g, n0 + g, kb);
+            rp[1] = row_ptrs<FMT>(st, mc, g + 8, n0 + g + 8, kb);
+        }
+        const uint8_t* xt = xrow + (size_t)kb * KT * 2;             // x of the tile's first k
+        const uint16_t* xgt = xgrow + (long long)kb * KT;
+        for (int gg = 0; gg < ng; ++gg) {
+            // this lane's code words for the group's GB blocks
+            uint32_t wv[WPG];
+            {
+                constexpr int BPCH = F::BPC;                        // blocks per 512-byte chunk
+                const int blk = gg * GB;                            // first block of the group in the tile
+                const uint8_t* cp = st + (blk / BPCH) * CHUNK + lane * 16 + ((blk % BPCH) * WPG / GB) * 4;
+                if constexpr (WPG == 4) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(cp);
+                    wv[0] = v.x; wv[1] = v.y; wv[2] = v.z; wv[3] = v.w;
+                } else if constexpr (WPG == 8) {
+                    const uint4 v0 = *reinterpret_cast<const uint4*>(cp);
+                    const uint4 v1 = *reinterpret_cast<const uint4*>(cp + CHUNK);
+                    wv[0] = v0.x; wv[1] = v0.y; wv[2] = v0.z; wv[3] = v0.w;
+                    wv[4] = v1.x; wv[5] = v1.y; wv[6] = v1.z; wv[7] = v1.w;
+                } else if constexpr (WPG == 2) {
+                    const uint2 v = *reinterpret_cast<const uint2*>(cp);
+                    wv[0] = v.x; wv[1] = v.y;
+                } else {
+                    wv[0] = *reinterpret_cast<const uint32_t*>(cp);
+                }
+            }
+            // B fragments of the group's blocks (x at k = 16 blk + 4c .. +3 of row mrow)
+            uint2 bfr[GB];
+            if constexpr (XS) {
+#pragma unroll
+                for (int j = 0; j < GB; ++j) bfr[j] = *reinterpret_cast<const uint2*>(xt + (gg * GB + j) * 32);
+            } else {
+#pragma unroll
+                for (int j = 0; j < GB; ++j) {
+                    const int kk = (gg * GB + j) * 16;
+                    bfr[j] = (kb * KT + kk + 4 * c < a.K) ? ldg_nc_v2(xgt + kk) : make_uint2(0, 0);
+                }
+            }
+            float dd[2][4];
+#pragma unroll
+            for (int j = 0; j < GB; ++j) {
+                const uint2 b = bfr[j];
+                uint32_t a0, a1, a2, a3;
+                if constexpr (FMT == UQ_INT2_ASYM) {
+                    const uint32_t wd = wv[j >> 1];
+                    const int pb = (j & 1) * 4;
+                    a0 = crumb_pair_bf16(wd, pb + 0); a1 = crumb_pair_bf16(wd, pb + 1);
+                    a2 = crumb_pair_bf16(wd, pb + 2); a3 = crumb_pair_bf16(wd, pb + 3);
+                } else {
+                    const uint32_t wd = wv[j];
+                    a0 = nib_pair_bf16(wd, 0); a1 = nib_pair_bf16(wd, 1);
+                    a2 = nib_pair_bf16(wd, 2); a3 = nib_pair_bf16(wd, 3);
+                }
+                if (j < 2) mma_bf16_zero(dd[j & 1], a0, a1, a2, a3, b.x, b.y);
+                else mma_bf16(dd[j & 1], a0, a1, a2, a3, b.x, b.y);
+            }
+            // fold the group into the row sums
+            const int gi = gi0 + gg;
+            const float2 sxv = *reinterpret_cast<const float2*>(sxg + gi * 8 + 2 * c);
+            float d[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d[e] = dd[0][e] + dd[1][e];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                if constexpr (FMT == UQ_K4) {
+                    float dsc, dmm;
+                    row_meta_k4(st, g + 8 * j, gg, dsc, dmm);
+                    const float off = fmaf(128.0f, dsc, dmm);
+                    acc[2 * j] = fmaf(dsc, d[2 * j], fmaf(-off, sxv.x, acc[2 * j]));
+                    acc[2 * j + 1] = fmaf(dsc, d[2 * j + 1], fmaf(-off, sxv.y, acc[2 * j + 1]));
+                } else {
+                    float sc, zc;
+                    row_meta<FMT>(rp[j], gg, sc, zc);
+                    const float szc = sc * zc;
+                    acc[2 * j] = fmaf(sc, d[2 * j], fmaf(-szc, sxv.x, acc[2 * j]));
+                    acc[2 * j + 1] = fmaf(sc, d[2 * j + 1], fmaf(-szc, sxv.y, acc[2 * j + 1]));
+                }
+            }
+        }
+        __syncwarp();
+        if (t + S < t1) {
+            issue_tile<FMT>(a, L, mc, pnb, pkb, st, &bars[s], lane);
+            if (++pkb == L.KB) { pkb = 0; ++pnb; }
+        }
+
+        if (kb == L.KB - 1 || t == t1 - 1) {
+            const bool full = (kb == L.KB - 1) && (nb != first_nb || (t0 % L.KB) == 0);
+            if (full) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int n = n0 + g + 8 * j, m = 2 * c + e;
+                        if (m < M && n < a.N)
+                            a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * j + e]));
+                    }
+            } else {
+                const int slot = 2 * w + (nb == first_nb ? 0 : 1);
+                float* part = a.partials + (long long)slot * RB * M;
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        if (2 * c + e < M) part[(g + 8 * j) * M + 2 * c + e] = acc[2 * j + e];
+                __threadfence();
+                __syncwarp();
+                unsigned int old = 0;
+                if (lane == 0) old = atomicAdd(a.tickets + nb, 1u);
+                old = __shfl_sync(0xffffffffu, old, 0);
+                const long long tf = (long long)nb * L.KB;
+                const int wf = worker_of(tf, a.T, a.P), wl = worker_of(tf + L.KB - 1, a.T, a.P);
+                if (old == (unsigned int)(wl - wf)) {
+                    __threadfence();
+                    for (int e = lane; e < RB * M; e += 32) {
+                        const int r = e / M, m = e % M;
+                        if (n0 + r >= a.N) continue;
+                        float sum = 0.f;
+                        for (int w2 = wf; w2 <= wl; ++w2) {
+                            const int nb2 = (int)(range_begin(w2, a.T, a.P) / L.KB);
+                            const int slot2 = 2 * w2 + (nb == nb2 ? 0 : 1);
+                            sum += __ldcg(a.partials + (long long)slot2 * RB * M + e);
+                        }
+                        a.y[(long long)m * a.ldy + n0 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+                    }
+                    if (lane == 0) a.tickets[nb] = 0u;
+                }
+            }
+            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+        }
+        if (++kb == L.KB) { kb = 0; ++nb; }
+    }
+}
+
+inline bool gemv_is_mma(int fmt) {
+    return fmt == UQ_INT4_SYM || fmt == UQ_INT4_ASYM || fmt == UQ_INT2_ASYM || fmt == UQ_K4;
+}
+inline GemvSmem gemv_any_plan(int fmt, int K, int group, int M, bool xs) {
+    return gemv_is_mma(fmt) ? gemv_mma_smem_plan(fmt, K, group, M, xs) : gemv_smem_plan(fmt, K, group, M, xs);
+}
 inline bool gemv_x_in_smem(int fmt, int K, int group, int M) {
-    return gemv_smem_plan(fmt, K, group, M, true).total <= 227 * 1024;
+    return gemv_any_plan(fmt, K, group, M, true).total <= 227 * 1024;
 }
 inline size_t gemv_smem_bytes_impl(int fmt, int K, int group, int M) {
-    return gemv_smem_plan(fmt, K, group, M, gemv_x_in_smem(fmt, K, group, M)).total;
+    return gemv_any_plan(fmt, K, group, M, gemv_x_in_smem(fmt, K, group, M)).total;
+}
+inline int gemv_warps_impl(int fmt) {
+    switch (fmt) {
+        case UQ_INT4_SYM: return MmaCfg<UQ_INT4_SYM>::WARPS;
+        case UQ_INT4_ASYM: return MmaCfg<UQ_INT4_ASYM>::WARPS;
+        case UQ_INT2_ASYM: return MmaCfg<UQ_INT2_ASYM>::WARPS;
+        case UQ_K4: return MmaCfg<UQ_K4>::WARPS;
+        default: return GEMV_WARPS;
+    }
 }
 inline size_t gemv_partials_floats_impl(int P, int M) { return (size_t)2 * P * RB * M; }
 
@@ -682,8 +972,60 @@ cudaError_t launch_xs(const GemvArgs& a, int grid, cudaStream_t st) {
 }
 }  // namespace gemv_detail
 
+namespace gemv_detail {
+template <int FMT, int GB, bool XS>
+cudaError_t launch_mma(const GemvArgs& a, int grid, cudaStream_t st) {
+    static bool configured[64] = {};
+    const size_t smem = gemv_mma_smem_plan(FMT, a.K, a.group, a.M, XS).total;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(gemv_mma_kernel<FMT, GB, XS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 227 * 1024);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    const int threads = MmaCfg<FMT>::WARPS * 32;
+    if (launch_overlap()) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(threads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, gemv_mma_kernel<FMT, GB, XS>, a);
+        if (e != cudaSuccess) return e;
+    } else {
+        gemv_mma_kernel<FMT, GB, XS><<<grid, threads, smem, st>>>(a);
+    }
+    return cudaGetLastError();
+}
+template <int FMT, int GB>
+cudaError_t launch_mma_xs(const GemvArgs& a, int grid, cudaStream_t st) {
+    if (gemv_x_in_smem(FMT, a.K, a.group, a.M)) return launch_mma<FMT, GB, true>(a, grid, st);
+    return launch_mma<FMT, GB, false>(a, grid, st);
+}
+}  // namespace gemv_detail
+
 template <int FMT>
 cudaError_t launch_gemv_fmt(const GemvArgs& a, int grid, cudaStream_t st) {
+    if constexpr (FMT == UQ_INT4_SYM || FMT == UQ_INT4_ASYM || FMT == UQ_INT2_ASYM || FMT == UQ_K4) {
+        const int gs = (FMT == UQ_K4) ? 32 : a.group;
+        switch (gs) {
+            case 32: return gemv_detail::launch_mma_xs<FMT, 2>(a, grid, st);
+            case 64: if constexpr (FMT != UQ_K4) return gemv_detail::launch_mma_xs<FMT, 4>(a, grid, st);
+                     return cudaErrorInvalidValue;
+            case 128: if constexpr (FMT != UQ_K4) return gemv_detail::launch_mma_xs<FMT, 8>(a, grid, st);
+                      return cudaErrorInvalidValue;
+            default: return cudaErrorInvalidValue;
+        }
+    } else {
     switch (a.M) {
         case 1: return gemv_detail::launch_xs<FMT, 1>(a, grid, st);
         case 2: return gemv_detail::launch_xs<FMT, 2>(a, grid, st);
@@ -694,6 +1036,7 @@ cudaError_t launch_gemv_fmt(const GemvArgs& a, int grid, cudaStream_t st) {
         case 7: return gemv_detail::launch_xs<FMT, 7>(a, grid, st);
         case 8: return gemv_detail::launch_xs<FMT, 8>(a, grid, st);
         default: return cudaErrorInvalidValue;
+    }
     }
 }
 

@@ -115,7 +115,8 @@ uq_status uq_gemm_noalloc(const uint16_t* x, const void* wq, const void* scales,
 
     const uq::Layout L(N, K, fmt);
     const long long T = (long long)L.NB * L.KB;
-    long long P = (long long)sms * uq::GEMV_WARPS;
+    const int warps = uq::gemv_warps(fmt);
+    long long P = (long long)sms * warps;
     if (P > T) P = T;
     const int mb_max = M < 8 ? M : 8;
     if ((size_t)L.NB * sizeof(unsigned int) > TICKET_BYTES ||
@@ -148,7 +149,7 @@ uq_status uq_gemm_noalloc(const uint16_t* x, const void* wq, const void* scales,
         a.partials = partials;
         a.tickets = tickets;
         a.fault = reinterpret_cast<unsigned int*>(scratch);
-        e = uq::launch_gemv(fmt, a, (int)((P + uq::GEMV_WARPS - 1) / uq::GEMV_WARPS), st);
+        e = uq::launch_gemv(fmt, a, (int)((P + warps - 1) / warps), st);
         if (e != cudaSuccess) { snprintf(g_err, sizeof g_err, "GEMV launch: %s", cudaGetErrorString(e)); return err(UQ_ERR_CUDA); }
     }
     return UQ_OK;
