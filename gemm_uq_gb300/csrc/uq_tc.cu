@@ -34,10 +34,11 @@ namespace uq {
 
 namespace {
 
-constexpr int TC_THREADS = 384;
+constexpr int TC_THREADS = 512;
 constexpr int TC_ROWS = 128;
 constexpr int TC_STAGE_CODES = TC_ROWS * 128;     // bytes of codes per stage
 constexpr int TMEM_COLS = 512;
+constexpr int TC_BAR_BYTES = 2048;                 // barriers and flags after the stages
 
 __device__ __forceinline__ long long trange_begin(int c, long long U, int P) { return (long long)c * U / P; }
 __device__ __forceinline__ int tworker_of(long long u, long long U, int P) {
@@ -67,13 +68,45 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
                  :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+// 16 lanes x 256 bits per repetition, fragment layout of an m16n8 accumulator: thread t holds
+// (lane t/4, columns 2(t%4), 2(t%4)+1) and (lane t/4 + 8, same columns); .x4 repeats it over 32 columns
+__device__ __forceinline__ void tmem_st_16x256b_x4(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], "
                  "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
                  :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
                     "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
                     "r"(v[14]), "r"(v[15]) : "memory");
 }
+__device__ __forceinline__ void tmem_st_16x256b_x2(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x2.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                    "r"(v[7]) : "memory");
+}
+__device__ __forceinline__ void tc_cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void tc_cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
+// Copy the aligned 32-bit words that cover bytes [lo, lo + len) of `base` into dst[0 .. nw) (word 0
+// holds byte lo & ~3).  Words that would reach past `end` (the array's size) are assembled from byte
+// loads instead, so nothing outside the array is read.
+__device__ __forceinline__ void stage_span(uint32_t* dst, const uint8_t* base, long long lo, int len, long long end) {
+    const long long w0 = lo & ~3ll;
+    for (long long src = w0; src < lo + len; src += 4, ++dst) {
+        if (src + 4 <= end) {
+            tc_cp_async4(dst, base + src);
+        } else {
+            uint32_t v = 0;
+            for (int b = 0; b < 4; ++b)
+                if (src + b < end) v |= (uint32_t)__ldg(base + src + b) << (8 * b);
+            *dst = v;
+        }
+    }
+}
+
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
@@ -118,7 +151,12 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
 template <int FMT> struct TcFmt {
     static constexpr int KC = (FMT == UQ_INT8_SYM) ? 128 : 256;   // codes per row per unit
     static constexpr int ACOLS = KC / 2;                           // tensor-memory columns of A per unit
+    // per-thread metadata rings (3 units deep): epilogue scale words per row, dequant zero words
+    static constexpr int SWORDS = (FMT == UQ_K4) ? 4 : 5;
+    static constexpr int EPI_RING = 3 * 128 * SWORDS * 4;           // bytes
+    static constexpr int DQ_RING = (FMT == UQ_INT4_ASYM) ? 3 * 8 * 16 * 2 * 4 : 0;
 };
+constexpr int TC_DQ_WARPS = 8;                     // dequant warps (one 16-row block each)
 
 }  // namespace
 
@@ -130,13 +168,15 @@ struct TcSmem {
     }
 };
 
-template <int FMT, int MPAD>
+// GB = 16-k blocks per scaling group (2, 4 or 8); used by the INT4_ASYM zero points, ignored otherwise
+template <int FMT, int MPAD, int GB>
 __global__ void __launch_bounds__(TC_THREADS, 1)
 tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
     constexpr int KC = TcFmt<FMT>::KC;
     constexpr int ACOLS = TcFmt<FMT>::ACOLS;
     constexpr int XB = TcSmem::x_bytes(KC, MPAD);
     constexpr int SB = TcSmem::stage_bytes(KC, MPAD);
+    constexpr int SWORDS = TcFmt<FMT>::SWORDS;
     constexpr uint32_t IDESC = idesc_bf16(MPAD);
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -155,6 +195,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
     uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(ebar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_smem + 1);
     unsigned int* ticket_smem = reinterpret_cast<unsigned int*>(tmem_base_smem + 2);
+    uint32_t* epi_ring = reinterpret_cast<uint32_t*>(smem + S * SB + TC_BAR_BYTES);          // [3][128][SWORDS]
+    uint32_t* dq_ring = epi_ring + TcFmt<FMT>::EPI_RING / 4;                                // [3][8 warps][16][2]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
@@ -162,8 +204,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 5); }
-        for (int i = 0; i < 2; ++i) { mbar_init(&afull[i], 4); mbar_init(&aempty[i], 1); }
+        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1 + TC_DQ_WARPS); }
+        for (int i = 0; i < 2; ++i) { mbar_init(&afull[i], TC_DQ_WARPS); mbar_init(&aempty[i], 1); }
         for (int d = 0; d < DS; ++d) { mbar_init(&dfull[d], 1); mbar_init(&dempty[d], 4); }
         mbar_init(ebar, 128);
         *abort_flag = 0;
@@ -253,31 +295,62 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                 tc_commit(&empty[s]);
             }
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ---------------------------------------------------------------- dequant warpgroup
-        const int wq = warp - 4;
-        const int r = wq * 32 + lane;                   // row within the 128-row block
-        const uint32_t lane_addr = tmem + ((uint32_t)(wq * 32) << 16);
+    } else if (warp >= 4 && warp < 4 + TC_DQ_WARPS) {
+        // ---------------------------------------------------------------- dequant warps
+        // warp -> one 16-row block of the unit, in the tensor-memory lane quarter (warp % 4) it may
+        // access; lane (g, c) holds the fragment-order words of rows g and g + 8, which the 16x256b
+        // store shape takes as they are: no shuffles, one 16-byte shared-memory read per 4 words.
+        const int quarter = warp & 3, hf = (warp >= 8) ? 1 : 0;
+        const int rbl = 2 * quarter + hf;               // row block (16 rows) within the 128-row unit
+        const int g = lane >> 2, c4 = lane & 3;
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter + 16 * hf) << 16);
+        uint32_t* zr = dq_ring + (warp - 4) * 32;       // this warp's slot: 16 rows x 2 words
+        // INT4_ASYM: the zero-point words of rows g and g + 8, staged three units ahead by lanes c = 0, 1
+        auto issue_zeros = [&](long long u) {
+            if constexpr (FMT == UQ_INT4_ASYM) {
+                if (u < u1 && c4 < 2) {
+                    const int rb = (int)(u / a.CH), c = (int)(u % a.CH);
+                    const int r = g + 8 * c4;
+                    const long long n = (long long)rb * TC_ROWS + rbl * 16 + r;
+                    const int Gn = a.K / G, ZB = (Gn + 1) >> 1;
+                    if (n < a.N)
+                        stage_span(zr + ((u - u0) % 3) * (TC_DQ_WARPS * 32) + r * 2, a.zc,
+                                   n * ZB + (long long)c * (GPC >> 1), GPC >> 1, (long long)a.N * ZB);
+                }
+                cp_async_commit();
+            }
+        };
+        issue_zeros(u0);
+        issue_zeros(u0 + 1);
         for (long long u = u0; u < u1 && !*abort_flag; ++u) {
             const int i = (int)(u - u0), s = i % S, ab = i & 1;
-            const int rb = (int)(u / a.CH), c = (int)(u % a.CH);
-            const int n = rb * TC_ROWS + r;
-            // subtrahend per group as a bf16 pair (128 + z, or 128 + 8 for INT4_SYM, 128 for K4)
-            uint32_t zsub[8];
+            __syncwarp();
+            issue_zeros(u + 2);
+            // subtrahend per group as a bf16 pair: 128 + z (INT4_ASYM), 128 + 8 (INT4_SYM), 128 (K4)
+            constexpr int ZG = (FMT == UQ_INT4_ASYM) ? 16 / GB : 1;   // groups per unit
+            uint32_t zlo[ZG], zhi[ZG];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) zsub[j] = 0x43004300u;
-            if constexpr (FMT == UQ_INT4_SYM) {
+            for (int j = 0; j < ZG; ++j) zlo[j] = zhi[j] = (FMT == UQ_INT4_SYM) ? 0x43084308u : 0x43004300u;
+            if constexpr (FMT == UQ_INT4_ASYM) {
+                cp_async_wait2();
+                __syncwarp();
+                const int rb = (int)(u / a.CH), c = (int)(u % a.CH);
+                const int Gn = a.K / G, ZB = (Gn + 1) >> 1;
+                const uint32_t* slot = zr + (i % 3) * (TC_DQ_WARPS * 32);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) zsub[j] = 0x43084308u;
-            } else if constexpr (FMT == UQ_INT4_ASYM) {
-                if (n < a.N) {
-                    const int Gn = a.K / G;
-                    const uint8_t* zr = a.zc + (long long)n * ((Gn + 1) >> 1);
-                    for (int j = 0; j < GPC; ++j) {
-                        const int gi = (c * KC) / G + j;
-                        const uint8_t b = __ldg(zr + (gi >> 1));
-                        const uint32_t z = (gi & 1) ? (b >> 4) : (b & 15u);
-                        zsub[j] = 0x43004300u | z | (z << 16);
+                for (int h = 0; h < 2; ++h) {
+                    const long long n = (long long)rb * TC_ROWS + rbl * 16 + g + 8 * h;
+                    uint32_t zb = 0;
+                    if (n < a.N) {
+                        const int o = (int)((n * ZB + (long long)c * (GPC >> 1)) & 3);
+                        const uint64_t w = (uint64_t)slot[(g + 8 * h) * 2] | ((uint64_t)slot[(g + 8 * h) * 2 + 1] << 32);
+                        zb = (uint32_t)(w >> (8 * o));
+                    }
+#pragma unroll
+                    for (int j = 0; j < ZG; ++j) {
+                        const uint32_t z = (zb >> (4 * j)) & 15u;
+                        const uint32_t zz = 0x43004300u | z | (z << 16);
+                        if (h == 0) zlo[j] = zz; else zhi[j] = zz;
                     }
                 }
             }
@@ -286,56 +359,46 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) { *abort_flag = 1; break; }
             tc_fence_after();
-            // row r = 16 rbl + 8 h + g sits in lane chunks 4g .. 4g + 3 of its row block (fragment
-            // order); read them rotated by g / 2 so a quarter warp touches 8 distinct 16-byte slots
-            const int rbl = r >> 4, hh = (r >> 3) & 1, gg = r & 7;
-            const uint8_t* rbase = smem + s * SB + rbl * 2048 + gg * 64;
+            const uint8_t* rbase = smem + s * SB + rbl * 2048 + lane * 16;
             const uint32_t acol = lane_addr + A_COL0 + ab * ACOLS;
             if constexpr (FMT == UQ_INT8_SYM) {
-                // chunk q = 32 k: words h (block 0) and 2 + h (block 1), 4 bytes each -> 16 columns
+                // chunk q = 32 k = blocks 2q, 2q + 1; word 2b + h = row g + 8h, k 4c .. 4c + 3 of block b
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    uint32_t v[16];
+                    const uint4 w4 = *reinterpret_cast<const uint4*>(rbase + q * 512);
+                    const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+                    uint32_t v[8];
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const int cc = (jj + (gg >> 1)) & 3;
-                        const uint4 w4 = *reinterpret_cast<const uint4*>(rbase + q * 512 + cc * 16);
-                        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+                    for (int b = 0; b < 2; ++b)
 #pragma unroll
-                        for (int b2 = 0; b2 < 2; ++b2) {
-                            const uint32_t wd = wv[2 * b2 + hh];
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t wd = wv[2 * b + h];
                             const float f0 = byte_magic_f32(wd, 0) - 8388736.0f;
                             const float f1 = byte_magic_f32(wd, 1) - 8388736.0f;
                             const float f2 = byte_magic_f32(wd, 2) - 8388736.0f;
                             const float f3 = byte_magic_f32(wd, 3) - 8388736.0f;
-                            v[b2 * 8 + 2 * cc] = f32x2_to_bf16x2(f0, f1);
-                            v[b2 * 8 + 2 * cc + 1] = f32x2_to_bf16x2(f2, f3);
+                            v[4 * b + 2 * h] = f32x2_to_bf16x2(f0, f1);
+                            v[4 * b + 2 * h + 1] = f32x2_to_bf16x2(f2, f3);
                         }
-                    }
-                    tmem_st16(acol + q * 16, v);
+                    tmem_st_16x256b_x2(acol + q * 16, v);
                 }
             } else {
-                // chunk q = 64 k: words i = 16-k blocks; pairs hh (k 4c, 4c+1) and hh + 2 (k 4c+2, 4c+3)
+                // chunk q = 64 k = blocks 4q .. 4q + 3, one word each; pairs 0/2 are row g (k 4c, 4c+1 /
+                // 4c+2, 4c+3), pairs 1/3 row g + 8
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    uint32_t v[32];
+                    const uint4 w4 = *reinterpret_cast<const uint4*>(rbase + q * 512);
+                    const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+                    uint32_t v[16];
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const int cc = (jj + (gg >> 1)) & 3;
-                        const uint4 w4 = *reinterpret_cast<const uint4*>(rbase + q * 512 + cc * 16);
-                        const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const uint32_t zs = zsub[(q * 64 + i * 16) / G];
-                            v[i * 8 + 2 * cc] = bf16x2_sub(nib_pair_bf16(wv[i], hh), zs);
-                            v[i * 8 + 2 * cc + 1] = bf16x2_sub(nib_pair_bf16(wv[i], hh + 2), zs);
-                        }
+                    for (int b = 0; b < 4; ++b) {
+                        const int j = (FMT == UQ_INT4_ASYM) ? (4 * q + b) / GB : 0;
+                        v[4 * b + 0] = bf16x2_sub(nib_pair_bf16(wv[b], 0), zlo[j]);
+                        v[4 * b + 1] = bf16x2_sub(nib_pair_bf16(wv[b], 2), zlo[j]);
+                        v[4 * b + 2] = bf16x2_sub(nib_pair_bf16(wv[b], 1), zhi[j]);
+                        v[4 * b + 3] = bf16x2_sub(nib_pair_bf16(wv[b], 3), zhi[j]);
                     }
-                    uint32_t lo[16], hi[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) { lo[e] = v[e]; hi[e] = v[16 + e]; }
-                    tmem_st16(acol + q * 32, lo);
-                    tmem_st16(acol + q * 32 + 16, hi);
+                    tmem_st_16x256b_x4(acol + q * 32, v);
                 }
             }
             tmem_st_wait();
@@ -343,12 +406,33 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             __syncwarp();
             if (lane == 0) { mbar_arrive(&afull[ab]); mbar_arrive(&empty[s]); }
         }
-    } else if (warp >= 8) {
+        if constexpr (FMT == UQ_INT4_ASYM) asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (warp >= 4 + TC_DQ_WARPS) {
         // ---------------------------------------------------------------- epilogue warpgroup
         asm volatile("griddepcontrol.wait;" ::: "memory");   // sx, workspace and y follow earlier work
-        const int we = warp - 8;
+        const int we = warp & 3;
         const int r = we * 32 + lane;
         const uint32_t lane_addr = tmem + ((uint32_t)(we * 32) << 16);
+        uint32_t* er = epi_ring + r * SWORDS;            // this thread's slot (ring stride 128 * SWORDS)
+        // this row's scale words (K4: its super-block record) staged three units ahead
+        auto issue_scales = [&](long long u) {
+            if (u < u1) {
+                const int rb = (int)(u / a.CH), c = (int)(u % a.CH);
+                const long long n = (long long)rb * TC_ROWS + r;
+                uint32_t* dst = er + ((u - u0) % 3) * (128 * SWORDS);
+                if (n < a.N) {
+                    if constexpr (FMT == UQ_K4) {
+                        tc_cp_async16(dst, a.scales + (n * (a.K >> 8) + c) * 16);
+                    } else {
+                        const long long Gn = a.K / G;
+                        stage_span(dst, a.scales, (n * Gn + (long long)c * GPC) * 2, GPC * 2, (long long)a.N * Gn * 2);
+                    }
+                }
+            }
+            cp_async_commit();
+        };
+        issue_scales(u0);
+        issue_scales(u0 + 1);
         float acc[MPAD];
 #pragma unroll
         for (int m = 0; m < MPAD; ++m) acc[m] = 0.f;
@@ -366,23 +450,22 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             const int rb = (int)(u / a.CH), c = (int)(u % a.CH);
             const int n = rb * TC_ROWS + r;
             const bool live = n < a.N;
+            issue_scales(u + 2);
+            cp_async_wait2();
+            const uint32_t* sw = er + ((u - u0) % 3) * (128 * SWORDS);
+            const int so = live ? (int)(((long long)n * (a.K / G) + (long long)c * GPC) & 1) : 0;   // halves
             bool ok = true;
             for (int j = 0; j < GPC; ++j, ++dctr) {
                 float s1 = 0.f, s2 = 0.f;
                 if (live) {
                     if constexpr (FMT == UQ_K4) {
-                        const int kk = c * KC + j * 32;
-                        const uint4 rec = *reinterpret_cast<const uint4*>(
-                            a.scales + ((long long)n * (a.K >> 8) + (kk >> 8)) * 16);
-                        const int sj = (kk & 255) >> 5;
+                        const uint4 rec = *reinterpret_cast<const uint4*>(sw);
                         const uint64_t sc48 = (uint64_t)rec.y | ((uint64_t)(rec.z & 0xFFFFu) << 32);
                         const uint64_t m48 = (uint64_t)(rec.z >> 16) | ((uint64_t)rec.w << 16);
-                        s1 = half_bits_f32((uint16_t)(rec.x & 0xFFFF)) * (float)((sc48 >> (6 * sj)) & 63);
-                        s2 = half_bits_f32((uint16_t)(rec.x >> 16)) * (float)((m48 >> (6 * sj)) & 63);
+                        s1 = half_bits_f32((uint16_t)(rec.x & 0xFFFF)) * (float)((sc48 >> (6 * j)) & 63);
+                        s2 = half_bits_f32((uint16_t)(rec.x >> 16)) * (float)((m48 >> (6 * j)) & 63);
                     } else {
-                        const int gi = (c * KC) / G + j;
-                        s1 = half_bits_f32(__ldg(reinterpret_cast<const uint16_t*>(a.scales) +
-                                                 (long long)n * (a.K / G) + gi));
+                        s1 = half_bits_f32(reinterpret_cast<const uint16_t*>(sw)[so + j]);
                     }
                 }
                 const int d = (int)(dctr % DS);
@@ -431,21 +514,21 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     const int cf = tworker_of(uf, a.U, a.P), cl = tworker_of(uf + a.CH - 1, a.U, a.P);
                     if (old == (unsigned int)(cl - cf)) {
                         __threadfence();
-                        float sum[MPAD];
+                        // the partials of all contributors, summed in CTA order into acc
 #pragma unroll
-                        for (int m = 0; m < MPAD; ++m) sum[m] = 0.f;
+                        for (int m = 0; m < MPAD; ++m) acc[m] = 0.f;
                         for (int c2 = cf; c2 <= cl; ++c2) {
                             const int rb2 = (int)(trange_begin(c2, a.U, a.P) / a.CH);
                             const int slot2 = 2 * c2 + (rb == rb2 ? 0 : 1);
                             const float* p2 = a.partials + ((long long)slot2 * TC_ROWS + r) * MPAD;
 #pragma unroll
-                            for (int m = 0; m < MPAD; ++m) sum[m] += __ldcg(p2 + m);
+                            for (int m = 0; m < MPAD; ++m) acc[m] += __ldcg(p2 + m);
                         }
                         if (live)
 #pragma unroll
                             for (int m = 0; m < MPAD; ++m)
                                 if (m < a.M)
-                                    a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum[m]));
+                                    a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
                         if (r == 0) a.tickets[rb] = 0u;
                     }
                     if (!epi_sync()) { *abort_flag = 1; break; }
@@ -454,6 +537,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                 for (int m = 0; m < MPAD; ++m) acc[m] = 0.f;
             }
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");
     }
 
     tc_fence_before();
@@ -504,7 +588,7 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-template <int FMT, int MPAD>
+template <int FMT, int MPAD, int GB>
 cudaError_t launch_tc_t(const CUtensorMap& mx, const TcArgs& a, size_t smem, int grid, cudaStream_t st) {
     static bool configured[64] = {};
     int dev = 0;
@@ -512,7 +596,7 @@ cudaError_t launch_tc_t(const CUtensorMap& mx, const TcArgs& a, size_t smem, int
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(tc_kernel<FMT, MPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        e = cudaFuncSetAttribute(tc_kernel<FMT, MPAD, GB>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
@@ -527,23 +611,37 @@ cudaError_t launch_tc_t(const CUtensorMap& mx, const TcArgs& a, size_t smem, int
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, tc_kernel<FMT, MPAD>, mx, a);
+        e = cudaLaunchKernelEx(&cfg, tc_kernel<FMT, MPAD, GB>, mx, a);
         if (e != cudaSuccess) return e;
     } else {
-        tc_kernel<FMT, MPAD><<<grid, TC_THREADS, smem, st>>>(mx, a);
+        tc_kernel<FMT, MPAD, GB><<<grid, TC_THREADS, smem, st>>>(mx, a);
     }
     return cudaGetLastError();
 }
 
+template <int FMT, int GB>
+cudaError_t launch_tc_mg(int mpad, const CUtensorMap& mx, const TcArgs& a, size_t smem, int grid,
+                         cudaStream_t st) {
+    switch (mpad) {
+        case 16: return launch_tc_t<FMT, 16, GB>(mx, a, smem, grid, st);
+        case 32: return launch_tc_t<FMT, 32, GB>(mx, a, smem, grid, st);
+        case 48: return launch_tc_t<FMT, 48, GB>(mx, a, smem, grid, st);
+        case 64: return launch_tc_t<FMT, 64, GB>(mx, a, smem, grid, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
 template <int FMT>
 cudaError_t launch_tc_m(int mpad, const CUtensorMap& mx, const TcArgs& a, size_t smem, int grid,
                         cudaStream_t st) {
-    switch (mpad) {
-        case 16: return launch_tc_t<FMT, 16>(mx, a, smem, grid, st);
-        case 32: return launch_tc_t<FMT, 32>(mx, a, smem, grid, st);
-        case 48: return launch_tc_t<FMT, 48>(mx, a, smem, grid, st);
-        case 64: return launch_tc_t<FMT, 64>(mx, a, smem, grid, st);
-        default: return cudaErrorInvalidValue;
+    if constexpr (FMT == UQ_INT4_ASYM) {
+        switch (a.group) {
+            case 32: return launch_tc_mg<FMT, 2>(mpad, mx, a, smem, grid, st);
+            case 64: return launch_tc_mg<FMT, 4>(mpad, mx, a, smem, grid, st);
+            case 128: return launch_tc_mg<FMT, 8>(mpad, mx, a, smem, grid, st);
+            default: return cudaErrorInvalidValue;
+        }
+    } else {
+        return launch_tc_mg<FMT, 8>(mpad, mx, a, smem, grid, st);
     }
 }
 }  // namespace
@@ -557,14 +655,23 @@ bool tc_supported(int fmt, int N, int K) {
 int tc_plan(int fmt, int mpad, int* stages, int* dslots, size_t* smem) {
     const int kc = (fmt == UQ_INT8_SYM) ? 128 : 256;
     const int sb = TcSmem::stage_bytes(kc, mpad);
-    int s = (200 * 1024) / sb;
+    int rings = 0;
+    switch (fmt) {
+        case UQ_INT4_SYM: rings = TcFmt<UQ_INT4_SYM>::EPI_RING + TcFmt<UQ_INT4_SYM>::DQ_RING; break;
+        case UQ_INT4_ASYM: rings = TcFmt<UQ_INT4_ASYM>::EPI_RING + TcFmt<UQ_INT4_ASYM>::DQ_RING; break;
+        case UQ_INT8_SYM: rings = TcFmt<UQ_INT8_SYM>::EPI_RING + TcFmt<UQ_INT8_SYM>::DQ_RING; break;
+        case UQ_K4: rings = TcFmt<UQ_K4>::EPI_RING + TcFmt<UQ_K4>::DQ_RING; break;
+        default: return -1;
+    }
+    const int budget = 227 * 1024 - 1024 - TC_BAR_BYTES - rings;
+    int s = budget / sb;
     if (s > 6) s = 6;
     if (s < 2) return -1;
     int ds = (TMEM_COLS - kc) / mpad;       // A takes 2 * kc/2 columns
     if (ds > 8) ds = 8;
     *stages = s;
     *dslots = ds;
-    *smem = 1024 + (size_t)s * sb + (size_t)(2 * s + 4 + 2 * ds + 1) * 8 + 64;
+    *smem = 1024 + (size_t)s * sb + TC_BAR_BYTES + rings;
     return 0;
 }
 
