@@ -179,6 +179,7 @@ uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const 
     a.partials = ws->partials;
     a.tickets = ws->tickets;
     a.fault = ds.words;
+    a.overlap = 0;
     const int grid = (int)((P + warps - 1) / warps);
     cudaError_t e = uq::launch_gemv(fmt, a, grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "GEMV launch");

@@ -60,7 +60,7 @@ __host__ __device__ inline size_t gemv_x_stride(int Kp) { return (size_t)Kp * 2 
 
 // shared-memory plan; identical on host and device
 struct GemvSmem {
-    size_t bars, lut, sx, x, total;
+    size_t bars, lut, sx, ps, x, total;
 };
 template <int FMT>
 __host__ __device__ inline GemvSmem gemv_smem_plan_t(int K, int group, int M, bool x_in_smem) {
@@ -72,6 +72,7 @@ __host__ __device__ inline GemvSmem gemv_smem_plan_t(int K, int group, int M, bo
     p.lut = p.bars + (size_t)(GEMV_WARPS * F::STAGES + 1) * 8;     // + the x mbarrier
     p.sx = p.lut + 64;
     p.x = p.sx + (F::NEEDS_SX ? (size_t)((Kp + gs - 1) / gs) * 8 * 4 : 0);   // sums padded to 8 columns
+    p.ps = p.x;
     p.x = (p.x + 127) / 128 * 128;
     p.total = p.x + (x_in_smem ? (size_t)M * gemv_x_stride(Kp) : 0);
     return p;
@@ -640,10 +641,20 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
 // 4-bit and 2-bit formats: the GEMV on mma.sync.  GB = 16-k blocks per scaling group (2, 4 or 8;
 // K4 uses its 32-weight sub-blocks, GB = 2).  M (1..8) is a runtime value: the instruction always
 // computes 8 columns, so the work per weight does not depend on it.
+//
+// Per 16 x 16 block of weights a lane issues: its share of one 16-byte code load (a quarter or an
+// eighth), four lop3 (three after a shift) to form the A fragment, half a 16-byte load of x (the x
+// rows are stored pair-interleaved so one load gives the B fragments of two blocks) and the mma.
+// Per group: two fp32 FMAs per accumulator with the group's scale and zero term.  A tile whose
+// groups all lie inside K (every tile but a ragged last one) runs a fully unrolled group loop.
 template <int FMT> struct MmaCfg {
     static constexpr int WARPS = (FMT == UQ_INT2_ASYM) ? 6 : 8;    // workers per CTA
     static constexpr int STAGES = 2;                               // tiles in flight per worker
 };
+
+// bytes per row of the pair-interleaved x in shared memory: 64 bytes of padding put rows g and
+// g + 1 of a quarter-warp's 16-byte loads into different banks
+__host__ __device__ inline size_t gemv_mma_x_stride(int Kp) { return (size_t)Kp * 2 + 64; }
 
 __host__ __device__ inline GemvSmem gemv_mma_smem_plan(int fmt, int K, int group, int M, bool x_in_smem) {
     int stage = 0, warps = 0, kc = fmt_kc(fmt);
@@ -660,10 +671,36 @@ __host__ __device__ inline GemvSmem gemv_mma_smem_plan(int fmt, int K, int group
     p.bars = (size_t)warps * stages * stage;
     p.lut = p.bars + (size_t)(warps * stages + 1) * 8;
     p.sx = p.lut + 64;
-    p.x = p.sx + (size_t)((Kp + gs - 1) / gs) * 8 * 4;
+    p.ps = p.sx + (size_t)((Kp + gs - 1) / gs) * 8 * 4;             // per-group sums, 8 columns
+    p.x = p.ps + (x_in_smem ? (size_t)(Kp / 32) * 8 * 4 : 0);       // per-32-k partial sums
     p.x = (p.x + 127) / 128 * 128;
-    p.total = p.x + (x_in_smem ? (size_t)M * gemv_x_stride(Kp) : 0);
+    p.total = p.x + (x_in_smem ? (size_t)M * gemv_mma_x_stride(Kp) : 0);
     return p;
+}
+
+// bf16x2 (128 + code) of nibble pair P (bits 4P.. of each half) / crumb pair P (bits 2P..): one
+// lop3 ((w & mask) | magic), after a shift unless P == 0
+template <int P>
+__device__ __forceinline__ uint32_t nib_pair_lop3(uint32_t w) {
+    uint32_t r;
+    if constexpr (P == 0) {
+        asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(r) : "r"(w));
+    } else {
+        asm("{\n\t.reg .b32 t;\n\tshr.b32 t, %1, %2;\n\tlop3.b32 %0, t, 0x000F000F, 0x43004300, 0xEA;\n\t}"
+            : "=r"(r) : "r"(w), "n"(4 * P));
+    }
+    return r;
+}
+template <int P>
+__device__ __forceinline__ uint32_t crumb_pair_lop3(uint32_t w) {
+    uint32_t r;
+    if constexpr (P == 0) {
+        asm("lop3.b32 %0, %1, 0x00030003, 0x43004300, 0xEA;" : "=r"(r) : "r"(w));
+    } else {
+        asm("{\n\t.reg .b32 t;\n\tshr.b32 t, %1, %2;\n\tlop3.b32 %0, t, 0x00030003, 0x43004300, 0xEA;\n\t}"
+            : "=r"(r) : "r"(w), "n"(2 * P));
+    }
+    return r;
 }
 
 template <int FMT, int GB, bool XS>
@@ -673,11 +710,13 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
     constexpr int GS = GB * 16;                                     // k per scaling group
     constexpr int GPT = KT / GS;                                    // groups per full tile row
     constexpr int WPG = (FMT == UQ_INT2_ASYM) ? GB / 2 : GB;        // code words per lane per group
+    constexpr int BPCH = F::BPC;                                    // 16-k blocks per 512-byte chunk
     extern __shared__ __align__(128) uint8_t smem[];
     const int M = a.M;
     const GemvSmem plan = gemv_mma_smem_plan(FMT, a.K, a.group, M, XS);
     uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + plan.bars);
     float* sxg = reinterpret_cast<float*>(smem + plan.sx);
+    float* psx = reinterpret_cast<float*>(smem + plan.ps);
     uint8_t* xs = smem + plan.x;
     uint64_t* xbar = bars_all + W * S;
 
@@ -697,47 +736,82 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
     mc.S4 = a.K / 256;
     mc.aligned = (a.K % (8 * a.group)) == 0 && (mc.GT % 8) == 0;
     const int G_all = a.K / GS;                                     // real scaling groups per row
-    const size_t xstride = gemv_x_stride(L.Kp);
+    const size_t xstride = gemv_mma_x_stride(L.Kp);
 
+    // ---- prologue.  x (a few KB, written by the previous kernel) is requested ahead of the weights
+    // so it is not queued behind them; with launch overlap the first weight stage is streamed
+    // before the wait for the previous kernel instead, as the weights do not depend on it.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (has_work) {
-        if (lane == 0) {
+    if (has_work && lane == 0) {
 #pragma unroll
-            for (int s = 0; s < S; ++s) mbar_init(&bars[s], 33);
-            fence_barrier_init();
-        }
-        __syncwarp();
-        int inb = (int)(t0 / L.KB), ikb = (int)(t0 % L.KB);
-        for (int s = 0; s < S && t0 + s < t1; ++s) {
-            issue_tile<FMT>(a, L, mc, inb, ikb, ring + s * F::STAGE_BYTES, &bars[s], lane);
-            if (++ikb == L.KB) { ikb = 0; ++inb; }
-        }
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 33);
+        fence_barrier_init();
     }
+    if (XS && threadIdx.x == 0) {
+        mbar_init(xbar, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    int inb = (int)(t0 / L.KB), ikb = (int)(t0 % L.KB);
+    int issued = 0;
+    auto issue_next = [&]() {
+        issue_tile<FMT>(a, L, mc, inb, ikb, ring + issued * F::STAGE_BYTES, &bars[issued], lane);
+        if (++ikb == L.KB) { ikb = 0; ++inb; }
+        ++issued;
+    };
+    if (a.overlap && has_work && t0 < t1) issue_next();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if constexpr (XS) {
         if (threadIdx.x == 0) {
-            mbar_init(xbar, 1);
-            fence_barrier_init();
             mbar_arrive_expect_tx(xbar, (uint32_t)(M * a.K * 2));
             for (int m = 0; m < M; ++m) bulk_g2s(xs + m * xstride, a.x + (long long)m * a.ldx, (uint32_t)(a.K * 2), xbar);
         }
+    }
+    if (has_work)
+        while (issued < S && t0 + issued < t1) issue_next();
+    if constexpr (XS) {
         const int padw = (L.Kp - a.K) / 2;
         for (int e = threadIdx.x; e < M * padw; e += blockDim.x)
             reinterpret_cast<uint32_t*>(xs + (e / padw) * xstride + a.K * 2)[e % padw] = 0u;
         __syncthreads();
         mbar_wait_bounded(xbar, 0, a.fault, FAULT_GEMV_WAIT);
-    }
-    {
-        // sxg[gi * 8 + m] = sum of x[m][k] over group gi, in k order; 0 for m >= M
+        // Interleave each 32-k pair of blocks: natural 8-byte unit u = 4 jj + c (k = 16 jj + 4c .. +3)
+        // moves to position 2c + jj, so lane c finds its B fragments of both blocks in 16 bytes.
+        // The same pass forms the sum of x over each 32 k (in k order).
+        const int PB = L.Kp / 32;
+        for (int e = threadIdx.x; e < PB * M; e += blockDim.x) {
+            const int pb = e / M, m = e % M;
+            uint4* p = reinterpret_cast<uint4*>(xs + m * xstride + pb * 64);
+            const uint4 q0 = p[0], q1 = p[1], q2 = p[2], q3 = p[3];
+            const uint32_t u[16] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w,
+                                    q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
+            float s0 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) s0 += bf16lo_f32(u[j]) + bf16hi_f32(u[j]);
+            p[0] = make_uint4(u[0], u[1], u[8], u[9]);
+            p[1] = make_uint4(u[2], u[3], u[10], u[11]);
+            p[2] = make_uint4(u[4], u[5], u[12], u[13]);
+            p[3] = make_uint4(u[6], u[7], u[14], u[15]);
+            psx[pb * 8 + m] = s0;
+        }
+        __syncthreads();
+        // sxg[gi * 8 + m] = sum of x[m][k] over group gi (its 32-k sums in k order); 0 for m >= M
+        for (int e = threadIdx.x; e < G_all * 8; e += blockDim.x) {
+            const int gi = e >> 3, m = e & 7;
+            float s0 = 0.f;
+            if (m < M)
+#pragma unroll
+                for (int t = 0; t < GS / 32; ++t) s0 += psx[(gi * (GS / 32) + t) * 8 + m];
+            sxg[e] = s0;
+        }
+    } else {
         for (int e = threadIdx.x; e < G_all * 8; e += blockDim.x) {
             const int gi = e >> 3, m = e & 7;
             float s0 = 0.f;
             if (m < M) {
 #pragma unroll
                 for (int k = 0; k < GS; k += 8) {
-                    uint4 q;
-                    if constexpr (XS) q = *reinterpret_cast<const uint4*>(xs + m * xstride + (gi * GS + k) * 2);
-                    else q = ldg_nc_v4(a.x + (long long)m * a.ldx + gi * GS + k);
+                    const uint4 q = ldg_nc_v4(a.x + (long long)m * a.ldx + gi * GS + k);
                     const uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) s0 += bf16lo_f32(u[j]) + bf16hi_f32(u[j]);
@@ -752,12 +826,9 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
     const int first_nb = (int)(t0 / L.KB);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};        // rows g + 8j, columns 2c + e
     const int mrow = g < M ? g : M - 1;          // B rows beyond M repeat a real row; their D columns are unused
-    const uint8_t* xrow = xs + mrow * xstride + 8 * c;
+    const uint8_t* xrow = xs + mrow * xstride + 16 * c;
     const uint16_t* xgrow = a.x + (long long)mrow * a.ldx + 4 * c;
     int nb = (int)(t0 / L.KB), kb = (int)(t0 % L.KB);
-    int pnb = nb, pkb = kb;
-    for (int s = 0; s < S; ++s)
-        if (++pkb == L.KB) { pkb = 0; ++pnb; }
 
     for (long long t = t0; t < t1; ++t) {
         const int it = (int)(t - t0);
@@ -781,11 +852,12 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
         }
         const uint8_t* xt = xrow + (size_t)kb * KT * 2;             // x of the tile's first k
         const uint16_t* xgt = xgrow + (long long)kb * KT;
-        for (int gg = 0; gg < ng; ++gg) {
+        const float* sxt = sxg + gi0 * 8 + 2 * c;
+
+        auto group_step = [&](const int gg) {
             // this lane's code words for the group's GB blocks
             uint32_t wv[WPG];
             {
-                constexpr int BPCH = F::BPC;                        // blocks per 512-byte chunk
                 const int blk = gg * GB;                            // first block of the group in the tile
                 const uint8_t* cp = st + (blk / BPCH) * CHUNK + lane * 16 + ((blk % BPCH) * WPG / GB) * 4;
                 if constexpr (WPG == 4) {
@@ -803,39 +875,45 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
                     wv[0] = *reinterpret_cast<const uint32_t*>(cp);
                 }
             }
-            // B fragments of the group's blocks (x at k = 16 blk + 4c .. +3 of row mrow)
-            uint2 bfr[GB];
+            // B fragments: x at k = 16 blk + 4c .. +3 of row mrow, two blocks per 16-byte load
+            uint32_t bx[GB], by[GB];
             if constexpr (XS) {
 #pragma unroll
-                for (int j = 0; j < GB; ++j) bfr[j] = *reinterpret_cast<const uint2*>(xt + (gg * GB + j) * 32);
+                for (int jp = 0; jp < GB / 2; ++jp) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(xt + (gg * (GB / 2) + jp) * 64);
+                    bx[2 * jp] = v.x; by[2 * jp] = v.y; bx[2 * jp + 1] = v.z; by[2 * jp + 1] = v.w;
+                }
             } else {
 #pragma unroll
                 for (int j = 0; j < GB; ++j) {
                     const int kk = (gg * GB + j) * 16;
-                    bfr[j] = (kb * KT + kk + 4 * c < a.K) ? ldg_nc_v2(xgt + kk) : make_uint2(0, 0);
+                    const uint2 v = (kb * KT + kk + 4 * c < a.K) ? ldg_nc_v2(xgt + kk) : make_uint2(0, 0);
+                    bx[j] = v.x; by[j] = v.y;
                 }
             }
             float dd[2][4];
 #pragma unroll
             for (int j = 0; j < GB; ++j) {
-                const uint2 b = bfr[j];
                 uint32_t a0, a1, a2, a3;
                 if constexpr (FMT == UQ_INT2_ASYM) {
                     const uint32_t wd = wv[j >> 1];
-                    const int pb = (j & 1) * 4;
-                    a0 = crumb_pair_bf16(wd, pb + 0); a1 = crumb_pair_bf16(wd, pb + 1);
-                    a2 = crumb_pair_bf16(wd, pb + 2); a3 = crumb_pair_bf16(wd, pb + 3);
+                    if (j & 1) {
+                        a0 = crumb_pair_lop3<4>(wd); a1 = crumb_pair_lop3<5>(wd);
+                        a2 = crumb_pair_lop3<6>(wd); a3 = crumb_pair_lop3<7>(wd);
+                    } else {
+                        a0 = crumb_pair_lop3<0>(wd); a1 = crumb_pair_lop3<1>(wd);
+                        a2 = crumb_pair_lop3<2>(wd); a3 = crumb_pair_lop3<3>(wd);
+                    }
                 } else {
                     const uint32_t wd = wv[j];
-                    a0 = nib_pair_bf16(wd, 0); a1 = nib_pair_bf16(wd, 1);
-                    a2 = nib_pair_bf16(wd, 2); a3 = nib_pair_bf16(wd, 3);
+                    a0 = nib_pair_lop3<0>(wd); a1 = nib_pair_lop3<1>(wd);
+                    a2 = nib_pair_lop3<2>(wd); a3 = nib_pair_lop3<3>(wd);
                 }
-                if (j < 2) mma_bf16_zero(dd[j & 1], a0, a1, a2, a3, b.x, b.y);
-                else mma_bf16(dd[j & 1], a0, a1, a2, a3, b.x, b.y);
+                if (j < 2) mma_bf16_zero(dd[j & 1], a0, a1, a2, a3, bx[j], by[j]);
+                else mma_bf16(dd[j & 1], a0, a1, a2, a3, bx[j], by[j]);
             }
             // fold the group into the row sums
-            const int gi = gi0 + gg;
-            const float2 sxv = *reinterpret_cast<const float2*>(sxg + gi * 8 + 2 * c);
+            const float2 sxv = *reinterpret_cast<const float2*>(sxt + gg * 8);
             float d[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) d[e] = dd[0][e] + dd[1][e];
@@ -855,11 +933,18 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
                     acc[2 * j + 1] = fmaf(sc, d[2 * j + 1], fmaf(-szc, sxv.y, acc[2 * j + 1]));
                 }
             }
+        };
+        if (ng == GPT) {
+#pragma unroll
+            for (int gg = 0; gg < GPT; ++gg) group_step(gg);
+        } else {
+#pragma unroll 1
+            for (int gg = 0; gg < ng; ++gg) group_step(gg);
         }
         __syncwarp();
         if (t + S < t1) {
-            issue_tile<FMT>(a, L, mc, pnb, pkb, st, &bars[s], lane);
-            if (++pkb == L.KB) { pkb = 0; ++pnb; }
+            issue_tile<FMT>(a, L, mc, inb, ikb, st, &bars[s], lane);
+            if (++ikb == L.KB) { ikb = 0; ++inb; }
         }
 
         if (kb == L.KB - 1 || t == t1 - 1) {
@@ -988,7 +1073,9 @@ cudaError_t launch_mma(const GemvArgs& a, int grid, cudaStream_t st) {
         configured[dev] = true;
     }
     const int threads = MmaCfg<FMT>::WARPS * 32;
-    if (launch_overlap()) {
+    GemvArgs a2 = a;
+    a2.overlap = launch_overlap() ? 1 : 0;
+    if (a2.overlap) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid);
         cfg.blockDim = dim3(threads);
@@ -999,10 +1086,10 @@ cudaError_t launch_mma(const GemvArgs& a, int grid, cudaStream_t st) {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, gemv_mma_kernel<FMT, GB, XS>, a);
+        e = cudaLaunchKernelEx(&cfg, gemv_mma_kernel<FMT, GB, XS>, a2);
         if (e != cudaSuccess) return e;
     } else {
-        gemv_mma_kernel<FMT, GB, XS><<<grid, threads, smem, st>>>(a);
+        gemv_mma_kernel<FMT, GB, XS><<<grid, threads, smem, st>>>(a2);
     }
     return cudaGetLastError();
 }

@@ -38,6 +38,7 @@ struct GemvArgs {
     float* partials;          // [2P][16][M] fp32 split-K partial sums
     unsigned int* tickets;    // [NB], zero between calls
     unsigned int* fault;      // device fault word
+    int overlap;              // launched with programmatic stream serialization (set by the launcher)
 };
 constexpr int GEMV_WARPS = 4;     // worker warps per CTA
 size_t gemv_smem_bytes(int fmt, int K, int group, int M);

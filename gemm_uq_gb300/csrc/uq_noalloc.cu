@@ -149,6 +149,7 @@ uq_status uq_gemm_noalloc(const uint16_t* x, const void* wq, const void* scales,
         a.partials = partials;
         a.tickets = tickets;
         a.fault = reinterpret_cast<unsigned int*>(scratch);
+        a.overlap = 0;
         e = uq::launch_gemv(fmt, a, (int)((P + warps - 1) / warps), st);
         if (e != cudaSuccess) { snprintf(g_err, sizeof g_err, "GEMV launch: %s", cudaGetErrorString(e)); return err(UQ_ERR_CUDA); }
     }
