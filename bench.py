@@ -107,6 +107,18 @@ def read_traffic(workload, avg_alg_bytes):
         return None
 
 
+def dominant_kernel(fmt, group, M, recs):
+    """Name of the kernel template the library dispatches for this workload's linears."""
+    kt = {"INT4_SYM": 1024, "INT4_ASYM": 1024, "INT8_SYM": 512, "INT2_ASYM": 2048, "NF4": 1024, "K4": 1024}[fmt]
+    if M >= 16 and fmt in ("INT4_SYM", "INT4_ASYM", "INT8_SYM", "K4") and all(r["K"] % kt == 0 for r in recs):
+        mpad = (min(M, 64) + 15) // 16 * 16
+        return f"tc_kernel<{fmt},{mpad}>"
+    if fmt in ("INT4_SYM", "INT4_ASYM", "INT2_ASYM", "K4"):
+        gs = 32 if fmt == "K4" else group
+        return f"gemv_mma_kernel<{fmt},GB={gs // 16}>"
+    return f"gemv_kernel<{fmt},{min(M, 8)}>"
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -370,7 +382,7 @@ def run_uq(args, rank, world, dist):
                 "h2d_bytes_per_step": xbuf.numel() * 2, "d2h_bytes_per_step": ybuf.numel() * 2},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} HBM copy bandwidth",
-                     "traffic": traffic, "kernel": f"gemv_kernel<{fmt},{min(M, 8)}>",
+                     "traffic": traffic, "kernel": dominant_kernel(fmt, group, M, recs),
                      "kernel_ms_per_step": round(kern_ms, 4), "timing": kern_src},
         "clocks": clocks,
     }

@@ -112,6 +112,30 @@ __device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w, int p) {
 __device__ __forceinline__ uint32_t crumb_pair_bf16(uint32_t w, int p) {
     return ((w >> (2 * p)) & 0x00030003u) | 0x43004300u;
 }
+// bf16x2 (128 + code) of nibble pair P (bits 4P.. of each half) / crumb pair P (bits 2P..): one
+// lop3 ((w & mask) | magic), after a shift unless P == 0
+template <int P>
+__device__ __forceinline__ uint32_t nib_pair_lop3(uint32_t w) {
+    uint32_t r;
+    if constexpr (P == 0) {
+        asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(r) : "r"(w));
+    } else {
+        asm("{\n\t.reg .b32 t;\n\tshr.b32 t, %1, %2;\n\tlop3.b32 %0, t, 0x000F000F, 0x43004300, 0xEA;\n\t}"
+            : "=r"(r) : "r"(w), "n"(4 * P));
+    }
+    return r;
+}
+template <int P>
+__device__ __forceinline__ uint32_t crumb_pair_lop3(uint32_t w) {
+    uint32_t r;
+    if constexpr (P == 0) {
+        asm("lop3.b32 %0, %1, 0x00030003, 0x43004300, 0xEA;" : "=r"(r) : "r"(w));
+    } else {
+        asm("{\n\t.reg .b32 t;\n\tshr.b32 t, %1, %2;\n\tlop3.b32 %0, t, 0x00030003, 0x43004300, 0xEA;\n\t}"
+            : "=r"(r) : "r"(w), "n"(2 * P));
+    }
+    return r;
+}
 // fp32 (2^23 + byte i of w): a float with biased exponent 150 and the byte in the mantissa
 __device__ __forceinline__ float byte_magic_f32(uint32_t w, int i) {
     return __uint_as_float(__byte_perm(w, 0x4B000000u, (unsigned)(i | 0x7540)));

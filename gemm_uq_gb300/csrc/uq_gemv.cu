@@ -12,6 +12,11 @@ extern template cudaError_t launch_gemv_fmt<UQ_K4>(const GemvArgs&, int, cudaStr
 
 size_t gemv_smem_bytes(int fmt, int K, int group, int M) { return gemv_smem_bytes_impl(fmt, K, group, M); }
 int gemv_warps(int fmt) { return gemv_warps_impl(fmt); }
+int gemv_grid(int fmt, int P, int sms) {
+    // the mma kernel strides its workers over the CTAs, so it can use every SM whatever P is
+    if (gemv_is_mma(fmt)) return P < sms ? P : sms;
+    return (P + GEMV_WARPS - 1) / GEMV_WARPS;
+}
 size_t gemv_partials_floats(int P, int M) { return gemv_partials_floats_impl(P, M); }
 
 cudaError_t launch_gemv(int fmt, const GemvArgs& a, int grid, cudaStream_t st) {

@@ -678,31 +678,6 @@ __host__ __device__ inline GemvSmem gemv_mma_smem_plan(int fmt, int K, int group
     return p;
 }
 
-// bf16x2 (128 + code) of nibble pair P (bits 4P.. of each half) / crumb pair P (bits 2P..): one
-// lop3 ((w & mask) | magic), after a shift unless P == 0
-template <int P>
-__device__ __forceinline__ uint32_t nib_pair_lop3(uint32_t w) {
-    uint32_t r;
-    if constexpr (P == 0) {
-        asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(r) : "r"(w));
-    } else {
-        asm("{\n\t.reg .b32 t;\n\tshr.b32 t, %1, %2;\n\tlop3.b32 %0, t, 0x000F000F, 0x43004300, 0xEA;\n\t}"
-            : "=r"(r) : "r"(w), "n"(4 * P));
-    }
-    return r;
-}
-template <int P>
-__device__ __forceinline__ uint32_t crumb_pair_lop3(uint32_t w) {
-    uint32_t r;
-    if constexpr (P == 0) {
-        asm("lop3.b32 %0, %1, 0x00030003, 0x43004300, 0xEA;" : "=r"(r) : "r"(w));
-    } else {
-        asm("{\n\t.reg .b32 t;\n\tshr.b32 t, %1, %2;\n\tlop3.b32 %0, t, 0x00030003, 0x43004300, 0xEA;\n\t}"
-            : "=r"(r) : "r"(w), "n"(2 * P));
-    }
-    return r;
-}
-
 template <int FMT, int GB, bool XS>
 __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(const GemvArgs a) {
     using F = GemvFmt<FMT>;
@@ -722,7 +697,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
-    const int w = blockIdx.x * W + warp;
+    const int w = blockIdx.x + gridDim.x * warp;                 // workers strided over the CTAs (small P spreads over all SMs)
     const bool has_work = w < a.P;
     const Layout L(a.N, a.K, FMT);
     uint8_t* ring = smem + (size_t)warp * S * F::STAGE_BYTES;
@@ -766,6 +741,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
             mbar_arrive_expect_tx(xbar, (uint32_t)(M * a.K * 2));
             for (int m = 0; m < M; ++m) bulk_g2s(xs + m * xstride, a.x + (long long)m * a.ldx, (uint32_t)(a.K * 2), xbar);
         }
+        __syncthreads();                            // no warp's weight copies ahead of x
     }
     if (has_work)
         while (issued < S && t0 + issued < t1) issue_next();

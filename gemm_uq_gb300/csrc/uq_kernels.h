@@ -43,6 +43,7 @@ struct GemvArgs {
 constexpr int GEMV_WARPS = 4;     // worker warps per CTA
 size_t gemv_smem_bytes(int fmt, int K, int group, int M);
 int gemv_warps(int fmt);     // workers (warps) per CTA of the GEMV for this format
+int gemv_grid(int fmt, int P, int sms);   // CTAs of a GEMV launch with P workers
 size_t gemv_partials_floats(int P, int M);
 cudaError_t launch_gemv(int fmt, const GemvArgs& a, int grid, cudaStream_t st);
 

@@ -15,13 +15,14 @@
 //        scale in fp32: y += s_g * sum_k (q - z) x  (K4: d*sc_j * sum q x - dmin*m_j * sum x).
 // So the products and the per-group sums are exact up to fp32 accumulation, as in the GEMV.
 //
-// Roles (384 threads, one CTA per SM, persistent over an equal contiguous range of units):
+// Roles (512 threads, one CTA per SM, persistent over an equal contiguous range of units):
 //   warp 0       producer: per unit eight 2 KB bulk copies of codes (one per 16-row block of the
 //                fragment-order plane) and kc/64 TMA boxes of x, counted on full[stage];
 //   warp 1       MMA issuer (one thread): per group g/16 tcgen05.mma (M=128, N=Mpad, K=16);
-//   warps 4..7   dequant: thread = weight row; reads its codes from the fragment-order chunks,
-//                writes kc/2 columns of (q - z) into tensor memory;
-//   warps 8..11  epilogue: thread = weight row; scales, accumulates over the row block's units,
+//   warps 4..11  dequant: warp = one 16-row block; lane (g, c) turns its fragment-order words
+//                into (q - z) bf16 pairs and stores them with tcgen05.st.16x256b (the store
+//                shape whose thread layout is the mma fragment's), kc/2 columns per unit;
+//   warps 12..15 epilogue: thread = weight row; scales, accumulates over the row block's units,
 //                then stores y, or a partial sum plus a ticket (the last contributor reduces
 //                the partials in CTA order, so results are deterministic and nobody waits).
 // Unit = (128-row block, chunk of 128 code bytes per row = kc codes).  Every wait is bounded
@@ -224,8 +225,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
             int issued = 0;
-            auto issue_codes = [&](long long u, int s) {
-                const int rb = (int)(u / a.CH), c = (int)(u % a.CH);
+            auto issue_codes = [&](int rb, int c, int s) {
                 uint8_t* st = smem + s * SB;
                 // for each of the 8 row blocks of 16, the unit's 4 chunks (2 KB, contiguous)
                 const int nb0 = rb * 8;
@@ -236,8 +236,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     bulk_g2s(st + j * 2048, a.wq + (long long)(nb0 + j) * 16 * a.rowbytes + (long long)kb * 8192 + q0 * 512,
                              2048u, &full[s]);
             };
-            auto issue_x = [&](long long u, int s) {
-                const int c = (int)(u % a.CH);
+            auto issue_x = [&](int c, int s) {
                 uint8_t* st = smem + s * SB;
 #pragma unroll
                 for (int q = 0; q < KC / 64; ++q)
@@ -246,18 +245,30 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             // the first stages' weights are constant: stream them before waiting for the previous
             // kernel on the stream (launch overlap); x is loaded only after that wait
             const int pre = (u1 - u0) < S ? (int)(u1 - u0) : S;
-            for (int j = 0; j < pre; ++j) issue_codes(u0 + j, j);
+            const int CH = a.CH;
+            int rb = (int)(u0 / CH), c = (int)(u0 % CH);
+            for (int j = 0, r2 = rb, c2 = c; j < pre; ++j) {
+                issue_codes(r2, c2, j);
+                if (++c2 == CH) { c2 = 0; ++r2; }
+            }
             asm volatile("griddepcontrol.wait;" ::: "memory");
-            for (int j = 0; j < pre; ++j) issue_x(u0 + j, j);
+            for (int j = 0; j < pre; ++j) {
+                issue_x(c, j);
+                if (++c == CH) { c = 0; ++rb; }
+            }
             issued = pre;
+            int s = 0;
+            uint32_t eph = 1;                                // empty[] of the first round counts as free
             for (long long u = u0 + pre; u < u1 && !*abort_flag; ++u, ++issued) {
-                const int i = (int)(u - u0), s = i % S;
-                if (!mbar_wait_bounded(&empty[s], (uint32_t)(((i / S) & 1) ^ 1), a.fault, FAULT_TC_WAIT)) {
+                if (s == 0) eph ^= 1;
+                if (!mbar_wait_bounded(&empty[s], eph, a.fault, FAULT_TC_WAIT)) {
                     *abort_flag = 1;
                     break;
                 }
-                issue_codes(u, s);
-                issue_x(u, s);
+                issue_codes(rb, c, s);
+                issue_x(c, s);
+                if (++c == CH) { c = 0; ++rb; }
+                if (++s == S) s = 0;
             }
             // let the last copies land before the CTA can leave
             for (int j = issued - 1; j >= 0 && j >= issued - S; --j)
@@ -266,33 +277,39 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            long long dctr = 0;
+            int s = 0, ab = 0, d = 0;
+            uint32_t sph = 0, aph = 0, dph = 0;          // phases of full[s], afull[ab], dempty[d] (^1)
+            const int KS = G / 16;                       // MMAs per group
             for (long long u = u0; u < u1 && !*abort_flag; ++u) {
-                const int i = (int)(u - u0), s = i % S, ab = i & 1;
-                bool ok = mbar_wait_bounded(&full[s], (uint32_t)((i / S) & 1), a.fault, FAULT_TC_WAIT) &&
-                          mbar_wait_bounded(&afull[ab], (uint32_t)((i >> 1) & 1), a.fault, FAULT_TC_WAIT);
+                bool ok = mbar_wait_bounded(&full[s], sph, a.fault, FAULT_TC_WAIT) &&
+                          mbar_wait_bounded(&afull[ab], aph, a.fault, FAULT_TC_WAIT);
                 if (!ok) { *abort_flag = 1; break; }
                 tc_fence_after();
-                const uint8_t* xs = smem + s * SB + TC_STAGE_CODES;
-                for (int j = 0; j < GPC && ok; ++j, ++dctr) {
-                    const int d = (int)(dctr % DS);
-                    if (!mbar_wait_bounded(&dempty[d], (uint32_t)(((dctr / DS) & 1) ^ 1), a.fault, FAULT_TC_WAIT)) {
+                // B descriptors advance by 32 bytes per 16-k slice and by one x box (MPAD x 128 B)
+                // per 64 k: the start-address field is byte address / 16
+                const uint64_t bdesc0 = sw128_desc(smem + s * SB + TC_STAGE_CODES);
+                const uint32_t acol0 = tmem + A_COL0 + ab * ACOLS;
+                int ks = 0;
+                for (int j = 0; j < GPC; ++j) {
+                    if (!mbar_wait_bounded(&dempty[d], dph ^ 1u, a.fault, FAULT_TC_WAIT)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const int ks_per_group = G / 16;
-                    for (int t = 0; t < ks_per_group; ++t) {
-                        const int ks = j * ks_per_group + t;                 // 16-k slice within the unit
-                        const uint64_t bdesc = sw128_desc(xs + (ks >> 2) * (MPAD * 128) + (ks & 3) * 32);
-                        mma_ts(tmem + D_COL0 + d * MPAD, tmem + A_COL0 + ab * ACOLS + ks * 8, bdesc, IDESC,
-                               t > 0 ? 1u : 0u);
+                    const uint32_t dcol = tmem + D_COL0 + d * MPAD;
+                    for (int t = 0; t < KS; ++t, ++ks) {
+                        const uint64_t bdesc = bdesc0 + (uint64_t)((ks >> 2) * (MPAD * 8) + (ks & 3) * 2);
+                        mma_ts(dcol, acol0 + ks * 8, bdesc, IDESC, t > 0 ? 1u : 0u);
                     }
                     tc_commit(&dfull[d]);
+                    if (++d == DS) { d = 0; dph ^= 1u; }
                 }
                 if (!ok) { *abort_flag = 1; break; }
                 tc_commit(&aempty[ab]);
                 tc_commit(&empty[s]);
+                if (++s == S) { s = 0; sph ^= 1u; }
+                ab ^= 1;
+                if (ab == 0) aph ^= 1u;
             }
         }
     } else if (warp >= 4 && warp < 4 + TC_DQ_WARPS) {
@@ -309,12 +326,12 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         auto issue_zeros = [&](long long u) {
             if constexpr (FMT == UQ_INT4_ASYM) {
                 if (u < u1 && c4 < 2) {
-                    const int rb = (int)(u / a.CH), c = (int)(u % a.CH);
+                    const int rb = (int)u / a.CH, c = (int)u % a.CH;
                     const int r = g + 8 * c4;
                     const long long n = (long long)rb * TC_ROWS + rbl * 16 + r;
                     const int Gn = a.K / G, ZB = (Gn + 1) >> 1;
                     if (n < a.N)
-                        stage_span(zr + ((u - u0) % 3) * (TC_DQ_WARPS * 32) + r * 2, a.zc,
+                        stage_span(zr + ((int)(u - u0) % 3) * (TC_DQ_WARPS * 32) + r * 2, a.zc,
                                    n * ZB + (long long)c * (GPC >> 1), GPC >> 1, (long long)a.N * ZB);
                 }
                 cp_async_commit();
@@ -322,8 +339,10 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         };
         issue_zeros(u0);
         issue_zeros(u0 + 1);
+        int s = 0, ab = 0, zslot = 0;
+        uint32_t sph = 0, aph = 1;                      // full[s] phase; aempty[] of the first round is free
+        int rb = (int)u0 / a.CH, c = (int)u0 % a.CH;
         for (long long u = u0; u < u1 && !*abort_flag; ++u) {
-            const int i = (int)(u - u0), s = i % S, ab = i & 1;
             __syncwarp();
             issue_zeros(u + 2);
             // subtrahend per group as a bf16 pair: 128 + z (INT4_ASYM), 128 + 8 (INT4_SYM), 128 (K4)
@@ -334,9 +353,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             if constexpr (FMT == UQ_INT4_ASYM) {
                 cp_async_wait2();
                 __syncwarp();
-                const int rb = (int)(u / a.CH), c = (int)(u % a.CH);
                 const int Gn = a.K / G, ZB = (Gn + 1) >> 1;
-                const uint32_t* slot = zr + (i % 3) * (TC_DQ_WARPS * 32);
+                const uint32_t* slot = zr + zslot * (TC_DQ_WARPS * 32);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const long long n = (long long)rb * TC_ROWS + rbl * 16 + g + 8 * h;
@@ -354,8 +372,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     }
                 }
             }
-            bool ok = mbar_wait_bounded(&full[s], (uint32_t)((i / S) & 1), a.fault, FAULT_TC_WAIT) &&
-                      mbar_wait_bounded(&aempty[ab], (uint32_t)(((i >> 1) & 1) ^ 1), a.fault, FAULT_TC_WAIT);
+            bool ok = mbar_wait_bounded(&full[s], sph, a.fault, FAULT_TC_WAIT) &&
+                      mbar_wait_bounded(&aempty[ab], aph, a.fault, FAULT_TC_WAIT);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) { *abort_flag = 1; break; }
             tc_fence_after();
@@ -393,10 +411,10 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
 #pragma unroll
                     for (int b = 0; b < 4; ++b) {
                         const int j = (FMT == UQ_INT4_ASYM) ? (4 * q + b) / GB : 0;
-                        v[4 * b + 0] = bf16x2_sub(nib_pair_bf16(wv[b], 0), zlo[j]);
-                        v[4 * b + 1] = bf16x2_sub(nib_pair_bf16(wv[b], 2), zlo[j]);
-                        v[4 * b + 2] = bf16x2_sub(nib_pair_bf16(wv[b], 1), zhi[j]);
-                        v[4 * b + 3] = bf16x2_sub(nib_pair_bf16(wv[b], 3), zhi[j]);
+                        v[4 * b + 0] = bf16x2_sub(nib_pair_lop3<0>(wv[b]), zlo[j]);
+                        v[4 * b + 1] = bf16x2_sub(nib_pair_lop3<2>(wv[b]), zlo[j]);
+                        v[4 * b + 2] = bf16x2_sub(nib_pair_lop3<1>(wv[b]), zhi[j]);
+                        v[4 * b + 3] = bf16x2_sub(nib_pair_lop3<3>(wv[b]), zhi[j]);
                     }
                     tmem_st_16x256b_x4(acol + q * 32, v);
                 }
@@ -405,6 +423,11 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) { mbar_arrive(&afull[ab]); mbar_arrive(&empty[s]); }
+            if (++s == S) { s = 0; sph ^= 1u; }
+            ab ^= 1;
+            if (ab == 0) aph ^= 1u;
+            if (++zslot == 3) zslot = 0;
+            if (++c == a.CH) { c = 0; ++rb; }
         }
         if constexpr (FMT == UQ_INT4_ASYM) asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (warp >= 4 + TC_DQ_WARPS) {
@@ -417,9 +440,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         // this row's scale words (K4: its super-block record) staged three units ahead
         auto issue_scales = [&](long long u) {
             if (u < u1) {
-                const int rb = (int)(u / a.CH), c = (int)(u % a.CH);
+                const int rb = (int)u / a.CH, c = (int)u % a.CH;
                 const long long n = (long long)rb * TC_ROWS + r;
-                uint32_t* dst = er + ((u - u0) % 3) * (128 * SWORDS);
+                uint32_t* dst = er + ((int)(u - u0) % 3) * (128 * SWORDS);
                 if (n < a.N) {
                     if constexpr (FMT == UQ_K4) {
                         tc_cp_async16(dst, a.scales + (n * (a.K >> 8) + c) * 16);
@@ -436,8 +459,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         float acc[MPAD];
 #pragma unroll
         for (int m = 0; m < MPAD; ++m) acc[m] = 0.f;
-        long long dctr = 0;
-        uint32_t ephase = 0;
+        int d = 0, eslot = 0;
+        uint32_t dph = 0, ephase = 0;
         // all 128 epilogue threads meet here (bounded: returns false after the time limit)
         auto epi_sync = [&]() -> bool {
             mbar_arrive(ebar);
@@ -445,17 +468,18 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             ephase ^= 1u;
             return r_ok;
         };
-        const int first_rb = (int)(u0 / a.CH);
+        const int first_rb = (int)u0 / a.CH;
+        int rb = first_rb, c = (int)u0 % a.CH;
         for (long long u = u0; u < u1 && !*abort_flag; ++u) {
-            const int rb = (int)(u / a.CH), c = (int)(u % a.CH);
             const int n = rb * TC_ROWS + r;
             const bool live = n < a.N;
             issue_scales(u + 2);
             cp_async_wait2();
-            const uint32_t* sw = er + ((u - u0) % 3) * (128 * SWORDS);
+            const uint32_t* sw = er + eslot * (128 * SWORDS);
+            if (++eslot == 3) eslot = 0;
             const int so = live ? (int)(((long long)n * (a.K / G) + (long long)c * GPC) & 1) : 0;   // halves
             bool ok = true;
-            for (int j = 0; j < GPC; ++j, ++dctr) {
+            for (int j = 0; j < GPC; ++j) {
                 float s1 = 0.f, s2 = 0.f;
                 if (live) {
                     if constexpr (FMT == UQ_K4) {
@@ -468,9 +492,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                         s1 = half_bits_f32(reinterpret_cast<const uint16_t*>(sw)[so + j]);
                     }
                 }
-                const int d = (int)(dctr % DS);
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait_bounded(&dfull[d], (uint32_t)((dctr / DS) & 1), a.fault, FAULT_TC_WAIT));
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&dfull[d], dph, a.fault, FAULT_TC_WAIT));
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -484,6 +506,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&dempty[d]);
+                if (++d == DS) { d = 0; dph ^= 1u; }
                 if constexpr (FMT == UQ_K4) {
                     const float* sx = a.sx + (long long)((c * KC + j * 32) >> 5) * MPAD;
 #pragma unroll
@@ -502,9 +525,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                                 a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
                 } else {
                     const int slot = 2 * cta + (rb == first_rb ? 0 : 1);
-                    float* part = a.partials + ((long long)slot * TC_ROWS + r) * MPAD;
+                    float* part = a.partials + (long long)slot * TC_ROWS * MPAD + r;   // [slot][m][row]
 #pragma unroll
-                    for (int m = 0; m < MPAD; ++m) part[m] = acc[m];
+                    for (int m = 0; m < MPAD; ++m) part[m * TC_ROWS] = acc[m];
                     __threadfence();
                     if (!epi_sync()) { *abort_flag = 1; break; }
                     if (r == 0) *ticket_smem = atomicAdd(a.tickets + rb, 1u);
@@ -520,9 +543,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                         for (int c2 = cf; c2 <= cl; ++c2) {
                             const int rb2 = (int)(trange_begin(c2, a.U, a.P) / a.CH);
                             const int slot2 = 2 * c2 + (rb == rb2 ? 0 : 1);
-                            const float* p2 = a.partials + ((long long)slot2 * TC_ROWS + r) * MPAD;
+                            const float* p2 = a.partials + (long long)slot2 * TC_ROWS * MPAD + r;
 #pragma unroll
-                            for (int m = 0; m < MPAD; ++m) acc[m] += __ldcg(p2 + m);
+                            for (int m = 0; m < MPAD; ++m) acc[m] += __ldcg(p2 + m * TC_ROWS);
                         }
                         if (live)
 #pragma unroll
@@ -536,6 +559,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
 #pragma unroll
                 for (int m = 0; m < MPAD; ++m) acc[m] = 0.f;
             }
+            if (++c == a.CH) { c = 0; ++rb; }
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
     }
