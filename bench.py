@@ -119,6 +119,16 @@ def dominant_kernel(fmt, group, M, recs):
     return f"gemv_kernel<{fmt},{min(M, 8)}>"
 
 
+def kernels_per_call(fmt, M, K):
+    """Kernel launches one uq_gemm call makes: the tensor-core path (one launch per 64 rows of x,
+    plus the K4 column-sum pre-kernel), or the GEMV per 8 rows of x (the mma GEMV adds its split-K
+    reduce launch)."""
+    kt = {"INT4_SYM": 1024, "INT4_ASYM": 1024, "INT8_SYM": 512, "INT2_ASYM": 2048, "NF4": 1024, "K4": 1024}[fmt]
+    if M >= 16 and fmt in ("INT4_SYM", "INT4_ASYM", "INT8_SYM", "K4") and K % kt == 0:
+        return ((M + 63) // 64) * (2 if fmt == "K4" else 1)
+    return ((M + 7) // 8) * (2 if fmt in ("INT4_SYM", "INT4_ASYM", "INT2_ASYM", "K4") else 1)
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -377,7 +387,7 @@ def run_uq(args, rank, world, dist):
                    "l2": "no flush: packed weights per step exceed L2 (%.2f GB)" % (step_bytes / 1e9),
                    "launch": "one CUDA graph per step",
                    "launch_overlap": not args.no_overlap},
-        "gpu_launches": launches * args.steps,
+        "gpu_launches": sum(kernels_per_call(fmt, M, r["K"]) for r in recs) * args.steps,
         "e2e": {"value": round(step_bytes * args.steps * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": xbuf.numel() * 2, "d2h_bytes_per_step": ybuf.numel() * 2},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

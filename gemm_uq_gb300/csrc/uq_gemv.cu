@@ -19,16 +19,70 @@ int gemv_grid(int fmt, int P, int sms) {
 }
 size_t gemv_partials_floats(int P, int M) { return gemv_partials_floats_impl(P, M); }
 
+// Second pass of the mma GEMV's split-K: for every row block that several workers share, sum their
+// partials in worker order (fixed, so results are bit-reproducible) and store y.  Launched right
+// after the GEMV with programmatic stream serialization: it becomes resident early and its
+// griddepcontrol.wait returns once the GEMV grid has finished and its stores are visible, so the
+// GEMV itself needs no fence, ticket or waiting between workers.
+__global__ void __launch_bounds__(256) gemv_split_reduce(const GemvArgs a) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int M = a.M, KB = a.KB;
+    const long long total = (long long)a.NB * RB * M;
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int nb = (int)(e / (RB * M));
+        const int rm = (int)(e % (RB * M));                 // r * M + m
+        const int n = nb * RB + rm / M, m = rm % M;
+        if (n >= a.N) continue;
+        const long long tf = (long long)nb * KB;
+        const int wf = worker_of(tf, a.T, a.P), wl = worker_of(tf + KB - 1, a.T, a.P);
+        if (wf == wl) continue;                            // one worker covered it and stored y
+        float sum = 0.f;
+        for (int w2 = wf; w2 <= wl; ++w2) {
+            const int nb2 = (int)(range_begin(w2, a.T, a.P) / KB);
+            const int slot2 = 2 * w2 + (nb == nb2 ? 0 : 1);
+            sum += a.partials[(long long)slot2 * RB * M + rm];
+        }
+        a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+    }
+}
+
+static cudaError_t launch_split_reduce(const GemvArgs& a, int sms, cudaStream_t st) {
+    const long long total = (long long)a.NB * RB * a.M;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 4LL * sms) blocks = 4LL * sms;
+    if (blocks < 1) blocks = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_split_reduce, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 cudaError_t launch_gemv(int fmt, const GemvArgs& a, int grid, cudaStream_t st) {
+    cudaError_t e;
     switch (fmt) {
-        case UQ_INT4_SYM: return launch_gemv_fmt<UQ_INT4_SYM>(a, grid, st);
-        case UQ_INT4_ASYM: return launch_gemv_fmt<UQ_INT4_ASYM>(a, grid, st);
-        case UQ_INT8_SYM: return launch_gemv_fmt<UQ_INT8_SYM>(a, grid, st);
-        case UQ_INT2_ASYM: return launch_gemv_fmt<UQ_INT2_ASYM>(a, grid, st);
-        case UQ_NF4: return launch_gemv_fmt<UQ_NF4>(a, grid, st);
-        case UQ_K4: return launch_gemv_fmt<UQ_K4>(a, grid, st);
+        case UQ_INT4_SYM: e = launch_gemv_fmt<UQ_INT4_SYM>(a, grid, st); break;
+        case UQ_INT4_ASYM: e = launch_gemv_fmt<UQ_INT4_ASYM>(a, grid, st); break;
+        case UQ_INT8_SYM: e = launch_gemv_fmt<UQ_INT8_SYM>(a, grid, st); break;
+        case UQ_INT2_ASYM: e = launch_gemv_fmt<UQ_INT2_ASYM>(a, grid, st); break;
+        case UQ_NF4: e = launch_gemv_fmt<UQ_NF4>(a, grid, st); break;
+        case UQ_K4: e = launch_gemv_fmt<UQ_K4>(a, grid, st); break;
         default: return cudaErrorInvalidValue;
     }
+    if (e != cudaSuccess || !gemv_is_mma(fmt)) return e;
+    // the mma kernel leaves row blocks shared between workers as partial sums (grid = its CTAs,
+    // one per SM at most, so it is also the SM count bound for the reduce grid)
+    return launch_split_reduce(a, grid, st);
 }
 
 }  // namespace uq

@@ -935,6 +935,8 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
                             a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * j + e]));
                     }
             } else {
+                // row block shared with other workers: its fp32 partial sums go to this worker's slot
+                // (first or last row block of its range); gemv_split_reduce adds them up afterwards
                 const int slot = 2 * w + (nb == first_nb ? 0 : 1);
                 float* part = a.partials + (long long)slot * RB * M;
 #pragma unroll
@@ -942,28 +944,6 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
 #pragma unroll
                     for (int e = 0; e < 2; ++e)
                         if (2 * c + e < M) part[(g + 8 * j) * M + 2 * c + e] = acc[2 * j + e];
-                __threadfence();
-                __syncwarp();
-                unsigned int old = 0;
-                if (lane == 0) old = atomicAdd(a.tickets + nb, 1u);
-                old = __shfl_sync(0xffffffffu, old, 0);
-                const long long tf = (long long)nb * L.KB;
-                const int wf = worker_of(tf, a.T, a.P), wl = worker_of(tf + L.KB - 1, a.T, a.P);
-                if (old == (unsigned int)(wl - wf)) {
-                    __threadfence();
-                    for (int e = lane; e < RB * M; e += 32) {
-                        const int r = e / M, m = e % M;
-                        if (n0 + r >= a.N) continue;
-                        float sum = 0.f;
-                        for (int w2 = wf; w2 <= wl; ++w2) {
-                            const int nb2 = (int)(range_begin(w2, a.T, a.P) / L.KB);
-                            const int slot2 = 2 * w2 + (nb == nb2 ? 0 : 1);
-                            sum += __ldcg(a.partials + (long long)slot2 * RB * M + e);
-                        }
-                        a.y[(long long)m * a.ldy + n0 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
-                    }
-                    if (lane == 0) a.tickets[nb] = 0u;
-                }
             }
             acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
         }
