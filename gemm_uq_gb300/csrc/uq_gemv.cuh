@@ -221,7 +221,7 @@ __device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, c
         const uint32_t bytes = (uint32_t)L.tile_bytes(kb);
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(st, a.wq + L.tile_offset(nb, kb), bytes, bar);
+        bulk_g2s_stream(st, a.wq + L.tile_offset(nb, kb), bytes, bar, l2_evict_first_policy());
     }
 }
 

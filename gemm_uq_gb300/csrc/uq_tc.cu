@@ -225,6 +225,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
             int issued = 0;
+            const uint64_t pol = l2_evict_first_policy();
             auto issue_codes = [&](int rb, int c, int s) {
                 uint8_t* st = smem + s * SB;
                 // for each of the 8 row blocks of 16, the unit's 4 chunks (2 KB, contiguous)
@@ -233,8 +234,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                 mbar_arrive_expect_tx(&full[s], (uint32_t)(nbs * 2048 + XB));
                 const int kb = c >> 2, q0 = (c & 3) * 4;
                 for (int j = 0; j < nbs; ++j)
-                    bulk_g2s(st + j * 2048, a.wq + (long long)(nb0 + j) * 16 * a.rowbytes + (long long)kb * 8192 + q0 * 512,
-                             2048u, &full[s]);
+                    bulk_g2s_stream(st + j * 2048, a.wq + (long long)(nb0 + j) * 16 * a.rowbytes + (long long)kb * 8192 + q0 * 512,
+                                    2048u, &full[s], pol);
             };
             auto issue_x = [&](int c, int s) {
                 uint8_t* st = smem + s * SB;
