@@ -652,9 +652,9 @@ template <int FMT> struct MmaCfg {
     static constexpr int STAGES = 2;                               // tiles in flight per worker
 };
 
-// bytes per row of the pair-interleaved x in shared memory: 64 bytes of padding put rows g and
-// g + 1 of a quarter-warp's 16-byte loads into different banks
-__host__ __device__ inline size_t gemv_mma_x_stride(int Kp) { return (size_t)Kp * 2 + 64; }
+// bytes per row of x in shared memory: 32 bytes of padding put the four rows a half-warp's 8-byte
+// B-fragment loads touch into different banks
+__host__ __device__ inline size_t gemv_mma_x_stride(int Kp) { return (size_t)Kp * 2 + 32; }
 
 __host__ __device__ inline GemvSmem gemv_mma_smem_plan(int fmt, int K, int group, int M, bool x_in_smem) {
     int stage = 0, warps = 0, kc = fmt_kc(fmt);
@@ -666,14 +666,12 @@ __host__ __device__ inline GemvSmem gemv_mma_smem_plan(int fmt, int K, int group
     }
     const int stages = 2;
     const int Kp = (K + kc - 1) / kc * kc;
-    const int gs = (fmt == UQ_K4) ? 32 : group;
+    (void)group;
     GemvSmem p;
     p.bars = (size_t)warps * stages * stage;
-    p.lut = p.bars + (size_t)(warps * stages + 1) * 8;
-    p.sx = p.lut + 64;
-    p.ps = p.sx + (size_t)((Kp + gs - 1) / gs) * 8 * 4;             // per-group sums, 8 columns
-    p.x = p.ps + (x_in_smem ? (size_t)(Kp / 32) * 8 * 4 : 0);       // per-32-k partial sums
-    p.x = (p.x + 127) / 128 * 128;
+    p.lut = p.bars + (size_t)(warps * stages + 1) * 8;              // + the x mbarrier
+    p.sx = p.ps = p.lut + 64;
+    p.x = (p.sx + 127) / 128 * 128;
     p.total = p.x + (x_in_smem ? (size_t)M * gemv_mma_x_stride(Kp) : 0);
     return p;
 }
@@ -690,8 +688,6 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
     const int M = a.M;
     const GemvSmem plan = gemv_mma_smem_plan(FMT, a.K, a.group, M, XS);
     uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + plan.bars);
-    float* sxg = reinterpret_cast<float*>(smem + plan.sx);
-    float* psx = reinterpret_cast<float*>(smem + plan.ps);
     uint8_t* xs = smem + plan.x;
     uint64_t* xbar = bars_all + W * S;
 
@@ -749,60 +745,15 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
         const int padw = (L.Kp - a.K) / 2;
         for (int e = threadIdx.x; e < M * padw; e += blockDim.x)
             reinterpret_cast<uint32_t*>(xs + (e / padw) * xstride + a.K * 2)[e % padw] = 0u;
-        __syncthreads();
+        __syncthreads();                            // the zero padding is visible
         mbar_wait_bounded(xbar, 0, a.fault, FAULT_GEMV_WAIT);
-        // Interleave each 32-k pair of blocks: natural 8-byte unit u = 4 jj + c (k = 16 jj + 4c .. +3)
-        // moves to position 2c + jj, so lane c finds its B fragments of both blocks in 16 bytes.
-        // The same pass forms the sum of x over each 32 k (in k order).
-        const int PB = L.Kp / 32;
-        for (int e = threadIdx.x; e < PB * M; e += blockDim.x) {
-            const int pb = e / M, m = e % M;
-            uint4* p = reinterpret_cast<uint4*>(xs + m * xstride + pb * 64);
-            const uint4 q0 = p[0], q1 = p[1], q2 = p[2], q3 = p[3];
-            const uint32_t u[16] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w,
-                                    q2.x, q2.y, q2.z, q2.w, q3.x, q3.y, q3.z, q3.w};
-            float s0 = 0.f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) s0 += bf16lo_f32(u[j]) + bf16hi_f32(u[j]);
-            p[0] = make_uint4(u[0], u[1], u[8], u[9]);
-            p[1] = make_uint4(u[2], u[3], u[10], u[11]);
-            p[2] = make_uint4(u[4], u[5], u[12], u[13]);
-            p[3] = make_uint4(u[6], u[7], u[14], u[15]);
-            psx[pb * 8 + m] = s0;
-        }
-        __syncthreads();
-        // sxg[gi * 8 + m] = sum of x[m][k] over group gi (its 32-k sums in k order); 0 for m >= M
-        for (int e = threadIdx.x; e < G_all * 8; e += blockDim.x) {
-            const int gi = e >> 3, m = e & 7;
-            float s0 = 0.f;
-            if (m < M)
-#pragma unroll
-                for (int t = 0; t < GS / 32; ++t) s0 += psx[(gi * (GS / 32) + t) * 8 + m];
-            sxg[e] = s0;
-        }
-    } else {
-        for (int e = threadIdx.x; e < G_all * 8; e += blockDim.x) {
-            const int gi = e >> 3, m = e & 7;
-            float s0 = 0.f;
-            if (m < M) {
-#pragma unroll
-                for (int k = 0; k < GS; k += 8) {
-                    const uint4 q = ldg_nc_v4(a.x + (long long)m * a.ldx + gi * GS + k);
-                    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) s0 += bf16lo_f32(u[j]) + bf16hi_f32(u[j]);
-                }
-            }
-            sxg[e] = s0;
-        }
     }
-    __syncthreads();
     if (!has_work) return;
 
     const int first_nb = (int)(t0 / L.KB);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};        // rows g + 8j, columns 2c + e
     const int mrow = g < M ? g : M - 1;          // B rows beyond M repeat a real row; their D columns are unused
-    const uint8_t* xrow = xs + mrow * xstride + 16 * c;
+    const uint8_t* xrow = xs + mrow * xstride + 8 * c;
     const uint16_t* xgrow = a.x + (long long)mrow * a.ldx + 4 * c;
     int nb = (int)(t0 / L.KB), kb = (int)(t0 % L.KB);
 
@@ -828,7 +779,6 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
         }
         const uint8_t* xt = xrow + (size_t)kb * KT * 2;             // x of the tile's first k
         const uint16_t* xgt = xgrow + (long long)kb * KT;
-        const float* sxt = sxg + gi0 * 8 + 2 * c;
 
         auto group_step = [&](const int gg) {
             // this lane's code words for the group's GB blocks
@@ -851,13 +801,13 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
                     wv[0] = *reinterpret_cast<const uint32_t*>(cp);
                 }
             }
-            // B fragments: x at k = 16 blk + 4c .. +3 of row mrow, two blocks per 16-byte load
+            // B fragments: x at k = 16 blk + 4c .. +3 of row mrow (8 bytes per block)
             uint32_t bx[GB], by[GB];
             if constexpr (XS) {
 #pragma unroll
-                for (int jp = 0; jp < GB / 2; ++jp) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(xt + (gg * (GB / 2) + jp) * 64);
-                    bx[2 * jp] = v.x; by[2 * jp] = v.y; bx[2 * jp + 1] = v.z; by[2 * jp + 1] = v.w;
+                for (int j = 0; j < GB; ++j) {
+                    const uint2 v = *reinterpret_cast<const uint2*>(xt + (gg * GB + j) * 32);
+                    bx[j] = v.x; by[j] = v.y;
                 }
             } else {
 #pragma unroll
@@ -867,7 +817,10 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
                     bx[j] = v.x; by[j] = v.y;
                 }
             }
-            float dd[2][4];
+            // dd: the group's sum of (128 + q) x;  ds: the same mma with A = 1, i.e. the sum of x over the
+            // group for columns 2c, 2c + 1 (rows of D are all equal), which the zero-point term needs
+            float dd[2][4], ds[2][4];
+            constexpr uint32_t ONES = 0x3F803F80u;                  // bf16 pair (1, 1)
 #pragma unroll
             for (int j = 0; j < GB; ++j) {
                 uint32_t a0, a1, a2, a3;
@@ -885,11 +838,18 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
                     a0 = nib_pair_lop3<0>(wd); a1 = nib_pair_lop3<1>(wd);
                     a2 = nib_pair_lop3<2>(wd); a3 = nib_pair_lop3<3>(wd);
                 }
-                if (j < 2) mma_bf16_zero(dd[j & 1], a0, a1, a2, a3, bx[j], by[j]);
-                else mma_bf16(dd[j & 1], a0, a1, a2, a3, bx[j], by[j]);
+                if (j < 2) {
+                    mma_bf16_zero(dd[j & 1], a0, a1, a2, a3, bx[j], by[j]);
+                    mma_bf16_zero(ds[j & 1], ONES, ONES, ONES, ONES, bx[j], by[j]);
+                } else {
+                    mma_bf16(dd[j & 1], a0, a1, a2, a3, bx[j], by[j]);
+                    mma_bf16(ds[j & 1], ONES, ONES, ONES, ONES, bx[j], by[j]);
+                }
             }
             // fold the group into the row sums
-            const float2 sxv = *reinterpret_cast<const float2*>(sxt + gg * 8);
+            float2 sxv;
+            sxv.x = ds[0][0] + ds[1][0];
+            sxv.y = ds[0][1] + ds[1][1];
             float d[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) d[e] = dd[0][e] + dd[1][e];
@@ -911,7 +871,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
             }
         };
         if (ng == GPT) {
-#pragma unroll
+#pragma unroll 4
             for (int gg = 0; gg < GPT; ++gg) group_step(gg);
         } else {
 #pragma unroll 1
