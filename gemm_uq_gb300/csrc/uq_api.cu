@@ -78,7 +78,7 @@ std::map<int, DeviceState> g_dev;
 struct Workspace {
     float* partials = nullptr;
     size_t partial_bytes = 0;
-    float* aux = nullptr;              // K4 column sums for the tensor-core path
+    float* aux = nullptr;              // tensor-core path: fp16 copy of x and its row scales
     size_t aux_bytes = 0;
     unsigned int* tickets = nullptr;   // zero between calls (the kernels reset what they use)
     size_t ticket_bytes = 0;
@@ -191,9 +191,9 @@ uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const 
 uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const void* zc, uint16_t* y, int Mb, int N,
                  int K, int ldx, int ldy, int group, int fmt, cudaStream_t st, const DeviceState& ds, int dev) {
     const int mpad = (Mb + 15) / 16 * 16;
-    int stages = 0, dslots = 0;
+    int stages = 0, nabuf = 0;
     size_t smem = 0;
-    if (uq::tc_plan(fmt, mpad, &stages, &dslots, &smem) != 0)
+    if (uq::tc_plan(fmt, mpad, &stages, &nabuf, &smem) != 0)
         return fail(UQ_ERR_UNSUPPORTED, "no tensor-core plan for M=%d", Mb);
     const int kc = (fmt == UQ_INT8_SYM) ? 128 : 256;
     const int nblk = (N + 127) / 128;
@@ -202,15 +202,15 @@ uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const vo
     long long P = ds.sms;
     if (P > U) P = U;
     Workspace* ws = nullptr;
-    const size_t aux = (fmt == UQ_K4) ? (size_t)(K / 32) * mpad * sizeof(float) : 0;
+    // aux: the fp16 copy of x [Mb][K], then the 64 column scales
+    const size_t xh_bytes = ((size_t)Mb * K * 2 + 255) / 256 * 256;
     uq_status s = workspace(dev, st, (size_t)2 * P * 128 * mpad * sizeof(float), (size_t)nblk * sizeof(unsigned int),
-                            &ws, aux);
+                            &ws, xh_bytes + 64 * sizeof(float));
     if (s != UQ_OK) return s;
-    cudaError_t e;
-    if (fmt == UQ_K4) {
-        e = uq::launch_colsum32(x, ws->aux, Mb, mpad, K, ldx, st);
-        if (e != cudaSuccess) return cuda_fail(e, "column-sum launch");
-    }
+    uint16_t* xh = reinterpret_cast<uint16_t*>(ws->aux);
+    float* xsc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws->aux) + xh_bytes);
+    cudaError_t e = uq::launch_tc_prep(x, ldx, K, Mb, mpad, xh, xsc, st);
+    if (e != cudaSuccess) return cuda_fail(e, "x conversion launch");
     uq::TcArgs a;
     const uq::Layout L(N, K, fmt);
     a.wq = static_cast<const uint8_t*>(wq);
@@ -219,14 +219,14 @@ uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const vo
     a.scales = static_cast<const uint8_t*>(scales);
     a.zc = static_cast<const uint8_t*>(zc);
     a.y = y;
-    a.sx = ws->aux;
+    a.xscale = xsc;
     a.M = Mb; a.Mpad = mpad; a.N = N; a.K = K; a.group = group; a.ldx = ldx; a.ldy = ldy;
     a.CH = CH; a.U = U; a.P = (int)P;
-    a.stages = stages; a.dslots = dslots;
+    a.stages = stages; a.nabuf = nabuf;
     a.partials = ws->partials;
     a.tickets = ws->tickets;
     a.fault = ds.words;
-    e = uq::launch_tc(fmt, x, a, smem, (int)P, st);
+    e = uq::launch_tc(fmt, xh, a, smem, (int)P, st);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core launch");
     return UQ_OK;
 }

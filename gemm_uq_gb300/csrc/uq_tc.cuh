@@ -1,0 +1,638 @@
+// uq_tc.cuh -- tensor-core fused dequantize + GEMM for M >= 16 (tcgen05, sm_103a).
+//
+// "Ultra LLM Engine", section "Fused Kernels": the dequantized-weight GEMM of batched decode.
+// With 16..64 activation rows the product is a dense contraction, so it runs on the 5th-gen
+// tensor cores; the kernel still streams each packed weight byte from HBM exactly once.
+//
+// Operands (swap-AB: the 128 weight rows are the MMA's M dimension, the activation rows its N):
+//   A  = the dequantized weights s * (q - z) (K4: d*sc*q - dmin*m), each rounded once to fp16
+//        (relative error <= 2^-11), written by the dequant warps straight into TENSOR MEMORY with
+//        tcgen05.st -- the dequantized operand never crosses shared memory;
+//   B  = x in fp16: a small pre-kernel scales each row of x by a power of two 2^-e_m (exact) so that
+//        its largest magnitude lies in [2^14, 2^15), and the tile is loaded by TMA with the
+//        128-byte swizzle (the canonical K-major operand layout);
+//   D  = one fp32 accumulator per 128-row block in tensor memory (128 lanes x Mpad columns), summed
+//        over all of the block's k: the epilogue reads it once per row block and multiplies column
+//        m by 2^e_m.
+// Error: |A - w_hat| <= 2^-11 |w_hat| per weight, x is exact, accumulation is fp32, so
+// |y - y_ref| stays within about 5e-4 * sum |x * w_hat| -- inside the 1e-3 tolerance.
+//
+// Roles (512 threads, one CTA per SM, persistent over an equal contiguous range of units):
+//   warp 0       producer: per unit eight 2 KB bulk copies of codes (one per 16-row block of the
+//                fragment-order plane, L2 evict_first) and kc/64 TMA boxes of x, on full[stage];
+//   warp 1       MMA issuer (one thread): kc/16 tcgen05.mma per unit (M=128, N=Mpad, K=16) into
+//                the row block's accumulator; commits free the A buffer and the stage, and hand a
+//                finished row block to the epilogue;
+//   warps 4..11  dequant: warp = one 16-row block; lane (g, c) turns its fragment-order words into
+//                fp16 pairs of s*(q - z) and stores them with tcgen05.st.16x256b (the store shape
+//                whose thread layout is the mma fragment's); scales, zero points and K4 records
+//                arrive through per-warp cp.async rings three units ahead;
+//   warps 12..15 epilogue: thread = weight row; at a row block's end in this CTA it reads the
+//                accumulator, scales the columns, and stores y, or a partial sum plus a ticket
+//                (the last contributor reduces the partials in CTA order: deterministic, no waits).
+// Unit = (128-row block, chunk of 128 code bytes per row = kc codes).  Every wait is bounded
+// (mbar_wait_bounded); on a timeout the roles stop, the CTA frees its tensor memory and leaves.
+#pragma once
+#include <cuda.h>
+
+#include "uq_kernels.h"
+
+namespace uq {
+
+constexpr int TC_THREADS = 512;
+constexpr int TC_ROWS = 128;
+constexpr int TC_STAGE_CODES = TC_ROWS * 128;     // bytes of codes per stage
+constexpr int TMEM_COLS = 512;
+constexpr int TC_BAR_BYTES = 2048;                 // barriers and flags after the stages
+constexpr int TC_DQ_WARPS = 8;                     // dequant warps (one 16-row block each)
+constexpr int TC_DQW = 8;                          // staged metadata words per row and unit
+constexpr int TC_DQ_RING = 3 * TC_DQ_WARPS * 16 * TC_DQW * 4;   // bytes: 3 units of metadata
+
+template <int FMT> struct TcFmt {
+    static constexpr int KC = (FMT == UQ_INT8_SYM) ? 128 : 256;   // codes per row per unit
+    static constexpr int ACOLS = KC / 2;                           // tensor-memory columns of A per unit
+};
+struct TcSmem {
+    static __host__ __device__ constexpr int x_bytes(int kc, int mpad) { return kc * mpad * 2; }
+    static __host__ __device__ constexpr int stage_bytes(int kc, int mpad) { return TC_STAGE_CODES + x_bytes(kc, mpad); }
+};
+
+namespace {
+
+
+
+__device__ __forceinline__ long long trange_begin(int c, long long U, int P) { return (long long)c * U / P; }
+__device__ __forceinline__ int tworker_of(long long u, long long U, int P) {
+    return (int)(((u + 1) * (long long)P - 1) / U);
+}
+
+// ---- tcgen05 / TMA wrappers ------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_u32(dst_smem)), "r"(ncols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(smem_u32(bar)) : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc]
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// 16 lanes x 256 bits per repetition, fragment layout of an m16n8 accumulator: thread t holds
+// (lane t/4, columns 2(t%4), 2(t%4)+1) and (lane t/4 + 8, same columns); .x4 repeats it over 32 columns
+__device__ __forceinline__ void tmem_st_16x256b_x4(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], "
+                 "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+                 :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                    "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
+                    "r"(v[14]), "r"(v[15]) : "memory");
+}
+__device__ __forceinline__ void tmem_st_16x256b_x2(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x2.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                    "r"(v[7]) : "memory");
+}
+__device__ __forceinline__ void tc_cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void tc_cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
+// Copy the aligned 32-bit words that cover bytes [lo, lo + len) of `base` into dst[0 .. nw) (word 0
+// holds byte lo & ~3).  Words that would reach past `end` (the array's size) are assembled from byte
+// loads instead, so nothing outside the array is read.
+__device__ __forceinline__ void stage_span(uint32_t* dst, const uint8_t* base, long long lo, int len, long long end) {
+    const long long w0 = lo & ~3ll;
+    for (long long src = w0; src < lo + len; src += 4, ++dst) {
+        if (src + 4 <= end) {
+            tc_cp_async4(dst, base + src);
+        } else {
+            uint32_t v = 0;
+            for (int b = 0; b < 4; ++b)
+                if (src + b < end) v |= (uint32_t)__ldg(base + src + b) << (8 * b);
+            *dst = v;
+        }
+    }
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                   "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr) : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];"
+                 :: "r"(smem_u32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar)) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row core groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(const void* p) {
+    const uint64_t addr = smem_u32(p);
+    return ((addr & 0x3FFFFull) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major, M = 128, N = mpad.
+__host__ __device__ constexpr uint32_t idesc_f16(int mpad) {
+    return (1u << 4) | ((uint32_t)(mpad >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+// fp16 pair (1024 + code) of nibble pair P (bits 4P.. of each half): fp16 0x6400 = 1024 with ulp 1
+template <int P>
+__device__ __forceinline__ uint32_t nib_pair_f16(uint32_t w) {
+    uint32_t r;
+    if constexpr (P == 0) {
+        asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;" : "=r"(r) : "r"(w));
+    } else {
+        asm("{\n\t.reg .b32 t;\n\tshr.b32 t, %1, %2;\n\tlop3.b32 %0, t, 0x000F000F, 0x64006400, 0xEA;\n\t}"
+            : "=r"(r) : "r"(w), "n"(4 * P));
+    }
+    return r;
+}
+// fp16 pairs (1024 + byte) of bytes 0, 1 and 2, 3 of w
+__device__ __forceinline__ uint32_t byte01_f16(uint32_t w) { return __byte_perm(w, 0x6464u, 0x5140u); }
+__device__ __forceinline__ uint32_t byte23_f16(uint32_t w) { return __byte_perm(w, 0x6464u, 0x5342u); }
+__device__ __forceinline__ float f16lo_f32(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu))); }
+__device__ __forceinline__ float f16hi_f32(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
+
+}  // namespace
+
+// GB = 16-k blocks per scaling group (2, 4 or 8; K4: its 32-weight sub-blocks, GB = 2)
+template <int FMT, int MPAD, int GB>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
+    constexpr int KC = TcFmt<FMT>::KC;
+    constexpr int ACOLS = TcFmt<FMT>::ACOLS;
+    constexpr int XB = TcSmem::x_bytes(KC, MPAD);
+    constexpr int SB = TcSmem::stage_bytes(KC, MPAD);
+    constexpr uint32_t IDESC = idesc_f16(MPAD);
+    constexpr int GS = GB * 16;                    // k per scaling group (K4: per sub-block)
+    constexpr int GPC = KC / GS;                   // groups per unit
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int S = a.stages, NA = a.nabuf;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * SB);
+    uint64_t* full = bars;                          // [S]
+    uint64_t* empty = full + S;                     // [S]
+    uint64_t* afull = empty + S;                    // [NA]
+    uint64_t* aempty = afull + NA;                  // [NA]
+    uint64_t* dfull = aempty + NA;                  // [2]
+    uint64_t* dempty = dfull + 2;                   // [2]
+    uint64_t* ebar = dempty + 2;                    // epilogue warpgroup rendezvous (128 arrivals)
+    uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(ebar + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_smem + 1);
+    unsigned int* ticket_smem = reinterpret_cast<unsigned int*>(tmem_base_smem + 2);
+    uint32_t* dq_ring = reinterpret_cast<uint32_t*>(smem + S * SB + TC_BAR_BYTES);   // [3][8 warps][16][TC_DQW]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const long long u0 = trange_begin(cta, a.U, a.P), u1 = trange_begin(cta + 1, a.U, a.P);
+    const int CH = a.CH;
+
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1 + TC_DQ_WARPS); }
+        for (int i = 0; i < NA; ++i) { mbar_init(&afull[i], TC_DQ_WARPS); mbar_init(&aempty[i], 1); }
+        for (int d = 0; d < 2; ++d) { mbar_init(&dfull[d], 1); mbar_init(&dempty[d], 4); }
+        mbar_init(ebar, 128);
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0) tmem_alloc(tmem_base_smem, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_base_smem;
+    const uint32_t A_COL0 = 0;                      // A buffers: columns [0, NA*ACOLS)
+    const uint32_t D_COL0 = NA * ACOLS;             // 2 accumulators of MPAD columns after them
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            const uint64_t pol = l2_evict_first_policy();
+            auto issue_codes = [&](int rb, int c, int s) {
+                uint8_t* st = smem + s * SB;
+                // for each of the 8 row blocks of 16, the unit's 4 chunks (2 KB, contiguous)
+                const int nb0 = rb * 8;
+                const int nbs = (a.NB - nb0) < 8 ? (a.NB - nb0) : 8;
+                mbar_arrive_expect_tx(&full[s], (uint32_t)(nbs * 2048 + XB));
+                const int kb = c >> 2, q0 = (c & 3) * 4;
+                for (int j = 0; j < nbs; ++j)
+                    bulk_g2s_stream(st + j * 2048, a.wq + (long long)(nb0 + j) * 16 * a.rowbytes + (long long)kb * 8192 + q0 * 512,
+                                    2048u, &full[s], pol);
+            };
+            auto issue_x = [&](int c, int s) {
+                uint8_t* st = smem + s * SB;
+#pragma unroll
+                for (int q = 0; q < KC / 64; ++q)
+                    tma_load_2d(st + TC_STAGE_CODES + q * (MPAD * 128), &tmap_x, c * KC + q * 64, 0, &full[s]);
+            };
+            // the first stages' weights are constant: stream them before waiting for the previous
+            // kernel on the stream (launch overlap); x is loaded only after that wait
+            const int pre = (u1 - u0) < S ? (int)(u1 - u0) : S;
+            int rb = (int)(u0 / CH), c = (int)(u0 % CH);
+            for (int j = 0, r2 = rb, c2 = c; j < pre; ++j) {
+                issue_codes(r2, c2, j);
+                if (++c2 == CH) { c2 = 0; ++r2; }
+            }
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            for (int j = 0; j < pre; ++j) {
+                issue_x(c, j);
+                if (++c == CH) { c = 0; ++rb; }
+            }
+            issued = pre;
+            int s = 0;
+            uint32_t eph = 1;                                // empty[] of the first round counts as free
+            for (long long u = u0 + pre; u < u1 && !*abort_flag; ++u, ++issued) {
+                if (s == 0) eph ^= 1;
+                if (!mbar_wait_bounded(&empty[s], eph, a.fault, FAULT_TC_WAIT)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                issue_codes(rb, c, s);
+                issue_x(c, s);
+                if (++c == CH) { c = 0; ++rb; }
+                if (++s == S) s = 0;
+            }
+            // let the last copies land before the CTA can leave
+            for (int j = issued - 1; j >= 0 && j >= issued - S; --j)
+                mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1), a.fault, FAULT_TC_WAIT);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int s = 0, ab = 0, dsl = 0;
+            uint32_t sph = 0, aph = 0, dph = 0;          // phases of full[s], afull[ab], dempty[dsl] (^1)
+            int c = (int)(u0 % CH);
+            bool rb_start = true;                        // this unit opens a row block in this CTA
+            for (long long u = u0; u < u1 && !*abort_flag; ++u) {
+                bool ok = mbar_wait_bounded(&full[s], sph, a.fault, FAULT_TC_WAIT) &&
+                          mbar_wait_bounded(&afull[ab], aph, a.fault, FAULT_TC_WAIT);
+                if (ok && rb_start) ok = mbar_wait_bounded(&dempty[dsl], dph ^ 1u, a.fault, FAULT_TC_WAIT);
+                if (!ok) { *abort_flag = 1; break; }
+                tc_fence_after();
+                // B descriptors advance by 32 bytes per 16-k slice and by one x box (MPAD x 128 B)
+                // per 64 k: the start-address field is byte address / 16
+                const uint64_t bdesc0 = sw128_desc(smem + s * SB + TC_STAGE_CODES);
+                const uint32_t acol0 = tmem + A_COL0 + ab * ACOLS;
+                const uint32_t dcol = tmem + D_COL0 + dsl * MPAD;
+                for (int ks = 0; ks < KC / 16; ++ks) {
+                    const uint64_t bdesc = bdesc0 + (uint64_t)((ks >> 2) * (MPAD * 8) + (ks & 3) * 2);
+                    mma_ts(dcol, acol0 + ks * 8, bdesc, IDESC, (rb_start && ks == 0) ? 0u : 1u);
+                }
+                tc_commit(&aempty[ab]);
+                tc_commit(&empty[s]);
+                const bool rb_end = (c == CH - 1) || (u == u1 - 1);
+                if (rb_end) {
+                    tc_commit(&dfull[dsl]);
+                    if (++dsl == 2) { dsl = 0; dph ^= 1u; }
+                }
+                rb_start = rb_end;
+                if (++s == S) { s = 0; sph ^= 1u; }
+                if (++ab == NA) { ab = 0; aph ^= 1u; }
+                if (++c == CH) c = 0;
+            }
+        }
+    } else if (warp >= 4 && warp < 4 + TC_DQ_WARPS) {
+        // ---------------------------------------------------------------- dequant warps
+        // warp -> one 16-row block of the unit, in the tensor-memory lane quarter (warp % 4) it may
+        // access; lane (g, c) holds the fragment-order words of rows g and g + 8, which the 16x256b
+        // store shape takes as they are: no shuffles, one 16-byte shared-memory read per 4 words.
+        const int quarter = warp & 3, hf = (warp >= 8) ? 1 : 0;
+        const int rbl = 2 * quarter + hf;               // row block (16 rows) within the 128-row unit
+        const int g = lane >> 2, c4 = lane & 3;
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter + 16 * hf) << 16);
+        uint32_t* wr = dq_ring + (warp - 4) * (16 * TC_DQW);   // this warp's slot 0; slots TC_DQ_WARPS*16*TC_DQW apart
+        constexpr int RING_STRIDE = TC_DQ_WARPS * 16 * TC_DQW;
+        const int Gn = a.K / GS, ZB = (Gn + 1) >> 1;
+        // metadata of unit u for rows g and g + 8: lanes c = 0, 1 stage the scales (K4: the record)
+        // of row g + 8c, lanes c = 2, 3 the INT4_ASYM zero points of row g + 8(c - 2)
+        auto issue_meta = [&](long long u, int slot) {
+            if (u < u1) {
+                const int ui = (int)u;
+                const int rb = ui / CH, c = ui % CH;
+                const int r = g + 8 * (c4 & 1);
+                const long long n = (long long)rb * TC_ROWS + rbl * 16 + r;
+                uint32_t* dst = wr + slot * RING_STRIDE + r * TC_DQW;
+                if (n < a.N) {
+                    if constexpr (FMT == UQ_K4) {
+                        if (c4 < 2) tc_cp_async16(dst, a.scales + (n * (a.K >> 8) + c) * 16);
+                    } else {
+                        if (c4 < 2)
+                            stage_span(dst, a.scales, (n * Gn + (long long)c * GPC) * 2, GPC * 2, (long long)a.N * Gn * 2);
+                        if constexpr (FMT == UQ_INT4_ASYM)
+                            if (c4 >= 2)
+                                stage_span(dst + 5, a.zc, n * ZB + (long long)c * (GPC >> 1), GPC >> 1, (long long)a.N * ZB);
+                    }
+                }
+            }
+            cp_async_commit();
+        };
+        issue_meta(u0, 0);
+        issue_meta(u0 + 1, 1);
+        int s = 0, ab = 0, slot = 0;
+        uint32_t sph = 0, aph = 1;                      // full[s] phase; aempty[] of the first round is free
+        int rb = (int)(u0 / CH), c = (int)(u0 % CH);
+        for (long long u = u0; u < u1 && !*abort_flag; ++u) {
+            __syncwarp();
+            issue_meta(u + 2, slot == 0 ? 2 : slot - 1);
+            cp_async_wait2();
+            __syncwarp();
+            // per-group operands for rows g (h = 0) and g + 8 (h = 1)
+            uint32_t sc2[2][GPC], zz[2][GPC];           // fp16 pairs (s, s) and (1024 + z)
+            float ka[2][GPC], kb[2][GPC];               // K4: d*sc_j and dmin*m_j
+            const uint32_t* sl = wr + slot * RING_STRIDE;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = g + 8 * h;
+                const long long n = (long long)rb * TC_ROWS + rbl * 16 + r;
+                const bool live = n < a.N;
+                const uint32_t* rw = sl + r * TC_DQW;
+                if constexpr (FMT == UQ_K4) {
+                    const uint4 rec = live ? *reinterpret_cast<const uint4*>(rw) : make_uint4(0, 0, 0, 0);
+                    const uint64_t sc48 = (uint64_t)rec.y | ((uint64_t)(rec.z & 0xFFFFu) << 32);
+                    const uint64_t m48 = (uint64_t)(rec.z >> 16) | ((uint64_t)rec.w << 16);
+                    const float d = half_bits_f32((uint16_t)(rec.x & 0xFFFF)), dm = half_bits_f32((uint16_t)(rec.x >> 16));
+#pragma unroll
+                    for (int j = 0; j < GPC; ++j) {
+                        ka[h][j] = d * (float)((sc48 >> (6 * j)) & 63);
+                        kb[h][j] = dm * (float)((m48 >> (6 * j)) & 63);
+                    }
+                } else {
+                    const int so = live ? (int)(((long long)n * Gn + (long long)c * GPC) & 1) : 0;
+                    const uint16_t* hs = reinterpret_cast<const uint16_t*>(rw) + so;
+                    uint32_t zb = 0;
+                    if constexpr (FMT == UQ_INT4_ASYM) {
+                        if (live) {
+                            const int o = (int)((n * ZB + (long long)c * (GPC >> 1)) & 3);
+                            const uint64_t w = (uint64_t)rw[5] | ((uint64_t)rw[6] << 32);
+                            zb = (uint32_t)(w >> (8 * o));
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < GPC; ++j) {
+                        const uint32_t s16 = live ? (uint32_t)hs[j] : 0u;
+                        sc2[h][j] = s16 | (s16 << 16);
+                        uint32_t zp;
+                        if constexpr (FMT == UQ_INT4_ASYM) zp = 0x6400u | ((zb >> (4 * j)) & 15u);
+                        else if constexpr (FMT == UQ_INT8_SYM) zp = 0x6480u;       // 1024 + 128
+                        else zp = 0x6408u;                                         // 1024 + 8
+                        zz[h][j] = zp | (zp << 16);
+                    }
+                }
+            }
+            bool ok = mbar_wait_bounded(&full[s], sph, a.fault, FAULT_TC_WAIT) &&
+                      mbar_wait_bounded(&aempty[ab], aph, a.fault, FAULT_TC_WAIT);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) { *abort_flag = 1; break; }
+            tc_fence_after();
+            const uint8_t* rbase = smem + s * SB + rbl * 2048 + lane * 16;
+            const uint32_t acol = lane_addr + A_COL0 + ab * ACOLS;
+            if constexpr (FMT == UQ_INT8_SYM) {
+                // chunk q = 32 k = blocks 2q, 2q + 1; word 2b + h = row g + 8h, k 4c .. 4c + 3 of block b
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 w4 = *reinterpret_cast<const uint4*>(rbase + q * 512);
+                    const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+                    uint32_t v[8];
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        const int j = (2 * q + b) / GB;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t wd = wv[2 * b + h];
+                            v[4 * b + 2 * h] = f16x2_mul(f16x2_sub(byte01_f16(wd), zz[h][j]), sc2[h][j]);
+                            v[4 * b + 2 * h + 1] = f16x2_mul(f16x2_sub(byte23_f16(wd), zz[h][j]), sc2[h][j]);
+                        }
+                    }
+                    tmem_st_16x256b_x2(acol + q * 16, v);
+                }
+            } else {
+                // chunk q = 64 k = blocks 4q .. 4q + 3, one word each; pairs 0/2 are row g (k 4c, 4c+1 /
+                // 4c+2, 4c+3), pairs 1/3 row g + 8
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 w4 = *reinterpret_cast<const uint4*>(rbase + q * 512);
+                    const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+                    uint32_t v[16];
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        const int j = (4 * q + b) / GB;
+                        const uint32_t p0 = nib_pair_f16<0>(wv[b]), p2 = nib_pair_f16<2>(wv[b]);
+                        const uint32_t p1 = nib_pair_f16<1>(wv[b]), p3 = nib_pair_f16<3>(wv[b]);
+                        if constexpr (FMT == UQ_K4) {
+                            // w = d*sc*q - dmin*m in fp32 (q from 1024 + q exactly), rounded once to fp16
+                            const uint32_t pp[4] = {p0, p2, p1, p3};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int h = e >> 1;
+                                const float qlo = f16lo_f32(pp[e]) - 1024.0f, qhi = f16hi_f32(pp[e]) - 1024.0f;
+                                v[4 * b + e] = f32x2_to_f16x2(fmaf(ka[h][j], qlo, -kb[h][j]), fmaf(ka[h][j], qhi, -kb[h][j]));
+                            }
+                        } else {
+                            v[4 * b + 0] = f16x2_mul(f16x2_sub(p0, zz[0][j]), sc2[0][j]);
+                            v[4 * b + 1] = f16x2_mul(f16x2_sub(p2, zz[0][j]), sc2[0][j]);
+                            v[4 * b + 2] = f16x2_mul(f16x2_sub(p1, zz[1][j]), sc2[1][j]);
+                            v[4 * b + 3] = f16x2_mul(f16x2_sub(p3, zz[1][j]), sc2[1][j]);
+                        }
+                    }
+                    tmem_st_16x256b_x4(acol + q * 32, v);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) { mbar_arrive(&afull[ab]); mbar_arrive(&empty[s]); }
+            if (++s == S) { s = 0; sph ^= 1u; }
+            if (++ab == NA) { ab = 0; aph ^= 1u; }
+            if (++slot == 3) slot = 0;
+            if (++c == CH) { c = 0; ++rb; }
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (warp >= 4 + TC_DQ_WARPS) {
+        // ---------------------------------------------------------------- epilogue warpgroup
+        asm volatile("griddepcontrol.wait;" ::: "memory");   // x scales, workspace and y follow earlier work
+        const int we = warp & 3;
+        const int r = we * 32 + lane;
+        const uint32_t lane_addr = tmem + ((uint32_t)(we * 32) << 16);
+        int dsl = 0;
+        uint32_t dph = 0, ephase = 0;
+        // all 128 epilogue threads meet here (bounded: returns false after the time limit)
+        auto epi_sync = [&]() -> bool {
+            mbar_arrive(ebar);
+            const bool r_ok = mbar_wait_bounded(ebar, ephase, a.fault, FAULT_TC_WAIT);
+            ephase ^= 1u;
+            return r_ok;
+        };
+        const int first_rb = (int)(u0 / CH);
+        int rb = first_rb, c = (int)(u0 % CH);
+        for (long long u = u0; u < u1 && !*abort_flag; ++u) {
+            if (c == CH - 1 || u == u1 - 1) {
+                // the row block's accumulation in this CTA is complete
+                const int n = rb * TC_ROWS + r;
+                const bool live = n < a.N;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(&dfull[dsl], dph, a.fault, FAULT_TC_WAIT))) {
+                    *abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
+                float acc[MPAD];
+#pragma unroll
+                for (int q = 0; q < MPAD / 16; ++q) {
+                    float v[16];
+                    tmem_ld16(lane_addr + D_COL0 + dsl * MPAD + q * 16, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) acc[q * 16 + e] = v[e] * __ldg(a.xscale + q * 16 + e);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&dempty[dsl]);
+                if (++dsl == 2) { dsl = 0; dph ^= 1u; }
+                const bool fullcov = (c == CH - 1) && (rb != first_rb || (u0 % CH) == 0);
+                if (fullcov) {
+                    if (live)
+#pragma unroll
+                        for (int m = 0; m < MPAD; ++m)
+                            if (m < a.M)
+                                a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+                } else {
+                    const int pslot = 2 * cta + (rb == first_rb ? 0 : 1);
+                    float* part = a.partials + (long long)pslot * TC_ROWS * MPAD + r;   // [slot][m][row]
+#pragma unroll
+                    for (int m = 0; m < MPAD; ++m) part[m * TC_ROWS] = acc[m];
+                    __threadfence();
+                    if (!epi_sync()) { *abort_flag = 1; break; }
+                    if (r == 0) *ticket_smem = atomicAdd(a.tickets + rb, 1u);
+                    if (!epi_sync()) { *abort_flag = 1; break; }
+                    const unsigned int old = *ticket_smem;
+                    const long long uf = (long long)rb * CH;
+                    const int cf = tworker_of(uf, a.U, a.P), cl = tworker_of(uf + CH - 1, a.U, a.P);
+                    if (old == (unsigned int)(cl - cf)) {
+                        __threadfence();
+                        // the partials of all contributors, summed in CTA order
+#pragma unroll
+                        for (int m = 0; m < MPAD; ++m) acc[m] = 0.f;
+                        for (int c2 = cf; c2 <= cl; ++c2) {
+                            const int rb2 = (int)(trange_begin(c2, a.U, a.P) / CH);
+                            const int slot2 = 2 * c2 + (rb == rb2 ? 0 : 1);
+                            const float* p2 = a.partials + (long long)slot2 * TC_ROWS * MPAD + r;
+#pragma unroll
+                            for (int m = 0; m < MPAD; ++m) acc[m] += __ldcg(p2 + m * TC_ROWS);
+                        }
+                        if (live)
+#pragma unroll
+                            for (int m = 0; m < MPAD; ++m)
+                                if (m < a.M)
+                                    a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+                        if (r == 0) a.tickets[rb] = 0u;
+                    }
+                    if (!epi_sync()) { *abort_flag = 1; break; }
+                }
+            }
+            if (++c == CH) { c = 0; ++rb; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+namespace tc_detail {
+template <int FMT, int MPAD, int GB>
+cudaError_t launch_t(const CUtensorMap& mx, const TcArgs& a, size_t smem, int grid, cudaStream_t st) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(tc_kernel<FMT, MPAD, GB>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    // always after the x pre-kernel on the stream: programmatic serialization lets the constant
+    // weights stream in while that kernel (and, with launch overlap, the work before it) finishes
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, tc_kernel<FMT, MPAD, GB>, mx, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+template <int FMT, int GB>
+cudaError_t launch_mg(const CUtensorMap& mx, const TcArgs& a, size_t smem, int grid, cudaStream_t st) {
+    switch (a.Mpad) {
+        case 16: return launch_t<FMT, 16, GB>(mx, a, smem, grid, st);
+        case 32: return launch_t<FMT, 32, GB>(mx, a, smem, grid, st);
+        case 48: return launch_t<FMT, 48, GB>(mx, a, smem, grid, st);
+        case 64: return launch_t<FMT, 64, GB>(mx, a, smem, grid, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+}  // namespace tc_detail
+
+// one format's launch (instantiated in uq_tc_<fmt>.cu)
+template <int FMT>
+cudaError_t launch_tc_fmt(const CUtensorMap& mx, const TcArgs& a, size_t smem, int grid, cudaStream_t st) {
+    if constexpr (FMT == UQ_K4) {
+        return tc_detail::launch_mg<FMT, 2>(mx, a, smem, grid, st);
+    } else {
+        switch (a.group) {
+            case 32: return tc_detail::launch_mg<FMT, 2>(mx, a, smem, grid, st);
+            case 64: return tc_detail::launch_mg<FMT, 4>(mx, a, smem, grid, st);
+            case 128: return tc_detail::launch_mg<FMT, 8>(mx, a, smem, grid, st);
+            default: return cudaErrorInvalidValue;
+        }
+    }
+}
+
+}  // namespace uq
