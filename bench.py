@@ -120,12 +120,12 @@ def dominant_kernel(fmt, group, M, recs):
 
 
 def kernels_per_call(fmt, M, K):
-    """Kernel launches one uq_gemm call makes: the tensor-core path (one launch per 64 rows of x,
-    plus the K4 column-sum pre-kernel), or the GEMV per 8 rows of x (the mma GEMV adds its split-K
+    """Kernel launches one uq_gemm call makes: the tensor-core path (per 64 rows of x: the x
+    conversion pre-kernel and the GEMM), or the GEMV per 8 rows of x (the mma GEMV adds its split-K
     reduce launch)."""
     kt = {"INT4_SYM": 1024, "INT4_ASYM": 1024, "INT8_SYM": 512, "INT2_ASYM": 2048, "NF4": 1024, "K4": 1024}[fmt]
     if M >= 16 and fmt in ("INT4_SYM", "INT4_ASYM", "INT8_SYM", "K4") and K % kt == 0:
-        return ((M + 63) // 64) * (2 if fmt == "K4" else 1)
+        return ((M + 63) // 64) * 2
     return ((M + 7) // 8) * (2 if fmt in ("INT4_SYM", "INT4_ASYM", "INT2_ASYM", "K4") else 1)
 
 
