@@ -180,7 +180,7 @@ uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const 
     a.tickets = ws->tickets;
     a.fault = ds.words;
     a.overlap = 0;
-    const int grid = uq::gemv_grid(fmt, (int)P, ds.sms);
+    const int grid = uq::gemv_grid(a, fmt, ds.sms);
     cudaError_t e = uq::launch_gemv(fmt, a, grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "GEMV launch");
     return UQ_OK;

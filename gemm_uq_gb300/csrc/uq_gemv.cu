@@ -12,10 +12,21 @@ extern template cudaError_t launch_gemv_fmt<UQ_K4>(const GemvArgs&, int, cudaStr
 
 size_t gemv_smem_bytes(int fmt, int K, int group, int M) { return gemv_smem_bytes_impl(fmt, K, group, M); }
 int gemv_warps(int fmt) { return gemv_warps_impl(fmt); }
-int gemv_grid(int fmt, int P, int sms) {
-    // the mma kernel strides its workers over the CTAs, so it can use every SM whatever P is
-    if (gemv_is_mma(fmt)) return P < sms ? P : sms;
-    return (P + GEMV_WARPS - 1) / GEMV_WARPS;
+int gemv_grid(GemvArgs& a, int fmt, int sms) {
+    a.cta_rows = 0;
+    if (!gemv_is_mma(fmt)) return (a.P + GEMV_WARPS - 1) / GEMV_WARPS;
+    // Whole row blocks per CTA need no second pass; take them when no warp gets more tiles than
+    // under the stream-K split (the workers are strided over the CTAs, so every SM is used).
+    const int W = gemv_warps(fmt);
+    const int G = a.NB < sms ? a.NB : sms;
+    const long long rbs = (a.NB + G - 1) / G;
+    const long long per_warp_rows = (rbs * a.KB + W - 1) / W;
+    const long long per_warp_split = (a.T + a.P - 1) / a.P;
+    if (G > 0 && per_warp_rows <= per_warp_split) {
+        a.cta_rows = 1;
+        return G;
+    }
+    return a.P < sms ? a.P : sms;
 }
 size_t gemv_partials_floats(int P, int M) { return gemv_partials_floats_impl(P, M); }
 
@@ -79,7 +90,7 @@ cudaError_t launch_gemv(int fmt, const GemvArgs& a, int grid, cudaStream_t st) {
         case UQ_K4: e = launch_gemv_fmt<UQ_K4>(a, grid, st); break;
         default: return cudaErrorInvalidValue;
     }
-    if (e != cudaSuccess || !gemv_is_mma(fmt)) return e;
+    if (e != cudaSuccess || !gemv_is_mma(fmt) || a.cta_rows) return e;
     // the mma kernel leaves row blocks shared between workers as partial sums (grid = its CTAs,
     // one per SM at most, so it is also the SM count bound for the reduce grid)
     return launch_split_reduce(a, grid, st);

@@ -670,8 +670,9 @@ __host__ __device__ inline GemvSmem gemv_mma_smem_plan(int fmt, int K, int group
     GemvSmem p;
     p.bars = (size_t)warps * stages * stage;
     p.lut = p.bars + (size_t)(warps * stages + 1) * 8;              // + the x mbarrier
-    p.sx = p.ps = p.lut + 64;
-    p.x = (p.sx + 127) / 128 * 128;
+    p.sx = p.lut + 64;
+    p.ps = p.sx;                                                    // [warps][2][16 rows][8 columns] fp32
+    p.x = (p.ps + (size_t)warps * 2 * RB * 8 * 4 + 127) / 128 * 128;
     p.total = p.x + (x_in_smem ? (size_t)M * gemv_mma_x_stride(Kp) : 0);
     return p;
 }
@@ -689,17 +690,27 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
     const GemvSmem plan = gemv_mma_smem_plan(FMT, a.K, a.group, M, XS);
     uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + plan.bars);
     uint8_t* xs = smem + plan.x;
+    float* cpart = reinterpret_cast<float*>(smem + plan.ps);
     uint64_t* xbar = bars_all + W * S;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
-    const int w = blockIdx.x + gridDim.x * warp;                 // workers strided over the CTAs (small P spreads over all SMs)
-    const bool has_work = w < a.P;
     const Layout L(a.N, a.K, FMT);
+    // Work split.  cta_rows: CTA b owns row blocks [rb0, rb1) and its W warps split those tiles
+    // evenly (range_begin over the CTA's tiles); otherwise worker w = CTA + grid * warp (strided, so a
+    // small matrix still spreads over every SM) owns an equal share of all tiles.
+    const bool cta_rows = a.cta_rows != 0;
+    const int rb0 = cta_rows ? (int)((long long)blockIdx.x * a.NB / gridDim.x) : 0;
+    const int rb1 = cta_rows ? (int)((long long)(blockIdx.x + 1) * a.NB / gridDim.x) : 0;
+    const long long Tc = (long long)(rb1 - rb0) * L.KB;             // the CTA's tiles (cta_rows)
+    const int w = cta_rows ? warp : (int)(blockIdx.x + gridDim.x * warp);
+    const bool has_work = cta_rows ? true : w < a.P;
     uint8_t* ring = smem + (size_t)warp * S * F::STAGE_BYTES;
     uint64_t* bars = bars_all + warp * S;
-    const long long t0 = has_work ? range_begin(w, a.T, a.P) : 0;
-    const long long t1 = has_work ? range_begin(w + 1, a.T, a.P) : 0;
+    const long long t0 = cta_rows ? (long long)rb0 * L.KB + range_begin(warp, Tc, W)
+                                  : (has_work ? range_begin(w, a.T, a.P) : 0);
+    const long long t1 = cta_rows ? (long long)rb0 * L.KB + range_begin(warp + 1, Tc, W)
+                                  : (has_work ? range_begin(w + 1, a.T, a.P) : 0);
     MetaConst mc;
     mc.G = a.K / a.group;
     mc.GT = KT / a.group;
@@ -748,7 +759,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
         __syncthreads();                            // the zero padding is visible
         mbar_wait_bounded(xbar, 0, a.fault, FAULT_GEMV_WAIT);
     }
-    if (!has_work) return;
+    if (!has_work) return;                          // (never in cta_rows mode: every warp meets the end barrier)
 
     const int first_nb = (int)(t0 / L.KB);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};        // rows g + 8j, columns 2c + e
@@ -768,7 +779,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
                 const int sj = (it + j) % S;
                 mbar_wait_bounded(&bars[sj], (uint32_t)(((it + j) / S) & 1), a.fault, FAULT_GEMV_WAIT);
             }
-            return;
+            break;
         }
         const int gi0 = kb * GPT;
         const int ng = (G_all - gi0) < GPT ? (G_all - gi0) : GPT;   // groups of the tile inside K
@@ -894,6 +905,13 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
                         if (m < M && n < a.N)
                             a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * j + e]));
                     }
+            } else if (cta_rows) {
+                // row block shared with other warps of this CTA: partial sums to shared memory
+                float* part = cpart + ((warp * 2 + (nb == first_nb ? 0 : 1)) * RB) * 8;
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) part[(g + 8 * j) * 8 + 2 * c + e] = acc[2 * j + e];
             } else {
                 // row block shared with other workers: its fp32 partial sums go to this worker's slot
                 // (first or last row block of its range); gemv_split_reduce adds them up afterwards
@@ -908,6 +926,25 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
             acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
         }
         if (++kb == L.KB) { kb = 0; ++nb; }
+    }
+    if (!cta_rows) return;
+    // cta_rows: row blocks whose tiles were split between warps of this CTA, summed in warp order
+    __syncthreads();
+    for (int e = threadIdx.x; e < (rb1 - rb0) * RB * M; e += blockDim.x) {
+        const int rbi = e / (RB * M), rm = e % (RB * M), r = rm / M, m = rm % M;
+        const int nb2 = rb0 + rbi, n = nb2 * RB + r;
+        if (n >= a.N) continue;
+        const long long tf = (long long)rbi * L.KB;                 // tiles relative to the CTA's first
+        const int wf = worker_of(tf, Tc, W), wl = worker_of(tf + L.KB - 1, Tc, W);
+        if (wf == wl) continue;                                    // one warp covered it and stored y
+        float sum = 0.f;
+        for (int w2 = wf; w2 <= wl; ++w2) {
+            const long long b2 = range_begin(w2, Tc, W);
+            if (b2 == range_begin(w2 + 1, Tc, W)) continue;        // a warp without tiles (Tc < W)
+            const int first2 = (int)((long long)rb0 + b2 / L.KB);
+            sum += cpart[((w2 * 2 + (nb2 == first2 ? 0 : 1)) * RB + r) * 8 + m];
+        }
+        a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
     }
 }
 

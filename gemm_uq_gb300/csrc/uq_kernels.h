@@ -39,11 +39,15 @@ struct GemvArgs {
     unsigned int* tickets;    // [NB], zero between calls
     unsigned int* fault;      // device fault word
     int overlap;              // launched with programmatic stream serialization (set by the launcher)
+    int cta_rows;             // mma GEMV: 1 = every CTA owns whole row blocks (combined in shared memory,
+                              // no second pass); 0 = workers split row blocks anywhere (second pass)
 };
 constexpr int GEMV_WARPS = 4;     // worker warps per CTA
 size_t gemv_smem_bytes(int fmt, int K, int group, int M);
 int gemv_warps(int fmt);     // workers (warps) per CTA of the GEMV for this format
-int gemv_grid(int fmt, int P, int sms);   // CTAs of a GEMV launch with P workers
+// work split of a GEMV launch whose a.P (stream-K workers) is set: may switch the mma GEMV to
+// whole row blocks per CTA (a.cta_rows = 1); returns the grid
+int gemv_grid(GemvArgs& a, int fmt, int sms);
 size_t gemv_partials_floats(int P, int M);
 cudaError_t launch_gemv(int fmt, const GemvArgs& a, int grid, cudaStream_t st);
 

@@ -150,7 +150,8 @@ uq_status uq_gemm_noalloc(const uint16_t* x, const void* wq, const void* scales,
         a.tickets = tickets;
         a.fault = reinterpret_cast<unsigned int*>(scratch);
         a.overlap = 0;
-        e = uq::launch_gemv(fmt, a, uq::gemv_grid(fmt, (int)P, sms), st);
+        const int grid = uq::gemv_grid(a, fmt, sms);
+        e = uq::launch_gemv(fmt, a, grid, st);
         if (e != cudaSuccess) { snprintf(g_err, sizeof g_err, "GEMV launch: %s", cudaGetErrorString(e)); return err(UQ_ERR_CUDA); }
     }
     return UQ_OK;

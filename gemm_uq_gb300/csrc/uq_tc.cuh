@@ -89,6 +89,12 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
                  :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
+// D[tmem] += A[tmem] * B[smem desc]
+__device__ __forceinline__ void mma_ts_acc(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.eq.b32 p, 1, 1;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc) : "memory");
+}
 // 16 lanes x 256 bits per repetition, fragment layout of an m16n8 accumulator: thread t holds
 // (lane t/4, columns 2(t%4), 2(t%4)+1) and (lane t/4 + 8, same columns); .x4 repeats it over 32 columns
 __device__ __forceinline__ void tmem_st_16x256b_x4(uint32_t taddr, const uint32_t (&v)[16]) {
@@ -315,10 +321,13 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                 const uint64_t bdesc0 = sw128_desc(smem + s * SB + TC_STAGE_CODES);
                 const uint32_t acol0 = tmem + A_COL0 + ab * ACOLS;
                 const uint32_t dcol = tmem + D_COL0 + dsl * MPAD;
-                for (int ks = 0; ks < KC / 16; ++ks) {
-                    const uint64_t bdesc = bdesc0 + (uint64_t)((ks >> 2) * (MPAD * 8) + (ks & 3) * 2);
-                    mma_ts(dcol, acol0 + ks * 8, bdesc, IDESC, (rb_start && ks == 0) ? 0u : 1u);
-                }
+                // fully unrolled: every operand is the unit's base plus a constant, so the issuing
+                // thread (which shares its SM sub-partition with two busy dequant warps) spends as
+                // few issue slots as possible per instruction
+                mma_ts(dcol, acol0, bdesc0, IDESC, rb_start ? 0u : 1u);
+#pragma unroll
+                for (int ks = 1; ks < KC / 16; ++ks)
+                    mma_ts_acc(dcol, acol0 + ks * 8, bdesc0 + (uint64_t)((ks >> 2) * (MPAD * 8) + (ks & 3) * 2), IDESC);
                 tc_commit(&aempty[ab]);
                 tc_commit(&empty[s]);
                 const bool rb_end = (c == CH - 1) || (u == u1 - 1);
