@@ -81,7 +81,7 @@ def kernel_source_hash():
     h = hashlib.sha256()
     d = os.path.join(ROOT, "gemm_uq_gb300", "csrc")
     for name in sorted(os.listdir(d)):
-        if name.startswith("uq_gemv") or name == "uq_common.cuh":
+        if name in ("uq_gemv.cuh", "uq_common.cuh"):             # the GEMV kernels' own sources
             with open(os.path.join(d, name), "rb") as f:
                 h.update(f.read())
     return h.hexdigest()[:16]

@@ -16,13 +16,15 @@ int gemv_grid(GemvArgs& a, int fmt, int sms) {
     a.cta_rows = 0;
     if (!gemv_is_mma(fmt)) return (a.P + GEMV_WARPS - 1) / GEMV_WARPS;
     // Whole row blocks per CTA need no second pass; take them when no warp gets more tiles than
-    // under the stream-K split (the workers are strided over the CTAs, so every SM is used).
+    // under the stream-K split and either the busiest CTA streams at most ~6 % more bytes than the
+    // average one (bandwidth-bound shapes) or no warp has more than one tile (latency-bound ones).
     const int W = gemv_warps(fmt);
     const int G = a.NB < sms ? a.NB : sms;
     const long long rbs = (a.NB + G - 1) / G;
     const long long per_warp_rows = (rbs * a.KB + W - 1) / W;
     const long long per_warp_split = (a.T + a.P - 1) / a.P;
-    if (G > 0 && per_warp_rows <= per_warp_split) {
+    const bool even = rbs * G * 100 <= (long long)a.NB * 106;
+    if (G > 0 && per_warp_rows <= per_warp_split && (even || per_warp_rows <= 1)) {
         a.cta_rows = 1;
         return G;
     }
@@ -42,16 +44,29 @@ __global__ void __launch_bounds__(256) gemv_split_reduce(const GemvArgs a) {
     const long long total = (long long)a.NB * RB * M;
     for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
          e += (long long)gridDim.x * blockDim.x) {
-        const int nb = (int)(e / (RB * M));
-        const int rm = (int)(e % (RB * M));                 // r * M + m
+        const bool e32 = total < (1ll << 31);
+        const int nb = e32 ? (int)((unsigned)e / (unsigned)(RB * M)) : (int)(e / (RB * M));
+        const int rm = e32 ? (int)((unsigned)e % (unsigned)(RB * M)) : (int)(e % (RB * M));   // r * M + m
         const int n = nb * RB + rm / M, m = rm % M;
         if (n >= a.N) continue;
         const long long tf = (long long)nb * KB;
-        const int wf = worker_of(tf, a.T, a.P), wl = worker_of(tf + KB - 1, a.T, a.P);
+        // worker ranges: 32-bit arithmetic when T * (P + 1) fits (every practical shape)
+        const bool small = a.T * (long long)(a.P + 1) < (1ll << 31);
+        int wf, wl;
+        if (small) {
+            const unsigned T = (unsigned)a.T, P = (unsigned)a.P, t = (unsigned)tf;
+            wf = (int)(((t + 1) * P - 1) / T);
+            wl = (int)(((t + KB) * P - 1) / T);
+        } else {
+            wf = worker_of(tf, a.T, a.P);
+            wl = worker_of(tf + KB - 1, a.T, a.P);
+        }
         if (wf == wl) continue;                            // one worker covered it and stored y
         float sum = 0.f;
         for (int w2 = wf; w2 <= wl; ++w2) {
-            const int nb2 = (int)(range_begin(w2, a.T, a.P) / KB);
+            const long long b2 = small ? (long long)((unsigned)w2 * (unsigned)a.T / (unsigned)a.P)
+                                       : range_begin(w2, a.T, a.P);
+            const int nb2 = small ? (int)((unsigned)b2 / (unsigned)KB) : (int)(b2 / KB);
             const int slot2 = 2 * w2 + (nb == nb2 ? 0 : 1);
             sum += a.partials[(long long)slot2 * RB * M + rm];
         }
