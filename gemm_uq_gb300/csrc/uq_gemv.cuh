@@ -162,10 +162,13 @@ struct MetaConst {
     bool aligned;     // every tile row's scale slice is 16-byte aligned and a multiple of 16 bytes
 };
 
-// Issue the copies of tile t into stage buffer `st` (all lanes take part).
+// Issue the copies of tile t into stage buffer `st` (all lanes take part).  XB > 0: the tile's
+// slice of x (XB bytes per row, rows of M) follows the metadata; with x_now the slice is copied
+// here and the arrival made, otherwise only the codes' bytes are expected and issue_x_slice()
+// arrives later (the weights may stream before x, which the previous kernel writes, is ready).
 template <int FMT>
 __device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, const MetaConst& mc, int nb, int kb,
-                                           uint8_t* st, uint64_t* bar, int lane) {
+                                           uint8_t* st, uint64_t* bar, int lane, int XB = 0, bool x_now = true) {
     using F = GemvFmt<FMT>;
     const int n0 = nb * RB;
     const int rows = (a.N - n0) < RB ? (a.N - n0) : RB;            // rows with metadata
@@ -220,9 +223,30 @@ __device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, c
     if (lane == 0) {
         const uint32_t bytes = (uint32_t)L.tile_bytes(kb);
         fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar, bytes);
+        if (XB == 0) {
+            mbar_arrive_expect_tx(bar, bytes);
+        } else {
+            const int kx = (a.K - kb * F::KT) < F::KT ? (a.K - kb * F::KT) : F::KT;   // k of the slice inside K
+            mbar_expect_tx(bar, bytes);
+            if (x_now) {
+                mbar_arrive_expect_tx(bar, (uint32_t)(a.M * kx * 2));
+                for (int m = 0; m < a.M; ++m)
+                    bulk_g2s(st + F::STAGE_BYTES + m * XB, a.x + (long long)m * a.ldx + (long long)kb * F::KT,
+                             (uint32_t)(kx * 2), bar);
+            }
+        }
         bulk_g2s_stream(st, a.wq + L.tile_offset(nb, kb), bytes, bar, l2_evict_first_policy());
     }
+}
+// the x slice of a tile whose codes issue_tile(..., x_now = false) requested (lane 0 only)
+template <int FMT>
+__device__ __forceinline__ void issue_x_slice(const GemvArgs& a, int kb, uint8_t* st, uint64_t* bar, int XB) {
+    using F = GemvFmt<FMT>;
+    const int kx = (a.K - kb * F::KT) < F::KT ? (a.K - kb * F::KT) : F::KT;
+    mbar_arrive_expect_tx(bar, (uint32_t)(a.M * kx * 2));
+    for (int m = 0; m < a.M; ++m)
+        bulk_g2s(st + F::STAGE_BYTES + m * XB, a.x + (long long)m * a.ldx + (long long)kb * F::KT, (uint32_t)(kx * 2),
+                 bar);
 }
 
 // Pointers to row r's staged scales (fp16) and zero points for tile kb: the staged words start
@@ -656,7 +680,18 @@ template <int FMT> struct MmaCfg {
 // B-fragment loads touch into different banks
 __host__ __device__ inline size_t gemv_mma_x_stride(int Kp) { return (size_t)Kp * 2 + 32; }
 
-__host__ __device__ inline GemvSmem gemv_mma_smem_plan(int fmt, int K, int group, int M, bool x_in_smem) {
+// Where the mma GEMV reads x (template parameter XM):
+//   MMA_X_GLOBAL  straight from global memory (through L1);
+//   MMA_X_WHOLE   all of x copied into shared memory once per CTA, before the first tile;
+//   MMA_X_SLICE   each stage carries its tile's slice of x (KT k of every row), copied with the
+//                 codes: no prologue copy to wait for, and a warp reads only the x it uses.
+constexpr int MMA_X_GLOBAL = 0, MMA_X_WHOLE = 1, MMA_X_SLICE = 2;
+// bytes per row of a staged x slice (row padding as for the whole x when there are several rows)
+__host__ __device__ inline int gemv_mma_xslice_stride(int fmt, int M) {
+    return M <= 1 ? fmt_kt(fmt) * 2 : fmt_kt(fmt) * 2 + 32;
+}
+
+__host__ __device__ inline GemvSmem gemv_mma_smem_plan(int fmt, int K, int group, int M, int xm) {
     int stage = 0, warps = 0, kc = fmt_kc(fmt);
     switch (fmt) {
         case UQ_INT4_SYM: stage = GemvFmt<UQ_INT4_SYM>::STAGE_BYTES; warps = MmaCfg<UQ_INT4_SYM>::WARPS; break;
@@ -667,17 +702,25 @@ __host__ __device__ inline GemvSmem gemv_mma_smem_plan(int fmt, int K, int group
     const int stages = 2;
     const int Kp = (K + kc - 1) / kc * kc;
     (void)group;
+    if (xm == MMA_X_SLICE) stage += M * gemv_mma_xslice_stride(fmt, M);
     GemvSmem p;
     p.bars = (size_t)warps * stages * stage;
     p.lut = p.bars + (size_t)(warps * stages + 1) * 8;              // + the x mbarrier
     p.sx = p.lut + 64;
     p.ps = p.sx;                                                    // [warps][2][16 rows][8 columns] fp32
     p.x = (p.ps + (size_t)warps * 2 * RB * 8 * 4 + 127) / 128 * 128;
-    p.total = p.x + (x_in_smem ? (size_t)M * gemv_mma_x_stride(Kp) : 0);
+    p.total = p.x + (xm == MMA_X_WHOLE ? (size_t)M * gemv_mma_x_stride(Kp) : 0);
     return p;
 }
+// x slices for one or two rows (a slice of 8 rows would crowd the stages out of shared memory),
+// else the whole x if it fits, else global memory
+__host__ __device__ inline int gemv_mma_xmode(int fmt, int K, int group, int M) {
+    if (M <= 2 && gemv_mma_smem_plan(fmt, K, group, M, MMA_X_SLICE).total <= 227 * 1024) return MMA_X_SLICE;
+    if (gemv_mma_smem_plan(fmt, K, group, M, MMA_X_WHOLE).total <= 227 * 1024) return MMA_X_WHOLE;
+    return MMA_X_GLOBAL;
+}
 
-template <int FMT, int GB, bool XS>
+template <int FMT, int GB, int XM>
 __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(const GemvArgs a) {
     using F = GemvFmt<FMT>;
     constexpr int KT = F::KT, S = MmaCfg<FMT>::STAGES, W = MmaCfg<FMT>::WARPS;
@@ -687,7 +730,10 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
     constexpr int BPCH = F::BPC;                                    // 16-k blocks per 512-byte chunk
     extern __shared__ __align__(128) uint8_t smem[];
     const int M = a.M;
-    const GemvSmem plan = gemv_mma_smem_plan(FMT, a.K, a.group, M, XS);
+    constexpr bool XS = XM == MMA_X_WHOLE;
+    const GemvSmem plan = gemv_mma_smem_plan(FMT, a.K, a.group, M, XM);
+    const int XB = gemv_mma_xslice_stride(FMT, M);                 // x slice: bytes per row
+    const int SB = F::STAGE_BYTES + (XM == MMA_X_SLICE ? M * XB : 0);   // bytes per stage
     uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + plan.bars);
     uint8_t* xs = smem + plan.x;
     float* cpart = reinterpret_cast<float*>(smem + plan.ps);
@@ -705,7 +751,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
     const long long Tc = (long long)(rb1 - rb0) * L.KB;             // the CTA's tiles (cta_rows)
     const int w = cta_rows ? warp : (int)(blockIdx.x + gridDim.x * warp);
     const bool has_work = cta_rows ? true : w < a.P;
-    uint8_t* ring = smem + (size_t)warp * S * F::STAGE_BYTES;
+    uint8_t* ring = smem + (size_t)warp * S * SB;
     uint64_t* bars = bars_all + warp * S;
     const long long t0 = cta_rows ? (long long)rb0 * L.KB + range_begin(warp, Tc, W)
                                   : (has_work ? range_begin(w, a.T, a.P) : 0);
@@ -737,12 +783,29 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
     int inb = (int)(t0 / L.KB), ikb = (int)(t0 % L.KB);
     int issued = 0;
     auto issue_next = [&]() {
-        issue_tile<FMT>(a, L, mc, inb, ikb, ring + issued * F::STAGE_BYTES, &bars[issued], lane);
+        issue_tile<FMT>(a, L, mc, inb, ikb, ring + issued * SB, &bars[issued], lane, XM == MMA_X_SLICE ? XB : 0);
         if (++ikb == L.KB) { ikb = 0; ++inb; }
         ++issued;
     };
-    if (a.overlap && has_work && t0 < t1) issue_next();
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if constexpr (XM == MMA_X_SLICE) {
+        // with launch overlap every stage's codes are requested before the wait for the previous
+        // kernel, and their x slices after it
+        if (a.overlap && has_work) {
+            for (; issued < S && t0 + issued < t1; ++issued) {
+                issue_tile<FMT>(a, L, mc, inb, ikb, ring + issued * SB, &bars[issued], lane, XB, false);
+                if (++ikb == L.KB) { ikb = 0; ++inb; }
+            }
+        }
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (a.overlap && has_work && lane == 0) {
+            const int kb0 = (int)(t0 % L.KB);
+            for (int j = 0; j < issued; ++j)
+                issue_x_slice<FMT>(a, (kb0 + j) % L.KB, ring + j * SB, &bars[j], XB);
+        }
+    } else {
+        if (a.overlap && has_work && t0 < t1) issue_next();
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
     if constexpr (XS) {
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(xbar, (uint32_t)(M * a.K * 2));
@@ -773,7 +836,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
         const int s = it % S;
         const uint32_t parity = (uint32_t)((it / S) & 1);
         const int n0 = nb * RB;
-        uint8_t* st = ring + s * F::STAGE_BYTES;
+        uint8_t* st = ring + s * SB;
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], parity, a.fault, FAULT_GEMV_WAIT))) {
             for (int j = 1; j < S && t + j < t1; ++j) {
                 const int sj = (it + j) % S;
@@ -788,7 +851,8 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
             rp[0] = row_ptrs<FMT>(st, mc, g, n0 + g, kb);
             rp[1] = row_ptrs<FMT>(st, mc, g + 8, n0 + g + 8, kb);
         }
-        const uint8_t* xt = xrow + (size_t)kb * KT * 2;             // x of the tile's first k
+        const uint8_t* xt = (XM == MMA_X_SLICE) ? st + F::STAGE_BYTES + mrow * XB + 8 * c
+                                                : xrow + (size_t)kb * KT * 2;   // x of the tile's first k
         const uint16_t* xgt = xgrow + (long long)kb * KT;
 
         auto group_step = [&](const int gg) {
@@ -814,7 +878,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
             }
             // B fragments: x at k = 16 blk + 4c .. +3 of row mrow (8 bytes per block)
             uint32_t bx[GB], by[GB];
-            if constexpr (XS) {
+            if constexpr (XM != MMA_X_GLOBAL) {
 #pragma unroll
                 for (int j = 0; j < GB; ++j) {
                     const uint2 v = *reinterpret_cast<const uint2*>(xt + (gg * GB + j) * 32);
@@ -890,7 +954,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
         }
         __syncwarp();
         if (t + S < t1) {
-            issue_tile<FMT>(a, L, mc, inb, ikb, st, &bars[s], lane);
+            issue_tile<FMT>(a, L, mc, inb, ikb, st, &bars[s], lane, XM == MMA_X_SLICE ? XB : 0);
             if (++ikb == L.KB) { ikb = 0; ++inb; }
         }
 
@@ -951,14 +1015,12 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
 inline bool gemv_is_mma(int fmt) {
     return fmt == UQ_INT4_SYM || fmt == UQ_INT4_ASYM || fmt == UQ_INT2_ASYM || fmt == UQ_K4;
 }
-inline GemvSmem gemv_any_plan(int fmt, int K, int group, int M, bool xs) {
-    return gemv_is_mma(fmt) ? gemv_mma_smem_plan(fmt, K, group, M, xs) : gemv_smem_plan(fmt, K, group, M, xs);
-}
 inline bool gemv_x_in_smem(int fmt, int K, int group, int M) {
-    return gemv_any_plan(fmt, K, group, M, true).total <= 227 * 1024;
+    return gemv_smem_plan(fmt, K, group, M, true).total <= 227 * 1024;
 }
 inline size_t gemv_smem_bytes_impl(int fmt, int K, int group, int M) {
-    return gemv_any_plan(fmt, K, group, M, gemv_x_in_smem(fmt, K, group, M)).total;
+    if (gemv_is_mma(fmt)) return gemv_mma_smem_plan(fmt, K, group, M, gemv_mma_xmode(fmt, K, group, M)).total;
+    return gemv_smem_plan(fmt, K, group, M, gemv_x_in_smem(fmt, K, group, M)).total;
 }
 inline int gemv_warps_impl(int fmt) {
     switch (fmt) {
@@ -1011,16 +1073,16 @@ cudaError_t launch_xs(const GemvArgs& a, int grid, cudaStream_t st) {
 }  // namespace gemv_detail
 
 namespace gemv_detail {
-template <int FMT, int GB, bool XS>
+template <int FMT, int GB, int XM>
 cudaError_t launch_mma(const GemvArgs& a, int grid, cudaStream_t st) {
     static bool configured[64] = {};
-    const size_t smem = gemv_mma_smem_plan(FMT, a.K, a.group, a.M, XS).total;
+    const size_t smem = gemv_mma_smem_plan(FMT, a.K, a.group, a.M, XM).total;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(gemv_mma_kernel<FMT, GB, XS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(gemv_mma_kernel<FMT, GB, XM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  227 * 1024);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
@@ -1039,17 +1101,20 @@ cudaError_t launch_mma(const GemvArgs& a, int grid, cudaStream_t st) {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, gemv_mma_kernel<FMT, GB, XS>, a2);
+        e = cudaLaunchKernelEx(&cfg, gemv_mma_kernel<FMT, GB, XM>, a2);
         if (e != cudaSuccess) return e;
     } else {
-        gemv_mma_kernel<FMT, GB, XS><<<grid, threads, smem, st>>>(a2);
+        gemv_mma_kernel<FMT, GB, XM><<<grid, threads, smem, st>>>(a2);
     }
     return cudaGetLastError();
 }
 template <int FMT, int GB>
 cudaError_t launch_mma_xs(const GemvArgs& a, int grid, cudaStream_t st) {
-    if (gemv_x_in_smem(FMT, a.K, a.group, a.M)) return launch_mma<FMT, GB, true>(a, grid, st);
-    return launch_mma<FMT, GB, false>(a, grid, st);
+    switch (gemv_mma_xmode(FMT, a.K, a.group, a.M)) {
+        case MMA_X_SLICE: return launch_mma<FMT, GB, MMA_X_SLICE>(a, grid, st);
+        case MMA_X_WHOLE: return launch_mma<FMT, GB, MMA_X_WHOLE>(a, grid, st);
+        default: return launch_mma<FMT, GB, MMA_X_GLOBAL>(a, grid, st);
+    }
 }
 }  // namespace gemv_detail
 
