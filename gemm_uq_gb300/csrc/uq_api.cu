@@ -165,7 +165,7 @@ uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const 
     long long P = (long long)ds.sms * warps;
     if (P > T) P = T;
     Workspace* ws = nullptr;
-    uq_status s = workspace(dev, st, uq::gemv_partials_floats((int)P, Mb) * sizeof(float),
+    uq_status s = workspace(dev, st, uq::gemv_partials_floats(fmt, T, (int)P, Mb) * sizeof(float),
                             (size_t)L.NB * sizeof(unsigned int), &ws);
     if (s != UQ_OK) return s;
     uq::GemvArgs a;

@@ -24,52 +24,37 @@ int gemv_grid(GemvArgs& a, int fmt, int sms) {
     const long long per_warp_rows = (rbs * a.KB + W - 1) / W;
     const long long per_warp_split = (a.T + a.P - 1) / a.P;
     const bool even = rbs * G * 100 <= (long long)a.NB * 106;
-    if (G > 0 && per_warp_rows <= per_warp_split && (even || per_warp_rows <= 1)) {
+    if (G > 0 && per_warp_rows <= MMA_TPW && per_warp_rows <= per_warp_split && (even || per_warp_rows <= 1)) {
         a.cta_rows = 1;
         return G;
     }
     return a.P < sms ? a.P : sms;
 }
-size_t gemv_partials_floats(int P, int M) { return gemv_partials_floats_impl(P, M); }
+size_t gemv_partials_floats(int fmt, long long T, int P, int M) {
+    // mma GEMV: one 16-row slot per tile (k-major tiles, summed over k by the second pass);
+    // CUDA-core GEMV: two slots per worker (the first and last row block of its range)
+    return gemv_is_mma(fmt) ? (size_t)T * RB * M : gemv_partials_floats_impl(P, M);
+}
 
-// Second pass of the mma GEMV's split-K: for every row block that several workers share, sum their
-// partials in worker order (fixed, so results are bit-reproducible) and store y.  Launched right
-// after the GEMV with programmatic stream serialization: it becomes resident early and its
-// griddepcontrol.wait returns once the GEMV grid has finished and its stores are visible, so the
-// GEMV itself needs no fence, ticket or waiting between workers.
+// Second pass of the mma GEMV when workers split the matrix's tiles (k-major, so every tile's
+// partial sums have a slot of their own): y[m][n] = the sum over k tiles, in k order (fixed, so
+// results are bit-reproducible).  Launched right after the GEMV with programmatic stream
+// serialization: it becomes resident early and its griddepcontrol.wait returns once the GEMV grid
+// has finished and its stores are visible, so the GEMV itself needs no fence or ticket.
 __global__ void __launch_bounds__(256) gemv_split_reduce(const GemvArgs a) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int M = a.M, KB = a.KB;
-    const long long total = (long long)a.NB * RB * M;
+    const int M = a.M, KB = a.KB, RM = RB * M;
+    const long long total = (long long)a.NB * RM;
+    const long long kstride = (long long)a.NB * RM;                 // floats between k tiles
     for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
          e += (long long)gridDim.x * blockDim.x) {
-        const bool e32 = total < (1ll << 31);
-        const int nb = e32 ? (int)((unsigned)e / (unsigned)(RB * M)) : (int)(e / (RB * M));
-        const int rm = e32 ? (int)((unsigned)e % (unsigned)(RB * M)) : (int)(e % (RB * M));   // r * M + m
+        const int nb = (int)(e / RM), rm = (int)(e % RM);           // rm = r * M + m
         const int n = nb * RB + rm / M, m = rm % M;
         if (n >= a.N) continue;
-        const long long tf = (long long)nb * KB;
-        // worker ranges: 32-bit arithmetic when T * (P + 1) fits (every practical shape)
-        const bool small = a.T * (long long)(a.P + 1) < (1ll << 31);
-        int wf, wl;
-        if (small) {
-            const unsigned T = (unsigned)a.T, P = (unsigned)a.P, t = (unsigned)tf;
-            wf = (int)(((t + 1) * P - 1) / T);
-            wl = (int)(((t + KB) * P - 1) / T);
-        } else {
-            wf = worker_of(tf, a.T, a.P);
-            wl = worker_of(tf + KB - 1, a.T, a.P);
-        }
-        if (wf == wl) continue;                            // one worker covered it and stored y
+        const float* p = a.partials + e;                            // k tile 0 of (nb, r, m)
         float sum = 0.f;
-        for (int w2 = wf; w2 <= wl; ++w2) {
-            const long long b2 = small ? (long long)((unsigned)w2 * (unsigned)a.T / (unsigned)a.P)
-                                       : range_begin(w2, a.T, a.P);
-            const int nb2 = small ? (int)((unsigned)b2 / (unsigned)KB) : (int)(b2 / KB);
-            const int slot2 = 2 * w2 + (nb == nb2 ? 0 : 1);
-            sum += a.partials[(long long)slot2 * RB * M + rm];
-        }
+        for (int kb = 0; kb < KB; ++kb) sum += p[kb * kstride];
         a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
     }
 }

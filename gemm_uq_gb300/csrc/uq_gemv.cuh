@@ -162,13 +162,10 @@ struct MetaConst {
     bool aligned;     // every tile row's scale slice is 16-byte aligned and a multiple of 16 bytes
 };
 
-// Issue the copies of tile t into stage buffer `st` (all lanes take part).  XB > 0: the tile's
-// slice of x (XB bytes per row, rows of M) follows the metadata; with x_now the slice is copied
-// here and the arrival made, otherwise only the codes' bytes are expected and issue_x_slice()
-// arrives later (the weights may stream before x, which the previous kernel writes, is ready).
+// Issue the copies of tile t into stage buffer `st` (all lanes take part).
 template <int FMT>
 __device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, const MetaConst& mc, int nb, int kb,
-                                           uint8_t* st, uint64_t* bar, int lane, int XB = 0, bool x_now = true) {
+                                           uint8_t* st, uint64_t* bar, int lane) {
     using F = GemvFmt<FMT>;
     const int n0 = nb * RB;
     const int rows = (a.N - n0) < RB ? (a.N - n0) : RB;            // rows with metadata
@@ -223,30 +220,9 @@ __device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, c
     if (lane == 0) {
         const uint32_t bytes = (uint32_t)L.tile_bytes(kb);
         fence_proxy_async_smem();
-        if (XB == 0) {
-            mbar_arrive_expect_tx(bar, bytes);
-        } else {
-            const int kx = (a.K - kb * F::KT) < F::KT ? (a.K - kb * F::KT) : F::KT;   // k of the slice inside K
-            mbar_expect_tx(bar, bytes);
-            if (x_now) {
-                mbar_arrive_expect_tx(bar, (uint32_t)(a.M * kx * 2));
-                for (int m = 0; m < a.M; ++m)
-                    bulk_g2s(st + F::STAGE_BYTES + m * XB, a.x + (long long)m * a.ldx + (long long)kb * F::KT,
-                             (uint32_t)(kx * 2), bar);
-            }
-        }
+        mbar_arrive_expect_tx(bar, bytes);
         bulk_g2s_stream(st, a.wq + L.tile_offset(nb, kb), bytes, bar, l2_evict_first_policy());
     }
-}
-// the x slice of a tile whose codes issue_tile(..., x_now = false) requested (lane 0 only)
-template <int FMT>
-__device__ __forceinline__ void issue_x_slice(const GemvArgs& a, int kb, uint8_t* st, uint64_t* bar, int XB) {
-    using F = GemvFmt<FMT>;
-    const int kx = (a.K - kb * F::KT) < F::KT ? (a.K - kb * F::KT) : F::KT;
-    mbar_arrive_expect_tx(bar, (uint32_t)(a.M * kx * 2));
-    for (int m = 0; m < a.M; ++m)
-        bulk_g2s(st + F::STAGE_BYTES + m * XB, a.x + (long long)m * a.ldx + (long long)kb * F::KT, (uint32_t)(kx * 2),
-                 bar);
 }
 
 // Pointers to row r's staged scales (fp16) and zero points for tile kb: the staged words start
@@ -666,15 +642,22 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
 // K4 uses its 32-weight sub-blocks, GB = 2).  M (1..8) is a runtime value: the instruction always
 // computes 8 columns, so the work per weight does not depend on it.
 //
-// Per 16 x 16 block of weights a lane issues: its share of one 16-byte code load (a quarter or an
-// eighth), four lop3 (three after a shift) to form the A fragment, half a 16-byte load of x (the x
-// rows are stored pair-interleaved so one load gives the B fragments of two blocks) and the mma.
-// Per group: two fp32 FMAs per accumulator with the group's scale and zero term.  A tile whose
-// groups all lie inside K (every tile but a ragged last one) runs a fully unrolled group loop.
+// Per 16 x 16 block of weights a lane issues its share of a 16-byte code load, four lop3 (three
+// after a shift) to form the A fragment, one 8-byte load of x and the mma.  Per group: two fp32
+// FMAs per accumulator with the group's scale and zero-point term, the latter using the group's
+// sum of x.
+//
+// Tile order is k-major: tile i of a range is (k tile i / R, row block i % R) for R row blocks, so
+// a warp's consecutive tiles share their k tile.  The sums of x over the k tile's groups (an mma
+// chain with A = 1) are computed once per run of equal k tile instead of once per tile, and with
+// one or two rows of x the warp copies only that k tile's slice of x, once per run.  Every tile's
+// partial sums are stored (shared memory when the CTA owns whole row blocks, global memory
+// otherwise) and summed over the k tiles in a fixed order afterwards.
 template <int FMT> struct MmaCfg {
     static constexpr int WARPS = (FMT == UQ_INT2_ASYM) ? 6 : 8;    // workers per CTA
     static constexpr int STAGES = 2;                               // tiles in flight per worker
 };
+constexpr int MMA_TPW = 4;        // tiles per warp at most when the CTA owns whole row blocks
 
 // bytes per row of x in shared memory: 32 bytes of padding put the four rows a half-warp's 8-byte
 // B-fragment loads touch into different banks
@@ -683,16 +666,19 @@ __host__ __device__ inline size_t gemv_mma_x_stride(int Kp) { return (size_t)Kp 
 // Where the mma GEMV reads x (template parameter XM):
 //   MMA_X_GLOBAL  straight from global memory (through L1);
 //   MMA_X_WHOLE   all of x copied into shared memory once per CTA, before the first tile;
-//   MMA_X_SLICE   each stage carries its tile's slice of x (KT k of every row), copied with the
-//                 codes: no prologue copy to wait for, and a warp reads only the x it uses.
+//   MMA_X_SLICE   each warp copies the slice of x of its current k tile (KT k of every row) into a
+//                 buffer of its own, the next run's slice while the current run computes.
 constexpr int MMA_X_GLOBAL = 0, MMA_X_WHOLE = 1, MMA_X_SLICE = 2;
-// bytes per row of a staged x slice (row padding as for the whole x when there are several rows)
+// bytes per row of an x slice (row padding as for the whole x when there are several rows)
 __host__ __device__ inline int gemv_mma_xslice_stride(int fmt, int M) {
     return M <= 1 ? fmt_kt(fmt) * 2 : fmt_kt(fmt) * 2 + 32;
 }
 
+// Shared memory: rings [warps][stages][stage] | ring and x mbarriers | sums of x [warps][groups of
+// a tile][8] | partial sums [warps][MMA_TPW][16][8] | x (whole, or [warps][2][M] slices)
 __host__ __device__ inline GemvSmem gemv_mma_smem_plan(int fmt, int K, int group, int M, int xm) {
-    int stage = 0, warps = 0, kc = fmt_kc(fmt);
+    int stage = 0, warps = 0;
+    const int kc = fmt_kc(fmt), kt = fmt_kt(fmt);
     switch (fmt) {
         case UQ_INT4_SYM: stage = GemvFmt<UQ_INT4_SYM>::STAGE_BYTES; warps = MmaCfg<UQ_INT4_SYM>::WARPS; break;
         case UQ_INT4_ASYM: stage = GemvFmt<UQ_INT4_ASYM>::STAGE_BYTES; warps = MmaCfg<UQ_INT4_ASYM>::WARPS; break;
@@ -701,19 +687,19 @@ __host__ __device__ inline GemvSmem gemv_mma_smem_plan(int fmt, int K, int group
     }
     const int stages = 2;
     const int Kp = (K + kc - 1) / kc * kc;
-    (void)group;
-    if (xm == MMA_X_SLICE) stage += M * gemv_mma_xslice_stride(fmt, M);
+    const int gs = (fmt == UQ_K4) ? 32 : group;
     GemvSmem p;
     p.bars = (size_t)warps * stages * stage;
-    p.lut = p.bars + (size_t)(warps * stages + 1) * 8;              // + the x mbarrier
-    p.sx = p.lut + 64;
-    p.ps = p.sx;                                                    // [warps][2][16 rows][8 columns] fp32
-    p.x = (p.ps + (size_t)warps * 2 * RB * 8 * 4 + 127) / 128 * 128;
-    p.total = p.x + (xm == MMA_X_WHOLE ? (size_t)M * gemv_mma_x_stride(Kp) : 0);
+    p.lut = p.bars + (size_t)(warps * stages + 2 * warps + 1) * 8;  // ring, x-slice and whole-x mbarriers
+    p.sx = (p.lut + 15) / 16 * 16;
+    p.ps = p.sx + (size_t)warps * (kt / gs) * 8 * 4;
+    p.x = (p.ps + (size_t)warps * MMA_TPW * RB * 8 * 4 + 127) / 128 * 128;
+    p.total = p.x;
+    if (xm == MMA_X_WHOLE) p.total += (size_t)M * gemv_mma_x_stride(Kp);
+    if (xm == MMA_X_SLICE) p.total += (size_t)warps * 2 * M * gemv_mma_xslice_stride(fmt, M);
     return p;
 }
-// x slices for one or two rows (a slice of 8 rows would crowd the stages out of shared memory),
-// else the whole x if it fits, else global memory
+// x slices for one or two rows, else the whole x if it fits, else global memory
 __host__ __device__ inline int gemv_mma_xmode(int fmt, int K, int group, int M) {
     if (M <= 2 && gemv_mma_smem_plan(fmt, K, group, M, MMA_X_SLICE).total <= 227 * 1024) return MMA_X_SLICE;
     if (gemv_mma_smem_plan(fmt, K, group, M, MMA_X_WHOLE).total <= 227 * 1024) return MMA_X_WHOLE;
@@ -728,35 +714,45 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
     constexpr int GPT = KT / GS;                                    // groups per full tile row
     constexpr int WPG = (FMT == UQ_INT2_ASYM) ? GB / 2 : GB;        // code words per lane per group
     constexpr int BPCH = F::BPC;                                    // 16-k blocks per 512-byte chunk
+    constexpr bool XS = XM == MMA_X_WHOLE;
+    constexpr uint32_t ONES = 0x3F803F80u;                          // bf16 pair (1, 1)
     extern __shared__ __align__(128) uint8_t smem[];
     const int M = a.M;
-    constexpr bool XS = XM == MMA_X_WHOLE;
     const GemvSmem plan = gemv_mma_smem_plan(FMT, a.K, a.group, M, XM);
     const int XB = gemv_mma_xslice_stride(FMT, M);                 // x slice: bytes per row
-    const int SB = F::STAGE_BYTES + (XM == MMA_X_SLICE ? M * XB : 0);   // bytes per stage
     uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + plan.bars);
     uint8_t* xs = smem + plan.x;
     float* cpart = reinterpret_cast<float*>(smem + plan.ps);
-    uint64_t* xbar = bars_all + W * S;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const Layout L(a.N, a.K, FMT);
-    // Work split.  cta_rows: CTA b owns row blocks [rb0, rb1) and its W warps split those tiles
-    // evenly (range_begin over the CTA's tiles); otherwise worker w = CTA + grid * warp (strided, so a
-    // small matrix still spreads over every SM) owns an equal share of all tiles.
+    uint8_t* ring = smem + (size_t)warp * S * F::STAGE_BYTES;
+    uint64_t* bars = bars_all + warp * S;
+    uint64_t* xsl_bar = bars_all + W * S + 2 * warp;               // this warp's two x-slice buffers
+    uint64_t* xbar = bars_all + W * S + 2 * W;                      // the whole x
+    float* sxw = reinterpret_cast<float*>(smem + plan.sx) + warp * GPT * 8;   // sums of x of the run's k tile
+    uint8_t* xsl = xs + (size_t)warp * 2 * M * XB;                  // this warp's x-slice buffers
+
+    // Work split.  cta_rows: CTA b owns row blocks [rb0, rb1), R of them, and its W warps split the
+    // R * KB tiles evenly; otherwise worker w = CTA + grid * warp (strided, so a small matrix still
+    // spreads over every SM) owns an equal share of all NB * KB tiles.  Tile i -> (k tile i / R,
+    // row block i % R) with R = NB for the whole matrix.
     const bool cta_rows = a.cta_rows != 0;
     const int rb0 = cta_rows ? (int)((long long)blockIdx.x * a.NB / gridDim.x) : 0;
-    const int rb1 = cta_rows ? (int)((long long)(blockIdx.x + 1) * a.NB / gridDim.x) : 0;
-    const long long Tc = (long long)(rb1 - rb0) * L.KB;             // the CTA's tiles (cta_rows)
+    const int R = cta_rows ? (int)((long long)(blockIdx.x + 1) * a.NB / gridDim.x) - rb0 : a.NB;
+    const unsigned Tc = (unsigned)(R * L.KB);                       // the CTA's tiles (cta_rows; small)
     const int w = cta_rows ? warp : (int)(blockIdx.x + gridDim.x * warp);
     const bool has_work = cta_rows ? true : w < a.P;
-    uint8_t* ring = smem + (size_t)warp * S * SB;
-    uint64_t* bars = bars_all + warp * S;
-    const long long t0 = cta_rows ? (long long)rb0 * L.KB + range_begin(warp, Tc, W)
-                                  : (has_work ? range_begin(w, a.T, a.P) : 0);
-    const long long t1 = cta_rows ? (long long)rb0 * L.KB + range_begin(warp + 1, Tc, W)
-                                  : (has_work ? range_begin(w + 1, a.T, a.P) : 0);
+    const long long t0 = cta_rows ? (long long)(warp * Tc / W) : (has_work ? range_begin(w, a.T, a.P) : 0);
+    const long long t1 = cta_rows ? (long long)((warp + 1) * Tc / W) : (has_work ? range_begin(w + 1, a.T, a.P) : 0);
+    int ntl = (int)(t1 - t0);                                       // this warp's tiles
+    if (cta_rows && ntl > MMA_TPW) {                                // the host never splits this way
+        if (lane == 0) atomicOr(a.fault, FAULT_GEMV_SPLIT);
+        ntl = 0;
+    }
+    auto kb_of = [&](long long i) { return (int)(i / R); };
+    auto nb_of = [&](long long i) { return rb0 + (int)(i % R); };
     MetaConst mc;
     mc.G = a.K / a.group;
     mc.GT = KT / a.group;
@@ -765,14 +761,27 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
     mc.aligned = (a.K % (8 * a.group)) == 0 && (mc.GT % 8) == 0;
     const int G_all = a.K / GS;                                     // real scaling groups per row
     const size_t xstride = gemv_mma_x_stride(L.Kp);
+    const int kb_first = ntl > 0 ? kb_of(t0) : 0;
+    const int kb_last = ntl > 0 ? kb_of(t1 - 1) : -1;
 
-    // ---- prologue.  x (a few KB, written by the previous kernel) is requested ahead of the weights
-    // so it is not queued behind them; with launch overlap the first weight stage is streamed
-    // before the wait for the previous kernel instead, as the weights do not depend on it.
+    // x slice of k tile kb into buffer `slot` (lane 0)
+    auto issue_xslice = [&](int kb, int slot) {
+        const int kx = (a.K - kb * KT) < KT ? (a.K - kb * KT) : KT;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&xsl_bar[slot], (uint32_t)(M * kx * 2));
+        for (int m = 0; m < M; ++m)
+            bulk_g2s(xsl + (slot * M + m) * XB, a.x + (long long)m * a.ldx + (long long)kb * KT, (uint32_t)(kx * 2),
+                     &xsl_bar[slot]);
+    };
+
+    // ---- prologue.  The weights and their metadata are constant: with launch overlap they are
+    // requested before the wait for the previous kernel (which may write x); x after it.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (has_work && lane == 0) {
 #pragma unroll
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 33);
+        mbar_init(&xsl_bar[0], 1);
+        mbar_init(&xsl_bar[1], 1);
         fence_barrier_init();
     }
     if (XS && threadIdx.x == 0) {
@@ -780,31 +789,22 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
         fence_barrier_init();
     }
     __syncwarp();
-    int inb = (int)(t0 / L.KB), ikb = (int)(t0 % L.KB);
-    int issued = 0;
+    int issued = 0;                                                 // tiles requested so far
     auto issue_next = [&]() {
-        issue_tile<FMT>(a, L, mc, inb, ikb, ring + issued * SB, &bars[issued], lane, XM == MMA_X_SLICE ? XB : 0);
-        if (++ikb == L.KB) { ikb = 0; ++inb; }
+        const long long i = t0 + issued;
+        issue_tile<FMT>(a, L, mc, nb_of(i), kb_of(i), ring + (issued % S) * F::STAGE_BYTES, &bars[issued % S], lane);
         ++issued;
     };
+    if (a.overlap && has_work)
+        while (issued < S && issued < ntl) issue_next();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    int xissued = 0;                                                // x-slice runs requested so far
     if constexpr (XM == MMA_X_SLICE) {
-        // with launch overlap every stage's codes are requested before the wait for the previous
-        // kernel, and their x slices after it
-        if (a.overlap && has_work) {
-            for (; issued < S && t0 + issued < t1; ++issued) {
-                issue_tile<FMT>(a, L, mc, inb, ikb, ring + issued * SB, &bars[issued], lane, XB, false);
-                if (++ikb == L.KB) { ikb = 0; ++inb; }
-            }
+        if (has_work && ntl > 0 && lane == 0) {
+            issue_xslice(kb_first, 0);
+            if (kb_last > kb_first) issue_xslice(kb_first + 1, 1);
         }
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        if (a.overlap && has_work && lane == 0) {
-            const int kb0 = (int)(t0 % L.KB);
-            for (int j = 0; j < issued; ++j)
-                issue_x_slice<FMT>(a, (kb0 + j) % L.KB, ring + j * SB, &bars[j], XB);
-        }
-    } else {
-        if (a.overlap && has_work && t0 < t1) issue_next();
-        asm volatile("griddepcontrol.wait;" ::: "memory");
+        xissued = (ntl > 0) ? ((kb_last > kb_first) ? 2 : 1) : 0;
     }
     if constexpr (XS) {
         if (threadIdx.x == 0) {
@@ -814,7 +814,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
         __syncthreads();                            // no warp's weight copies ahead of x
     }
     if (has_work)
-        while (issued < S && t0 + issued < t1) issue_next();
+        while (issued < S && issued < ntl) issue_next();
     if constexpr (XS) {
         const int padw = (L.Kp - a.K) / 2;
         for (int e = threadIdx.x; e < M * padw; e += blockDim.x)
@@ -824,36 +824,72 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
     }
     if (!has_work) return;                          // (never in cta_rows mode: every warp meets the end barrier)
 
-    const int first_nb = (int)(t0 / L.KB);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};        // rows g + 8j, columns 2c + e
     const int mrow = g < M ? g : M - 1;          // B rows beyond M repeat a real row; their D columns are unused
-    const uint8_t* xrow = xs + mrow * xstride + 8 * c;
     const uint16_t* xgrow = a.x + (long long)mrow * a.ldx + 4 * c;
-    int nb = (int)(t0 / L.KB), kb = (int)(t0 % L.KB);
+    int cur_kb = -1, run = -1;
+    const uint8_t* xt = nullptr;                 // this lane's x at the current k tile's first k
+    const uint16_t* xgt = xgrow;
 
-    for (long long t = t0; t < t1; ++t) {
-        const int it = (int)(t - t0);
-        const int s = it % S;
-        const uint32_t parity = (uint32_t)((it / S) & 1);
+    for (int li = 0; li < ntl; ++li) {
+        const long long i = t0 + li;
+        const int kb = kb_of(i), nb = nb_of(i);
         const int n0 = nb * RB;
-        uint8_t* st = ring + s * SB;
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], parity, a.fault, FAULT_GEMV_WAIT))) {
-            for (int j = 1; j < S && t + j < t1; ++j) {
-                const int sj = (it + j) % S;
-                mbar_wait_bounded(&bars[sj], (uint32_t)(((it + j) / S) & 1), a.fault, FAULT_GEMV_WAIT);
-            }
-            break;
-        }
         const int gi0 = kb * GPT;
         const int ng = (G_all - gi0) < GPT ? (G_all - gi0) : GPT;   // groups of the tile inside K
+        if (kb != cur_kb) {
+            // a new run of tiles at k tile kb: its x, then the sums of x over its groups
+            cur_kb = kb;
+            ++run;
+            if constexpr (XM == MMA_X_SLICE) {
+                const int slot = run & 1;
+                bool ok = mbar_wait_bounded(&xsl_bar[slot], (uint32_t)((run >> 1) & 1), a.fault, FAULT_GEMV_WAIT);
+                if (!__all_sync(0xffffffffu, ok)) break;
+                if (run >= 1 && kb + 1 <= kb_last) {
+                    __syncwarp();                                   // the buffer's previous run is done
+                    if (lane == 0) issue_xslice(kb + 1, slot ^ 1);
+                    ++xissued;
+                }
+                xt = xsl + (slot * M + mrow) * XB + 8 * c;
+            } else {
+                xt = xs + mrow * xstride + 8 * c + (size_t)kb * KT * 2;
+            }
+            xgt = xgrow + (long long)kb * KT;
+            __syncwarp();                                           // the previous run's sums are read
+            for (int gg = 0; gg < ng; ++gg) {
+                float ds[2][4];
+#pragma unroll
+                for (int j = 0; j < GB; ++j) {
+                    uint32_t bx, by;
+                    if constexpr (XM != MMA_X_GLOBAL) {
+                        const uint2 v = *reinterpret_cast<const uint2*>(xt + (gg * GB + j) * 32);
+                        bx = v.x; by = v.y;
+                    } else {
+                        const int kk = (gg * GB + j) * 16;
+                        const uint2 v = (kb * KT + kk + 4 * c < a.K) ? ldg_nc_v2(xgt + kk) : make_uint2(0, 0);
+                        bx = v.x; by = v.y;
+                    }
+                    if (j < 2) mma_bf16_zero(ds[j & 1], ONES, ONES, ONES, ONES, bx, by);
+                    else mma_bf16(ds[j & 1], ONES, ONES, ONES, ONES, bx, by);
+                }
+                if (g == 0) {
+                    float2 v;
+                    v.x = ds[0][0] + ds[1][0];
+                    v.y = ds[0][1] + ds[1][1];
+                    *reinterpret_cast<float2*>(sxw + gg * 8 + 2 * c) = v;
+                }
+            }
+            __syncwarp();
+        }
+        const int s = li % S;
+        uint8_t* st = ring + s * F::STAGE_BYTES;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (uint32_t)((li / S) & 1), a.fault, FAULT_GEMV_WAIT)))
+            break;
         RowPtrs<FMT> rp[2];
         if constexpr (FMT != UQ_K4) {
             rp[0] = row_ptrs<FMT>(st, mc, g, n0 + g, kb);
             rp[1] = row_ptrs<FMT>(st, mc, g + 8, n0 + g + 8, kb);
         }
-        const uint8_t* xt = (XM == MMA_X_SLICE) ? st + F::STAGE_BYTES + mrow * XB + 8 * c
-                                                : xrow + (size_t)kb * KT * 2;   // x of the tile's first k
-        const uint16_t* xgt = xgrow + (long long)kb * KT;
 
         auto group_step = [&](const int gg) {
             // this lane's code words for the group's GB blocks
@@ -892,10 +928,8 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
                     bx[j] = v.x; by[j] = v.y;
                 }
             }
-            // dd: the group's sum of (128 + q) x;  ds: the same mma with A = 1, i.e. the sum of x over the
-            // group for columns 2c, 2c + 1 (rows of D are all equal), which the zero-point term needs
-            float dd[2][4], ds[2][4];
-            constexpr uint32_t ONES = 0x3F803F80u;                  // bf16 pair (1, 1)
+            // the group's sum of (128 + q) x, in two chains (even / odd blocks)
+            float dd[2][4];
 #pragma unroll
             for (int j = 0; j < GB; ++j) {
                 uint32_t a0, a1, a2, a3;
@@ -913,18 +947,11 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
                     a0 = nib_pair_lop3<0>(wd); a1 = nib_pair_lop3<1>(wd);
                     a2 = nib_pair_lop3<2>(wd); a3 = nib_pair_lop3<3>(wd);
                 }
-                if (j < 2) {
-                    mma_bf16_zero(dd[j & 1], a0, a1, a2, a3, bx[j], by[j]);
-                    mma_bf16_zero(ds[j & 1], ONES, ONES, ONES, ONES, bx[j], by[j]);
-                } else {
-                    mma_bf16(dd[j & 1], a0, a1, a2, a3, bx[j], by[j]);
-                    mma_bf16(ds[j & 1], ONES, ONES, ONES, ONES, bx[j], by[j]);
-                }
+                if (j < 2) mma_bf16_zero(dd[j & 1], a0, a1, a2, a3, bx[j], by[j]);
+                else mma_bf16(dd[j & 1], a0, a1, a2, a3, bx[j], by[j]);
             }
-            // fold the group into the row sums
-            float2 sxv;
-            sxv.x = ds[0][0] + ds[1][0];
-            sxv.y = ds[0][1] + ds[1][1];
+            // fold the group into the row sums, with the run's sums of x over the group
+            const float2 sxv = *reinterpret_cast<const float2*>(sxw + gg * 8 + 2 * c);
             float d[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) d[e] = dd[0][e] + dd[1][e];
@@ -953,60 +980,47 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
             for (int gg = 0; gg < ng; ++gg) group_step(gg);
         }
         __syncwarp();
-        if (t + S < t1) {
-            issue_tile<FMT>(a, L, mc, inb, ikb, st, &bars[s], lane, XM == MMA_X_SLICE ? XB : 0);
-            if (++ikb == L.KB) { ikb = 0; ++inb; }
-        }
+        if (issued < ntl) issue_next();                             // into the stage just consumed
 
-        if (kb == L.KB - 1 || t == t1 - 1) {
-            const bool full = (kb == L.KB - 1) && (nb != first_nb || (t0 % L.KB) == 0);
-            if (full) {
+        // the tile's partial sums: shared memory (cta_rows) or global memory, summed over k tiles later
+        if (cta_rows) {
+            float* part = cpart + ((warp * MMA_TPW + li) * RB) * 8;
 #pragma unroll
-                for (int j = 0; j < 2; ++j)
+            for (int j = 0; j < 2; ++j)
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int n = n0 + g + 8 * j, m = 2 * c + e;
-                        if (m < M && n < a.N)
-                            a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * j + e]));
-                    }
-            } else if (cta_rows) {
-                // row block shared with other warps of this CTA: partial sums to shared memory
-                float* part = cpart + ((warp * 2 + (nb == first_nb ? 0 : 1)) * RB) * 8;
+                for (int e = 0; e < 2; ++e) part[(g + 8 * j) * 8 + 2 * c + e] = acc[2 * j + e];
+        } else {
+            float* part = a.partials + i * RB * M;
 #pragma unroll
-                for (int j = 0; j < 2; ++j)
+            for (int j = 0; j < 2; ++j)
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) part[(g + 8 * j) * 8 + 2 * c + e] = acc[2 * j + e];
-            } else {
-                // row block shared with other workers: its fp32 partial sums go to this worker's slot
-                // (first or last row block of its range); gemv_split_reduce adds them up afterwards
-                const int slot = 2 * w + (nb == first_nb ? 0 : 1);
-                float* part = a.partials + (long long)slot * RB * M;
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e)
-                        if (2 * c + e < M) part[(g + 8 * j) * M + 2 * c + e] = acc[2 * j + e];
-            }
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+                for (int e = 0; e < 2; ++e)
+                    if (2 * c + e < M) part[(g + 8 * j) * M + 2 * c + e] = acc[2 * j + e];
         }
-        if (++kb == L.KB) { kb = 0; ++nb; }
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+    }
+    // a wait that timed out (fault flag set) left copies in flight: let them land before leaving
+    for (int j = 0; j < S; ++j) {
+        const int li = issued - 1 - j;
+        if (li >= 0) mbar_wait_bounded(&bars[li % S], (uint32_t)((li / S) & 1), a.fault, FAULT_GEMV_WAIT);
+    }
+    if constexpr (XM == MMA_X_SLICE) {
+        for (int r = (run > 0 ? run : 0); r < xissued; ++r)
+            mbar_wait_bounded(&xsl_bar[r & 1], (uint32_t)((r >> 1) & 1), a.fault, FAULT_GEMV_WAIT);
     }
     if (!cta_rows) return;
-    // cta_rows: row blocks whose tiles were split between warps of this CTA, summed in warp order
+    // cta_rows: each row's sum over the k tiles, in k order, from the warps that computed them
     __syncthreads();
-    for (int e = threadIdx.x; e < (rb1 - rb0) * RB * M; e += blockDim.x) {
+    for (int e = threadIdx.x; e < R * RB * M; e += blockDim.x) {
         const int rbi = e / (RB * M), rm = e % (RB * M), r = rm / M, m = rm % M;
-        const int nb2 = rb0 + rbi, n = nb2 * RB + r;
+        const int n = (rb0 + rbi) * RB + r;
         if (n >= a.N) continue;
-        const long long tf = (long long)rbi * L.KB;                 // tiles relative to the CTA's first
-        const int wf = worker_of(tf, Tc, W), wl = worker_of(tf + L.KB - 1, Tc, W);
-        if (wf == wl) continue;                                    // one warp covered it and stored y
         float sum = 0.f;
-        for (int w2 = wf; w2 <= wl; ++w2) {
-            const long long b2 = range_begin(w2, Tc, W);
-            if (b2 == range_begin(w2 + 1, Tc, W)) continue;        // a warp without tiles (Tc < W)
-            const int first2 = (int)((long long)rb0 + b2 / L.KB);
-            sum += cpart[((w2 * 2 + (nb2 == first2 ? 0 : 1)) * RB + r) * 8 + m];
+        for (int kb = 0; kb < L.KB; ++kb) {
+            const unsigned ti = (unsigned)(kb * R + rbi);
+            const unsigned w2 = ((ti + 1) * W - 1) / Tc;            // the warp whose range holds ti
+            const unsigned l2 = ti - w2 * Tc / W;
+            sum += cpart[((w2 * MMA_TPW + l2) * RB + r) * 8 + m];
         }
         a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
     }

@@ -35,7 +35,7 @@ struct GemvArgs {
     int NB, KB;               // row blocks, k tiles
     long long T;              // tiles = NB * KB
     int P;                    // workers (warps), P <= T
-    float* partials;          // [2P][16][M] fp32 split-K partial sums
+    float* partials;          // fp32 split-K partial sums: [T][16][M] (mma GEMV), [2P][16][M] (CUDA cores)
     unsigned int* tickets;    // [NB], zero between calls
     unsigned int* fault;      // device fault word
     int overlap;              // launched with programmatic stream serialization (set by the launcher)
@@ -48,7 +48,8 @@ int gemv_warps(int fmt);     // workers (warps) per CTA of the GEMV for this for
 // work split of a GEMV launch whose a.P (stream-K workers) is set: may switch the mma GEMV to
 // whole row blocks per CTA (a.cta_rows = 1); returns the grid
 int gemv_grid(GemvArgs& a, int fmt, int sms);
-size_t gemv_partials_floats(int P, int M);
+// fp32 partial-sum floats a GEMV launch needs (T tiles, P workers, M rows of x)
+size_t gemv_partials_floats(int fmt, long long T, int P, int M);
 cudaError_t launch_gemv(int fmt, const GemvArgs& a, int grid, cudaStream_t st);
 
 

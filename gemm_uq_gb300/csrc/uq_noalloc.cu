@@ -120,7 +120,7 @@ uq_status uq_gemm_noalloc(const uint16_t* x, const void* wq, const void* scales,
     if (P > T) P = T;
     const int mb_max = M < 8 ? M : 8;
     if ((size_t)L.NB * sizeof(unsigned int) > TICKET_BYTES ||
-        uq::gemv_partials_floats((int)P, mb_max) * sizeof(float) > PARTIAL_BYTES) {
+        uq::gemv_partials_floats(fmt, T, (int)P, mb_max) * sizeof(float) > PARTIAL_BYTES) {
         snprintf(g_err, sizeof g_err,
                  "N=%d, M=%d needs more than the %zu-byte static scratch (at most %zu row blocks of 16 and "
                  "%zu bytes of partial sums)", N, M, SCRATCH_BYTES, TICKET_BYTES / 4, PARTIAL_BYTES);
