@@ -115,6 +115,9 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(bar)) : "memory");
 }
+__device__ __forceinline__ void cp_async_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
 // D += A * B for one 16 x 8 x 16 block (bf16 inputs, fp32 accumulate)
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -162,8 +165,12 @@ struct MetaConst {
     bool aligned;     // every tile row's scale slice is 16-byte aligned and a multiple of 16 bytes
 };
 
-// Issue the copies of tile t into stage buffer `st` (all lanes take part).
-template <int FMT>
+// Issue the copies of tile t into stage buffer `st` (all lanes take part).  The codes arrive on
+// `bar` (transaction bytes).  The metadata copies either arrive on `bar` too (33 arrivals in all:
+// one per lane when its copies land, and the codes' expect_tx) or, with GROUP, form one cp.async
+// group per lane that the issuing warp itself waits for (`bar` then expects one arrival): a warp
+// has little room for pending mbarrier arrivals of cp.async, and a group costs none of it.
+template <int FMT, bool GROUP = false>
 __device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, const MetaConst& mc, int nb, int kb,
                                            uint8_t* st, uint64_t* bar, int lane) {
     using F = GemvFmt<FMT>;
@@ -215,11 +222,12 @@ __device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, c
             }
         }
     }
-    cp_async_arrive_noinc(bar);
+    if (GROUP) cp_async_commit_group();
+    else cp_async_arrive_noinc(bar);
     __syncwarp();
     if (lane == 0) {
         const uint32_t bytes = (uint32_t)L.tile_bytes(kb);
-        fence_proxy_async_smem();
+        if (!GROUP) fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, bytes);
         bulk_g2s_stream(st, a.wq + L.tile_offset(nb, kb), bytes, bar, l2_evict_first_policy());
     }
@@ -779,7 +787,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (has_work && lane == 0) {
 #pragma unroll
-        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 33);
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
         mbar_init(&xsl_bar[0], 1);
         mbar_init(&xsl_bar[1], 1);
         fence_barrier_init();
@@ -792,11 +800,15 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
     int issued = 0;                                                 // tiles requested so far
     auto issue_next = [&]() {
         const long long i = t0 + issued;
-        issue_tile<FMT>(a, L, mc, nb_of(i), kb_of(i), ring + (issued % S) * F::STAGE_BYTES, &bars[issued % S], lane);
+        issue_tile<FMT, true>(a, L, mc, nb_of(i), kb_of(i), ring + (issued % S) * F::STAGE_BYTES, &bars[issued % S],
+                              lane);
         ++issued;
     };
-    if (a.overlap && has_work)
-        while (issued < S && issued < ntl) issue_next();
+    // Only the first tile before the sums of x of the first run: at the start every warp of the
+    // GPU requests its tiles at once and a copy's issue waits for room in the memory system, so
+    // the second tile is requested once this warp's sums of x are done (the memory system is
+    // still busy with the first tiles then).
+    if (a.overlap && has_work && ntl > 0) issue_next();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     int xissued = 0;                                                // x-slice runs requested so far
     if constexpr (XM == MMA_X_SLICE) {
@@ -813,8 +825,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
         }
         __syncthreads();                            // no warp's weight copies ahead of x
     }
-    if (has_work)
-        while (issued < S && issued < ntl) issue_next();
+    if (has_work && issued == 0 && ntl > 0) issue_next();
     if constexpr (XS) {
         const int padw = (L.Kp - a.K) / 2;
         for (int e = threadIdx.x; e < M * padw; e += blockDim.x)
@@ -881,8 +892,14 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
             }
             __syncwarp();
         }
+        while (issued < ntl && issued < li + S) issue_next();        // top up the ring (into stages consumed)
         const int s = li % S;
         uint8_t* st = ring + s * F::STAGE_BYTES;
+        // this tile's metadata group is complete once at most the groups of later tiles are pending
+        static_assert(S == 2, "one later group at most");
+        if (issued > li + 1) cp_async_wait_group<1>();
+        else cp_async_wait_group<0>();
+        __syncwarp();
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (uint32_t)((li / S) & 1), a.fault, FAULT_GEMV_WAIT)))
             break;
         RowPtrs<FMT> rp[2];
@@ -980,7 +997,6 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
             for (int gg = 0; gg < ng; ++gg) group_step(gg);
         }
         __syncwarp();
-        if (issued < ntl) issue_next();                             // into the stage just consumed
 
         // the tile's partial sums: shared memory (cta_rows) or global memory, summed over k tiles later
         if (cta_rows) {
@@ -1000,6 +1016,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
         acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
     }
     // a wait that timed out (fault flag set) left copies in flight: let them land before leaving
+    cp_async_wait_group<0>();
     for (int j = 0; j < S; ++j) {
         const int li = issued - 1 - j;
         if (li >= 0) mbar_wait_bounded(&bars[li % S], (uint32_t)((li / S) & 1), a.fault, FAULT_GEMV_WAIT);
