@@ -116,6 +116,11 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// 16-byte copy through L2 only, with an L2 eviction-priority hint
+__device__ __forceinline__ void cp_async16_hint(void* dst, const void* src, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
+                 :: "r"(smem_u32(dst)), "l"(src), "l"(policy) : "memory");
+}
 template <int N>
 __device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
@@ -165,11 +170,13 @@ struct MetaConst {
     bool aligned;     // every tile row's scale slice is 16-byte aligned and a multiple of 16 bytes
 };
 
-// Issue the copies of tile t into stage buffer `st` (all lanes take part).  The codes arrive on
-// `bar` (transaction bytes).  The metadata copies either arrive on `bar` too (33 arrivals in all:
-// one per lane when its copies land, and the codes' expect_tx) or, with GROUP, form one cp.async
-// group per lane that the issuing warp itself waits for (`bar` then expects one arrival): a warp
-// has little room for pending mbarrier arrivals of cp.async, and a group costs none of it.
+// Issue the copies of tile t into stage buffer `st` (all lanes take part).  Either the codes come
+// as one bulk copy counted on `bar` (transaction bytes) and the metadata copies arrive on `bar`
+// too (33 arrivals in all: one per lane when its copies land, and the codes' expect_tx), or, with
+// GROUP, everything is 16-byte cp.async (codes: 512 contiguous bytes per warp instruction) in one
+// cp.async group per lane that the issuing warp itself waits for (`bar` unused).  The per-lane
+// copies keep more of the tile stream in flight than one 8 KB bulk copy per tile: the copy engine
+// takes bulk copies one after another, at well under an SM's share of HBM bandwidth at this size.
 template <int FMT, bool GROUP = false>
 __device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, const MetaConst& mc, int nb, int kb,
                                            uint8_t* st, uint64_t* bar, int lane) {
@@ -222,14 +229,22 @@ __device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, c
             }
         }
     }
-    if (GROUP) cp_async_commit_group();
-    else cp_async_arrive_noinc(bar);
-    __syncwarp();
-    if (lane == 0) {
-        const uint32_t bytes = (uint32_t)L.tile_bytes(kb);
-        if (!GROUP) fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s_stream(st, a.wq + L.tile_offset(nb, kb), bytes, bar, l2_evict_first_policy());
+    if constexpr (GROUP) {
+        const int bytes = (int)L.tile_bytes(kb);
+        const uint8_t* src = a.wq + L.tile_offset(nb, kb);
+        const uint64_t pol = l2_evict_first_policy();
+        for (int off = lane * 16; off < bytes; off += 512) cp_async16_hint(st + off, src + off, pol);
+        cp_async_commit_group();
+        (void)bar;
+    } else {
+        cp_async_arrive_noinc(bar);
+        __syncwarp();
+        if (lane == 0) {
+            const uint32_t bytes = (uint32_t)L.tile_bytes(kb);
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_g2s_stream(st, a.wq + L.tile_offset(nb, kb), bytes, bar, l2_evict_first_policy());
+        }
     }
 }
 
@@ -867,6 +882,37 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
             }
             xgt = xgrow + (long long)kb * KT;
             __syncwarp();                                           // the previous run's sums are read
+            if constexpr (XM == MMA_X_SLICE) {
+                // one or two rows: lane l adds up k = KL l .. KL l + KL - 1 of each row in fp32 (a
+                // group spans GS / KL lanes, combined by shuffles, or a lane spans KL / GS groups)
+                constexpr int KL = KT / 32;
+                const int slot = run & 1;
+                for (int m = 0; m < M; ++m) {
+                    const uint4* xp = reinterpret_cast<const uint4*>(xsl + (slot * M + m) * XB + lane * KL * 2);
+                    constexpr int NGL = (KL / GS) > 1 ? (KL / GS) : 1;  // groups within the lane's k
+                    float gsum[NGL];
+#pragma unroll
+                    for (int q = 0; q < NGL; ++q) gsum[q] = 0.f;
+#pragma unroll
+                    for (int v = 0; v < KL / 8; ++v) {
+                        const uint4 w4 = xp[v];
+                        const uint32_t wv4[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const int q = (NGL > 1) ? (v * 8 + 2 * h) / GS : 0;
+                            gsum[q] += __uint_as_float(wv4[h] << 16) + __uint_as_float(wv4[h] & 0xFFFF0000u);
+                        }
+                    }
+                    if constexpr (GS >= KL) {
+#pragma unroll
+                        for (int o = 1; o < GS / KL; o <<= 1) gsum[0] += __shfl_xor_sync(0xffffffffu, gsum[0], o);
+                        if ((lane & (GS / KL - 1)) == 0) sxw[(lane / (GS / KL)) * 8 + m] = gsum[0];
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < NGL; ++q) sxw[(lane * NGL + q) * 8 + m] = gsum[q];
+                    }
+                }
+            } else {
             for (int gg = 0; gg < ng; ++gg) {
                 float ds[2][4];
 #pragma unroll
@@ -890,18 +936,18 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
                     *reinterpret_cast<float2*>(sxw + gg * 8 + 2 * c) = v;
                 }
             }
+            }
             __syncwarp();
         }
         while (issued < ntl && issued < li + S) issue_next();        // top up the ring (into stages consumed)
         const int s = li % S;
         uint8_t* st = ring + s * F::STAGE_BYTES;
-        // this tile's metadata group is complete once at most the groups of later tiles are pending
+        // this tile's copies (one cp.async group) are complete once at most the groups of later
+        // tiles are pending
         static_assert(S == 2, "one later group at most");
         if (issued > li + 1) cp_async_wait_group<1>();
         else cp_async_wait_group<0>();
         __syncwarp();
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (uint32_t)((li / S) & 1), a.fault, FAULT_GEMV_WAIT)))
-            break;
         RowPtrs<FMT> rp[2];
         if constexpr (FMT != UQ_K4) {
             rp[0] = row_ptrs<FMT>(st, mc, g, n0 + g, kb);
@@ -1017,10 +1063,6 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(co
     }
     // a wait that timed out (fault flag set) left copies in flight: let them land before leaving
     cp_async_wait_group<0>();
-    for (int j = 0; j < S; ++j) {
-        const int li = issued - 1 - j;
-        if (li >= 0) mbar_wait_bounded(&bars[li % S], (uint32_t)((li / S) & 1), a.fault, FAULT_GEMV_WAIT);
-    }
     if constexpr (XM == MMA_X_SLICE) {
         for (int r = (run > 0 ? run : 0); r < xissued; ++r)
             mbar_wait_bounded(&xsl_bar[r & 1], (uint32_t)((r >> 1) & 1), a.fault, FAULT_GEMV_WAIT);
