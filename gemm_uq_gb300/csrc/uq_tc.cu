@@ -72,16 +72,16 @@ bool tc_supported(int fmt, int N, int K) {
 int tc_plan(int fmt, int mpad, int* stages, int* nabuf, size_t* smem) {
     const int kc = (fmt == UQ_INT8_SYM) ? 128 : 256;
     const int sb = TcSmem::stage_bytes(kc, mpad);
-    const int budget = 227 * 1024 - 1024 - TC_BAR_BYTES - TC_DQ_RING;
-    int s = budget / sb;
+    const int budget = 227 * 1024 - 1024 - TC_BAR_BYTES;
+    int s = budget / (sb + TC_DQ_UNIT);
     if (s > 6) s = 6;
-    if (s < 2) return -1;
+    if (s < 3) return -1;                           // codes are requested two units ahead
     int na = (TMEM_COLS - 2 * mpad) / (kc / 2);     // A buffers beside two Mpad-column accumulators
     if (na > 4) na = 4;
     if (na < 2) return -1;
     *stages = s;
     *nabuf = na;
-    *smem = 1024 + (size_t)s * sb + TC_BAR_BYTES + TC_DQ_RING;
+    *smem = 1024 + (size_t)s * (sb + TC_DQ_UNIT) + TC_BAR_BYTES;
     return 0;
 }
 
@@ -101,6 +101,66 @@ cudaError_t launch_tc_prep(const uint16_t* x, int ldx, int K, int M, int mpad, u
     return cudaGetLastError();
 }
 
+// Second pass when CTAs share 128-row blocks: y[m][n] = the sum of the contributing CTAs' partial
+// sums in CTA order.  Launched right after the tensor-core kernel with programmatic stream
+// serialization: its griddepcontrol.wait returns once that grid has finished and its stores are
+// visible, so the kernel itself needs no fence or ticket.
+__global__ void __launch_bounds__(256) tc_split_reduce(const TcArgs a) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int nblk = (a.N + TC_ROWS - 1) / TC_ROWS;
+    const long long total = (long long)nblk * a.M * TC_ROWS;
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        const int rb = (int)(e / ((long long)a.M * TC_ROWS));
+        const int mr = (int)(e % ((long long)a.M * TC_ROWS));
+        const int m = mr / TC_ROWS, r = mr % TC_ROWS;
+        const int n = rb * TC_ROWS + r;
+        if (n >= a.N) continue;
+        const long long uf = (long long)rb * a.CH;
+        const int cf = tworker_of(uf, a.U, a.P), cl = tworker_of(uf + a.CH - 1, a.U, a.P);
+        if (cf == cl) continue;                                     // one CTA covered it and stored y
+        float sum = 0.f;
+        for (int c2 = cf; c2 <= cl; ++c2) {
+            const int rb2 = (int)(trange_begin(c2, a.U, a.P) / a.CH);
+            const int slot2 = 2 * c2 + (rb == rb2 ? 0 : 1);
+            sum += a.partials[((long long)slot2 * a.Mpad + m) * TC_ROWS + r];
+        }
+        a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+    }
+}
+
+// whether any 128-row block is shared by several CTAs (then the second pass runs)
+static bool tc_any_split(const TcArgs& a) {
+    const int nblk = (a.N + TC_ROWS - 1) / TC_ROWS;
+    for (int rb = 0; rb < nblk; ++rb) {
+        const long long uf = (long long)rb * a.CH, ul = uf + a.CH - 1;
+        const long long cf = ((uf + 1) * a.P - 1) / a.U, cl = ((ul + 1) * a.P - 1) / a.U;
+        if (cf != cl) return true;
+    }
+    return false;
+}
+
+static cudaError_t launch_tc_reduce(const TcArgs& a, int sms, cudaStream_t st) {
+    const int nblk = (a.N + TC_ROWS - 1) / TC_ROWS;
+    const long long total = (long long)nblk * a.M * TC_ROWS;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 4LL * sms) blocks = 4LL * sms;
+    if (blocks < 1) blocks = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, tc_split_reduce, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 cudaError_t launch_tc(int fmt, const uint16_t* xh, const TcArgs& a, size_t smem, int grid, cudaStream_t st) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
@@ -115,13 +175,19 @@ cudaError_t launch_tc(int fmt, const uint16_t* xh, const TcArgs& a, size_t smem,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
+    cudaError_t e;
     switch (fmt) {
-        case UQ_INT4_SYM: return launch_tc_fmt<UQ_INT4_SYM>(mx, a, smem, grid, st);
-        case UQ_INT4_ASYM: return launch_tc_fmt<UQ_INT4_ASYM>(mx, a, smem, grid, st);
-        case UQ_INT8_SYM: return launch_tc_fmt<UQ_INT8_SYM>(mx, a, smem, grid, st);
-        case UQ_K4: return launch_tc_fmt<UQ_K4>(mx, a, smem, grid, st);
+        case UQ_INT4_SYM: e = launch_tc_fmt<UQ_INT4_SYM>(mx, a, smem, grid, st); break;
+        case UQ_INT4_ASYM: e = launch_tc_fmt<UQ_INT4_ASYM>(mx, a, smem, grid, st); break;
+        case UQ_INT8_SYM: e = launch_tc_fmt<UQ_INT8_SYM>(mx, a, smem, grid, st); break;
+        case UQ_K4: e = launch_tc_fmt<UQ_K4>(mx, a, smem, grid, st); break;
         default: return cudaErrorInvalidValue;
     }
+    if (e != cudaSuccess || !tc_any_split(a)) return e;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return launch_tc_reduce(a, sms > 0 ? sms : 1, st);
 }
 
 }  // namespace uq

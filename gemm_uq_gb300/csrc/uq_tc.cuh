@@ -18,18 +18,19 @@
 // |y - y_ref| stays within about 5e-4 * sum |x * w_hat| -- inside the 1e-3 tolerance.
 //
 // Roles (512 threads, one CTA per SM, persistent over an equal contiguous range of units):
-//   warp 0       producer: per unit eight 2 KB bulk copies of codes (one per 16-row block of the
-//                fragment-order plane, L2 evict_first) and kc/64 TMA boxes of x, on full[stage];
+//   warp 0       producer: per unit the kc/64 TMA boxes of x, on full[stage];
 //   warp 1       MMA issuer (one thread): kc/16 tcgen05.mma per unit (M=128, N=Mpad, K=16) into
 //                the row block's accumulator; commits free the A buffer and the stage, and hand a
 //                finished row block to the epilogue;
 //   warps 4..11  dequant: warp = one 16-row block; lane (g, c) turns its fragment-order words into
 //                fp16 pairs of s*(q - z) and stores them with tcgen05.st.16x256b (the store shape
-//                whose thread layout is the mma fragment's); scales, zero points and K4 records
-//                arrive through per-warp cp.async rings three units ahead;
+//                whose thread layout is the mma fragment's); each warp copies its own 2 KB of
+//                codes per unit (16-byte cp.async) and the scales, zero points or K4 records,
+//                stages - 1 units ahead, one cp.async group per unit (a single thread issuing eight
+//                small bulk copies per unit could not keep up with the stream);
 //   warps 12..15 epilogue: thread = weight row; at a row block's end in this CTA it reads the
-//                accumulator, scales the columns, and stores y, or a partial sum plus a ticket
-//                (the last contributor reduces the partials in CTA order: deterministic, no waits).
+//                accumulator, scales the columns, and stores y, or its partial sums when other CTAs
+//                share the row block (tc_split_reduce then adds them in CTA order: deterministic).
 // Unit = (128-row block, chunk of 128 code bytes per row = kc codes).  Every wait is bounded
 // (mbar_wait_bounded); on a timeout the roles stop, the CTA frees its tensor memory and leaves.
 #pragma once
@@ -46,7 +47,7 @@ constexpr int TMEM_COLS = 512;
 constexpr int TC_BAR_BYTES = 2048;                 // barriers and flags after the stages
 constexpr int TC_DQ_WARPS = 8;                     // dequant warps (one 16-row block each)
 constexpr int TC_DQW = 8;                          // staged metadata words per row and unit
-constexpr int TC_DQ_RING = 3 * TC_DQ_WARPS * 16 * TC_DQW * 4;   // bytes: 3 units of metadata
+constexpr int TC_DQ_UNIT = TC_DQ_WARPS * 16 * TC_DQW * 4;       // bytes of staged metadata per unit (one per stage)
 
 template <int FMT> struct TcFmt {
     static constexpr int KC = (FMT == UQ_INT8_SYM) ? 128 : 256;   // codes per row per unit
@@ -112,11 +113,26 @@ __device__ __forceinline__ void tmem_st_16x256b_x2(uint32_t taddr, const uint32_
 __device__ __forceinline__ void tc_cp_async4(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
 }
+__device__ __forceinline__ void tc_cp_async16_hint(void* dst, const void* src, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
+                 :: "r"(smem_u32(dst)), "l"(src), "l"(policy) : "memory");
+}
 __device__ __forceinline__ void tc_cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
+// wait until at most n (0..5) of this thread's cp.async groups are pending
+__device__ __forceinline__ void cp_async_wait_n(int n) {
+    switch (n) {
+        case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+        case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+        case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    }
+}
 // Copy the aligned 32-bit words that cover bytes [lo, lo + len) of `base` into dst[0 .. nw) (word 0
 // holds byte lo & ~3).  Words that would reach past `end` (the array's size) are assembled from byte
 // loads instead, so nothing outside the array is read.
@@ -221,10 +237,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
     uint64_t* aempty = afull + NA;                  // [NA]
     uint64_t* dfull = aempty + NA;                  // [2]
     uint64_t* dempty = dfull + 2;                   // [2]
-    uint64_t* ebar = dempty + 2;                    // epilogue warpgroup rendezvous (128 arrivals)
-    uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(ebar + 1);
+    uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(dempty + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_smem + 1);
-    unsigned int* ticket_smem = reinterpret_cast<unsigned int*>(tmem_base_smem + 2);
     uint32_t* dq_ring = reinterpret_cast<uint32_t*>(smem + S * SB + TC_BAR_BYTES);   // [3][8 warps][16][TC_DQW]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -234,10 +248,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1 + TC_DQ_WARPS); }
+        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
         for (int i = 0; i < NA; ++i) { mbar_init(&afull[i], TC_DQ_WARPS); mbar_init(&aempty[i], 1); }
         for (int d = 0; d < 2; ++d) { mbar_init(&dfull[d], 1); mbar_init(&dempty[d], 4); }
-        mbar_init(ebar, 128);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -255,33 +268,22 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         if (lane == 0) {
             int issued = 0;
             const uint64_t pol = l2_evict_first_policy();
-            auto issue_codes = [&](int rb, int c, int s) {
-                uint8_t* st = smem + s * SB;
-                // for each of the 8 row blocks of 16, the unit's 4 chunks (2 KB, contiguous)
-                const int nb0 = rb * 8;
-                const int nbs = (a.NB - nb0) < 8 ? (a.NB - nb0) : 8;
-                mbar_arrive_expect_tx(&full[s], (uint32_t)(nbs * 2048 + XB));
-                const int kb = c >> 2, q0 = (c & 3) * 4;
-                for (int j = 0; j < nbs; ++j)
-                    bulk_g2s_stream(st + j * 2048, a.wq + (long long)(nb0 + j) * 16 * a.rowbytes + (long long)kb * 8192 + q0 * 512,
-                                    2048u, &full[s], pol);
-            };
             auto issue_x = [&](int c, int s) {
                 uint8_t* st = smem + s * SB;
+                if (c < 0 || c * KC + KC > a.K || s < 0 || s >= S) {   // self-check
+                    atomicOr(a.fault, FAULT_TC_BOUNDS);
+                    return;
+                }
 #pragma unroll
                 for (int q = 0; q < KC / 64; ++q)
                     tma_load_2d(st + TC_STAGE_CODES + q * (MPAD * 128), &tmap_x, c * KC + q * 64, 0, &full[s]);
             };
-            // the first stages' weights are constant: stream them before waiting for the previous
-            // kernel on the stream (launch overlap); x is loaded only after that wait
+            // x is written by the kernel before (the x pre-kernel): loaded after the wait for it
             const int pre = (u1 - u0) < S ? (int)(u1 - u0) : S;
             int rb = (int)(u0 / CH), c = (int)(u0 % CH);
-            for (int j = 0, r2 = rb, c2 = c; j < pre; ++j) {
-                issue_codes(r2, c2, j);
-                if (++c2 == CH) { c2 = 0; ++r2; }
-            }
             asm volatile("griddepcontrol.wait;" ::: "memory");
             for (int j = 0; j < pre; ++j) {
+                mbar_arrive_expect_tx(&full[j], (uint32_t)XB);
                 issue_x(c, j);
                 if (++c == CH) { c = 0; ++rb; }
             }
@@ -294,7 +296,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     *abort_flag = 1;
                     break;
                 }
-                issue_codes(rb, c, s);
+                mbar_arrive_expect_tx(&full[s], (uint32_t)XB);
                 issue_x(c, s);
                 if (++c == CH) { c = 0; ++rb; }
                 if (++s == S) s = 0;
@@ -350,15 +352,32 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         const int rbl = 2 * quarter + hf;               // row block (16 rows) within the 128-row unit
         const int g = lane >> 2, c4 = lane & 3;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter + 16 * hf) << 16);
-        uint32_t* wr = dq_ring + (warp - 4) * (16 * TC_DQW);   // this warp's slot 0; slots TC_DQ_WARPS*16*TC_DQW apart
+        uint32_t* wr = dq_ring + (warp - 4) * (16 * TC_DQW);   // this warp's slot 0; one slot per stage, RING_STRIDE apart
         constexpr int RING_STRIDE = TC_DQ_WARPS * 16 * TC_DQW;
         const int Gn = a.K / GS, ZB = (Gn + 1) >> 1;
         // metadata of unit u for rows g and g + 8: lanes c = 0, 1 stage the scales (K4: the record)
         // of row g + 8c, lanes c = 2, 3 the INT4_ASYM zero points of row g + 8(c - 2)
-        auto issue_meta = [&](long long u, int slot) {
+        auto issue_meta = [&](long long u, int slot, int stg) {
             if (u < u1) {
                 const int ui = (int)u;
                 const int rb = ui / CH, c = ui % CH;
+                // this warp's 2 KB of codes of the unit: 16-row block rb * 8 + rbl, k tile c / 4,
+                // chunks (c % 4) * 4 .. + 3 (contiguous in the fragment-order plane)
+                if (rb * 8 + rbl < a.NB) {
+                    const long long soff = (long long)(rb * 8 + rbl) * 16 * a.rowbytes + (long long)(c >> 2) * 8192 +
+                                           (c & 3) * 4 * 512;
+                    const long long doff = (long long)stg * SB + rbl * 2048;
+                    // self-check: inside the packed plane and the stage, 16-byte aligned
+                    if (soff < 0 || soff + 2048 > (long long)a.NB * 16 * a.rowbytes || (soff & 15) ||
+                        stg < 0 || stg >= S || doff + 2048 > (long long)S * SB ||
+                        ((reinterpret_cast<uintptr_t>(a.wq) + soff) & 15)) {
+                        atomicOr(a.fault, FAULT_TC_BOUNDS);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            tc_cp_async16(smem + doff + q * 512 + lane * 16, a.wq + soff + q * 512 + lane * 16);
+                    }
+                }
                 const int r = g + 8 * (c4 & 1);
                 const long long n = (long long)rb * TC_ROWS + rbl * 16 + r;
                 uint32_t* dst = wr + slot * RING_STRIDE + r * TC_DQW;
@@ -376,15 +395,15 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             }
             cp_async_commit();
         };
-        issue_meta(u0, 0);
-        issue_meta(u0 + 1, 1);
+        const int D = S - 1;                            // units requested ahead (slot = stage = unit mod S)
+        for (int j = 0; j < D; ++j) issue_meta(u0 + j, j, j);
         int s = 0, ab = 0, slot = 0;
         uint32_t sph = 0, aph = 1;                      // full[s] phase; aempty[] of the first round is free
         int rb = (int)(u0 / CH), c = (int)(u0 % CH);
         for (long long u = u0; u < u1 && !*abort_flag; ++u) {
             __syncwarp();
-            issue_meta(u + 2, slot == 0 ? 2 : slot - 1);
-            cp_async_wait2();
+            issue_meta(u + D, (s + D) % S, (s + D) % S);
+            cp_async_wait_n(D);                             // unit u's codes and metadata have landed
             __syncwarp();
             // per-group operands for rows g (h = 0) and g + 8 (h = 1)
             uint32_t sc2[2][GPC], zz[2][GPC];           // fp16 pairs (s, s) and (1024 + z)
@@ -429,8 +448,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     }
                 }
             }
-            bool ok = mbar_wait_bounded(&full[s], sph, a.fault, FAULT_TC_WAIT) &&
-                      mbar_wait_bounded(&aempty[ab], aph, a.fault, FAULT_TC_WAIT);
+            bool ok = mbar_wait_bounded(&aempty[ab], aph, a.fault, FAULT_TC_WAIT);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) { *abort_flag = 1; break; }
             tc_fence_after();
@@ -490,10 +508,10 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) { mbar_arrive(&afull[ab]); mbar_arrive(&empty[s]); }
+            if (lane == 0) mbar_arrive(&afull[ab]);
             if (++s == S) { s = 0; sph ^= 1u; }
             if (++ab == NA) { ab = 0; aph ^= 1u; }
-            if (++slot == 3) slot = 0;
+            if (++slot == S) slot = 0;
             if (++c == CH) { c = 0; ++rb; }
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
@@ -504,14 +522,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         const int r = we * 32 + lane;
         const uint32_t lane_addr = tmem + ((uint32_t)(we * 32) << 16);
         int dsl = 0;
-        uint32_t dph = 0, ephase = 0;
-        // all 128 epilogue threads meet here (bounded: returns false after the time limit)
-        auto epi_sync = [&]() -> bool {
-            mbar_arrive(ebar);
-            const bool r_ok = mbar_wait_bounded(ebar, ephase, a.fault, FAULT_TC_WAIT);
-            ephase ^= 1u;
-            return r_ok;
-        };
+        uint32_t dph = 0;
         const int first_rb = (int)(u0 / CH);
         int rb = first_rb, c = (int)(u0 % CH);
         for (long long u = u0; u < u1 && !*abort_flag; ++u) {
@@ -545,37 +556,11 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                             if (m < a.M)
                                 a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
                 } else {
+                    // row block shared with other CTAs: this CTA's partial sums, [slot][m][row]
                     const int pslot = 2 * cta + (rb == first_rb ? 0 : 1);
-                    float* part = a.partials + (long long)pslot * TC_ROWS * MPAD + r;   // [slot][m][row]
+                    float* part = a.partials + (long long)pslot * TC_ROWS * MPAD + r;
 #pragma unroll
                     for (int m = 0; m < MPAD; ++m) part[m * TC_ROWS] = acc[m];
-                    __threadfence();
-                    if (!epi_sync()) { *abort_flag = 1; break; }
-                    if (r == 0) *ticket_smem = atomicAdd(a.tickets + rb, 1u);
-                    if (!epi_sync()) { *abort_flag = 1; break; }
-                    const unsigned int old = *ticket_smem;
-                    const long long uf = (long long)rb * CH;
-                    const int cf = tworker_of(uf, a.U, a.P), cl = tworker_of(uf + CH - 1, a.U, a.P);
-                    if (old == (unsigned int)(cl - cf)) {
-                        __threadfence();
-                        // the partials of all contributors, summed in CTA order
-#pragma unroll
-                        for (int m = 0; m < MPAD; ++m) acc[m] = 0.f;
-                        for (int c2 = cf; c2 <= cl; ++c2) {
-                            const int rb2 = (int)(trange_begin(c2, a.U, a.P) / CH);
-                            const int slot2 = 2 * c2 + (rb == rb2 ? 0 : 1);
-                            const float* p2 = a.partials + (long long)slot2 * TC_ROWS * MPAD + r;
-#pragma unroll
-                            for (int m = 0; m < MPAD; ++m) acc[m] += __ldcg(p2 + m * TC_ROWS);
-                        }
-                        if (live)
-#pragma unroll
-                            for (int m = 0; m < MPAD; ++m)
-                                if (m < a.M)
-                                    a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
-                        if (r == 0) a.tickets[rb] = 0u;
-                    }
-                    if (!epi_sync()) { *abort_flag = 1; break; }
                 }
             }
             if (++c == CH) { c = 0; ++rb; }
