@@ -187,7 +187,8 @@ uq_status uq_set_launch_overlap(int enable);
  * uq_device_fault -- reads and clears the device-side fault word of the current device
  * (bit 0 / bit 1: a GEMV / tensor-core kernel's bounded wait on an mbarrier ran out and the
  * kernel returned early instead of hanging; bit 2: a GEMV launch was given a work split larger
- * than the kernel holds and computed nothing).  Synchronizes the device.  *flag = 0 when no fault.
+ * than the kernel holds and computed nothing; bit 3: a tensor-core copy address failed the
+ * kernel's self-check and was skipped).  Synchronizes the device.  *flag = 0 when no fault.
  */
 uq_status uq_device_fault(unsigned int* flag);
 
