@@ -119,14 +119,12 @@ def dominant_kernel(fmt, group, M, recs):
     return f"gemv_kernel<{fmt},{min(M, 8)}>"
 
 
-def kernels_per_call(fmt, M, K):
-    """Kernel launches one uq_gemm call makes: the tensor-core path (per 64 rows of x: the x
-    conversion pre-kernel and the GEMM), or the GEMV per 8 rows of x (the mma GEMV adds its split-K
-    reduce launch)."""
-    kt = {"INT4_SYM": 1024, "INT4_ASYM": 1024, "INT8_SYM": 512, "INT2_ASYM": 2048, "NF4": 1024, "K4": 1024}[fmt]
-    if M >= 16 and fmt in ("INT4_SYM", "INT4_ASYM", "INT8_SYM", "K4") and K % kt == 0:
-        return ((M + 63) // 64) * 2
-    return ((M + 7) // 8) * (2 if fmt in ("INT4_SYM", "INT4_ASYM", "INT2_ASYM", "K4") else 1)
+def kernels_per_call(fmt, group, M, N, K):
+    """Kernel launches one uq_gemm call of this shape makes on the current device, as the library
+    itself counts them (GEMV, or tensor-core x conversion + GEMM, plus a second pass where rows are
+    shared between SMs)."""
+    import gemm_uq_gb300 as uq
+    return uq.gemm_kernel_count(M, N, K, group, fmt)
 
 
 def measured_peak():
@@ -387,7 +385,7 @@ def run_uq(args, rank, world, dist):
                    "l2": "no flush: packed weights per step exceed L2 (%.2f GB)" % (step_bytes / 1e9),
                    "launch": "one CUDA graph per step",
                    "launch_overlap": not args.no_overlap},
-        "gpu_launches": sum(kernels_per_call(fmt, M, r["K"]) for r in recs) * args.steps,
+        "gpu_launches": sum(kernels_per_call(fmt, group, M, r["N"], r["K"]) for r in recs) * args.steps,
         "e2e": {"value": round(step_bytes * args.steps * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": xbuf.numel() * 2, "d2h_bytes_per_step": ybuf.numel() * 2},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

@@ -35,6 +35,7 @@ SIGNATURES = {
     "uq_device_fault": (_I, [ctypes.POINTER(ctypes.c_uint)]),
     "uq_gemm_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "uq_set_launch_overlap": (_I, [_I]),
+    "uq_gemm_kernel_count": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I)]),
 }
 
 _lib = None
@@ -193,6 +194,13 @@ def quantize_k4(w: torch.Tensor, stream=None):
 def set_launch_overlap(enable: bool) -> None:
     """uq_set_launch_overlap: let GEMV launches prefetch their (constant) weights early."""
     _check(lib().uq_set_launch_overlap(1 if enable else 0), "uq_set_launch_overlap")
+
+
+def gemm_kernel_count(M: int, N: int, K: int, group: int, fmt: str) -> int:
+    """uq_gemm_kernel_count: kernels one gemm() call of this shape launches on the current device."""
+    v = ctypes.c_int(0)
+    _check(lib().uq_gemm_kernel_count(M, N, K, group, FORMATS[fmt], ctypes.byref(v)), "uq_gemm_kernel_count")
+    return v.value
 
 
 def device_fault() -> int:

@@ -191,9 +191,9 @@ uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const 
 uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const void* zc, uint16_t* y, int Mb, int N,
                  int K, int ldx, int ldy, int group, int fmt, cudaStream_t st, const DeviceState& ds, int dev) {
     const int mpad = (Mb + 15) / 16 * 16;
-    int stages = 0, nabuf = 0;
+    int stages = 0, dslots = 0;
     size_t smem = 0;
-    if (uq::tc_plan(fmt, mpad, &stages, &nabuf, &smem) != 0)
+    if (uq::tc_plan(fmt, mpad, &stages, &dslots, &smem) != 0)
         return fail(UQ_ERR_UNSUPPORTED, "no tensor-core plan for M=%d", Mb);
     const int kc = (fmt == UQ_INT8_SYM) ? 128 : 256;
     const int nblk = (N + 127) / 128;
@@ -202,15 +202,15 @@ uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const vo
     long long P = ds.sms;
     if (P > U) P = U;
     Workspace* ws = nullptr;
-    // aux: the fp16 copy of x [Mb][K], then the 64 column scales
-    const size_t xh_bytes = ((size_t)Mb * K * 2 + 255) / 256 * 256;
+    const size_t aux = (fmt == UQ_K4) ? (size_t)(K / 32) * mpad * sizeof(float) : 0;
     uq_status s = workspace(dev, st, (size_t)2 * P * 128 * mpad * sizeof(float), (size_t)nblk * sizeof(unsigned int),
-                            &ws, xh_bytes + 64 * sizeof(float));
+                            &ws, aux);
     if (s != UQ_OK) return s;
-    uint16_t* xh = reinterpret_cast<uint16_t*>(ws->aux);
-    float* xsc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws->aux) + xh_bytes);
-    cudaError_t e = uq::launch_tc_prep(x, ldx, K, Mb, mpad, xh, xsc, st);
-    if (e != cudaSuccess) return cuda_fail(e, "x conversion launch");
+    cudaError_t e;
+    if (fmt == UQ_K4) {
+        e = uq::launch_colsum32(x, ws->aux, Mb, mpad, K, ldx, st);
+        if (e != cudaSuccess) return cuda_fail(e, "column-sum launch");
+    }
     uq::TcArgs a;
     const uq::Layout L(N, K, fmt);
     a.wq = static_cast<const uint8_t*>(wq);
@@ -219,14 +219,14 @@ uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const vo
     a.scales = static_cast<const uint8_t*>(scales);
     a.zc = static_cast<const uint8_t*>(zc);
     a.y = y;
-    a.xscale = xsc;
+    a.sx = ws->aux;
     a.M = Mb; a.Mpad = mpad; a.N = N; a.K = K; a.group = group; a.ldx = ldx; a.ldy = ldy;
     a.CH = CH; a.U = U; a.P = (int)P;
-    a.stages = stages; a.nabuf = nabuf;
+    a.stages = stages; a.dslots = dslots;
     a.partials = ws->partials;
     a.tickets = ws->tickets;
     a.fault = ds.words;
-    e = uq::launch_tc(fmt, xh, a, smem, (int)P, st);
+    e = uq::launch_tc(fmt, x, a, smem, (int)P, st);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core launch");
     return UQ_OK;
 }
@@ -430,6 +430,41 @@ uq_status uq_quantize_k4(const float* w, int8_t* codes, uint16_t* d, uint16_t* d
 
 uq_status uq_set_launch_overlap(int enable) {
     uq::g_overlap.store(enable ? 1 : 0);
+    return UQ_OK;
+}
+
+uq_status uq_gemm_kernel_count(int M, int N, int K, int group, uq_fmt fmt, int* count) {
+    if (!count) return fail(UQ_ERR_INVALID, "null pointer");
+    *count = 0;
+    uq_status s = check_shape(N, K, group, fmt);
+    if (s != UQ_OK) return s;
+    if (M < 0) return fail(UQ_ERR_INVALID, "negative M");
+    if (M == 0 || N == 0) return UQ_OK;
+    if (K == 0) { *count = 1; return UQ_OK; }                          // the cudaMemsetAsync of y
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess || sms < 1) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice, "SM count");
+    int n = 0;
+    if (M >= 16 && uq::tc_supported(fmt, N, K)) {
+        // per block of at most 64 rows: the GEMM (K4: after its x column-sum pre-kernel)
+        for (int m0 = 0; m0 < M; m0 += 64) n += (fmt == UQ_K4) ? 2 : 1;
+    } else {
+        // per block of at most 8 rows: the GEMV and, when its work split needs it, the second pass
+        const uq::Layout L(N, K, fmt);
+        for (int m0 = 0; m0 < M; m0 += 8) {
+            const int mb = (M - m0) < 8 ? (M - m0) : 8;
+            uq::GemvArgs a = {};
+            a.M = mb; a.N = N; a.K = K; a.group = group;
+            a.NB = L.NB; a.KB = L.KB; a.T = (long long)L.NB * L.KB;
+            long long P = (long long)sms * uq::gemv_warps(fmt);
+            a.P = (int)(P > a.T ? a.T : P);
+            uq::gemv_grid(a, fmt, sms);
+            const bool mma = fmt == UQ_INT4_SYM || fmt == UQ_INT4_ASYM || fmt == UQ_INT2_ASYM || fmt == UQ_K4;
+            n += 1 + ((mma && !a.cta_rows) ? 1 : 0);
+        }
+    }
+    *count = n;
     return UQ_OK;
 }
 

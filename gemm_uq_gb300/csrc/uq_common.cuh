@@ -243,7 +243,6 @@ __device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint
 // fault codes written to the device fault word
 constexpr unsigned int FAULT_GEMV_WAIT = 1u;
 constexpr unsigned int FAULT_TC_WAIT = 2u;
-constexpr unsigned int FAULT_TC_BOUNDS = 8u;    // a tensor-core copy address failed its self-check
 constexpr unsigned int FAULT_GEMV_SPLIT = 4u;   // a launch's work split exceeded what the kernel holds
 
 }  // namespace uq

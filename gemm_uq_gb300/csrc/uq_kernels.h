@@ -61,21 +61,19 @@ struct TcArgs {
     const uint8_t* scales;    // fp16 [N][K/group] or K4 records
     const uint8_t* zc;        // INT4_ASYM zero nibbles, else NULL
     uint16_t* y;              // bf16 [M][ldy]
-    const float* xscale;      // [Mpad] power-of-two scale of each fp16 x row (0 for padding rows)
+    const float* sx;          // K4: column sums of x per 32-k block [K/32][Mpad], else NULL
     int M, Mpad, N, K, group, ldx, ldy;
     int CH;                   // units (chunks of 128 code bytes) per 128-row block
     long long U;              // units = ceil(N/128) * CH
     int P;                    // CTAs, P <= U
-    int stages, nabuf;        // shared-memory stages, tensor-memory A buffers
+    int stages, dslots;
     float* partials;          // [2P][128][Mpad]
     unsigned int* tickets;    // [ceil(N/128)]
     unsigned int* fault;
 };
 bool tc_supported(int fmt, int N, int K);
-int tc_plan(int fmt, int mpad, int* stages, int* nabuf, size_t* smem);
-// x rows -> fp16 [M][K] scaled by 2^-e_m, xs[m] = 2^e_m (xs[M .. mpad) = 0)
-cudaError_t launch_tc_prep(const uint16_t* x, int ldx, int K, int M, int mpad, uint16_t* xh, float* xs,
-                           cudaStream_t st);
-cudaError_t launch_tc(int fmt, const uint16_t* xh, const TcArgs& a, size_t smem, int grid, cudaStream_t st);
+int tc_plan(int fmt, int mpad, int* stages, int* dslots, size_t* smem);
+cudaError_t launch_colsum32(const uint16_t* x, float* sx, int M, int mpad, int K, int ldx, cudaStream_t st);
+cudaError_t launch_tc(int fmt, const uint16_t* x, const TcArgs& a, size_t smem, int grid, cudaStream_t st);
 
 }  // namespace uq

@@ -184,11 +184,19 @@ uq_status uq_pack_zeros(const uint8_t* zeros, uint8_t* packed, int N, int G, voi
 uq_status uq_set_launch_overlap(int enable);
 
 /*
+ * uq_gemm_kernel_count -- how many kernels uq_gemm launches for this shape on the current device
+ * (the GEMV, or its second pass for rows shared between SMs; the tensor-core x conversion, GEMM
+ * and second pass), for callers that account for launches.  Queries the device's SM count
+ * (CUDA runtime, no kernel launched, nothing allocated).  *count = 0 for an empty call.
+ * UQ_ERR_INVALID / UQ_ERR_UNSUPPORTED as uq_gemm for shapes it rejects.
+ */
+uq_status uq_gemm_kernel_count(int M, int N, int K, int group, uq_fmt fmt, int* count);
+
+/*
  * uq_device_fault -- reads and clears the device-side fault word of the current device
  * (bit 0 / bit 1: a GEMV / tensor-core kernel's bounded wait on an mbarrier ran out and the
  * kernel returned early instead of hanging; bit 2: a GEMV launch was given a work split larger
- * than the kernel holds and computed nothing; bit 3: a tensor-core copy address failed the
- * kernel's self-check and was skipped).  Synchronizes the device.  *flag = 0 when no fault.
+ * than the kernel holds and computed nothing).  Synchronizes the device.  *flag = 0 when no fault.
  */
 uq_status uq_device_fault(unsigned int* flag);
 

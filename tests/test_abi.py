@@ -78,3 +78,12 @@ def test_gemm_host_validation_needs_no_gpu(L):
     mis = P(al.value + 2)
     assert L.uq_gemm(mis, al, al, None, al, 1, 8, 256, 32, 0, None) == 3            # misaligned x
     assert L.uq_gemm(al, al, al, None, mis, 1, 8, 256, 32, 0, None) == 3            # misaligned y
+
+
+def test_kernel_count_host_validation(L):
+    # shape errors and empty calls are answered on the host, before any CUDA call
+    n = ctypes.c_int(-1)
+    assert L.uq_gemm_kernel_count(1, 8, 256, 48, 0, ctypes.byref(n)) == 2   # group 48
+    assert L.uq_gemm_kernel_count(-1, 8, 256, 32, 0, ctypes.byref(n)) == 1  # M < 0
+    assert L.uq_gemm_kernel_count(0, 8, 256, 32, 0, ctypes.byref(n)) == 0 and n.value == 0
+    assert L.uq_gemm_kernel_count(1, 8, 256, 32, 0, None) == 1              # no output pointer

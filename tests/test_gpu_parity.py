@@ -153,6 +153,19 @@ def test_determinism_and_batched_rows(fmt, group):
         assert torch.equal(y1[0].view(torch.int16), y[m].view(torch.int16)), f"row {m} differs from M=1 call"
 
 
+def test_kernel_count_matches_the_paths():
+    # 14336 x 4096 at M = 1: whole row blocks per CTA, one launch; 4096 x 14336: the stream-K split
+    # and its second pass; the tensor-core path: one GEMM per 64 rows (K4: after its x column-sum
+    # pre-kernel); M = 20 on the GEMV formats without tensor cores: three 8-row blocks
+    assert uq.gemm_kernel_count(1, 14336, 4096, 128, "INT4_ASYM") == 1
+    assert uq.gemm_kernel_count(1, 4096, 14336, 128, "INT4_ASYM") == 2
+    assert uq.gemm_kernel_count(1, 8192, 8192, 128, "INT8_SYM") == 1
+    assert uq.gemm_kernel_count(64, 14336, 4096, 128, "INT4_ASYM") == 1
+    assert uq.gemm_kernel_count(128, 14336, 4096, 128, "INT4_ASYM") == 2
+    assert uq.gemm_kernel_count(32, 8192, 8192, 256, "K4") == 2
+    assert uq.gemm_kernel_count(20, 4096, 4096, 64, "NF4") == 3
+
+
 def test_edge_cases():
     fmt, group = "INT4_ASYM", 128
     # M == 0 and N == 0 are no-ops; K == 0 writes zeros
