@@ -205,7 +205,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1 + TC_DQ_WARPS); }
+        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
         for (int i = 0; i < 2; ++i) { mbar_init(&afull[i], TC_DQ_WARPS); mbar_init(&aempty[i], 1); }
         for (int d = 0; d < DS; ++d) { mbar_init(&dfull[d], 1); mbar_init(&dempty[d], 4); }
         mbar_init(ebar, 128);
@@ -226,34 +226,20 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         if (lane == 0) {
             int issued = 0;
             const uint64_t pol = l2_evict_first_policy();
-            auto issue_codes = [&](int rb, int c, int s) {
-                uint8_t* st = smem + s * SB;
-                // for each of the 8 row blocks of 16, the unit's 4 chunks (2 KB, contiguous)
-                const int nb0 = rb * 8;
-                const int nbs = (a.NB - nb0) < 8 ? (a.NB - nb0) : 8;
-                mbar_arrive_expect_tx(&full[s], (uint32_t)(nbs * 2048 + XB));
-                const int kb = c >> 2, q0 = (c & 3) * 4;
-                for (int j = 0; j < nbs; ++j)
-                    bulk_g2s_stream(st + j * 2048, a.wq + (long long)(nb0 + j) * 16 * a.rowbytes + (long long)kb * 8192 + q0 * 512,
-                                    2048u, &full[s], pol);
-            };
             auto issue_x = [&](int c, int s) {
                 uint8_t* st = smem + s * SB;
 #pragma unroll
                 for (int q = 0; q < KC / 64; ++q)
                     tma_load_2d(st + TC_STAGE_CODES + q * (MPAD * 128), &tmap_x, c * KC + q * 64, 0, &full[s]);
             };
-            // the first stages' weights are constant: stream them before waiting for the previous
-            // kernel on the stream (launch overlap); x is loaded only after that wait
+            // x may be written by the kernel before on the stream: loaded after the wait for it (the
+            // dequant warps request the codes themselves)
             const int pre = (u1 - u0) < S ? (int)(u1 - u0) : S;
             const int CH = a.CH;
             int rb = (int)(u0 / CH), c = (int)(u0 % CH);
-            for (int j = 0, r2 = rb, c2 = c; j < pre; ++j) {
-                issue_codes(r2, c2, j);
-                if (++c2 == CH) { c2 = 0; ++r2; }
-            }
             asm volatile("griddepcontrol.wait;" ::: "memory");
             for (int j = 0; j < pre; ++j) {
+                mbar_arrive_expect_tx(&full[j], (uint32_t)XB);
                 issue_x(c, j);
                 if (++c == CH) { c = 0; ++rb; }
             }
@@ -266,7 +252,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     *abort_flag = 1;
                     break;
                 }
-                issue_codes(rb, c, s);
+                mbar_arrive_expect_tx(&full[s], (uint32_t)XB);
                 issue_x(c, s);
                 if (++c == CH) { c = 0; ++rb; }
                 if (++s == S) s = 0;
@@ -323,8 +309,22 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         const int g = lane >> 2, c4 = lane & 3;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter + 16 * hf) << 16);
         uint32_t* zr = dq_ring + (warp - 4) * 32;       // this warp's slot: 16 rows x 2 words
-        // INT4_ASYM: the zero-point words of rows g and g + 8, staged three units ahead by lanes c = 0, 1
+        // Unit u's copies, two units ahead, one cp.async group per unit: this warp's 2 KB of codes
+        // (16-row block rb * 8 + rbl, k tile c / 4, chunks (c % 4) * 4 .. + 3, contiguous in the
+        // fragment-order plane) into stage (u - u0) % S, and for INT4_ASYM the zero-point words of
+        // rows g and g + 8 (lanes c = 0, 1).  A single thread issuing the eight 2 KB bulk copies of
+        // a unit could not keep up with the stream (~0.14 us per copy).
         auto issue_zeros = [&](long long u) {
+            if (u < u1) {
+                const int rbc = (int)u / a.CH, cc = (int)u % a.CH;
+                if (rbc * 8 + rbl < a.NB) {
+                    const uint8_t* src = a.wq + (long long)(rbc * 8 + rbl) * 16 * a.rowbytes + (long long)(cc >> 2) * 8192 +
+                                         (cc & 3) * 4 * 512;
+                    uint8_t* dst = smem + ((int)(u - u0) % S) * SB + rbl * 2048;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) tc_cp_async16(dst + q * 512 + lane * 16, src + q * 512 + lane * 16);
+                }
+            }
             if constexpr (FMT == UQ_INT4_ASYM) {
                 if (u < u1 && c4 < 2) {
                     const int rb = (int)u / a.CH, c = (int)u % a.CH;
@@ -335,8 +335,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                         stage_span(zr + ((int)(u - u0) % 3) * (TC_DQ_WARPS * 32) + r * 2, a.zc,
                                    n * ZB + (long long)c * (GPC >> 1), GPC >> 1, (long long)a.N * ZB);
                 }
-                cp_async_commit();
             }
+            cp_async_commit();
         };
         issue_zeros(u0);
         issue_zeros(u0 + 1);
@@ -351,9 +351,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             uint32_t zlo[ZG], zhi[ZG];
 #pragma unroll
             for (int j = 0; j < ZG; ++j) zlo[j] = zhi[j] = (FMT == UQ_INT4_SYM) ? 0x43084308u : 0x43004300u;
+            cp_async_wait2();                               // unit u's codes (and zero words) landed
+            __syncwarp();
             if constexpr (FMT == UQ_INT4_ASYM) {
-                cp_async_wait2();
-                __syncwarp();
                 const int Gn = a.K / G, ZB = (Gn + 1) >> 1;
                 const uint32_t* slot = zr + zslot * (TC_DQ_WARPS * 32);
 #pragma unroll
@@ -373,8 +373,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     }
                 }
             }
-            bool ok = mbar_wait_bounded(&full[s], sph, a.fault, FAULT_TC_WAIT) &&
-                      mbar_wait_bounded(&aempty[ab], aph, a.fault, FAULT_TC_WAIT);
+            bool ok = mbar_wait_bounded(&aempty[ab], aph, a.fault, FAULT_TC_WAIT);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) { *abort_flag = 1; break; }
             tc_fence_after();
@@ -423,7 +422,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) { mbar_arrive(&afull[ab]); mbar_arrive(&empty[s]); }
+            if (lane == 0) mbar_arrive(&afull[ab]);
             if (++s == S) { s = 0; sph ^= 1u; }
             ab ^= 1;
             if (ab == 0) aph ^= 1u;
@@ -691,7 +690,7 @@ int tc_plan(int fmt, int mpad, int* stages, int* dslots, size_t* smem) {
     const int budget = 227 * 1024 - 1024 - TC_BAR_BYTES - rings;
     int s = budget / sb;
     if (s > 6) s = 6;
-    if (s < 2) return -1;
+    if (s < 3) return -1;                           // codes are requested two units ahead
     int ds = (TMEM_COLS - kc) / mpad;       // A takes 2 * kc/2 columns
     if (ds > 8) ds = 8;
     *stages = s;
