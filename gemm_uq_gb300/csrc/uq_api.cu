@@ -162,7 +162,7 @@ uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const 
         return fail(UQ_ERR_UNSUPPORTED, "K=%d is too long for the GEMV's shared-memory x-sum table at M=%d", K, Mb);
     const long long T = (long long)L.NB * L.KB;
     const int warps = uq::gemv_warps(fmt);
-    long long P = (long long)ds.sms * warps;
+    long long P = (long long)ds.sms * uq::gemv_ctas_per_sm(fmt) * warps;
     if (P > T) P = T;
     Workspace* ws = nullptr;
     uq_status s = workspace(dev, st, uq::gemv_partials_floats(fmt, T, (int)P, Mb) * sizeof(float),
@@ -457,7 +457,7 @@ uq_status uq_gemm_kernel_count(int M, int N, int K, int group, uq_fmt fmt, int* 
             uq::GemvArgs a = {};
             a.M = mb; a.N = N; a.K = K; a.group = group;
             a.NB = L.NB; a.KB = L.KB; a.T = (long long)L.NB * L.KB;
-            long long P = (long long)sms * uq::gemv_warps(fmt);
+            long long P = (long long)sms * uq::gemv_ctas_per_sm(fmt) * uq::gemv_warps(fmt);
             a.P = (int)(P > a.T ? a.T : P);
             uq::gemv_grid(a, fmt, sms);
             const bool mma = fmt == UQ_INT4_SYM || fmt == UQ_INT4_ASYM || fmt == UQ_INT2_ASYM || fmt == UQ_K4;

@@ -19,7 +19,8 @@ int gemv_grid(GemvArgs& a, int fmt, int sms) {
     // under the stream-K split and either the busiest CTA streams at most ~6 % more bytes than the
     // average one (bandwidth-bound shapes) or no warp has more than one tile (latency-bound ones).
     const int W = gemv_warps(fmt);
-    const int G = a.NB < sms ? a.NB : sms;
+    const int slots = sms * MMA_CTAS_PER_SM;                           // CTAs resident at once
+    const int G = a.NB < slots ? a.NB : slots;
     const long long rbs = (a.NB + G - 1) / G;
     const long long per_warp_rows = (rbs * a.KB + W - 1) / W;
     const long long per_warp_split = (a.T + a.P - 1) / a.P;
@@ -28,8 +29,9 @@ int gemv_grid(GemvArgs& a, int fmt, int sms) {
         a.cta_rows = 1;
         return G;
     }
-    return a.P < sms ? a.P : sms;
+    return a.P < slots ? a.P : slots;
 }
+int gemv_ctas_per_sm(int fmt) { return gemv_ctas_per_sm_impl(fmt); }
 size_t gemv_partials_floats(int fmt, long long T, int P, int M) {
     // mma GEMV: one 16-row slot per tile (k-major tiles, summed over k by the second pass);
     // CUDA-core GEMV: two slots per worker (the first and last row block of its range)

@@ -676,10 +676,14 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
 // one or two rows of x the warp copies only that k tile's slice of x, once per run.  Every tile's
 // partial sums are stored (shared memory when the CTA owns whole row blocks, global memory
 // otherwise) and summed over the k tiles in a fixed order afterwards.
+// Two CTAs of 4 warps per SM (INT2: 3) rather than one of 8: the same warps per SM, and each
+// CTA's shared memory (~105 KB) leaves room for a CTA of the next kernel on the stream, which with
+// launch overlap starts streaming its weights while this kernel's last CTAs finish.
 template <int FMT> struct MmaCfg {
-    static constexpr int WARPS = (FMT == UQ_INT2_ASYM) ? 6 : 8;    // workers per CTA
+    static constexpr int WARPS = (FMT == UQ_INT2_ASYM) ? 3 : 4;    // workers per CTA
     static constexpr int STAGES = 2;                               // tiles in flight per worker
 };
+constexpr int MMA_CTAS_PER_SM = 2;
 constexpr int MMA_TPW = 4;        // tiles per warp at most when the CTA owns whole row blocks
 
 // bytes per row of x in shared memory: 32 bytes of padding put the four rows a half-warp's 8-byte
@@ -722,15 +726,17 @@ __host__ __device__ inline GemvSmem gemv_mma_smem_plan(int fmt, int K, int group
     if (xm == MMA_X_SLICE) p.total += (size_t)warps * 2 * M * gemv_mma_xslice_stride(fmt, M);
     return p;
 }
-// x slices for one or two rows, else the whole x if it fits, else global memory
+// x slices for one or two rows, else the whole x if it fits, else global memory (each within the
+// shared memory that keeps MMA_CTAS_PER_SM CTAs on an SM)
+constexpr int MMA_SMEM_LIMIT = (228 * 1024) / MMA_CTAS_PER_SM - 1024;
 __host__ __device__ inline int gemv_mma_xmode(int fmt, int K, int group, int M) {
-    if (M <= 2 && gemv_mma_smem_plan(fmt, K, group, M, MMA_X_SLICE).total <= 227 * 1024) return MMA_X_SLICE;
-    if (gemv_mma_smem_plan(fmt, K, group, M, MMA_X_WHOLE).total <= 227 * 1024) return MMA_X_WHOLE;
+    if (M <= 2 && gemv_mma_smem_plan(fmt, K, group, M, MMA_X_SLICE).total <= MMA_SMEM_LIMIT) return MMA_X_SLICE;
+    if (gemv_mma_smem_plan(fmt, K, group, M, MMA_X_WHOLE).total <= MMA_SMEM_LIMIT) return MMA_X_WHOLE;
     return MMA_X_GLOBAL;
 }
 
 template <int FMT, int GB, int XM>
-__global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, 1) gemv_mma_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv_mma_kernel(const GemvArgs a) {
     using F = GemvFmt<FMT>;
     constexpr int KT = F::KT, S = MmaCfg<FMT>::STAGES, W = MmaCfg<FMT>::WARPS;
     constexpr int GS = GB * 16;                                     // k per scaling group
@@ -1105,6 +1111,7 @@ inline int gemv_warps_impl(int fmt) {
     }
 }
 inline size_t gemv_partials_floats_impl(int P, int M) { return (size_t)2 * P * RB * M; }
+inline int gemv_ctas_per_sm_impl(int fmt) { return gemv_is_mma(fmt) ? MMA_CTAS_PER_SM : 1; }
 
 namespace gemv_detail {
 template <int FMT, int M, bool XS>

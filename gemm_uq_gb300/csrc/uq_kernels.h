@@ -45,6 +45,7 @@ struct GemvArgs {
 constexpr int GEMV_WARPS = 4;     // worker warps per CTA
 size_t gemv_smem_bytes(int fmt, int K, int group, int M);
 int gemv_warps(int fmt);     // workers (warps) per CTA of the GEMV for this format
+int gemv_ctas_per_sm(int fmt);   // CTAs of the GEMV resident per SM (workers = SMs x this x warps)
 // work split of a GEMV launch whose a.P (stream-K workers) is set: may switch the mma GEMV to
 // whole row blocks per CTA (a.cta_rows = 1); returns the grid
 int gemv_grid(GemvArgs& a, int fmt, int sms);

@@ -116,7 +116,7 @@ uq_status uq_gemm_noalloc(const uint16_t* x, const void* wq, const void* scales,
     const uq::Layout L(N, K, fmt);
     const long long T = (long long)L.NB * L.KB;
     const int warps = uq::gemv_warps(fmt);
-    long long P = (long long)sms * warps;
+    long long P = (long long)sms * uq::gemv_ctas_per_sm(fmt) * warps;
     if (P > T) P = T;
     const int mb_max = M < 8 ? M : 8;
     if ((size_t)L.NB * sizeof(unsigned int) > TICKET_BYTES ||
