@@ -1042,7 +1042,10 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
             }
         };
         if (ng == GPT) {
-#pragma unroll 4
+            // 8 groups per step for 32-k groups: a K4 record (8 sub-blocks) is then read and
+            // decoded once per row per step, its 6-bit fields at constant shifts
+            constexpr int GUNROLL = (GB == 2) ? 8 : 4;
+#pragma unroll GUNROLL
             for (int gg = 0; gg < GPT; ++gg) group_step(gg);
         } else {
 #pragma unroll 1
