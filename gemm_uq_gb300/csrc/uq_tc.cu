@@ -16,10 +16,11 @@
 // So the products and the per-group sums are exact up to fp32 accumulation, as in the GEMV.
 //
 // Roles (512 threads, one CTA per SM, persistent over an equal contiguous range of units):
-//   warp 0       producer: per unit eight 2 KB bulk copies of codes (one per 16-row block of the
-//                fragment-order plane) and kc/64 TMA boxes of x, counted on full[stage];
-//   warp 1       MMA issuer (one thread): per group g/16 tcgen05.mma (M=128, N=Mpad, K=16);
-//   warps 4..11  dequant: warp = one 16-row block; lane (g, c) turns its fragment-order words
+//   warp 0       producer: per unit kc/64 TMA boxes of x, counted on full[stage];
+//   warps 1, 2   MMA issuers (one thread each; for Mpad <= 32 two of them, on alternate units):
+//                per group g/16 tcgen05.mma (M=128, N=Mpad, K=16) into the issuer's slots;
+//   warps 4..11  dequant: warp = one 16-row block; it copies its 2 KB of codes per unit itself
+//                (cp.async, two units ahead), and lane (g, c) turns its fragment-order words
 //                into (q - z) bf16 pairs and stores them with tcgen05.st.16x256b (the store
 //                shape whose thread layout is the mma fragment's), kc/2 columns per unit;
 //   warps 12..15 epilogue: thread = weight row; scales, accumulates over the row block's units,
@@ -40,6 +41,7 @@ constexpr int TC_ROWS = 128;
 constexpr int TC_STAGE_CODES = TC_ROWS * 128;     // bytes of codes per stage
 constexpr int TMEM_COLS = 512;
 constexpr int TC_BAR_BYTES = 2048;                 // barriers and flags after the stages
+constexpr int TC_MAX_STAGES = 6;
 
 __device__ __forceinline__ long long trange_begin(int c, long long U, int P) { return (long long)c * U / P; }
 __device__ __forceinline__ int tworker_of(long long u, long long U, int P) {
@@ -179,6 +181,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
     constexpr int SB = TcSmem::stage_bytes(KC, MPAD);
     constexpr int SWORDS = TcFmt<FMT>::SWORDS;
     constexpr uint32_t IDESC = idesc_bf16(MPAD);
+    constexpr int NISS = MPAD <= 32 ? 2 : 1;        // MMA issuing threads
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -261,13 +264,21 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             for (int j = issued - 1; j >= 0 && j >= issued - S; --j)
                 mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1), a.fault, FAULT_TC_WAIT);
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || (NISS == 2 && warp == 2)) {
+        // ---------------------------------------------------------------- MMA issuers
+        // A thread issuing tcgen05.mma is held for tens of cycles per instruction, longer than
+        // MMAs with N <= 32 keep the tensor pipe busy, so there two threads issue: warp 1 the
+        // CTA's even units (A buffer 0, accumulator slots [0, DH)), warp 2 the odd ones (A buffer
+        // 1, slots [DH, 2 DH)).  Each thread's MMAs and commits stay in its own order.
         if (lane == 0) {
-            int s = 0, ab = 0, d = 0;
-            uint32_t sph = 0, aph = 0, dph = 0;          // phases of full[s], afull[ab], dempty[d] (^1)
+            const int me = warp - 1, DH = DS / NISS;
+            int d = 0;
+            uint32_t dph = 0;                            // phase of dempty[me * DH + d] (^1)
             const int KS = G / 16;                       // MMAs per group
-            for (long long u = u0; u < u1 && !*abort_flag; ++u) {
+            for (long long u = u0 + me; u < u1 && !*abort_flag; u += NISS) {
+                const int i = (int)(u - u0);
+                const int s = i % S, ab = i & 1;
+                const uint32_t sph = (uint32_t)((i / S) & 1), aph = (uint32_t)((i >> 1) & 1);
                 bool ok = mbar_wait_bounded(&full[s], sph, a.fault, FAULT_TC_WAIT) &&
                           mbar_wait_bounded(&afull[ab], aph, a.fault, FAULT_TC_WAIT);
                 if (!ok) { *abort_flag = 1; break; }
@@ -278,25 +289,23 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                 const uint32_t acol0 = tmem + A_COL0 + ab * ACOLS;
                 int ks = 0;
                 for (int j = 0; j < GPC; ++j) {
-                    if (!mbar_wait_bounded(&dempty[d], dph ^ 1u, a.fault, FAULT_TC_WAIT)) {
+                    const int slot = me * DH + d;
+                    if (!mbar_wait_bounded(&dempty[slot], dph ^ 1u, a.fault, FAULT_TC_WAIT)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t dcol = tmem + D_COL0 + d * MPAD;
+                    const uint32_t dcol = tmem + D_COL0 + slot * MPAD;
                     for (int t = 0; t < KS; ++t, ++ks) {
                         const uint64_t bdesc = bdesc0 + (uint64_t)((ks >> 2) * (MPAD * 8) + (ks & 3) * 2);
                         mma_ts(dcol, acol0 + ks * 8, bdesc, IDESC, t > 0 ? 1u : 0u);
                     }
-                    tc_commit(&dfull[d]);
-                    if (++d == DS) { d = 0; dph ^= 1u; }
+                    tc_commit(&dfull[slot]);
+                    if (++d == DH) { d = 0; dph ^= 1u; }
                 }
                 if (!ok) { *abort_flag = 1; break; }
                 tc_commit(&aempty[ab]);
                 tc_commit(&empty[s]);
-                if (++s == S) { s = 0; sph ^= 1u; }
-                ab ^= 1;
-                if (ab == 0) aph ^= 1u;
             }
         }
     } else if (warp >= 4 && warp < 4 + TC_DQ_WARPS) {
@@ -429,7 +438,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             if (++zslot == 3) zslot = 0;
             if (++c == a.CH) { c = 0; ++rb; }
         }
-        if constexpr (FMT == UQ_INT4_ASYM) asm volatile("cp.async.wait_all;" ::: "memory");
+        asm volatile("cp.async.wait_all;" ::: "memory");   // no copy lands after the CTA left
     } else if (warp >= 4 + TC_DQ_WARPS) {
         // ---------------------------------------------------------------- epilogue warpgroup
         asm volatile("griddepcontrol.wait;" ::: "memory");   // sx, workspace and y follow earlier work
@@ -459,8 +468,11 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         float acc[MPAD];
 #pragma unroll
         for (int m = 0; m < MPAD; ++m) acc[m] = 0.f;
-        int d = 0, eslot = 0;
-        uint32_t dph = 0, ephase = 0;
+        // accumulator slots: unit u's groups are in the ring of the issuer that took it ((u - u0) mod
+        // the issuer count), slots [DH * ring, DH * ring + DH), consumed in that issuer's order
+        const int DH = DS / NISS;
+        int dring[2] = {0, 0}, eslot = 0;
+        uint32_t dphr[2] = {0u, 0u}, ephase = 0;
         // all 128 epilogue threads meet here (bounded: returns false after the time limit)
         auto epi_sync = [&]() -> bool {
             mbar_arrive(ebar);
@@ -478,6 +490,9 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             const uint32_t* sw = er + eslot * (128 * SWORDS);
             if (++eslot == 3) eslot = 0;
             const int so = live ? (int)(((long long)n * (a.K / G) + (long long)c * GPC) & 1) : 0;   // halves
+            const int ring = NISS == 2 ? (int)((u - u0) & 1) : 0;
+            int d = ring ? dring[1] : dring[0];
+            uint32_t dph = ring ? dphr[1] : dphr[0];
             bool ok = true;
             for (int j = 0; j < GPC; ++j) {
                 float s1 = 0.f, s2 = 0.f;
@@ -492,27 +507,37 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                         s1 = half_bits_f32(reinterpret_cast<const uint16_t*>(sw)[so + j]);
                     }
                 }
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&dfull[d], dph, a.fault, FAULT_TC_WAIT));
+                const int slot = ring * DH + d;
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&dfull[slot], dph, a.fault, FAULT_TC_WAIT));
                 if (!ok) break;
                 tc_fence_after();
+                // up to 32 columns per wait for the loads (more would spill beside acc[64])
+                constexpr int QN = MPAD / 16, QB = QN < 2 ? QN : 2;
 #pragma unroll
-                for (int q = 0; q < MPAD / 16; ++q) {
-                    float v[16];
-                    tmem_ld16(lane_addr + D_COL0 + d * MPAD + q * 16, v);
+                for (int q0 = 0; q0 < QN; q0 += QB) {
+                    float v[QB][16];
+#pragma unroll
+                    for (int q = 0; q < QB; ++q)
+                        if (q0 + q < QN) tmem_ld16(lane_addr + D_COL0 + slot * MPAD + (q0 + q) * 16, v[q]);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) acc[q * 16 + e] = fmaf(s1, v[e], acc[q * 16 + e]);
+                    for (int q = 0; q < QB; ++q)
+                        if (q0 + q < QN)
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                acc[(q0 + q) * 16 + e] = fmaf(s1, v[q][e], acc[(q0 + q) * 16 + e]);
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&dempty[d]);
-                if (++d == DS) { d = 0; dph ^= 1u; }
+                if (lane == 0) mbar_arrive(&dempty[slot]);
+                if (++d == DH) { d = 0; dph ^= 1u; }
                 if constexpr (FMT == UQ_K4) {
                     const float* sx = a.sx + (long long)((c * KC + j * 32) >> 5) * MPAD;
 #pragma unroll
                     for (int m = 0; m < MPAD; ++m) acc[m] = fmaf(-s2, __ldg(sx + m), acc[m]);
                 }
             }
+            if (ring) { dring[1] = d; dphr[1] = dph; } else { dring[0] = d; dphr[0] = dph; }
             if (!ok) { *abort_flag = 1; break; }
             if (c == a.CH - 1 || u == u1 - 1) {
                 // row block finished for this CTA: store y, or a partial and a ticket
@@ -689,7 +714,7 @@ int tc_plan(int fmt, int mpad, int* stages, int* dslots, size_t* smem) {
     }
     const int budget = 227 * 1024 - 1024 - TC_BAR_BYTES - rings;
     int s = budget / sb;
-    if (s > 6) s = 6;
+    if (s > TC_MAX_STAGES) s = TC_MAX_STAGES;
     if (s < 3) return -1;                           // codes are requested two units ahead
     int ds = (TMEM_COLS - kc) / mpad;       // A takes 2 * kc/2 columns
     if (ds > 8) ds = 8;
