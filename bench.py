@@ -57,6 +57,8 @@ WORKLOADS = {
     "k4-70b-stack": dict(fmt="K4", group=256, sigma=0.015, outlier_p=0.0, layers=8, linears=_L70, m=1,
                          title="70B-shaped decode linear stack (8 layers x 7), two-level INT4"),
 }
+# linears that read the same input as the linear before them in a decoder layer
+SHARES_INPUT_WITH_PREVIOUS = ("k", "v", "up")
 BITS = {"INT4_SYM": 4, "INT4_ASYM": 4, "INT8_SYM": 8, "INT2_ASYM": 2, "NF4": 4, "K4": 4}
 
 
@@ -265,20 +267,46 @@ def run_uq(args, rank, world, dist):
     step_bytes = sum(alg_bytes(fmt, group, r["N"], r["K"], M) for r in recs)
 
     stream = torch.cuda.Stream(device=dev)
-    sh = stream.cuda_stream
     # consecutive linears of a decode step read fixed weights: let each launch stream its weights
     # while the previous one drains (uq_set_launch_overlap)
     uq.set_launch_overlap(not args.no_overlap)
 
+    def launch(r, st):
+        uq.gemm_ptrs(r["x"].data_ptr(), r["wq"].data_ptr(), r["scales"].data_ptr(),
+                     r["zc"].data_ptr() if r["zc"] is not None else 0, r["y"].data_ptr(),
+                     M, r["N"], r["K"], group, fmt, st.cuda_stream)
+
+    # Linears that read the same input in a decoder layer (q, k, v; gate, up) do not depend on one
+    # another: the step launches each such group on parallel branches (side streams forked from and
+    # joined back to the main stream); every other linear follows the one before it.
+    groups = []
+    for i, r in enumerate(recs):
+        if groups and r["name"].split(".")[-1] in SHARES_INPUT_WITH_PREVIOUS:
+            groups[-1].append(i)
+        else:
+            groups.append([i])
+    width = max(len(gr) for gr in groups)
+    side = [torch.cuda.Stream(device=dev) for _ in range(width - 1)]
+
     def issue(events=None):
-        for i, r in enumerate(recs):
-            if events is not None:
+        if events is not None:             # per-launch timing: one launch after another
+            for i, r in enumerate(recs):
                 events[i][0].record(stream)
-            uq.gemm_ptrs(r["x"].data_ptr(), r["wq"].data_ptr(), r["scales"].data_ptr(),
-                         r["zc"].data_ptr() if r["zc"] is not None else 0, r["y"].data_ptr(),
-                         M, r["N"], r["K"], group, fmt, sh)
-            if events is not None:
+                launch(r, stream)
                 events[i][1].record(stream)
+            return
+        for gr in groups:
+            if len(gr) > 1:
+                fork = torch.cuda.Event()
+                fork.record(stream)
+                for j, i in enumerate(gr[1:]):
+                    side[j].wait_event(fork)
+                    launch(recs[i], side[j])
+            launch(recs[gr[0]], stream)
+            for j in range(len(gr) - 1):
+                join = torch.cuda.Event()
+                join.record(side[j])
+                stream.wait_event(join)
 
     with torch.cuda.stream(stream):
         for _ in range(2):
@@ -383,7 +411,9 @@ def run_uq(args, rank, world, dist):
                    "linears_per_step": launches, "bytes_per_step": step_bytes,
                    "parallelism": f"replicas x{world}",
                    "l2": "no flush: packed weights per step exceed L2 (%.2f GB)" % (step_bytes / 1e9),
-                   "launch": "one CUDA graph per step",
+                   "launch": "one CUDA graph per step" + (
+                       "; linears reading the same input (q, k, v; gate, up) on parallel branches"
+                       if width > 1 else ""),
                    "launch_overlap": not args.no_overlap},
         "gpu_launches": sum(kernels_per_call(fmt, group, M, r["N"], r["K"]) for r in recs) * args.steps,
         "e2e": {"value": round(step_bytes * args.steps * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
