@@ -59,6 +59,21 @@ WORKLOADS = {
 }
 # linears that read the same input as the linear before them in a decoder layer
 SHARES_INPUT_WITH_PREVIOUS = ("k", "v", "up")
+
+
+def launch_groups(names):
+    """Indices of the step's linears grouped for launch: a linear whose short name (after the last
+    '.') reads the same input as the one before it joins that one's group; groups run in order, the
+    members of a group on parallel branches."""
+    groups = []
+    for i, name in enumerate(names):
+        if groups and name.split(".")[-1] in SHARES_INPUT_WITH_PREVIOUS:
+            groups[-1].append(i)
+        else:
+            groups.append([i])
+    return groups
+
+
 BITS = {"INT4_SYM": 4, "INT4_ASYM": 4, "INT8_SYM": 8, "INT2_ASYM": 2, "NF4": 4, "K4": 4}
 
 
@@ -279,12 +294,7 @@ def run_uq(args, rank, world, dist):
     # Linears that read the same input in a decoder layer (q, k, v; gate, up) do not depend on one
     # another: the step launches each such group on parallel branches (side streams forked from and
     # joined back to the main stream); every other linear follows the one before it.
-    groups = []
-    for i, r in enumerate(recs):
-        if groups and r["name"].split(".")[-1] in SHARES_INPUT_WITH_PREVIOUS:
-            groups[-1].append(i)
-        else:
-            groups.append([i])
+    groups = launch_groups([r["name"] for r in recs])
     width = max(len(gr) for gr in groups)
     side = [torch.cuda.Stream(device=dev) for _ in range(width - 1)]
 
