@@ -116,9 +116,14 @@ uq_status uq_pack_kmeta(const uint16_t* d, const uint16_t* dmin, const uint8_t* 
  *   M >= 0, N >= 0, K >= 0; M == 0 or N == 0 is a no-op; K == 0 writes zeros.
  *   group: 32, 64 or 128 for the flat formats (K % group == 0; UQ_INT2_ASYM also needs
  *   K % 64 == 0); 256 for UQ_K4 (K % 256 == 0).
- * Paths: M <= 8 one CUDA-core GEMV launch (split-K over the GPU's SMs, the partial
- * sums reduced in a fixed order, so repeated calls are bit-identical);
- * 9 <= M <= 15 the GEMV over row blocks of at most 8; M >= 16 the tcgen05 path.
+ * Paths: M <= 8 the GEMV (mma.sync tensor instructions for INT4_SYM, INT4_ASYM, INT2_ASYM
+ * and K4; CUDA-core FMAs for INT8_SYM and NF4): one launch when each CTA owns whole row
+ * blocks, else the GEMV and a second launch that sums each row's k-tile partials in a
+ * fixed order, so repeated calls are bit-identical; 9 <= M <= 15 the GEMV over row blocks
+ * of x of at most 8 rows; M >= 16 the tcgen05 tensor-core kernel for INT4_SYM, INT4_ASYM,
+ * INT8_SYM and K4 when K is a multiple of the code tile (1024 4-bit / 512 8-bit codes; K4
+ * adds a small column-sum launch), otherwise (and for INT2_ASYM and NF4) the GEMV over
+ * 8-row blocks of x.  uq_gemm_kernel_count gives the launches of a shape.
  * Scratch: a library-owned workspace per (device, stream), grown on the first call
  * that needs more; that growth is refused (UQ_ERR_NOMEM) while `stream` is being
  * captured, so make one call of the largest size before capturing.  Calls on the
