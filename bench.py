@@ -1,5 +1,5 @@
 #!/usr/bin/env python
-"""Benchmark of the quantized decode GEMV/GEMM: achieved GB/s and fraction of the HBM roofline.
+"""Benchmark of the quantized decode GEMV/GEMM: achieved GB/s, TFLOP/s and fraction of the HBM roofline.
 
 Default workload (one "step" = one decode token through every linear of an 8B-shaped decoder):
 32 layers x {q 4096x4096, k 1024x4096, v 1024x4096, o 4096x4096, gate 14336x4096,
@@ -9,9 +9,12 @@ quantized by the library's GPU quantizer and packed once (untimed); x is bf16 N(
 row per linear.  The 224 uq_gemm calls of a step are captured in one CUDA graph.  The packed
 weights (3.6 GB) exceed L2 (~129 MB), so no flush is needed between steps.
 
-Metric: algorithmic bytes (packed codes + scales + zeros + x + y, each once) per second.
+Metric: algorithmic bytes (packed codes + scales + zeros + x + y, each once) per second.  The
+same JSON line carries a `sweep` of the other workloads (the batched-decode M sweep, the
+8192 x 8192 format sweep and the 70B-shaped two-level INT4 stack), each timed on its own graph.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl uq|reference] [--workload NAME] [--m M]
+                    [--no-sweep] [--no-cpu-baseline]
 
 Under torchrun each rank runs an independent replica on its own GPU (the path has no
 exchange step); value = bytes of all ranks / max-over-ranks time ("weak" scaling).
@@ -34,8 +37,8 @@ if ROOT not in sys.path:
 
 METRIC = "quantized decode GEMV/GEMM GB/s and % of HBM roofline vs M (1 GB300)"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
-# (fmt, group, sigma, outlier_p, layers, linears, default M)
 _L8 = [("q", 4096, 4096), ("k", 1024, 4096), ("v", 1024, 4096), ("o", 4096, 4096),
        ("gate", 14336, 4096), ("up", 14336, 4096), ("down", 4096, 14336)]
 _L70 = [("q", 8192, 8192), ("k", 1024, 8192), ("v", 1024, 8192), ("o", 8192, 8192),
@@ -57,8 +60,15 @@ WORKLOADS = {
     "k4-70b-stack": dict(fmt="K4", group=256, sigma=0.015, outlier_p=0.0, layers=8, linears=_L70, m=1,
                          title="70B-shaped decode linear stack (8 layers x 7), two-level INT4"),
 }
+# The sweep carried in the default line: (workload, layers = weight copies per graph, M values).
+# Every graph streams more packed weight bytes than L2 holds, so each replay reads them from HBM.
+SWEEP = [("sweep-int4a", 8, (1, 2, 4, 8, 16, 32, 64)),
+         ("int8s-8192", 8, (1, 16)), ("int2a-8192", 16, (1, 16)), ("nf4-8192", 8, (1, 16)),
+         ("k4-70b-stack", 8, (1, 8, 32))]
 # linears that read the same input as the linear before them in a decoder layer
 SHARES_INPUT_WITH_PREVIOUS = ("k", "v", "up")
+BITS = {"INT4_SYM": 4, "INT4_ASYM": 4, "INT8_SYM": 8, "INT2_ASYM": 2, "NF4": 4, "K4": 4}
+KT = {"INT4_SYM": 1024, "INT4_ASYM": 1024, "INT8_SYM": 512, "INT2_ASYM": 2048, "NF4": 1024, "K4": 1024}
 
 
 def launch_groups(names):
@@ -72,9 +82,6 @@ def launch_groups(names):
         else:
             groups.append([i])
     return groups
-
-
-BITS = {"INT4_SYM": 4, "INT4_ASYM": 4, "INT8_SYM": 8, "INT2_ASYM": 2, "NF4": 4, "K4": 4}
 
 
 def alg_bytes(fmt, group, N, K, M):
@@ -92,6 +99,11 @@ def alg_bytes(fmt, group, N, K, M):
         elif fmt == "NF4":
             meta += 64
     return codes + meta + 2 * M * K + 2 * M * N
+
+
+def alg_flops(N, K, M):
+    """Multiply-adds of one linear counted as two flops each."""
+    return 2 * M * N * K
 
 
 def kernel_source_hash():
@@ -124,10 +136,23 @@ def read_traffic(workload, avg_alg_bytes):
         return None
 
 
-def dominant_kernel(fmt, group, M, recs):
+def read_share(workload):
+    """Share of the step's device time in the dominant kernel, from the committed ncu launch list."""
+    path = os.path.join(ROOT, "profiles", f"launches_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        if line.strip().startswith("- dominant_share:"):
+            try:
+                return float(line.split(":", 1)[1])
+            except ValueError:
+                return None
+    return None
+
+
+def dominant_kernel(fmt, group, M, shapes):
     """Name of the kernel template the library dispatches for this workload's linears."""
-    kt = {"INT4_SYM": 1024, "INT4_ASYM": 1024, "INT8_SYM": 512, "INT2_ASYM": 2048, "NF4": 1024, "K4": 1024}[fmt]
-    if M >= 16 and fmt in ("INT4_SYM", "INT4_ASYM", "INT8_SYM", "K4") and all(r["K"] % kt == 0 for r in recs):
+    if M >= 16 and fmt in ("INT4_SYM", "INT4_ASYM", "INT8_SYM", "K4") and all(K % KT[fmt] == 0 for _, K in shapes):
         mpad = (min(M, 64) + 15) // 16 * 16
         return f"tc_kernel<{fmt},{mpad}>"
     if fmt in ("INT4_SYM", "INT4_ASYM", "INT2_ASYM", "K4"):
@@ -138,23 +163,26 @@ def dominant_kernel(fmt, group, M, recs):
 
 def kernels_per_call(fmt, group, M, N, K):
     """Kernel launches one uq_gemm call of this shape makes on the current device, as the library
-    itself counts them (GEMV, or tensor-core x conversion + GEMM, plus a second pass where rows are
-    shared between SMs)."""
+    itself counts them."""
     import gemm_uq_gb300 as uq
     return uq.gemm_kernel_count(M, N, K, group, fmt)
 
 
-def measured_peak():
+def measured_peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, source) from MEASURED_PEAKS.json, else the fallback figures."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         try:
             d = json.load(open(path))
-            for key in ("hbm_gbs", "hbm_GBs", "hbm"):
-                if key in d:
-                    return float(d[key]), "measured"
+            return float(d["hbm_gbs"]), float(d.get("bf16_tflops", FALLBACK_BF16_TFLOPS)), "measured"
         except Exception:
             pass
-    return FALLBACK_HBM_GBS, "fallback"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def roofline_time_s(nbytes, flops, hbm_gbs, tflops):
+    """The roofline time: the slower of the bytes at HBM bandwidth and the flops at bf16 dense peak."""
+    return max(nbytes / (hbm_gbs * 1e9), flops / (tflops * 1e12))
 
 
 class ClockSampler:
@@ -214,7 +242,7 @@ def max_over_ranks(values, dist, device):
 
 
 # ---------------------------------------------------------------------------------------------
-def build_weights(spec, m, dev, seed_base=12345):
+def build_weights(spec, dev, layers=None, seed_base=12345):
     """Quantize and pack every linear of the workload on the GPU; returns per-linear records."""
     import torch
     import gemm_uq_gb300 as uq
@@ -227,7 +255,7 @@ def build_weights(spec, m, dev, seed_base=12345):
         cb = torch.from_numpy(np.loadtxt(os.path.join(ROOT, "tests", "golden", "nf4_codebook.txt"),
                                          dtype=np.float64).astype(np.float32)).to(dev)
     idx = 0
-    for layer in range(spec["layers"]):
+    for layer in range(layers or spec["layers"]):
         for name, N, K in spec["linears"]:
             gen.manual_seed(seed_base + idx)
             w = torch.randn((N, K), generator=gen, device=dev, dtype=torch.float32) * spec["sigma"]
@@ -252,6 +280,123 @@ def build_weights(spec, m, dev, seed_base=12345):
     return recs
 
 
+class Step:
+    """One pass over every linear of a workload at M rows: x and y buffers, the launch order (groups
+    of linears reading the same input on parallel branches), and its CUDA graph."""
+
+    def __init__(self, recs, fmt, group, M, dev, stream, seed):
+        import torch
+        self.recs, self.fmt, self.group, self.M, self.stream = recs, fmt, group, M, stream
+        x_sizes = [M * r["K"] for r in recs]
+        y_sizes = [M * r["N"] for r in recs]
+        # x of every linear in one device buffer (the end-to-end leg copies it with one memcpy)
+        self.xbuf = torch.empty(sum(x_sizes), dtype=torch.bfloat16, device=dev)
+        self.ybuf = torch.empty(sum(y_sizes), dtype=torch.bfloat16, device=dev)
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        self.xbuf.copy_(torch.randn(self.xbuf.numel(), generator=g, device=dev,
+                                    dtype=torch.float32).to(torch.bfloat16))
+        self.io = []
+        ox = oy = 0
+        for xs, ys in zip(x_sizes, y_sizes):
+            self.io.append((self.xbuf[ox:ox + xs], self.ybuf[oy:oy + ys]))
+            ox += xs
+            oy += ys
+        self.bytes = sum(alg_bytes(fmt, group, r["N"], r["K"], M) for r in recs)
+        self.flops = sum(alg_flops(r["N"], r["K"], M) for r in recs)
+        self.groups = launch_groups([r["name"] for r in recs])
+        width = max(len(gr) for gr in self.groups)
+        self.side = [torch.cuda.Stream(device=dev) for _ in range(width - 1)]
+        self.graph = None
+
+    def launch(self, i, st):
+        import gemm_uq_gb300 as uq
+        r = self.recs[i]
+        x, y = self.io[i]
+        uq.gemm_ptrs(x.data_ptr(), r["wq"].data_ptr(), r["scales"].data_ptr(),
+                     r["zc"].data_ptr() if r["zc"] is not None else 0, y.data_ptr(),
+                     self.M, r["N"], r["K"], self.group, self.fmt, st.cuda_stream)
+
+    def issue(self):
+        import torch
+        for gr in self.groups:
+            if len(gr) > 1:
+                fork = torch.cuda.Event()
+                fork.record(self.stream)
+                for j, i in enumerate(gr[1:]):
+                    self.side[j].wait_event(fork)
+                    self.launch(i, self.side[j])
+            self.launch(gr[0], self.stream)
+            for j in range(len(gr) - 1):
+                join = torch.cuda.Event()
+                join.record(self.side[j])
+                self.stream.wait_event(join)
+
+    def capture(self):
+        import torch
+        with torch.cuda.stream(self.stream):
+            for _ in range(2):
+                self.issue()               # grows the per-stream workspaces outside capture
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            self.issue()
+        torch.cuda.synchronize()
+        return self
+
+    def replay(self, n):
+        import torch
+        with torch.cuda.stream(self.stream):
+            for _ in range(n):
+                self.graph.replay()
+
+    def time(self, warmup, steps):
+        """Device time per replay (ms): CUDA events on the launching stream, synchronized on both sides."""
+        import torch
+        self.replay(warmup)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        self.replay(steps)
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    def launches(self):
+        return sum(kernels_per_call(self.fmt, self.group, self.M, r["N"], r["K"]) for r in self.recs)
+
+
+def run_sweep(dev, stream, hbm, tf):
+    """The M sweep, the format sweep and the 70B-shaped stack, each point on its own graph."""
+    import torch
+    out = []
+    for wl, layers, ms in SWEEP:
+        spec = WORKLOADS[wl]
+        fmt, group = spec["fmt"], spec["group"]
+        recs = build_weights(spec, dev, layers=layers, seed_base=20000)
+        shapes = sorted({(r["N"], r["K"]) for r in recs})
+        for M in ms:
+            st = Step(recs, fmt, group, M, dev, stream, seed=4242 + M).capture()
+            probe = st.time(3, 2)
+            reps = int(min(200, max(5, 25.0 / max(probe, 1e-3))))
+            ms_ = st.time(3, reps)
+            t_roof = roofline_time_s(st.bytes, st.flops, hbm, tf)
+            out.append({"workload": wl, "fmt": fmt, "group": group, "M": M, "linears": len(recs),
+                        "shapes": [f"{n}x{k}" for n, k in shapes],
+                        "GB/s": round(st.bytes / (ms_ * 1e-3) / 1e9, 1),
+                        "TFLOP/s": round(st.flops / (ms_ * 1e-3) / 1e12, 2),
+                        "frac": round(t_roof / (ms_ * 1e-3), 4),
+                        "bound": "hbm" if st.bytes / (hbm * 1e9) >= st.flops / (tf * 1e12) else "tensor",
+                        "us_per_linear": round(ms_ * 1e3 / len(recs), 2),
+                        "kernel": dominant_kernel(fmt, group, M, shapes), "launches": st.launches(),
+                        "reps": reps})
+            del st
+        del recs
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_uq(args, rank, world, dist):
     import torch
     import gemm_uq_gb300 as uq
@@ -260,79 +405,16 @@ def run_uq(args, rank, world, dist):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     spec = dict(WORKLOADS[args.workload])
-    if args.layers:
-        spec["layers"] = args.layers
     fmt, group = spec["fmt"], spec["group"]
     M = args.m if args.m else spec["m"]
-    recs = build_weights(spec, M, dev)
-
-    # x for every linear lives in one device buffer (so the e2e leg copies it with one memcpy)
-    x_sizes = [M * r["K"] for r in recs]
-    y_sizes = [M * r["N"] for r in recs]
-    xbuf = torch.empty(sum(x_sizes), dtype=torch.bfloat16, device=dev)
-    ybuf = torch.empty(sum(y_sizes), dtype=torch.bfloat16, device=dev)
-    g = torch.Generator(device=dev)
-    g.manual_seed(777 + rank)
-    xbuf.copy_(torch.randn(xbuf.numel(), generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16))
-    ox = oy = 0
-    for r, xs, ys in zip(recs, x_sizes, y_sizes):
-        r["x"], r["y"] = xbuf[ox:ox + xs], ybuf[oy:oy + ys]
-        ox += xs
-        oy += ys
-    step_bytes = sum(alg_bytes(fmt, group, r["N"], r["K"], M) for r in recs)
-
+    recs = build_weights(spec, dev, layers=args.layers or None)
     stream = torch.cuda.Stream(device=dev)
     # consecutive linears of a decode step read fixed weights: let each launch stream its weights
     # while the previous one drains (uq_set_launch_overlap)
     uq.set_launch_overlap(not args.no_overlap)
+    step = Step(recs, fmt, group, M, dev, stream, seed=777 + rank).capture()
 
-    def launch(r, st):
-        uq.gemm_ptrs(r["x"].data_ptr(), r["wq"].data_ptr(), r["scales"].data_ptr(),
-                     r["zc"].data_ptr() if r["zc"] is not None else 0, r["y"].data_ptr(),
-                     M, r["N"], r["K"], group, fmt, st.cuda_stream)
-
-    # Linears that read the same input in a decoder layer (q, k, v; gate, up) do not depend on one
-    # another: the step launches each such group on parallel branches (side streams forked from and
-    # joined back to the main stream); every other linear follows the one before it.
-    groups = launch_groups([r["name"] for r in recs])
-    width = max(len(gr) for gr in groups)
-    side = [torch.cuda.Stream(device=dev) for _ in range(width - 1)]
-
-    def issue(events=None):
-        if events is not None:             # per-launch timing: one launch after another
-            for i, r in enumerate(recs):
-                events[i][0].record(stream)
-                launch(r, stream)
-                events[i][1].record(stream)
-            return
-        for gr in groups:
-            if len(gr) > 1:
-                fork = torch.cuda.Event()
-                fork.record(stream)
-                for j, i in enumerate(gr[1:]):
-                    side[j].wait_event(fork)
-                    launch(recs[i], side[j])
-            launch(recs[gr[0]], stream)
-            for j in range(len(gr) - 1):
-                join = torch.cuda.Event()
-                join.record(side[j])
-                stream.wait_event(join)
-
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            issue()                        # grows the per-stream workspace outside capture
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        issue()
-    torch.cuda.synchronize()
-
-    def replay(n):
-        with torch.cuda.stream(stream):
-            for _ in range(n):
-                graph.replay()
-
-    replay(args.warmup)
+    step.replay(args.warmup)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -343,7 +425,7 @@ def run_uq(args, rank, world, dist):
         if dist:
             dist.barrier()
         t_start.record(stream)
-        replay(args.steps)
+        step.replay(args.steps)
         t_end.record(stream)
         torch.cuda.synchronize()
     if dist:
@@ -352,97 +434,94 @@ def run_uq(args, rank, world, dist):
     clocks = clk.summary()
 
     # end to end through the public API: H2D of every x, the step, D2H of every y, each step
-    xh = torch.empty(xbuf.numel(), dtype=torch.bfloat16, pin_memory=True)
-    yh = torch.empty(ybuf.numel(), dtype=torch.bfloat16, pin_memory=True)
-    xh.copy_(xbuf.cpu())
+    xh = torch.empty(step.xbuf.numel(), dtype=torch.bfloat16, pin_memory=True)
+    yh = torch.empty(step.ybuf.numel(), dtype=torch.bfloat16, pin_memory=True)
+    xh.copy_(step.xbuf.cpu())
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+
+    def e2e_step():
+        step.xbuf.copy_(xh, non_blocking=True)
+        step.graph.replay()
+        yh.copy_(step.ybuf, non_blocking=True)
+
     with torch.cuda.stream(stream):
-        for _ in range(max(1, args.warmup)):
-            xbuf.copy_(xh, non_blocking=True)
-            graph.replay()
-            yh.copy_(ybuf, non_blocking=True)
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
     torch.cuda.synchronize()
     e0.record(stream)
     with torch.cuda.stream(stream):
         for _ in range(args.steps):
-            xbuf.copy_(xh, non_blocking=True)
-            graph.replay()
-            yh.copy_(ybuf, non_blocking=True)
+            e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
 
-    # per-kernel durations: a second graph with an event pair around every launch
-    kern_ms = None
-    try:
-        evs = [(torch.cuda.Event(enable_timing=True, external=True),
-                torch.cuda.Event(enable_timing=True, external=True)) for _ in recs]
-        g2 = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g2, stream=stream):
-            issue(evs)
-        totals = []
-        for _ in range(3):
-            with torch.cuda.stream(stream):
-                g2.replay()
-            torch.cuda.synchronize()
-            totals.append(sum(a.elapsed_time(b) for a, b in evs))
-        kern_ms = statistics.median(totals)
-        kern_src = "events around each launch inside a replayed graph"
-    except Exception:
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in recs]
-        totals = []
-        for _ in range(3):
-            with torch.cuda.stream(stream):
-                issue(evs)
-            torch.cuda.synchronize()
-            totals.append(sum(a.elapsed_time(b) for a, b in evs))
-        kern_ms = statistics.median(totals)
-        kern_src = "events around each eager launch"
-
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], dist, dev)
+    info = dict(bytes=step.bytes, flops=step.flops, linears=len(recs), launches=step.launches(),
+                width=len(step.side) + 1, h2d=step.xbuf.numel() * 2, d2h=step.ybuf.numel() * 2,
+                shapes=sorted({(r["N"], r["K"]) for r in recs}), layers=len(recs) // len(spec["linears"]))
+    sweep = None
+    if world == 1 and not args.no_sweep:
+        del step, recs
+        torch.cuda.empty_cache()
+        sweep = run_sweep(dev, stream, *measured_peaks()[:2])
     if rank != 0:
         return
-
-    launches = len(recs)
-    total_bytes = step_bytes * args.steps * world
-    value = total_bytes / (ms * 1e-3) / 1e9
-    peak, peak_src = measured_peak()
-    achieved = step_bytes / (kern_ms * 1e-3) / 1e9
-    traffic = read_traffic(args.workload, step_bytes / launches) if M == WORKLOADS[args.workload]["m"] else None
-    out = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x int4 -> fp32 acc" if BITS[fmt] == 4 else
-        f"bf16 x {fmt.lower()} -> fp32 acc",
-        "data": "synthetic (seeded N(0,sigma) weights quantized on the GPU; bf16 N(0,1) x)",
-        "config": {"workload": args.workload, "description": spec["title"], "fmt": fmt, "group": group, "M": M,
-                   "layers": spec["layers"],
-                   "linears_per_step": launches, "bytes_per_step": step_bytes,
-                   "parallelism": f"replicas x{world}",
-                   "l2": "no flush: packed weights per step exceed L2 (%.2f GB)" % (step_bytes / 1e9),
-                   "launch": "one CUDA graph per step" + (
-                       "; linears reading the same input (q, k, v; gate, up) on parallel branches"
-                       if width > 1 else ""),
-                   "launch_overlap": not args.no_overlap},
-        "gpu_launches": sum(kernels_per_call(fmt, group, M, r["N"], r["K"]) for r in recs) * args.steps,
-        "e2e": {"value": round(step_bytes * args.steps * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": xbuf.numel() * 2, "d2h_bytes_per_step": ybuf.numel() * 2},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} HBM copy bandwidth",
-                     "traffic": traffic, "kernel": dominant_kernel(fmt, group, M, recs),
-                     "kernel_ms_per_step": round(kern_ms, 4), "timing": kern_src},
-        "clocks": clocks,
-    }
+    out = report(args, spec, M, world, ms, e2e_ms, clocks, info, sweep)
     if world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(spec, M)
+        out["cpu_baseline"] = cpu_baseline(args.workload, M)
     print(json.dumps(out), flush=True)
 
 
+def report(args, spec, M, world, ms, e2e_ms, clocks, info, sweep):
+    """The JSON line of the GPU arm."""
+    fmt, group = spec["fmt"], spec["group"]
+    hbm, tf, peak_src = measured_peaks()
+    step_s = ms * 1e-3 / args.steps
+    value = info["bytes"] * world / step_s / 1e9
+    achieved = info["bytes"] / step_s / 1e9
+    t_roof = roofline_time_s(info["bytes"], info["flops"], hbm, tf)
+    share = read_share(args.workload) if M == spec["m"] and not args.layers else None
+    traffic = read_traffic(args.workload, info["bytes"] / info["linears"]) if M == spec["m"] else None
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": f"bf16 x {fmt.lower()} -> fp32 acc",
+        "data": "synthetic (seeded N(0,sigma) weights quantized on the GPU; bf16 N(0,1) x)",
+        "config": {"workload": args.workload, "description": spec["title"], "fmt": fmt, "group": group, "M": M,
+                   "layers": info["layers"], "linears_per_step": info["linears"], "bytes_per_step": info["bytes"],
+                   "flops_per_step": info["flops"], "parallelism": f"replicas x{world}",
+                   "l2": "no flush: packed weights per step exceed L2 (%.2f GB)" % (info["bytes"] / 1e9),
+                   "launch": "one CUDA graph per step" + (
+                       "; linears reading the same input (q, k, v; gate, up) on parallel branches"
+                       if info["width"] > 1 else ""),
+                   "launch_overlap": not args.no_overlap},
+        "tflops": round(info["flops"] * world / step_s / 1e12, 4),
+        "gpu_launches": info["launches"] * args.steps,
+        "e2e": {"value": round(info["bytes"] * args.steps * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": info["h2d"], "d2h_bytes_per_step": info["d2h"]},
+        # the step is the dominant kernel's launches (plus the small second passes of the split
+        # linears); its algorithmic bytes over the step's device time can therefore not exceed what
+        # the kernel moves, and the ncu launch list gives the kernel's share of that time
+        "roofline": {"bound": "hbm" if info["bytes"] / (hbm * 1e9) >= info["flops"] / (tf * 1e12) else "tensor",
+                     "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(t_roof / step_s, 4), "traffic": traffic,
+                     "peak_source": f"{peak_src} HBM copy bandwidth (burst)",
+                     "kernel": dominant_kernel(fmt, group, M, info["shapes"]),
+                     "kernel_share_of_step": share,
+                     "timing": "algorithmic bytes per step / step device time (CUDA events over the timed region)"},
+        "clocks": clocks,
+        "sweep": sweep,
+    }
+
+
 # ---------------------------------------------------------------------------------------------
+# the oracle legs: cpu_baseline of the GPU arm and the reference arm
+
 def _oracle_sample(spec, M, rows_per_linear):
     """Oracle inputs for a bounded sample: the first rows of one layer's linears (quantized untimed)."""
-    import numpy as np
     from oracle import quant as oquant
     from oracle.nf4 import nf4_codebook
     from synth import activations, normal_weights
@@ -463,21 +542,60 @@ def _oracle_pass(items):
         ogemm.quantized_gemm(x, qz)
 
 
-def cpu_baseline(spec, M, target_s=10.0, rows_per_linear=512):
+def _threads_in_use():
+    """Threads the oracle's BLAS calls may use: the thread-count variables if set, else the CPUs this
+    process may run on (NumPy's elementwise dequantization itself runs on one thread)."""
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def oracle_leg(workload, M, target_s, rows_per_linear):
+    """Times the oracle (as it stands) on a bounded sample; returns the cpu_baseline fields."""
+    spec = WORKLOADS[workload]
     items = _oracle_sample(spec, M, rows_per_linear)
     nbytes = sum(b for _, _, b in items)
+    _oracle_pass(items)
     t0 = time.perf_counter()
     passes = 0
     while True:
         _oracle_pass(items)
         passes += 1
         el = time.perf_counter() - t0
-        if el >= target_s or el > 30.0:
+        if el >= target_s:
             break
-    return {"value": round(nbytes * passes / el / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
+    return {"value": round(nbytes * passes / el / 1e9, 4), "unit": "GB/s", "cores": _threads_in_use(),
             "kind": "oracle",
             "sample": f"first {rows_per_linear} rows of each of the {len(items)} linears of one layer, M={M}, "
                       f"{passes} passes of the float64 dequantize-then-matmul ({el:.1f} s)"}
+
+
+def cpu_baseline(workload, M, target_s=10.0, rows_per_linear=512):
+    """The oracle timed twice in fresh processes (the BLAS thread count is fixed at start-up): on one
+    thread and on every core this process may use."""
+    legs = {}
+    for name, threads in (("single_thread", 1), ("all_cores", None)):
+        env = dict(os.environ)
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            if threads:
+                env[var] = str(threads)
+            else:
+                env.pop(var, None)
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-leg", workload, "--m", str(M),
+                            "--oracle-seconds", str(target_s), "--oracle-rows", str(rows_per_linear)],
+                           env=env, capture_output=True, text=True, timeout=600)
+        if r.returncode != 0:
+            legs[name] = {"error": r.stderr.strip().splitlines()[-1:] or ["oracle leg failed"]}
+            continue
+        legs[name] = json.loads(r.stdout.strip().splitlines()[-1])
+    out = dict(legs.get("all_cores", {}))
+    out["single_thread"] = legs.get("single_thread")
+    out["cpus_on_host"] = os.cpu_count()
+    return out
 
 
 def run_reference(args, rank, world):
@@ -501,8 +619,8 @@ def run_reference(args, rank, world):
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic", "config": {"workload": args.workload, "description": spec["title"],
                                            "fmt": spec["fmt"], "group": spec["group"], "M": M},
-           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
-                            "sample": sample},
+           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": _threads_in_use(),
+                            "cpus_on_host": os.cpu_count(), "kind": "oracle", "sample": sample},
            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
@@ -516,9 +634,17 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama8b-int4a-decode")
     ap.add_argument("--m", type=int, default=0, help="override the batch rows M")
     ap.add_argument("--layers", type=int, default=0, help="override the number of layers (profiling runs)")
+    ap.add_argument("--no-sweep", action="store_true", help="leave the sweep workloads out of the line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-overlap", action="store_true", help="launch without programmatic dependent launch")
+    ap.add_argument("--oracle-leg", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-seconds", type=float, default=10.0, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-rows", type=int, default=512, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_leg:
+        spec = WORKLOADS[args.oracle_leg]
+        print(json.dumps(oracle_leg(args.oracle_leg, args.m or spec["m"], args.oracle_seconds, args.oracle_rows)))
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -11,6 +11,7 @@
 #include <mutex>
 #include <string>
 #include <utility>
+#include <vector>
 
 #include "uq_kernels.h"
 
@@ -85,6 +86,18 @@ struct Workspace {
 };
 std::map<std::pair<int, void*>, Workspace> g_ws;
 
+// Workspace buffers replaced by a larger one.  They are never freed: a CUDA graph captured before
+// the growth still holds their addresses and may be replayed at any time, so they stay allocated
+// (and their tickets zero) until the process exits.  Growth doubles, so they add up to less than
+// the buffer that replaced them.
+struct Retired {
+    int dev;
+    void* ptr;
+    size_t bytes;
+    bool tickets;
+};
+std::vector<Retired> g_retired;
+
 uq_status device_state(DeviceState** out, int* dev_out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -110,7 +123,7 @@ uq_status device_state(DeviceState** out, int* dev_out) {
     return UQ_OK;
 }
 
-uq_status grow(void** ptr, size_t* have, size_t need, bool zero, cudaStream_t st) {
+uq_status grow(void** ptr, size_t* have, size_t need, bool zero, cudaStream_t st, int dev) {
     if (*have >= need) return UQ_OK;
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     cudaError_t e = cudaStreamIsCapturing(st, &cs);
@@ -120,15 +133,11 @@ uq_status grow(void** ptr, size_t* have, size_t need, bool zero, cudaStream_t st
                                   "make one call of this size before capturing", need);
     size_t bytes = *have ? *have : 4096;
     while (bytes < need) bytes *= 2;
-    if (*ptr) {
-        e = cudaStreamSynchronize(st);     // in-flight kernels of this stream may still use the old buffer
-        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-        cudaFree(*ptr);
-        *ptr = nullptr;
-        *have = 0;
-    }
-    e = cudaMalloc(ptr, bytes);
-    if (e != cudaSuccess) { *ptr = nullptr; return fail(UQ_ERR_NOMEM, "cudaMalloc(%zu) failed", bytes); }
+    void* fresh = nullptr;
+    e = cudaMalloc(&fresh, bytes);
+    if (e != cudaSuccess) return fail(UQ_ERR_NOMEM, "cudaMalloc(%zu) failed", bytes);
+    if (*ptr) g_retired.push_back({dev, *ptr, *have, zero});   // graphs captured earlier may still use it
+    *ptr = fresh;
     if (zero) {
         e = cudaMemsetAsync(*ptr, 0, bytes, st);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
@@ -141,13 +150,13 @@ uq_status workspace(int dev, cudaStream_t st, size_t partial_bytes, size_t ticke
                     size_t aux_bytes = 0) {
     std::lock_guard<std::mutex> lk(g_mu);
     Workspace& w = g_ws[{dev, (void*)st}];
-    uq_status s = grow(reinterpret_cast<void**>(&w.partials), &w.partial_bytes, partial_bytes, false, st);
+    uq_status s = grow(reinterpret_cast<void**>(&w.partials), &w.partial_bytes, partial_bytes, false, st, dev);
     if (s != UQ_OK) return s;
     if (aux_bytes) {
-        s = grow(reinterpret_cast<void**>(&w.aux), &w.aux_bytes, aux_bytes, false, st);
+        s = grow(reinterpret_cast<void**>(&w.aux), &w.aux_bytes, aux_bytes, false, st, dev);
         if (s != UQ_OK) return s;
     }
-    s = grow(reinterpret_cast<void**>(&w.tickets), &w.ticket_bytes, ticket_bytes, true, st);
+    s = grow(reinterpret_cast<void**>(&w.tickets), &w.ticket_bytes, ticket_bytes, true, st, dev);
     if (s != UQ_OK) return s;
     *out = &w;
     return UQ_OK;
@@ -470,25 +479,41 @@ uq_status uq_gemm_kernel_count(int M, int N, int K, int group, uq_fmt fmt, int* 
 
 uq_status uq_device_fault(unsigned int* flag) {
     if (!flag) return fail(UQ_ERR_INVALID, "null pointer");
-    DeviceState* ds = nullptr;
+    *flag = 0;
     int dev = 0;
-    uq_status s = device_state(&ds, &dev);
-    if (s != UQ_OK) return s;
-    cudaError_t e = cudaDeviceSynchronize();
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    // the word of uq_gemm and the debug calls (only if this device has run one: nothing is allocated here)
     unsigned int v = 0;
-    e = cudaMemcpy(&v, ds->words, sizeof v, cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy");
-    *flag = v;
-    if (v) {
-        // a kernel returned early: its tickets may be left non-zero; clear this device's workspaces
-        cudaMemset(ds->words, 0, sizeof v);
+    unsigned int* words = nullptr;
+    {
         std::lock_guard<std::mutex> lk(g_mu);
-        for (auto& kv : g_ws)
-            if (kv.first.first == dev && kv.second.tickets)
-                cudaMemset(kv.second.tickets, 0, kv.second.ticket_bytes);
-        cudaDeviceSynchronize();
+        auto it = g_dev.find(dev);
+        if (it != g_dev.end()) words = it->second.words;
     }
+    if (words) {
+        e = cudaMemcpy(&v, words, sizeof v, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy");
+        if (v) {
+            // a kernel returned early: its tickets may be left non-zero; clear this device's workspaces
+            cudaMemset(words, 0, sizeof v);
+            std::lock_guard<std::mutex> lk(g_mu);
+            for (auto& kv : g_ws)
+                if (kv.first.first == dev && kv.second.tickets)
+                    cudaMemset(kv.second.tickets, 0, kv.second.ticket_bytes);
+            for (auto& r : g_retired)
+                if (r.dev == dev && r.tickets) cudaMemset(r.ptr, 0, r.bytes);
+        }
+    }
+    // the word of uq_gemm_noalloc (the first word of its static array)
+    unsigned int vn = 0;
+    e = uq::noalloc_take_fault(&vn);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the no-alloc fault word");
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    *flag = v | vn;
     return UQ_OK;
 }
 

@@ -104,14 +104,6 @@ __host__ __device__ inline int slot_bitpos(int bits, int s) {
 // A bf16 with biased exponent 134 (0x43) and a 7-bit mantissa m equals 128 + m exactly, so
 // OR-ing a small code into the mantissa field of 0x4300 yields 128 + code without a conversion.
 
-// bf16x2 (128 + code[2p], 128 + code[2p+1]) from a 4-bit word
-__device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w, int p) {
-    return ((w >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
-}
-// bf16x2 (128 + code[2p], 128 + code[2p+1]) from a 2-bit word
-__device__ __forceinline__ uint32_t crumb_pair_bf16(uint32_t w, int p) {
-    return ((w >> (2 * p)) & 0x00030003u) | 0x43004300u;
-}
 // bf16x2 (128 + code) of nibble pair P (bits 4P.. of each half) / crumb pair P (bits 2P..): one
 // lop3 ((w & mask) | magic), after a shift unless P == 0
 template <int P>
@@ -223,21 +215,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
-}
-
-// The same copy with an L2 eviction-priority hint: the packed weights of a decode step are read
-// once and are far larger than L2, so they are streamed with evict_first and do not push x, the
-// metadata or y (which the next kernel reads) out of L2.
-__device__ __forceinline__ uint64_t l2_evict_first_policy() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-__device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                                uint64_t policy) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-                 " [%0], [%1], %2, [%3], %4;"
-                 :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy) : "memory");
 }
 
 // fault codes written to the device fault word

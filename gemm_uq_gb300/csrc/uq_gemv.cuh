@@ -3,33 +3,36 @@
 // "Ultra LLM Engine", section "Fused Kernels": dequantized-weight GEMV for single-token
 // decode and GEMM for batched decode.  Decode is bound by streaming the packed weights from
 // HBM once; on this GPU the arithmetic of a CUDA-core dot product (unpack, widen, FMA: about
-// three issue slots per 4-bit weight) cannot keep up with HBM, so the kernel is organised to
-// spend as few instructions per weight as possible:
+// three issue slots per 4-bit weight) cannot keep up with HBM, so the 4-bit and 2-bit formats
+// run on warp-level tensor instructions:
 //
-//  * Work is the list of tiles (16 rows x 8 KB of codes) in row-block-major order.  Every warp
-//    is an independent worker that owns a contiguous, equal share of that list (a "stream-K"
-//    split: balanced over all SMs whatever N and K are).
-//  * Each warp keeps a ring of stages in shared memory.  A stage holds a tile's codes (one
-//    1-D bulk async copy, cp.async.bulk, issued by lane 0) and the tile's scales / zero points /
-//    K4 records (4- or 16-byte cp.async copies issued by all lanes); both complete on the
-//    stage's mbarrier (expect_tx for the bulk bytes, one cp.async.mbarrier.arrive.noinc per
-//    lane), so metadata is prefetched as deep as the weights.
-//  * x is copied once per CTA into shared memory (one bulk copy per row, rows padded so the
-//    rows of a B fragment hit different banks), then the per-group sums of x are formed from it;
-//    the prologue runs while the first weight tiles are in flight.
-//  * 4-bit and 2-bit codes: the packed plane is in mma.m16n8k16 A-fragment order, so one
-//    16-byte load per lane, a shift and a lop3 per register (magic exponent: bf16 0x4300 | code
-//    = 128 + code) give four A fragments, and the warp-wide mma.sync (bf16 x bf16 -> fp32)
-//    does the multiply-accumulate and the reduction over the 16-wide k block in one
-//    instruction; the M <= 8 activation rows are the N = 8 side of the instruction, so every
-//    M <= 8 costs the same.  Per quantization group the fp32 accumulators are scaled:
-//        y += s * (sum x*(128 + q) - (128 + z) * sum x).
-//  * INT8 and NF4 (whose codes do not map onto bf16 exactly by bit tricks) use CUDA-core FMAs
-//    on the same layout; the four lanes sharing a row are reduced with warp shuffles.
-//  * A row block whose k range is split between workers is finished by a deterministic second
-//    pass: each contributor stores its fp32 partial sums, takes a ticket, and the last one sums
-//    the partials in worker order (fixed, so results are bit-reproducible) and writes y.  No
-//    worker ever waits for another.
+//  * gemv_mma_kernel (INT4_SYM, INT4_ASYM, INT2_ASYM, K4).  Work is the list of tiles (16 rows x
+//    8 KB of codes), taken in k-major order so a warp's consecutive tiles share their k tile.
+//    Either every CTA owns whole 16-row blocks and its warps split their tiles evenly (partial
+//    sums of each tile in shared memory, summed per row in k order after one CTA barrier: no
+//    second launch), or every warp owns an equal contiguous range of all tiles (stream-K) and
+//    stores each tile's partial sums in global memory for gemv_split_reduce, a second launch
+//    that sums each row over its k tiles in k order.  Both orders are fixed, so results are
+//    bit-reproducible, and no warp ever waits for another.
+//  * Each warp keeps a ring of two stages; a stage is one tile's codes plus the tile rows'
+//    scales / zero points / K4 records, copied by all 32 lanes with 16-byte (codes: 512
+//    contiguous bytes per warp instruction) or 4-byte cp.async in one cp.async group per tile
+//    that the warp waits for itself.  With launch overlap the first tile is requested before
+//    the wait for the previous kernel on the stream (the weights are constant).
+//  * x: one or two rows are copied per warp a k tile at a time (one bulk copy per row, double
+//    buffered); more rows are copied whole into shared memory once per CTA, or read through L1
+//    when they do not fit.  The sums of x over each scaling group of a k tile are formed once
+//    per run of tiles at that k tile.
+//  * The packed plane is in mma.m16n8k16 A-fragment order: one 16-byte shared-memory load per
+//    lane, a shift and a lop3 per register (magic exponent: bf16 0x4300 | code = 128 + code)
+//    give the A fragments, and mma.sync (bf16 x bf16 -> fp32) does the multiply-accumulate and
+//    the reduction over the 16-wide k block in one instruction; the M <= 8 activation rows are
+//    the instruction's N = 8, so every M <= 8 costs the same.  Per scaling group the fp32 group
+//    sum is folded into the row's accumulator:  y += s * (sum x*(128 + q) - (128 + z) * sum x).
+//  * gemv_kernel (INT8_SYM, NF4, whose codes do not map onto bf16 exactly by a bit trick): the
+//    same layout on CUDA-core FMAs, four stages per warp on mbarriers; the four lanes sharing a
+//    row are reduced with warp shuffles, and a row block split between workers is finished by
+//    the last contributor (fence + ticket), summing the partials in worker order.
 #pragma once
 #include "uq_kernels.h"
 
@@ -116,11 +119,6 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// 16-byte copy through L2 only, with an L2 eviction-priority hint
-__device__ __forceinline__ void cp_async16_hint(void* dst, const void* src, uint64_t policy) {
-    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
-                 :: "r"(smem_u32(dst)), "l"(src), "l"(policy) : "memory");
-}
 template <int N>
 __device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
@@ -232,8 +230,7 @@ __device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, c
     if constexpr (GROUP) {
         const int bytes = (int)L.tile_bytes(kb);
         const uint8_t* src = a.wq + L.tile_offset(nb, kb);
-        const uint64_t pol = l2_evict_first_policy();
-        for (int off = lane * 16; off < bytes; off += 512) cp_async16_hint(st + off, src + off, pol);
+        for (int off = lane * 16; off < bytes; off += 512) cp_async16(st + off, src + off);
         cp_async_commit_group();
         (void)bar;
     } else {
@@ -243,7 +240,7 @@ __device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, c
             const uint32_t bytes = (uint32_t)L.tile_bytes(kb);
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(bar, bytes);
-            bulk_g2s_stream(st, a.wq + L.tile_offset(nb, kb), bytes, bar, l2_evict_first_policy());
+            bulk_g2s(st, a.wq + L.tile_offset(nb, kb), bytes, bar);
         }
     }
 }
@@ -437,73 +434,8 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
             return;
         }
 
-        if constexpr (F::MMA) {
-            const int G_all = (FMT == UQ_K4) ? a.K / 32 : mc.G;
-            const int gi0 = (kb * KT) / gs;                        // first global group of the tile
-            RowPtrs<FMT> rp[2];
-            if constexpr (FMT != UQ_K4) {
-                rp[0] = row_ptrs<FMT>(st, mc, g, n0 + g, kb);
-                rp[1] = row_ptrs<FMT>(st, mc, g + 8, n0 + g + 8, kb);
-            }
-            // B fragment source: x row min(g, M - 1) (columns >= M of D are never used), k = 4c..
-            const uint8_t* xrow = xs + (g < M ? g : M - 1) * xstride + 8 * c;
-            const uint16_t* xgrow = a.x + (long long)(g < M ? g : M - 1) * a.ldx + 4 * c;
-            // two accumulator chains (k block parity); each group starts them from zero
-            float dd[2][4];
-            for (int q = 0; q < nchunks; ++q) {
-                const uint4 cw = *reinterpret_cast<const uint4*>(st + q * CHUNK + lane * 16);
-                const uint32_t wv[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-                for (int bi = 0; bi < BPC; ++bi) {
-                    const int lb = q * BPC + bi;                   // block within the tile
-                    const int blk = blk0 + lb;
-                    uint2 b;
-                    if constexpr (XS) b = *reinterpret_cast<const uint2*>(xrow + blk * 32);
-                    else b = (blk * 16 + 4 * c < a.K) ? ldg_nc_v2(xgrow + blk * 16) : make_uint2(0, 0);
-                    uint32_t a0, a1, a2, a3;
-                    if constexpr (FMT == UQ_INT2_ASYM) {
-                        const uint32_t wd = wv[bi >> 1];
-                        const int pb = (bi & 1) * 4;
-                        a0 = crumb_pair_bf16(wd, pb + 0); a1 = crumb_pair_bf16(wd, pb + 1);
-                        a2 = crumb_pair_bf16(wd, pb + 2); a3 = crumb_pair_bf16(wd, pb + 3);
-                    } else {
-                        const uint32_t wd = wv[bi];
-                        a0 = nib_pair_bf16(wd, 0); a1 = nib_pair_bf16(wd, 1);
-                        a2 = nib_pair_bf16(wd, 2); a3 = nib_pair_bf16(wd, 3);
-                    }
-                    const int pos = lb & (bpg - 1);                // position inside the group
-                    if (pos < 2) mma_bf16_zero(dd[bi & 1], a0, a1, a2, a3, b.x, b.y);
-                    else mma_bf16(dd[bi & 1], a0, a1, a2, a3, b.x, b.y);
-                    if (pos == bpg - 1) {
-                        // end of a scaling group: fold it into the row sums
-                        const int li = lb >> bpg_log;              // group within the tile row
-                        const int gi = gi0 + li;                   // global group
-                        if (gi < G_all) {
-                            const float2 sxv = *reinterpret_cast<const float2*>(sxg + gi * 8 + 2 * c);
-                            float d[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) d[e] = dd[0][e] + dd[1][e];
-#pragma unroll
-                            for (int j = 0; j < 2; ++j) {
-                                if constexpr (FMT == UQ_K4) {
-                                    float dsc, dmm;
-                                    row_meta_k4(st, g + 8 * j, li, dsc, dmm);
-                                    const float off = fmaf(128.0f, dsc, dmm);   // (128 dsc + dmin m) per unit of sum x
-                                    acc[2 * j] = fmaf(dsc, d[2 * j], fmaf(-off, sxv.x, acc[2 * j]));
-                                    acc[2 * j + 1] = fmaf(dsc, d[2 * j + 1], fmaf(-off, sxv.y, acc[2 * j + 1]));
-                                } else {
-                                    float sc, zc;
-                                    row_meta<FMT>(rp[j], li, sc, zc);
-                                    const float szc = sc * zc;
-                                    acc[2 * j] = fmaf(sc, d[2 * j], fmaf(-szc, sxv.x, acc[2 * j]));
-                                    acc[2 * j + 1] = fmaf(sc, d[2 * j + 1], fmaf(-szc, sxv.y, acc[2 * j + 1]));
-                                }
-                            }
-                        }
-                    }
-                }
-            }
-        } else {
+        static_assert(!F::MMA, "the 4-bit and 2-bit formats run gemv_mma_kernel");
+        {
             // CUDA-core path (INT8_SYM, NF4): lane holds rows g and g + 8 at k = 16 blk + 4c .. +3
             const int G_all = mc.G;
             RowPtrs<FMT> rp[2];
@@ -1094,9 +1026,6 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
     }
 }
 
-inline bool gemv_is_mma(int fmt) {
-    return fmt == UQ_INT4_SYM || fmt == UQ_INT4_ASYM || fmt == UQ_INT2_ASYM || fmt == UQ_K4;
-}
 inline bool gemv_x_in_smem(int fmt, int K, int group, int M) {
     return gemv_smem_plan(fmt, K, group, M, true).total <= 227 * 1024;
 }

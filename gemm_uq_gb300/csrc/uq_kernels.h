@@ -10,6 +10,9 @@ void set_last_error(const char* msg);
 // whether GEMV kernels are launched with programmatic dependent launch (uq_set_launch_overlap)
 bool launch_overlap();
 
+// reads and clears the fault word of uq_gemm_noalloc launches on the current device (uq_noalloc.cu)
+cudaError_t noalloc_take_fault(unsigned int* v);
+
 // offline kernels (uq_pack.cu)
 cudaError_t launch_pack(int fmt, const int8_t* codes, uint8_t* wq, int N, int K, unsigned int* bad,
                         cudaStream_t st);
@@ -43,6 +46,10 @@ struct GemvArgs {
                               // no second pass); 0 = workers split row blocks anywhere (second pass)
 };
 constexpr int GEMV_WARPS = 4;     // worker warps per CTA
+// formats whose GEMV runs on mma.sync (the others on CUDA-core FMAs)
+inline bool gemv_is_mma(int fmt) {
+    return fmt == UQ_INT4_SYM || fmt == UQ_INT4_ASYM || fmt == UQ_INT2_ASYM || fmt == UQ_K4;
+}
 size_t gemv_smem_bytes(int fmt, int K, int group, int M);
 int gemv_warps(int fmt);     // workers (warps) per CTA of the GEMV for this format
 int gemv_ctas_per_sm(int fmt);   // CTAs of the GEMV resident per SM (workers = SMs x this x warps)

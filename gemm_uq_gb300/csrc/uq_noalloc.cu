@@ -14,12 +14,13 @@
 
 namespace {
 
-// Scratch layout (bytes): [0, 256) fault word; [256, 256 + TICKET_BYTES) row-block tickets;
-// then the fp32 partial sums.  Every GPU that loads the library holds this array until exit.
+// Scratch layout (bytes): [0, 256) the fault word of no-alloc launches; from 256 the row-block
+// tickets of the CUDA-core GEMV (INT8_SYM, NF4; 4 bytes per 16-row block, rounded up to 256 bytes),
+// then the fp32 partial sums of row blocks split between workers.  A launch uses tickets and partial
+// sums only when its work split needs them, so the limit depends on the shape (see uq.h).
+// Every GPU that loads the library holds this array until the process exits.
 constexpr size_t SCRATCH_BYTES = 1u << 20;                 // 1 MiB
-constexpr size_t TICKET_BYTES = 256u << 10;                // 65536 row blocks of 16 = N <= 1048576
-constexpr size_t PARTIAL_OFFSET = 256 + TICKET_BYTES;
-constexpr size_t PARTIAL_BYTES = SCRATCH_BYTES - PARTIAL_OFFSET;
+constexpr size_t DATA_OFFSET = 256;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SCRATCH_BYTES];
 
@@ -30,7 +31,7 @@ void* g_scratch_ptr[64] = {};
 int g_sms[64] = {};
 
 // message of the last failure on the calling thread, reported through uq_last_error()
-thread_local char g_err[256] = "";
+thread_local char g_err[320] = "";
 uq_status err(uq_status s) {
     uq::set_last_error(g_err);
     return s;
@@ -69,8 +70,34 @@ uq_status setup(int* dev_out, unsigned char** scratch, int* sms) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
 }  // namespace
+
+namespace uq {
+
+// Reads and clears the fault word of no-alloc launches on the current device (the first word of the
+// static array: the same address uq_gemm_noalloc hands its kernels).  *v = 0 when no no-alloc call
+// ran on this device.  Synchronous; allocates nothing.
+cudaError_t noalloc_take_fault(unsigned int* v) {
+    *v = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    void* p = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        p = g_scratch_ptr[dev];
+    }
+    if (!p) return cudaSuccess;
+    e = cudaMemcpy(v, p, sizeof(unsigned int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess || *v == 0) return e;
+    // a launch gave up early: clear the word (every call clears the tickets it uses itself)
+    return cudaMemset(p, 0, sizeof(unsigned int));
+}
+
+}  // namespace uq
 
 extern "C" {
 
@@ -119,26 +146,39 @@ uq_status uq_gemm_noalloc(const uint16_t* x, const void* wq, const void* scales,
     long long P = (long long)sms * uq::gemv_ctas_per_sm(fmt) * warps;
     if (P > T) P = T;
     const int mb_max = M < 8 ? M : 8;
-    if ((size_t)L.NB * sizeof(unsigned int) > TICKET_BYTES ||
-        uq::gemv_partials_floats(fmt, T, (int)P, mb_max) * sizeof(float) > PARTIAL_BYTES) {
-        snprintf(g_err, sizeof g_err,
-                 "N=%d, M=%d needs more than the %zu-byte static scratch (at most %zu row blocks of 16 and "
-                 "%zu bytes of partial sums)", N, M, SCRATCH_BYTES, TICKET_BYTES / 4, PARTIAL_BYTES);
-        return err(UQ_ERR_NOMEM);
-    }
     if (uq::gemv_smem_bytes(fmt, K, group, mb_max) > 227 * 1024) {
         snprintf(g_err, sizeof g_err, "K=%d is too long for the GEMV at M=%d", K, mb_max);
         return err(UQ_ERR_UNSUPPORTED);
     }
+    // the work split of the launches (the same for every 8-row block of x: it depends on N and K only)
+    uq::GemvArgs probe = {};
+    probe.M = mb_max; probe.N = N; probe.K = K; probe.group = group;
+    probe.NB = L.NB; probe.KB = L.KB; probe.T = T; probe.P = (int)P;
+    uq::gemv_grid(probe, fmt, sms);
+    const bool mma = uq::gemv_is_mma(fmt);
+    const bool uses_tickets = !mma;                          // the CUDA-core GEMV's last-contributor sums
+    const bool uses_partials = !mma || !probe.cta_rows;      // mma: only with the second-pass split
+    const size_t ticket_bytes = uses_tickets ? round256((size_t)L.NB * sizeof(unsigned int)) : 0;
+    const size_t partial_bytes =
+        uses_partials ? uq::gemv_partials_floats(fmt, T, (int)P, mb_max) * sizeof(float) : 0;
+    if (DATA_OFFSET + ticket_bytes + partial_bytes > SCRATCH_BYTES) {
+        snprintf(g_err, sizeof g_err,
+                 "M=%d, N=%d, K=%d needs %zu bytes of tickets and %zu bytes of partial sums; the static scratch "
+                 "holds %zu bytes in all", M, N, K, ticket_bytes, partial_bytes, SCRATCH_BYTES - DATA_OFFSET);
+        return err(UQ_ERR_NOMEM);
+    }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    unsigned int* tickets = reinterpret_cast<unsigned int*>(scratch + 256);
-    float* partials = reinterpret_cast<float*>(scratch + PARTIAL_OFFSET);
-    // the tickets must start at zero; the array keeps whatever the previous call left
-    cudaError_t e = cudaMemsetAsync(tickets, 0, (size_t)L.NB * sizeof(unsigned int), st);
-    if (e != cudaSuccess) { snprintf(g_err, sizeof g_err, "clearing tickets: %s", cudaGetErrorString(e)); return err(UQ_ERR_CUDA); }
+    unsigned int* tickets = reinterpret_cast<unsigned int*>(scratch + DATA_OFFSET);
+    float* partials = reinterpret_cast<float*>(scratch + DATA_OFFSET + ticket_bytes);
+    cudaError_t e = cudaSuccess;
+    if (uses_tickets) {
+        // the tickets must start at zero; the array keeps whatever the previous call left
+        e = cudaMemsetAsync(tickets, 0, (size_t)L.NB * sizeof(unsigned int), st);
+        if (e != cudaSuccess) { snprintf(g_err, sizeof g_err, "clearing tickets: %s", cudaGetErrorString(e)); return err(UQ_ERR_CUDA); }
+    }
     for (int m0 = 0; m0 < M; m0 += 8) {
         const int mb = (M - m0) < 8 ? (M - m0) : 8;
-        uq::GemvArgs a;
+        uq::GemvArgs a = {};
         a.x = x + (long long)m0 * K;
         a.wq = static_cast<const uint8_t*>(wq);
         a.scales = static_cast<const uint8_t*>(scales);
@@ -148,7 +188,7 @@ uq_status uq_gemm_noalloc(const uint16_t* x, const void* wq, const void* scales,
         a.NB = L.NB; a.KB = L.KB; a.T = T; a.P = (int)P;
         a.partials = partials;
         a.tickets = tickets;
-        a.fault = reinterpret_cast<unsigned int*>(scratch);
+        a.fault = reinterpret_cast<unsigned int*>(scratch);     // read back by uq_device_fault
         a.overlap = 0;
         const int grid = uq::gemv_grid(a, fmt, sms);
         e = uq::launch_gemv(fmt, a, grid, st);

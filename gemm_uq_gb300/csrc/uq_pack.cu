@@ -10,18 +10,27 @@ namespace uq {
 // word is mapped to its (row, k) by Layout::slot_nk.  Slots outside [N) x [K) are padding and
 // hold the stored form of code 0.
 
-// value (code + bias, as stored) of slot s of word w, through the same register unpacking the
-// GEMV and GEMM kernels use
+// values (code + bias, as stored) of every slot of word w, through the register unpacking the GEMV
+// and tensor-core kernels run on their code words: the shift + lop3 magic-exponent pairs
+// (nib_pair_lop3 / crumb_pair_lop3: bf16 128 + code) and the fp32 byte magic for 8-bit codes
+template <int P>
+__device__ __forceinline__ void pair_codes(uint32_t t, int* v) {
+    v[2 * P] = (int)bf16lo_f32(t) - 128;
+    v[2 * P + 1] = (int)bf16hi_f32(t) - 128;
+}
 template <int FMT>
-__device__ __forceinline__ int stored_code(uint32_t w, int s) {
+__device__ __forceinline__ void stored_codes(uint32_t w, int (&v)[fmt_cpw(FMT)]) {
     if constexpr (FMT == UQ_INT8_SYM) {
-        return (int)(byte_magic_f32(w, s) - 8388608.0f);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) v[s] = (int)(byte_magic_f32(w, s) - 8388608.0f);
     } else if constexpr (FMT == UQ_INT2_ASYM) {
-        const uint32_t t = crumb_pair_bf16(w, s >> 1);
-        return (int)((s & 1) ? bf16hi_f32(t) : bf16lo_f32(t)) - 128;
+        pair_codes<0>(crumb_pair_lop3<0>(w), v); pair_codes<1>(crumb_pair_lop3<1>(w), v);
+        pair_codes<2>(crumb_pair_lop3<2>(w), v); pair_codes<3>(crumb_pair_lop3<3>(w), v);
+        pair_codes<4>(crumb_pair_lop3<4>(w), v); pair_codes<5>(crumb_pair_lop3<5>(w), v);
+        pair_codes<6>(crumb_pair_lop3<6>(w), v); pair_codes<7>(crumb_pair_lop3<7>(w), v);
     } else {
-        const uint32_t t = nib_pair_bf16(w, s >> 1);
-        return (int)((s & 1) ? bf16hi_f32(t) : bf16lo_f32(t)) - 128;
+        pair_codes<0>(nib_pair_lop3<0>(w), v); pair_codes<1>(nib_pair_lop3<1>(w), v);
+        pair_codes<2>(nib_pair_lop3<2>(w), v); pair_codes<3>(nib_pair_lop3<3>(w), v);
     }
 }
 
@@ -62,11 +71,13 @@ __global__ void unpack_kernel(const uint8_t* __restrict__ wq, int8_t* __restrict
     for (long long wi = blockIdx.x * (long long)blockDim.x + threadIdx.x; wi < words;
          wi += (long long)gridDim.x * blockDim.x) {
         const uint32_t word = reinterpret_cast<const uint32_t*>(wq)[wi];
+        int v[CPW];
+        stored_codes<FMT>(word, v);
 #pragma unroll
         for (int s = 0; s < CPW; ++s) {
             int n, k;
             L.slot_nk(wi * 4, s, &n, &k);
-            if (n < N && k < K) codes[(long long)n * K + k] = (int8_t)(stored_code<FMT>(word, s) - BIAS);
+            if (n < N && k < K) codes[(long long)n * K + k] = (int8_t)(v[s] - BIAS);
         }
     }
 }
@@ -83,12 +94,14 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ wq, const uint8_t* __
     for (long long wi = blockIdx.x * (long long)blockDim.x + threadIdx.x; wi < words;
          wi += (long long)gridDim.x * blockDim.x) {
         const uint32_t word = reinterpret_cast<const uint32_t*>(wq)[wi];
+        int v[CPW];
+        stored_codes<FMT>(word, v);
 #pragma unroll
         for (int s = 0; s < CPW; ++s) {
             int n, k;
             L.slot_nk(wi * 4, s, &n, &k);
             if (n >= N || k >= K) continue;
-            const float q = (float)(stored_code<FMT>(word, s) - BIAS);
+            const float q = (float)(v[s] - BIAS);
             float out;
             if constexpr (FMT == UQ_K4) {
                 const int sb = k / 256, j = (k % 256) / 32;

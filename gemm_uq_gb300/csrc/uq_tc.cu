@@ -228,7 +228,6 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
             int issued = 0;
-            const uint64_t pol = l2_evict_first_policy();
             auto issue_x = [&](int c, int s) {
                 uint8_t* st = smem + s * SB;
 #pragma unroll

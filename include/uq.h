@@ -10,8 +10,10 @@
  *
  * where x is M x K bf16, W_hat is the N x K dequantized weight (a linear layer's
  * weight, K contiguous) and y is M x N bf16.  W_hat is never materialised: the
- * kernels stream packed codes from HBM and dequantize them in registers (M <= 15,
- * CUDA cores) or in shared memory feeding tcgen05 tensor cores (M >= 16).
+ * kernels stream packed codes from HBM and unpack them in registers, where they feed
+ * warp-level mma.sync instructions or CUDA-core FMAs (M <= 15), or are written as the
+ * integer part of the weights straight into tensor memory as the A operand of tcgen05
+ * tensor-core MMAs (M >= 16); per-group scales are applied to fp32 group sums.
  *
  * Weight formats (g = group size along K):
  *   UQ_INT4_SYM   codes q in [-8, 7],  fp16 scale s per group        W_hat = s*q
@@ -68,7 +70,9 @@ const char* uq_last_error(void);
 
 /*
  * uq_packed_size -- bytes of every buffer a (N, K, group, fmt) weight needs.
- *   wq_bytes     packed code plane written by uq_pack_layout      (N*K*bits/8)
+ *   wq_bytes     packed code plane written by uq_pack_layout: Np*Kp*bits/8 with N padded
+ *                to Np (a multiple of 16) and K to Kp (a multiple of 64 4-bit, 128 2-bit or
+ *                32 8-bit codes), so at least N*K*bits/8
  *   scales_bytes `scales` argument of uq_gemm: fp16 [N][K/group]; UQ_K4: 16-byte
  *                records [N][K/256] written by uq_pack_kmeta
  *   zeros_bytes  `zeros_or_codebook` argument: UQ_INT4_ASYM uint8 [N][ceil(K/group/2)]
@@ -86,10 +90,13 @@ uq_status uq_packed_size(int N, int K, int group, uq_fmt fmt,
  *   codes (device)  int8 [N][K] row-major: the signed code for the SYM formats, the
  *                   unsigned code (stored in int8) otherwise.
  *   wq    (device)  uq_packed_size(...).wq_bytes bytes, written.
- * Layout (library-defined): tiles of 8 rows x 512 bytes of codes (the last tile of a
- * row is narrower, the last row block shorter), each tile contiguous; inside a
- * 16-byte lane chunk the codes are ordered per 32-bit word so that in-register
- * unpacking yields k-consecutive pairs.  Offline call: it SYNCHRONIZES `stream`
+ * Layout (library-defined): rows in blocks of 16 (padding rows hold code 0), k in
+ * chunks of 512 bytes per row block (32 lanes x 16 bytes), 16 chunks to an 8 KB tile;
+ * the tiles of a row block follow in k order (the last one narrower when K is not a
+ * multiple of the tile), row blocks follow each other.  Inside a chunk each 16-byte
+ * lane slice holds the codes of rows g and g + 8 in the order of the mma.m16n8k16 A
+ * fragment, so a shift and a lop3 per register unpack a bf16 pair.  Signed formats are
+ * stored biased (+8, +128).  Offline call: it SYNCHRONIZES `stream`
  * and returns UQ_ERR_INVALID if any code is outside the format's range (wq is then
  * unspecified).
  */
@@ -126,8 +133,12 @@ uq_status uq_pack_kmeta(const uint16_t* d, const uint16_t* dmin, const uint8_t* 
  * 8-row blocks of x.  uq_gemm_kernel_count gives the launches of a shape.
  * Scratch: a library-owned workspace per (device, stream), grown on the first call
  * that needs more; that growth is refused (UQ_ERR_NOMEM) while `stream` is being
- * captured, so make one call of the largest size before capturing.  Calls on the
- * same stream are serialised by the stream; concurrent streams use separate workspaces.
+ * captured, so make one call of the largest size before capturing.  A buffer replaced
+ * by growth is kept allocated until the process exits, so a CUDA graph captured before
+ * the growth stays valid and may be replayed afterwards.  Calls on the same stream are
+ * serialised by the stream; concurrent streams use separate workspaces.  A captured
+ * graph uses the workspace of the stream it was captured on: do not run it concurrently
+ * with other calls on that stream (or with another replay of itself).
  */
 uq_status uq_gemm(const uint16_t* x, const void* wq, const void* scales,
                   const void* zeros_or_codebook, uint16_t* y,
@@ -135,7 +146,9 @@ uq_status uq_gemm(const uint16_t* x, const void* wq, const void* scales,
 
 /*
  * uq_unpack_codes -- debug: packed plane -> int8 codes [N][K] (device), bit-exact
- * inverse of uq_pack_layout, using the same unpacking as the GEMV kernels.
+ * inverse of uq_pack_layout.  It decodes every code word with the register unpacking
+ * the GEMV and tensor-core kernels run (shift + lop3 magic-exponent pairs for 4- and
+ * 2-bit codes, the fp32 byte magic for 8-bit codes).
  */
 uq_status uq_unpack_codes(const void* wq, int8_t* codes, int N, int K, int group, uq_fmt fmt,
                           void* stream);
@@ -198,10 +211,12 @@ uq_status uq_set_launch_overlap(int enable);
 uq_status uq_gemm_kernel_count(int M, int N, int K, int group, uq_fmt fmt, int* count);
 
 /*
- * uq_device_fault -- reads and clears the device-side fault word of the current device
- * (bit 0 / bit 1: a GEMV / tensor-core kernel's bounded wait on an mbarrier ran out and the
- * kernel returned early instead of hanging; bit 2: a GEMV launch was given a work split larger
- * than the kernel holds and computed nothing).  Synchronizes the device.  *flag = 0 when no fault.
+ * uq_device_fault -- reads and clears the device-side fault words of the current device: the
+ * one of uq_gemm and the one of uq_gemm_noalloc, OR-ed together (bit 0 / bit 1: a GEMV /
+ * tensor-core kernel's bounded wait ran out and the kernel returned early instead of hanging;
+ * its output is then unspecified; bit 2: a GEMV launch was given a work split larger than the
+ * kernel holds and computed nothing).  Synchronizes the device; allocates nothing.
+ * *flag = 0 when no fault.
  */
 uq_status uq_device_fault(unsigned int* flag);
 
@@ -215,13 +230,22 @@ uq_status uq_device_fault(unsigned int* flag);
  * owned device buffers), computed with the same GEMV kernel for every M (row blocks of 8; no
  * tensor-core path), so the output equals uq_gemm's for M <= 15.
  * Scratch: a 1 MiB static device array inside the library (every GPU that loads the library holds
- * it until the process exits): room for N <= 1048576 and for the split-K partial sums of one
- * 8-row block of x; larger requests return UQ_ERR_NOMEM with the limit in uq_last_error().  K == 0 returns
+ * it until the process exits); 256 bytes hold the fault word, and the rest must hold what the
+ * launch's work split uses, for one 8-row block of x (Mb = min(M, 8)):
+ *   - INT4_SYM, INT4_ASYM, INT2_ASYM, K4 (mma.sync GEMV): nothing when every CTA owns whole
+ *     16-row blocks (the split uq_gemm_kernel_count reports as one launch); otherwise fp32
+ *     partial sums of every tile, 64*Mb*ceil(N/16)*ceil(K/T) bytes (T = 1024 codes, 2048 for
+ *     INT2_ASYM): ceil(N/16)*ceil(K/T)*Mb <= 16380;
+ *   - INT8_SYM, NF4 (CUDA-core GEMV): 4*ceil(N/16) bytes of tickets, rounded up to 256, plus
+ *     fp32 partial sums of two row blocks per worker warp (128*Mb*workers bytes, workers =
+ *     min(4 * SMs, ceil(N/16)*ceil(K/T)), T = 512 codes for INT8_SYM, 1024 for NF4).
+ * Larger requests return UQ_ERR_NOMEM with the sizes in uq_last_error().  K == 0 returns
  * UQ_ERR_UNSUPPORTED.  Calls no cudaMalloc, cudaFree or other allocating routine.
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress) with
  * that device current; make that first call before any stream capture.  Every call shares the one
  * array and clears the part that must start at zero; calls whose kernels overlap on the GPU (for
- * example on two streams at once) race on it and must be serialised by the caller.
+ * example on two streams at once) race on it and must be serialised by the caller.  A wait that
+ * runs out inside a no-alloc launch is reported by uq_device_fault like any other.
  */
 uq_status uq_gemm_noalloc(const uint16_t* x, const void* wq, const void* scales,
                           const void* zeros_or_codebook, uint16_t* y,

@@ -199,60 +199,129 @@ def test_errors_on_device():
 
 
 # ------------------------------------------------------------------------------------------
-# full workload sizes: GPU quantizer on the whole weight, oracle on sampled rows
+# full workload sizes: every output element of every M against the oracle.  The weight is quantized
+# on the GPU (the library's quantizer) and by the oracle in row blocks (to bound host memory); the
+# two must agree bit for bit on every row, and every row of y is checked against the oracle's
+# float64 dequantize-then-matmul of its own quantization.
 
-def _sample_rows(N, n=48, seed=0):
-    rng = np.random.default_rng(seed)
-    rows = set(range(0, 8)) | set(range(N - 8, N)) | set(rng.integers(0, N, n).tolist())
-    return np.array(sorted(rows))
+ORACLE_ROWS = 2048
 
 
-def _full_case(fmt, group, N, K, M, seed, sigma, outliers):
+def _oracle_rows(w, fmt, group, cb, r0, r1):
+    if fmt == "K4":
+        return oquant.quantize_k4(w[r0:r1])
+    return oquant.quantize(w[r0:r1], fmt, group, codebook=cb)
+
+
+def _full_shape(fmt, group, N, K, Ms, seed, sigma, outliers):
     w = normal_weights(seed, N, K, sigma, outlier_p=0.001 if outliers else 0.0, outlier_mult=20.0)
-    x = activations(seed, M, K)
-    rows = _sample_rows(N, seed=seed)
+    xs = {M: activations(seed + 7919 * M, M, K) for M in Ms}
     wd = torch.from_numpy(w).to(DEV)
     cb = nf4_codebook() if fmt == "NF4" else None
     if fmt == "K4":
         codes, d, dmin, sc, m = uq.quantize_k4(wd)
         scales = uq.pack_kmeta(d, dmin, sc, m)
         zc = None
-        qz_rows = oquant.quantize_k4(w[rows])
-        assert np.array_equal(codes[rows].cpu().numpy(), qz_rows.codes)
-        assert np.array_equal(d[rows].cpu().numpy().view(np.uint16), qz_rows.d.view(np.uint16))
+        gpu_meta = {"d": d.cpu().numpy().view(np.uint16), "dmin": dmin.cpu().numpy().view(np.uint16),
+                    "sc": sc.cpu().numpy(), "m": m.cpu().numpy()}
+        del d, dmin, sc, m
     else:
         cbd = torch.from_numpy(cb).to(DEV) if cb is not None else None
         codes, scales, zeros = uq.quantize(wd, group, fmt, codebook=cbd)
-        qz_rows = oquant.quantize(w[rows], fmt, group, codebook=cb)
-        assert np.array_equal(codes[rows].cpu().numpy(), qz_rows.codes)
-        assert np.array_equal(scales[rows].cpu().numpy().view(np.uint16), qz_rows.scale.view(np.uint16))
+        gpu_meta = {"scale": scales.cpu().numpy().view(np.uint16)}
+        if fmt == "INT4_ASYM":
+            gpu_meta["zero"] = zeros.cpu().numpy()
+        if fmt == "INT2_ASYM":
+            gpu_meta["zero"] = zeros.cpu().numpy().view(np.uint16)
         zc = uq.pack_zeros(zeros) if fmt == "INT4_ASYM" else (zeros if fmt == "INT2_ASYM" else cbd)
     del wd
+    gpu_codes = codes.cpu().numpy()
     wq = uq.pack_layout(codes, group, fmt)
-    y = uq.gemm(device_x(x, DEV), wq, scales, zc, N, group, fmt)
-    y_ref, b = ogemm.reference(x, oquant.dequant(qz_rows))
-    r = ogemm.error_ratio(y_to_f64(y)[:, rows], y_ref, b)
-    assert r.max() <= 1.0, f"{fmt} {N}x{K} M={M}: max error ratio {r.max():.3g}"
+    del codes
+    ys = {M: y_to_f64(uq.gemm(device_x(xs[M], DEV), wq, scales, zc, N, group, fmt)) for M in Ms}
+    worst = {M: 0.0 for M in Ms}
+    for r0 in range(0, N, ORACLE_ROWS):
+        r1 = min(N, r0 + ORACLE_ROWS)
+        qz = _oracle_rows(w, fmt, group, cb, r0, r1)
+        assert np.array_equal(gpu_codes[r0:r1], qz.codes), f"GPU codes differ in rows {r0}..{r1}"
+        if fmt == "K4":
+            assert np.array_equal(gpu_meta["d"][r0:r1], qz.d.view(np.uint16))
+            assert np.array_equal(gpu_meta["dmin"][r0:r1], qz.dmin.view(np.uint16))
+            assert np.array_equal(gpu_meta["sc"][r0:r1], qz.sc)
+            assert np.array_equal(gpu_meta["m"][r0:r1], qz.m)
+        else:
+            assert np.array_equal(gpu_meta["scale"][r0:r1], qz.scale.view(np.uint16))
+            if fmt == "INT4_ASYM":
+                assert np.array_equal(gpu_meta["zero"][r0:r1], qz.zero)
+            if fmt == "INT2_ASYM":
+                assert np.array_equal(gpu_meta["zero"][r0:r1], qz.zero.view(np.uint16))
+        w_hat = oquant.dequant(qz)
+        for M in Ms:
+            y_ref, b = ogemm.reference(xs[M], w_hat)
+            r = ogemm.error_ratio(ys[M][:, r0:r1], y_ref, b)
+            worst[M] = max(worst[M], float(r.max()))
+    for M in Ms:
+        assert worst[M] <= 1.0, f"{fmt} {N}x{K} M={M}: max error ratio {worst[M]:.3g}"
 
 
 @pytest.mark.parametrize("N,K", [(4096, 4096), (1024, 4096), (14336, 4096), (4096, 14336)])
 def test_full_size_llama8b_linears_m1(N, K):
-    _full_case("INT4_ASYM", 128, N, K, 1, seed=2000 + N + K, sigma=0.02, outliers=True)
+    _full_shape("INT4_ASYM", 128, N, K, [1], seed=2000 + N + K, sigma=0.02, outliers=True)
 
 
-@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 64])
 @pytest.mark.parametrize("N,K", [(14336, 4096), (4096, 14336)])
-def test_full_size_batched_sweep(N, K, M):
-    _full_case("INT4_ASYM", 128, N, K, M, seed=3000 + M, sigma=0.02, outliers=False)
+def test_full_size_batched_sweep(N, K):
+    _full_shape("INT4_ASYM", 128, N, K, [1, 2, 4, 8, 16, 32, 64], seed=3000 + N // 1024, sigma=0.02,
+                outliers=False)
 
 
 @pytest.mark.parametrize("fmt,group", [("INT8_SYM", 128), ("INT2_ASYM", 64), ("NF4", 64)])
-@pytest.mark.parametrize("M", [1, 16])
-def test_full_size_format_sweep(fmt, group, M):
-    _full_case(fmt, group, 8192, 8192, M, seed=4000 + M, sigma=0.02, outliers=False)
+def test_full_size_format_sweep(fmt, group):
+    _full_shape(fmt, group, 8192, 8192, [1, 16], seed=4000 + group, sigma=0.02, outliers=False)
 
 
 @pytest.mark.parametrize("N,K", [(8192, 8192), (1024, 8192), (28672, 8192), (8192, 28672)])
+def test_full_size_k4_70b_linears(N, K):
+    _full_shape("K4", 256, N, K, [1, 8, 32], seed=5000 + N // 1024 + K // 1024, sigma=0.015, outliers=False)
+
+
+# ------------------------------------------------------------------------------------------
+# fp16 subnormal d and dmin in K4 records: decoded exactly by the dequant export and the GEMM paths
+
+def _subnormal_k4(N, K, seed):
+    """Hand-set K4 weights whose every super-block has an fp16 subnormal d and dmin (bit patterns
+    1..1023), full-range 6-bit sc and m, and random 4-bit codes: the decode must be exact there."""
+    rng = np.random.default_rng(seed)
+    S = K // 256
+    d = rng.integers(1, 1024, (N, S)).astype(np.uint16).view(np.float16)
+    dmin = rng.integers(1, 1024, (N, S)).astype(np.uint16).view(np.float16)
+    d[0, 0] = np.uint16(1).view(np.float16)            # the smallest subnormal
+    dmin[0, 0] = np.uint16(0x03FF).view(np.float16)    # the largest subnormal
+    sc = rng.integers(0, 64, (N, S, 8)).astype(np.uint8)
+    m = rng.integers(0, 64, (N, S, 8)).astype(np.uint8)
+    sc[0, 0, :2] = (63, 0)
+    m[0, 0, :2] = (0, 63)
+    codes = rng.integers(0, 16, (N, K)).astype(np.int8)
+    return oquant.Quantized("K4", 256, codes, d=d, dmin=dmin, sc=sc, m=m)
+
+
+def test_k4_subnormal_d_dmin_dequant_bit_exact():
+    qz = _subnormal_k4(48, 1024, 61)
+    assert np.all(np.abs(qz.d.astype(np.float64)) < 2.0 ** -14)
+    assert np.all(np.abs(qz.dmin.astype(np.float64)) < 2.0 ** -14)
+    wq, scales, zc = device_weights(qz, DEV)
+    got = uq.dequant(wq, scales, zc, 48, 1024, 256, "K4").cpu().numpy()
+    want = oquant.dequant(qz)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
 @pytest.mark.parametrize("M", [1, 8, 32])
-def test_full_size_k4_70b_linears(N, K, M):
-    _full_case("K4", 256, N, K, M, seed=5000 + M, sigma=0.015, outliers=False)
+def test_k4_subnormal_d_dmin_gemm(M):
+    N, K = 300, 2048
+    qz = _subnormal_k4(N, K, 62)
+    x = activations(63, M, K)
+    wq, scales, zc = device_weights(qz, DEV)
+    y = uq.gemm(device_x(x, DEV), wq, scales, zc, N, 256, "K4")
+    y_ref, b = ogemm.quantized_gemm(x, qz)
+    r = ogemm.error_ratio(y_to_f64(y), y_ref, b)
+    assert r.max() <= 1.0, f"max error ratio {r.max():.3g}"
