@@ -200,9 +200,8 @@ uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const 
 uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const void* zc, uint16_t* y, int Mb, int N,
                  int K, int ldx, int ldy, int group, int fmt, cudaStream_t st, const DeviceState& ds, int dev) {
     const int mpad = (Mb + 15) / 16 * 16;
-    int stages = 0, dslots = 0;
     size_t smem = 0;
-    if (uq::tc_plan(fmt, mpad, &stages, &dslots, &smem) != 0)
+    if (uq::tc_plan(fmt, mpad, group, &smem) != 0)
         return fail(UQ_ERR_UNSUPPORTED, "no tensor-core plan for M=%d", Mb);
     const int kc = (fmt == UQ_INT8_SYM) ? 128 : 256;
     const int nblk = (N + 127) / 128;
@@ -231,7 +230,6 @@ uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const vo
     a.sx = ws->aux;
     a.M = Mb; a.Mpad = mpad; a.N = N; a.K = K; a.group = group; a.ldx = ldx; a.ldy = ldy;
     a.CH = CH; a.U = U; a.P = (int)P;
-    a.stages = stages; a.dslots = dslots;
     a.partials = ws->partials;
     a.tickets = ws->tickets;
     a.fault = ds.words;

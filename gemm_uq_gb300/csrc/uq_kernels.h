@@ -74,13 +74,12 @@ struct TcArgs {
     int CH;                   // units (chunks of 128 code bytes) per 128-row block
     long long U;              // units = ceil(N/128) * CH
     int P;                    // CTAs, P <= U
-    int stages, dslots;
     float* partials;          // [2P][128][Mpad]
     unsigned int* tickets;    // [ceil(N/128)]
     unsigned int* fault;
 };
 bool tc_supported(int fmt, int N, int K);
-int tc_plan(int fmt, int mpad, int* stages, int* dslots, size_t* smem);
+int tc_plan(int fmt, int mpad, int group, size_t* smem);   // dynamic shared memory of the launch
 cudaError_t launch_colsum32(const uint16_t* x, float* sx, int M, int mpad, int K, int ldx, cudaStream_t st);
 cudaError_t launch_tc(int fmt, const uint16_t* x, const TcArgs& a, size_t smem, int grid, cudaStream_t st);
 

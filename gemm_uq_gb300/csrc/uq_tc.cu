@@ -36,12 +36,10 @@ namespace uq {
 
 namespace {
 
-constexpr int TC_THREADS = 512;
 constexpr int TC_ROWS = 128;
 constexpr int TC_STAGE_CODES = TC_ROWS * 128;     // bytes of codes per stage
 constexpr int TMEM_COLS = 512;
 constexpr int TC_BAR_BYTES = 2048;                 // barriers and flags after the stages
-constexpr int TC_MAX_STAGES = 6;
 
 __device__ __forceinline__ long long trange_begin(int c, long long U, int P) { return (long long)c * U / P; }
 __device__ __forceinline__ int tworker_of(long long u, long long U, int P) {
@@ -59,17 +57,22 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                 :: "r"(smem_u32(bar)) : "memory");
-}
-// D[tmem] (+)= A[tmem] * B[smem desc]
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-    asm volatile("{\n\t.reg .pred p;\n\t"
+// D[tmem] (+)= A[tmem] * B[smem desc], executed by the whole (converged) warp: the operands are
+// warp-uniform and the elected lane (the lowest active one) issues the instruction
+__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p, e;\n\t"
                  "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
                  :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// tcgen05.commit by the elected lane of the converged warp (the lane that issued the MMAs)
+__device__ __forceinline__ void tc_commit_elect(uint64_t* bar) {
+    asm volatile("{\n\t.reg .pred e;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+                 :: "r"(smem_u32(bar)) : "memory");
 }
 // 16 lanes x 256 bits per repetition, fragment layout of an m16n8 accumulator: thread t holds
 // (lane t/4, columns 2(t%4), 2(t%4)+1) and (lane t/4 + 8, same columns); .x4 repeats it over 32 columns
@@ -92,7 +95,6 @@ __device__ __forceinline__ void tc_cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
 // Copy the aligned 32-bit words that cover bytes [lo, lo + len) of `base` into dst[0 .. nw) (word 0
 // holds byte lo & ~3).  Words that would reach past `end` (the array's size) are assembled from byte
 // loads instead, so nothing outside the array is read.
@@ -111,16 +113,13 @@ __device__ __forceinline__ void stage_span(uint32_t* dst, const uint8_t* base, l
 }
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-                 "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-                   "=r"(r[14]), "=r"(r[15])
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
                  : "r"(taddr) : "memory");
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
@@ -151,67 +150,106 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
     return d;
 }
 
+// cp.async.wait_group with a compile-time count
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
 template <int FMT> struct TcFmt {
     static constexpr int KC = (FMT == UQ_INT8_SYM) ? 128 : 256;   // codes per row per unit
     static constexpr int ACOLS = KC / 2;                           // tensor-memory columns of A per unit
-    // per-thread metadata rings (3 units deep): epilogue scale words per row, dequant zero words
-    static constexpr int SWORDS = (FMT == UQ_K4) ? 4 : 5;
-    static constexpr int EPI_RING = 3 * 128 * SWORDS * 4;           // bytes
-    static constexpr int DQ_RING = (FMT == UQ_INT4_ASYM) ? 3 * 8 * 16 * 2 * 4 : 0;
+    // staged scale words per row and unit: the unit's KC / (16 GB) fp16 scales plus one half for a
+    // start that is not word aligned (K4: its 16-byte super-block record)
+    template <int GB> static constexpr int swords() { return FMT == UQ_K4 ? 4 : (KC / (16 * GB) + 2) / 2; }
 };
 constexpr int TC_DQ_WARPS = 8;                     // dequant warps (one 16-row block each)
+// Epilogue warps: one per tensor-memory lane quarter for Mpad <= 32 (all columns), two per quarter
+// above (half the columns each, so the per-thread accumulators fit in registers)
+__host__ __device__ constexpr int tc_epi_warps(int mpad) { return mpad >= 48 ? 8 : 4; }
+__host__ __device__ constexpr int tc_threads(int mpad) { return (4 + TC_DQ_WARPS + tc_epi_warps(mpad)) * 32; }
+constexpr int TC_EPI_RING = 8;                     // epilogue scale ring: units staged 7 ahead
 
 }  // namespace
 
-struct TcSmem {
-    // barriers live after the stage buffers; offsets computed on the host and device alike
-    static __host__ __device__ constexpr int x_bytes(int kc, int mpad) { return kc * mpad * 2; }
-    static __host__ __device__ constexpr int stage_bytes(int kc, int mpad) {
-        return TC_STAGE_CODES + x_bytes(kc, mpad);
-    }
+// Shared-memory plan of the tensor-core kernel, the same on host and device:
+//   [x ring: XS stages of one unit's x tile][code ring: CS stages of one unit's 16 KB of codes]
+//   [barriers][epilogue scale ring][INT4_ASYM zero-point ring]
+// The code ring is separate from the x ring and deeper: the dequant warps request their codes
+// CS - 1 units ahead, which keeps enough bytes in flight per SM to cover the memory latency.
+template <int FMT, int MPAD, int GB> struct TcPlan {
+    static constexpr int KC = TcFmt<FMT>::KC;
+    static constexpr int XB = KC * MPAD * 2;                       // x bytes per unit (MPAD rows x KC k)
+    static constexpr int XS = 4;                                   // x stages
+    static constexpr int EPI_RING = TC_EPI_RING * 32 * tc_epi_warps(MPAD) * TcFmt<FMT>::template swords<GB>() * 4;
+    static constexpr int DQ_SLOT = (FMT == UQ_INT4_ASYM) ? TC_DQ_WARPS * 16 * 2 * 4 : 0;   // zero words per unit
+    static constexpr int BUDGET = 227 * 1024 - 1024 - TC_BAR_BYTES - EPI_RING - XS * XB;
+    static constexpr int CS_FIT = BUDGET / (TC_STAGE_CODES + DQ_SLOT);
+    static constexpr int CS = CS_FIT > 8 ? 8 : (CS_FIT > 4 && XB >= 24 * 1024 ? 4 : CS_FIT);   // code stages
+    static constexpr int CD = CS - 1;                              // code prefetch depth (units)
+    static constexpr int DS_FIT = (TMEM_COLS - 2 * (KC / 2)) / MPAD;
+    static constexpr int DS = DS_FIT > 8 ? 8 : DS_FIT;           // accumulator slots
+    // A buffers: at least two, more where tensor memory has room beside the accumulator slots (the
+    // dequant warps then run further ahead of the MMAs that free a buffer)
+    static constexpr int NA_FIT = (TMEM_COLS - DS * MPAD) / (KC / 2);
+    static constexpr int NA = NA_FIT > 4 ? 4 : NA_FIT;
+    static_assert(NA >= 2, "two A buffers at least");
+    static constexpr int CODE_OFF = XS * XB;
+    static constexpr int BAR_OFF = CODE_OFF + CS * TC_STAGE_CODES;
+    static constexpr int EPI_OFF = BAR_OFF + TC_BAR_BYTES;
+    static constexpr int DQ_OFF = EPI_OFF + EPI_RING;
+    static constexpr int SMEM = 1024 + DQ_OFF + CS * DQ_SLOT;      // + alignment slack
+    static_assert(CS >= 3, "the code ring needs at least three stages");
+    static_assert(SMEM <= 227 * 1024, "shared memory plan too large");
 };
 
 // GB = 16-k blocks per scaling group (2, 4 or 8); used by the INT4_ASYM zero points, ignored otherwise
 template <int FMT, int MPAD, int GB>
-__global__ void __launch_bounds__(TC_THREADS, 1)
+__global__ void __launch_bounds__(tc_threads(MPAD), 1)
 tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
+    using PL = TcPlan<FMT, MPAD, GB>;
     constexpr int KC = TcFmt<FMT>::KC;
     constexpr int ACOLS = TcFmt<FMT>::ACOLS;
-    constexpr int XB = TcSmem::x_bytes(KC, MPAD);
-    constexpr int SB = TcSmem::stage_bytes(KC, MPAD);
-    constexpr int SWORDS = TcFmt<FMT>::SWORDS;
+    constexpr int XB = PL::XB, XS = PL::XS, CS = PL::CS, CD = PL::CD, DS = PL::DS, NA = PL::NA;
+    constexpr int SWORDS = TcFmt<FMT>::template swords<GB>();
     constexpr uint32_t IDESC = idesc_bf16(MPAD);
-    constexpr int NISS = MPAD <= 32 ? 2 : 1;        // MMA issuing threads
+    // Two warps issue MMAs: for Mpad <= 32 on alternate units; for larger Mpad (4-bit codes) both on
+    // every unit, each with half of its groups (SPLIT); INT8 at larger Mpad has one group per unit, one issuer
+    constexpr bool SPLIT = MPAD >= 48 && KC == 256;
+    constexpr int NISS = (MPAD <= 32 || SPLIT) ? 2 : 1;
+    constexpr int EW = tc_epi_warps(MPAD);
+    constexpr int HW = MPAD / (EW / 4);             // columns per epilogue warp
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    const int S = a.stages, DS = a.dslots;
     const int G = (FMT == UQ_K4) ? 32 : a.group;   // scaling granularity (K4: the 32-weight sub-block)
     const int GPC = KC / G;                         // groups (K4: sub-blocks) per unit
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * SB);
-    uint64_t* full = bars;                          // [S]
-    uint64_t* empty = full + S;                     // [S]
-    uint64_t* afull = empty + S;                    // [2]
-    uint64_t* aempty = afull + 2;                   // [2]
-    uint64_t* dfull = aempty + 2;                   // [DS]
-    uint64_t* dempty = dfull + DS;                  // [DS]
-    uint64_t* ebar = dempty + DS;                   // epilogue warpgroup rendezvous (128 arrivals)
+    uint8_t* xring = smem;
+    uint8_t* cring = smem + PL::CODE_OFF;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PL::BAR_OFF);
+    uint64_t* full = bars;                          // [XS] x tile landed
+    uint64_t* empty = full + XS;                    // [XS] x tile consumed by the MMAs
+    uint64_t* afull = empty + XS;                   // [NA] A buffer written by the dequant warps
+    uint64_t* aempty = afull + NA;                  // [NA] A buffer consumed by the MMAs
+    uint64_t* dfull = aempty + NA;                  // [DS] accumulator slot complete
+    uint64_t* dempty = dfull + DS;                  // [DS] accumulator slot read by the epilogue
+    uint64_t* ebar = dempty + DS;                   // epilogue rendezvous (all epilogue threads)
     uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(ebar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_smem + 1);
     unsigned int* ticket_smem = reinterpret_cast<unsigned int*>(tmem_base_smem + 2);
-    uint32_t* epi_ring = reinterpret_cast<uint32_t*>(smem + S * SB + TC_BAR_BYTES);          // [3][128][SWORDS]
-    uint32_t* dq_ring = epi_ring + TcFmt<FMT>::EPI_RING / 4;                                // [3][8 warps][16][2]
+    uint32_t* epi_ring = reinterpret_cast<uint32_t*>(smem + PL::EPI_OFF);   // [ring][256 threads][SWORDS]
+    uint32_t* dq_ring = reinterpret_cast<uint32_t*>(smem + PL::DQ_OFF);     // [CS][8 warps][16][2]
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the warp index broadcast from lane 0, so that the compiler knows it (and everything derived from
+    // it: roles, tensor-memory addresses) to be the same across the warp
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0), lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
     const long long u0 = trange_begin(cta, a.U, a.P), u1 = trange_begin(cta + 1, a.U, a.P);
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(&afull[i], TC_DQ_WARPS); mbar_init(&aempty[i], 1); }
-        for (int d = 0; d < DS; ++d) { mbar_init(&dfull[d], 1); mbar_init(&dempty[d], 4); }
-        mbar_init(ebar, 128);
+        for (int s = 0; s < XS; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], SPLIT ? 2 : 1); }
+        for (int i = 0; i < NA; ++i) { mbar_init(&afull[i], TC_DQ_WARPS); mbar_init(&aempty[i], SPLIT ? 2 : 1); }
+        for (int d = 0; d < DS; ++d) { mbar_init(&dfull[d], 1); mbar_init(&dempty[d], EW); }
+        mbar_init(ebar, 32 * EW);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -222,30 +260,29 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
     tc_fence_after();
     const uint32_t tmem = *tmem_base_smem;
     const uint32_t A_COL0 = 0;                      // A buffers: columns [0, 2*ACOLS)
-    const uint32_t D_COL0 = 2 * ACOLS;              // D slots: columns [2*ACOLS, 2*ACOLS + DS*MPAD)
+    const uint32_t D_COL0 = NA * ACOLS;             // D slots: columns [NA*ACOLS, NA*ACOLS + DS*MPAD)
 
     if (warp == 0) {
-        // ---------------------------------------------------------------- TMA producer
+        // ---------------------------------------------------------------- TMA producer of x
         if (lane == 0) {
-            int issued = 0;
             auto issue_x = [&](int c, int s) {
-                uint8_t* st = smem + s * SB;
+                uint8_t* st = xring + s * XB;
 #pragma unroll
                 for (int q = 0; q < KC / 64; ++q)
-                    tma_load_2d(st + TC_STAGE_CODES + q * (MPAD * 128), &tmap_x, c * KC + q * 64, 0, &full[s]);
+                    tma_load_2d(st + q * (MPAD * 128), &tmap_x, c * KC + q * 64, 0, &full[s]);
             };
             // x may be written by the kernel before on the stream: loaded after the wait for it (the
             // dequant warps request the codes themselves)
-            const int pre = (u1 - u0) < S ? (int)(u1 - u0) : S;
+            const int pre = (u1 - u0) < XS ? (int)(u1 - u0) : XS;
             const int CH = a.CH;
-            int rb = (int)(u0 / CH), c = (int)(u0 % CH);
+            int c = (int)(u0 % CH);
             asm volatile("griddepcontrol.wait;" ::: "memory");
             for (int j = 0; j < pre; ++j) {
                 mbar_arrive_expect_tx(&full[j], (uint32_t)XB);
                 issue_x(c, j);
-                if (++c == CH) { c = 0; ++rb; }
+                if (++c == CH) c = 0;
             }
-            issued = pre;
+            int issued = pre;
             int s = 0;
             uint32_t eph = 1;                                // empty[] of the first round counts as free
             for (long long u = u0 + pre; u < u1 && !*abort_flag; ++u, ++issued) {
@@ -256,56 +293,60 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                 }
                 mbar_arrive_expect_tx(&full[s], (uint32_t)XB);
                 issue_x(c, s);
-                if (++c == CH) { c = 0; ++rb; }
-                if (++s == S) s = 0;
+                if (++c == CH) c = 0;
+                if (++s == XS) s = 0;
             }
             // let the last copies land before the CTA can leave
-            for (int j = issued - 1; j >= 0 && j >= issued - S; --j)
-                mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1), a.fault, FAULT_TC_WAIT);
+            for (int j = issued - 1; j >= 0 && j >= issued - XS; --j)
+                mbar_wait_bounded(&full[j % XS], (uint32_t)((j / XS) & 1), a.fault, FAULT_TC_WAIT);
         }
     } else if (warp == 1 || (NISS == 2 && warp == 2)) {
         // ---------------------------------------------------------------- MMA issuers
-        // A thread issuing tcgen05.mma is held for tens of cycles per instruction, longer than
-        // MMAs with N <= 32 keep the tensor pipe busy, so there two threads issue: warp 1 the
-        // CTA's even units (A buffer 0, accumulator slots [0, DH)), warp 2 the odd ones (A buffer
-        // 1, slots [DH, 2 DH)).  Each thread's MMAs and commits stay in its own order.
-        if (lane == 0) {
-            const int me = warp - 1, DH = DS / NISS;
-            int d = 0;
-            uint32_t dph = 0;                            // phase of dempty[me * DH + d] (^1)
-            const int KS = G / 16;                       // MMAs per group
-            for (long long u = u0 + me; u < u1 && !*abort_flag; u += NISS) {
-                const int i = (int)(u - u0);
-                const int s = i % S, ab = i & 1;
-                const uint32_t sph = (uint32_t)((i / S) & 1), aph = (uint32_t)((i >> 1) & 1);
-                bool ok = mbar_wait_bounded(&full[s], sph, a.fault, FAULT_TC_WAIT) &&
-                          mbar_wait_bounded(&afull[ab], aph, a.fault, FAULT_TC_WAIT);
-                if (!ok) { *abort_flag = 1; break; }
+        // The whole warp runs the issue loop, so every operand (descriptors, tensor-memory columns,
+        // ring positions) is computed once per warp as a warp-uniform value; one elected lane issues
+        // the tcgen05.mma and tcgen05.commit instructions (a commit tracks the MMAs of the thread
+        // that issues it, so the same lane issues both).  For Mpad <= 32 two warps issue: warp 1 the
+        // CTA's even units (A buffer 0, accumulator slots [0, DH)), warp 2 the odd ones (A buffer 1,
+        // slots [DH, 2 DH)).
+        const int me = warp - 1, DH = DS / NISS;
+        const bool leader = lane == 0;                   // the lane elect.sync picks in a converged warp
+        int d = 0;
+        uint32_t dph = 0;                                // phase of dempty[me * DH + d] (^1)
+        const int KS = G / 16;                           // MMAs per group
+        for (long long u = u0 + (SPLIT ? 0 : me); u < u1; u += (SPLIT ? 1 : NISS)) {
+            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+            const int i = (int)(u - u0);
+            const int s = i % XS, ab = i % NA;
+            const uint32_t sph = (uint32_t)((i / XS) & 1), aph = (uint32_t)((i / NA) & 1);
+            bool ok = mbar_wait_bounded(&full[s], sph, a.fault, FAULT_TC_WAIT) &&
+                      mbar_wait_bounded(&afull[ab], aph, a.fault, FAULT_TC_WAIT);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) { if (leader) *abort_flag = 1; break; }
+            tc_fence_after();
+            // B descriptors advance by 32 bytes per 16-k slice and by one x box (MPAD x 128 B)
+            // per 64 k: the start-address field is byte address / 16
+            const uint64_t bdesc0 = sw128_desc(xring + s * XB);
+            const uint32_t acol0 = tmem + A_COL0 + ab * ACOLS;
+            int ks = 0;
+            for (int j = 0; j < GPC; ++j) {
+                if (SPLIT && (j & 1) != me) { ks += KS; continue; }
+                const int slot = me * DH + d;
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&dempty[slot], dph ^ 1u, a.fault, FAULT_TC_WAIT));
+                if (!ok) break;
                 tc_fence_after();
-                // B descriptors advance by 32 bytes per 16-k slice and by one x box (MPAD x 128 B)
-                // per 64 k: the start-address field is byte address / 16
-                const uint64_t bdesc0 = sw128_desc(smem + s * SB + TC_STAGE_CODES);
-                const uint32_t acol0 = tmem + A_COL0 + ab * ACOLS;
-                int ks = 0;
-                for (int j = 0; j < GPC; ++j) {
-                    const int slot = me * DH + d;
-                    if (!mbar_wait_bounded(&dempty[slot], dph ^ 1u, a.fault, FAULT_TC_WAIT)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t dcol = tmem + D_COL0 + slot * MPAD;
-                    for (int t = 0; t < KS; ++t, ++ks) {
-                        const uint64_t bdesc = bdesc0 + (uint64_t)((ks >> 2) * (MPAD * 8) + (ks & 3) * 2);
-                        mma_ts(dcol, acol0 + ks * 8, bdesc, IDESC, t > 0 ? 1u : 0u);
-                    }
-                    tc_commit(&dfull[slot]);
-                    if (++d == DH) { d = 0; dph ^= 1u; }
+                const uint32_t dcol = tmem + D_COL0 + slot * MPAD;
+                for (int t = 0; t < KS; ++t) {
+                    const int kk = ks + t;
+                    const uint64_t bdesc = bdesc0 + (uint64_t)((kk >> 2) * (MPAD * 8) + (kk & 3) * 2);
+                    mma_ts_elect(dcol, acol0 + kk * 8, bdesc, IDESC, t > 0 ? 1u : 0u);
                 }
-                if (!ok) { *abort_flag = 1; break; }
-                tc_commit(&aempty[ab]);
-                tc_commit(&empty[s]);
+                tc_commit_elect(&dfull[slot]);
+                ks += KS;
+                if (++d == DH) { d = 0; dph ^= 1u; }
             }
+            if (!ok) { if (leader) *abort_flag = 1; break; }
+            tc_commit_elect(&aempty[ab]);
+            tc_commit_elect(&empty[s]);
         }
     } else if (warp >= 4 && warp < 4 + TC_DQ_WARPS) {
         // ---------------------------------------------------------------- dequant warps
@@ -316,54 +357,61 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         const int rbl = 2 * quarter + hf;               // row block (16 rows) within the 128-row unit
         const int g = lane >> 2, c4 = lane & 3;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter + 16 * hf) << 16);
-        uint32_t* zr = dq_ring + (warp - 4) * 32;       // this warp's slot: 16 rows x 2 words
-        // Unit u's copies, two units ahead, one cp.async group per unit: this warp's 2 KB of codes
+        // Unit u's copies, CD units ahead, one cp.async group per unit: this warp's 2 KB of codes
         // (16-row block rb * 8 + rbl, k tile c / 4, chunks (c % 4) * 4 .. + 3, contiguous in the
-        // fragment-order plane) into stage (u - u0) % S, and for INT4_ASYM the zero-point words of
-        // rows g and g + 8 (lanes c = 0, 1).  A single thread issuing the eight 2 KB bulk copies of
-        // a unit could not keep up with the stream (~0.14 us per copy).
-        auto issue_zeros = [&](long long u) {
+        // fragment-order plane) into code stage (u - u0) % CS, and for INT4_ASYM the zero-point words
+        // of rows g and g + 8 (lanes c = 0, 1).
+        auto issue_codes = [&](long long u) {
             if (u < u1) {
-                const int rbc = (int)u / a.CH, cc = (int)u % a.CH;
+                const int rbc = (int)(u / a.CH), cc = (int)(u % a.CH);
+                const int cs = (int)((u - u0) % CS);
                 if (rbc * 8 + rbl < a.NB) {
                     const uint8_t* src = a.wq + (long long)(rbc * 8 + rbl) * 16 * a.rowbytes + (long long)(cc >> 2) * 8192 +
                                          (cc & 3) * 4 * 512;
-                    uint8_t* dst = smem + ((int)(u - u0) % S) * SB + rbl * 2048;
+                    uint8_t* dst = cring + cs * TC_STAGE_CODES + rbl * 2048;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) tc_cp_async16(dst + q * 512 + lane * 16, src + q * 512 + lane * 16);
                 }
-            }
-            if constexpr (FMT == UQ_INT4_ASYM) {
-                if (u < u1 && c4 < 2) {
-                    const int rb = (int)u / a.CH, c = (int)u % a.CH;
-                    const int r = g + 8 * c4;
-                    const long long n = (long long)rb * TC_ROWS + rbl * 16 + r;
-                    const int Gn = a.K / G, ZB = (Gn + 1) >> 1;
-                    if (n < a.N)
-                        stage_span(zr + ((int)(u - u0) % 3) * (TC_DQ_WARPS * 32) + r * 2, a.zc,
-                                   n * ZB + (long long)c * (GPC >> 1), GPC >> 1, (long long)a.N * ZB);
+                if constexpr (FMT == UQ_INT4_ASYM) {
+                    if (c4 < 2) {
+                        const int r = g + 8 * c4;
+                        const long long n = (long long)rbc * TC_ROWS + rbl * 16 + r;
+                        const int Gn = a.K / G, ZB = (Gn + 1) >> 1;
+                        if (n < a.N)
+                            stage_span(dq_ring + cs * (TC_DQ_WARPS * 32) + (warp - 4) * 32 + r * 2, a.zc,
+                                       n * ZB + (long long)cc * (GPC >> 1), GPC >> 1, (long long)a.N * ZB);
+                    }
                 }
             }
             cp_async_commit();
         };
-        issue_zeros(u0);
-        issue_zeros(u0 + 1);
-        int s = 0, ab = 0, zslot = 0;
-        uint32_t sph = 0, aph = 1;                      // full[s] phase; aempty[] of the first round is free
-        int rb = (int)u0 / a.CH, c = (int)u0 % a.CH;
-        for (long long u = u0; u < u1 && !*abort_flag; ++u) {
-            __syncwarp();
-            issue_zeros(u + 2);
+        // the first unit alone at first: requested together with the next CD - 1 units, its bytes would
+        // arrive only with theirs; the others follow once it has landed
+        issue_codes(u0);
+        int ab = 0;
+        uint32_t aph = 1;                               // aempty[] of the first round counts as free
+        int rb = (int)(u0 / a.CH), c = (int)(u0 % a.CH);
+        for (long long u = u0; u < u1; ++u) {
+            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+            __syncwarp();                               // every lane is done with the stage refilled next
+            const int cs = (int)((u - u0) % CS);
             // subtrahend per group as a bf16 pair: 128 + z (INT4_ASYM), 128 + 8 (INT4_SYM), 128 (K4)
             constexpr int ZG = (FMT == UQ_INT4_ASYM) ? 16 / GB : 1;   // groups per unit
             uint32_t zlo[ZG], zhi[ZG];
 #pragma unroll
             for (int j = 0; j < ZG; ++j) zlo[j] = zhi[j] = (FMT == UQ_INT4_SYM) ? 0x43084308u : 0x43004300u;
-            cp_async_wait2();                               // unit u's codes (and zero words) landed
-            __syncwarp();
+            if (u == u0) {
+                cp_async_wait<0>();                     // the first unit's codes (and zero words) landed
+                __syncwarp();
+                for (int j = 1; j <= CD; ++j) issue_codes(u0 + j);
+            } else {
+                issue_codes(u + CD);
+                cp_async_wait<CD>();                    // unit u's codes (and zero words) landed
+                __syncwarp();
+            }
             if constexpr (FMT == UQ_INT4_ASYM) {
                 const int Gn = a.K / G, ZB = (Gn + 1) >> 1;
-                const uint32_t* slot = zr + zslot * (TC_DQ_WARPS * 32);
+                const uint32_t* slot = dq_ring + cs * (TC_DQ_WARPS * 32) + (warp - 4) * 32;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const long long n = (long long)rb * TC_ROWS + rbl * 16 + g + 8 * h;
@@ -385,7 +433,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) { *abort_flag = 1; break; }
             tc_fence_after();
-            const uint8_t* rbase = smem + s * SB + rbl * 2048 + lane * 16;
+            const uint8_t* rbase = cring + cs * TC_STAGE_CODES + rbl * 2048 + lane * 16;
             const uint32_t acol = lane_addr + A_COL0 + ab * ACOLS;
             if constexpr (FMT == UQ_INT8_SYM) {
                 // chunk q = 32 k = blocks 2q, 2q + 1; word 2b + h = row g + 8h, k 4c .. 4c + 3 of block b
@@ -431,69 +479,72 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&afull[ab]);
-            if (++s == S) { s = 0; sph ^= 1u; }
-            ab ^= 1;
-            if (ab == 0) aph ^= 1u;
-            if (++zslot == 3) zslot = 0;
+            if (++ab == NA) { ab = 0; aph ^= 1u; }
             if (++c == a.CH) { c = 0; ++rb; }
         }
         asm volatile("cp.async.wait_all;" ::: "memory");   // no copy lands after the CTA left
     } else if (warp >= 4 + TC_DQ_WARPS) {
-        // ---------------------------------------------------------------- epilogue warpgroup
+        // ---------------------------------------------------------------- epilogue warps
+        // Eight warps: warp 12 + e reads lane quarter e % 4 (rows 32 (e % 4) .. + 31, thread = row) and
+        // columns [HW (e / 4), HW (e / 4) + HW) of every accumulator slot.
         asm volatile("griddepcontrol.wait;" ::: "memory");   // sx, workspace and y follow earlier work
-        const int we = warp & 3;
-        const int r = we * 32 + lane;
-        const uint32_t lane_addr = tmem + ((uint32_t)(we * 32) << 16);
-        uint32_t* er = epi_ring + r * SWORDS;            // this thread's slot (ring stride 128 * SWORDS)
-        // this row's scale words (K4: its super-block record) staged three units ahead
+        const int we = warp - 4 - TC_DQ_WARPS;
+        const int quarter = we & 3, col0 = (we >> 2) * HW;
+        const int r = quarter * 32 + lane;
+        const int et = we * 32 + lane;                   // epilogue thread index
+        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+        uint32_t* er = epi_ring + et * SWORDS;           // this thread's slot (ring stride 256 * SWORDS)
+        constexpr int RSTRIDE = 32 * EW * SWORDS;
+        // this row's scale words (K4: its super-block record) staged TC_EPI_RING - 1 units ahead
         auto issue_scales = [&](long long u) {
             if (u < u1) {
-                const int rb = (int)u / a.CH, c = (int)u % a.CH;
-                const long long n = (long long)rb * TC_ROWS + r;
-                uint32_t* dst = er + ((int)(u - u0) % 3) * (128 * SWORDS);
+                const int rbu = (int)(u / a.CH), cu = (int)(u % a.CH);
+                const long long n = (long long)rbu * TC_ROWS + r;
+                uint32_t* dst = er + (int)((u - u0) % TC_EPI_RING) * RSTRIDE;
                 if (n < a.N) {
                     if constexpr (FMT == UQ_K4) {
-                        tc_cp_async16(dst, a.scales + (n * (a.K >> 8) + c) * 16);
+                        tc_cp_async16(dst, a.scales + (n * (a.K >> 8) + cu) * 16);
                     } else {
                         const long long Gn = a.K / G;
-                        stage_span(dst, a.scales, (n * Gn + (long long)c * GPC) * 2, GPC * 2, (long long)a.N * Gn * 2);
+                        stage_span(dst, a.scales, (n * Gn + (long long)cu * GPC) * 2, GPC * 2, (long long)a.N * Gn * 2);
                     }
                 }
             }
             cp_async_commit();
         };
-        issue_scales(u0);
-        issue_scales(u0 + 1);
-        float acc[MPAD];
+        for (int j = 0; j < TC_EPI_RING - 1; ++j) issue_scales(u0 + j);
+        float acc[HW];
 #pragma unroll
-        for (int m = 0; m < MPAD; ++m) acc[m] = 0.f;
+        for (int m = 0; m < HW; ++m) acc[m] = 0.f;
         // accumulator slots: unit u's groups are in the ring of the issuer that took it ((u - u0) mod
         // the issuer count), slots [DH * ring, DH * ring + DH), consumed in that issuer's order
         const int DH = DS / NISS;
-        int dring[2] = {0, 0}, eslot = 0;
-        uint32_t dphr[2] = {0u, 0u}, ephase = 0;
-        // all 128 epilogue threads meet here (bounded: returns false after the time limit)
+        int dr0 = 0, dr1 = 0;                            // next slot of issuer ring 0 / 1
+        uint32_t dp0 = 0u, dp1 = 0u, ephase = 0;         // and its phase
+        // all epilogue threads meet here (bounded: returns false after the time limit)
         auto epi_sync = [&]() -> bool {
             mbar_arrive(ebar);
             const bool r_ok = mbar_wait_bounded(ebar, ephase, a.fault, FAULT_TC_WAIT);
             ephase ^= 1u;
             return r_ok;
         };
-        const int first_rb = (int)u0 / a.CH;
-        int rb = first_rb, c = (int)u0 % a.CH;
-        for (long long u = u0; u < u1 && !*abort_flag; ++u) {
+        const int first_rb = (int)(u0 / a.CH);
+        int pend0 = -1, pend1 = -1;                      // row blocks whose partial sums this CTA stored
+        int rb = first_rb, c = (int)(u0 % a.CH);
+        for (long long u = u0; u < u1; ++u) {
+            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
             const int n = rb * TC_ROWS + r;
             const bool live = n < a.N;
-            issue_scales(u + 2);
-            cp_async_wait2();
-            const uint32_t* sw = er + eslot * (128 * SWORDS);
-            if (++eslot == 3) eslot = 0;
+            issue_scales(u + TC_EPI_RING - 1);
+            cp_async_wait<TC_EPI_RING - 1>();
+            const uint32_t* sw = er + (int)((u - u0) % TC_EPI_RING) * RSTRIDE;
             const int so = live ? (int)(((long long)n * (a.K / G) + (long long)c * GPC) & 1) : 0;   // halves
-            const int ring = NISS == 2 ? (int)((u - u0) & 1) : 0;
-            int d = ring ? dring[1] : dring[0];
-            uint32_t dph = ring ? dphr[1] : dphr[0];
             bool ok = true;
             for (int j = 0; j < GPC; ++j) {
+                // the issuer ring holding group j of unit u: SPLIT: j mod 2; alternate units: (u - u0) mod 2
+                const int ring = SPLIT ? (j & 1) : (NISS == 2 ? (int)((u - u0) & 1) : 0);
+                int d = ring ? dr1 : dr0;
+                uint32_t dph = ring ? dp1 : dp0;
                 float s1 = 0.f, s2 = 0.f;
                 if (live) {
                     if constexpr (FMT == UQ_K4) {
@@ -510,33 +561,23 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                 ok = __all_sync(0xffffffffu, mbar_wait_bounded(&dfull[slot], dph, a.fault, FAULT_TC_WAIT));
                 if (!ok) break;
                 tc_fence_after();
-                // up to 32 columns per wait for the loads (more would spill beside acc[64])
-                constexpr int QN = MPAD / 16, QB = QN < 2 ? QN : 2;
+                float v[HW];
 #pragma unroll
-                for (int q0 = 0; q0 < QN; q0 += QB) {
-                    float v[QB][16];
-#pragma unroll
-                    for (int q = 0; q < QB; ++q)
-                        if (q0 + q < QN) tmem_ld16(lane_addr + D_COL0 + slot * MPAD + (q0 + q) * 16, v[q]);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int q = 0; q < QB; ++q)
-                        if (q0 + q < QN)
-#pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                acc[(q0 + q) * 16 + e] = fmaf(s1, v[q][e], acc[(q0 + q) * 16 + e]);
-                }
+                for (int q = 0; q < HW / 8; ++q) tmem_ld8(lane_addr + D_COL0 + slot * MPAD + col0 + q * 8, &v[q * 8]);
+                tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&dempty[slot]);
-                if (++d == DH) { d = 0; dph ^= 1u; }
-                if constexpr (FMT == UQ_K4) {
-                    const float* sx = a.sx + (long long)((c * KC + j * 32) >> 5) * MPAD;
 #pragma unroll
-                    for (int m = 0; m < MPAD; ++m) acc[m] = fmaf(-s2, __ldg(sx + m), acc[m]);
+                for (int m = 0; m < HW; ++m) acc[m] = fmaf(s1, v[m], acc[m]);
+                if (++d == DH) { d = 0; dph ^= 1u; }
+                if (ring) { dr1 = d; dp1 = dph; } else { dr0 = d; dp0 = dph; }
+                if constexpr (FMT == UQ_K4) {
+                    const float* sx = a.sx + (long long)((c * KC + j * 32) >> 5) * MPAD + col0;
+#pragma unroll
+                    for (int m = 0; m < HW; ++m) acc[m] = fmaf(-s2, __ldg(sx + m), acc[m]);
                 }
             }
-            if (ring) { dring[1] = d; dphr[1] = dph; } else { dring[0] = d; dphr[0] = dph; }
             if (!ok) { *abort_flag = 1; break; }
             if (c == a.CH - 1 || u == u1 - 1) {
                 // row block finished for this CTA: store y, or a partial and a ticket
@@ -544,48 +585,62 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                 if (fullcov) {
                     if (live)
 #pragma unroll
-                        for (int m = 0; m < MPAD; ++m)
-                            if (m < a.M)
-                                a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+                        for (int m = 0; m < HW; ++m)
+                            if (col0 + m < a.M)
+                                a.y[(long long)(col0 + m) * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
                 } else {
-                    const int slot = 2 * cta + (rb == first_rb ? 0 : 1);
-                    float* part = a.partials + (long long)slot * TC_ROWS * MPAD + r;   // [slot][m][row]
+                    // partial sums of a row block shared with other CTAs: stored now, combined after the
+                    // CTA's last unit (so the pipeline never waits on other CTAs mid-run)
+                    const int pslot = 2 * cta + (rb == first_rb ? 0 : 1);
+                    float* part = a.partials + (long long)pslot * TC_ROWS * MPAD + r;   // [slot][m][row]
 #pragma unroll
-                    for (int m = 0; m < MPAD; ++m) part[m * TC_ROWS] = acc[m];
-                    __threadfence();
-                    if (!epi_sync()) { *abort_flag = 1; break; }
-                    if (r == 0) *ticket_smem = atomicAdd(a.tickets + rb, 1u);
-                    if (!epi_sync()) { *abort_flag = 1; break; }
-                    const unsigned int old = *ticket_smem;
-                    const long long uf = (long long)rb * a.CH;
-                    const int cf = tworker_of(uf, a.U, a.P), cl = tworker_of(uf + a.CH - 1, a.U, a.P);
-                    if (old == (unsigned int)(cl - cf)) {
-                        __threadfence();
-                        // the partials of all contributors, summed in CTA order into acc
-#pragma unroll
-                        for (int m = 0; m < MPAD; ++m) acc[m] = 0.f;
-                        for (int c2 = cf; c2 <= cl; ++c2) {
-                            const int rb2 = (int)(trange_begin(c2, a.U, a.P) / a.CH);
-                            const int slot2 = 2 * c2 + (rb == rb2 ? 0 : 1);
-                            const float* p2 = a.partials + (long long)slot2 * TC_ROWS * MPAD + r;
-#pragma unroll
-                            for (int m = 0; m < MPAD; ++m) acc[m] += __ldcg(p2 + m * TC_ROWS);
-                        }
-                        if (live)
-#pragma unroll
-                            for (int m = 0; m < MPAD; ++m)
-                                if (m < a.M)
-                                    a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
-                        if (r == 0) a.tickets[rb] = 0u;
-                    }
-                    if (!epi_sync()) { *abort_flag = 1; break; }
+                    for (int m = 0; m < HW; ++m) part[(col0 + m) * TC_ROWS] = acc[m];
+                    if (pend0 < 0) pend0 = rb; else pend1 = rb;
                 }
 #pragma unroll
-                for (int m = 0; m < MPAD; ++m) acc[m] = 0.f;
+                for (int m = 0; m < HW; ++m) acc[m] = 0.f;
             }
             if (++c == a.CH) { c = 0; ++rb; }
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
+        // Row blocks shared with other CTAs: every contributor makes its partial sums visible, then takes
+        // a ticket; the last one sums all contributors' partials in CTA order (fixed, so the result is
+        // deterministic) and writes y.  Nobody waits for another CTA.
+        if (pend0 >= 0 && !__shfl_sync(0xffffffffu, *abort_flag, 0)) {
+            __threadfence();
+            bool ok = epi_sync();
+            if (ok && et == 0) {
+                ticket_smem[0] = atomicAdd(a.tickets + pend0, 1u);
+                if (pend1 >= 0) ticket_smem[1] = atomicAdd(a.tickets + pend1, 1u);
+            }
+            ok = ok && epi_sync();
+            for (int k = 0; ok && k < 2; ++k) {
+                const int prb = k ? pend1 : pend0;
+                if (prb < 0) continue;
+                const unsigned int old = ticket_smem[k];
+                const long long uf = (long long)prb * a.CH;
+                const int cf = tworker_of(uf, a.U, a.P), cl = tworker_of(uf + a.CH - 1, a.U, a.P);
+                if (old != (unsigned int)(cl - cf)) continue;
+                __threadfence();
+#pragma unroll
+                for (int m = 0; m < HW; ++m) acc[m] = 0.f;
+                for (int c2 = cf; c2 <= cl; ++c2) {
+                    const int rb2 = (int)(trange_begin(c2, a.U, a.P) / a.CH);
+                    const int slot2 = 2 * c2 + (prb == rb2 ? 0 : 1);
+                    const float* p2 = a.partials + (long long)slot2 * TC_ROWS * MPAD + r;
+#pragma unroll
+                    for (int m = 0; m < HW; ++m) acc[m] += __ldcg(p2 + (col0 + m) * TC_ROWS);
+                }
+                const int n = prb * TC_ROWS + r;
+                if (n < a.N)
+#pragma unroll
+                    for (int m = 0; m < HW; ++m)
+                        if (col0 + m < a.M)
+                            a.y[(long long)(col0 + m) * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+                if (et == 0) a.tickets[prb] = 0u;
+            }
+            if (!ok) *abort_flag = 1;
+        }
     }
 
     tc_fence_before();
@@ -651,7 +706,7 @@ cudaError_t launch_tc_t(const CUtensorMap& mx, const TcArgs& a, size_t smem, int
     if (launch_overlap()) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid);
-        cfg.blockDim = dim3(TC_THREADS);
+        cfg.blockDim = dim3(tc_threads(MPAD));
         cfg.dynamicSmemBytes = smem;
         cfg.stream = st;
         cudaLaunchAttribute attr[1];
@@ -662,7 +717,7 @@ cudaError_t launch_tc_t(const CUtensorMap& mx, const TcArgs& a, size_t smem, int
         e = cudaLaunchKernelEx(&cfg, tc_kernel<FMT, MPAD, GB>, mx, a);
         if (e != cudaSuccess) return e;
     } else {
-        tc_kernel<FMT, MPAD, GB><<<grid, TC_THREADS, smem, st>>>(mx, a);
+        tc_kernel<FMT, MPAD, GB><<<grid, tc_threads(MPAD), smem, st>>>(mx, a);
     }
     return cudaGetLastError();
 }
@@ -681,7 +736,7 @@ cudaError_t launch_tc_mg(int mpad, const CUtensorMap& mx, const TcArgs& a, size_
 template <int FMT>
 cudaError_t launch_tc_m(int mpad, const CUtensorMap& mx, const TcArgs& a, size_t smem, int grid,
                         cudaStream_t st) {
-    if constexpr (FMT == UQ_INT4_ASYM) {
+    if constexpr (FMT != UQ_K4) {
         switch (a.group) {
             case 32: return launch_tc_mg<FMT, 2>(mpad, mx, a, smem, grid, st);
             case 64: return launch_tc_mg<FMT, 4>(mpad, mx, a, smem, grid, st);
@@ -689,7 +744,7 @@ cudaError_t launch_tc_m(int mpad, const CUtensorMap& mx, const TcArgs& a, size_t
             default: return cudaErrorInvalidValue;
         }
     } else {
-        return launch_tc_mg<FMT, 8>(mpad, mx, a, smem, grid, st);
+        return launch_tc_mg<FMT, 2>(mpad, mx, a, smem, grid, st);
     }
 }
 }  // namespace
@@ -700,26 +755,40 @@ bool tc_supported(int fmt, int N, int K) {
     return encode_fn() != nullptr;
 }
 
-int tc_plan(int fmt, int mpad, int* stages, int* dslots, size_t* smem) {
-    const int kc = (fmt == UQ_INT8_SYM) ? 128 : 256;
-    const int sb = TcSmem::stage_bytes(kc, mpad);
-    int rings = 0;
+namespace {
+template <int FMT, int GB>
+size_t tc_smem_fg(int mpad) {
+    switch (mpad) {
+        case 16: return TcPlan<FMT, 16, GB>::SMEM;
+        case 32: return TcPlan<FMT, 32, GB>::SMEM;
+        case 48: return TcPlan<FMT, 48, GB>::SMEM;
+        case 64: return TcPlan<FMT, 64, GB>::SMEM;
+        default: return 0;
+    }
+}
+template <int FMT>
+size_t tc_smem_fmt(int mpad, int group) {
+    if (FMT == UQ_K4) return tc_smem_fg<FMT, 2>(mpad);
+    switch (group) {
+        case 32: return tc_smem_fg<FMT, 2>(mpad);
+        case 64: return tc_smem_fg<FMT, 4>(mpad);
+        case 128: return tc_smem_fg<FMT, 8>(mpad);
+        default: return 0;
+    }
+}
+}  // namespace
+
+int tc_plan(int fmt, int mpad, int group, size_t* smem) {
+    size_t b = 0;
     switch (fmt) {
-        case UQ_INT4_SYM: rings = TcFmt<UQ_INT4_SYM>::EPI_RING + TcFmt<UQ_INT4_SYM>::DQ_RING; break;
-        case UQ_INT4_ASYM: rings = TcFmt<UQ_INT4_ASYM>::EPI_RING + TcFmt<UQ_INT4_ASYM>::DQ_RING; break;
-        case UQ_INT8_SYM: rings = TcFmt<UQ_INT8_SYM>::EPI_RING + TcFmt<UQ_INT8_SYM>::DQ_RING; break;
-        case UQ_K4: rings = TcFmt<UQ_K4>::EPI_RING + TcFmt<UQ_K4>::DQ_RING; break;
+        case UQ_INT4_SYM: b = tc_smem_fmt<UQ_INT4_SYM>(mpad, group); break;
+        case UQ_INT4_ASYM: b = tc_smem_fmt<UQ_INT4_ASYM>(mpad, group); break;
+        case UQ_INT8_SYM: b = tc_smem_fmt<UQ_INT8_SYM>(mpad, group); break;
+        case UQ_K4: b = tc_smem_fmt<UQ_K4>(mpad, group); break;
         default: return -1;
     }
-    const int budget = 227 * 1024 - 1024 - TC_BAR_BYTES - rings;
-    int s = budget / sb;
-    if (s > TC_MAX_STAGES) s = TC_MAX_STAGES;
-    if (s < 3) return -1;                           // codes are requested two units ahead
-    int ds = (TMEM_COLS - kc) / mpad;       // A takes 2 * kc/2 columns
-    if (ds > 8) ds = 8;
-    *stages = s;
-    *dslots = ds;
-    *smem = 1024 + (size_t)s * sb + TC_BAR_BYTES + rings;
+    if (!b) return -1;
+    *smem = b;
     return 0;
 }
 
