@@ -36,6 +36,8 @@ SIGNATURES = {
     "uq_gemm_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "uq_set_launch_overlap": (_I, [_I]),
     "uq_gemm_kernel_count": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I)]),
+    "uq_gemm_gated": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "uq_gemm_gated_kernel_count": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I)]),
 }
 
 _lib = None
@@ -126,6 +128,35 @@ def gemm(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, zc, N: int, gr
     _check(lib().uq_gemm(_ptr(x), _ptr(wq), _ptr(scales), _ptr(zc), _ptr(y), M, N, K, group, FORMATS[fmt],
                          _stream(stream)), "uq_gemm")
     return y
+
+
+def gemm_gated(x: torch.Tensor, gate: tuple, up: tuple, N: int, group: int, fmt: str,
+               h: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """h = silu(x . W_gate_hat^T) * (x . W_up_hat^T) (bf16 [M][N]); gate and up are (wq, scales, zc)."""
+    M, K = x.shape
+    assert x.dtype == torch.bfloat16
+    if h is None:
+        h = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    (wg, sg, zg), (wu, su, zu) = gate, up
+    _check(lib().uq_gemm_gated(_ptr(x), _ptr(wg), _ptr(sg), _ptr(zg), _ptr(wu), _ptr(su), _ptr(zu), _ptr(h),
+                               M, N, K, group, FORMATS[fmt], _stream(stream)), "uq_gemm_gated")
+    return h
+
+
+def gemm_gated_ptrs(x_ptr: int, gate: tuple, up: tuple, h_ptr: int, M: int, N: int, K: int, group: int, fmt: str,
+                    stream_handle: int) -> None:
+    """Raw-pointer form of uq_gemm_gated; gate and up are (wq_ptr, scales_ptr, zc_ptr or 0)."""
+    P = ctypes.c_void_p
+    _check(lib().uq_gemm_gated(P(x_ptr), P(gate[0]), P(gate[1]), P(gate[2]) if gate[2] else None, P(up[0]),
+                               P(up[1]), P(up[2]) if up[2] else None, P(h_ptr), M, N, K, group, FORMATS[fmt],
+                               P(stream_handle)), "uq_gemm_gated")
+
+
+def gemm_gated_kernel_count(M: int, N: int, K: int, group: int, fmt: str) -> int:
+    v = ctypes.c_int(0)
+    _check(lib().uq_gemm_gated_kernel_count(M, N, K, group, FORMATS[fmt], ctypes.byref(v)),
+           "uq_gemm_gated_kernel_count")
+    return v.value
 
 
 def gemm_noalloc(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, zc, N: int, group: int, fmt: str,

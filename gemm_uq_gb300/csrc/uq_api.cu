@@ -83,6 +83,8 @@ struct Workspace {
     size_t aux_bytes = 0;
     unsigned int* tickets = nullptr;   // zero between calls (the kernels reset what they use)
     size_t ticket_bytes = 0;
+    float* gate32 = nullptr;           // gated projection: fp32 gate outputs [M][N]
+    size_t gate32_bytes = 0;
 };
 std::map<std::pair<int, void*>, Workspace> g_ws;
 
@@ -162,10 +164,17 @@ uq_status workspace(int dev, cudaStream_t st, size_t partial_bytes, size_t ticke
     return UQ_OK;
 }
 
+// Output mode of a launch: plain bf16 y; or the gated projection's gate pass (fp32 into out32) or up
+// pass (bf16 silu(gate32) * result into y)
+struct OutMode {
+    float* out32 = nullptr;
+    const float* gate32 = nullptr;
+};
+
 // one GEMV launch for Mb <= 8 rows of x
 uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const void* zc, uint16_t* y,
                    int Mb, int N, int K, int ldx, int ldy, int group, int fmt, cudaStream_t st,
-                   const DeviceState& ds, int dev) {
+                   const DeviceState& ds, int dev, OutMode om = OutMode()) {
     const uq::Layout L(N, K, fmt);
     if (uq::gemv_smem_bytes(fmt, K, group, Mb) > 227 * 1024)
         return fail(UQ_ERR_UNSUPPORTED, "K=%d is too long for the GEMV's shared-memory x-sum table at M=%d", K, Mb);
@@ -177,7 +186,7 @@ uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const 
     uq_status s = workspace(dev, st, uq::gemv_partials_floats(fmt, T, (int)P, Mb) * sizeof(float),
                             (size_t)L.NB * sizeof(unsigned int), &ws);
     if (s != UQ_OK) return s;
-    uq::GemvArgs a;
+    uq::GemvArgs a = {};
     a.x = x;
     a.wq = static_cast<const uint8_t*>(wq);
     a.scales = static_cast<const uint8_t*>(scales);
@@ -189,6 +198,8 @@ uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const 
     a.tickets = ws->tickets;
     a.fault = ds.words;
     a.overlap = 0;
+    a.out32 = om.out32;
+    a.gate32 = om.gate32;
     const int grid = uq::gemv_grid(a, fmt, ds.sms);
     cudaError_t e = uq::launch_gemv(fmt, a, grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "GEMV launch");
@@ -198,7 +209,8 @@ uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const 
 
 // one tensor-core launch for 16 <= Mb <= 64 rows of x
 uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const void* zc, uint16_t* y, int Mb, int N,
-                 int K, int ldx, int ldy, int group, int fmt, cudaStream_t st, const DeviceState& ds, int dev) {
+                 int K, int ldx, int ldy, int group, int fmt, cudaStream_t st, const DeviceState& ds, int dev,
+                 OutMode om = OutMode()) {
     const int mpad = (Mb + 15) / 16 * 16;
     size_t smem = 0;
     if (uq::tc_plan(fmt, mpad, group, &smem) != 0)
@@ -219,7 +231,7 @@ uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const vo
         e = uq::launch_colsum32(x, ws->aux, Mb, mpad, K, ldx, st);
         if (e != cudaSuccess) return cuda_fail(e, "column-sum launch");
     }
-    uq::TcArgs a;
+    uq::TcArgs a = {};
     const uq::Layout L(N, K, fmt);
     a.wq = static_cast<const uint8_t*>(wq);
     a.rowbytes = L.rowbytes;
@@ -233,6 +245,8 @@ uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const vo
     a.partials = ws->partials;
     a.tickets = ws->tickets;
     a.fault = ds.words;
+    a.out32 = om.out32;
+    a.gate32 = om.gate32;
     e = uq::launch_tc(fmt, x, a, smem, (int)P, st);
     if (e != cudaSuccess) return cuda_fail(e, "tensor-core launch");
     return UQ_OK;
@@ -373,6 +387,69 @@ uq_status uq_gemm(const uint16_t* x, const void* wq, const void* scales, const v
                      group, fmt, st, *ds, dev);
         if (s != UQ_OK) return s;
     }
+    return UQ_OK;
+}
+
+uq_status uq_gemm_gated(const uint16_t* x, const void* wq_gate, const void* scales_gate, const void* zc_gate,
+                        const void* wq_up, const void* scales_up, const void* zc_up, uint16_t* h,
+                        int M, int N, int K, int group, uq_fmt fmt, void* stream) {
+    uq_status s = check_shape(N, K, group, fmt);
+    if (s != UQ_OK) return s;
+    if (M < 0) return fail(UQ_ERR_INVALID, "negative M");
+    if (M == 0 || N == 0) return UQ_OK;
+    if (!h) return fail(UQ_ERR_INVALID, "h is NULL");
+    if (!aligned16(h)) return fail(UQ_ERR_ALIGN, "h must be 16-byte aligned");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (K == 0) {   // g = u = 0, silu(0) * 0 = 0
+        cudaError_t e = cudaMemsetAsync(h, 0, (size_t)M * N * 2, st);
+        return e == cudaSuccess ? UQ_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    if (!x || !wq_gate || !wq_up) return fail(UQ_ERR_INVALID, "x, wq_gate or wq_up is NULL");
+    if (!aligned16(x) || !aligned16(wq_gate) || !aligned16(wq_up))
+        return fail(UQ_ERR_ALIGN, "x, wq_gate and wq_up must be 16-byte aligned");
+    if ((s = check_meta_ptrs(scales_gate, zc_gate, fmt)) != UQ_OK) return s;
+    if ((s = check_meta_ptrs(scales_up, zc_up, fmt)) != UQ_OK) return s;
+    DeviceState* ds = nullptr;
+    int dev = 0;
+    if ((s = device_state(&ds, &dev)) != UQ_OK) return s;
+    const bool tc = M >= 16 && uq::tc_supported(fmt, N, K);
+    const int block = tc ? 64 : 8;
+    const int rows = M < block ? M : block;
+    float* g32 = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        Workspace& w = g_ws[{dev, (void*)st}];
+        s = grow(reinterpret_cast<void**>(&w.gate32), &w.gate32_bytes, (size_t)rows * N * sizeof(float), false, st, dev);
+        if (s != UQ_OK) return s;
+        g32 = w.gate32;
+    }
+    // per block of rows of x: the gate projection into fp32 scratch, then the up projection, whose
+    // epilogue writes h = bf16(silu(g) * u)
+    for (int m0 = 0; m0 < M; m0 += block) {
+        const int mb = (M - m0) < block ? (M - m0) : block;
+        const uint16_t* xb = x + (long long)m0 * K;
+        uint16_t* hb = h + (long long)m0 * N;
+        OutMode gate_pass, up_pass;
+        gate_pass.out32 = g32;
+        up_pass.gate32 = g32;
+        if (tc) {
+            s = run_tc(xb, wq_gate, scales_gate, zc_gate, hb, mb, N, K, K, N, group, fmt, st, *ds, dev, gate_pass);
+            if (s == UQ_OK)
+                s = run_tc(xb, wq_up, scales_up, zc_up, hb, mb, N, K, K, N, group, fmt, st, *ds, dev, up_pass);
+        } else {
+            s = run_gemv(xb, wq_gate, scales_gate, zc_gate, hb, mb, N, K, K, N, group, fmt, st, *ds, dev, gate_pass);
+            if (s == UQ_OK)
+                s = run_gemv(xb, wq_up, scales_up, zc_up, hb, mb, N, K, K, N, group, fmt, st, *ds, dev, up_pass);
+        }
+        if (s != UQ_OK) return s;
+    }
+    return UQ_OK;
+}
+
+uq_status uq_gemm_gated_kernel_count(int M, int N, int K, int group, uq_fmt fmt, int* count) {
+    uq_status s = uq_gemm_kernel_count(M, N, K, group, fmt, count);
+    if (s != UQ_OK || M == 0 || N == 0) return s;
+    if (K > 0) *count *= 2;                                 // the gate pass and the up pass
     return UQ_OK;
 }
 

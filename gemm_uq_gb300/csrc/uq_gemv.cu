@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(256) gemv_split_reduce(const GemvArgs a) {
         const float* p = a.partials + e;                            // k tile 0 of (nb, r, m)
         float sum = 0.f;
         for (int kb = 0; kb < KB; ++kb) sum += p[kb * kstride];
-        a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+        store_out(a, m, n, sum);
     }
 }
 

@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
                     for (int m = 0; m < M; ++m) {
                         const int n = n0 + g + 8 * j;
                         if (mine[j][m] && n < a.N)
-                            a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(out[j][m]));
+                            store_out(a, m, n, out[j][m]);
                     }
             } else {
                 const int slot = 2 * w + (nb == first_nb ? 0 : 1);
@@ -576,7 +576,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
                             const int slot2 = 2 * w2 + (nb == nb2 ? 0 : 1);
                             sum += __ldcg(a.partials + (long long)slot2 * RB * M + e);
                         }
-                        a.y[(long long)m * a.ldy + n0 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+                        store_out(a, m, n0 + r, sum);
                     }
                     if (lane == 0) a.tickets[nb] = 0u;
                 }
@@ -1022,7 +1022,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
             const unsigned l2 = ti - w2 * Tc / W;
             sum += cpart[((w2 * MMA_TPW + l2) * RB + r) * 8 + m];
         }
-        a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+        store_out(a, m, n, sum);
     }
 }
 

@@ -44,6 +44,8 @@ struct GemvArgs {
     int overlap;              // launched with programmatic stream serialization (set by the launcher)
     int cta_rows;             // mma GEMV: 1 = every CTA owns whole row blocks (combined in shared memory,
                               // no second pass); 0 = workers split row blocks anywhere (second pass)
+    float* out32;             // gate pass of the gated projection: fp32 results [M][ldy] instead of y
+    const float* gate32;      // up pass: y = bf16(silu(gate32) * result), gate32 [M][ldy] fp32
 };
 constexpr int GEMV_WARPS = 4;     // worker warps per CTA
 // formats whose GEMV runs on mma.sync (the others on CUDA-core FMAs)
@@ -77,7 +79,26 @@ struct TcArgs {
     float* partials;          // [2P][128][Mpad]
     unsigned int* tickets;    // [ceil(N/128)]
     unsigned int* fault;
+    float* out32;             // gate pass of the gated projection: fp32 results [M][ldy] instead of y
+    const float* gate32;      // up pass: y = bf16(silu(gate32) * result)
 };
+
+// The one place every kernel writes an output element (row m of x, output column n): bf16 y; or, for
+// the gated projection, fp32 g (the gate pass) or bf16 silu(g) * u (the up pass; silu(g) = g / (1 + e^-g)
+// in fp32, the product in fp32, one rounding to bf16).
+template <class Args>
+__device__ __forceinline__ void store_out(const Args& a, int m, int n, float v) {
+    const long long idx = (long long)m * a.ldy + n;
+    if (a.out32) {
+        a.out32[idx] = v;
+        return;
+    }
+    if (a.gate32) {
+        const float g = a.gate32[idx];
+        v = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), v);
+    }
+    a.y[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
 bool tc_supported(int fmt, int N, int K);
 int tc_plan(int fmt, int mpad, int group, size_t* smem);   // dynamic shared memory of the launch
 cudaError_t launch_colsum32(const uint16_t* x, float* sx, int M, int mpad, int K, int ldx, cudaStream_t st);

@@ -587,7 +587,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
 #pragma unroll
                         for (int m = 0; m < HW; ++m)
                             if (col0 + m < a.M)
-                                a.y[(long long)(col0 + m) * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+                                store_out(a, col0 + m, n, acc[m]);
                 } else {
                     // partial sums of a row block shared with other CTAs: stored now, combined after the
                     // CTA's last unit (so the pipeline never waits on other CTAs mid-run)
@@ -636,7 +636,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
 #pragma unroll
                     for (int m = 0; m < HW; ++m)
                         if (col0 + m < a.M)
-                            a.y[(long long)(col0 + m) * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+                            store_out(a, col0 + m, n, acc[m]);
                 if (et == 0) a.tickets[prb] = 0u;
             }
             if (!ok) *abort_flag = 1;

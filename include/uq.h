@@ -145,6 +145,28 @@ uq_status uq_gemm(const uint16_t* x, const void* wq, const void* scales,
                   int M, int N, int K, int group, uq_fmt fmt, void* stream);
 
 /*
+ * uq_gemm_gated -- the gated MLP's gate and up projections with the SiLU-multiply epilogue
+ * ("Ultra LLM Engine", section "How the Engine Works": every layer ends in a gated MLP; read as the
+ * Llama-style SiLU gate):
+ *     h[m][n] = bf16_RNE( silu(g) * u ),  g = sum_k x[m][k] W_gate_hat[n][k],  u = sum_k x[m][k] W_up_hat[n][k],
+ * g and u accumulated in fp32 exactly as uq_gemm does, silu(g) = g / (1 + e^-g) and the product in
+ * fp32, one rounding to bf16 (no bf16 rounding of g or u).
+ *   x (device) bf16 [M][K]; wq_gate / scales_gate / zc_gate and wq_up / scales_up / zc_up (device):
+ *   two weights of the same N, K, group and format, each as uq_gemm takes them; h (device) bf16
+ *   [M][N], written.  M == 0 or N == 0 is a no-op; K == 0 writes zeros.
+ * Paths, per block of rows of x (8 on the GEMV, 64 on the tensor-core path, routed as uq_gemm):
+ * the gate projection into fp32 library scratch, then the up projection, whose epilogue reads g and
+ * writes h; uq_gemm_gated_kernel_count gives the launches.  Scratch, errors and stream capture as
+ * uq_gemm (the fp32 gate scratch, rows x N floats, is part of the per-stream workspace).
+ */
+uq_status uq_gemm_gated(const uint16_t* x, const void* wq_gate, const void* scales_gate, const void* zc_gate,
+                        const void* wq_up, const void* scales_up, const void* zc_up, uint16_t* h,
+                        int M, int N, int K, int group, uq_fmt fmt, void* stream);
+
+/* uq_gemm_gated_kernel_count -- kernels one uq_gemm_gated call of this shape launches (as uq_gemm_kernel_count). */
+uq_status uq_gemm_gated_kernel_count(int M, int N, int K, int group, uq_fmt fmt, int* count);
+
+/*
  * uq_unpack_codes -- debug: packed plane -> int8 codes [N][K] (device), bit-exact
  * inverse of uq_pack_layout.  It decodes every code word with the register unpacking
  * the GEMV and tensor-core kernels run (shift + lop3 magic-exponent pairs for 4- and
