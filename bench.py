@@ -280,16 +280,43 @@ def build_weights(spec, dev, layers=None, seed_base=12345):
     return recs
 
 
-class Step:
-    """One pass over every linear of a workload at M rows: x and y buffers, the launch order (groups
-    of linears reading the same input on parallel branches), and its CUDA graph."""
+def gated_bytes(fmt, group, N, K, M):
+    """Algorithmic bytes of the gated projection: both weights' codes and metadata, x once, h once."""
+    w = alg_bytes(fmt, group, N, K, 0)
+    return 2 * w + 2 * M * K + 2 * M * N
 
-    def __init__(self, recs, fmt, group, M, dev, stream, seed):
+
+def step_ops(recs, gated):
+    """The step's ops in launch order: one uq_gemm per linear, except that with `gated` a layer's gate
+    linear and the up linear right after it (same shape) form one uq_gemm_gated op."""
+    ops = []
+    i = 0
+    while i < len(recs):
+        r = recs[i]
+        nxt = recs[i + 1] if i + 1 < len(recs) else None
+        if (gated and r["name"].endswith(".gate") and nxt is not None and nxt["name"].endswith(".up")
+                and (nxt["N"], nxt["K"]) == (r["N"], r["K"])):
+            ops.append(dict(kind="gated", recs=[r, nxt], name=r["name"][:-len("gate")] + "gate_up",
+                            N=r["N"], K=r["K"]))
+            i += 2
+        else:
+            ops.append(dict(kind="gemm", recs=[r], name=r["name"], N=r["N"], K=r["K"]))
+            i += 1
+    return ops
+
+
+class Step:
+    """One pass over every linear of a workload at M rows: x and output buffers, the launch order (ops
+    reading the same input on parallel branches), and its CUDA graph.  With `gated`, a layer's gate
+    and up linears are one op: uq_gemm_gated, h = silu(x Wg^T) * (x Wu^T)."""
+
+    def __init__(self, recs, fmt, group, M, dev, stream, seed, gated=True):
         import torch
         self.recs, self.fmt, self.group, self.M, self.stream = recs, fmt, group, M, stream
-        x_sizes = [M * r["K"] for r in recs]
-        y_sizes = [M * r["N"] for r in recs]
-        # x of every linear in one device buffer (the end-to-end leg copies it with one memcpy)
+        self.ops = step_ops(recs, gated)
+        x_sizes = [M * op["K"] for op in self.ops]
+        y_sizes = [M * op["N"] for op in self.ops]
+        # x of every op in one device buffer (the end-to-end leg copies it with one memcpy)
         self.xbuf = torch.empty(sum(x_sizes), dtype=torch.bfloat16, device=dev)
         self.ybuf = torch.empty(sum(y_sizes), dtype=torch.bfloat16, device=dev)
         g = torch.Generator(device=dev)
@@ -302,20 +329,29 @@ class Step:
             self.io.append((self.xbuf[ox:ox + xs], self.ybuf[oy:oy + ys]))
             ox += xs
             oy += ys
-        self.bytes = sum(alg_bytes(fmt, group, r["N"], r["K"], M) for r in recs)
+        self.bytes = sum(gated_bytes(fmt, group, op["N"], op["K"], M) if op["kind"] == "gated"
+                         else alg_bytes(fmt, group, op["N"], op["K"], M) for op in self.ops)
         self.flops = sum(alg_flops(r["N"], r["K"], M) for r in recs)
-        self.groups = launch_groups([r["name"] for r in recs])
+        self.groups = launch_groups([op["name"] for op in self.ops])
         width = max(len(gr) for gr in self.groups)
         self.side = [torch.cuda.Stream(device=dev) for _ in range(width - 1)]
         self.graph = None
 
     def launch(self, i, st):
         import gemm_uq_gb300 as uq
-        r = self.recs[i]
+        op = self.ops[i]
         x, y = self.io[i]
-        uq.gemm_ptrs(x.data_ptr(), r["wq"].data_ptr(), r["scales"].data_ptr(),
-                     r["zc"].data_ptr() if r["zc"] is not None else 0, y.data_ptr(),
-                     self.M, r["N"], r["K"], self.group, self.fmt, st.cuda_stream)
+
+        def ptrs(r):
+            return (r["wq"].data_ptr(), r["scales"].data_ptr(), r["zc"].data_ptr() if r["zc"] is not None else 0)
+
+        if op["kind"] == "gated":
+            uq.gemm_gated_ptrs(x.data_ptr(), ptrs(op["recs"][0]), ptrs(op["recs"][1]), y.data_ptr(), self.M,
+                               op["N"], op["K"], self.group, self.fmt, st.cuda_stream)
+        else:
+            w, sc, zc = ptrs(op["recs"][0])
+            uq.gemm_ptrs(x.data_ptr(), w, sc, zc, y.data_ptr(), self.M, op["N"], op["K"], self.group, self.fmt,
+                         st.cuda_stream)
 
     def issue(self):
         import torch
@@ -364,10 +400,17 @@ class Step:
         return e0.elapsed_time(e1) / steps
 
     def launches(self):
-        return sum(kernels_per_call(self.fmt, self.group, self.M, r["N"], r["K"]) for r in self.recs)
+        import gemm_uq_gb300 as uq
+        n = 0
+        for op in self.ops:
+            if op["kind"] == "gated":
+                n += uq.gemm_gated_kernel_count(self.M, op["N"], op["K"], self.group, self.fmt)
+            else:
+                n += kernels_per_call(self.fmt, self.group, self.M, op["N"], op["K"])
+        return n
 
 
-def run_sweep(dev, stream, hbm, tf):
+def run_sweep(dev, stream, hbm, tf, gated=True):
     """The M sweep, the format sweep and the 70B-shaped stack, each point on its own graph."""
     import torch
     out = []
@@ -377,12 +420,13 @@ def run_sweep(dev, stream, hbm, tf):
         recs = build_weights(spec, dev, layers=layers, seed_base=20000)
         shapes = sorted({(r["N"], r["K"]) for r in recs})
         for M in ms:
-            st = Step(recs, fmt, group, M, dev, stream, seed=4242 + M).capture()
+            st = Step(recs, fmt, group, M, dev, stream, seed=4242 + M, gated=gated).capture()
             probe = st.time(3, 2)
             reps = int(min(200, max(5, 25.0 / max(probe, 1e-3))))
             ms_ = st.time(3, reps)
             t_roof = roofline_time_s(st.bytes, st.flops, hbm, tf)
             out.append({"workload": wl, "fmt": fmt, "group": group, "M": M, "linears": len(recs),
+                        "ops": len(st.ops),
                         "shapes": [f"{n}x{k}" for n, k in shapes],
                         "GB/s": round(st.bytes / (ms_ * 1e-3) / 1e9, 1),
                         "TFLOP/s": round(st.flops / (ms_ * 1e-3) / 1e12, 2),
@@ -412,7 +456,7 @@ def run_uq(args, rank, world, dist):
     # consecutive linears of a decode step read fixed weights: let each launch stream its weights
     # while the previous one drains (uq_set_launch_overlap)
     uq.set_launch_overlap(not args.no_overlap)
-    step = Step(recs, fmt, group, M, dev, stream, seed=777 + rank).capture()
+    step = Step(recs, fmt, group, M, dev, stream, seed=777 + rank, gated=not args.no_gated).capture()
 
     step.replay(args.warmup)
     torch.cuda.synchronize()
@@ -458,14 +502,15 @@ def run_uq(args, rank, world, dist):
     e2e_ms = e0.elapsed_time(e1)
 
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], dist, dev)
-    info = dict(bytes=step.bytes, flops=step.flops, linears=len(recs), launches=step.launches(),
+    info = dict(bytes=step.bytes, flops=step.flops, linears=len(recs), ops=len(step.ops), launches=step.launches(),
+                gated=any(op["kind"] == "gated" for op in step.ops),
                 width=len(step.side) + 1, h2d=step.xbuf.numel() * 2, d2h=step.ybuf.numel() * 2,
                 shapes=sorted({(r["N"], r["K"]) for r in recs}), layers=len(recs) // len(spec["linears"]))
     sweep = None
     if world == 1 and not args.no_sweep:
         del step, recs
         torch.cuda.empty_cache()
-        sweep = run_sweep(dev, stream, *measured_peaks()[:2])
+        sweep = run_sweep(dev, stream, *measured_peaks()[:2], gated=not args.no_gated)
     if rank != 0:
         return
     out = report(args, spec, M, world, ms, e2e_ms, clocks, info, sweep)
@@ -483,7 +528,7 @@ def report(args, spec, M, world, ms, e2e_ms, clocks, info, sweep):
     achieved = info["bytes"] / step_s / 1e9
     t_roof = roofline_time_s(info["bytes"], info["flops"], hbm, tf)
     share = read_share(args.workload) if M == spec["m"] and not args.layers else None
-    traffic = read_traffic(args.workload, info["bytes"] / info["linears"]) if M == spec["m"] else None
+    traffic = read_traffic(args.workload, info["bytes"] / info["ops"]) if M == spec["m"] else None
     return {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
@@ -494,9 +539,11 @@ def report(args, spec, M, world, ms, e2e_ms, clocks, info, sweep):
                    "layers": info["layers"], "linears_per_step": info["linears"], "bytes_per_step": info["bytes"],
                    "flops_per_step": info["flops"], "parallelism": f"replicas x{world}",
                    "l2": "no flush: packed weights per step exceed L2 (%.2f GB)" % (info["bytes"] / 1e9),
+                   "ops_per_step": info["ops"],
                    "launch": "one CUDA graph per step" + (
-                       "; linears reading the same input (q, k, v; gate, up) on parallel branches"
-                       if info["width"] > 1 else ""),
+                       "; ops reading the same input (q, k, v) on parallel branches" if info["width"] > 1 else "")
+                   + ("; each layer's gate and up as one fused uq_gemm_gated op (h = silu(x Wg^T) * (x Wu^T))"
+                      if info["gated"] else ""),
                    "launch_overlap": not args.no_overlap},
         "tflops": round(info["flops"] * world / step_s / 1e12, 4),
         "gpu_launches": info["launches"] * args.steps,
@@ -637,6 +684,7 @@ def main():
     ap.add_argument("--no-sweep", action="store_true", help="leave the sweep workloads out of the line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-overlap", action="store_true", help="launch without programmatic dependent launch")
+    ap.add_argument("--no-gated", action="store_true", help="gate and up as two separate uq_gemm launches")
     ap.add_argument("--oracle-leg", default=None, help=argparse.SUPPRESS)
     ap.add_argument("--oracle-seconds", type=float, default=10.0, help=argparse.SUPPRESS)
     ap.add_argument("--oracle-rows", type=int, default=512, help=argparse.SUPPRESS)

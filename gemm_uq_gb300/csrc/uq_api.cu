@@ -207,6 +207,42 @@ uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const 
 }
 
 
+// the gated projection for Mb <= 8 rows of x in one mma-GEMV launch (plus the second pass when the
+// work split shares row blocks between CTAs): gate and up row blocks interleaved in one work list
+uq_status run_gemv_gated(const uint16_t* x, const void* wg, const void* sg, const void* zg, const void* wu,
+                         const void* su, const void* zu, uint16_t* h, int Mb, int N, int K, int ldx, int ldy,
+                         int group, int fmt, cudaStream_t st, const DeviceState& ds, int dev) {
+    const uq::Layout L(N, K, fmt);
+    if (uq::gemv_smem_bytes(fmt, K, group, Mb) > 227 * 1024)
+        return fail(UQ_ERR_UNSUPPORTED, "K=%d is too long for the GEMV's shared-memory x-sum table at M=%d", K, Mb);
+    const long long T = 2LL * L.NB * L.KB;
+    long long P = (long long)ds.sms * uq::gemv_ctas_per_sm(fmt) * uq::gemv_warps(fmt);
+    if (P > T) P = T;
+    Workspace* ws = nullptr;
+    uq_status s = workspace(dev, st, uq::gemv_partials_floats(fmt, T, (int)P, Mb) * sizeof(float),
+                            (size_t)L.NB * sizeof(unsigned int), &ws);
+    if (s != UQ_OK) return s;
+    uq::GemvArgs a = {};
+    a.x = x;
+    a.wq = static_cast<const uint8_t*>(wg);
+    a.scales = static_cast<const uint8_t*>(sg);
+    a.zc = static_cast<const uint8_t*>(zg);
+    a.wq2 = static_cast<const uint8_t*>(wu);
+    a.scales2 = static_cast<const uint8_t*>(su);
+    a.zc2 = static_cast<const uint8_t*>(zu);
+    a.gated = 1;
+    a.y = h;
+    a.M = Mb; a.N = N; a.K = K; a.group = group; a.ldx = ldx; a.ldy = ldy;
+    a.NB = 2 * L.NB; a.KB = L.KB; a.T = T; a.P = (int)P;
+    a.partials = ws->partials;
+    a.tickets = ws->tickets;
+    a.fault = ds.words;
+    const int grid = uq::gemv_grid(a, fmt, ds.sms);
+    cudaError_t e = uq::launch_gemv(fmt, a, grid, st);
+    if (e != cudaSuccess) return cuda_fail(e, "gated GEMV launch");
+    return UQ_OK;
+}
+
 // one tensor-core launch for 16 <= Mb <= 64 rows of x
 uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const void* zc, uint16_t* y, int Mb, int N,
                  int K, int ldx, int ldy, int group, int fmt, cudaStream_t st, const DeviceState& ds, int dev,
@@ -414,6 +450,16 @@ uq_status uq_gemm_gated(const uint16_t* x, const void* wq_gate, const void* scal
     if ((s = device_state(&ds, &dev)) != UQ_OK) return s;
     const bool tc = M >= 16 && uq::tc_supported(fmt, N, K);
     const int block = tc ? 64 : 8;
+    if (!tc && uq::gemv_is_mma(fmt)) {
+        // one launch per block of 8 rows: the mma GEMV over the gate and up weights together
+        for (int m0 = 0; m0 < M; m0 += 8) {
+            const int mb = (M - m0) < 8 ? (M - m0) : 8;
+            s = run_gemv_gated(x + (long long)m0 * K, wq_gate, scales_gate, zc_gate, wq_up, scales_up, zc_up,
+                               h + (long long)m0 * N, mb, N, K, K, N, group, fmt, st, *ds, dev);
+            if (s != UQ_OK) return s;
+        }
+        return UQ_OK;
+    }
     const int rows = M < block ? M : block;
     float* g32 = nullptr;
     {
@@ -448,8 +494,27 @@ uq_status uq_gemm_gated(const uint16_t* x, const void* wq_gate, const void* scal
 
 uq_status uq_gemm_gated_kernel_count(int M, int N, int K, int group, uq_fmt fmt, int* count) {
     uq_status s = uq_gemm_kernel_count(M, N, K, group, fmt, count);
-    if (s != UQ_OK || M == 0 || N == 0) return s;
-    if (K > 0) *count *= 2;                                 // the gate pass and the up pass
+    if (s != UQ_OK || M == 0 || N == 0 || K == 0) return s;
+    if ((M >= 16 && uq::tc_supported(fmt, N, K)) || !uq::gemv_is_mma(fmt)) {
+        *count *= 2;                                        // the gate pass and the up pass
+        return UQ_OK;
+    }
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess || sms < 1) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice, "SM count");
+    const uq::Layout L(N, K, fmt);
+    int n = 0;
+    for (int m0 = 0; m0 < M; m0 += 8) {                     // per block of 8 rows: one launch, + the second pass
+        uq::GemvArgs a = {};
+        a.M = (M - m0) < 8 ? (M - m0) : 8; a.N = N; a.K = K; a.group = group;
+        a.gated = 1; a.NB = 2 * L.NB; a.KB = L.KB; a.T = (long long)a.NB * L.KB;
+        const long long P = (long long)sms * uq::gemv_ctas_per_sm(fmt) * uq::gemv_warps(fmt);
+        a.P = (int)(P > a.T ? a.T : P);
+        uq::gemv_grid(a, fmt, sms);
+        n += 1 + (a.cta_rows ? 0 : 1);
+    }
+    *count = n;
     return UQ_OK;
 }
 

@@ -18,13 +18,16 @@ int gemv_grid(GemvArgs& a, int fmt, int sms) {
     // Whole row blocks per CTA need no second pass; take them when no warp gets more tiles than
     // under the stream-K split and either the busiest CTA streams at most ~6 % more bytes than the
     // average one (bandwidth-bound shapes) or no warp has more than one tile (latency-bound ones).
+    // (gated: the units CTAs own are gate/up pairs of row blocks)
     const int W = gemv_warps(fmt);
+    const int WU = a.gated ? 2 : 1;
+    const int NBU = a.NB / WU;
     const int slots = sms * MMA_CTAS_PER_SM;                           // CTAs resident at once
-    const int G = a.NB < slots ? a.NB : slots;
-    const long long rbs = (a.NB + G - 1) / G;
-    const long long per_warp_rows = (rbs * a.KB + W - 1) / W;
+    const int G = NBU < slots ? NBU : slots;
+    const long long rbs = (NBU + G - 1) / G;
+    const long long per_warp_rows = (rbs * WU * a.KB + W - 1) / W;
     const long long per_warp_split = (a.T + a.P - 1) / a.P;
-    const bool even = rbs * G * 100 <= (long long)a.NB * 106;
+    const bool even = rbs * G * 100 <= (long long)NBU * 106;
     if (G > 0 && per_warp_rows <= MMA_TPW && per_warp_rows <= per_warp_split && (even || per_warp_rows <= 1)) {
         a.cta_rows = 1;
         return G;
@@ -43,26 +46,34 @@ size_t gemv_partials_floats(int fmt, long long T, int P, int M) {
 // results are bit-reproducible).  Launched right after the GEMV with programmatic stream
 // serialization: it becomes resident early and its griddepcontrol.wait returns once the GEMV grid
 // has finished and its stores are visible, so the GEMV itself needs no fence or ticket.
+// Gated (a.gated): work row block 2j is gate row block j, 2j + 1 the up one; h = silu(g) * u.
 __global__ void __launch_bounds__(256) gemv_split_reduce(const GemvArgs a) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int M = a.M, KB = a.KB, RM = RB * M;
-    const long long total = (long long)a.NB * RM;
+    const int WU = a.gated ? 2 : 1;
+    const long long total = (long long)(a.NB / WU) * RM;
     const long long kstride = (long long)a.NB * RM;                 // floats between k tiles
     for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
          e += (long long)gridDim.x * blockDim.x) {
         const int nb = (int)(e / RM), rm = (int)(e % RM);           // rm = r * M + m
         const int n = nb * RB + rm / M, m = rm % M;
         if (n >= a.N) continue;
-        const float* p = a.partials + e;                            // k tile 0 of (nb, r, m)
+        const float* p = a.partials + (long long)nb * WU * RM + rm; // k tile 0 of (work row block, r, m)
         float sum = 0.f;
         for (int kb = 0; kb < KB; ++kb) sum += p[kb * kstride];
-        store_out(a, m, n, sum);
+        if (a.gated) {
+            float usum = 0.f;
+            for (int kb = 0; kb < KB; ++kb) usum += p[kb * kstride + RM];
+            a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(silu_mul(sum, usum)));
+        } else {
+            store_out(a, m, n, sum);
+        }
     }
 }
 
 static cudaError_t launch_split_reduce(const GemvArgs& a, int sms, cudaStream_t st) {
-    const long long total = (long long)a.NB * RB * a.M;
+    const long long total = (long long)(a.gated ? a.NB / 2 : a.NB) * RB * a.M;
     long long blocks = (total + 255) / 256;
     if (blocks > 4LL * sms) blocks = 4LL * sms;
     if (blocks < 1) blocks = 1;

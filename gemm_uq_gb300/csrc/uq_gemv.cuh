@@ -168,6 +168,13 @@ struct MetaConst {
     bool aligned;     // every tile row's scale slice is 16-byte aligned and a multiple of 16 bytes
 };
 
+// One weight's packed codes and metadata (the gated kernel reads two: gate and up).
+struct GemvSrc {
+    const uint8_t* wq;
+    const uint8_t* scales;
+    const uint8_t* zc;
+};
+
 // Issue the copies of tile t into stage buffer `st` (all lanes take part).  Either the codes come
 // as one bulk copy counted on `bar` (transaction bytes) and the metadata copies arrive on `bar`
 // too (33 arrivals in all: one per lane when its copies land, and the codes' expect_tx), or, with
@@ -176,7 +183,7 @@ struct MetaConst {
 // copies keep more of the tile stream in flight than one 8 KB bulk copy per tile: the copy engine
 // takes bulk copies one after another, at well under an SM's share of HBM bandwidth at this size.
 template <int FMT, bool GROUP = false>
-__device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, const MetaConst& mc, int nb, int kb,
+__device__ __forceinline__ void issue_tile(const GemvArgs& a, const GemvSrc& w, const Layout& L, const MetaConst& mc, int nb, int kb,
                                            uint8_t* st, uint64_t* bar, int lane) {
     using F = GemvFmt<FMT>;
     const int n0 = nb * RB;
@@ -189,7 +196,7 @@ __device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, c
         if (recs > F::KT / 256) recs = F::KT / 256;
         for (int e = lane; e < rows * recs; e += 32) {
             const int r = e / recs, j = e % recs;
-            cp_async16(md + r * F::MW + 4 * j, a.scales + ((long long)(n0 + r) * mc.S4 + sb0 + j) * 16);
+            cp_async16(md + r * F::MW + 4 * j, w.scales + ((long long)(n0 + r) * mc.S4 + sb0 + j) * 16);
         }
     } else if (mc.aligned) {
         // scale slices of GT halves (16-byte multiples, 16-byte aligned): 16-byte copies; INT4
@@ -201,12 +208,12 @@ __device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, c
             const int r = e / per, j = e % per;
             const long long n = n0 + r;
             if (j < sv) {
-                cp_async16(md + r * F::MW + 4 * j, a.scales + (n * mc.G + (long long)kb * mc.GT) * 2 + 16 * j);
+                cp_async16(md + r * F::MW + 4 * j, w.scales + (n * mc.G + (long long)kb * mc.GT) * 2 + 16 * j);
             } else if constexpr (FMT == UQ_INT4_ASYM) {
                 cp_async4(md + r * F::MW + F::SW + (j - sv),
-                          a.zc + n * mc.ZB + (long long)kb * (mc.GT >> 1) + 4 * (j - sv));
+                          w.zc + n * mc.ZB + (long long)kb * (mc.GT >> 1) + 4 * (j - sv));
             } else if constexpr (FMT == UQ_INT2_ASYM) {
-                cp_async16(md + r * F::MW + F::SW + 4 * (j - sv), a.zc + (n * mc.G + (long long)kb * mc.GT) * 2 + 16 * (j - sv));
+                cp_async16(md + r * F::MW + F::SW + 4 * (j - sv), w.zc + (n * mc.G + (long long)kb * mc.GT) * 2 + 16 * (j - sv));
             }
         }
     } else {
@@ -217,19 +224,19 @@ __device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, c
             const int r = e / F::MW, j = e % F::MW;
             const long long n = n0 + r;
             if (j < F::SW) {
-                stage_words(md + r * F::MW, a.scales, (n * mc.G + (long long)kb * mc.GT) * 2, gc * 2, send, j);
+                stage_words(md + r * F::MW, w.scales, (n * mc.G + (long long)kb * mc.GT) * 2, gc * 2, send, j);
             } else if constexpr (FMT == UQ_INT4_ASYM) {
-                stage_words(md + r * F::MW + F::SW, a.zc, n * mc.ZB + (long long)kb * (mc.GT >> 1), (gc + 1) >> 1,
+                stage_words(md + r * F::MW + F::SW, w.zc, n * mc.ZB + (long long)kb * (mc.GT >> 1), (gc + 1) >> 1,
                             (long long)a.N * mc.ZB, j - F::SW);
             } else if constexpr (FMT == UQ_INT2_ASYM) {
-                stage_words(md + r * F::MW + F::SW, a.zc, (n * mc.G + (long long)kb * mc.GT) * 2, gc * 2, send,
+                stage_words(md + r * F::MW + F::SW, w.zc, (n * mc.G + (long long)kb * mc.GT) * 2, gc * 2, send,
                             j - F::SW);
             }
         }
     }
     if constexpr (GROUP) {
         const int bytes = (int)L.tile_bytes(kb);
-        const uint8_t* src = a.wq + L.tile_offset(nb, kb);
+        const uint8_t* src = w.wq + L.tile_offset(nb, kb);
         for (int off = lane * 16; off < bytes; off += 512) cp_async16(st + off, src + off);
         cp_async_commit_group();
         (void)bar;
@@ -240,7 +247,7 @@ __device__ __forceinline__ void issue_tile(const GemvArgs& a, const Layout& L, c
             const uint32_t bytes = (uint32_t)L.tile_bytes(kb);
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(bar, bytes);
-            bulk_g2s(st, a.wq + L.tile_offset(nb, kb), bytes, bar);
+            bulk_g2s(st, w.wq + L.tile_offset(nb, kb), bytes, bar);
         }
     }
 }
@@ -347,7 +354,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
         __syncwarp();
         int inb = (int)(t0 / L.KB), ikb = (int)(t0 % L.KB);
         for (int s = 0; s < S && t0 + s < t1; ++s) {
-            issue_tile<FMT>(a, L, mc, inb, ikb, ring + s * F::STAGE_BYTES, &bars[s], lane);
+            issue_tile<FMT>(a, GemvSrc{a.wq, a.scales, a.zc}, L, mc, inb, ikb, ring + s * F::STAGE_BYTES, &bars[s], lane);
             if (++ikb == L.KB) { ikb = 0; ++inb; }
         }
     }
@@ -507,7 +514,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
         }
         __syncwarp();
         if (t + S < t1) {
-            issue_tile<FMT>(a, L, mc, pnb, pkb, st, &bars[s], lane);
+            issue_tile<FMT>(a, GemvSrc{a.wq, a.scales, a.zc}, L, mc, pnb, pkb, st, &bars[s], lane);
             if (++pkb == L.KB) { pkb = 0; ++pnb; }
         }
 
@@ -616,7 +623,7 @@ template <int FMT> struct MmaCfg {
     static constexpr int STAGES = 2;                               // tiles in flight per worker
 };
 constexpr int MMA_CTAS_PER_SM = 2;
-constexpr int MMA_TPW = 4;        // tiles per warp at most when the CTA owns whole row blocks
+constexpr int MMA_TPW = 6;        // tiles per warp at most when the CTA owns whole row blocks
 
 // bytes per row of x in shared memory: 32 bytes of padding put the four rows a half-warp's 8-byte
 // B-fragment loads touch into different banks
@@ -667,7 +674,10 @@ __host__ __device__ inline int gemv_mma_xmode(int fmt, int K, int group, int M) 
     return MMA_X_GLOBAL;
 }
 
-template <int FMT, int GB, int XM>
+// GATED: the gated projection in one launch.  The work list interleaves the gate and up weights' row
+// blocks (work row block 2j = gate row block j, 2j + 1 = up row block j), every CTA owns whole pairs,
+// and the per-row reduction forms h = silu(g) * u (or the second pass does, for the stream-K split).
+template <int FMT, int GB, int XM, bool GATED>
 __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv_mma_kernel(const GemvArgs a) {
     using F = GemvFmt<FMT>;
     constexpr int KT = F::KT, S = MmaCfg<FMT>::STAGES, W = MmaCfg<FMT>::WARPS;
@@ -699,9 +709,11 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
     // R * KB tiles evenly; otherwise worker w = CTA + grid * warp (strided, so a small matrix still
     // spreads over every SM) owns an equal share of all NB * KB tiles.  Tile i -> (k tile i / R,
     // row block i % R) with R = NB for the whole matrix.
+    constexpr int WU = GATED ? 2 : 1;                              // work row blocks per weight row block
     const bool cta_rows = a.cta_rows != 0;
-    const int rb0 = cta_rows ? (int)((long long)blockIdx.x * a.NB / gridDim.x) : 0;
-    const int R = cta_rows ? (int)((long long)(blockIdx.x + 1) * a.NB / gridDim.x) - rb0 : a.NB;
+    const int NBU = a.NB / WU;                                      // pairs (gated) or row blocks
+    const int rb0 = cta_rows ? WU * (int)((long long)blockIdx.x * NBU / gridDim.x) : 0;
+    const int R = cta_rows ? WU * (int)((long long)(blockIdx.x + 1) * NBU / gridDim.x) - rb0 : a.NB;
     const unsigned Tc = (unsigned)(R * L.KB);                       // the CTA's tiles (cta_rows; small)
     const int w = cta_rows ? warp : (int)(blockIdx.x + gridDim.x * warp);
     const bool has_work = cta_rows ? true : w < a.P;
@@ -751,10 +763,13 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
     }
     __syncwarp();
     int issued = 0;                                                 // tiles requested so far
+    // the weight and weight row block of a work row block
+    const GemvSrc src_gate{a.wq, a.scales, a.zc}, src_up{a.wq2, a.scales2, a.zc2};
     auto issue_next = [&]() {
         const long long i = t0 + issued;
-        issue_tile<FMT, true>(a, L, mc, nb_of(i), kb_of(i), ring + (issued % S) * F::STAGE_BYTES, &bars[issued % S],
-                              lane);
+        const int nbw = nb_of(i);
+        issue_tile<FMT, true>(a, (GATED && (nbw & 1)) ? src_up : src_gate, L, mc, GATED ? nbw >> 1 : nbw, kb_of(i),
+                              ring + (issued % S) * F::STAGE_BYTES, &bars[issued % S], lane);
         ++issued;
     };
     // Only the first tile before the sums of x of the first run: at the start every warp of the
@@ -797,7 +812,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
 
     for (int li = 0; li < ntl; ++li) {
         const long long i = t0 + li;
-        const int kb = kb_of(i), nb = nb_of(i);
+        const int kb = kb_of(i), nb = GATED ? nb_of(i) >> 1 : nb_of(i);
         const int n0 = nb * RB;
         const int gi0 = kb * GPT;
         const int ng = (G_all - gi0) < GPT ? (G_all - gi0) : GPT;   // groups of the tile inside K
@@ -1011,10 +1026,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
     if (!cta_rows) return;
     // cta_rows: each row's sum over the k tiles, in k order, from the warps that computed them
     __syncthreads();
-    for (int e = threadIdx.x; e < R * RB * M; e += blockDim.x) {
-        const int rbi = e / (RB * M), rm = e % (RB * M), r = rm / M, m = rm % M;
-        const int n = (rb0 + rbi) * RB + r;
-        if (n >= a.N) continue;
+    auto row_sum = [&](int rbi, int r, int m) {
         float sum = 0.f;
         for (int kb = 0; kb < L.KB; ++kb) {
             const unsigned ti = (unsigned)(kb * R + rbi);
@@ -1022,7 +1034,18 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
             const unsigned l2 = ti - w2 * Tc / W;
             sum += cpart[((w2 * MMA_TPW + l2) * RB + r) * 8 + m];
         }
-        store_out(a, m, n, sum);
+        return sum;
+    };
+    for (int e = threadIdx.x; e < (R / WU) * RB * M; e += blockDim.x) {
+        const int rbi = e / (RB * M), rm = e % (RB * M), r = rm / M, m = rm % M;
+        const int n = (rb0 / WU + rbi) * RB + r;
+        if (n >= a.N) continue;
+        if constexpr (GATED) {
+            const float gsum = row_sum(2 * rbi, r, m), usum = row_sum(2 * rbi + 1, r, m);
+            a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(silu_mul(gsum, usum)));
+        } else {
+            store_out(a, m, n, row_sum(rbi, r, m));
+        }
     }
 }
 
@@ -1085,7 +1108,7 @@ cudaError_t launch_xs(const GemvArgs& a, int grid, cudaStream_t st) {
 }  // namespace gemv_detail
 
 namespace gemv_detail {
-template <int FMT, int GB, int XM>
+template <int FMT, int GB, int XM, bool GATED>
 cudaError_t launch_mma(const GemvArgs& a, int grid, cudaStream_t st) {
     static bool configured[64] = {};
     const size_t smem = gemv_mma_smem_plan(FMT, a.K, a.group, a.M, XM).total;
@@ -1094,7 +1117,7 @@ cudaError_t launch_mma(const GemvArgs& a, int grid, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(gemv_mma_kernel<FMT, GB, XM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(gemv_mma_kernel<FMT, GB, XM, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  227 * 1024);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
@@ -1113,20 +1136,24 @@ cudaError_t launch_mma(const GemvArgs& a, int grid, cudaStream_t st) {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, gemv_mma_kernel<FMT, GB, XM>, a2);
+        e = cudaLaunchKernelEx(&cfg, gemv_mma_kernel<FMT, GB, XM, GATED>, a2);
         if (e != cudaSuccess) return e;
     } else {
-        gemv_mma_kernel<FMT, GB, XM><<<grid, threads, smem, st>>>(a2);
+        gemv_mma_kernel<FMT, GB, XM, GATED><<<grid, threads, smem, st>>>(a2);
     }
     return cudaGetLastError();
 }
+template <int FMT, int GB, bool GATED>
+cudaError_t launch_mma_xg(const GemvArgs& a, int grid, cudaStream_t st) {
+    switch (gemv_mma_xmode(FMT, a.K, a.group, a.M)) {
+        case MMA_X_SLICE: return launch_mma<FMT, GB, MMA_X_SLICE, GATED>(a, grid, st);
+        case MMA_X_WHOLE: return launch_mma<FMT, GB, MMA_X_WHOLE, GATED>(a, grid, st);
+        default: return launch_mma<FMT, GB, MMA_X_GLOBAL, GATED>(a, grid, st);
+    }
+}
 template <int FMT, int GB>
 cudaError_t launch_mma_xs(const GemvArgs& a, int grid, cudaStream_t st) {
-    switch (gemv_mma_xmode(FMT, a.K, a.group, a.M)) {
-        case MMA_X_SLICE: return launch_mma<FMT, GB, MMA_X_SLICE>(a, grid, st);
-        case MMA_X_WHOLE: return launch_mma<FMT, GB, MMA_X_WHOLE>(a, grid, st);
-        default: return launch_mma<FMT, GB, MMA_X_GLOBAL>(a, grid, st);
-    }
+    return a.gated ? launch_mma_xg<FMT, GB, true>(a, grid, st) : launch_mma_xg<FMT, GB, false>(a, grid, st);
 }
 }  // namespace gemv_detail
 

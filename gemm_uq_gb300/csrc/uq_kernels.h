@@ -46,6 +46,11 @@ struct GemvArgs {
                               // no second pass); 0 = workers split row blocks anywhere (second pass)
     float* out32;             // gate pass of the gated projection: fp32 results [M][ldy] instead of y
     const float* gate32;      // up pass: y = bf16(silu(gate32) * result), gate32 [M][ldy] fp32
+    int gated;                // mma GEMV only: the gated projection in one launch; (wq, scales, zc) are the
+                              // gate weight, (wq2, scales2, zc2) the up weight, NB and T count both
+    const uint8_t* wq2;
+    const uint8_t* scales2;
+    const uint8_t* zc2;
 };
 constexpr int GEMV_WARPS = 4;     // worker warps per CTA
 // formats whose GEMV runs on mma.sync (the others on CUDA-core FMAs)
@@ -86,6 +91,11 @@ struct TcArgs {
 // The one place every kernel writes an output element (row m of x, output column n): bf16 y; or, for
 // the gated projection, fp32 g (the gate pass) or bf16 silu(g) * u (the up pass; silu(g) = g / (1 + e^-g)
 // in fp32, the product in fp32, one rounding to bf16).
+// silu(g) * u in fp32 (silu(g) = g / (1 + e^-g)), the gated projection's epilogue
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
 template <class Args>
 __device__ __forceinline__ void store_out(const Args& a, int m, int n, float v) {
     const long long idx = (long long)m * a.ldy + n;
@@ -93,10 +103,7 @@ __device__ __forceinline__ void store_out(const Args& a, int m, int n, float v) 
         a.out32[idx] = v;
         return;
     }
-    if (a.gate32) {
-        const float g = a.gate32[idx];
-        v = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), v);
-    }
+    if (a.gate32) v = silu_mul(a.gate32[idx], v);
     a.y[idx] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 bool tc_supported(int fmt, int N, int K);

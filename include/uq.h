@@ -155,9 +155,13 @@ uq_status uq_gemm(const uint16_t* x, const void* wq, const void* scales,
  *   two weights of the same N, K, group and format, each as uq_gemm takes them; h (device) bf16
  *   [M][N], written.  M == 0 or N == 0 is a no-op; K == 0 writes zeros.
  * Paths, per block of rows of x (8 on the GEMV, 64 on the tensor-core path, routed as uq_gemm):
- * the gate projection into fp32 library scratch, then the up projection, whose epilogue reads g and
- * writes h; uq_gemm_gated_kernel_count gives the launches.  Scratch, errors and stream capture as
- * uq_gemm (the fp32 gate scratch, rows x N floats, is part of the per-stream workspace).
+ * INT4_SYM, INT4_ASYM, INT2_ASYM and K4 with M <= 15 run one mma-GEMV launch over both weights (gate and
+ * up row blocks interleaved, each CTA owning whole gate/up pairs, h formed in its per-row reduction),
+ * plus the second pass when the work split shares row blocks between CTAs; INT8_SYM and NF4, and the
+ * tensor-core path (M >= 16), run the gate projection into fp32 library scratch and then the up
+ * projection, whose epilogue reads g and writes h.  uq_gemm_gated_kernel_count gives the launches.
+ * Scratch, errors and stream capture as uq_gemm (the fp32 gate scratch, rows x N floats, is part of
+ * the per-stream workspace).
  */
 uq_status uq_gemm_gated(const uint16_t* x, const void* wq_gate, const void* scales_gate, const void* zc_gate,
                         const void* wq_up, const void* scales_up, const void* zc_up, uint16_t* h,

@@ -80,7 +80,12 @@ def test_gated_edge_cases():
 
 
 def test_gated_kernel_count():
-    assert uq.gemm_gated_kernel_count(1, 14336, 4096, 128, "INT4_ASYM") == 2
+    # decode (mma GEMV formats, M <= 8): gate and up in one launch, plus the second pass when the work
+    # split shares row blocks; INT8 / NF4 and the tensor-core path: a gate pass and an up pass
+    assert uq.gemm_gated_kernel_count(1, 14336, 4096, 128, "INT4_ASYM") == 1
+    assert uq.gemm_gated_kernel_count(1, 28672, 8192, 256, "K4") == 2
+    assert uq.gemm_gated_kernel_count(9, 14336, 4096, 128, "INT4_ASYM") == 2
+    assert uq.gemm_gated_kernel_count(1, 8192, 8192, 128, "INT8_SYM") == 2
     assert uq.gemm_gated_kernel_count(16, 14336, 4096, 128, "INT4_ASYM") == 2
     assert uq.gemm_gated_kernel_count(0, 14336, 4096, 128, "INT4_ASYM") == 0
 
