@@ -251,7 +251,7 @@ uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const vo
     size_t smem = 0;
     if (uq::tc_plan(fmt, mpad, group, &smem) != 0)
         return fail(UQ_ERR_UNSUPPORTED, "no tensor-core plan for M=%d", Mb);
-    const int kc = (fmt == UQ_INT8_SYM) ? 128 : 256;
+    const int kc = (fmt == UQ_INT8_SYM || fmt == UQ_NF4) ? 128 : 256;   // codes per row per unit
     const int nblk = (N + 127) / 128;
     const int CH = K / kc;
     const long long U = (long long)nblk * CH;

@@ -37,7 +37,6 @@ namespace uq {
 namespace {
 
 constexpr int TC_ROWS = 128;
-constexpr int TC_STAGE_CODES = TC_ROWS * 128;     // bytes of codes per stage
 constexpr int TMEM_COLS = 512;
 constexpr int TC_BAR_BYTES = 2048;                 // barriers and flags after the stages
 
@@ -155,8 +154,15 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
 template <int FMT> struct TcFmt {
-    static constexpr int KC = (FMT == UQ_INT8_SYM) ? 128 : 256;   // codes per row per unit
-    static constexpr int ACOLS = KC / 2;                           // tensor-memory columns of A per unit
+    static constexpr int BITS = fmt_bits(FMT);
+    static constexpr int KC = (FMT == UQ_INT8_SYM || FMT == UQ_NF4) ? 128 : 256;   // codes per row per unit
+    // A planes: NF4's non-integer codebook value c[q] is written as two bf16 planes, hi = bf16(c[q]) and
+    // lo = bf16(c[q] - hi), multiplied into the same accumulator; the other formats' A is an exact integer
+    static constexpr int PLANES = (FMT == UQ_NF4) ? 2 : 1;
+    static constexpr int ACOLS = KC / 2 * PLANES;                  // tensor-memory columns of A per unit
+    static constexpr int WBYTES = 16 * KC * BITS / 8;              // code bytes of one 16-row block per unit
+    static constexpr int CODES = 8 * WBYTES;                       // code bytes per unit (128 rows)
+    static constexpr int CPU = KC / fmt_kc(FMT);                   // 512-byte chunks per 16-row block per unit
     // staged scale words per row and unit: the unit's KC / (16 GB) fp16 scales plus one half for a
     // start that is not word aligned (K4: its 16-byte super-block record)
     template <int GB> static constexpr int swords() { return FMT == UQ_K4 ? 4 : (KC / (16 * GB) + 2) / 2; }
@@ -180,20 +186,22 @@ template <int FMT, int MPAD, int GB> struct TcPlan {
     static constexpr int XB = KC * MPAD * 2;                       // x bytes per unit (MPAD rows x KC k)
     static constexpr int XS = 4;                                   // x stages
     static constexpr int EPI_RING = TC_EPI_RING * 32 * tc_epi_warps(MPAD) * TcFmt<FMT>::template swords<GB>() * 4;
-    static constexpr int DQ_SLOT = (FMT == UQ_INT4_ASYM) ? TC_DQ_WARPS * 16 * 2 * 4 : 0;   // zero words per unit
+    // zero-point words staged per row and unit: INT4_ASYM two (its nibbles), INT2_ASYM the unit's fp16 zeros
+    static constexpr int ZW = FMT == UQ_INT4_ASYM ? 2 : (FMT == UQ_INT2_ASYM ? (KC / (16 * GB) + 2) / 2 : 0);
+    static constexpr int DQ_SLOT = TC_DQ_WARPS * 16 * ZW * 4;     // zero words per unit
     static constexpr int BUDGET = 227 * 1024 - 1024 - TC_BAR_BYTES - EPI_RING - XS * XB;
-    static constexpr int CS_FIT = BUDGET / (TC_STAGE_CODES + DQ_SLOT);
+    static constexpr int CS_FIT = BUDGET / (TcFmt<FMT>::CODES + DQ_SLOT);
     static constexpr int CS = CS_FIT > 8 ? 8 : (CS_FIT > 4 && XB >= 24 * 1024 ? 4 : CS_FIT);   // code stages
     static constexpr int CD = CS - 1;                              // code prefetch depth (units)
-    static constexpr int DS_FIT = (TMEM_COLS - 2 * (KC / 2)) / MPAD;
+    static constexpr int DS_FIT = (TMEM_COLS - 2 * TcFmt<FMT>::ACOLS) / MPAD;
     static constexpr int DS = DS_FIT > 8 ? 8 : DS_FIT;           // accumulator slots
     // A buffers: at least two, more where tensor memory has room beside the accumulator slots (the
     // dequant warps then run further ahead of the MMAs that free a buffer)
-    static constexpr int NA_FIT = (TMEM_COLS - DS * MPAD) / (KC / 2);
+    static constexpr int NA_FIT = (TMEM_COLS - DS * MPAD) / TcFmt<FMT>::ACOLS;
     static constexpr int NA = NA_FIT > 4 ? 4 : NA_FIT;
     static_assert(NA >= 2, "two A buffers at least");
     static constexpr int CODE_OFF = XS * XB;
-    static constexpr int BAR_OFF = CODE_OFF + CS * TC_STAGE_CODES;
+    static constexpr int BAR_OFF = CODE_OFF + CS * TcFmt<FMT>::CODES;
     static constexpr int EPI_OFF = BAR_OFF + TC_BAR_BYTES;
     static constexpr int DQ_OFF = EPI_OFF + EPI_RING;
     static constexpr int SMEM = 1024 + DQ_OFF + CS * DQ_SLOT;      // + alignment slack
@@ -235,6 +243,7 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
     uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(ebar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_base_smem + 1);
     unsigned int* ticket_smem = reinterpret_cast<unsigned int*>(tmem_base_smem + 2);
+    uint32_t* nlut = reinterpret_cast<uint32_t*>(smem + PL::BAR_OFF + 1024);   // NF4: (hi | lo << 16) per code
     uint32_t* epi_ring = reinterpret_cast<uint32_t*>(smem + PL::EPI_OFF);   // [ring][256 threads][SWORDS]
     uint32_t* dq_ring = reinterpret_cast<uint32_t*>(smem + PL::DQ_OFF);     // [CS][8 warps][16][2]
 
@@ -253,6 +262,16 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
+    }
+    if constexpr (FMT == UQ_NF4) {
+        // the codebook value c[q] as hi = bf16(c[q]) and lo = bf16(c[q] - hi): hi + lo carries 16 significant
+        // bits of c[q] (relative error below 2^-16), so the MMAs multiply x by c[q] within that
+        if (threadIdx.x < 16) {
+            const float cq = reinterpret_cast<const float*>(a.zc)[threadIdx.x];
+            const __nv_bfloat16 hi = __float2bfloat16_rn(cq);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(cq - __bfloat162float(hi));
+            nlut[threadIdx.x] = (uint32_t)__bfloat16_as_ushort(hi) | ((uint32_t)__bfloat16_as_ushort(lo) << 16);
+        }
     }
     if (warp == 0) tmem_alloc(tmem_base_smem, TMEM_COLS);
     tc_fence_before();
@@ -339,6 +358,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                     const int kk = ks + t;
                     const uint64_t bdesc = bdesc0 + (uint64_t)((kk >> 2) * (MPAD * 8) + (kk & 3) * 2);
                     mma_ts_elect(dcol, acol0 + kk * 8, bdesc, IDESC, t > 0 ? 1u : 0u);
+                    if constexpr (TcFmt<FMT>::PLANES == 2)                 // NF4: the lo plane into the same sum
+                        mma_ts_elect(dcol, acol0 + KC / 2 + kk * 8, bdesc, IDESC, 1u);
                 }
                 tc_commit_elect(&dfull[slot]);
                 ks += KS;
@@ -357,29 +378,38 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
         const int rbl = 2 * quarter + hf;               // row block (16 rows) within the 128-row unit
         const int g = lane >> 2, c4 = lane & 3;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter + 16 * hf) << 16);
-        // Unit u's copies, CD units ahead, one cp.async group per unit: this warp's 2 KB of codes
-        // (16-row block rb * 8 + rbl, k tile c / 4, chunks (c % 4) * 4 .. + 3, contiguous in the
-        // fragment-order plane) into code stage (u - u0) % CS, and for INT4_ASYM the zero-point words
-        // of rows g and g + 8 (lanes c = 0, 1).
+        // Unit u's copies, CD units ahead, one cp.async group per unit: this warp's codes (16-row block
+        // rb * 8 + rbl, the unit's CPU 512-byte chunks, contiguous in the fragment-order plane) into code
+        // stage (u - u0) % CS, and the zero points of rows g and g + 8 (lanes c = 0, 1): INT4_ASYM's
+        // nibble bytes, INT2_ASYM's fp16 zeros.
+        constexpr int WB = TcFmt<FMT>::WBYTES, CPU = TcFmt<FMT>::CPU;
+        constexpr int ZW = PL::ZW;
         auto issue_codes = [&](long long u) {
             if (u < u1) {
                 const int rbc = (int)(u / a.CH), cc = (int)(u % a.CH);
                 const int cs = (int)((u - u0) % CS);
                 if (rbc * 8 + rbl < a.NB) {
-                    const uint8_t* src = a.wq + (long long)(rbc * 8 + rbl) * 16 * a.rowbytes + (long long)(cc >> 2) * 8192 +
-                                         (cc & 3) * 4 * 512;
-                    uint8_t* dst = cring + cs * TC_STAGE_CODES + rbl * 2048;
+                    const int ch0 = cc * CPU;                    // first chunk of the unit in the row block
+                    const uint8_t* src = a.wq + (long long)(rbc * 8 + rbl) * 16 * a.rowbytes +
+                                         (long long)(ch0 >> 4) * TILE_BYTES + (ch0 & 15) * CHUNK;
+                    uint8_t* dst = cring + cs * TcFmt<FMT>::CODES + rbl * WB;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) tc_cp_async16(dst + q * 512 + lane * 16, src + q * 512 + lane * 16);
+                    for (int q = 0; q < CPU; ++q) tc_cp_async16(dst + q * CHUNK + lane * 16, src + q * CHUNK + lane * 16);
                 }
-                if constexpr (FMT == UQ_INT4_ASYM) {
+                if constexpr (ZW > 0) {
                     if (c4 < 2) {
                         const int r = g + 8 * c4;
                         const long long n = (long long)rbc * TC_ROWS + rbl * 16 + r;
-                        const int Gn = a.K / G, ZB = (Gn + 1) >> 1;
-                        if (n < a.N)
-                            stage_span(dq_ring + cs * (TC_DQ_WARPS * 32) + (warp - 4) * 32 + r * 2, a.zc,
-                                       n * ZB + (long long)cc * (GPC >> 1), GPC >> 1, (long long)a.N * ZB);
+                        const int Gn = a.K / G;
+                        uint32_t* zdst = dq_ring + (cs * TC_DQ_WARPS + (warp - 4)) * 16 * ZW + r * ZW;
+                        if (n < a.N) {
+                            if constexpr (FMT == UQ_INT4_ASYM) {
+                                const int ZB = (Gn + 1) >> 1;
+                                stage_span(zdst, a.zc, n * ZB + (long long)cc * (GPC >> 1), GPC >> 1, (long long)a.N * ZB);
+                            } else {
+                                stage_span(zdst, a.zc, (n * Gn + (long long)cc * GPC) * 2, GPC * 2, (long long)a.N * Gn * 2);
+                            }
+                        }
                     }
                 }
             }
@@ -395,8 +425,8 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
             __syncwarp();                               // every lane is done with the stage refilled next
             const int cs = (int)((u - u0) % CS);
-            // subtrahend per group as a bf16 pair: 128 + z (INT4_ASYM), 128 + 8 (INT4_SYM), 128 (K4)
-            constexpr int ZG = (FMT == UQ_INT4_ASYM) ? 16 / GB : 1;   // groups per unit
+            // subtrahend per group as a bf16 pair: 128 + z (INT4_ASYM, INT2_ASYM), 128 + 8 (INT4_SYM), 128 (K4)
+            constexpr int ZG = (FMT == UQ_INT4_ASYM || FMT == UQ_INT2_ASYM) ? KC / (16 * GB) : 1;   // groups per unit
             uint32_t zlo[ZG], zhi[ZG];
 #pragma unroll
             for (int j = 0; j < ZG; ++j) zlo[j] = zhi[j] = (FMT == UQ_INT4_SYM) ? 0x43084308u : 0x43004300u;
@@ -409,21 +439,28 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                 cp_async_wait<CD>();                    // unit u's codes (and zero words) landed
                 __syncwarp();
             }
-            if constexpr (FMT == UQ_INT4_ASYM) {
-                const int Gn = a.K / G, ZB = (Gn + 1) >> 1;
-                const uint32_t* slot = dq_ring + cs * (TC_DQ_WARPS * 32) + (warp - 4) * 32;
+            if constexpr (ZW > 0) {
+                const int Gn = a.K / G;
+                const uint32_t* slot = dq_ring + (cs * TC_DQ_WARPS + (warp - 4)) * 16 * ZW;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const long long n = (long long)rb * TC_ROWS + rbl * 16 + g + 8 * h;
-                    uint32_t zb = 0;
-                    if (n < a.N) {
-                        const int o = (int)((n * ZB + (long long)c * (GPC >> 1)) & 3);
-                        const uint64_t w = (uint64_t)slot[(g + 8 * h) * 2] | ((uint64_t)slot[(g + 8 * h) * 2 + 1] << 32);
-                        zb = (uint32_t)(w >> (8 * o));
-                    }
+                    const uint32_t* zr = slot + (g + 8 * h) * ZW;
 #pragma unroll
                     for (int j = 0; j < ZG; ++j) {
-                        const uint32_t z = (zb >> (4 * j)) & 15u;
+                        uint32_t z = 0;
+                        if (n < a.N) {
+                            if constexpr (FMT == UQ_INT4_ASYM) {
+                                const int o = (int)((n * ((Gn + 1) >> 1) + (long long)c * (GPC >> 1)) & 3);
+                                const uint64_t w = (uint64_t)zr[0] | ((uint64_t)zr[1] << 32);
+                                z = (uint32_t)(w >> (8 * o + 4 * j)) & 15u;
+                            } else {
+                                // fp16 integer zero of group j: half (start parity) + j of the staged words
+                                const int hi = (int)(((n * Gn + (long long)c * GPC) & 1) + j);
+                                const uint16_t zh = (uint16_t)(zr[hi >> 1] >> (16 * (hi & 1)));
+                                z = (uint32_t)half_bits_f32(zh);
+                            }
+                        }
                         const uint32_t zz = 0x43004300u | z | (z << 16);
                         if (h == 0) zlo[j] = zz; else zhi[j] = zz;
                     }
@@ -433,13 +470,13 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) { *abort_flag = 1; break; }
             tc_fence_after();
-            const uint8_t* rbase = cring + cs * TC_STAGE_CODES + rbl * 2048 + lane * 16;
+            const uint8_t* rbase = cring + cs * TcFmt<FMT>::CODES + rbl * WB + lane * 16;
             const uint32_t acol = lane_addr + A_COL0 + ab * ACOLS;
             if constexpr (FMT == UQ_INT8_SYM) {
                 // chunk q = 32 k = blocks 2q, 2q + 1; word 2b + h = row g + 8h, k 4c .. 4c + 3 of block b
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 w4 = *reinterpret_cast<const uint4*>(rbase + q * 512);
+                for (int q = 0; q < CPU; ++q) {
+                    const uint4 w4 = *reinterpret_cast<const uint4*>(rbase + q * CHUNK);
                     const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
                     uint32_t v[8];
 #pragma unroll
@@ -456,12 +493,65 @@ tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const TcArgs a) {
                         }
                     tmem_st_16x256b_x2(acol + q * 16, v);
                 }
+            } else if constexpr (FMT == UQ_INT2_ASYM) {
+                // chunk q = 128 k = blocks 8q .. 8q + 7; word i holds blocks 2i (crumb pairs 0..3) and 2i + 1
+                // (pairs 4..7), pair 4bb + pp laid out as the 4-bit pairs pp (0/2 row g, 1/3 row g + 8)
+#pragma unroll
+                for (int q = 0; q < CPU; ++q) {
+                    const uint4 w4 = *reinterpret_cast<const uint4*>(rbase + q * CHUNK);
+                    const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                    for (int hs = 0; hs < 2; ++hs) {              // blocks 8q + 4hs .. + 3: one 16x256b x4 store
+                        uint32_t v[16];
+#pragma unroll
+                        for (int b4 = 0; b4 < 4; ++b4) {
+                            const int b = 4 * hs + b4;             // block within the chunk
+                            const uint32_t wd = wv[b >> 1];
+                            const int j = (8 * q + b) / GB;
+                            uint32_t p0, p1, p2, p3;
+                            if (b & 1) {
+                                p0 = crumb_pair_lop3<4>(wd); p1 = crumb_pair_lop3<5>(wd);
+                                p2 = crumb_pair_lop3<6>(wd); p3 = crumb_pair_lop3<7>(wd);
+                            } else {
+                                p0 = crumb_pair_lop3<0>(wd); p1 = crumb_pair_lop3<1>(wd);
+                                p2 = crumb_pair_lop3<2>(wd); p3 = crumb_pair_lop3<3>(wd);
+                            }
+                            v[4 * b4 + 0] = bf16x2_sub(p0, zlo[j]);
+                            v[4 * b4 + 1] = bf16x2_sub(p2, zlo[j]);
+                            v[4 * b4 + 2] = bf16x2_sub(p1, zhi[j]);
+                            v[4 * b4 + 3] = bf16x2_sub(p3, zhi[j]);
+                        }
+                        tmem_st_16x256b_x4(acol + (2 * q + hs) * 32, v);
+                    }
+                }
+            } else if constexpr (FMT == UQ_NF4) {
+                // chunk q = 64 k = blocks 4q .. 4q + 3, one word each; each code's codebook value as the bf16
+                // pair (hi, lo) from the shared table: hi pairs into plane 0, lo pairs into plane 1
+#pragma unroll
+                for (int q = 0; q < CPU; ++q) {
+                    const uint4 w4 = *reinterpret_cast<const uint4*>(rbase + q * CHUNK);
+                    const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+                    uint32_t vh[16], vl[16];
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+#pragma unroll
+                        for (int P = 0; P < 4; ++P) {
+                            const uint32_t e = nlut[(wv[b] >> (4 * P)) & 15u];
+                            const uint32_t o = nlut[(wv[b] >> (16 + 4 * P)) & 15u];
+                            const int slot = 4 * b + (P == 0 ? 0 : (P == 1 ? 2 : (P == 2 ? 1 : 3)));
+                            vh[slot] = __byte_perm(e, o, 0x5410);
+                            vl[slot] = __byte_perm(e, o, 0x7632);
+                        }
+                    }
+                    tmem_st_16x256b_x4(acol + q * 32, vh);
+                    tmem_st_16x256b_x4(acol + KC / 2 + q * 32, vl);
+                }
             } else {
                 // chunk q = 64 k = blocks 4q .. 4q + 3, one word each; pairs 0/2 are row g (k 4c, 4c+1 /
                 // 4c+2, 4c+3), pairs 1/3 row g + 8
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 w4 = *reinterpret_cast<const uint4*>(rbase + q * 512);
+                for (int q = 0; q < CPU; ++q) {
+                    const uint4 w4 = *reinterpret_cast<const uint4*>(rbase + q * CHUNK);
                     const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
                     uint32_t v[16];
 #pragma unroll
@@ -750,7 +840,7 @@ cudaError_t launch_tc_m(int mpad, const CUtensorMap& mx, const TcArgs& a, size_t
 }  // namespace
 
 bool tc_supported(int fmt, int N, int K) {
-    if (fmt != UQ_INT4_SYM && fmt != UQ_INT4_ASYM && fmt != UQ_INT8_SYM && fmt != UQ_K4) return false;
+    if (fmt < UQ_INT4_SYM || fmt > UQ_K4) return false;
     if (N < 1 || K % fmt_kt(fmt)) return false;
     return encode_fn() != nullptr;
 }
@@ -784,6 +874,8 @@ int tc_plan(int fmt, int mpad, int group, size_t* smem) {
         case UQ_INT4_SYM: b = tc_smem_fmt<UQ_INT4_SYM>(mpad, group); break;
         case UQ_INT4_ASYM: b = tc_smem_fmt<UQ_INT4_ASYM>(mpad, group); break;
         case UQ_INT8_SYM: b = tc_smem_fmt<UQ_INT8_SYM>(mpad, group); break;
+        case UQ_INT2_ASYM: b = tc_smem_fmt<UQ_INT2_ASYM>(mpad, group); break;
+        case UQ_NF4: b = tc_smem_fmt<UQ_NF4>(mpad, group); break;
         case UQ_K4: b = tc_smem_fmt<UQ_K4>(mpad, group); break;
         default: return -1;
     }
@@ -818,6 +910,8 @@ cudaError_t launch_tc(int fmt, const uint16_t* x, const TcArgs& a, size_t smem, 
         case UQ_INT4_SYM: return launch_tc_m<UQ_INT4_SYM>(a.Mpad, mx, a, smem, grid, st);
         case UQ_INT4_ASYM: return launch_tc_m<UQ_INT4_ASYM>(a.Mpad, mx, a, smem, grid, st);
         case UQ_INT8_SYM: return launch_tc_m<UQ_INT8_SYM>(a.Mpad, mx, a, smem, grid, st);
+        case UQ_INT2_ASYM: return launch_tc_m<UQ_INT2_ASYM>(a.Mpad, mx, a, smem, grid, st);
+        case UQ_NF4: return launch_tc_m<UQ_NF4>(a.Mpad, mx, a, smem, grid, st);
         case UQ_K4: return launch_tc_m<UQ_K4>(a.Mpad, mx, a, smem, grid, st);
         default: return cudaErrorInvalidValue;
     }

@@ -9,12 +9,14 @@ pytestmark = pytest.mark.gpu
 import gemm_uq_gb300 as uq  # noqa: E402
 from oracle import gemm as ogemm  # noqa: E402
 from oracle import quant as oquant  # noqa: E402
+from oracle.nf4 import nf4_codebook  # noqa: E402
 from synth import activations, normal_weights  # noqa: E402
 from tests.uq_helpers import device_weights, device_x, y_to_f64  # noqa: E402
 
 DEV = torch.device("cuda:0")
 TC_FMTS = [("INT4_ASYM", 128), ("INT4_ASYM", 32), ("INT4_SYM", 32), ("INT4_SYM", 128), ("INT8_SYM", 128),
-           ("INT8_SYM", 32), ("K4", 256)]
+           ("INT8_SYM", 32), ("K4", 256), ("INT2_ASYM", 64), ("INT2_ASYM", 32), ("INT2_ASYM", 128), ("NF4", 64),
+           ("NF4", 32), ("NF4", 128)]
 
 
 @pytest.fixture(autouse=True)
@@ -26,7 +28,7 @@ def _no_fault():
 def _case(fmt, group, M, N, K, seed):
     w = normal_weights(seed, N, K, 0.015 if fmt == "K4" else 0.02, outlier_p=0.001, outlier_mult=20.0)
     x = activations(seed, M, K)
-    qz = oquant.quantize(w, fmt, group)
+    qz = oquant.quantize(w, fmt, group, codebook=nf4_codebook() if fmt == "NF4" else None)
     wq, scales, zc = device_weights(qz, DEV)
     xd = device_x(x, DEV)
     y = uq.gemm(xd, wq, scales, zc, N, group, fmt)
@@ -57,7 +59,15 @@ def test_tc_parity_wide_m(M):
     assert r.max() <= 1.0, f"max error ratio {r.max():.3g}"
 
 
-@pytest.mark.parametrize("fmt,group", [("INT4_ASYM", 128), ("K4", 256)])
+def test_tc_serves_every_format_in_one_launch():
+    """M >= 16 with K a multiple of the code tile: one tensor-core launch for every format (K4: after its
+    x column-sum pre-kernel), no 8-row GEMV blocks."""
+    for fmt, group in [("INT4_SYM", 32), ("INT4_ASYM", 128), ("INT8_SYM", 128), ("INT2_ASYM", 64), ("NF4", 64)]:
+        assert uq.gemm_kernel_count(16, 8192, 8192, group, fmt) == 1, fmt
+    assert uq.gemm_kernel_count(16, 8192, 8192, 256, "K4") == 2
+
+
+@pytest.mark.parametrize("fmt,group", [("INT4_ASYM", 128), ("K4", 256), ("INT2_ASYM", 64), ("NF4", 64)])
 def test_tc_deterministic(fmt, group):
     y, _, _, (xd, wq, scales, zc) = _case(fmt, group, 32, 1024, 4096, seed=700)
     for _ in range(3):
