@@ -28,6 +28,7 @@ Modules:
   nf4      -- construction of the NF4 codebook from normal quantiles
   gemm     -- dequantize-then-matmul in float64, the error bound, the pass rule
   mlp      -- the gated MLP's fused gate/up projection silu(x W_gate^T) * (x W_up^T), its pass rule
+  rope     -- RMSNorm followed by rotate-half RoPE over head_dim blocks, its pass rule
 
 Parity status: every function is pinned by ``tests/test_oracle_*.py`` against
 brute force, exact rational arithmetic (``fractions.Fraction``), hand-worked

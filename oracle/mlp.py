@@ -15,9 +15,10 @@ silu and the product in fp32 and rounds h to bf16 once.  Its error has three par
     carried through h = silu(g) * u with |silu'(t)| <= 1.1 for every t:
         <= 1e-3 * (1.1 * b_g * |u| + |silu(g)| * b_u)   (to first order);
   * fp32 rounding of silu and of the product: a few units in 2^-24 relative to |h|;
-  * the bf16 rounding of h: at most 2^-9 * |h|.
+  * the bf16 rounding of h: at most 2^-8 * |h| (half a unit in the last place of an 8-bit significand).
 The pass rule therefore is |h - h_ref| <= 1e-3 * B + 2^-8 * |h_ref| + 1e-6 with
-B = 1.1 * b_g * |u_ref| + |silu(g_ref)| * b_u, the second term twice the output rounding.
+B = 1.1 * b_g * |u_ref| + |silu(g_ref)| * b_u: the second term is the output rounding, and the first
+covers the fp32 errors (orders of magnitude below 1e-3 * B) together with the rounding's own slack.
 """
 from __future__ import annotations
 
