@@ -28,6 +28,7 @@ __all__ = [
     "Workload",
     "WORKLOADS",
     "seed_for",
+    "gguf_blocks",
 ]
 
 
@@ -74,6 +75,19 @@ def activations(seed: int, m: int, k: int) -> np.ndarray:
     """x (m x k) ~ N(0, 1) drawn in float32 from stream [seed, 1], rounded to bf16 (float32 array of bf16 values)."""
     rng = np.random.default_rng([seed, 1])
     return bf16_round(rng.standard_normal((m, k), dtype=np.float32))
+
+
+def gguf_blocks(seed: int, n: int, k: int, qtype: str, sigma: float = 0.01) -> np.ndarray:
+    """Random GGUF blocks (uint8 [n][k/32][block bytes]) of type "Q4_0" (18 bytes) or "Q8_0" (34 bytes):
+    uniform random code bytes and an fp16 d ~ N(0, sigma) in the first two bytes (little endian).
+    Every such byte pattern is a valid block; nothing here quantizes anything."""
+    nbytes = {"Q4_0": 18, "Q8_0": 34}[qtype]
+    rng = np.random.default_rng([seed, 3])
+    raw = rng.integers(0, 256, (n, k // 32, nbytes)).astype(np.uint8)
+    d = (rng.normal(0.0, sigma, (n, k // 32)).astype(np.float16)).view(np.uint16)
+    raw[..., 0] = (d & 0xFF).astype(np.uint8)
+    raw[..., 1] = (d >> 8).astype(np.uint8)
+    return raw
 
 
 def seed_for(workload: int, index: int) -> int:
