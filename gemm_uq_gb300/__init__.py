@@ -38,6 +38,9 @@ SIGNATURES = {
     "uq_gemm_kernel_count": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I)]),
     "uq_gemm_gated": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "uq_gemm_gated_kernel_count": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I)]),
+    "uq_pack_gguf": (_I, [_P, _I, _P, _P, _I, _I, _P]),
+    "uq_rope_table": (_I, [_P, _I, _I, ctypes.c_double, _P]),
+    "uq_rmsnorm_rope": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P]),
 }
 
 _lib = None
@@ -101,6 +104,21 @@ def pack_layout(codes: torch.Tensor, group: int, fmt: str, stream=None) -> torch
     return wq
 
 
+GGUF_TYPES = {"Q4_0": (0, "INT4_SYM"), "Q8_0": (1, "INT8_SYM")}
+
+
+def pack_gguf(blocks: torch.Tensor, qtype: str, N: int, K: int, stream=None):
+    """uq_pack_gguf: GGUF Q4_0 / Q8_0 block bytes (device uint8) -> (wq, scales) of INT4_SYM / INT8_SYM, group 32."""
+    t, fmt = GGUF_TYPES[qtype]
+    wq_bytes, sc_bytes, _ = packed_size(N, K, 32, fmt)
+    wq = torch.empty(max(wq_bytes, 16), dtype=torch.uint8, device=blocks.device)
+    scales = torch.empty((N, K // 32), dtype=torch.int16, device=blocks.device)
+    assert blocks.is_cuda and blocks.is_contiguous()
+    _check(lib().uq_pack_gguf(ctypes.c_void_p(blocks.data_ptr()), t, _ptr(wq), _ptr(scales), N, K, _stream(stream)),
+           "uq_pack_gguf")
+    return wq, scales
+
+
 def pack_kmeta(d, dmin, sc, m, stream=None) -> torch.Tensor:
     """K4 fp16 d, dmin [N][S] (as int16/uint16/float16 tensors), uint8 sc, m [N][S][8] -> records [N][S][16]."""
     N, S = d.shape
@@ -157,6 +175,25 @@ def gemm_gated_kernel_count(M: int, N: int, K: int, group: int, fmt: str) -> int
     _check(lib().uq_gemm_gated_kernel_count(M, N, K, group, FORMATS[fmt], ctypes.byref(v)),
            "uq_gemm_gated_kernel_count")
     return v.value
+
+
+def rope_table(max_pos: int, head_dim: int, base: float, device=None, stream=None) -> torch.Tensor:
+    """uq_rope_table: fp32 [max_pos][head_dim/2][2] (cos, sin) on the device."""
+    t = torch.empty((max_pos, head_dim // 2, 2), dtype=torch.float32, device=device or "cuda")
+    _check(lib().uq_rope_table(_ptr(t), max_pos, head_dim, float(base), _stream(stream)), "uq_rope_table")
+    return t
+
+
+def rmsnorm_rope(x: torch.Tensor, gamma: torch.Tensor, pos: torch.Tensor, table: torch.Tensor, head_dim: int,
+                 eps: float, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """uq_rmsnorm_rope: y = RoPE(RMSNorm(x) * gamma, pos) (bf16 [M][D]); y may be x."""
+    M, D = x.shape
+    assert x.dtype == torch.bfloat16 and gamma.dtype == torch.bfloat16 and pos.dtype == torch.int32
+    if y is None:
+        y = torch.empty_like(x)
+    _check(lib().uq_rmsnorm_rope(_ptr(x), _ptr(gamma), _ptr(pos), _ptr(table), _ptr(y), M, D, head_dim,
+                                 table.shape[0], float(eps), _stream(stream)), "uq_rmsnorm_rope")
+    return y
 
 
 def gemm_noalloc(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, zc, N: int, group: int, fmt: str,

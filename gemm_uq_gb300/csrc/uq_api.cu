@@ -518,6 +518,50 @@ uq_status uq_gemm_gated_kernel_count(int M, int N, int K, int group, uq_fmt fmt,
     return UQ_OK;
 }
 
+uq_status uq_rope_table(float* table, int max_pos, int head_dim, double base, void* stream) {
+    if (max_pos < 0) return fail(UQ_ERR_INVALID, "negative max_pos");
+    if (head_dim < 2 || head_dim % 2) return fail(UQ_ERR_INVALID, "head_dim must be even and positive (got %d)", head_dim);
+    if (!(base > 1.0)) return fail(UQ_ERR_INVALID, "base must be above 1");
+    if (max_pos == 0) return UQ_OK;
+    if (!table) return fail(UQ_ERR_INVALID, "table is NULL");
+    if (!aligned16(table)) return fail(UQ_ERR_ALIGN, "table must be 16-byte aligned");
+    cudaError_t e = uq::launch_rope_table(table, max_pos, head_dim, base, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? UQ_OK : cuda_fail(e, "rope table launch");
+}
+
+uq_status uq_rmsnorm_rope(const uint16_t* x, const uint16_t* gamma, const int32_t* pos, const float* table,
+                          uint16_t* y, int M, int D, int head_dim, int max_pos, float eps, void* stream) {
+    if (M < 0 || D < 0 || max_pos < 0) return fail(UQ_ERR_INVALID, "negative size");
+    if (head_dim < 16 || head_dim % 16)
+        return fail(UQ_ERR_UNSUPPORTED, "head_dim must be a positive multiple of 16 (got %d)", head_dim);
+    if (D % head_dim) return fail(UQ_ERR_INVALID, "D=%d is not a multiple of head_dim %d", D, head_dim);
+    if (!(eps >= 0.0f)) return fail(UQ_ERR_INVALID, "eps must be >= 0");
+    if (M == 0 || D == 0) return UQ_OK;
+    if (!x || !gamma || !pos || !table || !y) return fail(UQ_ERR_INVALID, "null pointer");
+    if (max_pos < 1) return fail(UQ_ERR_INVALID, "the rope table is empty");
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(table) || !aligned16(y) ||
+        (reinterpret_cast<uintptr_t>(pos) & 3u))
+        return fail(UQ_ERR_ALIGN, "x, gamma, table and y must be 16-byte aligned, pos 4-byte aligned");
+    DeviceState* ds = nullptr;
+    uq_status s = device_state(&ds, nullptr);
+    if (s != UQ_OK) return s;
+    cudaError_t e = uq::launch_rmsnorm_rope(x, gamma, pos, table, y, M, D, head_dim, max_pos, eps, ds->words, ds->sms,
+                                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? UQ_OK : cuda_fail(e, "rmsnorm_rope launch");
+}
+
+uq_status uq_pack_gguf(const void* blocks, uq_gguf_type type, void* wq, uint16_t* scales, int N, int K, void* stream) {
+    if (type != UQ_GGUF_Q4_0 && type != UQ_GGUF_Q8_0) return fail(UQ_ERR_UNSUPPORTED, "unknown GGUF block type %d", type);
+    if (N < 0 || K < 0) return fail(UQ_ERR_INVALID, "negative size");
+    if (K % 32) return fail(UQ_ERR_INVALID, "K=%d is not a multiple of the 32-weight block", K);
+    if ((long long)N * K == 0) return UQ_OK;
+    if (!blocks || !wq || !scales) return fail(UQ_ERR_INVALID, "null pointer");
+    if (!aligned16(wq) || !aligned16(scales)) return fail(UQ_ERR_ALIGN, "wq and scales must be 16-byte aligned");
+    cudaError_t e = uq::launch_pack_gguf(type == UQ_GGUF_Q4_0 ? 0 : 1, static_cast<const uint8_t*>(blocks),
+                                         static_cast<uint8_t*>(wq), scales, N, K, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? UQ_OK : cuda_fail(e, "GGUF pack launch");
+}
+
 uq_status uq_unpack_codes(const void* wq, int8_t* codes, int N, int K, int group, uq_fmt fmt, void* stream) {
     uq_status s = check_shape(N, K, group, fmt);
     if (s != UQ_OK) return s;

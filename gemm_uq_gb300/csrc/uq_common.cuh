@@ -221,5 +221,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 constexpr unsigned int FAULT_GEMV_WAIT = 1u;
 constexpr unsigned int FAULT_TC_WAIT = 2u;
 constexpr unsigned int FAULT_GEMV_SPLIT = 4u;   // a launch's work split exceeded what the kernel holds
+constexpr unsigned int FAULT_ROPE_POS = 8u;     // a row's position lay outside the rope table (row not written)
 
 }  // namespace uq

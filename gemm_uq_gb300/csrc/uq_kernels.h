@@ -17,6 +17,8 @@ cudaError_t noalloc_take_fault(unsigned int* v);
 cudaError_t launch_pack(int fmt, const int8_t* codes, uint8_t* wq, int N, int K, unsigned int* bad,
                         cudaStream_t st);
 cudaError_t launch_unpack(int fmt, const uint8_t* wq, int8_t* codes, int N, int K, cudaStream_t st);
+cudaError_t launch_pack_gguf(int qtype, const uint8_t* blocks, uint8_t* wq, uint16_t* scales, int N, int K,
+                             cudaStream_t st);   // qtype 0 = Q4_0, 1 = Q8_0
 cudaError_t launch_dequant(int fmt, const uint8_t* wq, const uint8_t* scales, const uint8_t* zc, float* w,
                            int N, int K, int group, cudaStream_t st);
 cudaError_t launch_pack_kmeta(const uint16_t* d, const uint16_t* dmin, const uint8_t* sc, const uint8_t* m,
@@ -26,6 +28,12 @@ cudaError_t launch_quantize(int fmt, const float* w, int8_t* codes, uint16_t* sc
                             const float* codebook, int N, int K, int group, cudaStream_t st);
 cudaError_t launch_quantize_k4(const float* w, int8_t* codes, uint16_t* d, uint16_t* dmin, uint8_t* sc,
                                uint8_t* m, int N, int K, cudaStream_t st);
+
+// fused RMSNorm + RoPE and its cos/sin table (uq_norm.cu)
+cudaError_t launch_rope_table(float* table, int max_pos, int head_dim, double base, cudaStream_t st);
+cudaError_t launch_rmsnorm_rope(const uint16_t* x, const uint16_t* gamma, const int32_t* pos, const float* table,
+                                uint16_t* y, int M, int D, int head_dim, int max_pos, float eps, unsigned int* fault,
+                                int sms, cudaStream_t st);
 
 // small-M GEMV (uq_gemv.cu)
 struct GemvArgs {

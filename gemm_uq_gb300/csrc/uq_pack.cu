@@ -63,6 +63,43 @@ __global__ void pack_kernel(const int8_t* __restrict__ codes, uint8_t* __restric
     }
 }
 
+// GGUF blocks -> the packed plane: Q4_0 is INT4_SYM at group 32 (code = nibble - 8), Q8_0 is INT8_SYM at
+// group 32 (code = signed byte).  A row of K weights is K / 32 blocks of BB bytes: fp16 d, then the codes
+// (Q4_0: byte j holds weight j in its low nibble and weight j + 16 in its high nibble).
+template <int FMT>
+__global__ void pack_gguf_kernel(const uint8_t* __restrict__ blocks, uint8_t* __restrict__ wq, int N, int K) {
+    constexpr int BITS = fmt_bits(FMT), CPW = fmt_cpw(FMT), BIAS = fmt_bias(FMT);
+    constexpr int BB = (FMT == UQ_INT4_SYM) ? 18 : 34;
+    const Layout L(N, K, FMT);
+    const long long words = L.bytes() / 4;
+    const int nb = K / 32;
+    for (long long wi = blockIdx.x * (long long)blockDim.x + threadIdx.x; wi < words;
+         wi += (long long)gridDim.x * blockDim.x) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int s = 0; s < CPW; ++s) {
+            int n, k;
+            L.slot_nk(wi * 4, s, &n, &k);
+            int c = 0;
+            if (n < N && k < K) {
+                const uint8_t* blk = blocks + ((long long)n * nb + k / 32) * BB + 2;
+                const int j = k & 31;
+                if constexpr (FMT == UQ_INT4_SYM) c = ((j < 16 ? blk[j] : (blk[j - 16] >> 4)) & 15) - 8;
+                else c = (int)(int8_t)blk[j];
+            }
+            word |= ((uint32_t)(c + BIAS) & ((1u << BITS) - 1u)) << slot_bitpos(BITS, s);
+        }
+        reinterpret_cast<uint32_t*>(wq)[wi] = word;
+    }
+}
+
+// the blocks' fp16 d as the fp16 scales [N][K/32] of the group-32 format
+__global__ void gguf_scales_kernel(const uint8_t* __restrict__ blocks, uint16_t* __restrict__ scales, long long nblk,
+                                   int BB) {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nblk; i += (long long)gridDim.x * blockDim.x)
+        scales[i] = (uint16_t)(blocks[i * BB] | (blocks[i * BB + 1] << 8));
+}
+
 template <int FMT>
 __global__ void unpack_kernel(const uint8_t* __restrict__ wq, int8_t* __restrict__ codes, int N, int K) {
     constexpr int CPW = fmt_cpw(FMT), BIAS = fmt_bias(FMT);
@@ -350,6 +387,24 @@ cudaError_t launch_pack(int fmt, const int8_t* codes, uint8_t* wq, int N, int K,
         case UQ_K4: pack_kernel<UQ_K4><<<g, 256, 0, st>>>(codes, wq, N, K, bad); break;
         default: return cudaErrorInvalidValue;
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_gguf(int qtype, const uint8_t* blocks, uint8_t* wq, uint16_t* scales, int N, int K,
+                             cudaStream_t st) {
+    const int fmt = qtype == 0 ? UQ_INT4_SYM : UQ_INT8_SYM;
+    const Layout L(N, K, fmt);
+    const long long words = L.bytes() / 4;
+    long long g = (words + 255) / 256;
+    if (g > 65536) g = 65536;
+    if (fmt == UQ_INT4_SYM) pack_gguf_kernel<UQ_INT4_SYM><<<(int)(g < 1 ? 1 : g), 256, 0, st>>>(blocks, wq, N, K);
+    else pack_gguf_kernel<UQ_INT8_SYM><<<(int)(g < 1 ? 1 : g), 256, 0, st>>>(blocks, wq, N, K);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long long nblk = (long long)N * (K / 32);
+    long long g2 = (nblk + 255) / 256;
+    if (g2 > 65536) g2 = 65536;
+    gguf_scales_kernel<<<(int)(g2 < 1 ? 1 : g2), 256, 0, st>>>(blocks, scales, nblk, qtype == 0 ? 18 : 34);
     return cudaGetLastError();
 }
 

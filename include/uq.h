@@ -62,6 +62,12 @@ typedef enum uq_fmt {
     UQ_K4 = 5
 } uq_fmt;
 
+/* GGUF block types uq_pack_gguf reads (the GGUF file format's block layouts). */
+typedef enum uq_gguf_type {
+    UQ_GGUF_Q4_0 = 0,   /* 32 weights in 18 bytes: fp16 d, 16 bytes of nibbles; w = d * (nibble - 8) */
+    UQ_GGUF_Q8_0 = 1    /* 32 weights in 34 bytes: fp16 d, 32 signed bytes q; w = d * q */
+} uq_gguf_type;
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* uq_status_string(uq_status s);
 
@@ -102,6 +108,18 @@ uq_status uq_packed_size(int N, int K, int group, uq_fmt fmt,
  */
 uq_status uq_pack_layout(const int8_t* codes, void* wq, int N, int K, int group, uq_fmt fmt,
                          void* stream);
+
+/*
+ * uq_pack_gguf -- GGUF block-quantized weights -> the library's packed plane and scales ("Ultra LLM
+ * Engine", section "Checkpoint Loading": GGUF block formats such as Q4_0; the other page's GGUF loader
+ * dequantizes them).  Q4_0 is exactly UQ_INT4_SYM with group 32 (code = nibble - 8, scale = d) and Q8_0
+ * exactly UQ_INT8_SYM with group 32 (code = q, scale = d), so the result feeds uq_gemm, uq_gemm_gated and
+ * uq_dequant with that format and group 32, and decodes to the same W_hat as the blocks.
+ *   blocks (device) the GGUF tensor's bytes: N rows of K/32 blocks (18 or 34 bytes each), byte aligned
+ *   wq (device) uq_packed_size(N, K, 32, fmt).wq_bytes, written; scales (device) fp16 [N][K/32], written.
+ * K a multiple of 32.  Asynchronous.
+ */
+uq_status uq_pack_gguf(const void* blocks, uq_gguf_type type, void* wq, uint16_t* scales, int N, int K, void* stream);
 
 /*
  * uq_pack_kmeta -- UQ_K4 metadata -> 16-byte records [N][K/256] (the `scales` argument).
@@ -169,6 +187,30 @@ uq_status uq_gemm_gated(const uint16_t* x, const void* wq_gate, const void* scal
 
 /* uq_gemm_gated_kernel_count -- kernels one uq_gemm_gated call of this shape launches (as uq_gemm_kernel_count). */
 uq_status uq_gemm_gated_kernel_count(int M, int N, int K, int group, uq_fmt fmt, int* count);
+
+/*
+ * uq_rope_table -- the cos/sin table of rotary position embedding for uq_rmsnorm_rope:
+ *     table[p][i] = ( cos(p * base^(-2i/head_dim)), sin(p * base^(-2i/head_dim)) ),  p < max_pos, i < head_dim/2,
+ * evaluated in fp64 and rounded to fp32 (table: device, fp32 [max_pos][head_dim/2][2], written).
+ * Build it once per (max_pos, head_dim, base).  head_dim even, base > 1.  Asynchronous.
+ */
+uq_status uq_rope_table(float* table, int max_pos, int head_dim, double base, void* stream);
+
+/*
+ * uq_rmsnorm_rope -- RMSNorm followed by rotary position embedding, fused ("Ultra LLM Engine", section
+ * "Fused Kernels": RMSNorm followed by RoPE; read as the Llama-style RMSNorm and rotate-half RoPE):
+ *     n[m][j] = x[m][j] / sqrt(mean_j(x[m][j]^2) + eps) * gamma[j]        (over the row's D values)
+ *     every head_dim block of row m rotated by the row's position p = pos[m]: for i < head_dim/2,
+ *     (n_i, n_{i+h/2}) -> (n_i cos - n_{i+h/2} sin, n_{i+h/2} cos + n_i sin), (cos, sin) = table[p][i]
+ *     y[m][j] = bf16_RNE of the result (fp32 arithmetic throughout).
+ *   x, y (device) bf16 [M][D] (y may be x); gamma (device) bf16 [D]; pos (device) int32 [M];
+ *   table from uq_rope_table with the same head_dim; head_dim a multiple of 16; D a multiple of head_dim.
+ * A row may be a token's hidden vector or one head's vector (per-head query/key norm: D = head_dim).
+ * A position outside [0, max_pos) leaves its row unwritten and sets bit 3 of the fault word
+ * (uq_device_fault).  Asynchronous.
+ */
+uq_status uq_rmsnorm_rope(const uint16_t* x, const uint16_t* gamma, const int32_t* pos, const float* table,
+                          uint16_t* y, int M, int D, int head_dim, int max_pos, float eps, void* stream);
 
 /*
  * uq_unpack_codes -- debug: packed plane -> int8 codes [N][K] (device), bit-exact
@@ -241,7 +283,7 @@ uq_status uq_gemm_kernel_count(int M, int N, int K, int group, uq_fmt fmt, int* 
  * one of uq_gemm and the one of uq_gemm_noalloc, OR-ed together (bit 0 / bit 1: a GEMV /
  * tensor-core kernel's bounded wait ran out and the kernel returned early instead of hanging;
  * its output is then unspecified; bit 2: a GEMV launch was given a work split larger than the
- * kernel holds and computed nothing).  Synchronizes the device; allocates nothing.
+ * kernel holds and computed nothing; bit 3: uq_rmsnorm_rope met a position outside its table).  Synchronizes the device; allocates nothing.
  * *flag = 0 when no fault.
  */
 uq_status uq_device_fault(unsigned int* flag);
