@@ -30,6 +30,7 @@ Modules:
   mlp      -- the gated MLP's fused gate/up projection silu(x W_gate^T) * (x W_up^T), its pass rule
   rope     -- RMSNorm followed by rotate-half RoPE over head_dim blocks, its pass rule
   gguf     -- decoding of GGUF Q4_0 / Q8_0 blocks (the block formats equal INT4_SYM / INT8_SYM, group 32)
+  w4a8     -- dynamic per-row int8 activations and integer group sums (W4A8 / W8A8), its pass rule
 
 Parity status: every function is pinned by ``tests/test_oracle_*.py`` against
 brute force, exact rational arithmetic (``fractions.Fraction``), hand-worked
