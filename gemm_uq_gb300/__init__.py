@@ -39,6 +39,8 @@ SIGNATURES = {
     "uq_gemm_gated": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "uq_gemm_gated_kernel_count": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I)]),
     "uq_pack_gguf": (_I, [_P, _I, _P, _P, _I, _I, _P]),
+    "uq_gemm_w4a8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "uq_gemm_w4a8_kernel_count": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I)]),
     "uq_rope_table": (_I, [_P, _I, _I, ctypes.c_double, _P]),
     "uq_rmsnorm_rope": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, ctypes.c_float, _P]),
 }
@@ -194,6 +196,31 @@ def rmsnorm_rope(x: torch.Tensor, gamma: torch.Tensor, pos: torch.Tensor, table:
     _check(lib().uq_rmsnorm_rope(_ptr(x), _ptr(gamma), _ptr(pos), _ptr(table), _ptr(y), M, D, head_dim,
                                  table.shape[0], float(eps), _stream(stream)), "uq_rmsnorm_rope")
     return y
+
+
+def gemm_w4a8(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, zc, N: int, group: int, fmt: str,
+              y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """uq_gemm_w4a8: y with x quantized per row to int8 and integer dot products (bf16 [M][N])."""
+    M, K = x.shape
+    assert x.dtype == torch.bfloat16
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(lib().uq_gemm_w4a8(_ptr(x), _ptr(wq), _ptr(scales), _ptr(zc), _ptr(y), M, N, K, group, FORMATS[fmt],
+                              _stream(stream)), "uq_gemm_w4a8")
+    return y
+
+
+def gemm_w4a8_ptrs(x_ptr: int, wq_ptr: int, scales_ptr: int, zc_ptr, y_ptr: int, M: int, N: int, K: int, group: int,
+                   fmt: str, stream_handle: int) -> None:
+    P = ctypes.c_void_p
+    _check(lib().uq_gemm_w4a8(P(x_ptr), P(wq_ptr), P(scales_ptr), P(zc_ptr) if zc_ptr else None, P(y_ptr), M, N, K,
+                              group, FORMATS[fmt], P(stream_handle)), "uq_gemm_w4a8")
+
+
+def gemm_w4a8_kernel_count(M: int, N: int, K: int, group: int, fmt: str) -> int:
+    v = ctypes.c_int(0)
+    _check(lib().uq_gemm_w4a8_kernel_count(M, N, K, group, FORMATS[fmt], ctypes.byref(v)), "uq_gemm_w4a8_kernel_count")
+    return v.value
 
 
 def gemm_noalloc(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, zc, N: int, group: int, fmt: str,

@@ -17,6 +17,7 @@
 
 namespace {
 
+constexpr int RB_ROWS = 16;   // rows per row block of the packed plane
 thread_local std::string g_last_error = "";
 
 uq_status fail(uq_status s, const char* fmt_msg, ...) {
@@ -560,6 +561,97 @@ uq_status uq_pack_gguf(const void* blocks, uq_gguf_type type, void* wq, uint16_t
     cudaError_t e = uq::launch_pack_gguf(type == UQ_GGUF_Q4_0 ? 0 : 1, static_cast<const uint8_t*>(blocks),
                                          static_cast<uint8_t*>(wq), scales, N, K, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? UQ_OK : cuda_fail(e, "GGUF pack launch");
+}
+
+namespace {
+bool a8_format(int fmt) { return fmt == UQ_INT4_SYM || fmt == UQ_INT4_ASYM || fmt == UQ_INT8_SYM; }
+// the work split of one A8 GEMV launch over Mb rows (the mma GEMV's rules)
+void a8_args(uq::GemvArgs& a, const uq::Layout& L, int Mb, int N, int K, int group, int sms) {
+    a.M = Mb; a.N = N; a.K = K; a.group = group; a.a8 = 1;
+    a.NB = L.NB; a.KB = L.KB; a.T = (long long)L.NB * L.KB;
+    const long long P = (long long)sms * 2 * 4;
+    a.P = (int)(P > a.T ? a.T : P);
+}
+}  // namespace
+
+uq_status uq_gemm_w4a8(const uint16_t* x, const void* wq, const void* scales, const void* zeros, uint16_t* y,
+                       int M, int N, int K, int group, uq_fmt fmt, void* stream) {
+    if (!a8_format(fmt)) return fail(UQ_ERR_UNSUPPORTED, "W4A8 takes INT4_SYM, INT4_ASYM or INT8_SYM weights");
+    uq_status s = check_shape(N, K, group, fmt);
+    if (s != UQ_OK) return s;
+    if (M < 0) return fail(UQ_ERR_INVALID, "negative M");
+    if (M == 0 || N == 0) return UQ_OK;
+    if (!y) return fail(UQ_ERR_INVALID, "y is NULL");
+    if (!aligned16(y)) return fail(UQ_ERR_ALIGN, "y must be 16-byte aligned");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        cudaError_t e = cudaMemsetAsync(y, 0, (size_t)M * N * 2, st);
+        return e == cudaSuccess ? UQ_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    if (!x || !wq) return fail(UQ_ERR_INVALID, "x or wq is NULL");
+    if (!aligned16(x) || !aligned16(wq)) return fail(UQ_ERR_ALIGN, "x and wq must be 16-byte aligned");
+    if ((s = check_meta_ptrs(scales, zeros, fmt)) != UQ_OK) return s;
+    DeviceState* ds = nullptr;
+    int dev = 0;
+    if ((s = device_state(&ds, &dev)) != UQ_OK) return s;
+    const uq::Layout L(N, K, fmt);
+    const int Kp = L.Kp, G = (Kp + group - 1) / group;
+    // scratch: x codes [M][Kp] | s_x [M] | per (row, group, lane column) code sums [M][G][4]; partial sums
+    const size_t xq_b = ((size_t)M * Kp + 255) / 256 * 256, sx_b = ((size_t)M * 4 + 255) / 256 * 256;
+    const size_t aux = xq_b + sx_b + (size_t)M * G * 4 * sizeof(int);
+    Workspace* ws = nullptr;
+    const int rows8 = M < 8 ? M : 8;
+    if ((s = workspace(dev, st, (size_t)L.NB * L.KB * RB_ROWS * rows8 * sizeof(float), (size_t)L.NB * sizeof(unsigned int),
+                       &ws, aux)) != UQ_OK)
+        return s;
+    int8_t* xq = reinterpret_cast<int8_t*>(ws->aux);
+    float* sx = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws->aux) + xq_b);
+    int* sxl = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ws->aux) + xq_b + sx_b);
+    cudaError_t e = uq::launch_quant_x(x, xq, sx, sxl, M, K, Kp, group, fmt == UQ_INT8_SYM ? 0 : 1, st);
+    if (e != cudaSuccess) return cuda_fail(e, "activation quantization launch");
+    for (int m0 = 0; m0 < M; m0 += 8) {
+        const int mb = (M - m0) < 8 ? (M - m0) : 8;
+        uq::GemvArgs a = {};
+        a8_args(a, L, mb, N, K, group, ds->sms);
+        a.x = x;
+        a.wq = static_cast<const uint8_t*>(wq);
+        a.scales = static_cast<const uint8_t*>(scales);
+        a.zc = static_cast<const uint8_t*>(zeros);
+        a.y = y + (long long)m0 * N;
+        a.ldx = K; a.ldy = N;
+        a.partials = ws->partials;
+        a.tickets = ws->tickets;
+        a.fault = ds->words;
+        const int grid = uq::gemv_grid(a, fmt, ds->sms);
+        e = uq::launch_gemv_a8(fmt, a, xq + (long long)m0 * Kp, sx + m0, sxl + (long long)m0 * G * 4, Kp, grid, st);
+        if (e != cudaSuccess) return cuda_fail(e, "W4A8 GEMV launch");
+    }
+    return UQ_OK;
+}
+
+uq_status uq_gemm_w4a8_kernel_count(int M, int N, int K, int group, uq_fmt fmt, int* count) {
+    if (!count) return fail(UQ_ERR_INVALID, "null pointer");
+    *count = 0;
+    if (!a8_format(fmt)) return fail(UQ_ERR_UNSUPPORTED, "W4A8 takes INT4_SYM, INT4_ASYM or INT8_SYM weights");
+    uq_status s = check_shape(N, K, group, fmt);
+    if (s != UQ_OK) return s;
+    if (M < 0) return fail(UQ_ERR_INVALID, "negative M");
+    if (M == 0 || N == 0) return UQ_OK;
+    if (K == 0) { *count = 1; return UQ_OK; }
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess || sms < 1) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice, "SM count");
+    const uq::Layout L(N, K, fmt);
+    int n = 1;                                                   // the activation quantization
+    for (int m0 = 0; m0 < M; m0 += 8) {
+        uq::GemvArgs a = {};
+        a8_args(a, L, (M - m0) < 8 ? (M - m0) : 8, N, K, group, sms);
+        uq::gemv_grid(a, fmt, sms);
+        n += 1 + (a.cta_rows ? 0 : 1);
+    }
+    *count = n;
+    return UQ_OK;
 }
 
 uq_status uq_unpack_codes(const void* wq, int8_t* codes, int N, int K, int group, uq_fmt fmt, void* stream) {

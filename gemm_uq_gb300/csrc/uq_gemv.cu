@@ -14,12 +14,12 @@ size_t gemv_smem_bytes(int fmt, int K, int group, int M) { return gemv_smem_byte
 int gemv_warps(int fmt) { return gemv_warps_impl(fmt); }
 int gemv_grid(GemvArgs& a, int fmt, int sms) {
     a.cta_rows = 0;
-    if (!gemv_is_mma(fmt)) return (a.P + GEMV_WARPS - 1) / GEMV_WARPS;
+    if (!gemv_is_mma(fmt) && !a.a8) return (a.P + GEMV_WARPS - 1) / GEMV_WARPS;
     // Whole row blocks per CTA need no second pass; take them when no warp gets more tiles than
     // under the stream-K split and either the busiest CTA streams at most ~6 % more bytes than the
     // average one (bandwidth-bound shapes) or no warp has more than one tile (latency-bound ones).
     // (gated: the units CTAs own are gate/up pairs of row blocks)
-    const int W = gemv_warps(fmt);
+    const int W = a.a8 ? 4 : gemv_warps(fmt);
     const int WU = a.gated ? 2 : 1;
     const int NBU = a.NB / WU;
     const int slots = sms * MMA_CTAS_PER_SM;                           // CTAs resident at once
@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(256) gemv_split_reduce(const GemvArgs a) {
     }
 }
 
-static cudaError_t launch_split_reduce(const GemvArgs& a, int sms, cudaStream_t st) {
+cudaError_t launch_gemv_second_pass(const GemvArgs& a, int sms, cudaStream_t st) {
     const long long total = (long long)(a.gated ? a.NB / 2 : a.NB) * RB * a.M;
     long long blocks = (total + 255) / 256;
     if (blocks > 4LL * sms) blocks = 4LL * sms;
@@ -106,7 +106,7 @@ cudaError_t launch_gemv(int fmt, const GemvArgs& a, int grid, cudaStream_t st) {
     if (e != cudaSuccess || !gemv_is_mma(fmt) || a.cta_rows) return e;
     // the mma kernel leaves row blocks shared between workers as partial sums (grid = its CTAs,
     // one per SM at most, so it is also the SM count bound for the reduce grid)
-    return launch_split_reduce(a, grid, st);
+    return launch_gemv_second_pass(a, grid, st);
 }
 
 }  // namespace uq

@@ -59,6 +59,7 @@ struct GemvArgs {
     const uint8_t* wq2;
     const uint8_t* scales2;
     const uint8_t* zc2;
+    int a8;                   // the W4A8 GEMV (integer x codes): its work split follows the mma GEMV's
 };
 constexpr int GEMV_WARPS = 4;     // worker warps per CTA
 // formats whose GEMV runs on mma.sync (the others on CUDA-core FMAs)
@@ -74,6 +75,15 @@ int gemv_grid(GemvArgs& a, int fmt, int sms);
 // fp32 partial-sum floats a GEMV launch needs (T tiles, P workers, M rows of x)
 size_t gemv_partials_floats(int fmt, long long T, int P, int M);
 cudaError_t launch_gemv(int fmt, const GemvArgs& a, int grid, cudaStream_t st);
+// the second pass of a stream-K split (tile partial sums [T][16][M] summed in k order)
+cudaError_t launch_gemv_second_pass(const GemvArgs& a, int sms, cudaStream_t st);
+
+// W4A8 / W8A8 (uq_w4a8.cu): x codes and scales, then the integer GEMV
+size_t a8_smem_bytes(int fmt);
+cudaError_t launch_quant_x(const uint16_t* x, int8_t* xq, float* sx, int* sxl, int M, int K, int Kp, int gs, int perm,
+                           cudaStream_t st);
+cudaError_t launch_gemv_a8(int fmt, const GemvArgs& a, const int8_t* xq, const float* sxs, const int* sxl, int Kp,
+                           int grid, cudaStream_t st);
 
 
 // tensor-core GEMM for M >= 16 (uq_tc.cu)

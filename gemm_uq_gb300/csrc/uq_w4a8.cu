@@ -1,0 +1,342 @@
+// uq_w4a8.cu -- W4A8 / W8A8: dynamic per-row int8 activations and integer dot products (sm_103a).
+//
+// "Ultra LLM Engine", section "Quantized Model": the activations are dynamically quantized for the
+// GEMV/GEMM paths.  Per row m of x: s_x = absmax / 127 (fp32), xq = clamp(RNE(x / s_x), -127, 127)
+// (fp32 quotient); then y[m][n] = s_x * sum_g s[n][g] * I, I = sum_{k in g} xq * (q - z), an exact
+// integer formed with dp4a (four int8 products and their sum per instruction).
+//
+// quant_x_kernel (one CTA per row): absmax, s_x, the codes, written with each 4-k group's bytes in the
+// order the weight words hold their codes (4-bit: k, k+2, k+1, k+3 -- the low nibbles of a fragment-
+// order word; 8-bit: k .. k+3), and per (group, lane column c) the sum of the codes that lane multiplies,
+// for the zero-point term.
+// gemv_a8_kernel: the decode GEMV's tiles, copy rings and work split (whole row blocks per CTA, or the
+// stream-K split and its second pass), with the integer inner loop: per 16-k block a lane takes its
+// code word, masks the two rows' codes into bytes (w & 0x0F0F0F0F, (w >> 4) & 0x0F0F0F0F for 4-bit),
+// and accumulates one dp4a per row and activation row.  Per group: acc += s * (I - zc * SX), zc the
+// stored code's offset (8 for INT4_SYM, z for INT4_ASYM, 128 for INT8_SYM).
+#include "uq_gemv.cuh"
+
+namespace uq {
+
+namespace {
+
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// one CTA (256 threads) per row of x
+__global__ void __launch_bounds__(256) quant_x_kernel(const uint16_t* __restrict__ x, int8_t* __restrict__ xq,
+                                                      float* __restrict__ sx, int* __restrict__ sxl, int M, int K,
+                                                      int Kp, int gs, int perm) {
+    __shared__ float red[8];
+    const int m = blockIdx.x;
+    if (m >= M) return;
+    const uint16_t* xr = x + (long long)m * K;
+    float mx = 0.f;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) mx = fmaxf(mx, fabsf(bf16lo_f32(xr[k])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    float amax = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) amax = fmaxf(amax, red[w]);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (threadIdx.x == 0) sx[m] = s;
+    // codes, 4 per thread step (one 4-k group), in the weight words' byte order
+    int8_t* qr = xq + (long long)m * Kp;
+    for (int k4 = threadIdx.x * 4; k4 < Kp; k4 += blockDim.x * 4) {
+        int q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int k = k4 + j;
+            float v = 0.f;
+            if (k < K && s > 0.f) v = rintf(__fdiv_rn(bf16lo_f32(xr[k]), s));
+            v = fminf(fmaxf(v, -127.f), 127.f);
+            q[j] = (int)v;
+        }
+        const uint32_t packed = perm ? ((uint32_t)(q[0] & 255) | ((uint32_t)(q[2] & 255) << 8) |
+                                        ((uint32_t)(q[1] & 255) << 16) | ((uint32_t)(q[3] & 255) << 24))
+                                     : ((uint32_t)(q[0] & 255) | ((uint32_t)(q[1] & 255) << 8) |
+                                        ((uint32_t)(q[2] & 255) << 16) | ((uint32_t)(q[3] & 255) << 24));
+        *reinterpret_cast<uint32_t*>(qr + k4) = packed;
+    }
+    // per (group, c): the sum of the codes at k = 16 b + 4 c .. + 3 of the group's blocks b
+    const int G = (Kp + gs - 1) / gs;
+    for (int e = threadIdx.x; e < G * 4; e += blockDim.x) {
+        const int gi = e >> 2, c = e & 3;
+        int tot = 0;
+        for (int k = gi * gs + 4 * c; k < gi * gs + gs && k < K; k += 16)
+            for (int j = 0; j < 4 && k + j < K; ++j) {
+                float v = (s > 0.f) ? rintf(__fdiv_rn(bf16lo_f32(xr[k + j]), s)) : 0.f;
+                tot += (int)fminf(fmaxf(v, -127.f), 127.f);
+            }
+        sxl[(long long)m * G * 4 + e] = tot;
+    }
+}
+
+}  // namespace
+
+// Shared memory of the A8 GEMV: rings [warps][stages][stage] | ring mbarriers | partial sums
+template <int FMT>
+__host__ __device__ inline GemvSmem gemv_a8_smem_plan() {
+    using F = GemvFmt<FMT>;
+    constexpr int W = 4, S = 2;
+    GemvSmem p;
+    p.bars = (size_t)W * S * F::STAGE_BYTES;
+    p.lut = p.bars + (size_t)W * S * 8;
+    p.sx = p.lut;
+    p.ps = (p.lut + 15) / 16 * 16;
+    p.x = p.ps + (size_t)W * MMA_TPW * RB * 8 * 4;
+    p.total = p.x;
+    return p;
+}
+
+// GB = 16-k blocks per scaling group
+template <int FMT, int GB>
+__global__ void __launch_bounds__(128, MMA_CTAS_PER_SM) gemv_a8_kernel(const GemvArgs a, const int8_t* __restrict__ xq,
+                                                                       const float* __restrict__ sxs,
+                                                                       const int* __restrict__ sxl, int Kp) {
+    using F = GemvFmt<FMT>;
+    constexpr int KT = F::KT, S = 2, W = 4;
+    constexpr int GS = GB * 16, GPT = KT / GS;
+    constexpr int BPCH = F::BPC;                                    // 16-k blocks per 512-byte chunk
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int M = a.M;
+    const GemvSmem plan = gemv_a8_smem_plan<FMT>();
+    float* cpart = reinterpret_cast<float*>(smem + plan.ps);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const Layout L(a.N, a.K, FMT);
+    uint8_t* ring = smem + (size_t)warp * S * F::STAGE_BYTES;
+
+    // work split as the mma GEMV's (k-major tiles; whole row blocks per CTA, or stream-K)
+    const bool cta_rows = a.cta_rows != 0;
+    const int rb0 = cta_rows ? (int)((long long)blockIdx.x * a.NB / gridDim.x) : 0;
+    const int R = cta_rows ? (int)((long long)(blockIdx.x + 1) * a.NB / gridDim.x) - rb0 : a.NB;
+    const unsigned Tc = (unsigned)(R * L.KB);
+    const int w = cta_rows ? warp : (int)(blockIdx.x + gridDim.x * warp);
+    const bool has_work = cta_rows ? true : w < a.P;
+    const long long t0 = cta_rows ? (long long)(warp * Tc / W) : (has_work ? range_begin(w, a.T, a.P) : 0);
+    const long long t1 = cta_rows ? (long long)((warp + 1) * Tc / W) : (has_work ? range_begin(w + 1, a.T, a.P) : 0);
+    int ntl = (int)(t1 - t0);
+    if (cta_rows && ntl > MMA_TPW) {
+        if (lane == 0) atomicOr(a.fault, FAULT_GEMV_SPLIT);
+        ntl = 0;
+    }
+    auto kb_of = [&](long long i) { return (int)(i / R); };
+    auto nb_of = [&](long long i) { return rb0 + (int)(i % R); };
+    MetaConst mc;
+    mc.G = a.K / a.group;
+    mc.GT = KT / a.group;
+    mc.ZB = (mc.G + 1) >> 1;
+    mc.S4 = a.K / 256;
+    mc.aligned = (a.K % (8 * a.group)) == 0 && (mc.GT % 8) == 0;
+    const int G_all = a.K / GS;
+    const int Gq = (Kp + GS - 1) / GS;                              // groups of the code-sum table
+    const GemvSrc src{a.wq, a.scales, a.zc};
+
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    int issued = 0;
+    auto issue_next = [&]() {
+        const long long i = t0 + issued;
+        issue_tile<FMT, true>(a, src, L, mc, nb_of(i), kb_of(i), ring + (issued % S) * F::STAGE_BYTES, nullptr, lane);
+        ++issued;
+    };
+    if (a.overlap && has_work && ntl > 0) issue_next();           // weights are constant: before the wait
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (has_work && issued == 0 && ntl > 0) issue_next();
+    if (!has_work) return;
+
+    float acc[2][8];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int m = 0; m < 8; ++m) acc[j][m] = 0.f;
+    float sxm[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) sxm[m] = m < M ? __ldg(sxs + m) : 0.f;
+
+    for (int li = 0; li < ntl; ++li) {
+        const long long i = t0 + li;
+        const int kb = kb_of(i), nb = nb_of(i);
+        const int n0 = nb * RB;
+        const int gi0 = kb * GPT;
+        const int ng = (G_all - gi0) < GPT ? (G_all - gi0) : GPT;
+        while (issued < ntl && issued < li + S) issue_next();
+        const int s = li % S;
+        uint8_t* st = ring + s * F::STAGE_BYTES;
+        if (issued > li + 1) cp_async_wait_group<1>();
+        else cp_async_wait_group<0>();
+        __syncwarp();
+        RowPtrs<FMT> rp[2];
+        rp[0] = row_ptrs<FMT>(st, mc, g, n0 + g, kb);
+        rp[1] = row_ptrs<FMT>(st, mc, g + 8, n0 + g + 8, kb);
+#pragma unroll 1
+        for (int gg = 0; gg < ng; ++gg) {
+            int I0[8], I1[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) I0[m] = I1[m] = 0;
+#pragma unroll
+            for (int j = 0; j < GB; ++j) {
+                const int blk = gg * GB + j;                        // block within the tile
+                const int kk = kb * KT + blk * 16 + 4 * c;          // this lane's 4 k
+                uint32_t lo, hi;
+                if constexpr (FMT == UQ_INT8_SYM) {
+                    // chunk = 2 blocks; word 2b + h of the lane's 16 bytes = row g + 8h, k 4c .. 4c + 3 of block b
+                    const uint8_t* cp = st + (blk / BPCH) * CHUNK + lane * 16 + (blk % BPCH) * 8;
+                    const uint2 v = *reinterpret_cast<const uint2*>(cp);
+                    lo = v.x;
+                    hi = v.y;
+                } else {
+                    const uint32_t wd = *reinterpret_cast<const uint32_t*>(st + (blk / BPCH) * CHUNK + lane * 16 +
+                                                                           (blk % BPCH) * 4);
+                    lo = wd & 0x0F0F0F0Fu;                          // row g:     k, k+2, k+1, k+3
+                    hi = (wd >> 4) & 0x0F0F0F0Fu;                   // row g + 8: the same order
+                }
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    if (m < M) {
+                        const uint32_t xw = (kk < Kp) ? __ldg(reinterpret_cast<const uint32_t*>(xq + (long long)m * Kp + kk)) : 0u;
+                        I0[m] = dp4a_us(lo, xw, I0[m]);
+                        I1[m] = dp4a_us(hi, xw, I1[m]);
+                    }
+                }
+            }
+            // fold the group: acc += s * (I - zc * SX)
+            const int gi = gi0 + gg;
+#pragma unroll
+            for (int jr = 0; jr < 2; ++jr) {
+                float sc, zcf;
+                row_meta<FMT>(rp[jr], gg, sc, zcf);               // 4-bit: zcf = 128 + the stored code offset
+                const int zc = (FMT == UQ_INT8_SYM) ? 128 : (int)zcf - 128;   // INT8 codes are stored + 128
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    if (m < M) {
+                        const int sxv = __ldg(sxl + ((long long)m * Gq + gi) * 4 + c);
+                        const int I = (jr ? I1[m] : I0[m]) - zc * sxv;
+                        acc[jr][m] = fmaf(sc, (float)I, acc[jr][m]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        // the tile's partial sums: the 4 lanes of a row combined (fixed order), then stored like the mma GEMV's
+        float out[2][8];
+#pragma unroll
+        for (int jr = 0; jr < 2; ++jr)
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                float v = acc[jr][m];
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                out[jr][m] = v * sxm[m];
+                acc[jr][m] = 0.f;
+            }
+        if (c == 0) {
+            if (cta_rows) {
+                float* part = cpart + ((warp * MMA_TPW + li) * RB) * 8;
+#pragma unroll
+                for (int jr = 0; jr < 2; ++jr)
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) part[(g + 8 * jr) * 8 + m] = out[jr][m];
+            } else {
+                float* part = a.partials + i * RB * M;
+#pragma unroll
+                for (int jr = 0; jr < 2; ++jr)
+#pragma unroll
+                    for (int m = 0; m < 8; ++m)
+                        if (m < M) part[(g + 8 * jr) * M + m] = out[jr][m];
+            }
+        }
+    }
+    cp_async_wait_group<0>();
+    if (!cta_rows) return;
+    __syncthreads();
+    for (int e = threadIdx.x; e < R * RB * M; e += blockDim.x) {
+        const int rbi = e / (RB * M), rm = e % (RB * M), r = rm / M, m = rm % M;
+        const int n = (rb0 + rbi) * RB + r;
+        if (n >= a.N) continue;
+        float sum = 0.f;
+        for (int kbb = 0; kbb < L.KB; ++kbb) {
+            const unsigned ti = (unsigned)(kbb * R + rbi);
+            const unsigned w2 = ((ti + 1) * W - 1) / Tc;
+            const unsigned l2 = ti - w2 * Tc / W;
+            sum += cpart[((w2 * MMA_TPW + l2) * RB + r) * 8 + m];
+        }
+        store_out(a, m, n, sum);
+    }
+}
+
+namespace {
+template <int FMT, int GB>
+cudaError_t launch_a8_t(const GemvArgs& a, const int8_t* xq, const float* sxs, const int* sxl, int Kp, int grid,
+                        cudaStream_t st) {
+    static bool configured[64] = {};
+    const size_t smem = gemv_a8_smem_plan<FMT>().total;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(gemv_a8_kernel<FMT, GB>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    GemvArgs a2 = a;
+    a2.overlap = launch_overlap() ? 1 : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = a2.overlap ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, gemv_a8_kernel<FMT, GB>, a2, xq, sxs, sxl, Kp);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+template <int FMT>
+cudaError_t launch_a8_f(const GemvArgs& a, const int8_t* xq, const float* sxs, const int* sxl, int Kp, int grid,
+                        cudaStream_t st) {
+    switch (a.group) {
+        case 32: return launch_a8_t<FMT, 2>(a, xq, sxs, sxl, Kp, grid, st);
+        case 64: return launch_a8_t<FMT, 4>(a, xq, sxs, sxl, Kp, grid, st);
+        case 128: return launch_a8_t<FMT, 8>(a, xq, sxs, sxl, Kp, grid, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+}  // namespace
+
+size_t a8_smem_bytes(int fmt) {
+    switch (fmt) {
+        case UQ_INT4_SYM: return gemv_a8_smem_plan<UQ_INT4_SYM>().total;
+        case UQ_INT4_ASYM: return gemv_a8_smem_plan<UQ_INT4_ASYM>().total;
+        default: return gemv_a8_smem_plan<UQ_INT8_SYM>().total;
+    }
+}
+
+cudaError_t launch_quant_x(const uint16_t* x, int8_t* xq, float* sx, int* sxl, int M, int K, int Kp, int gs, int perm,
+                           cudaStream_t st) {
+    quant_x_kernel<<<M, 256, 0, st>>>(x, xq, sx, sxl, M, K, Kp, gs, perm);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_a8(int fmt, const GemvArgs& a, const int8_t* xq, const float* sxs, const int* sxl, int Kp,
+                           int grid, cudaStream_t st) {
+    cudaError_t e;
+    switch (fmt) {
+        case UQ_INT4_SYM: e = launch_a8_f<UQ_INT4_SYM>(a, xq, sxs, sxl, Kp, grid, st); break;
+        case UQ_INT4_ASYM: e = launch_a8_f<UQ_INT4_ASYM>(a, xq, sxs, sxl, Kp, grid, st); break;
+        case UQ_INT8_SYM: e = launch_a8_f<UQ_INT8_SYM>(a, xq, sxs, sxl, Kp, grid, st); break;
+        default: return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess || a.cta_rows) return e;
+    return launch_gemv_second_pass(a, grid, st);
+}
+
+}  // namespace uq

@@ -213,6 +213,26 @@ uq_status uq_rmsnorm_rope(const uint16_t* x, const uint16_t* gamma, const int32_
                           uint16_t* y, int M, int D, int head_dim, int max_pos, float eps, void* stream);
 
 /*
+ * uq_gemm_w4a8 -- the quantized linear layer with dynamically quantized activations ("Ultra LLM Engine",
+ * section "Quantized Model": activations dynamically quantized for the GEMV/GEMM paths; read as
+ * symmetric per-row int8):
+ *     s_x[m] = absmax_k |x[m][k]| / 127 (fp32),  xq = clamp(RNE(x / s_x), -127, 127) (fp32 quotient),
+ *     y[m][n] = bf16_RNE( s_x[m] * sum_g s[n][g] * sum_{k in g} xq[m][k] * (q[n][k] - z[n][g]) ),
+ * the inner sums exact integers (dp4a), the per-group scaling and the sum over groups in fp32.
+ * Weights: UQ_INT4_SYM, UQ_INT4_ASYM (W4A8) or UQ_INT8_SYM (W8A8), as uq_gemm takes them.  Arguments,
+ * layouts, errors and scratch as uq_gemm (the x codes, s_x and the per-group code sums live in the
+ * per-stream workspace).  Launches: the activation quantization, then per block of 8 rows of x the
+ * integer GEMV (plus its second pass when the work split shares row blocks between CTAs);
+ * uq_gemm_w4a8_kernel_count gives the total.  The result differs from uq_gemm's by the activation
+ * quantization: that is the method, not an error.
+ */
+uq_status uq_gemm_w4a8(const uint16_t* x, const void* wq, const void* scales, const void* zeros, uint16_t* y,
+                       int M, int N, int K, int group, uq_fmt fmt, void* stream);
+
+/* uq_gemm_w4a8_kernel_count -- kernels one uq_gemm_w4a8 call of this shape launches. */
+uq_status uq_gemm_w4a8_kernel_count(int M, int N, int K, int group, uq_fmt fmt, int* count);
+
+/*
  * uq_unpack_codes -- debug: packed plane -> int8 codes [N][K] (device), bit-exact
  * inverse of uq_pack_layout.  It decodes every code word with the register unpacking
  * the GEMV and tensor-core kernels run (shift + lop3 magic-exponent pairs for 4- and
