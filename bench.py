@@ -14,7 +14,7 @@ same JSON line carries a `sweep` of the other workloads (the batched-decode M sw
 8192 x 8192 format sweep and the 70B-shaped two-level INT4 stack), each timed on its own graph.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl uq|reference] [--workload NAME] [--m M]
-                    [--no-sweep] [--no-cpu-baseline]
+                    [--gated] [--no-sweep] [--no-cpu-baseline]
 
 Under torchrun each rank runs an independent replica on its own GPU (the path has no
 exchange step); value = bytes of all ranks / max-over-ranks time ("weak" scaling).
@@ -59,12 +59,19 @@ WORKLOADS = {
                      linears=[("w", 8192, 8192)], m=1, title="8192x8192 NF4 g64"),
     "k4-70b-stack": dict(fmt="K4", group=256, sigma=0.015, outlier_p=0.0, layers=8, linears=_L70, m=1,
                          title="70B-shaped decode linear stack (8 layers x 7), two-level INT4"),
+    "w4a8-sweep": dict(fmt="INT4_ASYM", group=128, sigma=0.02, outlier_p=0.0, layers=8,
+                       linears=[("gate", 14336, 4096), ("down", 4096, 14336)], m=1, mode="w4a8",
+                       title="W4A8 (dynamic per-row int8 x, dp4a): 14336x4096 and 4096x14336, INT4 asym g128"),
+    "q4_0-8192": dict(fmt="INT4_SYM", group=32, sigma=0.01, outlier_p=0.0, layers=8, linears=[("w", 8192, 8192)],
+                      m=1, source="gguf:Q4_0", title="8192x8192 GGUF Q4_0 blocks (repacked, INT4_SYM g32)"),
 }
 # The sweep carried in the default line: (workload, layers = weight copies per graph, M values).
 # Every graph streams more packed weight bytes than L2 holds, so each replay reads them from HBM.
 SWEEP = [("sweep-int4a", 8, (1, 2, 4, 8, 16, 32, 64)),
          ("int8s-8192", 8, (1, 16)), ("int2a-8192", 16, (1, 16)), ("nf4-8192", 8, (1, 16)),
-         ("k4-70b-stack", 8, (1, 8, 32))]
+         ("k4-70b-stack", 8, (1, 8, 32)), ("w4a8-sweep", 8, (1, 8)), ("q4_0-8192", 8, (1, 16))]
+# the decode step again, with each layer's gate and up linears as one gated op (uq_gemm_gated)
+SWEEP_GATED = [("llama8b-int4a-decode", 8, (1, 4))]
 # linears that read the same input as the linear before them in a decoder layer
 SHARES_INPUT_WITH_PREVIOUS = ("k", "v", "up")
 BITS = {"INT4_SYM": 4, "INT4_ASYM": 4, "INT8_SYM": 8, "INT2_ASYM": 2, "NF4": 4, "K4": 4}
@@ -258,6 +265,16 @@ def build_weights(spec, dev, layers=None, seed_base=12345):
     for layer in range(layers or spec["layers"]):
         for name, N, K in spec["linears"]:
             gen.manual_seed(seed_base + idx)
+            if spec.get("source") == "gguf:Q4_0":
+                # random GGUF Q4_0 blocks (any byte pattern is a valid block) with an fp16 d, repacked
+                raw = torch.randint(0, 256, (N, K // 32, 18), generator=gen, device=dev, dtype=torch.int32).to(torch.uint8)
+                d = (torch.randn((N, K // 32), generator=gen, device=dev) * spec["sigma"]).half().view(torch.uint8)
+                raw[..., 0:2] = d.view(N, K // 32, 2)
+                wq, scales = uq.pack_gguf(raw.contiguous(), "Q4_0", N, K)
+                del raw, d
+                recs.append(dict(name=f"L{layer}.{name}", N=N, K=K, wq=wq, scales=scales, zc=None))
+                idx += 1
+                continue
             w = torch.randn((N, K), generator=gen, device=dev, dtype=torch.float32) * spec["sigma"]
             if spec["outlier_p"] > 0:
                 mask = torch.rand((N, K), generator=gen, device=dev) < spec["outlier_p"]
@@ -310,9 +327,10 @@ class Step:
     reading the same input on parallel branches), and its CUDA graph.  With `gated`, a layer's gate
     and up linears are one op: uq_gemm_gated, h = silu(x Wg^T) * (x Wu^T)."""
 
-    def __init__(self, recs, fmt, group, M, dev, stream, seed, gated=True):
+    def __init__(self, recs, fmt, group, M, dev, stream, seed, gated=False, mode="gemm"):
         import torch
         self.recs, self.fmt, self.group, self.M, self.stream = recs, fmt, group, M, stream
+        self.mode = mode                          # "gemm" (bf16 x) or "w4a8" (per-row int8 x)
         self.ops = step_ops(recs, gated)
         x_sizes = [M * op["K"] for op in self.ops]
         y_sizes = [M * op["N"] for op in self.ops]
@@ -350,8 +368,8 @@ class Step:
                                op["N"], op["K"], self.group, self.fmt, st.cuda_stream)
         else:
             w, sc, zc = ptrs(op["recs"][0])
-            uq.gemm_ptrs(x.data_ptr(), w, sc, zc, y.data_ptr(), self.M, op["N"], op["K"], self.group, self.fmt,
-                         st.cuda_stream)
+            f = uq.gemm_w4a8_ptrs if self.mode == "w4a8" else uq.gemm_ptrs
+            f(x.data_ptr(), w, sc, zc, y.data_ptr(), self.M, op["N"], op["K"], self.group, self.fmt, st.cuda_stream)
 
     def issue(self):
         import torch
@@ -405,39 +423,89 @@ class Step:
         for op in self.ops:
             if op["kind"] == "gated":
                 n += uq.gemm_gated_kernel_count(self.M, op["N"], op["K"], self.group, self.fmt)
+            elif self.mode == "w4a8":
+                n += uq.gemm_w4a8_kernel_count(self.M, op["N"], op["K"], self.group, self.fmt)
             else:
                 n += kernels_per_call(self.fmt, self.group, self.M, op["N"], op["K"])
         return n
 
 
-def run_sweep(dev, stream, hbm, tf, gated=True):
-    """The M sweep, the format sweep and the 70B-shaped stack, each point on its own graph."""
+def run_sweep(dev, stream, hbm, tf):
+    """The M sweep, the format sweep, the 70B-shaped stack and the gated decode step, each point on
+    its own graph."""
     import torch
     out = []
-    for wl, layers, ms in SWEEP:
+    for wl, layers, ms, gated in [p + (False,) for p in SWEEP] + [p + (True,) for p in SWEEP_GATED]:
         spec = WORKLOADS[wl]
         fmt, group = spec["fmt"], spec["group"]
         recs = build_weights(spec, dev, layers=layers, seed_base=20000)
         shapes = sorted({(r["N"], r["K"]) for r in recs})
         for M in ms:
-            st = Step(recs, fmt, group, M, dev, stream, seed=4242 + M, gated=gated).capture()
+            mode = spec.get("mode", "gemm")
+            st = Step(recs, fmt, group, M, dev, stream, seed=4242 + M, gated=gated, mode=mode).capture()
             probe = st.time(3, 2)
             reps = int(min(200, max(5, 25.0 / max(probe, 1e-3))))
             ms_ = st.time(3, reps)
             t_roof = roofline_time_s(st.bytes, st.flops, hbm, tf)
             out.append({"workload": wl, "fmt": fmt, "group": group, "M": M, "linears": len(recs),
-                        "ops": len(st.ops),
+                        "ops": len(st.ops), "gated": gated,
                         "shapes": [f"{n}x{k}" for n, k in shapes],
                         "GB/s": round(st.bytes / (ms_ * 1e-3) / 1e9, 1),
                         "TFLOP/s": round(st.flops / (ms_ * 1e-3) / 1e12, 2),
                         "frac": round(t_roof / (ms_ * 1e-3), 4),
                         "bound": "hbm" if st.bytes / (hbm * 1e9) >= st.flops / (tf * 1e12) else "tensor",
                         "us_per_linear": round(ms_ * 1e3 / len(recs), 2),
-                        "kernel": dominant_kernel(fmt, group, M, shapes), "launches": st.launches(),
+                        "kernel": (f"gemv_a8_kernel<{fmt}>" if mode == "w4a8" else dominant_kernel(fmt, group, M, shapes)),
+                        "launches": st.launches(),
                         "reps": reps})
             del st
         del recs
         torch.cuda.empty_cache()
+    out.extend(run_rope_points(dev, stream, hbm))
+    return out
+
+
+def run_rope_points(dev, stream, hbm):
+    """The fused RMSNorm + RoPE: a bulk case (8192 rows of 4096, bandwidth) and a decode row (latency)."""
+    import torch
+    import gemm_uq_gb300 as uq
+    out = []
+    D, hd, max_pos = 4096, 128, 8192
+    table = uq.rope_table(max_pos, hd, 500000.0, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(31337)
+    gamma = (1.0 + 0.1 * torch.randn(D, generator=g, device=dev)).to(torch.bfloat16)
+    for M, copies in ((8192, 4), (1, 64)):
+        xs = [torch.randn((M, D), generator=g, device=dev).to(torch.bfloat16) for _ in range(copies)]
+        ys = [torch.empty_like(x) for x in xs]
+        pos = torch.randint(0, max_pos, (M,), generator=g, device=dev, dtype=torch.int32)
+        with torch.cuda.stream(stream):
+            for x, y in zip(xs, ys):
+                uq.rmsnorm_rope(x, gamma, pos, table, hd, 1e-5, y=y, stream=stream)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for x, y in zip(xs, ys):
+                uq.rmsnorm_rope(x, gamma, pos, table, hd, 1e-5, y=y, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                graph.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        reps = 20
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) * 1e-3 / (reps * copies)
+        nbytes = 2 * M * D * 2 + D * 2 + M * 4 + M * (hd // 2) * 8       # x, y, gamma, positions, table rows
+        out.append({"workload": "rmsnorm-rope", "M": M, "D": D, "head_dim": hd, "GB/s": round(nbytes / t / 1e9, 1),
+                    "frac": round(nbytes / t / 1e9 / hbm, 4), "us_per_call": round(t * 1e6, 2),
+                    "kernel": "rmsnorm_rope_kernel", "launches": copies})
+        del xs, ys
     return out
 
 
@@ -456,7 +524,7 @@ def run_uq(args, rank, world, dist):
     # consecutive linears of a decode step read fixed weights: let each launch stream its weights
     # while the previous one drains (uq_set_launch_overlap)
     uq.set_launch_overlap(not args.no_overlap)
-    step = Step(recs, fmt, group, M, dev, stream, seed=777 + rank, gated=not args.no_gated).capture()
+    step = Step(recs, fmt, group, M, dev, stream, seed=777 + rank, gated=args.gated).capture()
 
     step.replay(args.warmup)
     torch.cuda.synchronize()
@@ -510,7 +578,7 @@ def run_uq(args, rank, world, dist):
     if world == 1 and not args.no_sweep:
         del step, recs
         torch.cuda.empty_cache()
-        sweep = run_sweep(dev, stream, *measured_peaks()[:2], gated=not args.no_gated)
+        sweep = run_sweep(dev, stream, *measured_peaks()[:2])
     if rank != 0:
         return
     out = report(args, spec, M, world, ms, e2e_ms, clocks, info, sweep)
@@ -684,7 +752,8 @@ def main():
     ap.add_argument("--no-sweep", action="store_true", help="leave the sweep workloads out of the line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-overlap", action="store_true", help="launch without programmatic dependent launch")
-    ap.add_argument("--no-gated", action="store_true", help="gate and up as two separate uq_gemm launches")
+    ap.add_argument("--gated", action="store_true",
+                    help="each layer's gate and up linears as one uq_gemm_gated op instead of two uq_gemm")
     ap.add_argument("--oracle-leg", default=None, help=argparse.SUPPRESS)
     ap.add_argument("--oracle-seconds", type=float, default=10.0, help=argparse.SUPPRESS)
     ap.add_argument("--oracle-rows", type=int, default=512, help=argparse.SUPPRESS)
