@@ -34,6 +34,7 @@ SIGNATURES = {
     "uq_pack_zeros": (_I, [_P, _P, _I, _I, _P]),
     "uq_device_fault": (_I, [ctypes.POINTER(ctypes.c_uint)]),
     "uq_gemm_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
+    "uq_gemm_noalloc_scratch": (_I, [_I, _I, _I, _I, _I, _SZ, _SZ]),
     "uq_set_launch_overlap": (_I, [_I]),
     "uq_gemm_kernel_count": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I)]),
     "uq_gemm_gated": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
@@ -230,6 +231,15 @@ def gemm_noalloc(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, zc, N:
     _check(lib().uq_gemm_noalloc(_ptr(x), _ptr(wq), _ptr(scales), _ptr(zc), _ptr(y), M, N, K, group, FORMATS[fmt],
                                  _stream(stream)), "uq_gemm_noalloc")
     return y
+
+
+def gemm_noalloc_scratch(M: int, N: int, K: int, group: int, fmt: str):
+    """uq_gemm_noalloc_scratch: (ticket_bytes, partial_bytes) of the static scratch the call would use
+    (host only; 0, 0 when every worker owns whole row blocks)."""
+    t, p = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().uq_gemm_noalloc_scratch(M, N, K, group, FORMATS[fmt], ctypes.byref(t), ctypes.byref(p)),
+           "uq_gemm_noalloc_scratch")
+    return t.value, p.value
 
 
 def gemm_ptrs(x_ptr: int, wq_ptr: int, scales_ptr: int, zc_ptr, y_ptr: int, M: int, N: int, K: int, group: int,

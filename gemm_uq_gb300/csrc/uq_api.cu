@@ -177,53 +177,49 @@ uq_status run_gemv(const uint16_t* x, const void* wq, const void* scales, const 
                    int Mb, int N, int K, int ldx, int ldy, int group, int fmt, cudaStream_t st,
                    const DeviceState& ds, int dev, OutMode om = OutMode()) {
     const uq::Layout L(N, K, fmt);
-    if (uq::gemv_smem_bytes(fmt, K, group, Mb) > 227 * 1024)
-        return fail(UQ_ERR_UNSUPPORTED, "K=%d is too long for the GEMV's shared-memory x-sum table at M=%d", K, Mb);
-    const long long T = (long long)L.NB * L.KB;
-    const int warps = uq::gemv_warps(fmt);
-    long long P = (long long)ds.sms * uq::gemv_ctas_per_sm(fmt) * warps;
-    if (P > T) P = T;
+    uq::GemvArgs a = {};
+    a.M = Mb; a.N = N; a.K = K; a.group = group; a.ldx = ldx; a.ldy = ldy;
+    a.NB = L.NB; a.KB = L.KB; a.T = (long long)L.NB * L.KB;
+    const int grid = uq::gemv_plan(a, fmt, ds.sms);
+    if (grid == 0)
+        return fail(UQ_ERR_UNSUPPORTED, "K=%d is too long for the GEMV's shared memory at M=%d", K, Mb);
     Workspace* ws = nullptr;
-    uq_status s = workspace(dev, st, uq::gemv_partials_floats(fmt, T, (int)P, Mb) * sizeof(float),
+    uq_status s = workspace(dev, st, uq::gemv_partials_floats(fmt, a) * sizeof(float),
                             (size_t)L.NB * sizeof(unsigned int), &ws);
     if (s != UQ_OK) return s;
-    uq::GemvArgs a = {};
     a.x = x;
     a.wq = static_cast<const uint8_t*>(wq);
     a.scales = static_cast<const uint8_t*>(scales);
     a.zc = static_cast<const uint8_t*>(zc);
     a.y = y;
-    a.M = Mb; a.N = N; a.K = K; a.group = group; a.ldx = ldx; a.ldy = ldy;
-    a.NB = L.NB; a.KB = L.KB; a.T = T; a.P = (int)P;
     a.partials = ws->partials;
     a.tickets = ws->tickets;
     a.fault = ds.words;
-    a.overlap = 0;
     a.out32 = om.out32;
     a.gate32 = om.gate32;
-    const int grid = uq::gemv_grid(a, fmt, ds.sms);
     cudaError_t e = uq::launch_gemv(fmt, a, grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "GEMV launch");
     return UQ_OK;
 }
 
 
-// the gated projection for Mb <= 8 rows of x in one mma-GEMV launch (plus the second pass when the
-// work split shares row blocks between CTAs): gate and up row blocks interleaved in one work list
+// the gated projection for Mb <= 8 rows of x in one mma-GEMV launch: gate and up row blocks
+// interleaved in one work list, every CTA owning whole gate/up pairs
 uq_status run_gemv_gated(const uint16_t* x, const void* wg, const void* sg, const void* zg, const void* wu,
                          const void* su, const void* zu, uint16_t* h, int Mb, int N, int K, int ldx, int ldy,
                          int group, int fmt, cudaStream_t st, const DeviceState& ds, int dev) {
     const uq::Layout L(N, K, fmt);
-    if (uq::gemv_smem_bytes(fmt, K, group, Mb) > 227 * 1024)
-        return fail(UQ_ERR_UNSUPPORTED, "K=%d is too long for the GEMV's shared-memory x-sum table at M=%d", K, Mb);
-    const long long T = 2LL * L.NB * L.KB;
-    long long P = (long long)ds.sms * uq::gemv_ctas_per_sm(fmt) * uq::gemv_warps(fmt);
-    if (P > T) P = T;
+    uq::GemvArgs a = {};
+    a.gated = 1;
+    a.M = Mb; a.N = N; a.K = K; a.group = group; a.ldx = ldx; a.ldy = ldy;
+    a.NB = 2 * L.NB; a.KB = L.KB; a.T = 2LL * L.NB * L.KB;
+    const int grid = uq::gemv_plan(a, fmt, ds.sms);
+    if (grid == 0)
+        return fail(UQ_ERR_UNSUPPORTED, "K=%d is too long for the GEMV's shared memory at M=%d", K, Mb);
     Workspace* ws = nullptr;
-    uq_status s = workspace(dev, st, uq::gemv_partials_floats(fmt, T, (int)P, Mb) * sizeof(float),
+    uq_status s = workspace(dev, st, uq::gemv_partials_floats(fmt, a) * sizeof(float),
                             (size_t)L.NB * sizeof(unsigned int), &ws);
     if (s != UQ_OK) return s;
-    uq::GemvArgs a = {};
     a.x = x;
     a.wq = static_cast<const uint8_t*>(wg);
     a.scales = static_cast<const uint8_t*>(sg);
@@ -231,14 +227,10 @@ uq_status run_gemv_gated(const uint16_t* x, const void* wg, const void* sg, cons
     a.wq2 = static_cast<const uint8_t*>(wu);
     a.scales2 = static_cast<const uint8_t*>(su);
     a.zc2 = static_cast<const uint8_t*>(zu);
-    a.gated = 1;
     a.y = h;
-    a.M = Mb; a.N = N; a.K = K; a.group = group; a.ldx = ldx; a.ldy = ldy;
-    a.NB = 2 * L.NB; a.KB = L.KB; a.T = T; a.P = (int)P;
     a.partials = ws->partials;
     a.tickets = ws->tickets;
     a.fault = ds.words;
-    const int grid = uq::gemv_grid(a, fmt, ds.sms);
     cudaError_t e = uq::launch_gemv(fmt, a, grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "gated GEMV launch");
     return UQ_OK;
@@ -506,14 +498,12 @@ uq_status uq_gemm_gated_kernel_count(int M, int N, int K, int group, uq_fmt fmt,
     if (e != cudaSuccess || sms < 1) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice, "SM count");
     const uq::Layout L(N, K, fmt);
     int n = 0;
-    for (int m0 = 0; m0 < M; m0 += 8) {                     // per block of 8 rows: one launch, + the second pass
+    for (int m0 = 0; m0 < M; m0 += 8) {                     // per block of 8 rows: one launch
         uq::GemvArgs a = {};
         a.M = (M - m0) < 8 ? (M - m0) : 8; a.N = N; a.K = K; a.group = group;
         a.gated = 1; a.NB = 2 * L.NB; a.KB = L.KB; a.T = (long long)a.NB * L.KB;
-        const long long P = (long long)sms * uq::gemv_ctas_per_sm(fmt) * uq::gemv_warps(fmt);
-        a.P = (int)(P > a.T ? a.T : P);
-        uq::gemv_grid(a, fmt, sms);
-        n += 1 + (a.cta_rows ? 0 : 1);
+        uq::gemv_plan(a, fmt, sms);
+        n += uq::gemv_launches(fmt, a);
     }
     *count = n;
     return UQ_OK;
@@ -565,12 +555,10 @@ uq_status uq_pack_gguf(const void* blocks, uq_gguf_type type, void* wq, uint16_t
 
 namespace {
 bool a8_format(int fmt) { return fmt == UQ_INT4_SYM || fmt == UQ_INT4_ASYM || fmt == UQ_INT8_SYM; }
-// the work split of one A8 GEMV launch over Mb rows (the mma GEMV's rules)
-void a8_args(uq::GemvArgs& a, const uq::Layout& L, int Mb, int N, int K, int group, int sms) {
+// the shape fields of one A8 GEMV launch over Mb rows (gemv_plan then sets the work split)
+void a8_args(uq::GemvArgs& a, const uq::Layout& L, int Mb, int N, int K, int group) {
     a.M = Mb; a.N = N; a.K = K; a.group = group; a.a8 = 1;
     a.NB = L.NB; a.KB = L.KB; a.T = (long long)L.NB * L.KB;
-    const long long P = (long long)sms * 2 * 4;
-    a.P = (int)(P > a.T ? a.T : P);
 }
 }  // namespace
 
@@ -612,7 +600,7 @@ uq_status uq_gemm_w4a8(const uint16_t* x, const void* wq, const void* scales, co
     for (int m0 = 0; m0 < M; m0 += 8) {
         const int mb = (M - m0) < 8 ? (M - m0) : 8;
         uq::GemvArgs a = {};
-        a8_args(a, L, mb, N, K, group, ds->sms);
+        a8_args(a, L, mb, N, K, group);
         a.x = x;
         a.wq = static_cast<const uint8_t*>(wq);
         a.scales = static_cast<const uint8_t*>(scales);
@@ -622,7 +610,7 @@ uq_status uq_gemm_w4a8(const uint16_t* x, const void* wq, const void* scales, co
         a.partials = ws->partials;
         a.tickets = ws->tickets;
         a.fault = ds->words;
-        const int grid = uq::gemv_grid(a, fmt, ds->sms);
+        const int grid = uq::gemv_plan(a, fmt, ds->sms);
         e = uq::launch_gemv_a8(fmt, a, xq + (long long)m0 * Kp, sx + m0, sxl + (long long)m0 * G * 4, Kp, grid, st);
         if (e != cudaSuccess) return cuda_fail(e, "W4A8 GEMV launch");
     }
@@ -646,9 +634,9 @@ uq_status uq_gemm_w4a8_kernel_count(int M, int N, int K, int group, uq_fmt fmt, 
     int n = 1;                                                   // the activation quantization
     for (int m0 = 0; m0 < M; m0 += 8) {
         uq::GemvArgs a = {};
-        a8_args(a, L, (M - m0) < 8 ? (M - m0) : 8, N, K, group, sms);
-        uq::gemv_grid(a, fmt, sms);
-        n += 1 + (a.cta_rows ? 0 : 1);
+        a8_args(a, L, (M - m0) < 8 ? (M - m0) : 8, N, K, group);
+        uq::gemv_plan(a, fmt, sms);
+        n += uq::gemv_launches(fmt, a);
     }
     *count = n;
     return UQ_OK;
@@ -735,18 +723,15 @@ uq_status uq_gemm_kernel_count(int M, int N, int K, int group, uq_fmt fmt, int* 
         // per block of at most 64 rows: the GEMM (K4: after its x column-sum pre-kernel)
         for (int m0 = 0; m0 < M; m0 += 64) n += (fmt == UQ_K4) ? 2 : 1;
     } else {
-        // per block of at most 8 rows: the GEMV and, when its work split needs it, the second pass
+        // per block of at most 8 rows: one GEMV launch
         const uq::Layout L(N, K, fmt);
         for (int m0 = 0; m0 < M; m0 += 8) {
             const int mb = (M - m0) < 8 ? (M - m0) : 8;
             uq::GemvArgs a = {};
             a.M = mb; a.N = N; a.K = K; a.group = group;
             a.NB = L.NB; a.KB = L.KB; a.T = (long long)L.NB * L.KB;
-            long long P = (long long)sms * uq::gemv_ctas_per_sm(fmt) * uq::gemv_warps(fmt);
-            a.P = (int)(P > a.T ? a.T : P);
-            uq::gemv_grid(a, fmt, sms);
-            const bool mma = fmt == UQ_INT4_SYM || fmt == UQ_INT4_ASYM || fmt == UQ_INT2_ASYM || fmt == UQ_K4;
-            n += 1 + ((mma && !a.cta_rows) ? 1 : 0);
+            uq::gemv_plan(a, fmt, sms);
+            n += uq::gemv_launches(fmt, a);
         }
     }
     *count = n;

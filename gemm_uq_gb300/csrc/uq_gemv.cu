@@ -10,16 +10,23 @@ extern template cudaError_t launch_gemv_fmt<UQ_INT2_ASYM>(const GemvArgs&, int, 
 extern template cudaError_t launch_gemv_fmt<UQ_NF4>(const GemvArgs&, int, cudaStream_t);
 extern template cudaError_t launch_gemv_fmt<UQ_K4>(const GemvArgs&, int, cudaStream_t);
 
-size_t gemv_smem_bytes(int fmt, int K, int group, int M) { return gemv_smem_bytes_impl(fmt, K, group, M); }
-int gemv_warps(int fmt) { return gemv_warps_impl(fmt); }
-int gemv_grid(GemvArgs& a, int fmt, int sms) {
+int gemv_plan(GemvArgs& a, int fmt, int sms) {
     a.cta_rows = 0;
-    if (!gemv_is_mma(fmt) && !a.a8) return (a.P + GEMV_WARPS - 1) / GEMV_WARPS;
-    // Whole row blocks per CTA need no second pass; take them when no warp gets more tiles than
-    // under the stream-K split and either the busiest CTA streams at most ~6 % more bytes than the
-    // average one (bandwidth-bound shapes) or no warp has more than one tile (latency-bound ones).
-    // (gated: the units CTAs own are gate/up pairs of row blocks)
-    const int W = a.a8 ? 4 : gemv_warps(fmt);
+    if (!gemv_is_mma(fmt) && !a.a8) {
+        if (gemv_smem_bytes_impl(fmt, a.K, a.group, a.M) > 227 * 1024) return 0;
+        const long long P = (long long)sms * GEMV_WARPS;
+        a.P = (int)(P < a.T ? P : a.T);
+        return (a.P + GEMV_WARPS - 1) / GEMV_WARPS;
+    }
+    if (!a.a8 && gemv_smem_bytes_impl(fmt, a.K, a.group, a.M) > 227 * 1024) return 0;
+    // mma and W4A8 GEMVs: W warps per CTA, two CTAs per SM.  Whole row blocks per CTA need no second
+    // pass; take them when no warp gets more tiles than under the stream-K split and either the
+    // busiest CTA streams at most ~6 % more bytes than the average one (bandwidth-bound shapes) or
+    // no warp has more than one tile (latency-bound ones).  (gated: the units CTAs own are gate/up
+    // pairs of row blocks)
+    const int W = a.a8 ? 4 : gemv_warps_impl(fmt);
+    const long long P = (long long)sms * MMA_CTAS_PER_SM * W;
+    a.P = (int)(P < a.T ? P : a.T);
     const int WU = a.gated ? 2 : 1;
     const int NBU = a.NB / WU;
     const int slots = sms * MMA_CTAS_PER_SM;                           // CTAs resident at once
@@ -34,11 +41,16 @@ int gemv_grid(GemvArgs& a, int fmt, int sms) {
     }
     return a.P < slots ? a.P : slots;
 }
-int gemv_ctas_per_sm(int fmt) { return gemv_ctas_per_sm_impl(fmt); }
-size_t gemv_partials_floats(int fmt, long long T, int P, int M) {
-    // mma GEMV: one 16-row slot per tile (k-major tiles, summed over k by the second pass);
+
+size_t gemv_partials_floats(int fmt, const GemvArgs& a) {
+    // mma / W4A8 GEMV: one 16-row slot per tile (k-major tiles, summed over k by the second pass);
     // CUDA-core GEMV: two slots per worker (the first and last row block of its range)
-    return gemv_is_mma(fmt) ? (size_t)T * RB * M : gemv_partials_floats_impl(P, M);
+    if (gemv_is_mma(fmt) || a.a8) return a.cta_rows ? 0 : (size_t)a.T * RB * a.M;
+    return gemv_partials_floats_impl(a.P, a.M);
+}
+bool gemv_uses_tickets(int fmt, const GemvArgs& a) { return !gemv_is_mma(fmt) && !a.a8; }
+int gemv_launches(int fmt, const GemvArgs& a) {
+    return ((gemv_is_mma(fmt) || a.a8) && !a.cta_rows) ? 2 : 1;
 }
 
 // Second pass of the mma GEMV when workers split the matrix's tiles (k-major, so every tile's

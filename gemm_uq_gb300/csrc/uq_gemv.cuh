@@ -182,7 +182,8 @@ struct GemvSrc {
 // cp.async group per lane that the issuing warp itself waits for (`bar` unused).  The per-lane
 // copies keep more of the tile stream in flight than one 8 KB bulk copy per tile: the copy engine
 // takes bulk copies one after another, at well under an SM's share of HBM bandwidth at this size.
-template <int FMT, bool GROUP = false>
+// GTC: the groups per tile row when the caller knows them at compile time (0: mc.GT at run time).
+template <int FMT, bool GROUP = false, int GTC = 0>
 __device__ __forceinline__ void issue_tile(const GemvArgs& a, const GemvSrc& w, const Layout& L, const MetaConst& mc, int nb, int kb,
                                            uint8_t* st, uint64_t* bar, int lane) {
     using F = GemvFmt<FMT>;
@@ -201,19 +202,20 @@ __device__ __forceinline__ void issue_tile(const GemvArgs& a, const GemvSrc& w, 
     } else if (mc.aligned) {
         // scale slices of GT halves (16-byte multiples, 16-byte aligned): 16-byte copies; INT4
         // zero slices of GT/2 bytes: 4-byte copies; INT2 zero slices like the scales
-        const int sv = mc.GT / 8;                       // 16-byte vectors of scales per row
-        const int zv = (FMT == UQ_INT4_ASYM) ? mc.GT / 8 : ((FMT == UQ_INT2_ASYM) ? sv : 0);
+        const int GT = GTC ? GTC : mc.GT;
+        const int sv = GT / 8;                          // 16-byte vectors of scales per row
+        const int zv = (FMT == UQ_INT4_ASYM) ? GT / 8 : ((FMT == UQ_INT2_ASYM) ? sv : 0);
         const int per = sv + zv;
         for (int e = lane; e < rows * per; e += 32) {
             const int r = e / per, j = e % per;
             const long long n = n0 + r;
             if (j < sv) {
-                cp_async16(md + r * F::MW + 4 * j, w.scales + (n * mc.G + (long long)kb * mc.GT) * 2 + 16 * j);
+                cp_async16(md + r * F::MW + 4 * j, w.scales + (n * mc.G + (long long)kb * GT) * 2 + 16 * j);
             } else if constexpr (FMT == UQ_INT4_ASYM) {
                 cp_async4(md + r * F::MW + F::SW + (j - sv),
-                          w.zc + n * mc.ZB + (long long)kb * (mc.GT >> 1) + 4 * (j - sv));
+                          w.zc + n * mc.ZB + (long long)kb * (GT >> 1) + 4 * (j - sv));
             } else if constexpr (FMT == UQ_INT2_ASYM) {
-                cp_async16(md + r * F::MW + F::SW + 4 * (j - sv), w.zc + (n * mc.G + (long long)kb * mc.GT) * 2 + 16 * (j - sv));
+                cp_async16(md + r * F::MW + F::SW + 4 * (j - sv), w.zc + (n * mc.G + (long long)kb * GT) * 2 + 16 * (j - sv));
             }
         }
     } else {
@@ -765,11 +767,14 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
     int issued = 0;                                                 // tiles requested so far
     // the weight and weight row block of a work row block
     const GemvSrc src_gate{a.wq, a.scales, a.zc}, src_up{a.wq2, a.scales2, a.zc2};
+    // k-major tile coordinates (k tile, row block index in [0, R)) are advanced incrementally: a
+    // 64-bit division per tile would cost more than the tile's scale folds
+    int ikb = ntl > 0 ? kb_of(t0) : 0, irb = ntl > 0 ? (int)(t0 % R) : 0;   // the next tile to request
     auto issue_next = [&]() {
-        const long long i = t0 + issued;
-        const int nbw = nb_of(i);
-        issue_tile<FMT, true>(a, (GATED && (nbw & 1)) ? src_up : src_gate, L, mc, GATED ? nbw >> 1 : nbw, kb_of(i),
-                              ring + (issued % S) * F::STAGE_BYTES, &bars[issued % S], lane);
+        const int nbw = rb0 + irb;
+        issue_tile<FMT, true, GPT>(a, (GATED && (nbw & 1)) ? src_up : src_gate, L, mc, GATED ? nbw >> 1 : nbw, ikb,
+                                   ring + (issued % S) * F::STAGE_BYTES, &bars[issued % S], lane);
+        if (++irb == R) { irb = 0; ++ikb; }
         ++issued;
     };
     // Only the first tile before the sums of x of the first run: at the start every warp of the
@@ -810,9 +815,11 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
     const uint8_t* xt = nullptr;                 // this lane's x at the current k tile's first k
     const uint16_t* xgt = xgrow;
 
+    int ckb = ntl > 0 ? kb_of(t0) : 0, crb = ntl > 0 ? (int)(t0 % R) : 0;   // the tile being consumed
     for (int li = 0; li < ntl; ++li) {
         const long long i = t0 + li;
-        const int kb = kb_of(i), nb = GATED ? nb_of(i) >> 1 : nb_of(i);
+        const int kb = ckb, nb = GATED ? (rb0 + crb) >> 1 : rb0 + crb;
+        if (++crb == R) { crb = 0; ++ckb; }
         const int n0 = nb * RB;
         const int gi0 = kb * GPT;
         const int ng = (G_all - gi0) < GPT ? (G_all - gi0) : GPT;   // groups of the tile inside K
@@ -1066,7 +1073,6 @@ inline int gemv_warps_impl(int fmt) {
     }
 }
 inline size_t gemv_partials_floats_impl(int P, int M) { return (size_t)2 * P * RB * M; }
-inline int gemv_ctas_per_sm_impl(int fmt) { return gemv_is_mma(fmt) ? MMA_CTAS_PER_SM : 1; }
 
 namespace gemv_detail {
 template <int FMT, int M, bool XS>

@@ -46,12 +46,14 @@ struct GemvArgs {
     int NB, KB;               // row blocks, k tiles
     long long T;              // tiles = NB * KB
     int P;                    // workers (warps), P <= T
-    float* partials;          // fp32 split-K partial sums: [T][16][M] (mma GEMV), [2P][16][M] (CUDA cores)
+    float* partials;          // fp32 split-K partial sums: [T][16][M] (mma and W4A8 GEMVs, summed by the
+                              // second pass), [2P][16][M] (CUDA-core GEMV: first and last row block of
+                              // each worker)
     unsigned int* tickets;    // [NB], zero between calls
     unsigned int* fault;      // device fault word
     int overlap;              // launched with programmatic stream serialization (set by the launcher)
-    int cta_rows;             // mma GEMV: 1 = every CTA owns whole row blocks (combined in shared memory,
-                              // no second pass); 0 = workers split row blocks anywhere (second pass)
+    int cta_rows;             // mma / W4A8 GEMV: 1 = every CTA owns whole row blocks (combined in shared
+                              // memory, no second pass); 0 = workers split row blocks anywhere (second pass)
     float* out32;             // gate pass of the gated projection: fp32 results [M][ldy] instead of y
     const float* gate32;      // up pass: y = bf16(silu(gate32) * result), gate32 [M][ldy] fp32
     int gated;                // mma GEMV only: the gated projection in one launch; (wq, scales, zc) are the
@@ -59,21 +61,21 @@ struct GemvArgs {
     const uint8_t* wq2;
     const uint8_t* scales2;
     const uint8_t* zc2;
-    int a8;                   // the W4A8 GEMV (integer x codes): its work split follows the mma GEMV's
+    int a8;                   // the W4A8 GEMV (integer x codes)
 };
-constexpr int GEMV_WARPS = 4;     // worker warps per CTA
+constexpr int GEMV_WARPS = 4;     // worker warps per CTA of the CUDA-core GEMV
 // formats whose GEMV runs on mma.sync (the others on CUDA-core FMAs)
 inline bool gemv_is_mma(int fmt) {
     return fmt == UQ_INT4_SYM || fmt == UQ_INT4_ASYM || fmt == UQ_INT2_ASYM || fmt == UQ_K4;
 }
-size_t gemv_smem_bytes(int fmt, int K, int group, int M);
-int gemv_warps(int fmt);     // workers (warps) per CTA of the GEMV for this format
-int gemv_ctas_per_sm(int fmt);   // CTAs of the GEMV resident per SM (workers = SMs x this x warps)
-// work split of a GEMV launch whose a.P (stream-K workers) is set: may switch the mma GEMV to
-// whole row blocks per CTA (a.cta_rows = 1); returns the grid
-int gemv_grid(GemvArgs& a, int fmt, int sms);
-// fp32 partial-sum floats a GEMV launch needs (T tiles, P workers, M rows of x)
-size_t gemv_partials_floats(int fmt, long long T, int P, int M);
+// Plans one GEMV launch from its shape fields (M, N, K, group, NB, KB, T, gated, a8) and the SM
+// count: sets a.P (worker warps) and a.cta_rows.  Returns the grid, or 0 when no plan fits (K too
+// long for the kernel's shared memory at this M).
+int gemv_plan(GemvArgs& a, int fmt, int sms);
+// what a planned launch needs: fp32 partial-sum floats, the per-row-block tickets, kernel launches
+size_t gemv_partials_floats(int fmt, const GemvArgs& a);
+bool gemv_uses_tickets(int fmt, const GemvArgs& a);
+int gemv_launches(int fmt, const GemvArgs& a);
 cudaError_t launch_gemv(int fmt, const GemvArgs& a, int grid, cudaStream_t st);
 // the second pass of a stream-K split (tile partial sums [T][16][M] summed in k order)
 cudaError_t launch_gemv_second_pass(const GemvArgs& a, int sms, cudaStream_t st);
@@ -106,14 +108,14 @@ struct TcArgs {
     const float* gate32;      // up pass: y = bf16(silu(gate32) * result)
 };
 
-// The one place every kernel writes an output element (row m of x, output column n): bf16 y; or, for
-// the gated projection, fp32 g (the gate pass) or bf16 silu(g) * u (the up pass; silu(g) = g / (1 + e^-g)
-// in fp32, the product in fp32, one rounding to bf16).
 // silu(g) * u in fp32 (silu(g) = g / (1 + e^-g)), the gated projection's epilogue
 __device__ __forceinline__ float silu_mul(float g, float u) {
     return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
 }
 
+// The one place every kernel writes an output element (row m of x, output column n): bf16 y; or, for
+// the gated projection, fp32 g (the gate pass) or bf16 silu(g) * u (the up pass; the product in fp32,
+// one rounding to bf16).
 template <class Args>
 __device__ __forceinline__ void store_out(const Args& a, int m, int n, float v) {
     const long long idx = (long long)m * a.ldy + n;

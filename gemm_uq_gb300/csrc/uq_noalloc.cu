@@ -72,6 +72,49 @@ uq_status setup(int* dev_out, unsigned char** scratch, int* sms) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
+// the shape rules of uq_gemm_noalloc (those of uq_gemm's GEMV)
+uq_status check_shape(int M, int N, int K, int group, uq_fmt fmt) {
+    if (fmt < UQ_INT4_SYM || fmt > UQ_K4) { snprintf(g_err, sizeof g_err, "unknown format"); return err(UQ_ERR_INVALID); }
+    if (M < 0 || N < 0 || K < 0) { snprintf(g_err, sizeof g_err, "negative size"); return err(UQ_ERR_INVALID); }
+    if (fmt == UQ_K4) {
+        if (group != 256) { snprintf(g_err, sizeof g_err, "UQ_K4 needs group 256"); return err(UQ_ERR_UNSUPPORTED); }
+        if (K % 256) { snprintf(g_err, sizeof g_err, "UQ_K4 needs K %% 256 == 0"); return err(UQ_ERR_INVALID); }
+    } else {
+        if (group != 32 && group != 64 && group != 128) {
+            snprintf(g_err, sizeof g_err, "group must be 32, 64 or 128");
+            return err(UQ_ERR_UNSUPPORTED);
+        }
+        if (K % group) { snprintf(g_err, sizeof g_err, "K is not a multiple of the group"); return err(UQ_ERR_INVALID); }
+        if (fmt == UQ_INT2_ASYM && (K % 64)) {
+            snprintf(g_err, sizeof g_err, "UQ_INT2_ASYM needs K %% 64 == 0");
+            return err(UQ_ERR_UNSUPPORTED);
+        }
+    }
+    return UQ_OK;
+}
+
+// The scratch a call needs: the work split of its launches (every 8-row block of x but a shorter last
+// one plans alike: the split depends on N and K, and the scratch it needs grows with the rows).
+struct ScratchNeed {
+    bool tickets;
+    size_t ticket_bytes, partial_bytes;
+};
+uq_status scratch_need(int M, int N, int K, int group, uq_fmt fmt, int sms, ScratchNeed* need) {
+    const uq::Layout L(N, K, fmt);
+    const int mb_max = M < 8 ? M : 8;
+    uq::GemvArgs probe = {};
+    probe.M = mb_max; probe.N = N; probe.K = K; probe.group = group;
+    probe.NB = L.NB; probe.KB = L.KB; probe.T = (long long)L.NB * L.KB;
+    if (uq::gemv_plan(probe, fmt, sms) == 0) {
+        snprintf(g_err, sizeof g_err, "K=%d is too long for the GEMV at M=%d", K, mb_max);
+        return err(UQ_ERR_UNSUPPORTED);
+    }
+    need->tickets = uq::gemv_uses_tickets(fmt, probe);
+    need->ticket_bytes = need->tickets ? round256((size_t)L.NB * sizeof(unsigned int)) : 0;
+    need->partial_bytes = uq::gemv_partials_floats(fmt, probe) * sizeof(float);
+    return UQ_OK;
+}
+
 }  // namespace
 
 namespace uq {
@@ -104,22 +147,8 @@ extern "C" {
 uq_status uq_gemm_noalloc(const uint16_t* x, const void* wq, const void* scales, const void* zeros_or_codebook,
                           uint16_t* y, int M, int N, int K, int group, uq_fmt fmt, void* stream) {
     g_err[0] = 0;
-    if (fmt < UQ_INT4_SYM || fmt > UQ_K4) { snprintf(g_err, sizeof g_err, "unknown format"); return err(UQ_ERR_INVALID); }
-    if (M < 0 || N < 0 || K < 0) { snprintf(g_err, sizeof g_err, "negative size"); return err(UQ_ERR_INVALID); }
-    if (fmt == UQ_K4) {
-        if (group != 256) { snprintf(g_err, sizeof g_err, "UQ_K4 needs group 256"); return err(UQ_ERR_UNSUPPORTED); }
-        if (K % 256) { snprintf(g_err, sizeof g_err, "UQ_K4 needs K %% 256 == 0"); return err(UQ_ERR_INVALID); }
-    } else {
-        if (group != 32 && group != 64 && group != 128) {
-            snprintf(g_err, sizeof g_err, "group must be 32, 64 or 128");
-            return err(UQ_ERR_UNSUPPORTED);
-        }
-        if (K % group) { snprintf(g_err, sizeof g_err, "K is not a multiple of the group"); return err(UQ_ERR_INVALID); }
-        if (fmt == UQ_INT2_ASYM && (K % 64)) {
-            snprintf(g_err, sizeof g_err, "UQ_INT2_ASYM needs K %% 64 == 0");
-            return err(UQ_ERR_UNSUPPORTED);
-        }
-    }
+    uq_status s0 = check_shape(M, N, K, group, fmt);
+    if (s0 != UQ_OK) return s0;
     if (M == 0 || N == 0 || K == 0) {
         // K == 0 would need a fill of y; keep this entry point to the kernel itself
         if (K == 0 && M > 0 && N > 0) { snprintf(g_err, sizeof g_err, "K == 0 is not supported here"); return err(UQ_ERR_UNSUPPORTED); }
@@ -142,25 +171,10 @@ uq_status uq_gemm_noalloc(const uint16_t* x, const void* wq, const void* scales,
 
     const uq::Layout L(N, K, fmt);
     const long long T = (long long)L.NB * L.KB;
-    const int warps = uq::gemv_warps(fmt);
-    long long P = (long long)sms * uq::gemv_ctas_per_sm(fmt) * warps;
-    if (P > T) P = T;
-    const int mb_max = M < 8 ? M : 8;
-    if (uq::gemv_smem_bytes(fmt, K, group, mb_max) > 227 * 1024) {
-        snprintf(g_err, sizeof g_err, "K=%d is too long for the GEMV at M=%d", K, mb_max);
-        return err(UQ_ERR_UNSUPPORTED);
-    }
-    // the work split of the launches (the same for every 8-row block of x: it depends on N and K only)
-    uq::GemvArgs probe = {};
-    probe.M = mb_max; probe.N = N; probe.K = K; probe.group = group;
-    probe.NB = L.NB; probe.KB = L.KB; probe.T = T; probe.P = (int)P;
-    uq::gemv_grid(probe, fmt, sms);
-    const bool mma = uq::gemv_is_mma(fmt);
-    const bool uses_tickets = !mma;                          // the CUDA-core GEMV's last-contributor sums
-    const bool uses_partials = !mma || !probe.cta_rows;      // mma: only with the second-pass split
-    const size_t ticket_bytes = uses_tickets ? round256((size_t)L.NB * sizeof(unsigned int)) : 0;
-    const size_t partial_bytes =
-        uses_partials ? uq::gemv_partials_floats(fmt, T, (int)P, mb_max) * sizeof(float) : 0;
+    ScratchNeed need;
+    if ((s = scratch_need(M, N, K, group, fmt, sms, &need)) != UQ_OK) return s;
+    const bool uses_tickets = need.tickets;
+    const size_t ticket_bytes = need.ticket_bytes, partial_bytes = need.partial_bytes;
     if (DATA_OFFSET + ticket_bytes + partial_bytes > SCRATCH_BYTES) {
         snprintf(g_err, sizeof g_err,
                  "M=%d, N=%d, K=%d needs %zu bytes of tickets and %zu bytes of partial sums; the static scratch "
@@ -185,15 +199,37 @@ uq_status uq_gemm_noalloc(const uint16_t* x, const void* wq, const void* scales,
         a.zc = static_cast<const uint8_t*>(zeros_or_codebook);
         a.y = y + (long long)m0 * N;
         a.M = mb; a.N = N; a.K = K; a.group = group; a.ldx = K; a.ldy = N;
-        a.NB = L.NB; a.KB = L.KB; a.T = T; a.P = (int)P;
+        a.NB = L.NB; a.KB = L.KB; a.T = T;
+        const int grid = uq::gemv_plan(a, fmt, sms);
         a.partials = partials;
         a.tickets = tickets;
         a.fault = reinterpret_cast<unsigned int*>(scratch);     // read back by uq_device_fault
         a.overlap = 0;
-        const int grid = uq::gemv_grid(a, fmt, sms);
         e = uq::launch_gemv(fmt, a, grid, st);
         if (e != cudaSuccess) { snprintf(g_err, sizeof g_err, "GEMV launch: %s", cudaGetErrorString(e)); return err(UQ_ERR_CUDA); }
     }
+    return UQ_OK;
+}
+
+uq_status uq_gemm_noalloc_scratch(int M, int N, int K, int group, uq_fmt fmt, size_t* ticket_bytes,
+                                  size_t* partial_bytes) {
+    g_err[0] = 0;
+    if (!ticket_bytes || !partial_bytes) { snprintf(g_err, sizeof g_err, "null pointer"); return err(UQ_ERR_INVALID); }
+    *ticket_bytes = *partial_bytes = 0;
+    uq_status s = check_shape(M, N, K, group, fmt);
+    if (s != UQ_OK) return s;
+    if (M == 0 || N == 0 || K == 0) return UQ_OK;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess || sms < 1) {
+        snprintf(g_err, sizeof g_err, "SM count: %s", cudaGetErrorString(e != cudaSuccess ? e : cudaErrorInvalidDevice));
+        return err(UQ_ERR_CUDA);
+    }
+    ScratchNeed need;
+    if ((s = scratch_need(M, N, K, group, fmt, sms, &need)) != UQ_OK) return s;
+    *ticket_bytes = need.ticket_bytes;
+    *partial_bytes = need.partial_bytes;
     return UQ_OK;
 }
 

@@ -139,9 +139,11 @@ __global__ void __launch_bounds__(128, MMA_CTAS_PER_SM) gemv_a8_kernel(const Gem
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     int issued = 0;
+    // k-major tile coordinates advanced incrementally (no 64-bit division per tile)
+    int ikb = ntl > 0 ? kb_of(t0) : 0, irb = ntl > 0 ? (int)(t0 % R) : 0;   // the next tile to request
     auto issue_next = [&]() {
-        const long long i = t0 + issued;
-        issue_tile<FMT, true>(a, src, L, mc, nb_of(i), kb_of(i), ring + (issued % S) * F::STAGE_BYTES, nullptr, lane);
+        issue_tile<FMT, true, GPT>(a, src, L, mc, rb0 + irb, ikb, ring + (issued % S) * F::STAGE_BYTES, nullptr, lane);
+        if (++irb == R) { irb = 0; ++ikb; }
         ++issued;
     };
     if (a.overlap && has_work && ntl > 0) issue_next();           // weights are constant: before the wait
@@ -158,9 +160,11 @@ __global__ void __launch_bounds__(128, MMA_CTAS_PER_SM) gemv_a8_kernel(const Gem
 #pragma unroll
     for (int m = 0; m < 8; ++m) sxm[m] = m < M ? __ldg(sxs + m) : 0.f;
 
+    int ckb = ntl > 0 ? kb_of(t0) : 0, crb = ntl > 0 ? (int)(t0 % R) : 0;   // the tile being consumed
     for (int li = 0; li < ntl; ++li) {
         const long long i = t0 + li;
-        const int kb = kb_of(i), nb = nb_of(i);
+        const int kb = ckb, nb = rb0 + crb;
+        if (++crb == R) { crb = 0; ++ckb; }
         const int n0 = nb * RB;
         const int gi0 = kb * GPT;
         const int ng = (G_all - gi0) < GPT ? (G_all - gi0) : GPT;

@@ -319,7 +319,8 @@ uq_status uq_device_fault(unsigned int* flag);
  * tensor-core path), so the output equals uq_gemm's for M <= 15.
  * Scratch: a 1 MiB static device array inside the library (every GPU that loads the library holds
  * it until the process exits); 256 bytes hold the fault word, and the rest must hold what the
- * launch's work split uses, for one 8-row block of x (Mb = min(M, 8)):
+ * launch's work split uses for one 8-row block of x (Mb = min(M, 8); uq_gemm_noalloc_scratch
+ * reports it):
  *   - INT4_SYM, INT4_ASYM, INT2_ASYM, K4 (mma.sync GEMV): nothing when every CTA owns whole
  *     16-row blocks (the split uq_gemm_kernel_count reports as one launch); otherwise fp32
  *     partial sums of every tile, 64*Mb*ceil(N/16)*ceil(K/T) bytes (T = 1024 codes, 2048 for
@@ -338,6 +339,16 @@ uq_status uq_device_fault(unsigned int* flag);
 uq_status uq_gemm_noalloc(const uint16_t* x, const void* wq, const void* scales,
                           const void* zeros_or_codebook, uint16_t* y,
                           int M, int N, int K, int group, uq_fmt fmt, void* stream);
+
+/*
+ * uq_gemm_noalloc_scratch -- the static scratch uq_gemm_noalloc would use for this shape on the
+ * current device: *ticket_bytes (row-block tickets of the CUDA-core GEMV, rounded up to 256) and
+ * *partial_bytes (fp32 partial sums; 0 when every worker owns whole row blocks), as listed above.
+ * Host-only (queries the SM count).  UQ_ERR_INVALID /
+ * UQ_ERR_UNSUPPORTED as uq_gemm_noalloc for shapes it rejects; it does not check the 1 MiB limit.
+ */
+uq_status uq_gemm_noalloc_scratch(int M, int N, int K, int group, uq_fmt fmt, size_t* ticket_bytes,
+                                  size_t* partial_bytes);
 
 #ifdef __cplusplus
 }

@@ -155,10 +155,13 @@ def test_determinism_and_batched_rows(fmt, group):
 
 def test_kernel_count_matches_the_paths():
     # 14336 x 4096 at M = 1: whole row blocks per CTA, one launch; 4096 x 14336: the stream-K split
-    # and its second pass; the tensor-core path: one GEMM per 64 rows (K4: after its x column-sum
-    # pre-kernel); a K that is not a multiple of the code tile keeps M = 20 on the GEMV: three 8-row blocks
+    # (a partial-sum slot per tile) and its second pass; the tensor-core path: one GEMM per 64 rows
+    # (K4: after its x column-sum pre-kernel); a K that is not a multiple of the code tile keeps M = 20
+    # on the GEMV: three 8-row blocks
     assert uq.gemm_kernel_count(1, 14336, 4096, 128, "INT4_ASYM") == 1
+    assert uq.gemm_noalloc_scratch(1, 14336, 4096, 128, "INT4_ASYM") == (0, 0)
     assert uq.gemm_kernel_count(1, 4096, 14336, 128, "INT4_ASYM") == 2
+    assert uq.gemm_noalloc_scratch(1, 4096, 14336, 128, "INT4_ASYM") == (0, 256 * 14 * 16 * 4)
     assert uq.gemm_kernel_count(1, 8192, 8192, 128, "INT8_SYM") == 1
     assert uq.gemm_kernel_count(64, 14336, 4096, 128, "INT4_ASYM") == 1
     assert uq.gemm_kernel_count(128, 14336, 4096, 128, "INT4_ASYM") == 2

@@ -75,6 +75,7 @@ def test_noalloc_refuses_partial_sums_beyond_its_scratch():
     8 columns of fp32 partial sums (1.8 MB) exceed the array; this format uses no tickets."""
     N, K, group, fmt, M = 4096, 14336, 128, "INT4_ASYM", 8
     assert uq.gemm_kernel_count(M, N, K, group, fmt) == 2
+    assert uq.gemm_noalloc_scratch(M, N, K, group, fmt) == (0, 256 * 14 * 16 * 8 * 4)
     assert 256 * 14 * 16 * 8 * 4 > SCRATCH
     xd, wq, sc, zc, y = _zeros_problem(N, K, group, fmt, M)
     with pytest.raises(uq.UqError) as e:
@@ -105,6 +106,7 @@ def test_noalloc_needs_no_partial_sums_when_ctas_own_whole_row_blocks():
     partial sums.  The output must equal uq_gemm's bit for bit."""
     N, K, group, fmt, M = 19456, 4096, 32, "INT4_SYM", 8
     assert uq.gemm_kernel_count(M, N, K, group, fmt) == 1
+    assert uq.gemm_noalloc_scratch(M, N, K, group, fmt) == (0, 0)
     assert (N // 16) * (K // 1024) * 16 * M * 4 > SCRATCH
     g = torch.Generator(device=DEV)
     g.manual_seed(806)
