@@ -643,7 +643,8 @@ __host__ __device__ inline int gemv_mma_xslice_stride(int fmt, int M) {
 }
 
 // Shared memory: rings [warps][stages][stage] | ring and x mbarriers | sums of x [warps][groups of
-// a tile][8] | partial sums [warps][MMA_TPW][16][8] | x (whole, or [warps][2][M] slices)
+// a tile][8] | partial sums [tiles of the CTA, at most warps x MMA_TPW][16][8] | x (whole, or
+// [warps][2][M] slices)
 __host__ __device__ inline GemvSmem gemv_mma_smem_plan(int fmt, int K, int group, int M, int xm) {
     int stage = 0, warps = 0;
     const int kc = fmt_kc(fmt), kt = fmt_kt(fmt);
@@ -1009,7 +1010,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
 
         // the tile's partial sums: shared memory (cta_rows) or global memory, summed over k tiles later
         if (cta_rows) {
-            float* part = cpart + ((warp * MMA_TPW + li) * RB) * 8;
+            float* part = cpart + (i * RB) * 8;                     // slot = the tile's index in the CTA's range
 #pragma unroll
             for (int j = 0; j < 2; ++j)
 #pragma unroll
@@ -1035,12 +1036,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
     __syncthreads();
     auto row_sum = [&](int rbi, int r, int m) {
         float sum = 0.f;
-        for (int kb = 0; kb < L.KB; ++kb) {
-            const unsigned ti = (unsigned)(kb * R + rbi);
-            const unsigned w2 = ((ti + 1) * W - 1) / Tc;            // the warp whose range holds ti
-            const unsigned l2 = ti - w2 * Tc / W;
-            sum += cpart[((w2 * MMA_TPW + l2) * RB + r) * 8 + m];
-        }
+        for (int kb = 0; kb < L.KB; ++kb) sum += cpart[((kb * R + rbi) * RB + r) * 8 + m];
         return sum;
     };
     for (int e = threadIdx.x; e < (R / WU) * RB * M; e += blockDim.x) {

@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(128, MMA_CTAS_PER_SM) gemv_a8_kernel(const Gem
             }
         if (c == 0) {
             if (cta_rows) {
-                float* part = cpart + ((warp * MMA_TPW + li) * RB) * 8;
+                float* part = cpart + (i * RB) * 8;                 // slot = the tile's index in the CTA's range
 #pragma unroll
                 for (int jr = 0; jr < 2; ++jr)
 #pragma unroll
@@ -263,12 +263,7 @@ __global__ void __launch_bounds__(128, MMA_CTAS_PER_SM) gemv_a8_kernel(const Gem
         const int n = (rb0 + rbi) * RB + r;
         if (n >= a.N) continue;
         float sum = 0.f;
-        for (int kbb = 0; kbb < L.KB; ++kbb) {
-            const unsigned ti = (unsigned)(kbb * R + rbi);
-            const unsigned w2 = ((ti + 1) * W - 1) / Tc;
-            const unsigned l2 = ti - w2 * Tc / W;
-            sum += cpart[((w2 * MMA_TPW + l2) * RB + r) * 8 + m];
-        }
+        for (int kbb = 0; kbb < L.KB; ++kbb) sum += cpart[((kbb * R + rbi) * RB + r) * 8 + m];
         store_out(a, m, n, sum);
     }
 }
