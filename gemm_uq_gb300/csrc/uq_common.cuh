@@ -189,9 +189,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
                  : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
     return ok != 0;
 }
-// Bounded wait: polls until the phase with `parity` completes or WAIT_LIMIT_NS of wall time
+// The same test, but a thread whose phase is not complete is suspended in the instruction until
+// the phase completes or up to `ns` nanoseconds pass, instead of returning at once: a waiting warp
+// then leaves its issue slots to the working ones rather than spinning.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(ns) : "memory");
+    return ok != 0;
+}
+// Bounded wait: waits until the phase with `parity` completes or WAIT_LIMIT_NS of wall time
 // (the %globaltimer nanosecond clock) have passed; then records `code` in the fault word and
-// returns false so the caller can leave instead of hanging the GPU.
+// returns false so the caller can leave instead of hanging the GPU.  Each attempt may suspend the
+// thread for up to 1 us (woken early when the phase completes).
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;   // 2 s
 __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
@@ -202,13 +214,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
                                                   unsigned int code) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
-    while (true) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > WAIT_LIMIT_NS) break;
-    }
-    atomicOr(fault, code);
-    return false;
+    while (!mbar_try_wait_sleep(bar, parity, 1000u))
+        if (global_ns() - t0 > WAIT_LIMIT_NS) {
+            atomicOr(fault, code);
+            return false;
+        }
+    return true;
 }
 // 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
 // Both addresses 16-byte aligned, size a multiple of 16.
