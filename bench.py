@@ -158,11 +158,18 @@ def read_share(workload):
 
 
 def dominant_kernel(fmt, group, M, shapes):
-    """Name of the kernel template the library dispatches for this workload's linears."""
-    if M >= 16 and fmt in ("INT4_SYM", "INT4_ASYM", "INT8_SYM", "K4") and all(K % KT[fmt] == 0 for _, K in shapes):
+    """Name of the kernel template the library dispatches for this workload's linears (uq_gemm's
+    automatic routing: the mma.sync GEMM for 9..15 rows of the 4-bit / 2-bit formats and for K4, the
+    tensor cores for other blocks of 16..64 rows, the GEMV below)."""
+    mma_fmt = fmt in ("INT4_SYM", "INT4_ASYM", "INT2_ASYM", "K4")
+    tc_ok = M >= 16 and all(K % KT[fmt] == 0 for _, K in shapes)
+    if mma_fmt and M >= 9 and (M <= 15 or fmt == "K4" or not tc_ok):
+        mb = min(M, 64)
+        return f"gemm_mma_kernel<{fmt},{16 if mb <= 16 else (32 if mb <= 32 else 64)} columns>"
+    if tc_ok:
         mpad = (min(M, 64) + 15) // 16 * 16
         return f"tc_kernel<{fmt},{mpad}>"
-    if fmt in ("INT4_SYM", "INT4_ASYM", "INT2_ASYM", "K4"):
+    if mma_fmt:
         gs = 32 if fmt == "K4" else group
         return f"gemv_mma_kernel<{fmt},GB={gs // 16}>"
     return f"gemv_kernel<{fmt},{min(M, 8)}>"

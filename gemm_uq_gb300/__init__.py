@@ -36,6 +36,7 @@ SIGNATURES = {
     "uq_gemm_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "uq_gemm_noalloc_scratch": (_I, [_I, _I, _I, _I, _I, _SZ, _SZ]),
     "uq_set_launch_overlap": (_I, [_I]),
+    "uq_set_gemm_path": (_I, [_I]),
     "uq_gemm_kernel_count": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I)]),
     "uq_gemm_gated": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "uq_gemm_gated_kernel_count": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I)]),
@@ -299,6 +300,15 @@ def quantize_k4(w: torch.Tensor, stream=None):
 def set_launch_overlap(enable: bool) -> None:
     """uq_set_launch_overlap: let GEMV launches prefetch their (constant) weights early."""
     _check(lib().uq_set_launch_overlap(1 if enable else 0), "uq_set_launch_overlap")
+
+
+GEMM_PATHS = {"auto": 0, "tensor_cores": 1, "mma": 2}
+
+
+def set_gemm_path(path: str) -> None:
+    """uq_set_gemm_path: "auto" (default), "tensor_cores" (the tcgen05 kernel for every block of 16..64
+    rows it supports) or "mma" (the mma.sync GEMM for every block of 9..64 rows of a 4-bit / 2-bit format)."""
+    _check(lib().uq_set_gemm_path(GEMM_PATHS[path]), "uq_set_gemm_path")
 
 
 def gemm_kernel_count(M: int, N: int, K: int, group: int, fmt: str) -> int:

@@ -80,7 +80,7 @@ std::map<int, DeviceState> g_dev;
 struct Workspace {
     float* partials = nullptr;
     size_t partial_bytes = 0;
-    float* aux = nullptr;              // tensor-core path: fp16 copy of x and its row scales
+    float* aux = nullptr;              // K4 GEMMs: column sums of x per 32-k block; W4A8: x codes
     size_t aux_bytes = 0;
     unsigned int* tickets = nullptr;   // zero between calls (the kernels reset what they use)
     size_t ticket_bytes = 0;
@@ -281,6 +281,67 @@ uq_status run_tc(const uint16_t* x, const void* wq, const void* scales, const vo
     return UQ_OK;
 }
 
+
+// one mma.sync GEMM launch (and its second pass when the k range is split) for 9 <= Mb <= 64 rows
+// of x, 4-bit and 2-bit formats
+uq_status run_gemm_mma(const uint16_t* x, const void* wq, const void* scales, const void* zc, uint16_t* y, int Mb,
+                       int N, int K, int ldx, int ldy, int group, int fmt, cudaStream_t st, const DeviceState& ds,
+                       int dev, OutMode om = OutMode()) {
+    const uq::Layout L(N, K, fmt);
+    uq::GemmArgs a = {};
+    a.M = Mb; a.N = N; a.K = K; a.group = group; a.ldx = ldx; a.ldy = ldy;
+    a.NB = L.NB;
+    a.UB = uq::gemm_mma_units(fmt, K);
+    a.KS = uq::gemm_mma_splits(a.NB, a.UB, ds.sms);
+    a.Mpad = Mb <= 16 ? 16 : (Mb <= 32 ? 32 : 64);
+    const size_t partial_bytes = a.KS > 1 ? (size_t)a.KS * a.NB * 16 * Mb * sizeof(float) : 0;
+    const size_t aux_bytes = (fmt == UQ_K4) ? (size_t)(K / 32) * a.Mpad * sizeof(float) : 0;
+    Workspace* ws = nullptr;
+    uq_status s = workspace(dev, st, partial_bytes, (size_t)L.NB * sizeof(unsigned int), &ws, aux_bytes);
+    if (s != UQ_OK) return s;
+    cudaError_t e;
+    if (fmt == UQ_K4) {
+        e = uq::launch_colsum32(x, ws->aux, Mb, a.Mpad, K, ldx, st);
+        if (e != cudaSuccess) return cuda_fail(e, "column-sum launch");
+    }
+    a.x = x;
+    a.wq = static_cast<const uint8_t*>(wq);
+    a.scales = static_cast<const uint8_t*>(scales);
+    a.zc = static_cast<const uint8_t*>(zc);
+    a.y = y;
+    a.sx = ws->aux;
+    a.partials = ws->partials;
+    a.out32 = om.out32;
+    a.gate32 = om.gate32;
+    e = uq::launch_gemm_mma(fmt, a, ds.sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "mma GEMM launch");
+    return UQ_OK;
+}
+
+// Which kernel runs a block of rows of x (automatic choice, from measurements of both GEMMs): the
+// 4-bit and 2-bit formats take the mma.sync GEMM for 9..15 rows (instead of two 8-row GEMV passes
+// over the weights) and K4 for any M >= 9; every format takes the tensor-core GEMM for 16..64 rows
+// otherwise, when the shape allows it; everything else runs the GEMV in blocks of at most 8 rows.
+// uq_set_gemm_path can force either GEMM for M >= 16.
+std::atomic<int> g_path{0};                 // uq_set_gemm_path: 0 automatic, 1 tensor cores, 2 mma.sync
+enum Route { ROUTE_GEMV = 0, ROUTE_MMA_GEMM = 1, ROUTE_TC = 2 };
+Route route(int fmt, int M, int N, int K) {
+    const int path = g_path.load(std::memory_order_relaxed);
+    const bool tc = M >= 16 && uq::tc_supported(fmt, N, K);
+    if (uq::gemv_is_mma(fmt) && M >= 9) {
+        if (path == 2) return ROUTE_MMA_GEMM;
+        if (path == 1 && tc) return ROUTE_TC;
+        if (path == 0 && (M <= 15 || fmt == UQ_K4 || !tc)) return ROUTE_MMA_GEMM;
+    }
+    return tc ? ROUTE_TC : ROUTE_GEMV;
+}
+// launches of one mma.sync GEMM block of Mb rows
+int gemm_mma_launches(int fmt, int Mb, int N, int K, int sms) {
+    const uq::Layout L(N, K, fmt);
+    const int ks = uq::gemm_mma_splits(L.NB, uq::gemm_mma_units(fmt, K), sms);
+    (void)Mb;
+    return 1 + (ks > 1 ? 1 : 0) + (fmt == UQ_K4 ? 1 : 0);
+}
 }  // namespace
 
 namespace uq {
@@ -399,7 +460,20 @@ uq_status uq_gemm(const uint16_t* x, const void* wq, const void* scales, const v
     DeviceState* ds = nullptr;
     int dev = 0;
     if ((s = device_state(&ds, &dev)) != UQ_OK) return s;
-    if (M >= 16 && uq::tc_supported(fmt, N, K)) {
+    const Route rt = route(fmt, M, N, K);
+    if (rt == ROUTE_MMA_GEMM) {
+        // blocks of at most 64 rows on the mma.sync GEMM; a last block of at most 8 rows on the GEMV
+        for (int m0 = 0; m0 < M; m0 += 64) {
+            const int mb = (M - m0) < 64 ? (M - m0) : 64;
+            const uint16_t* xb = x + (long long)m0 * K;
+            uint16_t* yb = y + (long long)m0 * N;
+            s = mb <= 8 ? run_gemv(xb, wq, scales, zeros_or_codebook, yb, mb, N, K, K, N, group, fmt, st, *ds, dev)
+                        : run_gemm_mma(xb, wq, scales, zeros_or_codebook, yb, mb, N, K, K, N, group, fmt, st, *ds, dev);
+            if (s != UQ_OK) return s;
+        }
+        return UQ_OK;
+    }
+    if (rt == ROUTE_TC) {
         // tensor cores, in blocks of at most 64 activation rows (the last block at least 16 rows
         // wide is padded to a multiple of 16 with zero rows by the TMA bounds)
         for (int m0 = 0; m0 < M; m0 += 64) {
@@ -441,17 +515,13 @@ uq_status uq_gemm_gated(const uint16_t* x, const void* wq_gate, const void* scal
     DeviceState* ds = nullptr;
     int dev = 0;
     if ((s = device_state(&ds, &dev)) != UQ_OK) return s;
-    const bool tc = M >= 16 && uq::tc_supported(fmt, N, K);
-    const int block = tc ? 64 : 8;
-    if (!tc && uq::gemv_is_mma(fmt)) {
-        // one launch per block of 8 rows: the mma GEMV over the gate and up weights together
-        for (int m0 = 0; m0 < M; m0 += 8) {
-            const int mb = (M - m0) < 8 ? (M - m0) : 8;
-            s = run_gemv_gated(x + (long long)m0 * K, wq_gate, scales_gate, zc_gate, wq_up, scales_up, zc_up,
-                               h + (long long)m0 * N, mb, N, K, K, N, group, fmt, st, *ds, dev);
-            if (s != UQ_OK) return s;
-        }
-        return UQ_OK;
+    const Route rt = route(fmt, M, N, K);
+    const bool tc = rt == ROUTE_TC;
+    const int block = rt == ROUTE_GEMV ? 8 : 64;
+    if (rt != ROUTE_TC && uq::gemv_is_mma(fmt) && M <= 8) {
+        // one launch: the mma GEMV over the gate and up weights together
+        return run_gemv_gated(x, wq_gate, scales_gate, zc_gate, wq_up, scales_up, zc_up, h, M, N, K, K, N, group,
+                              fmt, st, *ds, dev);
     }
     const int rows = M < block ? M : block;
     float* g32 = nullptr;
@@ -475,6 +545,13 @@ uq_status uq_gemm_gated(const uint16_t* x, const void* wq_gate, const void* scal
             s = run_tc(xb, wq_gate, scales_gate, zc_gate, hb, mb, N, K, K, N, group, fmt, st, *ds, dev, gate_pass);
             if (s == UQ_OK)
                 s = run_tc(xb, wq_up, scales_up, zc_up, hb, mb, N, K, K, N, group, fmt, st, *ds, dev, up_pass);
+        } else if (rt == ROUTE_MMA_GEMM && mb <= 8) {
+            s = run_gemv_gated(xb, wq_gate, scales_gate, zc_gate, wq_up, scales_up, zc_up, hb, mb, N, K, K, N, group,
+                               fmt, st, *ds, dev);
+        } else if (rt == ROUTE_MMA_GEMM) {
+            s = run_gemm_mma(xb, wq_gate, scales_gate, zc_gate, hb, mb, N, K, K, N, group, fmt, st, *ds, dev, gate_pass);
+            if (s == UQ_OK)
+                s = run_gemm_mma(xb, wq_up, scales_up, zc_up, hb, mb, N, K, K, N, group, fmt, st, *ds, dev, up_pass);
         } else {
             s = run_gemv(xb, wq_gate, scales_gate, zc_gate, hb, mb, N, K, K, N, group, fmt, st, *ds, dev, gate_pass);
             if (s == UQ_OK)
@@ -488,24 +565,34 @@ uq_status uq_gemm_gated(const uint16_t* x, const void* wq_gate, const void* scal
 uq_status uq_gemm_gated_kernel_count(int M, int N, int K, int group, uq_fmt fmt, int* count) {
     uq_status s = uq_gemm_kernel_count(M, N, K, group, fmt, count);
     if (s != UQ_OK || M == 0 || N == 0 || K == 0) return s;
-    if ((M >= 16 && uq::tc_supported(fmt, N, K)) || !uq::gemv_is_mma(fmt)) {
-        *count *= 2;                                        // the gate pass and the up pass
-        return UQ_OK;
-    }
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess || sms < 1) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice, "SM count");
+    const Route rt = route(fmt, M, N, K);
     const uq::Layout L(N, K, fmt);
-    int n = 0;
-    for (int m0 = 0; m0 < M; m0 += 8) {                     // per block of 8 rows: one launch
+    // one fused GEMV launch for a block of at most 8 rows of a 4-bit / 2-bit format
+    auto fused = [&](int mb) {
         uq::GemvArgs a = {};
-        a.M = (M - m0) < 8 ? (M - m0) : 8; a.N = N; a.K = K; a.group = group;
+        a.M = mb; a.N = N; a.K = K; a.group = group;
         a.gated = 1; a.NB = 2 * L.NB; a.KB = L.KB; a.T = (long long)a.NB * L.KB;
         uq::gemv_plan(a, fmt, sms);
-        n += uq::gemv_launches(fmt, a);
+        return uq::gemv_launches(fmt, a);
+    };
+    if (rt != ROUTE_TC && uq::gemv_is_mma(fmt) && M <= 8) {
+        *count = fused(M);
+        return UQ_OK;
     }
-    *count = n;
+    if (rt == ROUTE_MMA_GEMM) {
+        int n = 0;
+        for (int m0 = 0; m0 < M; m0 += 64) {
+            const int mb = (M - m0) < 64 ? (M - m0) : 64;
+            n += mb <= 8 ? fused(mb) : 2 * gemm_mma_launches(fmt, mb, N, K, sms);   // a gate pass and an up pass
+        }
+        *count = n;
+        return UQ_OK;
+    }
+    *count *= 2;                                            // the gate pass and the up pass
     return UQ_OK;
 }
 
@@ -701,6 +788,13 @@ uq_status uq_quantize_k4(const float* w, int8_t* codes, uint16_t* d, uint16_t* d
     return UQ_OK;
 }
 
+uq_status uq_set_gemm_path(int path) {
+    if (path < 0 || path > 2)
+        return fail(UQ_ERR_INVALID, "path must be 0 (automatic), 1 (tensor cores) or 2 (mma.sync GEMM)");
+    g_path.store(path);
+    return UQ_OK;
+}
+
 uq_status uq_set_launch_overlap(int enable) {
     uq::g_overlap.store(enable ? 1 : 0);
     return UQ_OK;
@@ -719,7 +813,24 @@ uq_status uq_gemm_kernel_count(int M, int N, int K, int group, uq_fmt fmt, int* 
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess || sms < 1) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice, "SM count");
     int n = 0;
-    if (M >= 16 && uq::tc_supported(fmt, N, K)) {
+    const Route rt = route(fmt, M, N, K);
+    if (rt == ROUTE_MMA_GEMM) {
+        // per block of at most 64 rows: the mma.sync GEMM (K4: after its x column-sum pre-kernel;
+        // plus the second pass when its k range is split); a last block of at most 8 rows: the GEMV
+        const uq::Layout L(N, K, fmt);
+        for (int m0 = 0; m0 < M; m0 += 64) {
+            const int mb = (M - m0) < 64 ? (M - m0) : 64;
+            if (mb > 8) {
+                n += gemm_mma_launches(fmt, mb, N, K, sms);
+            } else {
+                uq::GemvArgs a = {};
+                a.M = mb; a.N = N; a.K = K; a.group = group;
+                a.NB = L.NB; a.KB = L.KB; a.T = (long long)L.NB * L.KB;
+                uq::gemv_plan(a, fmt, sms);
+                n += uq::gemv_launches(fmt, a);
+            }
+        }
+    } else if (rt == ROUTE_TC) {
         // per block of at most 64 rows: the GEMM (K4: after its x column-sum pre-kernel)
         for (int m0 = 0; m0 < M; m0 += 64) n += (fmt == UQ_K4) ? 2 : 1;
     } else {

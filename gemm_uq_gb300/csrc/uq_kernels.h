@@ -80,6 +80,28 @@ cudaError_t launch_gemv(int fmt, const GemvArgs& a, int grid, cudaStream_t st);
 // the second pass of a stream-K split (tile partial sums [T][16][M] summed in k order)
 cudaError_t launch_gemv_second_pass(const GemvArgs& a, int sms, cudaStream_t st);
 
+// batched decode on mma.sync for the 4-bit and 2-bit formats, 9 <= M <= 64 (uq_gemm_mma.cu)
+struct GemmArgs {
+    const uint16_t* x;        // bf16 [M][ldx]
+    const uint8_t* wq;        // packed codes
+    const uint8_t* scales;    // fp16 [N][K/group] or K4 records
+    const uint8_t* zc;        // INT4_ASYM zero nibbles, INT2_ASYM fp16 zeros, else NULL
+    uint16_t* y;              // bf16 [M][ldy]
+    int M, N, K, group, ldx, ldy;
+    int NB;                   // row blocks of 16
+    int UB;                   // k units per row (4 chunks of codes each)
+    int KS;                   // k splits: CTAs per row group of 8 row blocks
+    const float* sx;          // K4: column sums of x per 32-k block [K/32][Mpad], else NULL
+    int Mpad;                 // columns of sx (8 x column blocks)
+    float* partials;          // KS > 1: [KS][NB * 16][M] fp32
+    float* out32;             // gate pass of the gated projection: fp32 results [M][ldy] instead of y
+    const float* gate32;      // up pass: y = bf16(silu(gate32) * result)
+};
+int gemm_mma_units(int fmt, int K);               // k units per row
+int gemm_mma_splits(int NB, int UB, int sms);     // k splits per row group
+// the kernel, then (KS > 1) the second pass over the splits
+cudaError_t launch_gemm_mma(int fmt, const GemmArgs& a, int sms, cudaStream_t st);
+
 // W4A8 / W8A8 (uq_w4a8.cu): x codes and scales, then the integer GEMV
 size_t a8_smem_bytes(int fmt);
 cudaError_t launch_quant_x(const uint16_t* x, int8_t* xq, float* sx, int* sxl, int M, int K, int Kp, int gs, int perm,

@@ -11,9 +11,10 @@
  * where x is M x K bf16, W_hat is the N x K dequantized weight (a linear layer's
  * weight, K contiguous) and y is M x N bf16.  W_hat is never materialised: the
  * kernels stream packed codes from HBM and unpack them in registers, where they feed
- * warp-level mma.sync instructions or CUDA-core FMAs (M <= 15), or are written as the
- * integer part of the weights straight into tensor memory as the A operand of tcgen05
- * tensor-core MMAs (M >= 16); per-group scales are applied to fp32 group sums.
+ * warp-level mma.sync instructions (4-bit and 2-bit formats: M <= 15, and K4 at any M) or
+ * CUDA-core FMAs (INT8 / NF4, M <= 15), or are written as the integer part of the weights straight
+ * into tensor memory as the A operand of tcgen05 tensor-core MMAs (M >= 16 otherwise); per-group
+ * scales are applied to fp32 group sums.
  *
  * Weight formats (g = group size along K):
  *   UQ_INT4_SYM   codes q in [-8, 7],  fp16 scale s per group        W_hat = s*q
@@ -141,14 +142,19 @@ uq_status uq_pack_kmeta(const uint16_t* d, const uint16_t* dmin, const uint8_t* 
  *   M >= 0, N >= 0, K >= 0; M == 0 or N == 0 is a no-op; K == 0 writes zeros.
  *   group: 32, 64 or 128 for the flat formats (K % group == 0; UQ_INT2_ASYM also needs
  *   K % 64 == 0); 256 for UQ_K4 (K % 256 == 0).
- * Paths: M <= 8 the GEMV (mma.sync tensor instructions for INT4_SYM, INT4_ASYM, INT2_ASYM
- * and K4; CUDA-core FMAs for INT8_SYM and NF4): one launch when each CTA owns whole row
- * blocks, else the GEMV and a second launch that sums each row's k-tile partials in a
- * fixed order, so repeated calls are bit-identical; 9 <= M <= 15 the GEMV over row blocks
- * of x of at most 8 rows; M >= 16 the tcgen05 tensor-core kernel for INT4_SYM, INT4_ASYM,
- * INT8_SYM and K4 when K is a multiple of the code tile (1024 4-bit / 512 8-bit codes; K4
- * adds a small column-sum launch), otherwise (and for INT2_ASYM and NF4) the GEMV over
- * 8-row blocks of x.  uq_gemm_kernel_count gives the launches of a shape.
+ * Paths, per block of rows of x:
+ *   - M <= 8: the GEMV (mma.sync for INT4_SYM, INT4_ASYM, INT2_ASYM and K4; CUDA-core FMAs for
+ *     INT8_SYM and NF4): one launch when each CTA owns whole row blocks, else the GEMV and a second
+ *     launch that sums each row's partials in a fixed order, so repeated calls are bit-identical,
+ *     and a row of x gives the same bits whatever the other rows of a call of M <= 8;
+ *   - INT4_SYM, INT4_ASYM, INT2_ASYM with 9 <= M <= 15, and K4 with M >= 9: the mma.sync GEMM in
+ *     blocks of 64 rows (each warp reuses an unpacked 16 x 16 block of exact integer (q - z) for
+ *     every 8 columns of x; K4 adds a small column-sum launch, a k range split between CTAs a
+ *     second pass), a last block of at most 8 rows on the GEMV;
+ *   - every other M >= 16 with K a multiple of the code tile (1024 4-bit / 512 8-bit / 2048 2-bit
+ *     codes): the tcgen05 tensor-core kernel in blocks of 64 rows; otherwise the GEMV over 8-row
+ *     blocks.  uq_set_gemm_path can force either GEMM.
+ * uq_gemm_kernel_count gives the launches of a shape.
  * Scratch: a library-owned workspace per (device, stream), grown on the first call
  * that needs more; that growth is refused (UQ_ERR_NOMEM) while `stream` is being
  * captured, so make one call of the largest size before capturing.  A buffer replaced
@@ -172,12 +178,13 @@ uq_status uq_gemm(const uint16_t* x, const void* wq, const void* scales,
  *   x (device) bf16 [M][K]; wq_gate / scales_gate / zc_gate and wq_up / scales_up / zc_up (device):
  *   two weights of the same N, K, group and format, each as uq_gemm takes them; h (device) bf16
  *   [M][N], written.  M == 0 or N == 0 is a no-op; K == 0 writes zeros.
- * Paths, per block of rows of x (8 on the GEMV, 64 on the tensor-core path, routed as uq_gemm):
- * INT4_SYM, INT4_ASYM, INT2_ASYM and K4 with M <= 15 run one mma-GEMV launch over both weights (gate and
- * up row blocks interleaved, each CTA owning whole gate/up pairs, h formed in its per-row reduction),
- * plus the second pass when the work split shares row blocks between CTAs; INT8_SYM and NF4, and the
- * tensor-core path (M >= 16), run the gate projection into fp32 library scratch and then the up
- * projection, whose epilogue reads g and writes h.  uq_gemm_gated_kernel_count gives the launches.
+ * Paths, routed as uq_gemm: INT4_SYM, INT4_ASYM, INT2_ASYM and K4 with M <= 8 (and a last block
+ * of at most 8 rows after mma.sync GEMM blocks) run one mma-GEMV launch over both weights (gate
+ * and up row blocks interleaved, each CTA owning whole gate/up pairs, h formed in its per-row
+ * reduction), plus the second pass when the work split shares row blocks between CTAs; everything
+ * else (the mma.sync GEMM, INT8_SYM and NF4, the tensor-core path) runs the gate projection into
+ * fp32 library scratch and then the up projection, whose epilogue reads g and writes h.
+ * uq_gemm_gated_kernel_count gives the launches.
  * Scratch, errors and stream capture as uq_gemm (the fp32 gate scratch, rows x N floats, is part of
  * the per-stream workspace).
  */
@@ -279,6 +286,16 @@ uq_status uq_quantize_k4(const float* w, int8_t* codes, uint16_t* d, uint16_t* d
 uq_status uq_pack_zeros(const uint8_t* zeros, uint8_t* packed, int N, int G, void* stream);
 
 /*
+ * uq_set_gemm_path -- process-wide choice (default 0) of the GEMM for blocks of rows of x of the
+ * 4-bit and 2-bit formats: 0 = automatic (as uq_gemm lists); 1 = the tcgen05 tensor-core kernel for
+ * every block of 16..64 rows whose shape it supports; 2 = the mma.sync GEMM for every block of
+ * 9..64 rows.  For comparing and testing the paths: all of them meet the same rule, but their
+ * roundings differ, so they are not bit-identical to each other.  Host-only; UQ_ERR_INVALID for
+ * another value.
+ */
+uq_status uq_set_gemm_path(int path);
+
+/*
  * uq_set_launch_overlap -- process-wide switch (default 0 = off) for how uq_gemm launches its
  * GEMV and tensor-core kernels.  When on, each launch uses programmatic dependent launch: the kernel may
  * begin while the previous kernel on the same stream is still finishing, and streams its packed
@@ -291,8 +308,9 @@ uq_status uq_set_launch_overlap(int enable);
 
 /*
  * uq_gemm_kernel_count -- how many kernels uq_gemm launches for this shape on the current device
- * (the GEMV, or its second pass for rows shared between SMs; the tensor-core x conversion, GEMM
- * and second pass), for callers that account for launches.  Queries the device's SM count
+ * (the GEMV and its second pass for rows shared between SMs; the mma.sync GEMM with its x
+ * column sums (K4) and second pass; the tensor-core kernel with its x column sums (K4)), for
+ * callers that account for launches.  Queries the device's SM count
  * (CUDA runtime, no kernel launched, nothing allocated).  *count = 0 for an empty call.
  * UQ_ERR_INVALID / UQ_ERR_UNSUPPORTED as uq_gemm for shapes it rejects.
  */
@@ -316,7 +334,7 @@ uq_status uq_device_fault(unsigned int* flag);
  * critical loops that cannot take the implicit device synchronisation of cudaMalloc/cudaFree.
  * Same arguments, layouts and result as uq_gemm (x, wq, scales, zeros_or_codebook, y are caller-
  * owned device buffers), computed with the same GEMV kernel for every M (row blocks of 8; no
- * tensor-core path), so the output equals uq_gemm's for M <= 15.
+ * GEMM path), so the output equals uq_gemm's for M <= 8.
  * Scratch: a 1 MiB static device array inside the library (every GPU that loads the library holds
  * it until the process exits); 256 bytes hold the fault word, and the rest must hold what the
  * launch's work split uses for one 8-row block of x (Mb = min(M, 8); uq_gemm_noalloc_scratch

@@ -15,7 +15,7 @@ from oracle import mlp as omlp  # noqa: E402
 from oracle import quant as oquant  # noqa: E402
 from oracle.nf4 import nf4_codebook  # noqa: E402
 from synth import activations, normal_weights  # noqa: E402
-from tests.uq_helpers import KT, device_weights, device_x, y_to_f64  # noqa: E402
+from tests.uq_helpers import mma_gemm_launches, KT, device_weights, device_x, y_to_f64  # noqa: E402
 
 DEV = torch.device("cuda:0")
 FMT_GROUPS = [("INT4_SYM", 32), ("INT4_ASYM", 128), ("INT8_SYM", 128), ("INT2_ASYM", 64), ("NF4", 64), ("K4", 256)]
@@ -81,12 +81,16 @@ def test_gated_edge_cases():
 
 def test_gated_kernel_count():
     # decode (mma GEMV formats, M <= 8): gate and up in one launch, plus the second pass when the work
-    # split shares row blocks; INT8 / NF4 and the tensor-core path: a gate pass and an up pass
+    # split shares row blocks; the mma.sync GEMM (M >= 9), INT8 / NF4 and the tensor-core path: a
+    # gate pass and an up pass
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    gemm = mma_gemm_launches("INT4_ASYM", 14336, 4096, sms)
     assert uq.gemm_gated_kernel_count(1, 14336, 4096, 128, "INT4_ASYM") == 1
     assert uq.gemm_gated_kernel_count(1, 28672, 8192, 256, "K4") == 2
-    assert uq.gemm_gated_kernel_count(9, 14336, 4096, 128, "INT4_ASYM") == 2
+    assert uq.gemm_gated_kernel_count(9, 14336, 4096, 128, "INT4_ASYM") == 2 * gemm
     assert uq.gemm_gated_kernel_count(1, 8192, 8192, 128, "INT8_SYM") == 2
-    assert uq.gemm_gated_kernel_count(16, 14336, 4096, 128, "INT4_ASYM") == 2
+    assert uq.gemm_gated_kernel_count(16, 14336, 4096, 128, "INT4_ASYM") == 2               # tensor cores
+    assert uq.gemm_gated_kernel_count(70, 14336, 4096, 128, "INT4_ASYM") == 4               # two 64-row blocks
     assert uq.gemm_gated_kernel_count(0, 14336, 4096, 128, "INT4_ASYM") == 0
 
 

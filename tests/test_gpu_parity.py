@@ -15,7 +15,7 @@ from oracle import gemm as ogemm  # noqa: E402
 from oracle import quant as oquant  # noqa: E402
 from oracle.nf4 import nf4_codebook  # noqa: E402
 from synth import activations, normal_weights  # noqa: E402
-from tests.uq_helpers import KT, device_weights, device_x, h16, y_to_f64  # noqa: E402
+from tests.uq_helpers import mma_gemm_launches, KT, device_weights, device_x, h16, y_to_f64  # noqa: E402
 
 DEV = torch.device("cuda:0")
 FMT_GROUPS = [("INT4_SYM", 32), ("INT4_ASYM", 128), ("INT8_SYM", 128), ("INT2_ASYM", 64), ("NF4", 64),
@@ -155,17 +155,19 @@ def test_determinism_and_batched_rows(fmt, group):
 
 def test_kernel_count_matches_the_paths():
     # 14336 x 4096 at M = 1: whole row blocks per CTA, one launch; 4096 x 14336: the stream-K split
-    # (a partial-sum slot per tile) and its second pass; the tensor-core path: one GEMM per 64 rows
-    # (K4: after its x column-sum pre-kernel); a K that is not a multiple of the code tile keeps M = 20
-    # on the GEMV: three 8-row blocks
+    # (a partial-sum slot per tile) and its second pass; M >= 16: the tensor cores per 64 rows; 9..15 rows
+    # and K4: the mma.sync GEMM (a split k range adds its second pass, K4 its x column-sum pre-kernel);
+    # NF4 with a K that is not a multiple of the code tile keeps M = 20 on the GEMV: three 8-row blocks
     assert uq.gemm_kernel_count(1, 14336, 4096, 128, "INT4_ASYM") == 1
     assert uq.gemm_noalloc_scratch(1, 14336, 4096, 128, "INT4_ASYM") == (0, 0)
     assert uq.gemm_kernel_count(1, 4096, 14336, 128, "INT4_ASYM") == 2
     assert uq.gemm_noalloc_scratch(1, 4096, 14336, 128, "INT4_ASYM") == (0, 256 * 14 * 16 * 4)
     assert uq.gemm_kernel_count(1, 8192, 8192, 128, "INT8_SYM") == 1
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert uq.gemm_kernel_count(64, 14336, 4096, 128, "INT4_ASYM") == 1
     assert uq.gemm_kernel_count(128, 14336, 4096, 128, "INT4_ASYM") == 2
-    assert uq.gemm_kernel_count(32, 8192, 8192, 256, "K4") == 2
+    assert uq.gemm_kernel_count(9, 14336, 4096, 128, "INT4_ASYM") == mma_gemm_launches("INT4_ASYM", 14336, 4096, sms)
+    assert uq.gemm_kernel_count(32, 8192, 8192, 256, "K4") == mma_gemm_launches("K4", 8192, 8192, sms)
     assert uq.gemm_kernel_count(20, 4096, 4096, 64, "NF4") == 1
     assert uq.gemm_kernel_count(20, 4096, 4096 + 64, 64, "NF4") == 3      # K not a multiple of the tile
 

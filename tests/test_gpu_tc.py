@@ -1,5 +1,7 @@
-"""GPU parity of the tensor-core path (M >= 16): shapes it serves (N % 8 == 0, K a multiple of the
-code tile width), including a ragged last 128-row block and M that is not a multiple of 16."""
+"""GPU parity of the tcgen05 tensor-core path (M >= 16): shapes it serves (N % 8 == 0, K a multiple of
+the code tile width), including a ragged last 128-row block and M that is not a multiple of 16.  Every
+test here selects the tensor-core path for all formats (uq_set_gemm_path(1)); by default the 4-bit and
+2-bit formats take the mma.sync GEMM instead (tests/test_gpu_gemm_mma.py)."""
 import numpy as np
 import pytest
 import torch
@@ -20,8 +22,10 @@ TC_FMTS = [("INT4_ASYM", 128), ("INT4_ASYM", 32), ("INT4_SYM", 32), ("INT4_SYM",
 
 
 @pytest.fixture(autouse=True)
-def _no_fault():
+def _tensor_core_path():
+    uq.set_gemm_path("tensor_cores")
     yield
+    uq.set_gemm_path("auto")
     assert uq.device_fault() == 0, "a kernel's bounded wait ran out"
 
 

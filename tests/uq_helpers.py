@@ -41,3 +41,19 @@ def device_x(x: np.ndarray, dev) -> torch.Tensor:
 
 def y_to_f64(y: torch.Tensor) -> np.ndarray:
     return y.float().cpu().numpy().astype(np.float64)
+
+
+def mma_gemm_launches(fmt, N, K, sms):
+    """Launches of one block of 9..64 rows on the mma.sync GEMM, by the library's split rule: the k
+    units of a row group (128 rows) are split over the fewest CTAs that minimise the units of the
+    busiest SM; a split adds the second pass, K4 its x column-sum pre-kernel."""
+    kc = 128 if fmt == "INT2_ASYM" else 64
+    kp = -(-K // kc) * kc
+    ub = -(-kp // (4 * kc))
+    rg = -(-(-(-N // 16)) // 8)
+    best, best_load = 1, None
+    for ks in range(1, min(ub, 64) + 1):
+        load = -(-(rg * ks) // sms) * -(-ub // ks)
+        if best_load is None or load < best_load:
+            best, best_load = ks, load
+    return 1 + (1 if best > 1 else 0) + (1 if fmt == "K4" else 0)
