@@ -671,9 +671,9 @@ uq_status uq_gemm_w4a8(const uint16_t* x, const void* wq, const void* scales, co
     if ((s = device_state(&ds, &dev)) != UQ_OK) return s;
     const uq::Layout L(N, K, fmt);
     const int Kp = L.Kp, G = (Kp + group - 1) / group;
-    // scratch: x codes [M][Kp] | s_x [M] | per (row, group, lane column) code sums [M][G][4]; partial sums
+    // scratch: x codes [M][Kp] | s_x [M] | per (row, group) code sums [M][G]; partial sums
     const size_t xq_b = ((size_t)M * Kp + 255) / 256 * 256, sx_b = ((size_t)M * 4 + 255) / 256 * 256;
-    const size_t aux = xq_b + sx_b + (size_t)M * G * 4 * sizeof(int);
+    const size_t aux = xq_b + sx_b + (size_t)M * G * sizeof(int);
     Workspace* ws = nullptr;
     const int rows8 = M < 8 ? M : 8;
     if ((s = workspace(dev, st, (size_t)L.NB * L.KB * RB_ROWS * rows8 * sizeof(float), (size_t)L.NB * sizeof(unsigned int),
@@ -698,7 +698,7 @@ uq_status uq_gemm_w4a8(const uint16_t* x, const void* wq, const void* scales, co
         a.tickets = ws->tickets;
         a.fault = ds->words;
         const int grid = uq::gemv_plan(a, fmt, ds->sms);
-        e = uq::launch_gemv_a8(fmt, a, xq + (long long)m0 * Kp, sx + m0, sxl + (long long)m0 * G * 4, Kp, grid, st);
+        e = uq::launch_gemv_a8(fmt, a, xq + (long long)m0 * Kp, sx + m0, sxl + (long long)m0 * G, Kp, grid, st);
         if (e != cudaSuccess) return cuda_fail(e, "W4A8 GEMV launch");
     }
     return UQ_OK;

@@ -3,27 +3,32 @@
 // "Ultra LLM Engine", section "Quantized Model": the activations are dynamically quantized for the
 // GEMV/GEMM paths.  Per row m of x: s_x = absmax / 127 (fp32), xq = clamp(RNE(x / s_x), -127, 127)
 // (fp32 quotient); then y[m][n] = s_x * sum_g s[n][g] * I, I = sum_{k in g} xq * (q - z), an exact
-// integer formed with dp4a (four int8 products and their sum per instruction).
+// integer formed on the integer tensor instructions (mma.m16n8k32, u8 x s8 -> s32).
 //
 // quant_x_kernel (one CTA per row): absmax, s_x, the codes, written with each 4-k group's bytes in the
 // order the weight words hold their codes (4-bit: k, k+2, k+1, k+3 -- the low nibbles of a fragment-
-// order word; 8-bit: k .. k+3), and per (group, lane column c) the sum of the codes that lane multiplies,
-// for the zero-point term.
+// order word; 8-bit: k .. k+3) and the 4-k groups placed in the integer mma's B fragment order, and per
+// group the sum of its codes, for the zero-point term.
 // gemv_a8_kernel: the decode GEMV's tiles, copy rings and work split (whole row blocks per CTA, or the
-// stream-K split and its second pass), with the integer inner loop: per 16-k block a lane takes its
-// code word, masks the two rows' codes into bytes (w & 0x0F0F0F0F, (w >> 4) & 0x0F0F0F0F for 4-bit),
-// and accumulates one dp4a per row and activation row.  Per group: acc += s * (I - zc * SX), zc the
-// stored code's offset (8 for INT4_SYM, z for INT4_ASYM, 128 for INT8_SYM).
+// stream-K split and its second pass), with an integer tensor-core inner loop: per pair of 16-k blocks
+// a lane takes its two code words, masks the two rows' codes into bytes (w & 0x0F0F0F0F,
+// (w >> 4) & 0x0F0F0F0F for 4-bit; INT8 words are already bytes) -- the A fragment of
+// mma.m16n8k32 (u8 x s8 -> s32) -- and one instruction forms the exact integer sums of 16 weight
+// rows x 8 rows of x over 32 k.  Per group: acc += s * (D - zc * SX), zc the stored code's offset
+// (8 for INT4_SYM, z for INT4_ASYM, 128 for INT8_SYM).
 #include "uq_gemv.cuh"
 
 namespace uq {
 
 namespace {
 
-__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
-    int d;
-    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
+// D += A * B for one 16 x 8 x 32 block: A unsigned 8-bit (the stored codes), B signed 8-bit (x codes),
+// exact 32-bit integer accumulation
+__device__ __forceinline__ void mma_u8s8(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // one CTA (256 threads) per row of x
@@ -44,7 +49,9 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const uint16_t* __restrict
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) amax = fmaxf(amax, red[w]);
     const float s = __fdiv_rn(amax, 127.0f);
     if (threadIdx.x == 0) sx[m] = s;
-    // codes, 4 per thread step (one 4-k group), in the weight words' byte order
+    // codes, 4 per thread step (one 4-k group), in the weight words' byte order, placed in the B
+    // fragment order of the integer mma: per 32 k and lane column c, the 4 codes of k = 32t + 4c ..
+    // then those of k = 32t + 16 + 4c .. (8 contiguous bytes, one load per instruction)
     int8_t* qr = xq + (long long)m * Kp;
     for (int k4 = threadIdx.x * 4; k4 < Kp; k4 += blockDim.x * 4) {
         int q[4];
@@ -60,19 +67,18 @@ __global__ void __launch_bounds__(256) quant_x_kernel(const uint16_t* __restrict
                                         ((uint32_t)(q[1] & 255) << 16) | ((uint32_t)(q[3] & 255) << 24))
                                      : ((uint32_t)(q[0] & 255) | ((uint32_t)(q[1] & 255) << 8) |
                                         ((uint32_t)(q[2] & 255) << 16) | ((uint32_t)(q[3] & 255) << 24));
-        *reinterpret_cast<uint32_t*>(qr + k4) = packed;
+        const int blk = k4 >> 4, cc = (k4 >> 2) & 3;
+        *reinterpret_cast<uint32_t*>(qr + (blk >> 1) * 32 + cc * 8 + (blk & 1) * 4) = packed;
     }
-    // per (group, c): the sum of the codes at k = 16 b + 4 c .. + 3 of the group's blocks b
+    // per group: the sum of its codes (k < K)
     const int G = (Kp + gs - 1) / gs;
-    for (int e = threadIdx.x; e < G * 4; e += blockDim.x) {
-        const int gi = e >> 2, c = e & 3;
+    for (int gi = threadIdx.x; gi < G; gi += blockDim.x) {
         int tot = 0;
-        for (int k = gi * gs + 4 * c; k < gi * gs + gs && k < K; k += 16)
-            for (int j = 0; j < 4 && k + j < K; ++j) {
-                float v = (s > 0.f) ? rintf(__fdiv_rn(bf16lo_f32(xr[k + j]), s)) : 0.f;
-                tot += (int)fminf(fmaxf(v, -127.f), 127.f);
-            }
-        sxl[(long long)m * G * 4 + e] = tot;
+        for (int k = gi * gs; k < gi * gs + gs && k < K; ++k) {
+            const float v = (s > 0.f) ? rintf(__fdiv_rn(bf16lo_f32(xr[k]), s)) : 0.f;
+            tot += (int)fminf(fmaxf(v, -127.f), 127.f);
+        }
+        sxl[(long long)m * G + gi] = tot;
     }
 }
 
@@ -151,14 +157,10 @@ __global__ void __launch_bounds__(128, MMA_CTAS_PER_SM) gemv_a8_kernel(const Gem
     if (has_work && issued == 0 && ntl > 0) issue_next();
     if (!has_work) return;
 
-    float acc[2][8];
+    float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};   // rows g + 8 jr, columns 2c + e
+    float sxm[2];                                 // the scales of x of columns 2c, 2c + 1
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int m = 0; m < 8; ++m) acc[j][m] = 0.f;
-    float sxm[8];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) sxm[m] = m < M ? __ldg(sxs + m) : 0.f;
+    for (int e = 0; e < 2; ++e) sxm[e] = 2 * c + e < M ? __ldg(sxs + 2 * c + e) : 0.f;
 
     int ckb = ntl > 0 ? kb_of(t0) : 0, crb = ntl > 0 ? (int)(t0 % R) : 0;   // the tile being consumed
     for (int li = 0; li < ntl; ++li) {
@@ -177,83 +179,58 @@ __global__ void __launch_bounds__(128, MMA_CTAS_PER_SM) gemv_a8_kernel(const Gem
         RowPtrs<FMT> rp[2];
         rp[0] = row_ptrs<FMT>(st, mc, g, n0 + g, kb);
         rp[1] = row_ptrs<FMT>(st, mc, g + 8, n0 + g + 8, kb);
+        // lane (g, c): rows g, g + 8 of D; columns (rows of x) 2c, 2c + 1
+        const int m0c = 2 * c < M ? 2 * c : M - 1, m1c = 2 * c + 1 < M ? 2 * c + 1 : M - 1;
+        const uint8_t* xg = reinterpret_cast<const uint8_t*>(xq) + (long long)(g < M ? g : M - 1) * Kp + 8 * c;
 #pragma unroll 1
         for (int gg = 0; gg < ng; ++gg) {
-            int I0[8], I1[8];
+            // the group's exact integer sum of (stored code) x (x code) per row and column: GB / 2
+            // instructions of m16n8k32 (u8 x s8 -> s32), each over two 16-k blocks
+            int d[4] = {0, 0, 0, 0};
 #pragma unroll
-            for (int m = 0; m < 8; ++m) I0[m] = I1[m] = 0;
-#pragma unroll
-            for (int j = 0; j < GB; ++j) {
-                const int blk = gg * GB + j;                        // block within the tile
-                const int kk = kb * KT + blk * 16 + 4 * c;          // this lane's 4 k
-                uint32_t lo, hi;
+            for (int t = 0; t < GB / 2; ++t) {
+                const int blk = gg * GB + 2 * t;                    // even block of the pair, within the tile
+                uint32_t a0, a1, a2, a3;
                 if constexpr (FMT == UQ_INT8_SYM) {
-                    // chunk = 2 blocks; word 2b + h of the lane's 16 bytes = row g + 8h, k 4c .. 4c + 3 of block b
-                    const uint8_t* cp = st + (blk / BPCH) * CHUNK + lane * 16 + (blk % BPCH) * 8;
-                    const uint2 v = *reinterpret_cast<const uint2*>(cp);
-                    lo = v.x;
-                    hi = v.y;
+                    // one chunk = the pair: row g, row g + 8 of the even block, then of the odd one
+                    const uint4 v = *reinterpret_cast<const uint4*>(st + (blk / BPCH) * CHUNK + lane * 16);
+                    a0 = v.x; a1 = v.y; a2 = v.z; a3 = v.w;
                 } else {
-                    const uint32_t wd = *reinterpret_cast<const uint32_t*>(st + (blk / BPCH) * CHUNK + lane * 16 +
-                                                                           (blk % BPCH) * 4);
-                    lo = wd & 0x0F0F0F0Fu;                          // row g:     k, k+2, k+1, k+3
-                    hi = (wd >> 4) & 0x0F0F0F0Fu;                   // row g + 8: the same order
+                    const uint2 v = *reinterpret_cast<const uint2*>(st + (blk / BPCH) * CHUNK + lane * 16 + (blk % BPCH) * 4);
+                    a0 = v.x & 0x0F0F0F0Fu;                         // row g:     k, k+2, k+1, k+3
+                    a1 = (v.x >> 4) & 0x0F0F0F0Fu;                  // row g + 8: the same order
+                    a2 = v.y & 0x0F0F0F0Fu;
+                    a3 = (v.y >> 4) & 0x0F0F0F0Fu;
                 }
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    if (m < M) {
-                        const uint32_t xw = (kk < Kp) ? __ldg(reinterpret_cast<const uint32_t*>(xq + (long long)m * Kp + kk)) : 0u;
-                        I0[m] = dp4a_us(lo, xw, I0[m]);
-                        I1[m] = dp4a_us(hi, xw, I1[m]);
-                    }
-                }
+                // x codes of the pair for column g, stored in this fragment's order
+                const uint2 bv = *reinterpret_cast<const uint2*>(xg + (long long)(kb * KT + blk * 16));
+                mma_u8s8(d, a0, a1, a2, a3, bv.x, bv.y);
             }
-            // fold the group: acc += s * (I - zc * SX)
+            // fold the group: acc += s * (D - zc * SX), SX the sum of the group's x codes of the column
             const int gi = gi0 + gg;
+            const int sx0 = __ldg(sxl + (long long)m0c * Gq + gi), sx1 = __ldg(sxl + (long long)m1c * Gq + gi);
 #pragma unroll
             for (int jr = 0; jr < 2; ++jr) {
                 float sc, zcf;
                 row_meta<FMT>(rp[jr], gg, sc, zcf);               // 4-bit: zcf = 128 + the stored code offset
                 const int zc = (FMT == UQ_INT8_SYM) ? 128 : (int)zcf - 128;   // INT8 codes are stored + 128
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    if (m < M) {
-                        const int sxv = __ldg(sxl + ((long long)m * Gq + gi) * 4 + c);
-                        const int I = (jr ? I1[m] : I0[m]) - zc * sxv;
-                        acc[jr][m] = fmaf(sc, (float)I, acc[jr][m]);
-                    }
-                }
+                acc[jr][0] = fmaf(sc, (float)(d[2 * jr] - zc * sx0), acc[jr][0]);
+                acc[jr][1] = fmaf(sc, (float)(d[2 * jr + 1] - zc * sx1), acc[jr][1]);
             }
         }
         __syncwarp();
-        // the tile's partial sums: the 4 lanes of a row combined (fixed order), then stored like the mma GEMV's
-        float out[2][8];
+        // the tile's partial sums (rows g + 8 jr, columns 2c + e), stored like the mma GEMV's
 #pragma unroll
         for (int jr = 0; jr < 2; ++jr)
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {
-                float v = acc[jr][m];
-                v += __shfl_xor_sync(0xffffffffu, v, 1);
-                v += __shfl_xor_sync(0xffffffffu, v, 2);
-                out[jr][m] = v * sxm[m];
-                acc[jr][m] = 0.f;
+            for (int e = 0; e < 2; ++e) {
+                const int m = 2 * c + e;
+                const float v = acc[jr][e] * sxm[e];
+                acc[jr][e] = 0.f;
+                if (m >= M) continue;
+                if (cta_rows) cpart[(i * RB + g + 8 * jr) * 8 + m] = v;   // slot = the tile's index in the CTA's range
+                else a.partials[(i * RB + g + 8 * jr) * M + m] = v;
             }
-        if (c == 0) {
-            if (cta_rows) {
-                float* part = cpart + (i * RB) * 8;                 // slot = the tile's index in the CTA's range
-#pragma unroll
-                for (int jr = 0; jr < 2; ++jr)
-#pragma unroll
-                    for (int m = 0; m < 8; ++m) part[(g + 8 * jr) * 8 + m] = out[jr][m];
-            } else {
-                float* part = a.partials + i * RB * M;
-#pragma unroll
-                for (int jr = 0; jr < 2; ++jr)
-#pragma unroll
-                    for (int m = 0; m < 8; ++m)
-                        if (m < M) part[(g + 8 * jr) * M + m] = out[jr][m];
-            }
-        }
     }
     cp_async_wait_group<0>();
     if (!cta_rows) return;

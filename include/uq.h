@@ -225,7 +225,8 @@ uq_status uq_rmsnorm_rope(const uint16_t* x, const uint16_t* gamma, const int32_
  * symmetric per-row int8):
  *     s_x[m] = absmax_k |x[m][k]| / 127 (fp32),  xq = clamp(RNE(x / s_x), -127, 127) (fp32 quotient),
  *     y[m][n] = bf16_RNE( s_x[m] * sum_g s[n][g] * sum_{k in g} xq[m][k] * (q[n][k] - z[n][g]) ),
- * the inner sums exact integers (dp4a), the per-group scaling and the sum over groups in fp32.
+ * the inner sums exact integers (integer tensor instructions, u8 x s8 -> s32), the per-group scaling
+ * and the sum over groups in fp32.
  * Weights: UQ_INT4_SYM, UQ_INT4_ASYM (W4A8) or UQ_INT8_SYM (W8A8), as uq_gemm takes them.  Arguments,
  * layouts, errors and scratch as uq_gemm (the x codes, s_x and the per-group code sums live in the
  * per-stream workspace).  Launches: the activation quantization, then per block of 8 rows of x the
