@@ -10,6 +10,29 @@ extern template cudaError_t launch_gemv_fmt<UQ_INT2_ASYM>(const GemvArgs&, int, 
 extern template cudaError_t launch_gemv_fmt<UQ_NF4>(const GemvArgs&, int, cudaStream_t);
 extern template cudaError_t launch_gemv_fmt<UQ_K4>(const GemvArgs&, int, cudaStream_t);
 
+// Per-warp rings (the W4A8 GEMV and gemv_warp_kernel): W warps per CTA, cps CTAs per SM.  Whole row
+// blocks per CTA need no second pass; take them when no warp gets more tiles than under the
+// stream-K split and either the busiest CTA streams at most ~6 % more bytes than the average one
+// (bandwidth-bound shapes) or no warp has more than one tile (latency-bound ones).  (gated: the
+// units CTAs own are gate/up pairs of row blocks)
+static int plan_warp_rings(GemvArgs& a, int sms, int W, int cps, int tpw) {
+    const int WU = a.gated ? 2 : 1;
+    const int NBU = a.NB / WU;
+    const long long P = (long long)sms * cps * W;
+    a.P = (int)(P < a.T ? P : a.T);
+    const int slots = sms * cps;                                       // CTAs resident at once
+    const int G = NBU < slots ? NBU : slots;
+    const long long rbs = G > 0 ? (NBU + G - 1) / G : 0;
+    const long long per_warp_rows = (rbs * WU * a.KB + W - 1) / W;
+    const long long per_warp_split = (a.T + a.P - 1) / a.P;
+    const bool even = rbs * G * 100 <= (long long)NBU * 106;
+    if (G > 0 && per_warp_rows <= tpw && per_warp_rows <= per_warp_split && (even || per_warp_rows <= 1)) {
+        a.cta_rows = 1;
+        return G;
+    }
+    return a.P < slots ? a.P : slots;
+}
+
 int gemv_plan(GemvArgs& a, int fmt, int sms) {
     a.cta_rows = 0;
     if (!gemv_is_mma(fmt) && !a.a8) {
@@ -18,28 +41,39 @@ int gemv_plan(GemvArgs& a, int fmt, int sms) {
         a.P = (int)(P < a.T ? P : a.T);
         return (a.P + GEMV_WARPS - 1) / GEMV_WARPS;
     }
-    if (!a.a8 && gemv_smem_bytes_impl(fmt, a.K, a.group, a.M) > 227 * 1024) return 0;
-    // mma and W4A8 GEMVs: W warps per CTA, two CTAs per SM.  Whole row blocks per CTA need no second
-    // pass; take them when no warp gets more tiles than under the stream-K split and either the
-    // busiest CTA streams at most ~6 % more bytes than the average one (bandwidth-bound shapes) or
-    // no warp has more than one tile (latency-bound ones).  (gated: the units CTAs own are gate/up
-    // pairs of row blocks)
-    const int W = a.a8 ? 4 : gemv_warps_impl(fmt);
-    const long long P = (long long)sms * MMA_CTAS_PER_SM * W;
-    a.P = (int)(P < a.T ? P : a.T);
     const int WU = a.gated ? 2 : 1;
     const int NBU = a.NB / WU;
-    const int slots = sms * MMA_CTAS_PER_SM;                           // CTAs resident at once
+    if (a.a8) return plan_warp_rings(a, sms, 4, A8_CTAS_PER_SM, A8_TPW);
+    if (gemv_warp_route(fmt, a.M)) return plan_warp_rings(a, sms, WarpCfg<UQ_INT4_ASYM>::WARPS, WARP_CTAS_PER_SM, WARP_TPW);
+    // mma GEMV: one CTA per SM, its work (pairs of k tiles) shared by MMA_CW compute warps.  Whole
+    // row blocks per CTA (a.cta_rows = the most tiles a CTA gets) need no second pass; take them
+    // when every compute warp has one tile at most (latency-bound shapes), or when no CTA gets more
+    // tiles than under the stream-K split and the busiest CTA streams at most ~6 % more bytes than
+    // the average one.
+    const int slots = sms;
+    const long long KB2 = (a.KB + 1) / 2;
+    const long long P2 = (long long)a.NB * KB2;                        // pairs of k tiles
+    if (P2 >= (1LL << 31)) return 0;                                   // the kernel splits in 32-bit arithmetic
+    const int grid_split = (int)(P2 < slots ? P2 : slots);
+    const long long per_cta_split = 2 * ((P2 + grid_split - 1) / grid_split);
     const int G = NBU < slots ? NBU : slots;
-    const long long rbs = (NBU + G - 1) / G;
-    const long long per_warp_rows = (rbs * WU * a.KB + W - 1) / W;
-    const long long per_warp_split = (a.T + a.P - 1) / a.P;
-    const bool even = rbs * G * 100 <= (long long)NBU * 106;
-    if (G > 0 && per_warp_rows <= MMA_TPW && per_warp_rows <= per_warp_split && (even || per_warp_rows <= 1)) {
-        a.cta_rows = 1;
-        return G;
+    int grid = grid_split;
+    if (G > 0) {
+        const long long rbs = (NBU + G - 1) / G;
+        const long long tc = rbs * WU * 2 * KB2;
+        const bool even = rbs * G * 100 <= (long long)NBU * 106;
+        if (tc <= MMA_TPC && (tc <= MMA_CW || (tc <= per_cta_split && even))) {
+            a.cta_rows = (int)tc;
+            grid = G;
+        }
     }
-    return a.P < slots ? a.P : slots;
+    a.P = grid;
+    const int sxg = gemv_mma_sx_groups(fmt, a.group, a.NB, a.KB, grid, a.cta_rows);
+    if (gemv_mma_smem(fmt, a.K, a.group, a.M, sxg, a.cta_rows, MMA_X_GLOBAL).S2 < MMA_CW / 2 + 2) {
+        a.cta_rows = 0;
+        return 0;
+    }
+    return grid;
 }
 
 size_t gemv_partials_floats(int fmt, const GemvArgs& a) {

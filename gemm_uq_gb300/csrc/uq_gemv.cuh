@@ -6,29 +6,29 @@
 // three issue slots per 4-bit weight) cannot keep up with HBM, so the 4-bit and 2-bit formats
 // run on warp-level tensor instructions:
 //
-//  * gemv_mma_kernel (INT4_SYM, INT4_ASYM, INT2_ASYM, K4).  Work is the list of tiles (16 rows x
-//    8 KB of codes), taken in k-major order so a warp's consecutive tiles share their k tile.
-//    Either every CTA owns whole 16-row blocks and its warps split their tiles evenly (partial
-//    sums of each tile in shared memory, summed per row in k order after one CTA barrier: no
-//    second launch), or every warp owns an equal contiguous range of all tiles (stream-K) and
-//    stores each tile's partial sums in global memory for gemv_split_reduce, a second launch
-//    that sums each row over its k tiles in k order.  Both orders are fixed, so results are
-//    bit-reproducible, and no warp ever waits for another.
-//  * Each warp keeps a ring of two stages; a stage is one tile's codes plus the tile rows'
-//    scales / zero points / K4 records, copied by all 32 lanes with 16-byte (codes: 512
-//    contiguous bytes per warp instruction) or 4-byte cp.async in one cp.async group per tile
-//    that the warp waits for itself.  With launch overlap the first tile is requested before
-//    the wait for the previous kernel on the stream (the weights are constant).
-//  * x: one or two rows are copied per warp a k tile at a time (one bulk copy per row, double
-//    buffered); more rows are copied whole into shared memory once per CTA, or read through L1
-//    when they do not fit.  The sums of x over each scaling group of a k tile are formed once
-//    per run of tiles at that k tile.
 //  * The packed plane is in mma.m16n8k16 A-fragment order: one 16-byte shared-memory load per
 //    lane, a shift and a lop3 per register (magic exponent: bf16 0x4300 | code = 128 + code)
 //    give the A fragments, and mma.sync (bf16 x bf16 -> fp32) does the multiply-accumulate and
 //    the reduction over the 16-wide k block in one instruction; the M <= 8 activation rows are
 //    the instruction's N = 8, so every M <= 8 costs the same.  Per scaling group the fp32 group
 //    sum is folded into the row's accumulator:  y += s * (sum x*(128 + q) - (128 + z) * sum x).
+//  * Work is the list of tiles (16 rows x 8 KB of codes) in k-major order.  Either every CTA owns
+//    whole 16-row blocks (partial sums of each tile in shared memory, summed per row in k order
+//    after a CTA barrier: no second launch), or CTAs own equal contiguous ranges of all tiles
+//    (stream-K) and store each tile's partial sums in global memory for gemv_split_reduce, a
+//    second launch that sums each row over its k tiles in k order.  Both orders are fixed, so
+//    results are bit-reproducible, and a row's result is the same for either split and any M.
+//  * gemv_mma_kernel (INT4_SYM, INT4_ASYM, INT2_ASYM, K4 at M = 1..8, except the case below):
+//    one CTA per SM, a copy warp feeding 12 compute warps through one ring of tile pairs (one
+//    16 KB bulk copy per pair) in nearly all of shared memory; x whole in shared memory or read
+//    through L1; the sums of x over each scaling group in a table formed once per CTA.
+//  * gemv_warp_kernel (INT4_SYM, INT4_ASYM at M = 1): the same per-tile arithmetic on per-warp
+//    rings of two stages (16-byte cp.async by each warp's own lanes) and double-buffered slices
+//    of x, two CTAs per SM.  Its launches are short, and two ~105 KB CTAs per SM let the next
+//    launch on the stream start streaming while the current one finishes; measured faster there.
+//    Both kernels form the sums of x in the same order, so they give the same rows.
+//    With launch overlap both request their first weights before waiting for the previous
+//    kernel on the stream (the weights are constant).
 //  * gemv_kernel (INT8_SYM, NF4, whose codes do not map onto bf16 exactly by a bit trick): the
 //    same layout on CUDA-core FMAs, four stages per warp on mbarriers; the four lanes sharing a
 //    row are reduced with warp shuffles, and a row block split between workers is finished by
@@ -45,16 +45,22 @@ template <int FMT> struct GemvFmt {
     static constexpr int BPC = KC / 16;                            // 16-wide k blocks per chunk
     static constexpr bool MMA = (FMT == UQ_INT4_SYM || FMT == UQ_INT4_ASYM || FMT == UQ_K4 || FMT == UQ_INT2_ASYM);
     static constexpr int GT_MAX = KT / 32;                         // groups per tile row at group 32
-    // 32-bit words of metadata staged per tile row: scales (+1 for a misaligned start), zeros
-    // (rounded up to 4 words so 16-byte copies land 16-byte aligned)
-    static constexpr int SW = (FMT == UQ_K4) ? 16 : (GT_MAX / 2 + 1 + 3) / 4 * 4;
-    static constexpr int ZW = (FMT == UQ_INT4_ASYM) ? (GT_MAX / 8 + 1 + 3) / 4 * 4
-                            : (FMT == UQ_INT2_ASYM ? (GT_MAX / 2 + 1 + 3) / 4 * 4 : 0);
+    static constexpr int STAGES = (FMT == UQ_INT2_ASYM) ? 3 : 4;
+    static constexpr bool NEEDS_SX = MMA;                          // per-group sums of x
+};
+
+// Stage geometry: a stage is one tile's codes followed by its rows' metadata, MW 32-bit words per
+// row: scales (+1 word for a misaligned start), then zeros, each rounded up to 4 words so 16-byte
+// copies land 16-byte aligned.  GT = groups per tile row the stage must hold (0: as many as the
+// smallest group, 32, gives).  K4 rows hold their 16-byte super-block records.
+template <int FMT, int GT = 0> struct MetaGeom {
+    static constexpr int GTM = GT ? GT : GemvFmt<FMT>::GT_MAX;
+    static constexpr int SW = (FMT == UQ_K4) ? 16 : (GTM / 2 + 1 + 3) / 4 * 4;
+    static constexpr int ZW = (FMT == UQ_INT4_ASYM) ? (GTM / 8 + 1 + 3) / 4 * 4
+                            : (FMT == UQ_INT2_ASYM ? (GTM / 2 + 1 + 3) / 4 * 4 : 0);
     static constexpr int MW = SW + ZW;
     static constexpr int META_BYTES = (RB * MW * 4 + 15) / 16 * 16;
     static constexpr int STAGE_BYTES = TILE_BYTES + META_BYTES;
-    static constexpr int STAGES = (FMT == UQ_INT2_ASYM) ? 3 : 4;
-    static constexpr bool NEEDS_SX = MMA;                          // per-group sums of x
 };
 
 // bytes per row of x in shared memory: the row zero-padded to Kp plus 32 bytes, so the rows of a
@@ -71,7 +77,7 @@ __host__ __device__ inline GemvSmem gemv_smem_plan_t(int K, int group, int M, bo
     const int Kp = (K + F::KC - 1) / F::KC * F::KC;
     const int gs = (FMT == UQ_K4) ? 32 : group;
     GemvSmem p;
-    p.bars = (size_t)GEMV_WARPS * F::STAGES * F::STAGE_BYTES;
+    p.bars = (size_t)GEMV_WARPS * F::STAGES * MetaGeom<FMT>::STAGE_BYTES;
     p.lut = p.bars + (size_t)(GEMV_WARPS * F::STAGES + 1) * 8;     // + the x mbarrier
     p.sx = p.lut + 64;
     p.x = p.sx + (F::NEEDS_SX ? (size_t)((Kp + gs - 1) / gs) * 8 * 4 : 0);   // sums padded to 8 columns
@@ -175,26 +181,20 @@ struct GemvSrc {
     const uint8_t* zc;
 };
 
-// Issue the copies of tile t into stage buffer `st` (all lanes take part).  Either the codes come
-// as one bulk copy counted on `bar` (transaction bytes) and the metadata copies arrive on `bar`
-// too (33 arrivals in all: one per lane when its copies land, and the codes' expect_tx), or, with
-// GROUP, everything is 16-byte cp.async (codes: 512 contiguous bytes per warp instruction) in one
-// cp.async group per lane that the issuing warp itself waits for (`bar` unused).  The per-lane
-// copies keep more of the tile stream in flight than one 8 KB bulk copy per tile: the copy engine
-// takes bulk copies one after another, at well under an SM's share of HBM bandwidth at this size.
-// GTC: the groups per tile row when the caller knows them at compile time (0: mc.GT at run time).
-template <int FMT, bool GROUP = false, int GTC = 0>
-__device__ __forceinline__ void issue_tile(const GemvArgs& a, const GemvSrc& w, const Layout& L, const MetaConst& mc, int nb, int kb,
-                                           uint8_t* st, uint64_t* bar, int lane) {
-    using F = GemvFmt<FMT>;
+// Copy the metadata of tile (nb, kb)'s rows (scales, zero points or K4 records) into md, laid out
+// as MetaGeom<FMT, GEO>, with cp.async by all lanes (not committed or counted here).  GTC: the
+// groups per tile row when the caller knows them at compile time (0: mc.GT at run time).
+template <int FMT, int GTC = 0, int GEO = 0>
+__device__ __forceinline__ void issue_meta(const GemvArgs& a, const GemvSrc& w, const MetaConst& mc, int nb, int kb,
+                                           uint32_t* md, int lane) {
+    using F = MetaGeom<FMT, GEO>;
     const int n0 = nb * RB;
     const int rows = (a.N - n0) < RB ? (a.N - n0) : RB;            // rows with metadata
-    uint32_t* md = reinterpret_cast<uint32_t*>(st + TILE_BYTES);
     if constexpr (FMT == UQ_K4) {
         // 16-byte records: one per 256 k of the tile row that lies inside K
-        const int sb0 = kb * (F::KT / 256);
+        const int sb0 = kb * (GemvFmt<FMT>::KT / 256);
         int recs = mc.S4 - sb0;
-        if (recs > F::KT / 256) recs = F::KT / 256;
+        if (recs > GemvFmt<FMT>::KT / 256) recs = GemvFmt<FMT>::KT / 256;
         for (int e = lane; e < rows * recs; e += 32) {
             const int r = e / recs, j = e % recs;
             cp_async16(md + r * F::MW + 4 * j, w.scales + ((long long)(n0 + r) * mc.S4 + sb0 + j) * 16);
@@ -236,7 +236,24 @@ __device__ __forceinline__ void issue_tile(const GemvArgs& a, const GemvSrc& w, 
             }
         }
     }
-    if constexpr (GROUP) {
+}
+
+// Issue the copies of tile t into stage buffer `st` (its codes, then its metadata at st +
+// TILE_BYTES; all lanes take part), in one of two modes:
+//   ISSUE_BULK   the codes as one bulk copy counted on `bar` (transaction bytes), the metadata as
+//                cp.async arriving on `bar` too (33 arrivals: one per lane when its copies land,
+//                and the codes' expect_tx);
+//   ISSUE_GROUP  everything 16-byte cp.async (codes: 512 contiguous bytes per warp instruction) in
+//                one cp.async group per lane that the issuing warp itself waits for (`bar` unused).
+// Per-lane copies keep more of a warp's tile stream in flight than one 8 KB bulk copy per tile:
+// the copy engine takes bulk copies one after another, at well under an SM's share of HBM
+// bandwidth at this size.
+constexpr int ISSUE_BULK = 0, ISSUE_GROUP = 1;
+template <int FMT, int MODE = ISSUE_BULK, int GTC = 0>
+__device__ __forceinline__ void issue_tile(const GemvArgs& a, const GemvSrc& w, const Layout& L, const MetaConst& mc, int nb, int kb,
+                                           uint8_t* st, uint64_t* bar, int lane) {
+    issue_meta<FMT, GTC>(a, w, mc, nb, kb, reinterpret_cast<uint32_t*>(st + TILE_BYTES), lane);
+    if constexpr (MODE == ISSUE_GROUP) {
         const int bytes = (int)L.tile_bytes(kb);
         const uint8_t* src = w.wq + L.tile_offset(nb, kb);
         for (int off = lane * 16; off < bytes; off += 512) cp_async16(st + off, src + off);
@@ -261,9 +278,9 @@ struct RowPtrs {
     const uint16_t* s;
     const uint8_t* z;
 };
-template <int FMT>
+template <int FMT, int GEO = 0>
 __device__ __forceinline__ RowPtrs<FMT> row_ptrs(const uint8_t* st, const MetaConst& mc, int r, int n, int kb) {
-    using F = GemvFmt<FMT>;
+    using F = MetaGeom<FMT, GEO>;
     const uint8_t* row = st + TILE_BYTES + r * F::MW * 4;
     const unsigned first = (unsigned)n * (unsigned)mc.G + (unsigned)kb * (unsigned)mc.GT;   // low bits only
     RowPtrs<FMT> p;
@@ -298,7 +315,7 @@ __device__ __forceinline__ void row_meta(const RowPtrs<FMT>& p, int li, float& s
 
 // K4: d*sc and dmin*m of row r for the tile's local 32-k sub-block li
 __device__ __forceinline__ void row_meta_k4(const uint8_t* st, int r, int li, float& dsc, float& dmm) {
-    const uint8_t* row = st + TILE_BYTES + r * GemvFmt<UQ_K4>::MW * 4;
+    const uint8_t* row = st + TILE_BYTES + r * MetaGeom<UQ_K4>::MW * 4;
     const uint4 rec = *reinterpret_cast<const uint4*>(row + 16 * (li >> 3));
     const int j = li & 7;
     const uint64_t sc48 = (uint64_t)rec.y | ((uint64_t)(rec.z & 0xFFFFu) << 32);
@@ -337,7 +354,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
     const size_t xstride = gemv_x_stride(L.Kp);
     // 16-byte metadata copies: row slices 16-byte aligned and a multiple of 16 bytes long
     mc.aligned = (a.K % (8 * a.group)) == 0 && (mc.GT % 8) == 0;
-    uint8_t* ring = smem + (size_t)warp * S * F::STAGE_BYTES;
+    uint8_t* ring = smem + (size_t)warp * S * MetaGeom<FMT>::STAGE_BYTES;
     uint64_t* bars = bars_all + warp * S;
     const long long t0 = has_work ? range_begin(w, a.T, a.P) : 0;
     const long long t1 = has_work ? range_begin(w + 1, a.T, a.P) : 0;
@@ -356,7 +373,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
         __syncwarp();
         int inb = (int)(t0 / L.KB), ikb = (int)(t0 % L.KB);
         for (int s = 0; s < S && t0 + s < t1; ++s) {
-            issue_tile<FMT>(a, GemvSrc{a.wq, a.scales, a.zc}, L, mc, inb, ikb, ring + s * F::STAGE_BYTES, &bars[s], lane);
+            issue_tile<FMT>(a, GemvSrc{a.wq, a.scales, a.zc}, L, mc, inb, ikb, ring + s * MetaGeom<FMT>::STAGE_BYTES, &bars[s], lane);
             if (++ikb == L.KB) { ikb = 0; ++inb; }
         }
     }
@@ -430,7 +447,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
         const int s = it % S;
         const uint32_t parity = (uint32_t)((it / S) & 1);
         const int n0 = nb * RB;
-        uint8_t* st = ring + s * F::STAGE_BYTES;
+        uint8_t* st = ring + s * MetaGeom<FMT>::STAGE_BYTES;
         const int nchunks = L.chunks(kb);
         const int blk0 = (kb * KT) / 16;                           // first global 16-k block of the tile
 
@@ -606,94 +623,592 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
 // K4 uses its 32-weight sub-blocks, GB = 2).  M (1..8) is a runtime value: the instruction always
 // computes 8 columns, so the work per weight does not depend on it.
 //
+// One CTA per SM: a copy warp and MMA_CW compute warps around one ring.  A ring slot holds a pair
+// of tiles, two consecutive k tiles of one row block (16 KB of codes, contiguous in the packed
+// plane, plus both tiles' metadata).  The copy warp requests the CTA's pairs in order: one 16 KB
+// bulk copy of the codes (lane 0) and the metadata by cp.async from all lanes, all counted on the
+// slot's "full" mbarrier.  Compute warp w takes tile w & 1 of the pairs w / 2, w / 2 + MMA_CW / 2,
+// ... and hands the slot back on its "empty" mbarrier (two arrivals per pair).  Bulk copies of
+// 16 KB keep an SM's share of HBM bandwidth streaming from a few copies in flight, where one warp
+// of 16-byte cp.async keeps about one tile in flight; the shared ring holds every tile in flight
+// once, so shared memory feeds 12 compute warps per SM instead of 8.
+//
 // Per 16 x 16 block of weights a lane issues its share of a 16-byte code load, four lop3 (three
 // after a shift) to form the A fragment, one 8-byte load of x and the mma.  Per group: two fp32
 // FMAs per accumulator with the group's scale and zero-point term, the latter using the group's
-// sum of x.
+// sum of x from a table the CTA forms before its first tile (8-k segments in a fixed order, then a
+// fixed shuffle tree: the same sums for every M, so a row's result does not depend on M).
 //
-// Tile order is k-major: tile i of a range is (k tile i / R, row block i % R) for R row blocks, so
-// a warp's consecutive tiles share their k tile.  The sums of x over the k tile's groups (an mma
-// chain with A = 1) are computed once per run of equal k tile instead of once per tile, and with
-// one or two rows of x the warp copies only that k tile's slice of x, once per run.  Every tile's
-// partial sums are stored (shared memory when the CTA owns whole row blocks, global memory
-// otherwise) and summed over the k tiles in a fixed order afterwards.
-// Two CTAs of 4 warps per SM (INT2: 3) rather than one of 8: the same warps per SM, and each
-// CTA's shared memory (~105 KB) leaves room for a CTA of the next kernel on the stream, which with
-// launch overlap starts streaming its weights while this kernel's last CTAs finish.
-template <int FMT> struct MmaCfg {
-    static constexpr int WARPS = (FMT == UQ_INT2_ASYM) ? 3 : 4;    // workers per CTA
-    static constexpr int STAGES = 2;                               // tiles in flight per worker
-};
-constexpr int MMA_CTAS_PER_SM = 2;
-constexpr int MMA_TPW = 6;        // tiles per warp at most when the CTA owns whole row blocks
+// Pair order is k-major: pair i of a range is (k tile pair i / R, row block i % R) for R row
+// blocks.  Every tile's partial sums are stored (shared memory when the CTA owns whole row blocks,
+// global memory otherwise) and summed over the k tiles in k order afterwards, so a row's result
+// does not depend on how the work was split either.
+constexpr int MMA_CW = 12;                  // compute warps per CTA (even: a warp keeps one half of its pairs)
+constexpr int MMA_PMAX = 16;                // ring slots (tile pairs) at most
+constexpr int MMA_TPC = 48;                 // tiles per CTA at most when it owns whole row blocks
+constexpr int MMA_SMEM = 227 * 1024;        // dynamic shared memory of the CTA at most
+// the W4A8 GEMV (uq_w4a8.cu) keeps per-warp rings: two CTAs of 4 warps per SM, at most 6 tiles per
+// warp when a CTA owns whole row blocks
+constexpr int A8_CTAS_PER_SM = 2;
+constexpr int A8_TPW = 6;
 
 // bytes per row of x in shared memory: 32 bytes of padding put the four rows a half-warp's 8-byte
 // B-fragment loads touch into different banks
 __host__ __device__ inline size_t gemv_mma_x_stride(int Kp) { return (size_t)Kp * 2 + 32; }
 
-// Where the mma GEMV reads x (template parameter XM):
-//   MMA_X_GLOBAL  straight from global memory (through L1);
-//   MMA_X_WHOLE   all of x copied into shared memory once per CTA, before the first tile;
-//   MMA_X_SLICE   each warp copies the slice of x of its current k tile (KT k of every row) into a
-//                 buffer of its own, the next run's slice while the current run computes.
-constexpr int MMA_X_GLOBAL = 0, MMA_X_WHOLE = 1, MMA_X_SLICE = 2;
-// bytes per row of an x slice (row padding as for the whole x when there are several rows)
-__host__ __device__ inline int gemv_mma_xslice_stride(int fmt, int M) {
-    return M <= 1 ? fmt_kt(fmt) * 2 : fmt_kt(fmt) * 2 + 32;
+// Where the mma GEMV reads x (template parameter XM): MMA_X_WHOLE, all of x copied into shared
+// memory once per CTA; MMA_X_GLOBAL, straight from global memory (through L1), when a whole x would
+// leave the ring too few slots.
+constexpr int MMA_X_GLOBAL = 0, MMA_X_WHOLE = 1;
+
+// metadata bytes of one tile at this group size
+template <int FMT>
+__host__ __device__ inline int gemv_mma_meta_t(int gs) {
+    constexpr int KT = fmt_kt(FMT);
+    if (FMT == UQ_K4 || gs == 32) return MetaGeom<FMT, KT / 32>::META_BYTES;
+    if (gs == 64) return MetaGeom<FMT, KT / 64>::META_BYTES;
+    return MetaGeom<FMT, KT / 128>::META_BYTES;
+}
+__host__ __device__ inline int gemv_mma_meta(int fmt, int group) {
+    switch (fmt) {
+        case UQ_INT4_SYM: return gemv_mma_meta_t<UQ_INT4_SYM>(group);
+        case UQ_INT4_ASYM: return gemv_mma_meta_t<UQ_INT4_ASYM>(group);
+        case UQ_INT2_ASYM: return gemv_mma_meta_t<UQ_INT2_ASYM>(group);
+        default: return gemv_mma_meta_t<UQ_K4>(32);
+    }
 }
 
-// Shared memory: rings [warps][stages][stage] | ring and x mbarriers | sums of x [warps][groups of
-// a tile][8] | partial sums [tiles of the CTA, at most warps x MMA_TPW][16][8] | x (whole, or
-// [warps][2][M] slices)
-__host__ __device__ inline GemvSmem gemv_mma_smem_plan(int fmt, int K, int group, int M, int xm) {
-    int stage = 0, warps = 0;
-    const int kc = fmt_kc(fmt), kt = fmt_kt(fmt);
-    switch (fmt) {
-        case UQ_INT4_SYM: stage = GemvFmt<UQ_INT4_SYM>::STAGE_BYTES; warps = MmaCfg<UQ_INT4_SYM>::WARPS; break;
-        case UQ_INT4_ASYM: stage = GemvFmt<UQ_INT4_ASYM>::STAGE_BYTES; warps = MmaCfg<UQ_INT4_ASYM>::WARPS; break;
-        case UQ_INT2_ASYM: stage = GemvFmt<UQ_INT2_ASYM>::STAGE_BYTES; warps = MmaCfg<UQ_INT2_ASYM>::WARPS; break;
-        default: stage = GemvFmt<UQ_K4>::STAGE_BYTES; warps = MmaCfg<UQ_K4>::WARPS; break;
+// Groups in the CTA's table of x sums: those of every k tile when CTAs own whole row blocks (tpc >
+// 0), else those of the k tiles a stream-K range of at most ceil(NB * KB2 / grid) consecutive
+// k-major pairs can touch (at most ceil(range / NB) + 1 pairs of k tiles).
+__host__ __device__ inline int gemv_mma_sx_groups(int fmt, int group, int NB, int KB, int grid, int tpc) {
+    const int gs = fmt == UQ_K4 ? 32 : group;
+    const int gpt = fmt_kt(fmt) / gs;
+    long long span = KB;
+    if (tpc == 0) {
+        const long long P2 = (long long)NB * ((KB + 1) / 2);
+        const long long per = (P2 + grid - 1) / grid;
+        const long long touched = 2 * ((per + NB - 1) / NB + 1);
+        if (touched < span) span = touched;
     }
-    const int stages = 2;
-    const int Kp = (K + kc - 1) / kc * kc;
-    const int gs = (fmt == UQ_K4) ? 32 : group;
-    GemvSmem p;
-    p.bars = (size_t)warps * stages * stage;
-    p.lut = p.bars + (size_t)(warps * stages + 2 * warps + 1) * 8;  // ring, x-slice and whole-x mbarriers
-    p.sx = (p.lut + 15) / 16 * 16;
-    p.ps = p.sx + (size_t)warps * (kt / gs) * 8 * 4;
-    p.x = (p.ps + (size_t)warps * MMA_TPW * RB * 8 * 4 + 127) / 128 * 128;
-    p.total = p.x;
-    if (xm == MMA_X_WHOLE) p.total += (size_t)M * gemv_mma_x_stride(Kp);
-    if (xm == MMA_X_SLICE) p.total += (size_t)warps * 2 * M * gemv_mma_xslice_stride(fmt, M);
+    return (int)span * gpt;
+}
+
+// Shared memory: codes [S2][2][8 KB] | metadata [S2][2][meta] | full[S2], empty[S2] and x
+// mbarriers | sums of x [groups][8] | partial sums [tiles of the CTA][16][8] (whole row blocks) |
+// x (MMA_X_WHOLE).  S2 = the slots that fit beside the rest (at most MMA_PMAX).  Identical on
+// host and device.
+struct MmaSmem {
+    size_t meta, bars, sx, ps, x, total;
+    int S2, mb;                                     // slots, metadata bytes per tile
+};
+// offsets for S2 slots (multiplications and additions only: the kernel forms them per launch)
+__host__ __device__ inline MmaSmem gemv_mma_offsets(int S2, int mb, int sxg, int tpc, int M, int Kp, int xm) {
+    MmaSmem p;
+    p.S2 = S2;
+    p.mb = mb;
+    p.meta = (size_t)S2 * 2 * TILE_BYTES;
+    p.bars = p.meta + (size_t)S2 * 2 * mb;
+    p.sx = (p.bars + (size_t)(2 * MMA_PMAX + 1) * 8 + 15) / 16 * 16;
+    p.ps = p.sx + (size_t)sxg * 8 * 4;
+    p.x = (p.ps + (size_t)tpc * RB * 8 * 4 + 127) / 128 * 128;
+    p.total = p.x + (xm == MMA_X_WHOLE ? (size_t)M * gemv_mma_x_stride(Kp) : 0);
     return p;
 }
-// x slices for one or two rows, else the whole x if it fits, else global memory (each within the
-// shared memory that keeps MMA_CTAS_PER_SM CTAs on an SM)
-constexpr int MMA_SMEM_LIMIT = (228 * 1024) / MMA_CTAS_PER_SM - 1024;
-__host__ __device__ inline int gemv_mma_xmode(int fmt, int K, int group, int M) {
-    if (M <= 2 && gemv_mma_smem_plan(fmt, K, group, M, MMA_X_SLICE).total <= MMA_SMEM_LIMIT) return MMA_X_SLICE;
-    if (gemv_mma_smem_plan(fmt, K, group, M, MMA_X_WHOLE).total <= MMA_SMEM_LIMIT) return MMA_X_WHOLE;
-    return MMA_X_GLOBAL;
+__host__ __device__ inline MmaSmem gemv_mma_smem(int fmt, int K, int group, int M, int sxg, int tpc, int xm) {
+    const int mb = gemv_mma_meta(fmt, group);
+    const int slot = 2 * (TILE_BYTES + mb);
+    const int kc = fmt_kc(fmt);
+    const int Kp = (K + kc - 1) / kc * kc;
+    const size_t bars = (size_t)(2 * MMA_PMAX + 1) * 8;
+    const size_t xb = xm == MMA_X_WHOLE ? (size_t)M * gemv_mma_x_stride(Kp) : 0;
+    const size_t rest = bars + 16 + (size_t)sxg * 8 * 4 + (size_t)tpc * RB * 8 * 4 + 128 + xb;   // + alignment
+    long long S2 = ((long long)MMA_SMEM - (long long)rest) / slot;
+    if (S2 > MMA_PMAX) S2 = MMA_PMAX;
+    if (S2 < 0) S2 = 0;
+    return gemv_mma_offsets((int)S2, mb, sxg, tpc, M, Kp, xm);
+}
+// x in shared memory when that leaves the ring 3 slots beyond those the compute warps hold
+__host__ __device__ inline int gemv_mma_xmode(int fmt, int K, int group, int M, int sxg, int tpc) {
+    return gemv_mma_smem(fmt, K, group, M, sxg, tpc, MMA_X_WHOLE).S2 >= MMA_CW / 2 + 3 ? MMA_X_WHOLE : MMA_X_GLOBAL;
+}
+
+__device__ __forceinline__ float bf16_pair_sum(uint32_t w) {
+    return __uint_as_float(w << 16) + __uint_as_float(w & 0xFFFF0000u);
+}
+__device__ __forceinline__ void compute_warps_sync() {
+    asm volatile("bar.sync 1, %0;" :: "n"(MMA_CW * 32) : "memory");
 }
 
 // GATED: the gated projection in one launch.  The work list interleaves the gate and up weights' row
 // blocks (work row block 2j = gate row block j, 2j + 1 = up row block j), every CTA owns whole pairs,
 // and the per-row reduction forms h = silu(g) * u (or the second pass does, for the stream-K split).
 template <int FMT, int GB, int XM, bool GATED>
-__global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv_mma_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const GemvArgs a) {
     using F = GemvFmt<FMT>;
-    constexpr int KT = F::KT, S = MmaCfg<FMT>::STAGES, W = MmaCfg<FMT>::WARPS;
+    constexpr int KT = F::KT, CW = MMA_CW, PW = MMA_CW / 2;
+    static_assert(MMA_CW % 2 == 0, "compute warps come in pairs");
+    constexpr int GS = GB * 16;                                     // k per scaling group
+    constexpr int GPT = KT / GS;                                    // groups per full tile row
+    constexpr int MB = MetaGeom<FMT, GPT>::META_BYTES;              // metadata bytes per tile
+    constexpr int WPG = (FMT == UQ_INT2_ASYM) ? GB / 2 : GB;        // code words per lane per group
+    constexpr int BPCH = F::BPC;                                    // 16-k blocks per 512-byte chunk
+    constexpr int SPG = GS / 8;                                     // 8-k segments of x per group
+    constexpr bool XS = XM == MMA_X_WHOLE;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int M = a.M;
+    const int tpc = a.cta_rows;                                     // > 0: CTAs own whole row blocks
+    const bool cta_rows = tpc > 0;
+    const Layout L(a.N, a.K, FMT);
+    const int sxg = a.sx_groups;
+    const MmaSmem plan = gemv_mma_offsets(a.ring_slots, MB, sxg, tpc, M, L.Kp, XM);
+    const int S2 = plan.S2;
+    uint8_t* ring = smem;                                           // codes: slot s, tile h at (2s + h) * 8 KB
+    uint8_t* metas = smem + plan.meta;                              // metadata: slot s, tile h at (2s + h) * MB
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + plan.bars);
+    uint64_t* empty = full + S2;
+    uint64_t* xbar = full + 2 * S2;
+    float* sxt = reinterpret_cast<float*>(smem + plan.sx);
+    float* cpart = reinterpret_cast<float*>(smem + plan.ps);
+    uint8_t* xs = smem + plan.x;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+
+    // Work split over pairs of k tiles (KB2 per row block; when KB is odd the last pair holds one
+    // tile): whole row blocks [rb0, rb0 + R) per CTA (gated: gate / up pairs), or the stream-K range
+    // [p0, p1) of all NB * KB2 pairs.  Local pair pl is pair p0 + pl of the k-major order over R row
+    // blocks: k tiles 2 ((p0 + pl) / R) + {0, 1}, row block rb0 + (p0 + pl) % R (R = NB for
+    // stream-K).  Local tile li = 2 pl + h.
+    // (32-bit arithmetic: the host plans no launch with 2^31 pairs or more; the divisions here sit
+    // on the copy warp's path to its first request)
+    constexpr int WU = GATED ? 2 : 1;
+    const unsigned b = blockIdx.x, nctas = gridDim.x;
+    const unsigned NBU = (unsigned)a.NB / WU;
+    const unsigned KB2 = ((unsigned)a.KB + 1) / 2;
+    int rb0 = 0, R = a.NB;
+    unsigned p0 = 0, npl;
+    if (cta_rows) {                              // the first NBU % nctas CTAs own one row block more
+        const unsigned q = NBU / nctas, r = NBU - q * nctas;
+        rb0 = WU * (int)(b * q + (b < r ? b : r));
+        R = WU * (int)(q + (b < r ? 1u : 0u));
+        npl = (unsigned)R * KB2;
+    } else {                                     // the first P2 % nctas CTAs take one pair more
+        const unsigned P2 = (unsigned)a.NB * KB2;
+        const unsigned q = P2 / nctas, r = P2 - q * nctas;
+        p0 = b * q + (b < r ? b : r);
+        npl = q + (b < r ? 1u : 0u);
+    }
+    // pair p0 + i as (k tile pair, row block index): one division here, increments afterwards
+    const int kp0 = (int)(p0 / (unsigned)R), rp0 = (int)(p0 - (unsigned)kp0 * (unsigned)R);
+    const int kb_first = npl > 0 ? 2 * kp0 : 0;
+    int kb_last = npl > 0 ? 2 * (int)((p0 + npl - 1) / (unsigned)R) + 1 : -1;
+    if (kb_last > a.KB - 1) kb_last = a.KB - 1;
+    const int nsx = (kb_last - kb_first + 1) * GPT;                 // table groups this CTA uses
+    const bool bad = (cta_rows && 2 * (int)npl > tpc) || nsx > sxg || S2 <= PW || R <= 0;   // never planned
+    if (bad) {
+        if (threadIdx.x == 0) atomicOr(a.fault, FAULT_GEMV_SPLIT);
+        return;
+    }
+    const int G_all = a.K / GS;                                     // scaling groups per row
+    const size_t xstride = gemv_mma_x_stride(L.Kp);
+
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    if (warp == CW) {
+        // ---- copy warp: initializes the mbarriers and signals named barrier 2 without waiting, then
+        // requests the CTA's pairs in order into the ring (per pair the codes, then the metadata),
+        // the first ring's worth at once and then pair by pair as slots come back.  The weights are
+        // constant, so it does not wait for the previous kernel on the stream.
+        if (lane == 0) {
+            for (int s = 0; s < S2; ++s) {
+                mbar_init(&full[s], 33);                            // 32 lanes' metadata + the codes' expect_tx
+                mbar_init(&empty[s], 2);                            // the pair's two compute warps
+            }
+            mbar_init(xbar, 1);
+            fence_barrier_init();
+        }
+        __syncwarp();
+        asm volatile("bar.arrive 2, %0;" :: "n"((CW + 1) * 32) : "memory");
+        const GemvSrc src_gate{a.wq, a.scales, a.zc}, src_up{a.wq2, a.scales2, a.zc2};
+        // the codes of pair (k tile pair kp, row block index rb) into slot s (lane 0)
+        auto codes = [&](int kp, int rb, int s) {
+            const int nbw = rb0 + rb, nb = GATED ? nbw >> 1 : nbw;
+            const uint8_t* wq = (GATED && (nbw & 1)) ? a.wq2 : a.wq;
+            const int kb0 = 2 * kp;
+            // tile kb0 is whole when kb0 + 1 exists (only the last k tile can be narrower)
+            const uint32_t bytes = kb0 + 1 < a.KB ? (uint32_t)(TILE_BYTES + L.tile_bytes(kb0 + 1)) : (uint32_t)L.tile_bytes(kb0);
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&full[s], bytes);
+            bulk_g2s(ring + (size_t)s * 2 * TILE_BYTES, wq + L.tile_offset(nb, kb0), bytes, &full[s]);
+        };
+        const int first = (int)npl < S2 ? (int)npl : S2;
+        MetaConst mc;
+        mc.G = a.K / a.group;
+        mc.GT = KT / a.group;
+        mc.ZB = (mc.G + 1) >> 1;
+        mc.S4 = a.K / 256;
+        mc.aligned = (a.K % (8 * a.group)) == 0 && (mc.GT % 8) == 0;
+        // the metadata of pair (kp, rb) into slot s, each lane's copies arriving on its full barrier
+        auto meta = [&](int kp, int rb, int s) {
+            const int nbw = rb0 + rb, nb = GATED ? nbw >> 1 : nbw;
+            const GemvSrc& src = (GATED && (nbw & 1)) ? src_up : src_gate;
+            const int kb0 = 2 * kp;
+            uint32_t* md = reinterpret_cast<uint32_t*>(metas + (size_t)s * 2 * MB);
+            issue_meta<FMT, GPT, GPT>(a, src, mc, nb, kb0, md, lane);
+            if (kb0 + 1 < a.KB) issue_meta<FMT, GPT, GPT>(a, src, mc, nb, kb0 + 1, md + MB / 4, lane);
+            cp_async_arrive_noinc(&full[s]);
+        };
+        int ikp = kp0, irb = rp0;
+        for (int s = 0; s < first; ++s) {
+            if (lane == 0) codes(ikp, irb, s);
+            meta(ikp, irb, s);
+            if (++irb == R) { irb = 0; ++ikp; }
+        }
+        int issued = first;
+        int slot = 0;                                               // first < S2 only when npl == first
+        uint32_t ph = 1;
+        for (int pl = first; pl < (int)npl; ++pl) {
+            // the slot's previous pair is done
+            const bool ok = mbar_wait_bounded(&empty[slot], ph ^ 1u, a.fault, FAULT_GEMV_WAIT);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            if (lane == 0) codes(ikp, irb, slot);
+            meta(ikp, irb, slot);
+            ++issued;
+            if (++irb == R) { irb = 0; ++ikp; }
+            if (++slot == S2) { slot = 0; ph ^= 1u; }
+        }
+        // nothing the warp requested may land after the CTA has left: its own cp.async, then the
+        // last pairs' bulk copies (their full phases complete)
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        for (int q = (issued > S2 ? issued - S2 : 0); q < issued; ++q)
+            mbar_wait_bounded(&full[q % S2], (uint32_t)((q / S2) & 1), a.fault, FAULT_GEMV_WAIT);
+        return;
+    }
+
+    // ---- compute warps.  x may be written by the previous kernel on the stream.
+    MetaConst mc;
+    mc.G = a.K / a.group;
+    mc.GT = KT / a.group;
+    mc.ZB = (mc.G + 1) >> 1;
+    mc.S4 = a.K / 256;
+    mc.aligned = (a.K % (8 * a.group)) == 0 && (mc.GT % 8) == 0;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("bar.sync 2, %0;" :: "n"((CW + 1) * 32) : "memory");   // the mbarriers are initialized
+    if constexpr (XS) {
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(xbar, (uint32_t)(M * a.K * 2));
+            for (int m = 0; m < M; ++m)
+                bulk_g2s(xs + m * xstride, a.x + (long long)m * a.ldx, (uint32_t)(a.K * 2), xbar);
+        }
+        const int padw = (L.Kp - a.K) / 2;                          // the rows' zero padding to Kp
+        for (int e = threadIdx.x; e < M * padw; e += CW * 32)
+            reinterpret_cast<uint32_t*>(xs + (e / padw) * xstride + a.K * 2)[e % padw] = 0u;
+    }
+    {
+        // table of x sums: entry (group gl of k tiles kb_first.., column m) = the sum of row m of x
+        // over the group.  A warp task is one row of x over one k tile: lane l adds k = KL l .. KL l
+        // + KL - 1 in order (a bf16 pair at a time), then a group's GS / KL lanes combine by a
+        // shuffle tree (or a lane's KL k hold KL / GS groups).  This is the order gemv_warp_kernel
+        // forms its sums in, so the two kernels give the same sums (and rows of y) for any M.  Each
+        // round issues its tasks' loads before any sum (a load's first use would stall the next).
+        // Columns m >= M are zero (their products are never stored).
+        constexpr int KL = KT / 32;                                 // k per lane
+        constexpr int NV = KL / 8;                                  // 16-byte loads per lane and task
+        constexpr int TU = NV >= 8 ? 1 : 8 / NV;                    // tasks per warp per round
+        constexpr int NGL = (KL / GS) > 1 ? (KL / GS) : 1;          // groups within a lane's k
+        const int nkt = kb_last - kb_first + 1;
+        const int ntask = M * nkt;
+        for (int tb = warp; tb < ntask; tb += TU * CW) {
+            uint4 w[TU][NV];
+#pragma unroll
+            for (int u = 0; u < TU; ++u) {
+                const int t = tb + u * CW;
+                const int m = t / nkt, kt = kb_first + (t - m * nkt);   // warp-uniform
+                const int k0 = kt * KT + lane * KL;
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    w[u][v] = make_uint4(0u, 0u, 0u, 0u);
+                    if (t < ntask && k0 + 8 * v < a.K) w[u][v] = ldg_nc_v4(a.x + (long long)m * a.ldx + k0 + 8 * v);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < TU; ++u) {
+                const int t = tb + u * CW;
+                const int m = t / nkt, ktl = t - m * nkt;
+                float gsum[NGL];
+#pragma unroll
+                for (int q = 0; q < NGL; ++q) gsum[q] = 0.f;
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    const uint32_t wv4[4] = {w[u][v].x, w[u][v].y, w[u][v].z, w[u][v].w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const int q = (NGL > 1) ? (v * 8 + 2 * h) / GS : 0;
+                        gsum[q] += bf16_pair_sum(wv4[h]);
+                    }
+                }
+                if constexpr (GS >= KL) {
+#pragma unroll
+                    for (int o = 1; o < GS / KL; o <<= 1) gsum[0] += __shfl_xor_sync(0xffffffffu, gsum[0], o);
+                    const int gl = ktl * GPT + lane / (GS / KL);
+                    if (t < ntask && (lane & (GS / KL - 1)) == 0 && kb_first * GPT + gl < G_all) sxt[gl * 8 + m] = gsum[0];
+                } else {
+#pragma unroll
+                    for (int q = 0; q < NGL; ++q) {
+                        const int gl = ktl * GPT + lane * NGL + q;
+                        if (t < ntask && kb_first * GPT + gl < G_all) sxt[gl * 8 + m] = gsum[q];
+                    }
+                }
+            }
+        }
+        for (int e = threadIdx.x; e < nsx * 8; e += CW * 32)
+            if ((e & 7) >= M) sxt[e] = 0.f;
+    }
+    compute_warps_sync();                                           // the table and x padding are written
+    bool xok = true;
+    if constexpr (XS) xok = mbar_wait_bounded(xbar, 0, a.fault, FAULT_GEMV_WAIT);
+    const int npl_w = __all_sync(0xffffffffu, xok) ? (int)npl : 0;
+
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};        // rows g + 8j, columns 2c + e
+    const int mrow = g < M ? g : M - 1;          // B rows beyond M repeat a real row; their D columns are unused
+    const uint16_t* xgrow = a.x + (long long)mrow * a.ldx + 4 * c;
+    const uint8_t* xrow = xs + mrow * xstride + 8 * c;
+    // this warp's tiles: tile hh of the pairs pl = warp / 2, warp / 2 + PW, ...; pair coordinates
+    // advanced by (PW / R, PW % R)
+    const int hh = warp & 1;
+    const int dq = PW / R, dr = PW % R;
+    int ckp = kp0, crb = rp0 + (warp >> 1);      // pair p0 + warp / 2 (warp / 2 < PW: a few steps at most)
+    while (crb >= R) { crb -= R; ++ckp; }
+    int slot = warp >> 1;                        // pl % S2 (PW < S2: one wrap per step at most)
+    uint32_t ph = 0;                             // (pl / S2) & 1
+    for (int pl = warp >> 1; pl < npl_w; pl += PW) {
+        const int kb = 2 * ckp + hh, nbw = rb0 + crb, nb = GATED ? nbw >> 1 : nbw;
+        ckp += dq;
+        crb += dr;
+        if (crb >= R) { crb -= R; ++ckp; }
+        const bool ok = mbar_wait_bounded(&full[slot], ph, a.fault, FAULT_GEMV_WAIT);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        if (kb < a.KB) {                         // (the second tile of a pair at an odd KB's end does not exist)
+            const int n0 = nb * RB;
+            const int gi0 = kb * GPT;
+            const int ng = (G_all - gi0) < GPT ? (G_all - gi0) : GPT;   // groups of the tile inside K
+            const float* sxk = sxt + (gi0 - kb_first * GPT) * 8 + 2 * c;
+            const uint8_t* xt = xrow + (size_t)kb * KT * 2;
+            const uint16_t* xgt = xgrow + (long long)kb * KT;
+            const uint8_t* st = ring + (size_t)(2 * slot + hh) * TILE_BYTES;
+            // the tile's metadata, addressed as if it followed the codes (row_ptrs / row_meta_k4 add
+            // TILE_BYTES; the address stays inside the ring)
+            const uint8_t* sm = metas + (size_t)(2 * slot + hh) * MB - TILE_BYTES;
+            RowPtrs<FMT> rp[2];
+            if constexpr (FMT != UQ_K4) {
+                rp[0] = row_ptrs<FMT, GPT>(sm, mc, g, n0 + g, kb);
+                rp[1] = row_ptrs<FMT, GPT>(sm, mc, g + 8, n0 + g + 8, kb);
+            }
+
+            auto group_step = [&](const int gg) {
+                // this lane's code words for the group's GB blocks
+                uint32_t wv[WPG];
+                {
+                    const int blk = gg * GB;                            // first block of the group in the tile
+                    const uint8_t* cp = st + (blk / BPCH) * CHUNK + lane * 16 + ((blk % BPCH) * WPG / GB) * 4;
+                    if constexpr (WPG == 4) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(cp);
+                        wv[0] = v.x; wv[1] = v.y; wv[2] = v.z; wv[3] = v.w;
+                    } else if constexpr (WPG == 8) {
+                        const uint4 v0 = *reinterpret_cast<const uint4*>(cp);
+                        const uint4 v1 = *reinterpret_cast<const uint4*>(cp + CHUNK);
+                        wv[0] = v0.x; wv[1] = v0.y; wv[2] = v0.z; wv[3] = v0.w;
+                        wv[4] = v1.x; wv[5] = v1.y; wv[6] = v1.z; wv[7] = v1.w;
+                    } else if constexpr (WPG == 2) {
+                        const uint2 v = *reinterpret_cast<const uint2*>(cp);
+                        wv[0] = v.x; wv[1] = v.y;
+                    } else {
+                        wv[0] = *reinterpret_cast<const uint32_t*>(cp);
+                    }
+                }
+                // B fragments: x at k = 16 blk + 4c .. +3 of row mrow (8 bytes per block); every block
+                // of a group inside K lies inside K (K is a multiple of the group)
+                uint32_t bx[GB], by[GB];
+#pragma unroll
+                for (int j = 0; j < GB; ++j) {
+                    uint2 v;
+                    if constexpr (XS) v = *reinterpret_cast<const uint2*>(xt + (gg * GB + j) * 32);
+                    else v = ldg_nc_v2(xgt + (gg * GB + j) * 16);
+                    bx[j] = v.x; by[j] = v.y;
+                }
+                // the group's sum of (128 + q) x, in two chains (even / odd blocks)
+                float dd[2][4];
+#pragma unroll
+                for (int j = 0; j < GB; ++j) {
+                    uint32_t a0, a1, a2, a3;
+                    if constexpr (FMT == UQ_INT2_ASYM) {
+                        const uint32_t wd = wv[j >> 1];
+                        if (j & 1) {
+                            a0 = crumb_pair_lop3<4>(wd); a1 = crumb_pair_lop3<5>(wd);
+                            a2 = crumb_pair_lop3<6>(wd); a3 = crumb_pair_lop3<7>(wd);
+                        } else {
+                            a0 = crumb_pair_lop3<0>(wd); a1 = crumb_pair_lop3<1>(wd);
+                            a2 = crumb_pair_lop3<2>(wd); a3 = crumb_pair_lop3<3>(wd);
+                        }
+                    } else {
+                        const uint32_t wd = wv[j];
+                        a0 = nib_pair_lop3<0>(wd); a1 = nib_pair_lop3<1>(wd);
+                        a2 = nib_pair_lop3<2>(wd); a3 = nib_pair_lop3<3>(wd);
+                    }
+                    if (j < 2) mma_bf16_zero(dd[j & 1], a0, a1, a2, a3, bx[j], by[j]);
+                    else mma_bf16(dd[j & 1], a0, a1, a2, a3, bx[j], by[j]);
+                }
+                // fold the group into the row sums, with the group's sums of x from the table
+                const float2 sxv = *reinterpret_cast<const float2*>(sxk + gg * 8);
+                float d[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) d[e] = dd[0][e] + dd[1][e];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    if constexpr (FMT == UQ_K4) {
+                        float dsc, dmm;
+                        row_meta_k4(sm, g + 8 * j, gg, dsc, dmm);
+                        const float off = fmaf(128.0f, dsc, dmm);
+                        acc[2 * j] = fmaf(dsc, d[2 * j], fmaf(-off, sxv.x, acc[2 * j]));
+                        acc[2 * j + 1] = fmaf(dsc, d[2 * j + 1], fmaf(-off, sxv.y, acc[2 * j + 1]));
+                    } else {
+                        float sc, zc;
+                        row_meta<FMT>(rp[j], gg, sc, zc);
+                        const float szc = sc * zc;
+                        acc[2 * j] = fmaf(sc, d[2 * j], fmaf(-szc, sxv.x, acc[2 * j]));
+                        acc[2 * j + 1] = fmaf(sc, d[2 * j + 1], fmaf(-szc, sxv.y, acc[2 * j + 1]));
+                    }
+                }
+            };
+            if (ng == GPT) {
+                // 8 groups per step for 32-k groups: a K4 record (8 sub-blocks) is then read and
+                // decoded once per row per step, its 6-bit fields at constant shifts
+                constexpr int GUNROLL = (GB == 2) ? 8 : 4;
+#pragma unroll GUNROLL
+                for (int gg = 0; gg < GPT; ++gg) group_step(gg);
+            } else {
+#pragma unroll 1
+                for (int gg = 0; gg < ng; ++gg) group_step(gg);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);                   // this warp's half of the slot is free
+        slot += PW;
+        if (slot >= S2) { slot -= S2; ph ^= 1u; }
+        if (kb < a.KB) {
+            // the tile's partial sums: shared memory (cta_rows; slot = the tile's index in the CTA's
+            // range) or global memory (slot = the tile's index in k-major order), summed over k later
+            if (cta_rows) {
+                float* part = cpart + (2 * pl + hh) * RB * 8;
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) part[(g + 8 * j) * 8 + 2 * c + e] = acc[2 * j + e];
+            } else {
+                float* part = a.partials + ((long long)kb * a.NB + nbw) * RB * M;
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        if (2 * c + e < M) part[(g + 8 * j) * M + 2 * c + e] = acc[2 * j + e];
+            }
+        }
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+    }
+    if (!cta_rows) return;
+    // cta_rows: each row's sum over the k tiles, in k order, once every compute warp's tiles are in
+    compute_warps_sync();
+    auto row_sum = [&](int rbi, int r, int m) {         // tile (kb, rbi) is local tile 2 ((kb / 2) R + rbi) + kb % 2
+        float sum = 0.f;
+        for (int kb = 0; kb < L.KB; ++kb) sum += cpart[((2 * ((kb >> 1) * R + rbi) + (kb & 1)) * RB + r) * 8 + m];
+        return sum;
+    };
+    for (int e = threadIdx.x; e < (R / WU) * RB * M; e += CW * 32) {
+        const int rbi = e / (RB * M), rm = e % (RB * M), r = rm / M, m = rm % M;
+        const int n = (rb0 / WU + rbi) * RB + r;
+        if (n >= a.N) continue;
+        if constexpr (GATED) {
+            const float gsum = row_sum(2 * rbi, r, m), usum = row_sum(2 * rbi + 1, r, m);
+            a.y[(long long)m * a.ldy + n] = __bfloat16_as_ushort(__float2bfloat16_rn(silu_mul(gsum, usum)));
+        } else {
+            store_out(a, m, n, row_sum(rbi, r, m));
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// One row of x (M = 1) on the 4-bit formats: gemv_warp_kernel, the same per-tile arithmetic on
+// per-warp rings.  Each warp owns its tiles and a ring of two stages (one computed, one in flight),
+// copied by its own lanes with 16-byte cp.async in one cp.async group per tile, and a double-
+// buffered slice of x (one bulk copy per k tile run).  Two CTAs of 4 warps per SM: each CTA's
+// shared memory (~105 KB) leaves room for a CTA of the next kernel on the stream, which with launch
+// overlap starts streaming its weights while this kernel's last CTAs finish.  A decode step's
+// launches at M = 1 are short (~10 us for 30 MB), so that overlap of consecutive launches is worth
+// more there than gemv_warp_kernel's deeper shared ring, which needs the whole SM.
+//
+// Tile order is k-major: tile i of a range is (k tile i / R, row block i % R) for R row blocks, so
+// a warp's consecutive tiles share their k tile; the sums of x over the k tile's groups are formed
+// once per run of equal k tile, in the order gemv_warp_kernel's table uses.  Every tile's partial
+// sums are stored (shared memory when the CTA owns whole row blocks, global memory otherwise) and
+// summed over the k tiles in k order afterwards, as gemv_warp_kernel does.
+template <int FMT> struct WarpCfg {
+    static constexpr int WARPS = 4;                                // workers per CTA
+    static constexpr int STAGES = 2;                               // tiles in flight per worker
+};
+constexpr int WARP_CTAS_PER_SM = 2;
+constexpr int WARP_TPW = 6;        // tiles per warp at most when the CTA owns whole row blocks
+
+// bytes per row of an x slice (KT k of each row; 32 bytes of padding when there are two rows put
+// the rows a half-warp's 8-byte B-fragment loads touch into different banks)
+__host__ __device__ inline int gemv_warp_xslice_stride(int fmt, int M) {
+    return M <= 1 ? fmt_kt(fmt) * 2 : fmt_kt(fmt) * 2 + 32;
+}
+
+// Shared memory: rings [warps][stages][stage] | ring and x-slice mbarriers | sums of x [warps][groups
+// of a tile][8] | partial sums [tiles of the CTA, at most warps x WARP_TPW][16][8] | x slices
+// [warps][2][M]
+__host__ __device__ inline GemvSmem gemv_warp_smem(int fmt, int group, int M) {
+    int stage = 0, warps = 0;
+    const int kt = fmt_kt(fmt);
+    switch (fmt) {
+        case UQ_INT4_SYM: stage = MetaGeom<UQ_INT4_SYM>::STAGE_BYTES; warps = WarpCfg<UQ_INT4_SYM>::WARPS; break;
+        default: stage = MetaGeom<UQ_INT4_ASYM>::STAGE_BYTES; warps = WarpCfg<UQ_INT4_ASYM>::WARPS; break;
+    }
+    const int stages = 2;
+    GemvSmem p;
+    p.bars = (size_t)warps * stages * stage;
+    p.lut = p.bars + (size_t)(warps * stages + 2 * warps) * 8;      // ring and x-slice mbarriers
+    p.sx = (p.lut + 15) / 16 * 16;
+    p.ps = p.sx + (size_t)warps * (kt / group) * 8 * 4;
+    p.x = (p.ps + (size_t)warps * WARP_TPW * RB * 8 * 4 + 127) / 128 * 128;
+    p.total = p.x + (size_t)warps * 2 * M * gemv_warp_xslice_stride(fmt, M);
+    return p;
+}
+// within the shared memory that keeps WARP_CTAS_PER_SM CTAs on an SM
+constexpr int WARP_SMEM_LIMIT = (228 * 1024) / WARP_CTAS_PER_SM - 1024;
+// the launches gemv_warp_kernel takes: one row of x on the 4-bit flat formats (measured faster there
+// than gemv_mma_kernel; the 2-bit formats, K4 and more rows have more work per byte, where
+// gemv_mma_kernel's 12 compute warps per SM are faster)
+__host__ __device__ inline bool gemv_warp_route(int fmt, int M) {
+    return M == 1 && (fmt == UQ_INT4_SYM || fmt == UQ_INT4_ASYM);
+}
+
+// GATED: the gated projection in one launch.  The work list interleaves the gate and up weights' row
+// blocks (work row block 2j = gate row block j, 2j + 1 = up row block j), every CTA owns whole pairs,
+// and the per-row reduction forms h = silu(g) * u (or the second pass does, for the stream-K split).
+template <int FMT, int GB, bool GATED>
+__global__ void __launch_bounds__(WarpCfg<FMT>::WARPS * 32, WARP_CTAS_PER_SM) gemv_warp_kernel(const GemvArgs a) {
+    using F = GemvFmt<FMT>;
+    constexpr int KT = F::KT, S = WarpCfg<FMT>::STAGES, W = WarpCfg<FMT>::WARPS;
     constexpr int GS = GB * 16;                                     // k per scaling group
     constexpr int GPT = KT / GS;                                    // groups per full tile row
     constexpr int WPG = (FMT == UQ_INT2_ASYM) ? GB / 2 : GB;        // code words per lane per group
     constexpr int BPCH = F::BPC;                                    // 16-k blocks per 512-byte chunk
-    constexpr bool XS = XM == MMA_X_WHOLE;
-    constexpr uint32_t ONES = 0x3F803F80u;                          // bf16 pair (1, 1)
     extern __shared__ __align__(128) uint8_t smem[];
     const int M = a.M;
-    const GemvSmem plan = gemv_mma_smem_plan(FMT, a.K, a.group, M, XM);
-    const int XB = gemv_mma_xslice_stride(FMT, M);                 // x slice: bytes per row
+    const GemvSmem plan = gemv_warp_smem(FMT, a.group, M);
+    const int XB = gemv_warp_xslice_stride(FMT, M);                 // x slice: bytes per row
     uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + plan.bars);
     uint8_t* xs = smem + plan.x;
     float* cpart = reinterpret_cast<float*>(smem + plan.ps);
@@ -701,10 +1216,9 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const Layout L(a.N, a.K, FMT);
-    uint8_t* ring = smem + (size_t)warp * S * F::STAGE_BYTES;
+    uint8_t* ring = smem + (size_t)warp * S * MetaGeom<FMT>::STAGE_BYTES;
     uint64_t* bars = bars_all + warp * S;
     uint64_t* xsl_bar = bars_all + W * S + 2 * warp;               // this warp's two x-slice buffers
-    uint64_t* xbar = bars_all + W * S + 2 * W;                      // the whole x
     float* sxw = reinterpret_cast<float*>(smem + plan.sx) + warp * GPT * 8;   // sums of x of the run's k tile
     uint8_t* xsl = xs + (size_t)warp * 2 * M * XB;                  // this warp's x-slice buffers
 
@@ -723,7 +1237,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
     const long long t0 = cta_rows ? (long long)(warp * Tc / W) : (has_work ? range_begin(w, a.T, a.P) : 0);
     const long long t1 = cta_rows ? (long long)((warp + 1) * Tc / W) : (has_work ? range_begin(w + 1, a.T, a.P) : 0);
     int ntl = (int)(t1 - t0);                                       // this warp's tiles
-    if (cta_rows && ntl > MMA_TPW) {                                // the host never splits this way
+    if (cta_rows && ntl > WARP_TPW) {                                // the host never splits this way
         if (lane == 0) atomicOr(a.fault, FAULT_GEMV_SPLIT);
         ntl = 0;
     }
@@ -736,7 +1250,6 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
     mc.S4 = a.K / 256;
     mc.aligned = (a.K % (8 * a.group)) == 0 && (mc.GT % 8) == 0;
     const int G_all = a.K / GS;                                     // real scaling groups per row
-    const size_t xstride = gemv_mma_x_stride(L.Kp);
     const int kb_first = ntl > 0 ? kb_of(t0) : 0;
     const int kb_last = ntl > 0 ? kb_of(t1 - 1) : -1;
 
@@ -760,10 +1273,6 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
         mbar_init(&xsl_bar[1], 1);
         fence_barrier_init();
     }
-    if (XS && threadIdx.x == 0) {
-        mbar_init(xbar, 1);
-        fence_barrier_init();
-    }
     __syncwarp();
     int issued = 0;                                                 // tiles requested so far
     // the weight and weight row block of a work row block
@@ -773,8 +1282,8 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
     int ikb = ntl > 0 ? kb_of(t0) : 0, irb = ntl > 0 ? (int)(t0 % R) : 0;   // the next tile to request
     auto issue_next = [&]() {
         const int nbw = rb0 + irb;
-        issue_tile<FMT, true, GPT>(a, (GATED && (nbw & 1)) ? src_up : src_gate, L, mc, GATED ? nbw >> 1 : nbw, ikb,
-                                   ring + (issued % S) * F::STAGE_BYTES, &bars[issued % S], lane);
+        issue_tile<FMT, ISSUE_GROUP, GPT>(a, (GATED && (nbw & 1)) ? src_up : src_gate, L, mc, GATED ? nbw >> 1 : nbw, ikb,
+                                   ring + (issued % S) * MetaGeom<FMT>::STAGE_BYTES, &bars[issued % S], lane);
         if (++irb == R) { irb = 0; ++ikb; }
         ++issued;
     };
@@ -784,37 +1293,18 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
     // still busy with the first tiles then).
     if (a.overlap && has_work && ntl > 0) issue_next();
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    int xissued = 0;                                                // x-slice runs requested so far
-    if constexpr (XM == MMA_X_SLICE) {
-        if (has_work && ntl > 0 && lane == 0) {
-            issue_xslice(kb_first, 0);
-            if (kb_last > kb_first) issue_xslice(kb_first + 1, 1);
-        }
-        xissued = (ntl > 0) ? ((kb_last > kb_first) ? 2 : 1) : 0;
+    if (has_work && ntl > 0 && lane == 0) {
+        issue_xslice(kb_first, 0);
+        if (kb_last > kb_first) issue_xslice(kb_first + 1, 1);
     }
-    if constexpr (XS) {
-        if (threadIdx.x == 0) {
-            mbar_arrive_expect_tx(xbar, (uint32_t)(M * a.K * 2));
-            for (int m = 0; m < M; ++m) bulk_g2s(xs + m * xstride, a.x + (long long)m * a.ldx, (uint32_t)(a.K * 2), xbar);
-        }
-        __syncthreads();                            // no warp's weight copies ahead of x
-    }
+    int xissued = (ntl > 0) ? ((kb_last > kb_first) ? 2 : 1) : 0;   // x-slice runs requested so far
     if (has_work && issued == 0 && ntl > 0) issue_next();
-    if constexpr (XS) {
-        const int padw = (L.Kp - a.K) / 2;
-        for (int e = threadIdx.x; e < M * padw; e += blockDim.x)
-            reinterpret_cast<uint32_t*>(xs + (e / padw) * xstride + a.K * 2)[e % padw] = 0u;
-        __syncthreads();                            // the zero padding is visible
-        mbar_wait_bounded(xbar, 0, a.fault, FAULT_GEMV_WAIT);
-    }
     if (!has_work) return;                          // (never in cta_rows mode: every warp meets the end barrier)
 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};        // rows g + 8j, columns 2c + e
     const int mrow = g < M ? g : M - 1;          // B rows beyond M repeat a real row; their D columns are unused
-    const uint16_t* xgrow = a.x + (long long)mrow * a.ldx + 4 * c;
     int cur_kb = -1, run = -1;
     const uint8_t* xt = nullptr;                 // this lane's x at the current k tile's first k
-    const uint16_t* xgt = xgrow;
 
     int ckb = ntl > 0 ? kb_of(t0) : 0, crb = ntl > 0 ? (int)(t0 % R) : 0;   // the tile being consumed
     for (int li = 0; li < ntl; ++li) {
@@ -828,7 +1318,7 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
             // a new run of tiles at k tile kb: its x, then the sums of x over its groups
             cur_kb = kb;
             ++run;
-            if constexpr (XM == MMA_X_SLICE) {
+            {
                 const int slot = run & 1;
                 bool ok = mbar_wait_bounded(&xsl_bar[slot], (uint32_t)((run >> 1) & 1), a.fault, FAULT_GEMV_WAIT);
                 if (!__all_sync(0xffffffffu, ok)) break;
@@ -838,12 +1328,9 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
                     ++xissued;
                 }
                 xt = xsl + (slot * M + mrow) * XB + 8 * c;
-            } else {
-                xt = xs + mrow * xstride + 8 * c + (size_t)kb * KT * 2;
             }
-            xgt = xgrow + (long long)kb * KT;
             __syncwarp();                                           // the previous run's sums are read
-            if constexpr (XM == MMA_X_SLICE) {
+            {
                 // one or two rows: lane l adds up k = KL l .. KL l + KL - 1 of each row in fp32 (a
                 // group spans GS / KL lanes, combined by shuffles, or a lane spans KL / GS groups)
                 constexpr int KL = KT / 32;
@@ -873,36 +1360,12 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
                         for (int q = 0; q < NGL; ++q) sxw[(lane * NGL + q) * 8 + m] = gsum[q];
                     }
                 }
-            } else {
-            for (int gg = 0; gg < ng; ++gg) {
-                float ds[2][4];
-#pragma unroll
-                for (int j = 0; j < GB; ++j) {
-                    uint32_t bx, by;
-                    if constexpr (XM != MMA_X_GLOBAL) {
-                        const uint2 v = *reinterpret_cast<const uint2*>(xt + (gg * GB + j) * 32);
-                        bx = v.x; by = v.y;
-                    } else {
-                        const int kk = (gg * GB + j) * 16;
-                        const uint2 v = (kb * KT + kk + 4 * c < a.K) ? ldg_nc_v2(xgt + kk) : make_uint2(0, 0);
-                        bx = v.x; by = v.y;
-                    }
-                    if (j < 2) mma_bf16_zero(ds[j & 1], ONES, ONES, ONES, ONES, bx, by);
-                    else mma_bf16(ds[j & 1], ONES, ONES, ONES, ONES, bx, by);
-                }
-                if (g == 0) {
-                    float2 v;
-                    v.x = ds[0][0] + ds[1][0];
-                    v.y = ds[0][1] + ds[1][1];
-                    *reinterpret_cast<float2*>(sxw + gg * 8 + 2 * c) = v;
-                }
-            }
             }
             __syncwarp();
         }
         while (issued < ntl && issued < li + S) issue_next();        // top up the ring (into stages consumed)
         const int s = li % S;
-        uint8_t* st = ring + s * F::STAGE_BYTES;
+        uint8_t* st = ring + s * MetaGeom<FMT>::STAGE_BYTES;
         // this tile's copies (one cp.async group) are complete once at most the groups of later
         // tiles are pending
         static_assert(S == 2, "one later group at most");
@@ -938,19 +1401,10 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
             }
             // B fragments: x at k = 16 blk + 4c .. +3 of row mrow (8 bytes per block)
             uint32_t bx[GB], by[GB];
-            if constexpr (XM != MMA_X_GLOBAL) {
 #pragma unroll
-                for (int j = 0; j < GB; ++j) {
-                    const uint2 v = *reinterpret_cast<const uint2*>(xt + (gg * GB + j) * 32);
-                    bx[j] = v.x; by[j] = v.y;
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < GB; ++j) {
-                    const int kk = (gg * GB + j) * 16;
-                    const uint2 v = (kb * KT + kk + 4 * c < a.K) ? ldg_nc_v2(xgt + kk) : make_uint2(0, 0);
-                    bx[j] = v.x; by[j] = v.y;
-                }
+            for (int j = 0; j < GB; ++j) {
+                const uint2 v = *reinterpret_cast<const uint2*>(xt + (gg * GB + j) * 32);
+                bx[j] = v.x; by[j] = v.y;
             }
             // the group's sum of (128 + q) x, in two chains (even / odd blocks)
             float dd[2][4];
@@ -1027,10 +1481,8 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
     }
     // a wait that timed out (fault flag set) left copies in flight: let them land before leaving
     cp_async_wait_group<0>();
-    if constexpr (XM == MMA_X_SLICE) {
-        for (int r = (run > 0 ? run : 0); r < xissued; ++r)
-            mbar_wait_bounded(&xsl_bar[r & 1], (uint32_t)((r >> 1) & 1), a.fault, FAULT_GEMV_WAIT);
-    }
+    for (int r = (run > 0 ? run : 0); r < xissued; ++r)
+        mbar_wait_bounded(&xsl_bar[r & 1], (uint32_t)((r >> 1) & 1), a.fault, FAULT_GEMV_WAIT);
     if (!cta_rows) return;
     // cta_rows: each row's sum over the k tiles, in k order, from the warps that computed them
     __syncthreads();
@@ -1052,21 +1504,13 @@ __global__ void __launch_bounds__(MmaCfg<FMT>::WARPS * 32, MMA_CTAS_PER_SM) gemv
     }
 }
 
+
 inline bool gemv_x_in_smem(int fmt, int K, int group, int M) {
     return gemv_smem_plan(fmt, K, group, M, true).total <= 227 * 1024;
 }
+// shared memory of the CUDA-core GEMV (INT8_SYM, NF4)
 inline size_t gemv_smem_bytes_impl(int fmt, int K, int group, int M) {
-    if (gemv_is_mma(fmt)) return gemv_mma_smem_plan(fmt, K, group, M, gemv_mma_xmode(fmt, K, group, M)).total;
     return gemv_smem_plan(fmt, K, group, M, gemv_x_in_smem(fmt, K, group, M)).total;
-}
-inline int gemv_warps_impl(int fmt) {
-    switch (fmt) {
-        case UQ_INT4_SYM: return MmaCfg<UQ_INT4_SYM>::WARPS;
-        case UQ_INT4_ASYM: return MmaCfg<UQ_INT4_ASYM>::WARPS;
-        case UQ_INT2_ASYM: return MmaCfg<UQ_INT2_ASYM>::WARPS;
-        case UQ_K4: return MmaCfg<UQ_K4>::WARPS;
-        default: return GEMV_WARPS;
-    }
 }
 inline size_t gemv_partials_floats_impl(int P, int M) { return (size_t)2 * P * RB * M; }
 
@@ -1111,20 +1555,64 @@ cudaError_t launch_xs(const GemvArgs& a, int grid, cudaStream_t st) {
 
 namespace gemv_detail {
 template <int FMT, int GB, int XM, bool GATED>
-cudaError_t launch_mma(const GemvArgs& a, int grid, cudaStream_t st) {
+cudaError_t launch_mma(const GemvArgs& a, int grid, int sxg, cudaStream_t st) {
     static bool configured[64] = {};
-    const size_t smem = gemv_mma_smem_plan(FMT, a.K, a.group, a.M, XM).total;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
         e = cudaFuncSetAttribute(gemv_mma_kernel<FMT, GB, XM, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 227 * 1024);
+                                 MMA_SMEM);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    const int threads = MmaCfg<FMT>::WARPS * 32;
+    const int threads = (MMA_CW + 1) * 32;
+    GemvArgs a2 = a;
+    a2.overlap = launch_overlap() ? 1 : 0;
+    const MmaSmem plan = gemv_mma_smem(FMT, a.K, a.group, a.M, sxg, a.cta_rows, XM);
+    a2.ring_slots = plan.S2;
+    a2.sx_groups = sxg;
+    if (a2.overlap) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(threads);
+        cfg.dynamicSmemBytes = plan.total;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, gemv_mma_kernel<FMT, GB, XM, GATED>, a2);
+        if (e != cudaSuccess) return e;
+    } else {
+        gemv_mma_kernel<FMT, GB, XM, GATED><<<grid, threads, plan.total, st>>>(a2);
+    }
+    return cudaGetLastError();
+}
+template <int FMT, int GB, bool GATED>
+cudaError_t launch_mma_x(const GemvArgs& a, int grid, cudaStream_t st) {
+    const int sxg = gemv_mma_sx_groups(FMT, a.group, a.NB, a.KB, grid, a.cta_rows);
+    if (gemv_mma_xmode(FMT, a.K, a.group, a.M, sxg, a.cta_rows) == MMA_X_WHOLE)
+        return launch_mma<FMT, GB, MMA_X_WHOLE, GATED>(a, grid, sxg, st);
+    return launch_mma<FMT, GB, MMA_X_GLOBAL, GATED>(a, grid, sxg, st);
+}
+template <int FMT, int GB, bool GATED>
+cudaError_t launch_warp(const GemvArgs& a, int grid, cudaStream_t st) {
+    static bool configured[64] = {};
+    const size_t smem = gemv_warp_smem(FMT, a.group, a.M).total;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(gemv_warp_kernel<FMT, GB, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 WARP_SMEM_LIMIT);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    const int threads = WarpCfg<FMT>::WARPS * 32;
     GemvArgs a2 = a;
     a2.overlap = launch_overlap() ? 1 : 0;
     if (a2.overlap) {
@@ -1138,20 +1626,18 @@ cudaError_t launch_mma(const GemvArgs& a, int grid, cudaStream_t st) {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, gemv_mma_kernel<FMT, GB, XM, GATED>, a2);
+        e = cudaLaunchKernelEx(&cfg, gemv_warp_kernel<FMT, GB, GATED>, a2);
         if (e != cudaSuccess) return e;
     } else {
-        gemv_mma_kernel<FMT, GB, XM, GATED><<<grid, threads, smem, st>>>(a2);
+        gemv_warp_kernel<FMT, GB, GATED><<<grid, threads, smem, st>>>(a2);
     }
     return cudaGetLastError();
 }
 template <int FMT, int GB, bool GATED>
 cudaError_t launch_mma_xg(const GemvArgs& a, int grid, cudaStream_t st) {
-    switch (gemv_mma_xmode(FMT, a.K, a.group, a.M)) {
-        case MMA_X_SLICE: return launch_mma<FMT, GB, MMA_X_SLICE, GATED>(a, grid, st);
-        case MMA_X_WHOLE: return launch_mma<FMT, GB, MMA_X_WHOLE, GATED>(a, grid, st);
-        default: return launch_mma<FMT, GB, MMA_X_GLOBAL, GATED>(a, grid, st);
-    }
+    if constexpr (FMT == UQ_INT4_SYM || FMT == UQ_INT4_ASYM)
+        if (gemv_warp_route(FMT, a.M)) return launch_warp<FMT, GB, GATED>(a, grid, st);
+    return launch_mma_x<FMT, GB, GATED>(a, grid, st);
 }
 template <int FMT, int GB>
 cudaError_t launch_mma_xs(const GemvArgs& a, int grid, cudaStream_t st) {

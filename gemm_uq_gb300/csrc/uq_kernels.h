@@ -45,15 +45,17 @@ struct GemvArgs {
     int M, N, K, group, ldx, ldy;
     int NB, KB;               // row blocks, k tiles
     long long T;              // tiles = NB * KB
-    int P;                    // workers (warps), P <= T
+    int P;                    // workers that split the tiles, P <= T: warps (CUDA-core GEMV, W4A8) or
+                              // CTAs (mma GEMV)
     float* partials;          // fp32 split-K partial sums: [T][16][M] (mma and W4A8 GEMVs, summed by the
                               // second pass), [2P][16][M] (CUDA-core GEMV: first and last row block of
                               // each worker)
     unsigned int* tickets;    // [NB], zero between calls
     unsigned int* fault;      // device fault word
     int overlap;              // launched with programmatic stream serialization (set by the launcher)
-    int cta_rows;             // mma / W4A8 GEMV: 1 = every CTA owns whole row blocks (combined in shared
-                              // memory, no second pass); 0 = workers split row blocks anywhere (second pass)
+    int cta_rows;             // mma / W4A8 GEMV: > 0 = every CTA owns whole row blocks (combined in shared
+                              // memory, no second pass; mma GEMV: the most tiles a CTA gets);
+                              // 0 = workers split row blocks anywhere (second pass)
     float* out32;             // gate pass of the gated projection: fp32 results [M][ldy] instead of y
     const float* gate32;      // up pass: y = bf16(silu(gate32) * result), gate32 [M][ldy] fp32
     int gated;                // mma GEMV only: the gated projection in one launch; (wq, scales, zc) are the
@@ -62,6 +64,8 @@ struct GemvArgs {
     const uint8_t* scales2;
     const uint8_t* zc2;
     int a8;                   // the W4A8 GEMV (integer x codes)
+    int ring_slots;           // mma GEMV: ring slots and x-sum table groups of the launch (set by its launcher)
+    int sx_groups;
 };
 constexpr int GEMV_WARPS = 4;     // worker warps per CTA of the CUDA-core GEMV
 // formats whose GEMV runs on mma.sync (the others on CUDA-core FMAs)
@@ -69,8 +73,8 @@ inline bool gemv_is_mma(int fmt) {
     return fmt == UQ_INT4_SYM || fmt == UQ_INT4_ASYM || fmt == UQ_INT2_ASYM || fmt == UQ_K4;
 }
 // Plans one GEMV launch from its shape fields (M, N, K, group, NB, KB, T, gated, a8) and the SM
-// count: sets a.P (worker warps) and a.cta_rows.  Returns the grid, or 0 when no plan fits (K too
-// long for the kernel's shared memory at this M).
+// count: sets a.P and a.cta_rows.  Returns the grid, or 0 when no plan fits (K too long for the
+// kernel's shared memory at this M).
 int gemv_plan(GemvArgs& a, int fmt, int sms);
 // what a planned launch needs: fp32 partial-sum floats, the per-row-block tickets, kernel launches
 size_t gemv_partials_floats(int fmt, const GemvArgs& a);

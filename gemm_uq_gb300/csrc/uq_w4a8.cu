@@ -90,18 +90,18 @@ __host__ __device__ inline GemvSmem gemv_a8_smem_plan() {
     using F = GemvFmt<FMT>;
     constexpr int W = 4, S = 2;
     GemvSmem p;
-    p.bars = (size_t)W * S * F::STAGE_BYTES;
+    p.bars = (size_t)W * S * MetaGeom<FMT>::STAGE_BYTES;
     p.lut = p.bars + (size_t)W * S * 8;
     p.sx = p.lut;
     p.ps = (p.lut + 15) / 16 * 16;
-    p.x = p.ps + (size_t)W * MMA_TPW * RB * 8 * 4;
+    p.x = p.ps + (size_t)W * A8_TPW * RB * 8 * 4;
     p.total = p.x;
     return p;
 }
 
 // GB = 16-k blocks per scaling group
 template <int FMT, int GB>
-__global__ void __launch_bounds__(128, MMA_CTAS_PER_SM) gemv_a8_kernel(const GemvArgs a, const int8_t* __restrict__ xq,
+__global__ void __launch_bounds__(128, A8_CTAS_PER_SM) gemv_a8_kernel(const GemvArgs a, const int8_t* __restrict__ xq,
                                                                        const float* __restrict__ sxs,
                                                                        const int* __restrict__ sxl, int Kp) {
     using F = GemvFmt<FMT>;
@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(128, MMA_CTAS_PER_SM) gemv_a8_kernel(const Gem
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const Layout L(a.N, a.K, FMT);
-    uint8_t* ring = smem + (size_t)warp * S * F::STAGE_BYTES;
+    uint8_t* ring = smem + (size_t)warp * S * MetaGeom<FMT>::STAGE_BYTES;
 
     // work split as the mma GEMV's (k-major tiles; whole row blocks per CTA, or stream-K)
     const bool cta_rows = a.cta_rows != 0;
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(128, MMA_CTAS_PER_SM) gemv_a8_kernel(const Gem
     const long long t0 = cta_rows ? (long long)(warp * Tc / W) : (has_work ? range_begin(w, a.T, a.P) : 0);
     const long long t1 = cta_rows ? (long long)((warp + 1) * Tc / W) : (has_work ? range_begin(w + 1, a.T, a.P) : 0);
     int ntl = (int)(t1 - t0);
-    if (cta_rows && ntl > MMA_TPW) {
+    if (cta_rows && ntl > A8_TPW) {
         if (lane == 0) atomicOr(a.fault, FAULT_GEMV_SPLIT);
         ntl = 0;
     }
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(128, MMA_CTAS_PER_SM) gemv_a8_kernel(const Gem
     // k-major tile coordinates advanced incrementally (no 64-bit division per tile)
     int ikb = ntl > 0 ? kb_of(t0) : 0, irb = ntl > 0 ? (int)(t0 % R) : 0;   // the next tile to request
     auto issue_next = [&]() {
-        issue_tile<FMT, true, GPT>(a, src, L, mc, rb0 + irb, ikb, ring + (issued % S) * F::STAGE_BYTES, nullptr, lane);
+        issue_tile<FMT, ISSUE_GROUP, GPT>(a, src, L, mc, rb0 + irb, ikb, ring + (issued % S) * MetaGeom<FMT>::STAGE_BYTES, nullptr, lane);
         if (++irb == R) { irb = 0; ++ikb; }
         ++issued;
     };
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(128, MMA_CTAS_PER_SM) gemv_a8_kernel(const Gem
         const int ng = (G_all - gi0) < GPT ? (G_all - gi0) : GPT;
         while (issued < ntl && issued < li + S) issue_next();
         const int s = li % S;
-        uint8_t* st = ring + s * F::STAGE_BYTES;
+        uint8_t* st = ring + s * MetaGeom<FMT>::STAGE_BYTES;
         if (issued > li + 1) cp_async_wait_group<1>();
         else cp_async_wait_group<0>();
         __syncwarp();
