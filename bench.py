@@ -534,7 +534,8 @@ def run_uq(args, rank, world, dist):
     # consecutive linears of a decode step read fixed weights: let each launch stream its weights
     # while the previous one drains (uq_set_launch_overlap)
     uq.set_launch_overlap(not args.no_overlap)
-    step = Step(recs, fmt, group, M, dev, stream, seed=777 + rank, gated=args.gated).capture()
+    step = Step(recs, fmt, group, M, dev, stream, seed=777 + rank, gated=args.gated,
+                mode=spec.get("mode", "gemm")).capture()
 
     step.replay(args.warmup)
     torch.cuda.synchronize()

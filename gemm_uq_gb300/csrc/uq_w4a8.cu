@@ -5,7 +5,7 @@
 // (fp32 quotient); then y[m][n] = s_x * sum_g s[n][g] * I, I = sum_{k in g} xq * (q - z), an exact
 // integer formed on the integer tensor instructions (mma.m16n8k32, u8 x s8 -> s32).
 //
-// quant_x_kernel (one CTA per row): absmax, s_x, the codes, written with each 4-k group's bytes in the
+// quant_x_kernel (one CTA per row, 8 k per thread step): absmax, s_x, the codes, written with each 4-k group's bytes in the
 // order the weight words hold their codes (4-bit: k, k+2, k+1, k+3 -- the low nibbles of a fragment-
 // order word; 8-bit: k .. k+3) and the 4-k groups placed in the integer mma's B fragment order, and per
 // group the sum of its codes, for the zero-point term.
@@ -31,54 +31,74 @@ __device__ __forceinline__ void mma_u8s8(int (&d)[4], uint32_t a0, uint32_t a1, 
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// one CTA (256 threads) per row of x
-__global__ void __launch_bounds__(256) quant_x_kernel(const uint16_t* __restrict__ x, int8_t* __restrict__ xq,
-                                                      float* __restrict__ sx, int* __restrict__ sxl, int M, int K,
-                                                      int Kp, int gs, int perm) {
-    __shared__ float red[8];
+// One CTA (QX_THREADS threads) per row of x.  Each thread takes 8 consecutive k at a time (one
+// 16-byte load of x): first the row's absmax, then per 8 k the codes (two 4-k groups, each written
+// as one word at its place in the B fragment order) and their sum, which a shuffle tree adds up
+// over the gs / 8 lanes of a scaling group (the group's lanes are consecutive lanes of one warp:
+// the step is a multiple of every group size).  Integer sums: any order gives the same result.
+constexpr int QX_THREADS = 512;
+__global__ void __launch_bounds__(QX_THREADS) quant_x_kernel(const uint16_t* __restrict__ x, int8_t* __restrict__ xq,
+                                                             float* __restrict__ sx, int* __restrict__ sxl, int M,
+                                                             int K, int Kp, int gs, int perm) {
+    __shared__ float red[QX_THREADS / 32];
     const int m = blockIdx.x;
     if (m >= M) return;
     const uint16_t* xr = x + (long long)m * K;
+    // K is a multiple of the group (>= 32), so whole 8-k segments: one 16-byte load each (x rows are
+    // 16-byte aligned: the row start and K * 2 are multiples of 16)
     float mx = 0.f;
-    for (int k = threadIdx.x; k < K; k += blockDim.x) mx = fmaxf(mx, fabsf(bf16lo_f32(xr[k])));
+    for (int k8 = threadIdx.x * 8; k8 < K; k8 += QX_THREADS * 8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xr + k8);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
     __syncthreads();
     float amax = 0.f;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) amax = fmaxf(amax, red[w]);
+    for (int w = 0; w < QX_THREADS / 32; ++w) amax = fmaxf(amax, red[w]);
     const float s = __fdiv_rn(amax, 127.0f);
     if (threadIdx.x == 0) sx[m] = s;
-    // codes, 4 per thread step (one 4-k group), in the weight words' byte order, placed in the B
-    // fragment order of the integer mma: per 32 k and lane column c, the 4 codes of k = 32t + 4c ..
-    // then those of k = 32t + 16 + 4c .. (8 contiguous bytes, one load per instruction)
+    // codes in the weight words' byte order, placed in the B fragment order of the integer mma:
+    // per 32 k and lane column c, the 4 codes of k = 32t + 4c .. then those of k = 32t + 16 + 4c ..
+    // (8 contiguous bytes, one load per instruction)
     int8_t* qr = xq + (long long)m * Kp;
-    for (int k4 = threadIdx.x * 4; k4 < Kp; k4 += blockDim.x * 4) {
-        int q[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int k = k4 + j;
-            float v = 0.f;
-            if (k < K && s > 0.f) v = rintf(__fdiv_rn(bf16lo_f32(xr[k]), s));
-            v = fminf(fmaxf(v, -127.f), 127.f);
-            q[j] = (int)v;
-        }
-        const uint32_t packed = perm ? ((uint32_t)(q[0] & 255) | ((uint32_t)(q[2] & 255) << 8) |
-                                        ((uint32_t)(q[1] & 255) << 16) | ((uint32_t)(q[3] & 255) << 24))
-                                     : ((uint32_t)(q[0] & 255) | ((uint32_t)(q[1] & 255) << 8) |
-                                        ((uint32_t)(q[2] & 255) << 16) | ((uint32_t)(q[3] & 255) << 24));
-        const int blk = k4 >> 4, cc = (k4 >> 2) & 3;
-        *reinterpret_cast<uint32_t*>(qr + (blk >> 1) * 32 + cc * 8 + (blk & 1) * 4) = packed;
-    }
-    // per group: the sum of its codes (k < K)
     const int G = (Kp + gs - 1) / gs;
-    for (int gi = threadIdx.x; gi < G; gi += blockDim.x) {
+    const int lpg = gs / 8;                                         // lanes per scaling group
+    for (int k8 = threadIdx.x * 8; k8 - threadIdx.x * 8 < Kp; k8 += QX_THREADS * 8) {
         int tot = 0;
-        for (int k = gi * gs; k < gi * gs + gs && k < K; ++k) {
-            const float v = (s > 0.f) ? rintf(__fdiv_rn(bf16lo_f32(xr[k]), s)) : 0.f;
-            tot += (int)fminf(fmaxf(v, -127.f), 127.f);
+        if (k8 < Kp) {
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (k8 < K) v = *reinterpret_cast<const uint4*>(xr + k8);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {                           // the two 4-k groups
+                int q[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t wd = w[2 * h + (j >> 1)];
+                    const float xv = __uint_as_float((j & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
+                    float c = 0.f;
+                    if (k8 + 4 * h + j < K && s > 0.f) c = rintf(__fdiv_rn(xv, s));
+                    c = fminf(fmaxf(c, -127.f), 127.f);
+                    q[j] = (int)c;
+                    tot += q[j];
+                }
+                const uint32_t packed = perm ? ((uint32_t)(q[0] & 255) | ((uint32_t)(q[2] & 255) << 8) |
+                                                ((uint32_t)(q[1] & 255) << 16) | ((uint32_t)(q[3] & 255) << 24))
+                                             : ((uint32_t)(q[0] & 255) | ((uint32_t)(q[1] & 255) << 8) |
+                                                ((uint32_t)(q[2] & 255) << 16) | ((uint32_t)(q[3] & 255) << 24));
+                const int k4 = k8 + 4 * h;
+                const int blk = k4 >> 4, cc = (k4 >> 2) & 3;
+                *reinterpret_cast<uint32_t*>(qr + (blk >> 1) * 32 + cc * 8 + (blk & 1) * 4) = packed;
+            }
         }
-        sxl[(long long)m * G + gi] = tot;
+        // the group's sum over its lpg lanes (the loop runs the same number of times on every lane)
+        for (int o = 1; o < lpg; o <<= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        if (k8 < Kp && (threadIdx.x % lpg) == 0) sxl[(long long)m * G + k8 / gs] = tot;
     }
 }
 
@@ -298,7 +318,7 @@ size_t a8_smem_bytes(int fmt) {
 
 cudaError_t launch_quant_x(const uint16_t* x, int8_t* xq, float* sx, int* sxl, int M, int K, int Kp, int gs, int perm,
                            cudaStream_t st) {
-    quant_x_kernel<<<M, 256, 0, st>>>(x, xq, sx, sxl, M, K, Kp, gs, perm);
+    quant_x_kernel<<<M, QX_THREADS, 0, st>>>(x, xq, sx, sxl, M, K, Kp, gs, perm);
     return cudaGetLastError();
 }
 
