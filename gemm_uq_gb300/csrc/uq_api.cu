@@ -718,7 +718,7 @@ uq_status uq_gemm_w4a8_kernel_count(int M, int N, int K, int group, uq_fmt fmt, 
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess || sms < 1) return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice, "SM count");
     const uq::Layout L(N, K, fmt);
-    int n = 1;                                                   // the activation quantization
+    int n = (M + 65534) / 65535;                                 // the activation quantization (65535 rows a launch)
     for (int m0 = 0; m0 < M; m0 += 8) {
         uq::GemvArgs a = {};
         a8_args(a, L, (M - m0) < 8 ? (M - m0) : 8, N, K, group);

@@ -5,7 +5,7 @@
 // (fp32 quotient); then y[m][n] = s_x * sum_g s[n][g] * I, I = sum_{k in g} xq * (q - z), an exact
 // integer formed on the integer tensor instructions (mma.m16n8k32, u8 x s8 -> s32).
 //
-// quant_x_kernel (one CTA per row, 8 k per thread step): absmax, s_x, the codes, written with each 4-k group's bytes in the
+// quant_x_kernel (a cluster of 8 CTAs per row): absmax, s_x, the codes, written with each 4-k group's bytes in the
 // order the weight words hold their codes (4-bit: k, k+2, k+1, k+3 -- the low nibbles of a fragment-
 // order word; 8-bit: k .. k+3) and the 4-k groups placed in the integer mma's B fragment order, and per
 // group the sum of its codes, for the zero-point term.
@@ -31,24 +31,34 @@ __device__ __forceinline__ void mma_u8s8(int (&d)[4], uint32_t a0, uint32_t a1, 
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// One CTA (QX_THREADS threads) per row of x.  Each thread takes 8 consecutive k at a time (one
-// 16-byte load of x): first the row's absmax, then per 8 k the codes (two 4-k groups, each written
-// as one word at its place in the B fragment order) and their sum, which a shuffle tree adds up
-// over the gs / 8 lanes of a scaling group (the group's lanes are consecutive lanes of one warp:
-// the step is a multiple of every group size).  Integer sums: any order gives the same result.
-constexpr int QX_THREADS = 512;
+// One cluster of QX_CTAS CTAs (QX_THREADS threads each) per row of x; CTA r of the cluster takes a
+// contiguous share of the row's 8-k segments (a multiple of 16 segments, so no scaling group spans
+// two CTAs).  Each thread takes 8 consecutive k at a time (one 16-byte load of x): first the share's
+// absmax, which the cluster combines through distributed shared memory into the row's absmax, then
+// per 8 k the codes (two 4-k groups, each written as one word at its place in the B fragment order)
+// and their sum, which a shuffle tree adds up over the gs / 8 lanes of a scaling group (consecutive
+// lanes of one warp).  Integer sums: any order gives the same result.
+constexpr int QX_THREADS = 256;
+constexpr int QX_CTAS = 8;
 __global__ void __launch_bounds__(QX_THREADS) quant_x_kernel(const uint16_t* __restrict__ x, int8_t* __restrict__ xq,
                                                              float* __restrict__ sx, int* __restrict__ sxl, int M,
                                                              int K, int Kp, int gs, int perm) {
     __shared__ float red[QX_THREADS / 32];
-    const int m = blockIdx.x;
-    if (m >= M) return;
+    __shared__ float share_max;
+    // the GEMV that reads these codes may start streaming its (constant) weights meanwhile; its
+    // griddepcontrol.wait returns once this grid has finished
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int m = blockIdx.y;
+    const int r = blockIdx.x;                                       // rank in the row's cluster
+    const int nseg = Kp / 8;
+    const int per = ((nseg + QX_CTAS - 1) / QX_CTAS + 15) / 16 * 16;
+    const int seg0 = r * per, seg1 = (seg0 + per) < nseg ? (seg0 + per) : nseg;
     const uint16_t* xr = x + (long long)m * K;
     // K is a multiple of the group (>= 32), so whole 8-k segments: one 16-byte load each (x rows are
     // 16-byte aligned: the row start and K * 2 are multiples of 16)
     float mx = 0.f;
-    for (int k8 = threadIdx.x * 8; k8 < K; k8 += QX_THREADS * 8) {
-        const uint4 v = *reinterpret_cast<const uint4*>(xr + k8);
+    for (int sg = seg0 + threadIdx.x; sg < seg1 && sg * 8 < K; sg += QX_THREADS) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xr + sg * 8);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -58,19 +68,34 @@ __global__ void __launch_bounds__(QX_THREADS) quant_x_kernel(const uint16_t* __r
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
     __syncthreads();
+    if (threadIdx.x == 0) {
+        float b = 0.f;
+        for (int w = 0; w < QX_THREADS / 32; ++w) b = fmaxf(b, red[w]);
+        share_max = b;
+    }
+    // every CTA's share_max is written before any CTA reads them
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
     float amax = 0.f;
-    for (int w = 0; w < QX_THREADS / 32; ++w) amax = fmaxf(amax, red[w]);
+    for (int q = 0; q < QX_CTAS; ++q) {
+        uint32_t remote;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(&share_max)), "r"(q));
+        float v;
+        asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+        amax = fmaxf(amax, v);
+    }
     const float s = __fdiv_rn(amax, 127.0f);
-    if (threadIdx.x == 0) sx[m] = s;
+    if (threadIdx.x == 0 && r == 0) sx[m] = s;
     // codes in the weight words' byte order, placed in the B fragment order of the integer mma:
     // per 32 k and lane column c, the 4 codes of k = 32t + 4c .. then those of k = 32t + 16 + 4c ..
     // (8 contiguous bytes, one load per instruction)
     int8_t* qr = xq + (long long)m * Kp;
     const int G = (Kp + gs - 1) / gs;
     const int lpg = gs / 8;                                         // lanes per scaling group
-    for (int k8 = threadIdx.x * 8; k8 - threadIdx.x * 8 < Kp; k8 += QX_THREADS * 8) {
+    for (int base = seg0; base < seg1; base += QX_THREADS) {       // the same trip count on every lane
+        const int sg = base + threadIdx.x;
+        const int k8 = sg * 8;
         int tot = 0;
-        if (k8 < Kp) {
+        if (sg < seg1) {
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
             if (k8 < K) v = *reinterpret_cast<const uint4*>(xr + k8);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -96,10 +121,13 @@ __global__ void __launch_bounds__(QX_THREADS) quant_x_kernel(const uint16_t* __r
                 *reinterpret_cast<uint32_t*>(qr + (blk >> 1) * 32 + cc * 8 + (blk & 1) * 4) = packed;
             }
         }
-        // the group's sum over its lpg lanes (the loop runs the same number of times on every lane)
+        // the group's sum over its lpg lanes (seg0 and the step are multiples of lpg, so a group's
+        // segments sit on consecutive lanes starting at a multiple of lpg)
         for (int o = 1; o < lpg; o <<= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-        if (k8 < Kp && (threadIdx.x % lpg) == 0) sxl[(long long)m * G + k8 / gs] = tot;
+        if (sg < seg1 && (sg % lpg) == 0) sxl[(long long)m * G + k8 / gs] = tot;
     }
+    // no CTA leaves while a peer may still read its share_max
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 }  // namespace
@@ -202,8 +230,7 @@ __global__ void __launch_bounds__(128, A8_CTAS_PER_SM) gemv_a8_kernel(const Gemv
         // lane (g, c): rows g, g + 8 of D; columns (rows of x) 2c, 2c + 1
         const int m0c = 2 * c < M ? 2 * c : M - 1, m1c = 2 * c + 1 < M ? 2 * c + 1 : M - 1;
         const uint8_t* xg = reinterpret_cast<const uint8_t*>(xq) + (long long)(g < M ? g : M - 1) * Kp + 8 * c;
-#pragma unroll 1
-        for (int gg = 0; gg < ng; ++gg) {
+        auto group_step = [&](const int gg) {
             // the group's exact integer sum of (stored code) x (x code) per row and column: GB / 2
             // instructions of m16n8k32 (u8 x s8 -> s32), each over two 16-k blocks
             int d[4] = {0, 0, 0, 0};
@@ -237,6 +264,14 @@ __global__ void __launch_bounds__(128, A8_CTAS_PER_SM) gemv_a8_kernel(const Gemv
                 acc[jr][0] = fmaf(sc, (float)(d[2 * jr] - zc * sx0), acc[jr][0]);
                 acc[jr][1] = fmaf(sc, (float)(d[2 * jr + 1] - zc * sx1), acc[jr][1]);
             }
+        };
+        if (ng == GPT) {
+            // whole tiles: several groups' loads (codes, x codes, their sums) in flight together
+#pragma unroll 4
+            for (int gg = 0; gg < GPT; ++gg) group_step(gg);
+        } else {
+#pragma unroll 1
+            for (int gg = 0; gg < ng; ++gg) group_step(gg);
         }
         __syncwarp();
         // the tile's partial sums (rows g + 8 jr, columns 2c + e), stored like the mma GEMV's
@@ -318,7 +353,25 @@ size_t a8_smem_bytes(int fmt) {
 
 cudaError_t launch_quant_x(const uint16_t* x, int8_t* xq, float* sx, int* sxl, int M, int K, int Kp, int gs, int perm,
                            cudaStream_t st) {
-    quant_x_kernel<<<M, QX_THREADS, 0, st>>>(x, xq, sx, sxl, M, K, Kp, gs, perm);
+    const int G = (Kp + gs - 1) / gs;
+    for (int m0 = 0; m0 < M; m0 += 65535) {                        // rows per launch: the grid's y extent
+        const int mb = (M - m0) < 65535 ? (M - m0) : 65535;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(QX_CTAS, (unsigned)mb);
+        cfg.blockDim = dim3(QX_THREADS);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = QX_CTAS;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, quant_x_kernel, x + (long long)m0 * K, xq + (long long)m0 * Kp, sx + m0,
+                                           sxl + (long long)m0 * G, mb, K, Kp, gs, perm);
+        if (e != cudaSuccess) return e;
+    }
     return cudaGetLastError();
 }
 
