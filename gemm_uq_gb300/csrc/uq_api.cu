@@ -328,7 +328,7 @@ enum Route { ROUTE_GEMV = 0, ROUTE_MMA_GEMM = 1, ROUTE_TC = 2 };
 Route route(int fmt, int M, int N, int K) {
     const int path = g_path.load(std::memory_order_relaxed);
     const bool tc = M >= 16 && uq::tc_supported(fmt, N, K);
-    if (uq::gemv_is_mma(fmt) && M >= 9) {
+    if (uq::gemm_mma_format(fmt) && M >= 9) {
         if (path == 2) return ROUTE_MMA_GEMM;
         if (path == 1 && tc) return ROUTE_TC;
         if (path == 0 && (M <= 15 || fmt == UQ_K4 || !tc)) return ROUTE_MMA_GEMM;

@@ -18,7 +18,9 @@
 //    (stream-K) and store each tile's partial sums in global memory for gemv_split_reduce, a
 //    second launch that sums each row over its k tiles in k order.  Both orders are fixed, so
 //    results are bit-reproducible, and a row's result is the same for either split and any M.
-//  * gemv_mma_kernel (INT4_SYM, INT4_ASYM, INT2_ASYM, K4 at M = 1..8, except the case below):
+//  * gemv_mma_kernel (INT4_SYM, INT4_ASYM, INT2_ASYM, K4, INT8_SYM at M = 1..8, except the case
+//    below; INT8: the stored byte q + 128 = 16 hi + lo, its two nibbles through the same bf16 magic,
+//    two mma chains per block, sum q x = 16 D_hi + D_lo - 2304 sum x):
 //    one CTA per SM, a copy warp feeding 12 compute warps through one ring of tile pairs (one
 //    16 KB bulk copy per pair) in nearly all of shared memory; x whole in shared memory or read
 //    through L1; the sums of x over each scaling group in a table formed once per CTA.
@@ -29,7 +31,7 @@
 //    Both kernels form the sums of x in the same order, so they give the same rows.
 //    With launch overlap both request their first weights before waiting for the previous
 //    kernel on the stream (the weights are constant).
-//  * gemv_kernel (INT8_SYM, NF4, whose codes do not map onto bf16 exactly by a bit trick): the
+//  * gemv_kernel (NF4, whose codebook values do not map onto bf16 exactly by a bit trick): the
 //    same layout on CUDA-core FMAs, four stages per warp on mbarriers; the four lanes sharing a
 //    row are reduced with warp shuffles, and a row block split between workers is finished by
 //    the last contributor (fence + ticket), summing the partials in worker order.
@@ -43,7 +45,8 @@ template <int FMT> struct GemvFmt {
     static constexpr int KT = fmt_kt(FMT);
     static constexpr int KC = fmt_kc(FMT);
     static constexpr int BPC = KC / 16;                            // 16-wide k blocks per chunk
-    static constexpr bool MMA = (FMT == UQ_INT4_SYM || FMT == UQ_INT4_ASYM || FMT == UQ_K4 || FMT == UQ_INT2_ASYM);
+    static constexpr bool MMA = (FMT == UQ_INT4_SYM || FMT == UQ_INT4_ASYM || FMT == UQ_K4 || FMT == UQ_INT2_ASYM ||
+                                 FMT == UQ_INT8_SYM);
     static constexpr int GT_MAX = KT / 32;                         // groups per tile row at group 32
     static constexpr int STAGES = (FMT == UQ_INT2_ASYM) ? 3 : 4;
     static constexpr bool NEEDS_SX = MMA;                          // per-group sums of x
@@ -460,9 +463,9 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
             return;
         }
 
-        static_assert(!F::MMA, "the 4-bit and 2-bit formats run gemv_mma_kernel");
+        static_assert(FMT == UQ_NF4, "every other format runs gemv_mma_kernel or gemv_warp_kernel");
         {
-            // CUDA-core path (INT8_SYM, NF4): lane holds rows g and g + 8 at k = 16 blk + 4c .. +3
+            // CUDA-core path (NF4): lane holds rows g and g + 8 at k = 16 blk + 4c .. +3
             const int G_all = mc.G;
             RowPtrs<FMT> rp[2];
             rp[0] = row_ptrs<FMT>(st, mc, g, n0 + g, kb);
@@ -480,12 +483,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
                     const int lb = q * BPC + bi;
                     const int blk = blk0 + lb;
                     float cv[2][4];
-                    if constexpr (FMT == UQ_INT8_SYM) {
-#pragma unroll
-                        for (int j = 0; j < 2; ++j)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) cv[j][e] = byte_magic_f32(wv[2 * bi + j], e) - 8388736.0f;
-                    } else {
+                    {
                         const uint32_t wd = wv[bi];
 #pragma unroll
                         for (int pp = 0; pp < 4; ++pp) {
@@ -674,6 +672,7 @@ __host__ __device__ inline int gemv_mma_meta(int fmt, int group) {
         case UQ_INT4_SYM: return gemv_mma_meta_t<UQ_INT4_SYM>(group);
         case UQ_INT4_ASYM: return gemv_mma_meta_t<UQ_INT4_ASYM>(group);
         case UQ_INT2_ASYM: return gemv_mma_meta_t<UQ_INT2_ASYM>(group);
+        case UQ_INT8_SYM: return gemv_mma_meta_t<UQ_INT8_SYM>(group);
         default: return gemv_mma_meta_t<UQ_K4>(32);
     }
 }
@@ -751,7 +750,7 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
     constexpr int GS = GB * 16;                                     // k per scaling group
     constexpr int GPT = KT / GS;                                    // groups per full tile row
     constexpr int MB = MetaGeom<FMT, GPT>::META_BYTES;              // metadata bytes per tile
-    constexpr int WPG = (FMT == UQ_INT2_ASYM) ? GB / 2 : GB;        // code words per lane per group
+    constexpr int WPG = (FMT == UQ_INT2_ASYM) ? GB / 2 : (FMT == UQ_INT8_SYM ? 2 * GB : GB);   // code words per lane per group
     constexpr int BPCH = F::BPC;                                    // 16-k blocks per 512-byte chunk
     constexpr int SPG = GS / 8;                                     // 8-k segments of x per group
     constexpr bool XS = XM == MMA_X_WHOLE;
@@ -1020,6 +1019,12 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
                         const uint4 v1 = *reinterpret_cast<const uint4*>(cp + CHUNK);
                         wv[0] = v0.x; wv[1] = v0.y; wv[2] = v0.z; wv[3] = v0.w;
                         wv[4] = v1.x; wv[5] = v1.y; wv[6] = v1.z; wv[7] = v1.w;
+                    } else if constexpr (WPG == 16) {                  // INT8 at 128-k groups: 4 chunks
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(cp + q * CHUNK);
+                            wv[4 * q] = v.x; wv[4 * q + 1] = v.y; wv[4 * q + 2] = v.z; wv[4 * q + 3] = v.w;
+                        }
                     } else if constexpr (WPG == 2) {
                         const uint2 v = *reinterpret_cast<const uint2*>(cp);
                         wv[0] = v.x; wv[1] = v.y;
@@ -1035,13 +1040,37 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
                     uint2 v;
                     if constexpr (XS) v = *reinterpret_cast<const uint2*>(xt + (gg * GB + j) * 32);
                     else v = ldg_nc_v2(xgt + (gg * GB + j) * 16);
-                    bx[j] = v.x; by[j] = v.y;
+                    if constexpr (FMT == UQ_INT8_SYM) {
+                        // an INT8 word holds k 4c .. 4c + 3 of one row and its nibble pairs come out as
+                        // (4c, 4c + 2) and (4c + 1, 4c + 3): x paired the same way
+                        bx[j] = __byte_perm(v.x, v.y, 0x5410);
+                        by[j] = __byte_perm(v.x, v.y, 0x7632);
+                    } else {
+                        bx[j] = v.x; by[j] = v.y;
+                    }
                 }
-                // the group's sum of (128 + q) x, in two chains (even / odd blocks)
+                // the group's sum of (128 + q) x, in two chains (even / odd blocks); INT8: the sums
+                // over the stored bytes' high and low nibbles, (128 + hi) x and (128 + lo) x
                 float dd[2][4];
 #pragma unroll
                 for (int j = 0; j < GB; ++j) {
                     uint32_t a0, a1, a2, a3;
+                    if constexpr (FMT == UQ_INT8_SYM) {
+                        // chunk j / 2 holds blocks j & ~1, j | 1: words (block, row g) and (block, row g + 8)
+                        const uint32_t wg = wv[4 * (j >> 1) + 2 * (j & 1)], wg8 = wv[4 * (j >> 1) + 2 * (j & 1) + 1];
+                        const uint32_t h0 = nib_pair_lop3<1>(wg), h1 = nib_pair_lop3<1>(wg8);
+                        const uint32_t h2 = nib_pair_lop3<3>(wg), h3 = nib_pair_lop3<3>(wg8);
+                        a0 = nib_pair_lop3<0>(wg); a1 = nib_pair_lop3<0>(wg8);
+                        a2 = nib_pair_lop3<2>(wg); a3 = nib_pair_lop3<2>(wg8);
+                        if (j == 0) {
+                            mma_bf16_zero(dd[0], a0, a1, a2, a3, bx[j], by[j]);
+                            mma_bf16_zero(dd[1], h0, h1, h2, h3, bx[j], by[j]);
+                        } else {
+                            mma_bf16(dd[0], a0, a1, a2, a3, bx[j], by[j]);
+                            mma_bf16(dd[1], h0, h1, h2, h3, bx[j], by[j]);
+                        }
+                        continue;
+                    }
                     if constexpr (FMT == UQ_INT2_ASYM) {
                         const uint32_t wd = wv[j >> 1];
                         if (j & 1) {
@@ -1063,7 +1092,12 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
                 const float2 sxv = *reinterpret_cast<const float2*>(sxk + gg * 8);
                 float d[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) d[e] = dd[0][e] + dd[1][e];
+                for (int e = 0; e < 4; ++e) {
+                    // INT8: the stored byte is u = q + 128 = 16 hi + lo, so sum u x = 16 D_hi + D_lo - 2176 sum x
+                    // and sum q x = 16 D_hi + D_lo - 2304 sum x (the offset folds in below)
+                    if constexpr (FMT == UQ_INT8_SYM) d[e] = fmaf(16.0f, dd[1][e], dd[0][e]);
+                    else d[e] = dd[0][e] + dd[1][e];
+                }
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     if constexpr (FMT == UQ_K4) {
@@ -1075,6 +1109,7 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
                     } else {
                         float sc, zc;
                         row_meta<FMT>(rp[j], gg, sc, zc);
+                        if constexpr (FMT == UQ_INT8_SYM) zc = 2304.0f;
                         const float szc = sc * zc;
                         acc[2 * j] = fmaf(sc, d[2 * j], fmaf(-szc, sxv.x, acc[2 * j]));
                         acc[2 * j + 1] = fmaf(sc, d[2 * j + 1], fmaf(-szc, sxv.y, acc[2 * j + 1]));
@@ -1508,7 +1543,7 @@ __global__ void __launch_bounds__(WarpCfg<FMT>::WARPS * 32, WARP_CTAS_PER_SM) ge
 inline bool gemv_x_in_smem(int fmt, int K, int group, int M) {
     return gemv_smem_plan(fmt, K, group, M, true).total <= 227 * 1024;
 }
-// shared memory of the CUDA-core GEMV (INT8_SYM, NF4)
+// shared memory of the CUDA-core GEMV (NF4)
 inline size_t gemv_smem_bytes_impl(int fmt, int K, int group, int M) {
     return gemv_smem_plan(fmt, K, group, M, gemv_x_in_smem(fmt, K, group, M)).total;
 }
@@ -1647,7 +1682,7 @@ cudaError_t launch_mma_xs(const GemvArgs& a, int grid, cudaStream_t st) {
 
 template <int FMT>
 cudaError_t launch_gemv_fmt(const GemvArgs& a, int grid, cudaStream_t st) {
-    if constexpr (FMT == UQ_INT4_SYM || FMT == UQ_INT4_ASYM || FMT == UQ_INT2_ASYM || FMT == UQ_K4) {
+    if constexpr (FMT == UQ_INT4_SYM || FMT == UQ_INT4_ASYM || FMT == UQ_INT2_ASYM || FMT == UQ_K4 || FMT == UQ_INT8_SYM) {
         const int gs = (FMT == UQ_K4) ? 32 : a.group;
         switch (gs) {
             case 32: return gemv_detail::launch_mma_xs<FMT, 2>(a, grid, st);

@@ -68,8 +68,12 @@ struct GemvArgs {
     int sx_groups;
 };
 constexpr int GEMV_WARPS = 4;     // worker warps per CTA of the CUDA-core GEMV
-// formats whose GEMV runs on mma.sync (the others on CUDA-core FMAs)
+// formats whose GEMV runs on mma.sync (NF4 on CUDA-core FMAs)
 inline bool gemv_is_mma(int fmt) {
+    return fmt == UQ_INT4_SYM || fmt == UQ_INT4_ASYM || fmt == UQ_INT2_ASYM || fmt == UQ_K4 || fmt == UQ_INT8_SYM;
+}
+// formats of the mma.sync GEMM (gemm_mma_kernel: 9..64 rows)
+inline bool gemm_mma_format(int fmt) {
     return fmt == UQ_INT4_SYM || fmt == UQ_INT4_ASYM || fmt == UQ_INT2_ASYM || fmt == UQ_K4;
 }
 // Plans one GEMV launch from its shape fields (M, N, K, group, NB, KB, T, gated, a8) and the SM

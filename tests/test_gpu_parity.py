@@ -162,7 +162,10 @@ def test_kernel_count_matches_the_paths():
     assert uq.gemm_noalloc_scratch(1, 14336, 4096, 128, "INT4_ASYM") == (0, 0)
     assert uq.gemm_kernel_count(1, 4096, 14336, 128, "INT4_ASYM") == 2
     assert uq.gemm_noalloc_scratch(1, 4096, 14336, 128, "INT4_ASYM") == (0, 256 * 14 * 16 * 4)
-    assert uq.gemm_kernel_count(1, 8192, 8192, 128, "INT8_SYM") == 1
+    # INT8 8192 x 8192 at M = 1 (512-k tiles): whole row blocks would give a CTA 64 tiles, more than
+    # it holds partial sums for, so the stream-K split and its second pass
+    assert uq.gemm_kernel_count(1, 8192, 8192, 128, "INT8_SYM") == 2
+    assert uq.gemm_noalloc_scratch(1, 8192, 8192, 128, "INT8_SYM") == (0, 512 * 16 * 16 * 4)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert uq.gemm_kernel_count(64, 14336, 4096, 128, "INT4_ASYM") == 1
     assert uq.gemm_kernel_count(128, 14336, 4096, 128, "INT4_ASYM") == 2

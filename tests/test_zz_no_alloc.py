@@ -88,11 +88,11 @@ def test_noalloc_refuses_partial_sums_beyond_its_scratch():
 
 
 def test_noalloc_refuses_tickets_beyond_its_scratch():
-    """INT8_SYM with K = 32 (one k tile): 4.2 M rows are 262,500 row blocks, whose 4-byte tickets
-    alone exceed the array, while the partial sums (two row blocks per worker warp) are small.  Every
-    buffer is sized for the request, so nothing outside the caller's memory would be read even if
-    the check did not fire."""
-    N, K, group, fmt, M = 4_200_000, 32, 32, "INT8_SYM", 1
+    """NF4 (the CUDA-core GEMV, the format that finishes split row blocks by tickets) with K = 32
+    (one k tile): 4.2 M rows are 262,500 row blocks, whose 4-byte tickets alone exceed the array,
+    while the partial sums (two row blocks per worker warp) are small.  Every buffer is sized for the
+    request, so nothing outside the caller's memory would be read even if the check did not fire."""
+    N, K, group, fmt, M = 4_200_000, 32, 32, "NF4", 1
     assert (N + 15) // 16 * 4 > SCRATCH - 256
     xd, wq, sc, zc, y = _zeros_problem(N, K, group, fmt, M)
     with pytest.raises(uq.UqError) as e:
