@@ -160,8 +160,8 @@ def read_share(workload):
 def dominant_kernel(fmt, group, M, shapes):
     """Name of the kernel template the library dispatches for this workload's linears (uq_gemm's
     automatic routing: the mma.sync GEMM for 9..15 rows of the 4-bit / 2-bit formats and for K4, the
-    tensor cores for other blocks of 16..64 rows, the GEMVs below: per-warp rings for one row of the
-    4-bit flat formats, the copy-warp ring otherwise)."""
+    tensor cores for other blocks of 16..64 rows, the mma.sync GEMVs below: per-warp rings for one
+    row of the 4-bit flat formats, the copy-warp ring otherwise)."""
     mma_fmt = fmt in ("INT4_SYM", "INT4_ASYM", "INT2_ASYM", "K4")        # the mma.sync GEMM's formats
     tc_ok = M >= 16 and all(K % KT[fmt] == 0 for _, K in shapes)
     if mma_fmt and M >= 9 and (M <= 15 or fmt == "K4" or not tc_ok):
@@ -170,12 +170,10 @@ def dominant_kernel(fmt, group, M, shapes):
     if tc_ok:
         mpad = (min(M, 64) + 15) // 16 * 16
         return f"tc_kernel<{fmt},{mpad}>"
-    if mma_fmt or fmt == "INT8_SYM":
-        gs = 32 if fmt == "K4" else group
-        if M == 1 and fmt in ("INT4_SYM", "INT4_ASYM"):
-            return f"gemv_warp_kernel<{fmt},GB={gs // 16}>"
-        return f"gemv_mma_kernel<{fmt},GB={gs // 16}>"
-    return f"gemv_kernel<{fmt},{min(M, 8)}>"
+    gs = 32 if fmt == "K4" else group
+    if M == 1 and fmt in ("INT4_SYM", "INT4_ASYM"):
+        return f"gemv_warp_kernel<{fmt},GB={gs // 16}>"
+    return f"gemv_mma_kernel<{fmt},GB={gs // 16}>"
 
 
 def kernels_per_call(fmt, group, M, N, K):

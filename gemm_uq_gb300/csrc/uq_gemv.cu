@@ -35,12 +35,6 @@ static int plan_warp_rings(GemvArgs& a, int sms, int W, int cps, int tpw) {
 
 int gemv_plan(GemvArgs& a, int fmt, int sms) {
     a.cta_rows = 0;
-    if (!gemv_is_mma(fmt) && !a.a8) {
-        if (gemv_smem_bytes_impl(fmt, a.K, a.group, a.M) > 227 * 1024) return 0;
-        const long long P = (long long)sms * GEMV_WARPS;
-        a.P = (int)(P < a.T ? P : a.T);
-        return (a.P + GEMV_WARPS - 1) / GEMV_WARPS;
-    }
     const int WU = a.gated ? 2 : 1;
     const int NBU = a.NB / WU;
     if (a.a8) return plan_warp_rings(a, sms, 4, A8_CTAS_PER_SM, A8_TPW);
@@ -77,14 +71,18 @@ int gemv_plan(GemvArgs& a, int fmt, int sms) {
 }
 
 size_t gemv_partials_floats(int fmt, const GemvArgs& a) {
-    // mma / W4A8 GEMV: one 16-row slot per tile (k-major tiles, summed over k by the second pass);
-    // CUDA-core GEMV: two slots per worker (the first and last row block of its range)
-    if (gemv_is_mma(fmt) || a.a8) return a.cta_rows ? 0 : (size_t)a.T * RB * a.M;
-    return gemv_partials_floats_impl(a.P, a.M);
+    // one 16-row slot per tile (k-major tiles, summed over k by the second pass)
+    (void)fmt;
+    return a.cta_rows ? 0 : (size_t)a.T * RB * a.M;
 }
-bool gemv_uses_tickets(int fmt, const GemvArgs& a) { return !gemv_is_mma(fmt) && !a.a8; }
+bool gemv_uses_tickets(int fmt, const GemvArgs& a) {
+    (void)fmt;
+    (void)a;
+    return false;                       // every GEMV sums shared row blocks in its second pass
+}
 int gemv_launches(int fmt, const GemvArgs& a) {
-    return ((gemv_is_mma(fmt) || a.a8) && !a.cta_rows) ? 2 : 1;
+    (void)fmt;
+    return a.cta_rows ? 1 : 2;
 }
 
 // Second pass of the mma GEMV when workers split the matrix's tiles (k-major, so every tile's
@@ -149,7 +147,7 @@ cudaError_t launch_gemv(int fmt, const GemvArgs& a, int grid, cudaStream_t st) {
         case UQ_K4: e = launch_gemv_fmt<UQ_K4>(a, grid, st); break;
         default: return cudaErrorInvalidValue;
     }
-    if (e != cudaSuccess || !gemv_is_mma(fmt) || a.cta_rows) return e;
+    if (e != cudaSuccess || a.cta_rows) return e;
     // the mma kernel leaves row blocks shared between workers as partial sums (grid = its CTAs,
     // one per SM at most, so it is also the SM count bound for the reduce grid)
     return launch_gemv_second_pass(a, grid, st);

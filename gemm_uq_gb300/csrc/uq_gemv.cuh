@@ -18,12 +18,13 @@
 //    (stream-K) and store each tile's partial sums in global memory for gemv_split_reduce, a
 //    second launch that sums each row over its k tiles in k order.  Both orders are fixed, so
 //    results are bit-reproducible, and a row's result is the same for either split and any M.
-//  * gemv_mma_kernel (INT4_SYM, INT4_ASYM, INT2_ASYM, K4, INT8_SYM at M = 1..8, except the case
-//    below; INT8: the stored byte q + 128 = 16 hi + lo, its two nibbles through the same bf16 magic,
-//    two mma chains per block, sum q x = 16 D_hi + D_lo - 2304 sum x):
-//    one CTA per SM, a copy warp feeding 12 compute warps through one ring of tile pairs (one
-//    16 KB bulk copy per pair) in nearly all of shared memory; x whole in shared memory or read
-//    through L1; the sums of x over each scaling group in a table formed once per CTA.
+//  * gemv_mma_kernel (every format at M = 1..8, except the case below): one CTA per SM, a copy
+//    warp feeding 12 compute warps through one ring of tile pairs (one 16 KB bulk copy per pair)
+//    in nearly all of shared memory; x whole in shared memory or read through L1; the sums of x
+//    over each scaling group in a table formed once per CTA.  INT8: the stored byte q + 128 =
+//    16 hi + lo, its two nibbles through the same bf16 magic, two mma chains per block, sum q x =
+//    16 D_hi + D_lo - 2304 sum x.  NF4: each codebook value c[q] as hi = bf16(c[q]) and lo =
+//    bf16(c[q] - hi) (16 significant bits) from a 16-entry shared table, two mma chains per block.
 //  * gemv_warp_kernel (INT4_SYM, INT4_ASYM at M = 1): the same per-tile arithmetic on per-warp
 //    rings of two stages (16-byte cp.async by each warp's own lanes) and double-buffered slices
 //    of x, two CTAs per SM.  Its launches are short, and two ~105 KB CTAs per SM let the next
@@ -31,10 +32,6 @@
 //    Both kernels form the sums of x in the same order, so they give the same rows.
 //    With launch overlap both request their first weights before waiting for the previous
 //    kernel on the stream (the weights are constant).
-//  * gemv_kernel (NF4, whose codebook values do not map onto bf16 exactly by a bit trick): the
-//    same layout on CUDA-core FMAs, four stages per warp on mbarriers; the four lanes sharing a
-//    row are reduced with warp shuffles, and a row block split between workers is finished by
-//    the last contributor (fence + ticket), summing the partials in worker order.
 #pragma once
 #include "uq_kernels.h"
 
@@ -46,10 +43,8 @@ template <int FMT> struct GemvFmt {
     static constexpr int KC = fmt_kc(FMT);
     static constexpr int BPC = KC / 16;                            // 16-wide k blocks per chunk
     static constexpr bool MMA = (FMT == UQ_INT4_SYM || FMT == UQ_INT4_ASYM || FMT == UQ_K4 || FMT == UQ_INT2_ASYM ||
-                                 FMT == UQ_INT8_SYM);
+                                 FMT == UQ_INT8_SYM || FMT == UQ_NF4);
     static constexpr int GT_MAX = KT / 32;                         // groups per tile row at group 32
-    static constexpr int STAGES = (FMT == UQ_INT2_ASYM) ? 3 : 4;
-    static constexpr bool NEEDS_SX = MMA;                          // per-group sums of x
 };
 
 // Stage geometry: a stage is one tile's codes followed by its rows' metadata, MW 32-bit words per
@@ -66,46 +61,14 @@ template <int FMT, int GT = 0> struct MetaGeom {
     static constexpr int STAGE_BYTES = TILE_BYTES + META_BYTES;
 };
 
-// bytes per row of x in shared memory: the row zero-padded to Kp plus 32 bytes, so the rows of a
-// B fragment (one 8-byte load per row) fall into different banks
-__host__ __device__ inline size_t gemv_x_stride(int Kp) { return (size_t)Kp * 2 + 32; }
-
-// shared-memory plan; identical on host and device
+// shared-memory offsets of a GEMV launch (the per-warp-ring kernels); identical on host and device
 struct GemvSmem {
     size_t bars, lut, sx, ps, x, total;
 };
-template <int FMT>
-__host__ __device__ inline GemvSmem gemv_smem_plan_t(int K, int group, int M, bool x_in_smem) {
-    using F = GemvFmt<FMT>;
-    const int Kp = (K + F::KC - 1) / F::KC * F::KC;
-    const int gs = (FMT == UQ_K4) ? 32 : group;
-    GemvSmem p;
-    p.bars = (size_t)GEMV_WARPS * F::STAGES * MetaGeom<FMT>::STAGE_BYTES;
-    p.lut = p.bars + (size_t)(GEMV_WARPS * F::STAGES + 1) * 8;     // + the x mbarrier
-    p.sx = p.lut + 64;
-    p.x = p.sx + (F::NEEDS_SX ? (size_t)((Kp + gs - 1) / gs) * 8 * 4 : 0);   // sums padded to 8 columns
-    p.ps = p.x;
-    p.x = (p.x + 127) / 128 * 128;
-    p.total = p.x + (x_in_smem ? (size_t)M * gemv_x_stride(Kp) : 0);
-    return p;
-}
-__host__ __device__ inline GemvSmem gemv_smem_plan(int fmt, int K, int group, int M, bool x_in_smem) {
-    switch (fmt) {
-        case UQ_INT4_SYM: return gemv_smem_plan_t<UQ_INT4_SYM>(K, group, M, x_in_smem);
-        case UQ_INT4_ASYM: return gemv_smem_plan_t<UQ_INT4_ASYM>(K, group, M, x_in_smem);
-        case UQ_INT8_SYM: return gemv_smem_plan_t<UQ_INT8_SYM>(K, group, M, x_in_smem);
-        case UQ_INT2_ASYM: return gemv_smem_plan_t<UQ_INT2_ASYM>(K, group, M, x_in_smem);
-        case UQ_NF4: return gemv_smem_plan_t<UQ_NF4>(K, group, M, x_in_smem);
-        default: return gemv_smem_plan_t<UQ_K4>(K, group, M, x_in_smem);
-    }
-}
 
 namespace {
 
 __device__ __forceinline__ long long range_begin(int w, long long T, int P) { return (long long)w * T / P; }
-__device__ __forceinline__ int worker_of(long long t, long long T, int P) {
-    return (int)(((t + 1) * (long long)P - 1) / T);
-}
 
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
     uint4 v;
@@ -242,36 +205,18 @@ __device__ __forceinline__ void issue_meta(const GemvArgs& a, const GemvSrc& w, 
 }
 
 // Issue the copies of tile t into stage buffer `st` (its codes, then its metadata at st +
-// TILE_BYTES; all lanes take part), in one of two modes:
-//   ISSUE_BULK   the codes as one bulk copy counted on `bar` (transaction bytes), the metadata as
-//                cp.async arriving on `bar` too (33 arrivals: one per lane when its copies land,
-//                and the codes' expect_tx);
-//   ISSUE_GROUP  everything 16-byte cp.async (codes: 512 contiguous bytes per warp instruction) in
-//                one cp.async group per lane that the issuing warp itself waits for (`bar` unused).
-// Per-lane copies keep more of a warp's tile stream in flight than one 8 KB bulk copy per tile:
-// the copy engine takes bulk copies one after another, at well under an SM's share of HBM
-// bandwidth at this size.
-constexpr int ISSUE_BULK = 0, ISSUE_GROUP = 1;
-template <int FMT, int MODE = ISSUE_BULK, int GTC = 0>
+// TILE_BYTES; all lanes take part): 16-byte cp.async for the codes (512 contiguous bytes per warp
+// instruction) and the metadata, in one cp.async group per lane that the issuing warp itself waits
+// for (the per-warp-ring kernels).  GTC: the groups per tile row when the caller knows them at
+// compile time (0: mc.GT at run time).
+template <int FMT, int GTC = 0>
 __device__ __forceinline__ void issue_tile(const GemvArgs& a, const GemvSrc& w, const Layout& L, const MetaConst& mc, int nb, int kb,
-                                           uint8_t* st, uint64_t* bar, int lane) {
+                                           uint8_t* st, int lane) {
     issue_meta<FMT, GTC>(a, w, mc, nb, kb, reinterpret_cast<uint32_t*>(st + TILE_BYTES), lane);
-    if constexpr (MODE == ISSUE_GROUP) {
-        const int bytes = (int)L.tile_bytes(kb);
-        const uint8_t* src = w.wq + L.tile_offset(nb, kb);
-        for (int off = lane * 16; off < bytes; off += 512) cp_async16(st + off, src + off);
-        cp_async_commit_group();
-        (void)bar;
-    } else {
-        cp_async_arrive_noinc(bar);
-        __syncwarp();
-        if (lane == 0) {
-            const uint32_t bytes = (uint32_t)L.tile_bytes(kb);
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar, bytes);
-            bulk_g2s(st, w.wq + L.tile_offset(nb, kb), bytes, bar);
-        }
-    }
+    const int bytes = (int)L.tile_bytes(kb);
+    const uint8_t* src = w.wq + L.tile_offset(nb, kb);
+    for (int off = lane * 16; off < bytes; off += 512) cp_async16(st + off, src + off);
+    cp_async_commit_group();
 }
 
 // Pointers to row r's staged scales (fp16) and zero points for tile kb: the staged words start
@@ -329,293 +274,6 @@ __device__ __forceinline__ void row_meta_k4(const uint8_t* st, int r, int li, fl
 
 }  // namespace
 
-template <int FMT, int M, bool XS>
-__global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs a) {
-    using F = GemvFmt<FMT>;
-    constexpr int KT = F::KT, S = F::STAGES, BPC = F::BPC;
-    extern __shared__ __align__(128) uint8_t smem[];
-    const GemvSmem plan = gemv_smem_plan_t<FMT>(a.K, a.group, M, XS);
-    uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + plan.bars);
-    float* lut = reinterpret_cast<float*>(smem + plan.lut);
-    float* sxg = reinterpret_cast<float*>(smem + plan.sx);
-    uint8_t* xs = smem + plan.x;                                   // x rows (+ a zero row), stride xstride
-    uint64_t* xbar = bars_all + GEMV_WARPS * S;
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, c = lane & 3;
-    const int w = blockIdx.x * GEMV_WARPS + warp;
-    const bool has_work = w < a.P;
-    const Layout L(a.N, a.K, FMT);
-    const int gs = (FMT == UQ_K4) ? 32 : a.group;                 // scaling granularity along k
-    MetaConst mc;
-    mc.G = a.K / a.group;
-    mc.GT = KT / a.group;
-    mc.ZB = (mc.G + 1) >> 1;
-    mc.S4 = a.K / 256;
-    const int bpg = gs / 16;                                       // 16-k blocks per group: 2, 4 or 8
-    const int bpg_log = bpg == 2 ? 1 : (bpg == 4 ? 2 : 3);
-    const size_t xstride = gemv_x_stride(L.Kp);
-    // 16-byte metadata copies: row slices 16-byte aligned and a multiple of 16 bytes long
-    mc.aligned = (a.K % (8 * a.group)) == 0 && (mc.GT % 8) == 0;
-    uint8_t* ring = smem + (size_t)warp * S * MetaGeom<FMT>::STAGE_BYTES;
-    uint64_t* bars = bars_all + warp * S;
-    const long long t0 = has_work ? range_begin(w, a.T, a.P) : 0;
-    const long long t1 = has_work ? range_begin(w + 1, a.T, a.P) : 0;
-
-    // 0. let the next kernel on the stream start launching (it only prefetches its own weights
-    //    before it waits for this grid; no effect unless launched with launch overlap)
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-    // 1. start the weight stream before anything else (weights and metadata are constant)
-    if (has_work) {
-        if (lane == 0) {
-#pragma unroll
-            for (int s = 0; s < S; ++s) mbar_init(&bars[s], 33);   // lane 0's expect_tx + 32 cp.async arrivals
-            fence_barrier_init();
-        }
-        __syncwarp();
-        int inb = (int)(t0 / L.KB), ikb = (int)(t0 % L.KB);
-        for (int s = 0; s < S && t0 + s < t1; ++s) {
-            issue_tile<FMT>(a, GemvSrc{a.wq, a.scales, a.zc}, L, mc, inb, ikb, ring + s * MetaGeom<FMT>::STAGE_BYTES, &bars[s], lane);
-            if (++ikb == L.KB) { ikb = 0; ++inb; }
-        }
-    }
-
-    // 2. everything below may depend on the previous kernel on the stream (x, the split-K
-    //    workspace, y): wait for it to complete (returns at once when not launched overlapped)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-
-    // CTA prologue: codebook, x rows, per-group sums of x
-    if constexpr (FMT == UQ_NF4) {
-        if (threadIdx.x < 16) lut[threadIdx.x] = reinterpret_cast<const float*>(a.zc)[threadIdx.x];
-    }
-    if constexpr (XS) {
-        // one bulk copy per row of x into shared memory (rows are K * 2 bytes, a multiple of 16);
-        // the pad [K, Kp) of every row is zero
-        if (threadIdx.x == 0) {
-            mbar_init(xbar, 1);
-            fence_barrier_init();
-            mbar_arrive_expect_tx(xbar, (uint32_t)(M * a.K * 2));
-#pragma unroll
-            for (int m = 0; m < M; ++m) bulk_g2s(xs + m * xstride, a.x + (long long)m * a.ldx, (uint32_t)(a.K * 2), xbar);
-        }
-        const int padw = (L.Kp - a.K) / 2;                          // 32-bit words of pad per row
-        for (int e = threadIdx.x; e < M * padw; e += blockDim.x)
-            reinterpret_cast<uint32_t*>(xs + (e / padw) * xstride + a.K * 2)[e % padw] = 0u;
-        __syncthreads();
-        // on a timeout the fault word is set and the kernel goes on (its results are then
-        // meaningless) so the ring's copies in flight are still drained below
-        mbar_wait_bounded(xbar, 0, a.fault, FAULT_GEMV_WAIT);
-    }
-    if constexpr (F::NEEDS_SX) {
-        // sxg[gi * 8 + m] = sum of x[m][k] over group gi (k < K), in k order; 0 for m >= M
-        const int gp = (L.Kp + gs - 1) / gs;
-        for (int e = threadIdx.x; e < gp * 8; e += blockDim.x) {
-            const int gi = e >> 3, m = e & 7;
-            float s0 = 0.f;
-            if (m < M) {
-                const int kend = (gi * gs + gs) < a.K ? (gi * gs + gs) : a.K;
-                for (int k = gi * gs; k < kend; k += 8) {
-                    uint4 q;
-                    if constexpr (XS) q = *reinterpret_cast<const uint4*>(xs + m * xstride + k * 2);
-                    else q = ldg_nc_v4(a.x + (long long)m * a.ldx + k);
-                    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) s0 += bf16lo_f32(u[j]) + bf16hi_f32(u[j]);
-                }
-            }
-            sxg[e] = s0;
-        }
-    }
-    __syncthreads();
-    if (!has_work) return;
-
-    const int first_nb = (int)(t0 / L.KB);
-    // MMA path: acc[j*2 + e] = row g + 8j, column 2c + e.  FFMA path: accf[j][m] = row g + 8j.
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float accf[2][M];
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int m = 0; m < M; ++m) accf[j][m] = 0.f;
-
-    // (row block, k tile) of the tile being consumed and of the next one to prefetch, advanced
-    // incrementally (no 64-bit division per tile)
-    int nb = (int)(t0 / L.KB), kb = (int)(t0 % L.KB);
-    int pnb = nb, pkb = kb;
-    for (int s = 0; s < S; ++s)
-        if (++pkb == L.KB) { pkb = 0; ++pnb; }
-    for (long long t = t0; t < t1; ++t) {
-        const int it = (int)(t - t0);
-        const int s = it % S;
-        const uint32_t parity = (uint32_t)((it / S) & 1);
-        const int n0 = nb * RB;
-        uint8_t* st = ring + s * MetaGeom<FMT>::STAGE_BYTES;
-        const int nchunks = L.chunks(kb);
-        const int blk0 = (kb * KT) / 16;                           // first global 16-k block of the tile
-
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], parity, a.fault, FAULT_GEMV_WAIT))) {
-            // give the copies still in flight a bounded chance to land, then leave
-            for (int j = 1; j < S && t + j < t1; ++j) {
-                const int sj = (it + j) % S;
-                mbar_wait_bounded(&bars[sj], (uint32_t)(((it + j) / S) & 1), a.fault, FAULT_GEMV_WAIT);
-            }
-            return;
-        }
-
-        static_assert(FMT == UQ_NF4, "every other format runs gemv_mma_kernel or gemv_warp_kernel");
-        {
-            // CUDA-core path (NF4): lane holds rows g and g + 8 at k = 16 blk + 4c .. +3
-            const int G_all = mc.G;
-            RowPtrs<FMT> rp[2];
-            rp[0] = row_ptrs<FMT>(st, mc, g, n0 + g, kb);
-            rp[1] = row_ptrs<FMT>(st, mc, g + 8, n0 + g + 8, kb);
-            float p[2][M];
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int m = 0; m < M; ++m) p[j][m] = 0.f;
-            for (int q = 0; q < nchunks; ++q) {
-                const uint4 cw = *reinterpret_cast<const uint4*>(st + q * CHUNK + lane * 16);
-                const uint32_t wv[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-                for (int bi = 0; bi < BPC; ++bi) {
-                    const int lb = q * BPC + bi;
-                    const int blk = blk0 + lb;
-                    float cv[2][4];
-                    {
-                        const uint32_t wd = wv[bi];
-#pragma unroll
-                        for (int pp = 0; pp < 4; ++pp) {
-                            // pair pp: row g + 8 (pp & 1), k = 4c + 2 (pp >> 1) + {0, 1}
-                            cv[pp & 1][2 * (pp >> 1)] = lut[(wd >> (4 * pp)) & 15u];
-                            cv[pp & 1][2 * (pp >> 1) + 1] = lut[(wd >> (16 + 4 * pp)) & 15u];
-                        }
-                    }
-#pragma unroll
-                    for (int m = 0; m < M; ++m) {
-                        uint2 xb;
-                        xb = make_uint2(0, 0);
-                        if (blk * 16 + 4 * c < a.K) {
-                            if constexpr (XS) xb = *reinterpret_cast<const uint2*>(xs + m * xstride + (blk * 16 + 4 * c) * 2);
-                            else xb = ldg_nc_v2(a.x + (long long)m * a.ldx + blk * 16 + 4 * c);
-                        }
-                        const float x0 = bf16lo_f32(xb.x), x1 = bf16hi_f32(xb.x);
-                        const float x2 = bf16lo_f32(xb.y), x3 = bf16hi_f32(xb.y);
-#pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            p[j][m] = fmaf(x0, cv[j][0], p[j][m]);
-                            p[j][m] = fmaf(x1, cv[j][1], p[j][m]);
-                            p[j][m] = fmaf(x2, cv[j][2], p[j][m]);
-                            p[j][m] = fmaf(x3, cv[j][3], p[j][m]);
-                        }
-                    }
-                    if (((lb + 1) & (bpg - 1)) == 0) {
-                        const int li = lb >> bpg_log;
-                        if (kb * mc.GT + li < G_all) {
-#pragma unroll
-                            for (int j = 0; j < 2; ++j) {
-                                float sc, zc;
-                                row_meta<FMT>(rp[j], li, sc, zc);
-#pragma unroll
-                                for (int m = 0; m < M; ++m) accf[j][m] = fmaf(sc, p[j][m], accf[j][m]);
-                            }
-                        }
-#pragma unroll
-                        for (int j = 0; j < 2; ++j)
-#pragma unroll
-                            for (int m = 0; m < M; ++m) p[j][m] = 0.f;
-                    }
-                }
-            }
-        }
-        __syncwarp();
-        if (t + S < t1) {
-            issue_tile<FMT>(a, GemvSrc{a.wq, a.scales, a.zc}, L, mc, pnb, pkb, st, &bars[s], lane);
-            if (++pkb == L.KB) { pkb = 0; ++pnb; }
-        }
-
-        if (kb == L.KB - 1 || t == t1 - 1) {
-            // row block done (for this worker): write y or a partial
-            const bool full = (kb == L.KB - 1) && (nb != first_nb || (t0 % L.KB) == 0);
-            // this thread's results: rows g + 8j, columns 2c + e (MMA) or all columns (FFMA, lane c == 0)
-            float out[2][M];
-            bool mine[2][M];
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int m = 0; m < M; ++m) { out[j][m] = 0.f; mine[j][m] = false; }
-            if constexpr (F::MMA) {
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e)
-#pragma unroll
-                        for (int m = 0; m < M; ++m)
-                            if (m == 2 * c + e) { out[j][m] = acc[2 * j + e]; mine[j][m] = true; }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-#pragma unroll
-                    for (int m = 0; m < M; ++m) {
-                        float v = accf[j][m];
-                        v += __shfl_xor_sync(0xffffffffu, v, 1);
-                        v += __shfl_xor_sync(0xffffffffu, v, 2);
-                        out[j][m] = v;
-                        mine[j][m] = (c == 0);
-                    }
-            }
-            if (full) {
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-#pragma unroll
-                    for (int m = 0; m < M; ++m) {
-                        const int n = n0 + g + 8 * j;
-                        if (mine[j][m] && n < a.N)
-                            store_out(a, m, n, out[j][m]);
-                    }
-            } else {
-                const int slot = 2 * w + (nb == first_nb ? 0 : 1);
-                float* part = a.partials + (long long)slot * RB * M;
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-#pragma unroll
-                    for (int m = 0; m < M; ++m)
-                        if (mine[j][m]) part[(g + 8 * j) * M + m] = out[j][m];
-                __threadfence();
-                __syncwarp();
-                unsigned int old = 0;
-                if (lane == 0) old = atomicAdd(a.tickets + nb, 1u);
-                old = __shfl_sync(0xffffffffu, old, 0);
-                const long long tf = (long long)nb * L.KB;
-                const int wf = worker_of(tf, a.T, a.P), wl = worker_of(tf + L.KB - 1, a.T, a.P);
-                if (old == (unsigned int)(wl - wf)) {
-                    __threadfence();
-                    for (int e = lane; e < RB * M; e += 32) {
-                        const int r = e / M, m = e % M;
-                        if (n0 + r >= a.N) continue;
-                        float sum = 0.f;
-                        for (int w2 = wf; w2 <= wl; ++w2) {
-                            const int nb2 = (int)(range_begin(w2, a.T, a.P) / L.KB);
-                            const int slot2 = 2 * w2 + (nb == nb2 ? 0 : 1);
-                            sum += __ldcg(a.partials + (long long)slot2 * RB * M + e);
-                        }
-                        store_out(a, m, n0 + r, sum);
-                    }
-                    if (lane == 0) a.tickets[nb] = 0u;
-                }
-            }
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int m = 0; m < M; ++m) accf[j][m] = 0.f;
-        }
-        if (++kb == L.KB) { kb = 0; ++nb; }
-    }
-}
-
-
 // ------------------------------------------------------------------------------------------------
 // 4-bit and 2-bit formats: the GEMV on mma.sync.  GB = 16-k blocks per scaling group (2, 4 or 8;
 // K4 uses its 32-weight sub-blocks, GB = 2).  M (1..8) is a runtime value: the instruction always
@@ -644,6 +302,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32, 1) gemv_kernel(const GemvArgs
 constexpr int MMA_CW = 12;                  // compute warps per CTA (even: a warp keeps one half of its pairs)
 constexpr int MMA_PMAX = 16;                // ring slots (tile pairs) at most
 constexpr int MMA_TPC = 48;                 // tiles per CTA at most when it owns whole row blocks
+constexpr int MMA_BAR_BYTES = (2 * MMA_PMAX + 1) * 8 + 64;   // mbarriers, then NF4's 16-entry table
 constexpr int MMA_SMEM = 227 * 1024;        // dynamic shared memory of the CTA at most
 // the W4A8 GEMV (uq_w4a8.cu) keeps per-warp rings: two CTAs of 4 warps per SM, at most 6 tiles per
 // warp when a CTA owns whole row blocks
@@ -673,6 +332,7 @@ __host__ __device__ inline int gemv_mma_meta(int fmt, int group) {
         case UQ_INT4_ASYM: return gemv_mma_meta_t<UQ_INT4_ASYM>(group);
         case UQ_INT2_ASYM: return gemv_mma_meta_t<UQ_INT2_ASYM>(group);
         case UQ_INT8_SYM: return gemv_mma_meta_t<UQ_INT8_SYM>(group);
+        case UQ_NF4: return gemv_mma_meta_t<UQ_NF4>(group);
         default: return gemv_mma_meta_t<UQ_K4>(32);
     }
 }
@@ -694,7 +354,7 @@ __host__ __device__ inline int gemv_mma_sx_groups(int fmt, int group, int NB, in
 }
 
 // Shared memory: codes [S2][2][8 KB] | metadata [S2][2][meta] | full[S2], empty[S2] and x
-// mbarriers | sums of x [groups][8] | partial sums [tiles of the CTA][16][8] (whole row blocks) |
+// mbarriers, NF4's table | sums of x [groups][8] | partial sums [tiles of the CTA][16][8] (whole row blocks) |
 // x (MMA_X_WHOLE).  S2 = the slots that fit beside the rest (at most MMA_PMAX).  Identical on
 // host and device.
 struct MmaSmem {
@@ -708,7 +368,7 @@ __host__ __device__ inline MmaSmem gemv_mma_offsets(int S2, int mb, int sxg, int
     p.mb = mb;
     p.meta = (size_t)S2 * 2 * TILE_BYTES;
     p.bars = p.meta + (size_t)S2 * 2 * mb;
-    p.sx = (p.bars + (size_t)(2 * MMA_PMAX + 1) * 8 + 15) / 16 * 16;
+    p.sx = (p.bars + (size_t)MMA_BAR_BYTES + 15) / 16 * 16;
     p.ps = p.sx + (size_t)sxg * 8 * 4;
     p.x = (p.ps + (size_t)tpc * RB * 8 * 4 + 127) / 128 * 128;
     p.total = p.x + (xm == MMA_X_WHOLE ? (size_t)M * gemv_mma_x_stride(Kp) : 0);
@@ -719,7 +379,7 @@ __host__ __device__ inline MmaSmem gemv_mma_smem(int fmt, int K, int group, int 
     const int slot = 2 * (TILE_BYTES + mb);
     const int kc = fmt_kc(fmt);
     const int Kp = (K + kc - 1) / kc * kc;
-    const size_t bars = (size_t)(2 * MMA_PMAX + 1) * 8;
+    const size_t bars = (size_t)MMA_BAR_BYTES;
     const size_t xb = xm == MMA_X_WHOLE ? (size_t)M * gemv_mma_x_stride(Kp) : 0;
     const size_t rest = bars + 16 + (size_t)sxg * 8 * 4 + (size_t)tpc * RB * 8 * 4 + 128 + xb;   // + alignment
     long long S2 = ((long long)MMA_SMEM - (long long)rest) / slot;
@@ -767,6 +427,7 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + plan.bars);
     uint64_t* empty = full + S2;
     uint64_t* xbar = full + 2 * S2;
+    uint32_t* nlut = reinterpret_cast<uint32_t*>(smem + plan.bars + (2 * MMA_PMAX + 1) * 8);   // NF4: (hi | lo << 16)
     float* sxt = reinterpret_cast<float*>(smem + plan.sx);
     float* cpart = reinterpret_cast<float*>(smem + plan.ps);
     uint8_t* xs = smem + plan.x;
@@ -964,6 +625,16 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
         for (int e = threadIdx.x; e < nsx * 8; e += CW * 32)
             if ((e & 7) >= M) sxt[e] = 0.f;
     }
+    if constexpr (FMT == UQ_NF4) {
+        // the codebook value c[q] as hi = bf16(c[q]) and lo = bf16(c[q] - hi): hi + lo carries 16
+        // significant bits of c[q] (relative error below 2^-16); two mma chains multiply x by both
+        if (threadIdx.x < 16) {
+            const float cq = reinterpret_cast<const float*>(a.zc)[threadIdx.x];
+            const __nv_bfloat16 hi = __float2bfloat16_rn(cq);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(cq - __bfloat162float(hi));
+            nlut[threadIdx.x] = (uint32_t)__bfloat16_as_ushort(hi) | ((uint32_t)__bfloat16_as_ushort(lo) << 16);
+        }
+    }
     compute_warps_sync();                                           // the table and x padding are written
     bool xok = true;
     if constexpr (XS) xok = mbar_wait_bounded(xbar, 0, a.fault, FAULT_GEMV_WAIT);
@@ -1050,7 +721,8 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
                     }
                 }
                 // the group's sum of (128 + q) x, in two chains (even / odd blocks); INT8: the sums
-                // over the stored bytes' high and low nibbles, (128 + hi) x and (128 + lo) x
+                // over the stored bytes' high and low nibbles, (128 + hi) x and (128 + lo) x; NF4: the
+                // sums over the codebook values' hi and lo parts (no offset: zc = 0)
                 float dd[2][4];
 #pragma unroll
                 for (int j = 0; j < GB; ++j) {
@@ -1068,6 +740,25 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
                         } else {
                             mma_bf16(dd[0], a0, a1, a2, a3, bx[j], by[j]);
                             mma_bf16(dd[1], h0, h1, h2, h3, bx[j], by[j]);
+                        }
+                        continue;
+                    }
+                    if constexpr (FMT == UQ_NF4) {
+                        // pair P: the codes at bits 4P and 16 + 4P, their values from the table
+                        const uint32_t wd = wv[j];
+                        uint32_t hi[4], lo[4];
+#pragma unroll
+                        for (int P = 0; P < 4; ++P) {
+                            const uint32_t e = nlut[(wd >> (4 * P)) & 15u], o = nlut[(wd >> (16 + 4 * P)) & 15u];
+                            hi[P] = __byte_perm(e, o, 0x5410);
+                            lo[P] = __byte_perm(e, o, 0x7632);
+                        }
+                        if (j == 0) {
+                            mma_bf16_zero(dd[0], hi[0], hi[1], hi[2], hi[3], bx[j], by[j]);
+                            mma_bf16_zero(dd[1], lo[0], lo[1], lo[2], lo[3], bx[j], by[j]);
+                        } else {
+                            mma_bf16(dd[0], hi[0], hi[1], hi[2], hi[3], bx[j], by[j]);
+                            mma_bf16(dd[1], lo[0], lo[1], lo[2], lo[3], bx[j], by[j]);
                         }
                         continue;
                     }
@@ -1317,8 +1008,8 @@ __global__ void __launch_bounds__(WarpCfg<FMT>::WARPS * 32, WARP_CTAS_PER_SM) ge
     int ikb = ntl > 0 ? kb_of(t0) : 0, irb = ntl > 0 ? (int)(t0 % R) : 0;   // the next tile to request
     auto issue_next = [&]() {
         const int nbw = rb0 + irb;
-        issue_tile<FMT, ISSUE_GROUP, GPT>(a, (GATED && (nbw & 1)) ? src_up : src_gate, L, mc, GATED ? nbw >> 1 : nbw, ikb,
-                                   ring + (issued % S) * MetaGeom<FMT>::STAGE_BYTES, &bars[issued % S], lane);
+        issue_tile<FMT, GPT>(a, (GATED && (nbw & 1)) ? src_up : src_gate, L, mc, GATED ? nbw >> 1 : nbw, ikb,
+                             ring + (issued % S) * MetaGeom<FMT>::STAGE_BYTES, lane);
         if (++irb == R) { irb = 0; ++ikb; }
         ++issued;
     };
@@ -1540,54 +1231,6 @@ __global__ void __launch_bounds__(WarpCfg<FMT>::WARPS * 32, WARP_CTAS_PER_SM) ge
 }
 
 
-inline bool gemv_x_in_smem(int fmt, int K, int group, int M) {
-    return gemv_smem_plan(fmt, K, group, M, true).total <= 227 * 1024;
-}
-// shared memory of the CUDA-core GEMV (NF4)
-inline size_t gemv_smem_bytes_impl(int fmt, int K, int group, int M) {
-    return gemv_smem_plan(fmt, K, group, M, gemv_x_in_smem(fmt, K, group, M)).total;
-}
-inline size_t gemv_partials_floats_impl(int P, int M) { return (size_t)2 * P * RB * M; }
-
-namespace gemv_detail {
-template <int FMT, int M, bool XS>
-cudaError_t launch_one(const GemvArgs& a, int grid, cudaStream_t st) {
-    static bool configured[64] = {};   // the shared-memory opt-in, once per device
-    const size_t smem = gemv_smem_plan_t<FMT>(a.K, a.group, M, XS).total;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(gemv_kernel<FMT, M, XS>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
-    if (launch_overlap()) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(grid);
-        cfg.blockDim = dim3(GEMV_WARPS * 32);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = st;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, gemv_kernel<FMT, M, XS>, a);
-        if (e != cudaSuccess) return e;
-    } else {
-        gemv_kernel<FMT, M, XS><<<grid, GEMV_WARPS * 32, smem, st>>>(a);
-    }
-    return cudaGetLastError();
-}
-template <int FMT, int M>
-cudaError_t launch_xs(const GemvArgs& a, int grid, cudaStream_t st) {
-    if (gemv_x_in_smem(FMT, a.K, a.group, M)) return launch_one<FMT, M, true>(a, grid, st);
-    return launch_one<FMT, M, false>(a, grid, st);
-}
-}  // namespace gemv_detail
-
 namespace gemv_detail {
 template <int FMT, int GB, int XM, bool GATED>
 cudaError_t launch_mma(const GemvArgs& a, int grid, int sxg, cudaStream_t st) {
@@ -1682,28 +1325,14 @@ cudaError_t launch_mma_xs(const GemvArgs& a, int grid, cudaStream_t st) {
 
 template <int FMT>
 cudaError_t launch_gemv_fmt(const GemvArgs& a, int grid, cudaStream_t st) {
-    if constexpr (FMT == UQ_INT4_SYM || FMT == UQ_INT4_ASYM || FMT == UQ_INT2_ASYM || FMT == UQ_K4 || FMT == UQ_INT8_SYM) {
-        const int gs = (FMT == UQ_K4) ? 32 : a.group;
-        switch (gs) {
-            case 32: return gemv_detail::launch_mma_xs<FMT, 2>(a, grid, st);
-            case 64: if constexpr (FMT != UQ_K4) return gemv_detail::launch_mma_xs<FMT, 4>(a, grid, st);
-                     return cudaErrorInvalidValue;
-            case 128: if constexpr (FMT != UQ_K4) return gemv_detail::launch_mma_xs<FMT, 8>(a, grid, st);
-                      return cudaErrorInvalidValue;
-            default: return cudaErrorInvalidValue;
-        }
-    } else {
-    switch (a.M) {
-        case 1: return gemv_detail::launch_xs<FMT, 1>(a, grid, st);
-        case 2: return gemv_detail::launch_xs<FMT, 2>(a, grid, st);
-        case 3: return gemv_detail::launch_xs<FMT, 3>(a, grid, st);
-        case 4: return gemv_detail::launch_xs<FMT, 4>(a, grid, st);
-        case 5: return gemv_detail::launch_xs<FMT, 5>(a, grid, st);
-        case 6: return gemv_detail::launch_xs<FMT, 6>(a, grid, st);
-        case 7: return gemv_detail::launch_xs<FMT, 7>(a, grid, st);
-        case 8: return gemv_detail::launch_xs<FMT, 8>(a, grid, st);
+    const int gs = (FMT == UQ_K4) ? 32 : a.group;
+    switch (gs) {
+        case 32: return gemv_detail::launch_mma_xs<FMT, 2>(a, grid, st);
+        case 64: if constexpr (FMT != UQ_K4) return gemv_detail::launch_mma_xs<FMT, 4>(a, grid, st);
+                 return cudaErrorInvalidValue;
+        case 128: if constexpr (FMT != UQ_K4) return gemv_detail::launch_mma_xs<FMT, 8>(a, grid, st);
+                  return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
-    }
     }
 }
 

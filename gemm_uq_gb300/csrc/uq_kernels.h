@@ -67,10 +67,10 @@ struct GemvArgs {
     int ring_slots;           // mma GEMV: ring slots and x-sum table groups of the launch (set by its launcher)
     int sx_groups;
 };
-constexpr int GEMV_WARPS = 4;     // worker warps per CTA of the CUDA-core GEMV
-// formats whose GEMV runs on mma.sync (NF4 on CUDA-core FMAs)
+// formats whose GEMV runs on mma.sync (all six)
 inline bool gemv_is_mma(int fmt) {
-    return fmt == UQ_INT4_SYM || fmt == UQ_INT4_ASYM || fmt == UQ_INT2_ASYM || fmt == UQ_K4 || fmt == UQ_INT8_SYM;
+    return fmt == UQ_INT4_SYM || fmt == UQ_INT4_ASYM || fmt == UQ_INT2_ASYM || fmt == UQ_K4 || fmt == UQ_INT8_SYM ||
+           fmt == UQ_NF4;
 }
 // formats of the mma.sync GEMM (gemm_mma_kernel: 9..64 rows)
 inline bool gemm_mma_format(int fmt) {

@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(128, A8_CTAS_PER_SM) gemv_a8_kernel(const Gemv
     // k-major tile coordinates advanced incrementally (no 64-bit division per tile)
     int ikb = ntl > 0 ? kb_of(t0) : 0, irb = ntl > 0 ? (int)(t0 % R) : 0;   // the next tile to request
     auto issue_next = [&]() {
-        issue_tile<FMT, ISSUE_GROUP, GPT>(a, src, L, mc, rb0 + irb, ikb, ring + (issued % S) * MetaGeom<FMT>::STAGE_BYTES, nullptr, lane);
+        issue_tile<FMT, GPT>(a, src, L, mc, rb0 + irb, ikb, ring + (issued % S) * MetaGeom<FMT>::STAGE_BYTES, lane);
         if (++irb == R) { irb = 0; ++ikb; }
         ++issued;
     };

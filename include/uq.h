@@ -11,8 +11,8 @@
  * where x is M x K bf16, W_hat is the N x K dequantized weight (a linear layer's
  * weight, K contiguous) and y is M x N bf16.  W_hat is never materialised: the
  * kernels stream packed codes from HBM and unpack them in registers, where they feed
- * warp-level mma.sync instructions (4-bit and 2-bit formats: M <= 15, and K4 at any M; INT8:
- * M <= 8) or CUDA-core FMAs (NF4, M <= 15), or are written as the integer part of the weights straight
+ * warp-level mma.sync instructions (4-bit and 2-bit formats: M <= 15, and K4 at any M; INT8 and
+ * NF4: M <= 15), or are written as the integer part of the weights straight
  * into tensor memory as the A operand of tcgen05 tensor-core MMAs (M >= 16 otherwise); per-group
  * scales are applied to fp32 group sums.
  *
@@ -143,8 +143,8 @@ uq_status uq_pack_kmeta(const uint16_t* d, const uint16_t* dmin, const uint8_t* 
  *   group: 32, 64 or 128 for the flat formats (K % group == 0; UQ_INT2_ASYM also needs
  *   K % 64 == 0); 256 for UQ_K4 (K % 256 == 0).
  * Paths, per block of rows of x:
- *   - M <= 8: the GEMV (mma.sync for INT4_SYM, INT4_ASYM, INT2_ASYM, K4 and INT8_SYM; CUDA-core
- *     FMAs for NF4): one launch when each CTA owns whole row blocks, else the GEMV and a second
+ *   - M <= 8: the GEMV on mma.sync (NF4's codebook values as two bf16 parts, hi + lo, with 16
+ *     significant bits): one launch when each CTA owns whole row blocks, else the GEMV and a second
  *     launch that sums each row's partials in a fixed order, so repeated calls are bit-identical,
  *     and a row of x gives the same bits whatever the other rows of a call of M <= 8;
  *   - INT4_SYM, INT4_ASYM, INT2_ASYM with 9 <= M <= 15, and K4 with M >= 9: the mma.sync GEMM in
@@ -178,11 +178,11 @@ uq_status uq_gemm(const uint16_t* x, const void* wq, const void* scales,
  *   x (device) bf16 [M][K]; wq_gate / scales_gate / zc_gate and wq_up / scales_up / zc_up (device):
  *   two weights of the same N, K, group and format, each as uq_gemm takes them; h (device) bf16
  *   [M][N], written.  M == 0 or N == 0 is a no-op; K == 0 writes zeros.
- * Paths, routed as uq_gemm: INT4_SYM, INT4_ASYM, INT2_ASYM, K4 and INT8_SYM with M <= 8 (and a last
- * block of at most 8 rows after mma.sync GEMM blocks) run one mma-GEMV launch over both weights (gate
+ * Paths, routed as uq_gemm: every format with M <= 8 (and a last block of at most 8 rows after
+ * mma.sync GEMM blocks) runs one mma-GEMV launch over both weights (gate
  * and up row blocks interleaved, each CTA owning whole gate/up pairs, h formed in its per-row
  * reduction), plus the second pass when the work split shares row blocks between CTAs; everything
- * else (the mma.sync GEMM, NF4, the tensor-core path) runs the gate projection into
+ * else (the mma.sync GEMM, the tensor-core path) runs the gate projection into
  * fp32 library scratch and then the up projection, whose epilogue reads g and writes h.
  * uq_gemm_gated_kernel_count gives the launches.
  * Scratch, errors and stream capture as uq_gemm (the fp32 gate scratch, rows x N floats, is part of
@@ -340,13 +340,9 @@ uq_status uq_device_fault(unsigned int* flag);
  * it until the process exits); 256 bytes hold the fault word, and the rest must hold what the
  * launch's work split uses for one 8-row block of x (Mb = min(M, 8); uq_gemm_noalloc_scratch
  * reports it):
- *   - INT4_SYM, INT4_ASYM, INT2_ASYM, K4, INT8_SYM (mma.sync GEMV): nothing when every CTA owns
- *     whole 16-row blocks (the split uq_gemm_kernel_count reports as one launch); otherwise fp32
- *     partial sums of every tile, 64*Mb*ceil(N/16)*ceil(K/T) bytes (T = 1024 codes, 2048 for
- *     INT2_ASYM, 512 for INT8_SYM): ceil(N/16)*ceil(K/T)*Mb <= 16380;
- *   - NF4 (CUDA-core GEMV): 4*ceil(N/16) bytes of tickets, rounded up to 256, plus fp32 partial
- *     sums of two row blocks per worker warp (128*Mb*workers bytes, workers = min(4 * SMs,
- *     ceil(N/16)*ceil(K/T)), T = 1024 codes).
+ *   nothing when every CTA owns whole 16-row blocks (the split uq_gemm_kernel_count reports as one
+ *   launch); otherwise fp32 partial sums of every tile, 64*Mb*ceil(N/16)*ceil(K/T) bytes (T = 1024
+ *   codes, 2048 for INT2_ASYM, 512 for INT8_SYM): ceil(N/16)*ceil(K/T)*Mb <= 16380.
  * Larger requests return UQ_ERR_NOMEM with the sizes in uq_last_error().  K == 0 returns
  * UQ_ERR_UNSUPPORTED.  Calls no cudaMalloc, cudaFree or other allocating routine.
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress) with
@@ -361,8 +357,9 @@ uq_status uq_gemm_noalloc(const uint16_t* x, const void* wq, const void* scales,
 
 /*
  * uq_gemm_noalloc_scratch -- the static scratch uq_gemm_noalloc would use for this shape on the
- * current device: *ticket_bytes (row-block tickets of the CUDA-core GEMV, rounded up to 256) and
- * *partial_bytes (fp32 partial sums; 0 when every worker owns whole row blocks), as listed above.
+ * current device: *ticket_bytes (row-block tickets; 0: every GEMV sums its partials in a second
+ * launch) and *partial_bytes (fp32 partial sums; 0 when every CTA owns whole row blocks), as listed
+ * above.
  * Host-only (queries the SM count).  UQ_ERR_INVALID /
  * UQ_ERR_UNSUPPORTED as uq_gemm_noalloc for shapes it rejects; it does not check the 1 MiB limit.
  */

@@ -87,19 +87,6 @@ def test_noalloc_refuses_partial_sums_beyond_its_scratch():
     assert uq.device_fault() == 0
 
 
-def test_noalloc_refuses_tickets_beyond_its_scratch():
-    """NF4 (the CUDA-core GEMV, the format that finishes split row blocks by tickets) with K = 32
-    (one k tile): 4.2 M rows are 262,500 row blocks, whose 4-byte tickets alone exceed the array,
-    while the partial sums (two row blocks per worker warp) are small.  Every buffer is sized for the
-    request, so nothing outside the caller's memory would be read even if the check did not fire."""
-    N, K, group, fmt, M = 4_200_000, 32, 32, "NF4", 1
-    assert (N + 15) // 16 * 4 > SCRATCH - 256
-    xd, wq, sc, zc, y = _zeros_problem(N, K, group, fmt, M)
-    with pytest.raises(uq.UqError) as e:
-        uq.gemm_noalloc(xd, wq, sc, zc, N, group, fmt, y=y)
-    assert e.value.status == 5
-
-
 def test_noalloc_needs_no_partial_sums_when_ctas_own_whole_row_blocks():
     """19456 x 4096 INT4_SYM at M = 8: every CTA owns whole 16-row blocks (one launch), so no scratch
     beyond the fault word is used, although the stream-K split of the same shape would need 2.5 MB of
