@@ -387,9 +387,10 @@ __host__ __device__ inline MmaSmem gemv_mma_smem(int fmt, int K, int group, int 
     if (S2 < 0) S2 = 0;
     return gemv_mma_offsets((int)S2, mb, sxg, tpc, M, Kp, xm);
 }
-// x in shared memory when that leaves the ring 3 slots beyond those the compute warps hold
+// x in shared memory when that leaves the ring 2 slots beyond those the compute warps hold
+// (measured: 8 rows of x through L1 cost more than a shallower ring)
 __host__ __device__ inline int gemv_mma_xmode(int fmt, int K, int group, int M, int sxg, int tpc) {
-    return gemv_mma_smem(fmt, K, group, M, sxg, tpc, MMA_X_WHOLE).S2 >= MMA_CW / 2 + 3 ? MMA_X_WHOLE : MMA_X_GLOBAL;
+    return gemv_mma_smem(fmt, K, group, M, sxg, tpc, MMA_X_WHOLE).S2 >= MMA_CW / 2 + 2 ? MMA_X_WHOLE : MMA_X_GLOBAL;
 }
 
 __device__ __forceinline__ float bf16_pair_sum(uint32_t w) {
