@@ -313,9 +313,10 @@ constexpr int A8_TPW = 6;
 // B-fragment loads touch into different banks
 __host__ __device__ inline size_t gemv_mma_x_stride(int Kp) { return (size_t)Kp * 2 + 32; }
 
-// Where the mma GEMV reads x (template parameter XM): MMA_X_WHOLE, all of x copied into shared
-// memory once per CTA; MMA_X_GLOBAL, straight from global memory (through L1), when a whole x would
-// leave the ring too few slots.
+// Where the mma GEMV reads x (template parameter XM): MMA_X_WHOLE, the CTA's window of x (the k
+// tiles its work touches: all of K when it owns whole row blocks, a few k tiles under the stream-K
+// split) copied into shared memory once per CTA; MMA_X_GLOBAL, straight from global memory (through
+// L1), when that window would leave the ring too few slots.
 constexpr int MMA_X_GLOBAL = 0, MMA_X_WHOLE = 1;
 
 // metadata bytes of one tile at this group size
@@ -362,7 +363,7 @@ struct MmaSmem {
     int S2, mb;                                     // slots, metadata bytes per tile
 };
 // offsets for S2 slots (multiplications and additions only: the kernel forms them per launch)
-__host__ __device__ inline MmaSmem gemv_mma_offsets(int S2, int mb, int sxg, int tpc, int M, int Kp, int xm) {
+__host__ __device__ inline MmaSmem gemv_mma_offsets(int S2, int mb, int sxg, int tpc, int M, int xk, int xm) {
     MmaSmem p;
     p.S2 = S2;
     p.mb = mb;
@@ -371,21 +372,22 @@ __host__ __device__ inline MmaSmem gemv_mma_offsets(int S2, int mb, int sxg, int
     p.sx = (p.bars + (size_t)MMA_BAR_BYTES + 15) / 16 * 16;
     p.ps = p.sx + (size_t)sxg * 8 * 4;
     p.x = (p.ps + (size_t)tpc * RB * 8 * 4 + 127) / 128 * 128;
-    p.total = p.x + (xm == MMA_X_WHOLE ? (size_t)M * gemv_mma_x_stride(Kp) : 0);
+    p.total = p.x + (xm == MMA_X_WHOLE ? (size_t)M * gemv_mma_x_stride(xk) : 0);
     return p;
 }
 __host__ __device__ inline MmaSmem gemv_mma_smem(int fmt, int K, int group, int M, int sxg, int tpc, int xm) {
     const int mb = gemv_mma_meta(fmt, group);
     const int slot = 2 * (TILE_BYTES + mb);
-    const int kc = fmt_kc(fmt);
-    const int Kp = (K + kc - 1) / kc * kc;
+    const int gpt = fmt_kt(fmt) / (fmt == UQ_K4 ? 32 : group);
+    const int xk = sxg / gpt * fmt_kt(fmt);                         // k extent of a CTA's window of x
+    (void)K;
     const size_t bars = (size_t)MMA_BAR_BYTES;
-    const size_t xb = xm == MMA_X_WHOLE ? (size_t)M * gemv_mma_x_stride(Kp) : 0;
+    const size_t xb = xm == MMA_X_WHOLE ? (size_t)M * gemv_mma_x_stride(xk) : 0;
     const size_t rest = bars + 16 + (size_t)sxg * 8 * 4 + (size_t)tpc * RB * 8 * 4 + 128 + xb;   // + alignment
     long long S2 = ((long long)MMA_SMEM - (long long)rest) / slot;
     if (S2 > MMA_PMAX) S2 = MMA_PMAX;
     if (S2 < 0) S2 = 0;
-    return gemv_mma_offsets((int)S2, mb, sxg, tpc, M, Kp, xm);
+    return gemv_mma_offsets((int)S2, mb, sxg, tpc, M, xk, xm);
 }
 // x in shared memory when that leaves the ring 2 slots beyond those the compute warps hold
 // (measured: 8 rows of x through L1 cost more than a shallower ring)
@@ -421,7 +423,8 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
     const bool cta_rows = tpc > 0;
     const Layout L(a.N, a.K, FMT);
     const int sxg = a.sx_groups;
-    const MmaSmem plan = gemv_mma_offsets(a.ring_slots, MB, sxg, tpc, M, L.Kp, XM);
+    const int XK = sxg / GPT * KT;                                  // k extent of the CTA's window of x
+    const MmaSmem plan = gemv_mma_offsets(a.ring_slots, MB, sxg, tpc, M, XK, XM);
     const int S2 = plan.S2;
     uint8_t* ring = smem;                                           // codes: slot s, tile h at (2s + h) * 8 KB
     uint8_t* metas = smem + plan.meta;                              // metadata: slot s, tile h at (2s + h) * MB
@@ -472,7 +475,7 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
         return;
     }
     const int G_all = a.K / GS;                                     // scaling groups per row
-    const size_t xstride = gemv_mma_x_stride(L.Kp);
+    const size_t xstride = gemv_mma_x_stride(XK);
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
@@ -557,14 +560,15 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("bar.sync 2, %0;" :: "n"((CW + 1) * 32) : "memory");   // the mbarriers are initialized
     if constexpr (XS) {
+        // the CTA's window of x: k tiles kb_first .. kb_last of every row (the tiles' groups lie
+        // inside K, so nothing past K is read)
         if (threadIdx.x == 0) {
-            mbar_arrive_expect_tx(xbar, (uint32_t)(M * a.K * 2));
+            const int k0 = kb_first * KT;
+            const int k1 = (kb_last + 1) * KT < a.K ? (kb_last + 1) * KT : a.K;
+            mbar_arrive_expect_tx(xbar, (uint32_t)(M * (k1 - k0) * 2));
             for (int m = 0; m < M; ++m)
-                bulk_g2s(xs + m * xstride, a.x + (long long)m * a.ldx, (uint32_t)(a.K * 2), xbar);
+                bulk_g2s(xs + m * xstride, a.x + (long long)m * a.ldx + k0, (uint32_t)((k1 - k0) * 2), xbar);
         }
-        const int padw = (L.Kp - a.K) / 2;                          // the rows' zero padding to Kp
-        for (int e = threadIdx.x; e < M * padw; e += CW * 32)
-            reinterpret_cast<uint32_t*>(xs + (e / padw) * xstride + a.K * 2)[e % padw] = 0u;
     }
     {
         // table of x sums: entry (group gl of k tiles kb_first.., column m) = the sum of row m of x
@@ -665,7 +669,7 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
             const int gi0 = kb * GPT;
             const int ng = (G_all - gi0) < GPT ? (G_all - gi0) : GPT;   // groups of the tile inside K
             const float* sxk = sxt + (gi0 - kb_first * GPT) * 8 + 2 * c;
-            const uint8_t* xt = xrow + (size_t)kb * KT * 2;
+            const uint8_t* xt = xrow + (size_t)(kb - kb_first) * KT * 2;
             const uint16_t* xgt = xgrow + (long long)kb * KT;
             const uint8_t* st = ring + (size_t)(2 * slot + hh) * TILE_BYTES;
             // the tile's metadata, addressed as if it followed the codes (row_ptrs / row_meta_k4 add
