@@ -10,7 +10,7 @@ extern template cudaError_t launch_gemv_fmt<UQ_INT2_ASYM>(const GemvArgs&, int, 
 extern template cudaError_t launch_gemv_fmt<UQ_NF4>(const GemvArgs&, int, cudaStream_t);
 extern template cudaError_t launch_gemv_fmt<UQ_K4>(const GemvArgs&, int, cudaStream_t);
 
-// Per-warp rings (the W4A8 GEMV and gemv_warp_kernel): W warps per CTA, cps CTAs per SM.  Whole row
+// Per-warp rings (gemv_warp_kernel): W warps per CTA, cps CTAs per SM.  Whole row
 // blocks per CTA need no second pass; take them when no warp gets more tiles than under the
 // stream-K split and either the busiest CTA streams at most ~6 % more bytes than the average one
 // (bandwidth-bound shapes) or no warp has more than one tile (latency-bound ones).  (gated: the
@@ -37,8 +37,8 @@ int gemv_plan(GemvArgs& a, int fmt, int sms) {
     a.cta_rows = 0;
     const int WU = a.gated ? 2 : 1;
     const int NBU = a.NB / WU;
-    if (a.a8) return plan_warp_rings(a, sms, 4, A8_CTAS_PER_SM, A8_TPW);
-    if (gemv_warp_route(fmt, a.M)) return plan_warp_rings(a, sms, WarpCfg<UQ_INT4_ASYM>::WARPS, WARP_CTAS_PER_SM, WARP_TPW);
+    if (!a.a8 && gemv_warp_route(fmt, a.M))
+        return plan_warp_rings(a, sms, WarpCfg<UQ_INT4_ASYM>::WARPS, WARP_CTAS_PER_SM, WARP_TPW);
     // mma GEMV: one CTA per SM, its work (pairs of k tiles) shared by MMA_CW compute warps.  Whole
     // row blocks per CTA (a.cta_rows = the most tiles a CTA gets) need no second pass; take them
     // when every compute warp has one tile at most (latency-bound shapes), or when no CTA gets more

@@ -113,6 +113,15 @@ __device__ __forceinline__ void mma_bf16_zero(float (&d)[4], uint32_t a0, uint32
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(z));
 }
 
+// D += A * B for one 16 x 8 x 32 block: A unsigned 8-bit (the stored codes), B signed 8-bit (x codes),
+// exact 32-bit integer accumulation
+__device__ __forceinline__ void mma_u8s8(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Copy the 4-byte-aligned words covering bytes [lo, lo + len) of `base` into dst (word 0 holds
 // byte lo & ~3).  A word that would reach past `end` (the array's end) is assembled from plain
 // byte loads instead, so nothing outside the caller's buffer is read.
@@ -304,14 +313,11 @@ constexpr int MMA_PMAX = 16;                // ring slots (tile pairs) at most
 constexpr int MMA_TPC = 48;                 // tiles per CTA at most when it owns whole row blocks
 constexpr int MMA_BAR_BYTES = (2 * MMA_PMAX + 1) * 8 + 64;   // mbarriers, then NF4's 16-entry table
 constexpr int MMA_SMEM = 227 * 1024;        // dynamic shared memory of the CTA at most
-// the W4A8 GEMV (uq_w4a8.cu) keeps per-warp rings: two CTAs of 4 warps per SM, at most 6 tiles per
-// warp when a CTA owns whole row blocks
-constexpr int A8_CTAS_PER_SM = 2;
-constexpr int A8_TPW = 6;
 
 // bytes per row of x in shared memory: 32 bytes of padding put the four rows a half-warp's 8-byte
 // B-fragment loads touch into different banks
-__host__ __device__ inline size_t gemv_mma_x_stride(int Kp) { return (size_t)Kp * 2 + 32; }
+// (xb bytes per k: 2 for bf16 x, 1 for W4A8's int8 codes)
+__host__ __device__ inline size_t gemv_mma_x_stride(int Kp, int xb = 2) { return (size_t)Kp * xb + 32; }
 
 // Where the mma GEMV reads x (template parameter XM): MMA_X_WHOLE, the CTA's window of x (the k
 // tiles its work touches: all of K when it owns whole row blocks, a few k tiles under the stream-K
@@ -363,7 +369,7 @@ struct MmaSmem {
     int S2, mb;                                     // slots, metadata bytes per tile
 };
 // offsets for S2 slots (multiplications and additions only: the kernel forms them per launch)
-__host__ __device__ inline MmaSmem gemv_mma_offsets(int S2, int mb, int sxg, int tpc, int M, int xk, int xm) {
+__host__ __device__ inline MmaSmem gemv_mma_offsets(int S2, int mb, int sxg, int tpc, int M, int xk, int xm, int xb = 2) {
     MmaSmem p;
     p.S2 = S2;
     p.mb = mb;
@@ -372,27 +378,27 @@ __host__ __device__ inline MmaSmem gemv_mma_offsets(int S2, int mb, int sxg, int
     p.sx = (p.bars + (size_t)MMA_BAR_BYTES + 15) / 16 * 16;
     p.ps = p.sx + (size_t)sxg * 8 * 4;
     p.x = (p.ps + (size_t)tpc * RB * 8 * 4 + 127) / 128 * 128;
-    p.total = p.x + (xm == MMA_X_WHOLE ? (size_t)M * gemv_mma_x_stride(xk) : 0);
+    p.total = p.x + (xm == MMA_X_WHOLE ? (size_t)M * gemv_mma_x_stride(xk, xb) : 0);
     return p;
 }
-__host__ __device__ inline MmaSmem gemv_mma_smem(int fmt, int K, int group, int M, int sxg, int tpc, int xm) {
+__host__ __device__ inline MmaSmem gemv_mma_smem(int fmt, int K, int group, int M, int sxg, int tpc, int xm, int xb = 2) {
     const int mb = gemv_mma_meta(fmt, group);
     const int slot = 2 * (TILE_BYTES + mb);
     const int gpt = fmt_kt(fmt) / (fmt == UQ_K4 ? 32 : group);
     const int xk = sxg / gpt * fmt_kt(fmt);                         // k extent of a CTA's window of x
     (void)K;
     const size_t bars = (size_t)MMA_BAR_BYTES;
-    const size_t xb = xm == MMA_X_WHOLE ? (size_t)M * gemv_mma_x_stride(xk) : 0;
-    const size_t rest = bars + 16 + (size_t)sxg * 8 * 4 + (size_t)tpc * RB * 8 * 4 + 128 + xb;   // + alignment
+    const size_t xbytes = xm == MMA_X_WHOLE ? (size_t)M * gemv_mma_x_stride(xk, xb) : 0;
+    const size_t rest = bars + 16 + (size_t)sxg * 8 * 4 + (size_t)tpc * RB * 8 * 4 + 128 + xbytes;   // + alignment
     long long S2 = ((long long)MMA_SMEM - (long long)rest) / slot;
     if (S2 > MMA_PMAX) S2 = MMA_PMAX;
     if (S2 < 0) S2 = 0;
-    return gemv_mma_offsets((int)S2, mb, sxg, tpc, M, xk, xm);
+    return gemv_mma_offsets((int)S2, mb, sxg, tpc, M, xk, xm, xb);
 }
 // x in shared memory when that leaves the ring 2 slots beyond those the compute warps hold
 // (measured: 8 rows of x through L1 cost more than a shallower ring)
-__host__ __device__ inline int gemv_mma_xmode(int fmt, int K, int group, int M, int sxg, int tpc) {
-    return gemv_mma_smem(fmt, K, group, M, sxg, tpc, MMA_X_WHOLE).S2 >= MMA_CW / 2 + 2 ? MMA_X_WHOLE : MMA_X_GLOBAL;
+__host__ __device__ inline int gemv_mma_xmode(int fmt, int K, int group, int M, int sxg, int tpc, int xb = 2) {
+    return gemv_mma_smem(fmt, K, group, M, sxg, tpc, MMA_X_WHOLE, xb).S2 >= MMA_CW / 2 + 2 ? MMA_X_WHOLE : MMA_X_GLOBAL;
 }
 
 __device__ __forceinline__ float bf16_pair_sum(uint32_t w) {
@@ -405,11 +411,18 @@ __device__ __forceinline__ void compute_warps_sync() {
 // GATED: the gated projection in one launch.  The work list interleaves the gate and up weights' row
 // blocks (work row block 2j = gate row block j, 2j + 1 = up row block j), every CTA owns whole pairs,
 // and the per-row reduction forms h = silu(g) * u (or the second pass does, for the stream-K split).
-template <int FMT, int GB, int XM, bool GATED>
+// A8: W4A8 / W8A8 (INT4_SYM, INT4_ASYM, INT8_SYM): x is the int8 codes of a.xq (1 byte per k, each
+// 32 k in the integer mma's B fragment order), the table holds the quantizer's integer code sums,
+// the group step is mma.m16n8k32 (u8 x s8 -> s32) on the stored codes as bytes, and each tile's
+// partial sums are scaled by the row's s_x.
+template <int FMT, int GB, int XM, bool GATED, bool A8 = false>
 __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const GemvArgs a) {
     using F = GemvFmt<FMT>;
     constexpr int KT = F::KT, CW = MMA_CW, PW = MMA_CW / 2;
     static_assert(MMA_CW % 2 == 0, "compute warps come in pairs");
+    static_assert(!A8 || ((FMT == UQ_INT4_SYM || FMT == UQ_INT4_ASYM || FMT == UQ_INT8_SYM) && !GATED),
+                  "the integer path takes INT4_SYM, INT4_ASYM and INT8_SYM, not gated");
+    constexpr int XBY = A8 ? 1 : 2;                                 // bytes of x per k
     constexpr int GS = GB * 16;                                     // k per scaling group
     constexpr int GPT = KT / GS;                                    // groups per full tile row
     constexpr int MB = MetaGeom<FMT, GPT>::META_BYTES;              // metadata bytes per tile
@@ -424,7 +437,7 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
     const Layout L(a.N, a.K, FMT);
     const int sxg = a.sx_groups;
     const int XK = sxg / GPT * KT;                                  // k extent of the CTA's window of x
-    const MmaSmem plan = gemv_mma_offsets(a.ring_slots, MB, sxg, tpc, M, XK, XM);
+    const MmaSmem plan = gemv_mma_offsets(a.ring_slots, MB, sxg, tpc, M, XK, XM, XBY);
     const int S2 = plan.S2;
     uint8_t* ring = smem;                                           // codes: slot s, tile h at (2s + h) * 8 KB
     uint8_t* metas = smem + plan.meta;                              // metadata: slot s, tile h at (2s + h) * MB
@@ -475,7 +488,7 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
         return;
     }
     const int G_all = a.K / GS;                                     // scaling groups per row
-    const size_t xstride = gemv_mma_x_stride(XK);
+    const size_t xstride = gemv_mma_x_stride(XK, XBY);
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
@@ -564,10 +577,14 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
         // inside K, so nothing past K is read)
         if (threadIdx.x == 0) {
             const int k0 = kb_first * KT;
-            const int k1 = (kb_last + 1) * KT < a.K ? (kb_last + 1) * KT : a.K;
-            mbar_arrive_expect_tx(xbar, (uint32_t)(M * (k1 - k0) * 2));
-            for (int m = 0; m < M; ++m)
-                bulk_g2s(xs + m * xstride, a.x + (long long)m * a.ldx + k0, (uint32_t)((k1 - k0) * 2), xbar);
+            const int kend = A8 ? a.Kpq : a.K;                      // (the codes are zero-padded to Kpq)
+            const int k1 = (kb_last + 1) * KT < kend ? (kb_last + 1) * KT : kend;
+            mbar_arrive_expect_tx(xbar, (uint32_t)(M * (k1 - k0) * XBY));
+            for (int m = 0; m < M; ++m) {
+                const void* src = A8 ? (const void*)(a.xq + (long long)m * a.Kpq + k0)
+                                     : (const void*)(a.x + (long long)m * a.ldx + k0);
+                bulk_g2s(xs + m * xstride, src, (uint32_t)((k1 - k0) * XBY), xbar);
+            }
         }
     }
     {
@@ -578,51 +595,60 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
         // forms its sums in, so the two kernels give the same sums (and rows of y) for any M.  Each
         // round issues its tasks' loads before any sum (a load's first use would stall the next).
         // Columns m >= M are zero (their products are never stored).
-        constexpr int KL = KT / 32;                                 // k per lane
-        constexpr int NV = KL / 8;                                  // 16-byte loads per lane and task
-        constexpr int TU = NV >= 8 ? 1 : 8 / NV;                    // tasks per warp per round
-        constexpr int NGL = (KL / GS) > 1 ? (KL / GS) : 1;          // groups within a lane's k
-        const int nkt = kb_last - kb_first + 1;
-        const int ntask = M * nkt;
-        for (int tb = warp; tb < ntask; tb += TU * CW) {
-            uint4 w[TU][NV];
-#pragma unroll
-            for (int u = 0; u < TU; ++u) {
-                const int t = tb + u * CW;
-                const int m = t / nkt, kt = kb_first + (t - m * nkt);   // warp-uniform
-                const int k0 = kt * KT + lane * KL;
-#pragma unroll
-                for (int v = 0; v < NV; ++v) {
-                    w[u][v] = make_uint4(0u, 0u, 0u, 0u);
-                    if (t < ntask && k0 + 8 * v < a.K) w[u][v] = ldg_nc_v4(a.x + (long long)m * a.ldx + k0 + 8 * v);
-                }
+        if constexpr (A8) {
+            // the quantizer's per-group code sums (exact integers, below 2^24 in magnitude)
+            const int Gq = (a.Kpq + GS - 1) / GS;
+            for (int e = threadIdx.x; e < M * nsx; e += CW * 32) {
+                const int m = e / nsx, gl = e - m * nsx, gi = kb_first * GPT + gl;
+                if (gi < G_all) sxt[gl * 8 + m] = (float)__ldg(a.sxl + (long long)m * Gq + gi);
             }
+        } else {
+            constexpr int KL = KT / 32;                                 // k per lane
+            constexpr int NV = KL / 8;                                  // 16-byte loads per lane and task
+            constexpr int TU = NV >= 8 ? 1 : 8 / NV;                    // tasks per warp per round
+            constexpr int NGL = (KL / GS) > 1 ? (KL / GS) : 1;          // groups within a lane's k
+            const int nkt = kb_last - kb_first + 1;
+            const int ntask = M * nkt;
+            for (int tb = warp; tb < ntask; tb += TU * CW) {
+                uint4 w[TU][NV];
 #pragma unroll
-            for (int u = 0; u < TU; ++u) {
-                const int t = tb + u * CW;
-                const int m = t / nkt, ktl = t - m * nkt;
-                float gsum[NGL];
+                for (int u = 0; u < TU; ++u) {
+                    const int t = tb + u * CW;
+                    const int m = t / nkt, kt = kb_first + (t - m * nkt);   // warp-uniform
+                    const int k0 = kt * KT + lane * KL;
 #pragma unroll
-                for (int q = 0; q < NGL; ++q) gsum[q] = 0.f;
-#pragma unroll
-                for (int v = 0; v < NV; ++v) {
-                    const uint32_t wv4[4] = {w[u][v].x, w[u][v].y, w[u][v].z, w[u][v].w};
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const int q = (NGL > 1) ? (v * 8 + 2 * h) / GS : 0;
-                        gsum[q] += bf16_pair_sum(wv4[h]);
+                    for (int v = 0; v < NV; ++v) {
+                        w[u][v] = make_uint4(0u, 0u, 0u, 0u);
+                        if (t < ntask && k0 + 8 * v < a.K) w[u][v] = ldg_nc_v4(a.x + (long long)m * a.ldx + k0 + 8 * v);
                     }
                 }
-                if constexpr (GS >= KL) {
 #pragma unroll
-                    for (int o = 1; o < GS / KL; o <<= 1) gsum[0] += __shfl_xor_sync(0xffffffffu, gsum[0], o);
-                    const int gl = ktl * GPT + lane / (GS / KL);
-                    if (t < ntask && (lane & (GS / KL - 1)) == 0 && kb_first * GPT + gl < G_all) sxt[gl * 8 + m] = gsum[0];
-                } else {
+                for (int u = 0; u < TU; ++u) {
+                    const int t = tb + u * CW;
+                    const int m = t / nkt, ktl = t - m * nkt;
+                    float gsum[NGL];
 #pragma unroll
-                    for (int q = 0; q < NGL; ++q) {
-                        const int gl = ktl * GPT + lane * NGL + q;
-                        if (t < ntask && kb_first * GPT + gl < G_all) sxt[gl * 8 + m] = gsum[q];
+                    for (int q = 0; q < NGL; ++q) gsum[q] = 0.f;
+#pragma unroll
+                    for (int v = 0; v < NV; ++v) {
+                        const uint32_t wv4[4] = {w[u][v].x, w[u][v].y, w[u][v].z, w[u][v].w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const int q = (NGL > 1) ? (v * 8 + 2 * h) / GS : 0;
+                            gsum[q] += bf16_pair_sum(wv4[h]);
+                        }
+                    }
+                    if constexpr (GS >= KL) {
+#pragma unroll
+                        for (int o = 1; o < GS / KL; o <<= 1) gsum[0] += __shfl_xor_sync(0xffffffffu, gsum[0], o);
+                        const int gl = ktl * GPT + lane / (GS / KL);
+                        if (t < ntask && (lane & (GS / KL - 1)) == 0 && kb_first * GPT + gl < G_all) sxt[gl * 8 + m] = gsum[0];
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < NGL; ++q) {
+                            const int gl = ktl * GPT + lane * NGL + q;
+                            if (t < ntask && kb_first * GPT + gl < G_all) sxt[gl * 8 + m] = gsum[q];
+                        }
                     }
                 }
             }
@@ -649,6 +675,13 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
     const int mrow = g < M ? g : M - 1;          // B rows beyond M repeat a real row; their D columns are unused
     const uint16_t* xgrow = a.x + (long long)mrow * a.ldx + 4 * c;
     const uint8_t* xrow = xs + mrow * xstride + 8 * c;
+    float sxm[2] = {1.f, 1.f};                   // A8: the scales of x of columns 2c, 2c + 1
+    const int8_t* xg8row = nullptr;              // A8: this lane's x codes in global memory
+    if constexpr (A8) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) sxm[e] = 2 * c + e < M ? __ldg(a.sxq + 2 * c + e) : 0.f;
+        xg8row = a.xq + (long long)mrow * a.Kpq + 8 * c;
+    }
     // this warp's tiles: tile hh of the pairs pl = warp / 2, warp / 2 + PW, ...; pair coordinates
     // advanced by (PW / R, PW % R)
     const int hh = warp & 1;
@@ -669,8 +702,9 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
             const int gi0 = kb * GPT;
             const int ng = (G_all - gi0) < GPT ? (G_all - gi0) : GPT;   // groups of the tile inside K
             const float* sxk = sxt + (gi0 - kb_first * GPT) * 8 + 2 * c;
-            const uint8_t* xt = xrow + (size_t)(kb - kb_first) * KT * 2;
+            const uint8_t* xt = xrow + (size_t)(kb - kb_first) * KT * XBY;
             const uint16_t* xgt = xgrow + (long long)kb * KT;
+            const int8_t* xg8 = A8 ? xg8row + (long long)kb * KT : nullptr;
             const uint8_t* st = ring + (size_t)(2 * slot + hh) * TILE_BYTES;
             // the tile's metadata, addressed as if it followed the codes (row_ptrs / row_meta_k4 add
             // TILE_BYTES; the address stays inside the ring)
@@ -682,6 +716,45 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
             }
 
             auto group_step = [&](const int gg) {
+                if constexpr (A8) {
+                    // the group's exact integer sums of (stored code) x (x code) per row and column: GB / 2
+                    // instructions of m16n8k32, each over two 16-k blocks (A: the two rows' codes as bytes,
+                    // w & 0x0F0F0F0F and (w >> 4) & 0x0F0F0F0F for 4-bit; INT8 words are already bytes)
+                    int di[4] = {0, 0, 0, 0};
+#pragma unroll
+                    for (int t = 0; t < GB / 2; ++t) {
+                        const int blk = gg * GB + 2 * t;
+                        uint32_t a0, a1, a2, a3;
+                        if constexpr (FMT == UQ_INT8_SYM) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(st + (blk / BPCH) * CHUNK + lane * 16);
+                            a0 = v.x; a1 = v.y; a2 = v.z; a3 = v.w;
+                        } else {
+                            const uint2 v = *reinterpret_cast<const uint2*>(st + (blk / BPCH) * CHUNK + lane * 16 +
+                                                                            (blk % BPCH) * 4);
+                            a0 = v.x & 0x0F0F0F0Fu;                 // row g:     k, k+2, k+1, k+3
+                            a1 = (v.x >> 4) & 0x0F0F0F0Fu;          // row g + 8: the same order
+                            a2 = v.y & 0x0F0F0F0Fu;
+                            a3 = (v.y >> 4) & 0x0F0F0F0Fu;
+                        }
+                        uint2 bv;                                   // the pair's x codes of column g, in B order
+                        if constexpr (XS) bv = *reinterpret_cast<const uint2*>(xt + blk * 16);
+                        else bv = ldg_nc_v2(xg8 + blk * 16);
+                        mma_u8s8(di, a0, a1, a2, a3, bv.x, bv.y);
+                    }
+                    // fold: acc += s * (D - zc * SX), SX the group's code sum of the column, zc the stored
+                    // code's offset (8 for INT4_SYM, z for INT4_ASYM, 128 for INT8_SYM)
+                    const float2 sxv = *reinterpret_cast<const float2*>(sxk + gg * 8);
+                    const int sx0 = (int)sxv.x, sx1 = (int)sxv.y;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        float sc, zcf;
+                        row_meta<FMT>(rp[j], gg, sc, zcf);
+                        const int zc = (FMT == UQ_INT8_SYM) ? 128 : (int)zcf - 128;
+                        acc[2 * j] = fmaf(sc, (float)(di[2 * j] - zc * sx0), acc[2 * j]);
+                        acc[2 * j + 1] = fmaf(sc, (float)(di[2 * j + 1] - zc * sx1), acc[2 * j + 1]);
+                    }
+                    return;
+                }
                 // this lane's code words for the group's GB blocks
                 uint32_t wv[WPG];
                 {
@@ -830,19 +903,20 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
         if (kb < a.KB) {
             // the tile's partial sums: shared memory (cta_rows; slot = the tile's index in the CTA's
             // range) or global memory (slot = the tile's index in k-major order), summed over k later
+            // (A8: scaled by the columns' s_x)
             if (cta_rows) {
                 float* part = cpart + (2 * pl + hh) * RB * 8;
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) part[(g + 8 * j) * 8 + 2 * c + e] = acc[2 * j + e];
+                    for (int e = 0; e < 2; ++e) part[(g + 8 * j) * 8 + 2 * c + e] = A8 ? acc[2 * j + e] * sxm[e] : acc[2 * j + e];
             } else {
                 float* part = a.partials + ((long long)kb * a.NB + nbw) * RB * M;
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
 #pragma unroll
                     for (int e = 0; e < 2; ++e)
-                        if (2 * c + e < M) part[(g + 8 * j) * M + 2 * c + e] = acc[2 * j + e];
+                        if (2 * c + e < M) part[(g + 8 * j) * M + 2 * c + e] = A8 ? acc[2 * j + e] * sxm[e] : acc[2 * j + e];
             }
         }
         acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
@@ -1237,7 +1311,7 @@ __global__ void __launch_bounds__(WarpCfg<FMT>::WARPS * 32, WARP_CTAS_PER_SM) ge
 
 
 namespace gemv_detail {
-template <int FMT, int GB, int XM, bool GATED>
+template <int FMT, int GB, int XM, bool GATED, bool A8 = false>
 cudaError_t launch_mma(const GemvArgs& a, int grid, int sxg, cudaStream_t st) {
     static bool configured[64] = {};
     int dev = 0;
@@ -1245,7 +1319,7 @@ cudaError_t launch_mma(const GemvArgs& a, int grid, int sxg, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        e = cudaFuncSetAttribute(gemv_mma_kernel<FMT, GB, XM, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(gemv_mma_kernel<FMT, GB, XM, GATED, A8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  MMA_SMEM);
         if (e != cudaSuccess) return e;
         configured[dev] = true;
@@ -1253,7 +1327,7 @@ cudaError_t launch_mma(const GemvArgs& a, int grid, int sxg, cudaStream_t st) {
     const int threads = (MMA_CW + 1) * 32;
     GemvArgs a2 = a;
     a2.overlap = launch_overlap() ? 1 : 0;
-    const MmaSmem plan = gemv_mma_smem(FMT, a.K, a.group, a.M, sxg, a.cta_rows, XM);
+    const MmaSmem plan = gemv_mma_smem(FMT, a.K, a.group, a.M, sxg, a.cta_rows, XM, A8 ? 1 : 2);
     a2.ring_slots = plan.S2;
     a2.sx_groups = sxg;
     if (a2.overlap) {
@@ -1267,19 +1341,19 @@ cudaError_t launch_mma(const GemvArgs& a, int grid, int sxg, cudaStream_t st) {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, gemv_mma_kernel<FMT, GB, XM, GATED>, a2);
+        e = cudaLaunchKernelEx(&cfg, gemv_mma_kernel<FMT, GB, XM, GATED, A8>, a2);
         if (e != cudaSuccess) return e;
     } else {
-        gemv_mma_kernel<FMT, GB, XM, GATED><<<grid, threads, plan.total, st>>>(a2);
+        gemv_mma_kernel<FMT, GB, XM, GATED, A8><<<grid, threads, plan.total, st>>>(a2);
     }
     return cudaGetLastError();
 }
-template <int FMT, int GB, bool GATED>
+template <int FMT, int GB, bool GATED, bool A8 = false>
 cudaError_t launch_mma_x(const GemvArgs& a, int grid, cudaStream_t st) {
     const int sxg = gemv_mma_sx_groups(FMT, a.group, a.NB, a.KB, grid, a.cta_rows);
-    if (gemv_mma_xmode(FMT, a.K, a.group, a.M, sxg, a.cta_rows) == MMA_X_WHOLE)
-        return launch_mma<FMT, GB, MMA_X_WHOLE, GATED>(a, grid, sxg, st);
-    return launch_mma<FMT, GB, MMA_X_GLOBAL, GATED>(a, grid, sxg, st);
+    if (gemv_mma_xmode(FMT, a.K, a.group, a.M, sxg, a.cta_rows, A8 ? 1 : 2) == MMA_X_WHOLE)
+        return launch_mma<FMT, GB, MMA_X_WHOLE, GATED, A8>(a, grid, sxg, st);
+    return launch_mma<FMT, GB, MMA_X_GLOBAL, GATED, A8>(a, grid, sxg, st);
 }
 template <int FMT, int GB, bool GATED>
 cudaError_t launch_warp(const GemvArgs& a, int grid, cudaStream_t st) {

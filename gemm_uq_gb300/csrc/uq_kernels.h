@@ -63,7 +63,11 @@ struct GemvArgs {
     const uint8_t* wq2;
     const uint8_t* scales2;
     const uint8_t* zc2;
-    int a8;                   // the W4A8 GEMV (integer x codes)
+    int a8;                   // the W4A8 GEMV (integer x codes):
+    const int8_t* xq;         //   x codes [M][Kpq], each 32 k in the integer mma's B fragment order
+    const float* sxq;         //   per-row scales of x [M]
+    const int* sxl;           //   per (row, group) sums of the codes [M][ceil(Kpq / group)]
+    int Kpq;                  //   bytes per row of xq
     int ring_slots;           // mma GEMV: ring slots and x-sum table groups of the launch (set by its launcher)
     int sx_groups;
 };
@@ -111,7 +115,6 @@ int gemm_mma_splits(int NB, int UB, int sms);     // k splits per row group
 cudaError_t launch_gemm_mma(int fmt, const GemmArgs& a, int sms, cudaStream_t st);
 
 // W4A8 / W8A8 (uq_w4a8.cu): x codes and scales, then the integer GEMV
-size_t a8_smem_bytes(int fmt);
 cudaError_t launch_quant_x(const uint16_t* x, int8_t* xq, float* sx, int* sxl, int M, int K, int Kp, int gs, int perm,
                            cudaStream_t st);
 cudaError_t launch_gemv_a8(int fmt, const GemvArgs& a, const int8_t* xq, const float* sxs, const int* sxl, int Kp,
