@@ -463,7 +463,8 @@ def run_sweep(dev, stream, hbm, tf):
                         "frac": round(t_roof / (ms_ * 1e-3), 4),
                         "bound": "hbm" if st.bytes / (hbm * 1e9) >= st.flops / (tf * 1e12) else "tensor",
                         "us_per_linear": round(ms_ * 1e3 / len(recs), 2),
-                        "kernel": (f"gemv_a8_kernel<{fmt}>" if mode == "w4a8" else dominant_kernel(fmt, group, M, shapes)),
+                        "kernel": (f"gemv_mma_kernel<{fmt},GB={group // 16},A8>" if mode == "w4a8"
+                                   else dominant_kernel(fmt, group, M, shapes)),
                         "launches": st.launches(),
                         "reps": reps})
             del st
