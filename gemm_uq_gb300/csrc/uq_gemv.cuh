@@ -11,7 +11,11 @@
 //    give the A fragments, and mma.sync (bf16 x bf16 -> fp32) does the multiply-accumulate and
 //    the reduction over the 16-wide k block in one instruction; the M <= 8 activation rows are
 //    the instruction's N = 8, so every M <= 8 costs the same.  Per scaling group the fp32 group
-//    sum is folded into the row's accumulator:  y += s * (sum x*(128 + q) - (128 + z) * sum x).
+//    sum is folded as  s * (sum x*(128 + q) - (128 + z) * sum x),  in rounds of 8 groups: each
+//    pair of groups folded from zero, then  tile += (p0 + p1) + (p2 + p3).  With one row of x the
+//    round's 8 groups ride in the instruction's 8 columns instead (zeros in the B fragments of the
+//    other groups' blocks), so the fold costs a lane 2 groups instead of 8: the same operations on
+//    the same values in the same order, so a row's result is the same alone and in a batch.
 //  * Work is the list of tiles (16 rows x 8 KB of codes) in k-major order.  Either every CTA owns
 //    whole 16-row blocks (partial sums of each tile in shared memory, summed per row in k order
 //    after a CTA barrier: no second launch), or CTAs own equal contiguous ranges of all tiles
@@ -63,7 +67,7 @@ template <int FMT, int GT = 0> struct MetaGeom {
 
 // shared-memory offsets of a GEMV launch (the per-warp-ring kernels); identical on host and device
 struct GemvSmem {
-    size_t bars, lut, sx, ps, x, total;
+    size_t bars, lut, sx, ps, x, zr, total;
 };
 
 namespace {
@@ -302,7 +306,8 @@ __device__ __forceinline__ void row_meta_k4(const uint8_t* st, int r, int li, fl
 // after a shift) to form the A fragment, one 8-byte load of x and the mma.  Per group: two fp32
 // FMAs per accumulator with the group's scale and zero-point term, the latter using the group's
 // sum of x from a table the CTA forms before its first tile (8-k segments in a fixed order, then a
-// fixed shuffle tree: the same sums for every M, so a row's result does not depend on M).
+// fixed shuffle tree: the same sums for every M, so a row's result does not depend on M), in the
+// rounds of 8 groups described at the top of this file.
 //
 // Pair order is k-major: pair i of a range is (k tile pair i / R, row block i % R) for R row
 // blocks.  Every tile's partial sums are stored (shared memory when the CTA owns whole row blocks,
@@ -323,7 +328,9 @@ __host__ __device__ inline size_t gemv_mma_x_stride(int Kp, int xb = 2) { return
 // tiles its work touches: all of K when it owns whole row blocks, a few k tiles under the stream-K
 // split) copied into shared memory once per CTA; MMA_X_GLOBAL, straight from global memory (through
 // L1), when that window would leave the ring too few slots.
-constexpr int MMA_X_GLOBAL = 0, MMA_X_WHOLE = 1;
+// MMA_X_ROW1: one row of x (M = 1, not gated, not A8) in shared memory as MMA_X_WHOLE, the groups
+// of a round in the mma's columns.
+constexpr int MMA_X_GLOBAL = 0, MMA_X_WHOLE = 1, MMA_X_ROW1 = 2;
 
 // metadata bytes of one tile at this group size
 template <int FMT>
@@ -362,12 +369,15 @@ __host__ __device__ inline int gemv_mma_sx_groups(int fmt, int group, int NB, in
 
 // Shared memory: codes [S2][2][8 KB] | metadata [S2][2][meta] | full[S2], empty[S2] and x
 // mbarriers, NF4's table | sums of x [groups][8] | partial sums [tiles of the CTA][16][8] (whole row blocks) |
-// x (MMA_X_WHOLE).  S2 = the slots that fit beside the rest (at most MMA_PMAX).  Identical on
+// x (MMA_X_WHOLE) | zeros (MMA_X_WHOLE, one row of x).  S2 = the slots that fit beside the rest (at most MMA_PMAX).  Identical on
 // host and device.
 struct MmaSmem {
-    size_t meta, bars, sx, ps, x, total;
+    size_t meta, bars, sx, ps, x, zr, total;
     int S2, mb;                                     // slots, metadata bytes per tile
 };
+// one row of x in shared memory also takes 256 bytes of zeros (B fragments of the other groups'
+// columns), 32 bytes past a 128-byte boundary so a load's x lanes and zero lanes hit different banks
+__host__ __device__ inline bool gemv_mma_colmode(int M, int xm) { return M == 1 && xm == MMA_X_ROW1; }
 // offsets for S2 slots (multiplications and additions only: the kernel forms them per launch)
 __host__ __device__ inline MmaSmem gemv_mma_offsets(int S2, int mb, int sxg, int tpc, int M, int xk, int xm, int xb = 2) {
     MmaSmem p;
@@ -378,7 +388,12 @@ __host__ __device__ inline MmaSmem gemv_mma_offsets(int S2, int mb, int sxg, int
     p.sx = (p.bars + (size_t)MMA_BAR_BYTES + 15) / 16 * 16;
     p.ps = p.sx + (size_t)sxg * 8 * 4;
     p.x = (p.ps + (size_t)tpc * RB * 8 * 4 + 127) / 128 * 128;
-    p.total = p.x + (xm == MMA_X_WHOLE ? (size_t)M * gemv_mma_x_stride(xk, xb) : 0);
+    p.total = p.x + (xm != MMA_X_GLOBAL ? (size_t)M * gemv_mma_x_stride(xk, xb) : 0);
+    p.zr = 0;
+    if (gemv_mma_colmode(M, xm)) {
+        p.zr = (p.total + 127) / 128 * 128 + 32;
+        p.total = p.zr + 256;
+    }
     return p;
 }
 __host__ __device__ inline MmaSmem gemv_mma_smem(int fmt, int K, int group, int M, int sxg, int tpc, int xm, int xb = 2) {
@@ -388,7 +403,8 @@ __host__ __device__ inline MmaSmem gemv_mma_smem(int fmt, int K, int group, int 
     const int xk = sxg / gpt * fmt_kt(fmt);                         // k extent of a CTA's window of x
     (void)K;
     const size_t bars = (size_t)MMA_BAR_BYTES;
-    const size_t xbytes = xm == MMA_X_WHOLE ? (size_t)M * gemv_mma_x_stride(xk, xb) : 0;
+    const size_t xbytes = (xm != MMA_X_GLOBAL ? (size_t)M * gemv_mma_x_stride(xk, xb) : 0) +
+                          (gemv_mma_colmode(M, xm) ? 127 + 32 + 256 : 0);
     const size_t rest = bars + 16 + (size_t)sxg * 8 * 4 + (size_t)tpc * RB * 8 * 4 + 128 + xbytes;   // + alignment
     long long S2 = ((long long)MMA_SMEM - (long long)rest) / slot;
     if (S2 > MMA_PMAX) S2 = MMA_PMAX;
@@ -397,8 +413,13 @@ __host__ __device__ inline MmaSmem gemv_mma_smem(int fmt, int K, int group, int 
 }
 // x in shared memory when that leaves the ring 2 slots beyond those the compute warps hold
 // (measured: 8 rows of x through L1 cost more than a shallower ring)
-__host__ __device__ inline int gemv_mma_xmode(int fmt, int K, int group, int M, int sxg, int tpc, int xb = 2) {
-    return gemv_mma_smem(fmt, K, group, M, sxg, tpc, MMA_X_WHOLE, xb).S2 >= MMA_CW / 2 + 2 ? MMA_X_WHOLE : MMA_X_GLOBAL;
+// (row1: MMA_X_ROW1 allowed, for one row of x when it fits as well)
+__host__ __device__ inline int gemv_mma_xmode(int fmt, int K, int group, int M, int sxg, int tpc, int xb = 2,
+                                              bool row1 = false) {
+    if (gemv_mma_smem(fmt, K, group, M, sxg, tpc, MMA_X_WHOLE, xb).S2 < MMA_CW / 2 + 2) return MMA_X_GLOBAL;
+    if (row1 && M == 1 && gemv_mma_smem(fmt, K, group, M, sxg, tpc, MMA_X_ROW1, xb).S2 >= MMA_CW / 2 + 2)
+        return MMA_X_ROW1;
+    return MMA_X_WHOLE;
 }
 
 __device__ __forceinline__ float bf16_pair_sum(uint32_t w) {
@@ -429,7 +450,9 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
     constexpr int WPG = (FMT == UQ_INT2_ASYM) ? GB / 2 : (FMT == UQ_INT8_SYM ? 2 * GB : GB);   // code words per lane per group
     constexpr int BPCH = F::BPC;                                    // 16-k blocks per 512-byte chunk
     constexpr int SPG = GS / 8;                                     // 8-k segments of x per group
-    constexpr bool XS = XM == MMA_X_WHOLE;
+    constexpr bool XS = XM != MMA_X_GLOBAL;                        // x in shared memory
+    constexpr bool COL = XM == MMA_X_ROW1;                          // one row of x, groups as columns
+    static_assert(!COL || (!A8 && !GATED), "the column scheme takes one plain row of x");
     extern __shared__ __align__(128) uint8_t smem[];
     const int M = a.M;
     const int tpc = a.cta_rows;                                     // > 0: CTAs own whole row blocks
@@ -451,6 +474,9 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
+    // COL: the groups of a round of 8 ride in the mma's columns (gemv_warp_kernel's scheme), and the
+    // scales fold once per group and row instead of once per group, row and lane
+    const uint8_t* xz = smem + plan.zr + 8 * c;                     // zeros (COL)
 
     // Work split over pairs of k tiles (KB2 per row block; when KB is odd the last pair holds one
     // tile): whole row blocks [rb0, rb0 + R) per CTA (gated: gate / up pairs), or the stream-K range
@@ -482,7 +508,8 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
     int kb_last = npl > 0 ? 2 * (int)((p0 + npl - 1) / (unsigned)R) + 1 : -1;
     if (kb_last > a.KB - 1) kb_last = a.KB - 1;
     const int nsx = (kb_last - kb_first + 1) * GPT;                 // table groups this CTA uses
-    const bool bad = (cta_rows && 2 * (int)npl > tpc) || nsx > sxg || S2 <= PW || R <= 0;   // never planned
+    const bool bad = (cta_rows && 2 * (int)npl > tpc) || nsx > sxg || S2 <= PW || R <= 0 ||
+                     (COL && M != 1);                               // never planned
     if (bad) {
         if (threadIdx.x == 0) atomicOr(a.fault, FAULT_GEMV_SPLIT);
         return;
@@ -655,6 +682,7 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
         }
         for (int e = threadIdx.x; e < nsx * 8; e += CW * 32)
             if ((e & 7) >= M) sxt[e] = 0.f;
+        if (COL && threadIdx.x < 64) reinterpret_cast<uint32_t*>(smem + plan.zr)[threadIdx.x] = 0u;
     }
     if constexpr (FMT == UQ_NF4) {
         // the codebook value c[q] as hi = bf16(c[q]) and lo = bf16(c[q] - hi): hi + lo carries 16
@@ -701,7 +729,8 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
             const int n0 = nb * RB;
             const int gi0 = kb * GPT;
             const int ng = (G_all - gi0) < GPT ? (G_all - gi0) : GPT;   // groups of the tile inside K
-            const float* sxk = sxt + (gi0 - kb_first * GPT) * 8 + 2 * c;
+            const float* sxc = sxt + (gi0 - kb_first * GPT) * 8;      // the tile's groups, column 0
+            const float* sxk = sxc + 2 * c;
             const uint8_t* xt = xrow + (size_t)(kb - kb_first) * KT * XBY;
             const uint16_t* xgt = xgrow + (long long)kb * KT;
             const int8_t* xg8 = A8 ? xg8row + (long long)kb * KT : nullptr;
@@ -715,7 +744,8 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
                 rp[1] = row_ptrs<FMT, GPT>(sm, mc, g + 8, n0 + g + 8, kb);
             }
 
-            auto group_step = [&](const int gg) {
+            // A8: one group's exact integer products, folded into p (= acc)
+            auto group_a8 = [&](const int gg, float (&p)[4]) {
                 if constexpr (A8) {
                     // the group's exact integer sums of (stored code) x (x code) per row and column: GB / 2
                     // instructions of m16n8k32, each over two 16-k blocks (A: the two rows' codes as bytes,
@@ -750,11 +780,14 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
                         float sc, zcf;
                         row_meta<FMT>(rp[j], gg, sc, zcf);
                         const int zc = (FMT == UQ_INT8_SYM) ? 128 : (int)zcf - 128;
-                        acc[2 * j] = fmaf(sc, (float)(di[2 * j] - zc * sx0), acc[2 * j]);
-                        acc[2 * j + 1] = fmaf(sc, (float)(di[2 * j + 1] - zc * sx1), acc[2 * j + 1]);
+                        p[2 * j] = fmaf(sc, (float)(di[2 * j] - zc * sx0), p[2 * j]);
+                        p[2 * j + 1] = fmaf(sc, (float)(di[2 * j + 1] - zc * sx1), p[2 * j + 1]);
                     }
                     return;
                 }
+            };
+            // one group's products into the chains dd
+            auto group_mma = [&](const int gg, float (&dd)[2][4], const bool first, const bool col) {
                 // this lane's code words for the group's GB blocks
                 uint32_t wv[WPG];
                 {
@@ -782,12 +815,15 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
                     }
                 }
                 // B fragments: x at k = 16 blk + 4c .. +3 of row mrow (8 bytes per block); every block
-                // of a group inside K lies inside K (K is a multiple of the group)
+                // of a group inside K lies inside K (K is a multiple of the group).  `col`: one row of
+                // x, column g carrying group 8r + g of the round (zeros for the other groups' blocks)
                 uint32_t bx[GB], by[GB];
+                const uint8_t* xg = xt + gg * GB * 32;
+                if (col && g != (gg & 7)) xg = xz;
 #pragma unroll
                 for (int j = 0; j < GB; ++j) {
                     uint2 v;
-                    if constexpr (XS) v = *reinterpret_cast<const uint2*>(xt + (gg * GB + j) * 32);
+                    if constexpr (XS) v = *reinterpret_cast<const uint2*>(xg + j * 32);
                     else v = ldg_nc_v2(xgt + (gg * GB + j) * 16);
                     if constexpr (FMT == UQ_INT8_SYM) {
                         // an INT8 word holds k 4c .. 4c + 3 of one row and its nibble pairs come out as
@@ -800,8 +836,8 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
                 }
                 // the group's sum of (128 + q) x, in two chains (even / odd blocks); INT8: the sums
                 // over the stored bytes' high and low nibbles, (128 + hi) x and (128 + lo) x; NF4: the
-                // sums over the codebook values' hi and lo parts (no offset: zc = 0)
-                float dd[2][4];
+                // sums over the codebook values' hi and lo parts (no offset: zc = 0).  The chains start
+                // from zero at the group (or round) when `first`.
 #pragma unroll
                 for (int j = 0; j < GB; ++j) {
                     uint32_t a0, a1, a2, a3;
@@ -812,7 +848,7 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
                         const uint32_t h2 = nib_pair_lop3<3>(wg), h3 = nib_pair_lop3<3>(wg8);
                         a0 = nib_pair_lop3<0>(wg); a1 = nib_pair_lop3<0>(wg8);
                         a2 = nib_pair_lop3<2>(wg); a3 = nib_pair_lop3<2>(wg8);
-                        if (j == 0) {
+                        if (first && j == 0) {
                             mma_bf16_zero(dd[0], a0, a1, a2, a3, bx[j], by[j]);
                             mma_bf16_zero(dd[1], h0, h1, h2, h3, bx[j], by[j]);
                         } else {
@@ -831,7 +867,7 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
                             hi[P] = __byte_perm(e, o, 0x5410);
                             lo[P] = __byte_perm(e, o, 0x7632);
                         }
-                        if (j == 0) {
+                        if (first && j == 0) {
                             mma_bf16_zero(dd[0], hi[0], hi[1], hi[2], hi[3], bx[j], by[j]);
                             mma_bf16_zero(dd[1], lo[0], lo[1], lo[2], lo[3], bx[j], by[j]);
                         } else {
@@ -854,10 +890,13 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
                         a0 = nib_pair_lop3<0>(wd); a1 = nib_pair_lop3<1>(wd);
                         a2 = nib_pair_lop3<2>(wd); a3 = nib_pair_lop3<3>(wd);
                     }
-                    if (j < 2) mma_bf16_zero(dd[j & 1], a0, a1, a2, a3, bx[j], by[j]);
+                    if (first && j < 2) mma_bf16_zero(dd[j & 1], a0, a1, a2, a3, bx[j], by[j]);
                     else mma_bf16(dd[j & 1], a0, a1, a2, a3, bx[j], by[j]);
                 }
-                // fold the group into the row sums, with the group's sums of x from the table
+            };
+            // p += the group's term from its chains: s * (D - zc * sum x) (K4: d sc D - (128 d sc +
+            // dmin m) sum x), with the group's sums of x from the table
+            auto fold = [&](const int gg, const float (&dd)[2][4], float (&p)[4]) {
                 const float2 sxv = *reinterpret_cast<const float2*>(sxk + gg * 8);
                 float d[4];
 #pragma unroll
@@ -873,27 +912,128 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
                         float dsc, dmm;
                         row_meta_k4(sm, g + 8 * j, gg, dsc, dmm);
                         const float off = fmaf(128.0f, dsc, dmm);
-                        acc[2 * j] = fmaf(dsc, d[2 * j], fmaf(-off, sxv.x, acc[2 * j]));
-                        acc[2 * j + 1] = fmaf(dsc, d[2 * j + 1], fmaf(-off, sxv.y, acc[2 * j + 1]));
+                        p[2 * j] = fmaf(dsc, d[2 * j], fmaf(-off, sxv.x, p[2 * j]));
+                        p[2 * j + 1] = fmaf(dsc, d[2 * j + 1], fmaf(-off, sxv.y, p[2 * j + 1]));
                     } else {
                         float sc, zc;
                         row_meta<FMT>(rp[j], gg, sc, zc);
                         if constexpr (FMT == UQ_INT8_SYM) zc = 2304.0f;
                         const float szc = sc * zc;
-                        acc[2 * j] = fmaf(sc, d[2 * j], fmaf(-szc, sxv.x, acc[2 * j]));
-                        acc[2 * j + 1] = fmaf(sc, d[2 * j + 1], fmaf(-szc, sxv.y, acc[2 * j + 1]));
+                        p[2 * j] = fmaf(sc, d[2 * j], fmaf(-szc, sxv.x, p[2 * j]));
+                        p[2 * j + 1] = fmaf(sc, d[2 * j + 1], fmaf(-szc, sxv.y, p[2 * j + 1]));
                     }
                 }
             };
-            if (ng == GPT) {
-                // 8 groups per step for 32-k groups: a K4 record (8 sub-blocks) is then read and
-                // decoded once per row per step, its 6-bit fields at constant shifts
-                constexpr int GUNROLL = (GB == 2) ? 8 : 4;
+            // one group, folded into p (p = acc for A8; a pair's sum from zero otherwise)
+            auto group_step = [&](const int gg, float (&p)[4]) {
+                if constexpr (A8) {
+                    group_a8(gg, p);
+                } else {
+                    float dd[2][4];
+                    group_mma(gg, dd, true, false);
+                    fold(gg, dd, p);
+                }
+            };
+            if constexpr (A8) {
+                if (ng == GPT) {
+                    constexpr int GUNROLL = (GB == 2) ? 8 : 4;
 #pragma unroll GUNROLL
-                for (int gg = 0; gg < GPT; ++gg) group_step(gg);
-            } else {
+                    for (int gg = 0; gg < GPT; ++gg) group_step(gg, acc);
+                } else {
 #pragma unroll 1
-                for (int gg = 0; gg < ng; ++gg) group_step(gg);
+                    for (int gg = 0; gg < ng; ++gg) group_step(gg, acc);
+                }
+            } else {
+                // The tile's sum in rounds of 8 groups (the order gemv_warp_kernel's columns give):
+                // each pair of groups folded from zero, p_q for groups 8r + 2q, 8r + 2q + 1, then
+                // acc += (p_0 + p_1) + (p_2 + p_3).  `full`: a whole tile, whose groups all lie inside K.
+                auto pair_step = [&](const int r, const int q, const bool full, float (&p)[4]) {
+                    p[0] = p[1] = p[2] = p[3] = 0.f;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int gg = 8 * r + 2 * q + h;
+                        if (full ? (GPT >= 8 || 2 * q + h < GPT) : gg < ng) group_step(gg, p);
+                    }
+                };
+                auto round_step = [&](const int r, const bool full) {
+                    float s01[4], sh[4], p[4];
+                    // halves of the round (pairs 0, 1 then 2, 3): 4 groups per iteration (8 for
+                    // 32-k groups), as deep as the compute warps' registers allow
+                    constexpr int HUNROLL = (GB == 2) ? 2 : 1;
+#pragma unroll HUNROLL
+                    for (int hf = 0; hf < 2; ++hf) {
+                        pair_step(r, 2 * hf, full, sh);
+                        pair_step(r, 2 * hf + 1, full, p);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            sh[e] += p[e];
+                            if (hf == 0) s01[e] = sh[e];
+                            else acc[e] += s01[e] + sh[e];
+                        }
+                    }
+                };
+                // One row of x: round r's groups in the mma's columns (chains over the whole round;
+                // blocks of other groups add exact zeros to a column), then lane (g, c) folds groups
+                // 8r + 2c, 8r + 2c + 1 of rows g, g + 8 from zero and two shuffles add the four lanes'
+                // pairs: the same operations on the same values as round_step, in the same order.
+                auto round_col = [&](const int r, const bool full) {
+                    float dd[2][4];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int gg = 8 * r + q;
+                        if (full ? (GPT >= 8 || q < GPT) : gg < ng) group_mma(gg, dd, q == 0, true);
+                    }
+                    float d[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if constexpr (FMT == UQ_INT8_SYM) d[e] = fmaf(16.0f, dd[1][e], dd[0][e]);
+                        else d[e] = dd[0][e] + dd[1][e];
+                    }
+                    float p[2] = {0.f, 0.f};
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int gg = 8 * r + 2 * c + e;
+                        if (!(full ? (GPT >= 8 || 2 * c + e < GPT) : gg < ng)) continue;
+                        const float sx = sxc[gg * 8];
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            if constexpr (FMT == UQ_K4) {
+                                float dsc, dmm;
+                                row_meta_k4(sm, g + 8 * j, gg, dsc, dmm);
+                                const float off = fmaf(128.0f, dsc, dmm);
+                                p[j] = fmaf(dsc, d[2 * j + e], fmaf(-off, sx, p[j]));
+                            } else {
+                                float sc, zc;
+                                row_meta<FMT>(rp[j], gg, sc, zc);
+                                if constexpr (FMT == UQ_INT8_SYM) zc = 2304.0f;
+                                const float szc = sc * zc;
+                                p[j] = fmaf(sc, d[2 * j + e], fmaf(-szc, sx, p[j]));
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const float s2 = p[j] + __shfl_xor_sync(0xffffffffu, p[j], 1);
+                        acc[2 * j] += s2 + __shfl_xor_sync(0xffffffffu, s2, 2);
+                    }
+                };
+                // (8 groups per round: a K4 record, 8 sub-blocks, is read and decoded once per row per
+                // round, its 6-bit fields at constant shifts)
+                if constexpr (COL) {
+                    if (ng == GPT) {
+#pragma unroll 1
+                        for (int r = 0; r < (GPT + 7) / 8; ++r) round_col(r, true);
+                    } else {
+#pragma unroll 1
+                        for (int r = 0; 8 * r < ng; ++r) round_col(r, false);
+                    }
+                } else if (ng == GPT) {
+#pragma unroll 1
+                    for (int r = 0; r < (GPT + 7) / 8; ++r) round_step(r, true);
+                } else {
+#pragma unroll 1
+                    for (int r = 0; 8 * r < ng; ++r) round_step(r, false);
+                }
             }
         }
         __syncwarp();
@@ -972,7 +1112,8 @@ __host__ __device__ inline int gemv_warp_xslice_stride(int fmt, int M) {
 
 // Shared memory: rings [warps][stages][stage] | ring and x-slice mbarriers | sums of x [warps][groups
 // of a tile][8] | partial sums [tiles of the CTA, at most warps x WARP_TPW][16][8] | x slices
-// [warps][2][M]
+// [warps][2][M] | zeros [warps][320 bytes: 256 from byte 32] (the B fragments of the other groups'
+// columns; 32 bytes off the x slices' alignment, so a load's x and zero lanes hit different banks)
 __host__ __device__ inline GemvSmem gemv_warp_smem(int fmt, int group, int M) {
     int stage = 0, warps = 0;
     const int kt = fmt_kt(fmt);
@@ -987,7 +1128,8 @@ __host__ __device__ inline GemvSmem gemv_warp_smem(int fmt, int group, int M) {
     p.sx = (p.lut + 15) / 16 * 16;
     p.ps = p.sx + (size_t)warps * (kt / group) * 8 * 4;
     p.x = (p.ps + (size_t)warps * WARP_TPW * RB * 8 * 4 + 127) / 128 * 128;
-    p.total = p.x + (size_t)warps * 2 * M * gemv_warp_xslice_stride(fmt, M);
+    p.zr = p.x + (size_t)warps * 2 * M * gemv_warp_xslice_stride(fmt, M);
+    p.total = p.zr + (size_t)warps * 320;
     return p;
 }
 // within the shared memory that keeps WARP_CTAS_PER_SM CTAs on an SM
@@ -1005,13 +1147,19 @@ __host__ __device__ inline bool gemv_warp_route(int fmt, int M) {
 template <int FMT, int GB, bool GATED>
 __global__ void __launch_bounds__(WarpCfg<FMT>::WARPS * 32, WARP_CTAS_PER_SM) gemv_warp_kernel(const GemvArgs a) {
     using F = GemvFmt<FMT>;
+    static_assert(FMT == UQ_INT4_SYM || FMT == UQ_INT4_ASYM, "one row of x on the 4-bit flat formats");
     constexpr int KT = F::KT, S = WarpCfg<FMT>::STAGES, W = WarpCfg<FMT>::WARPS;
     constexpr int GS = GB * 16;                                     // k per scaling group
-    constexpr int GPT = KT / GS;                                    // groups per full tile row
-    constexpr int WPG = (FMT == UQ_INT2_ASYM) ? GB / 2 : GB;        // code words per lane per group
+    constexpr int GPT = KT / GS;                                    // groups per full tile row (8, 16, 32)
+    static_assert(GPT % 8 == 0, "rounds of 8 groups");
+    constexpr int WPG = GB;                                         // code words per lane per group
     constexpr int BPCH = F::BPC;                                    // 16-k blocks per 512-byte chunk
     extern __shared__ __align__(128) uint8_t smem[];
     const int M = a.M;
+    if (M != 1) {                                                   // the host routes one row of x here only
+        if (threadIdx.x == 0) atomicOr(a.fault, FAULT_GEMV_SPLIT);
+        return;
+    }
     const GemvSmem plan = gemv_warp_smem(FMT, a.group, M);
     const int XB = gemv_warp_xslice_stride(FMT, M);                 // x slice: bytes per row
     uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + plan.bars);
@@ -1026,6 +1174,8 @@ __global__ void __launch_bounds__(WarpCfg<FMT>::WARPS * 32, WARP_CTAS_PER_SM) ge
     uint64_t* xsl_bar = bars_all + W * S + 2 * warp;               // this warp's two x-slice buffers
     float* sxw = reinterpret_cast<float*>(smem + plan.sx) + warp * GPT * 8;   // sums of x of the run's k tile
     uint8_t* xsl = xs + (size_t)warp * 2 * M * XB;                  // this warp's x-slice buffers
+    uint8_t* zrw = smem + plan.zr + warp * 320 + 32;                // this warp's 256 bytes of zeros
+    const uint8_t* xz = zrw + 8 * c;
 
     // Work split.  cta_rows: CTA b owns row blocks [rb0, rb1), R of them, and its W warps split the
     // R * KB tiles evenly; otherwise worker w = CTA + grid * warp (strided, so a small matrix still
@@ -1078,6 +1228,8 @@ __global__ void __launch_bounds__(WarpCfg<FMT>::WARPS * 32, WARP_CTAS_PER_SM) ge
         mbar_init(&xsl_bar[1], 1);
         fence_barrier_init();
     }
+    reinterpret_cast<uint32_t*>(zrw)[lane] = 0u;
+    reinterpret_cast<uint32_t*>(zrw)[lane + 32] = 0u;
     __syncwarp();
     int issued = 0;                                                 // tiles requested so far
     // the weight and weight row block of a work row block
@@ -1106,8 +1258,6 @@ __global__ void __launch_bounds__(WarpCfg<FMT>::WARPS * 32, WARP_CTAS_PER_SM) ge
     if (has_work && issued == 0 && ntl > 0) issue_next();
     if (!has_work) return;                          // (never in cta_rows mode: every warp meets the end barrier)
 
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};        // rows g + 8j, columns 2c + e
-    const int mrow = g < M ? g : M - 1;          // B rows beyond M repeat a real row; their D columns are unused
     int cur_kb = -1, run = -1;
     const uint8_t* xt = nullptr;                 // this lane's x at the current k tile's first k
 
@@ -1132,7 +1282,7 @@ __global__ void __launch_bounds__(WarpCfg<FMT>::WARPS * 32, WARP_CTAS_PER_SM) ge
                     if (lane == 0) issue_xslice(kb + 1, slot ^ 1);
                     ++xissued;
                 }
-                xt = xsl + (slot * M + mrow) * XB + 8 * c;
+                xt = xsl + slot * XB + 8 * c;                       // (one row of x)
             }
             __syncwarp();                                           // the previous run's sums are read
             {
@@ -1178,111 +1328,98 @@ __global__ void __launch_bounds__(WarpCfg<FMT>::WARPS * 32, WARP_CTAS_PER_SM) ge
         else cp_async_wait_group<0>();
         __syncwarp();
         RowPtrs<FMT> rp[2];
-        if constexpr (FMT != UQ_K4) {
-            rp[0] = row_ptrs<FMT>(st, mc, g, n0 + g, kb);
-            rp[1] = row_ptrs<FMT>(st, mc, g + 8, n0 + g + 8, kb);
-        }
+        rp[0] = row_ptrs<FMT>(st, mc, g, n0 + g, kb);
+        rp[1] = row_ptrs<FMT>(st, mc, g + 8, n0 + g + 8, kb);
 
-        auto group_step = [&](const int gg) {
-            // this lane's code words for the group's GB blocks
-            uint32_t wv[WPG];
-            {
+        // Round r: groups 8r .. 8r + 7 of the tile, one per column of the mma.  Lane group g feeds x
+        // of group 8r + g as its B column and zeros for the other groups' blocks, so column i of D
+        // is the sum over group 8r + i of (128 + q) x; blocks of other groups add exact zeros to it,
+        // and two chains (even / odd blocks) sum it as gemv_mma_kernel does per group.  Lane (g, c)
+        // folds groups 8r + 2c and 8r + 2c + 1 of rows g, g + 8 from zero, and two shuffles add the
+        // four lanes' pairs: acc += (p_0 + p_1) + (p_2 + p_3), gemv_mma_kernel's order, so a row's
+        // result is the same as in a batch.  The scales and zero points are read once per group and
+        // row instead of once per group, row and lane.  `full`: a whole tile (all groups inside K).
+        float acc[2] = {0.f, 0.f};                  // rows g, g + 8 (the one column of y)
+        auto round_step = [&](const int r, const bool full) {
+            float dd[2][4];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int gg = 8 * r + q;
+                if (!full && gg >= ng) continue;
+                // this lane's code words for the group's GB blocks
+                uint32_t wv[GB];
                 const int blk = gg * GB;                            // first block of the group in the tile
                 const uint8_t* cp = st + (blk / BPCH) * CHUNK + lane * 16 + ((blk % BPCH) * WPG / GB) * 4;
-                if constexpr (WPG == 4) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(cp);
-                    wv[0] = v.x; wv[1] = v.y; wv[2] = v.z; wv[3] = v.w;
-                } else if constexpr (WPG == 8) {
+                if constexpr (GB == 8) {
                     const uint4 v0 = *reinterpret_cast<const uint4*>(cp);
                     const uint4 v1 = *reinterpret_cast<const uint4*>(cp + CHUNK);
                     wv[0] = v0.x; wv[1] = v0.y; wv[2] = v0.z; wv[3] = v0.w;
                     wv[4] = v1.x; wv[5] = v1.y; wv[6] = v1.z; wv[7] = v1.w;
-                } else if constexpr (WPG == 2) {
+                } else if constexpr (GB == 4) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(cp);
+                    wv[0] = v.x; wv[1] = v.y; wv[2] = v.z; wv[3] = v.w;
+                } else {
                     const uint2 v = *reinterpret_cast<const uint2*>(cp);
                     wv[0] = v.x; wv[1] = v.y;
-                } else {
-                    wv[0] = *reinterpret_cast<const uint32_t*>(cp);
                 }
-            }
-            // B fragments: x at k = 16 blk + 4c .. +3 of row mrow (8 bytes per block)
-            uint32_t bx[GB], by[GB];
+                // B fragments: x at k = 16 blk + 4c .. +3 for the group's own column, else zeros
+                const uint8_t* xb = (g == q) ? xt + blk * 32 : xz;
 #pragma unroll
-            for (int j = 0; j < GB; ++j) {
-                const uint2 v = *reinterpret_cast<const uint2*>(xt + (gg * GB + j) * 32);
-                bx[j] = v.x; by[j] = v.y;
-            }
-            // the group's sum of (128 + q) x, in two chains (even / odd blocks)
-            float dd[2][4];
-#pragma unroll
-            for (int j = 0; j < GB; ++j) {
-                uint32_t a0, a1, a2, a3;
-                if constexpr (FMT == UQ_INT2_ASYM) {
-                    const uint32_t wd = wv[j >> 1];
-                    if (j & 1) {
-                        a0 = crumb_pair_lop3<4>(wd); a1 = crumb_pair_lop3<5>(wd);
-                        a2 = crumb_pair_lop3<6>(wd); a3 = crumb_pair_lop3<7>(wd);
-                    } else {
-                        a0 = crumb_pair_lop3<0>(wd); a1 = crumb_pair_lop3<1>(wd);
-                        a2 = crumb_pair_lop3<2>(wd); a3 = crumb_pair_lop3<3>(wd);
-                    }
-                } else {
+                for (int j = 0; j < GB; ++j) {
+                    const uint2 v = *reinterpret_cast<const uint2*>(xb + j * 32);
                     const uint32_t wd = wv[j];
-                    a0 = nib_pair_lop3<0>(wd); a1 = nib_pair_lop3<1>(wd);
-                    a2 = nib_pair_lop3<2>(wd); a3 = nib_pair_lop3<3>(wd);
+                    const uint32_t a0 = nib_pair_lop3<0>(wd), a1 = nib_pair_lop3<1>(wd);
+                    const uint32_t a2 = nib_pair_lop3<2>(wd), a3 = nib_pair_lop3<3>(wd);
+                    if (q == 0 && j < 2) mma_bf16_zero(dd[j & 1], a0, a1, a2, a3, v.x, v.y);
+                    else mma_bf16(dd[j & 1], a0, a1, a2, a3, v.x, v.y);
                 }
-                if (j < 2) mma_bf16_zero(dd[j & 1], a0, a1, a2, a3, bx[j], by[j]);
-                else mma_bf16(dd[j & 1], a0, a1, a2, a3, bx[j], by[j]);
             }
-            // fold the group into the row sums, with the run's sums of x over the group
-            const float2 sxv = *reinterpret_cast<const float2*>(sxw + gg * 8 + 2 * c);
+            // lane (g, c) holds rows g, g + 8 of columns 2c, 2c + 1: groups 8r + 2c, 8r + 2c + 1
             float d[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) d[e] = dd[0][e] + dd[1][e];
+            float p[2] = {0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                if constexpr (FMT == UQ_K4) {
-                    float dsc, dmm;
-                    row_meta_k4(st, g + 8 * j, gg, dsc, dmm);
-                    const float off = fmaf(128.0f, dsc, dmm);
-                    acc[2 * j] = fmaf(dsc, d[2 * j], fmaf(-off, sxv.x, acc[2 * j]));
-                    acc[2 * j + 1] = fmaf(dsc, d[2 * j + 1], fmaf(-off, sxv.y, acc[2 * j + 1]));
-                } else {
+            for (int e = 0; e < 2; ++e) {
+                const int gg = 8 * r + 2 * c + e;
+                if (!full && gg >= ng) continue;
+                const float sx = sxw[gg * 8];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
                     float sc, zc;
                     row_meta<FMT>(rp[j], gg, sc, zc);
                     const float szc = sc * zc;
-                    acc[2 * j] = fmaf(sc, d[2 * j], fmaf(-szc, sxv.x, acc[2 * j]));
-                    acc[2 * j + 1] = fmaf(sc, d[2 * j + 1], fmaf(-szc, sxv.y, acc[2 * j + 1]));
+                    p[j] = fmaf(sc, d[2 * j + e], fmaf(-szc, sx, p[j]));
                 }
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float s2 = p[j] + __shfl_xor_sync(0xffffffffu, p[j], 1);
+                acc[j] += s2 + __shfl_xor_sync(0xffffffffu, s2, 2);
             }
         };
         if (ng == GPT) {
-            // 8 groups per step for 32-k groups: a K4 record (8 sub-blocks) is then read and
-            // decoded once per row per step, its 6-bit fields at constant shifts
-            constexpr int GUNROLL = (GB == 2) ? 8 : 4;
-#pragma unroll GUNROLL
-            for (int gg = 0; gg < GPT; ++gg) group_step(gg);
+#pragma unroll
+            for (int r = 0; r < GPT / 8; ++r) round_step(r, true);
         } else {
 #pragma unroll 1
-            for (int gg = 0; gg < ng; ++gg) group_step(gg);
+            for (int r = 0; 8 * r < ng; ++r) round_step(r, false);
         }
         __syncwarp();
 
-        // the tile's partial sums: shared memory (cta_rows) or global memory, summed over k tiles later
-        if (cta_rows) {
-            float* part = cpart + (i * RB) * 8;                     // slot = the tile's index in the CTA's range
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) part[(g + 8 * j) * 8 + 2 * c + e] = acc[2 * j + e];
-        } else {
-            float* part = a.partials + i * RB * M;
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int e = 0; e < 2; ++e)
-                    if (2 * c + e < M) part[(g + 8 * j) * M + 2 * c + e] = acc[2 * j + e];
+        // the tile's partial sums (every lane holds them; lanes c = 0 store): shared memory
+        // (cta_rows) or global memory, summed over k tiles later
+        if (c == 0) {
+            if (cta_rows) {
+                float* part = cpart + (i * RB) * 8;                 // slot = the tile's index in the CTA's range
+                part[g * 8] = acc[0];
+                part[(g + 8) * 8] = acc[1];
+            } else {
+                float* part = a.partials + i * RB;                  // (one row of x)
+                part[g] = acc[0];
+                part[g + 8] = acc[1];
+            }
         }
-        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
     }
     // a wait that timed out (fault flag set) left copies in flight: let them land before leaving
     cp_async_wait_group<0>();
@@ -1351,8 +1488,10 @@ cudaError_t launch_mma(const GemvArgs& a, int grid, int sxg, cudaStream_t st) {
 template <int FMT, int GB, bool GATED, bool A8 = false>
 cudaError_t launch_mma_x(const GemvArgs& a, int grid, cudaStream_t st) {
     const int sxg = gemv_mma_sx_groups(FMT, a.group, a.NB, a.KB, grid, a.cta_rows);
-    if (gemv_mma_xmode(FMT, a.K, a.group, a.M, sxg, a.cta_rows, A8 ? 1 : 2) == MMA_X_WHOLE)
-        return launch_mma<FMT, GB, MMA_X_WHOLE, GATED, A8>(a, grid, sxg, st);
+    const int xm = gemv_mma_xmode(FMT, a.K, a.group, a.M, sxg, a.cta_rows, A8 ? 1 : 2, !A8 && !GATED);
+    if constexpr (!A8 && !GATED)
+        if (xm == MMA_X_ROW1) return launch_mma<FMT, GB, MMA_X_ROW1, GATED, A8>(a, grid, sxg, st);
+    if (xm == MMA_X_WHOLE) return launch_mma<FMT, GB, MMA_X_WHOLE, GATED, A8>(a, grid, sxg, st);
     return launch_mma<FMT, GB, MMA_X_GLOBAL, GATED, A8>(a, grid, sxg, st);
 }
 template <int FMT, int GB, bool GATED>
