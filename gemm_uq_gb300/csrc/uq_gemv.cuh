@@ -227,8 +227,14 @@ __device__ __forceinline__ void issue_tile(const GemvArgs& a, const GemvSrc& w, 
                                            uint8_t* st, int lane) {
     issue_meta<FMT, GTC>(a, w, mc, nb, kb, reinterpret_cast<uint32_t*>(st + TILE_BYTES), lane);
     const int bytes = (int)L.tile_bytes(kb);
-    const uint8_t* src = w.wq + L.tile_offset(nb, kb);
-    for (int off = lane * 16; off < bytes; off += 512) cp_async16(st + off, src + off);
+    const uint8_t* src = w.wq + L.tile_offset(nb, kb) + lane * 16;
+    uint8_t* dst = st + lane * 16;
+    if (bytes == TILE_BYTES) {
+#pragma unroll
+        for (int q = 0; q < TILE_BYTES / 512; ++q) cp_async16(dst + q * 512, src + q * 512);
+    } else {
+        for (int off = 0; lane * 16 + off < bytes; off += 512) cp_async16(dst + off, src + off);
+    }
     cp_async_commit_group();
 }
 
