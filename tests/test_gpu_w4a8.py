@@ -66,3 +66,15 @@ def test_w4a8_deterministic_and_kernel_count():
     assert uq.gemm_w4a8_kernel_count(1, 4096, 14336, 128, "INT4_ASYM") == 3     # + the second pass
     with pytest.raises(uq.UqError):
         uq.gemm_w4a8_kernel_count(1, 64, 256, 64, "NF4")
+
+
+@pytest.mark.parametrize("fmt,group", [("INT4_ASYM", 128), ("INT8_SYM", 128), ("INT4_SYM", 32)])
+def test_w4a8_rows_alone_and_batched(fmt, group):
+    # the integer sums are exact and the fp32 folds run in the same order for any M, so every row of
+    # a batch equals the row alone bit for bit (ragged last tile and row block included)
+    N, K, M = 300, 2 * KT[fmt] + 128, 8
+    y, _, _, (x, wq, scales, zc) = _case(fmt, group, M, N, K, seed=1800)
+    xd = device_x(x, DEV)
+    for m in range(M):
+        y1 = uq.gemm_w4a8(xd[m:m + 1].contiguous(), wq, scales, zc, N, group, fmt)
+        assert torch.equal(y1[0].view(torch.int16), y[m].view(torch.int16)), f"row {m} differs from M=1 call"
