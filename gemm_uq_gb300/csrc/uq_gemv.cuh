@@ -428,6 +428,15 @@ __host__ __device__ inline int gemv_mma_xmode(int fmt, int K, int group, int M, 
     return MMA_X_WHOLE;
 }
 
+// Pairs of compute warps that take tiles (the rest only help form the table of x sums).  Measured
+// (bench, 4 against 6 pairs, same box): INT8 8192^2 at M = 1 3060 / 3012 GB/s, the INT4 sweep at
+// M = 8 2433 / 2394 and M = 2, 4 level; NF4 1672 / 1719, K4 at M = 1 and 8 2798 / 2830 and
+// 1672 / 1747, W4A8 1911 / 2016.  With fewer pairs each holds more of the ring (3 slots of 12
+// instead of 2), which pays where a tile's compute is light; the heavier unpacks want the warps.
+__host__ __device__ inline int gemv_mma_pairs(int fmt, bool a8) {
+    return !a8 && (fmt == UQ_INT4_SYM || fmt == UQ_INT4_ASYM || fmt == UQ_INT8_SYM) ? 4 : MMA_CW / 2;
+}
+
 __device__ __forceinline__ float bf16_pair_sum(uint32_t w) {
     return __uint_as_float(w << 16) + __uint_as_float(w & 0xFFFF0000u);
 }
@@ -514,7 +523,10 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
     int kb_last = npl > 0 ? 2 * (int)((p0 + npl - 1) / (unsigned)R) + 1 : -1;
     if (kb_last > a.KB - 1) kb_last = a.KB - 1;
     const int nsx = (kb_last - kb_first + 1) * GPT;                 // table groups this CTA uses
-    const bool bad = (cta_rows && 2 * (int)npl > tpc) || nsx > sxg || S2 <= PW || R <= 0 ||
+    // pairs of compute warps that take tiles (the others only help form the table of x sums); a CTA
+    // with no more pairs than PW gives each pair to its own warp pair
+    const int PWn = (a.mma_pairs > 0 && a.mma_pairs < PW && (int)npl > PW) ? a.mma_pairs : PW;
+    const bool bad = (cta_rows && 2 * (int)npl > tpc) || nsx > sxg || S2 <= PWn || R <= 0 ||
                      (COL && M != 1);                               // never planned
     if (bad) {
         if (threadIdx.x == 0) atomicOr(a.fault, FAULT_GEMV_SPLIT);
@@ -716,15 +728,15 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
         for (int e = 0; e < 2; ++e) sxm[e] = 2 * c + e < M ? __ldg(a.sxq + 2 * c + e) : 0.f;
         xg8row = a.xq + (long long)mrow * a.Kpq + 8 * c;
     }
-    // this warp's tiles: tile hh of the pairs pl = warp / 2, warp / 2 + PW, ...; pair coordinates
-    // advanced by (PW / R, PW % R)
+    // this warp's tiles: tile hh of the pairs pl = warp / 2, warp / 2 + PWn, ...; pair coordinates
+    // advanced by (PWn / R, PWn % R)
     const int hh = warp & 1;
-    const int dq = PW / R, dr = PW % R;
+    const int dq = PWn / R, dr = PWn % R;
     int ckp = kp0, crb = rp0 + (warp >> 1);      // pair p0 + warp / 2 (warp / 2 < PW: a few steps at most)
     while (crb >= R) { crb -= R; ++ckp; }
-    int slot = warp >> 1;                        // pl % S2 (PW < S2: one wrap per step at most)
+    int slot = warp >> 1;                        // pl % S2 (PWn < S2: one wrap per step at most)
     uint32_t ph = 0;                             // (pl / S2) & 1
-    for (int pl = warp >> 1; pl < npl_w; pl += PW) {
+    for (int pl = (warp >> 1) < PWn ? warp >> 1 : npl_w; pl < npl_w; pl += PWn) {
         const int kb = 2 * ckp + hh, nbw = rb0 + crb, nb = GATED ? nbw >> 1 : nbw;
         ckp += dq;
         crb += dr;
@@ -1044,7 +1056,7 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);                   // this warp's half of the slot is free
-        slot += PW;
+        slot += PWn;
         if (slot >= S2) { slot -= S2; ph ^= 1u; }
         if (kb < a.KB) {
             // the tile's partial sums: shared memory (cta_rows; slot = the tile's index in the CTA's
@@ -1473,6 +1485,7 @@ cudaError_t launch_mma(const GemvArgs& a, int grid, int sxg, cudaStream_t st) {
     const MmaSmem plan = gemv_mma_smem(FMT, a.K, a.group, a.M, sxg, a.cta_rows, XM, A8 ? 1 : 2);
     a2.ring_slots = plan.S2;
     a2.sx_groups = sxg;
+    a2.mma_pairs = gemv_mma_pairs(FMT, A8);
     if (a2.overlap) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid);

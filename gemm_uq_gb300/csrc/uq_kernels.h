@@ -70,6 +70,7 @@ struct GemvArgs {
     int Kpq;                  //   bytes per row of xq
     int ring_slots;           // mma GEMV: ring slots and x-sum table groups of the launch (set by its launcher)
     int sx_groups;
+    int mma_pairs;            // mma GEMV: pairs of compute warps that take tiles (set by its launcher)
 };
 // formats whose GEMV runs on mma.sync (all six)
 inline bool gemv_is_mma(int fmt) {
