@@ -154,14 +154,17 @@ def test_determinism_and_batched_rows(fmt, group):
 
 
 def test_kernel_count_matches_the_paths():
-    # 14336 x 4096 at M = 1: whole row blocks per CTA, one launch; 4096 x 14336: the stream-K split
-    # (a partial-sum slot per tile) and its second pass; M >= 16: the tensor cores per 64 rows; 9..15 rows
-    # and K4: the mma.sync GEMM (a split k range adds its second pass, K4 its x column-sum pre-kernel);
-    # NF4 with a K that is not a multiple of the code tile keeps M = 20 on the GEMV: three 8-row blocks
+    # 14336 x 4096 at M = 1: whole row blocks per CTA, one launch; 4096 x 14336 too (4 tiles a warp
+    # against 3 under the split, one launch fewer); 1024 x 14336: the stream-K split (a partial-sum
+    # slot per tile) and its second pass; M >= 16: the tensor cores per 64 rows; 9..15 rows and K4:
+    # the mma.sync GEMM (a split k range adds its second pass, K4 its x column-sum pre-kernel); NF4
+    # with a K that is not a multiple of the code tile keeps M = 20 on the GEMV: three 8-row blocks
     assert uq.gemm_kernel_count(1, 14336, 4096, 128, "INT4_ASYM") == 1
     assert uq.gemm_noalloc_scratch(1, 14336, 4096, 128, "INT4_ASYM") == (0, 0)
-    assert uq.gemm_kernel_count(1, 4096, 14336, 128, "INT4_ASYM") == 2
-    assert uq.gemm_noalloc_scratch(1, 4096, 14336, 128, "INT4_ASYM") == (0, 256 * 14 * 16 * 4)
+    assert uq.gemm_kernel_count(1, 4096, 14336, 128, "INT4_ASYM") == 1
+    assert uq.gemm_noalloc_scratch(1, 4096, 14336, 128, "INT4_ASYM") == (0, 0)
+    assert uq.gemm_kernel_count(1, 1024, 14336, 128, "INT4_ASYM") == 2
+    assert uq.gemm_noalloc_scratch(1, 1024, 14336, 128, "INT4_ASYM") == (0, 64 * 14 * 16 * 4)
     # INT8 8192 x 8192 at M = 1 (512-k tiles): whole row blocks would give a CTA 64 tiles, more than
     # it holds partial sums for, so the stream-K split and its second pass
     assert uq.gemm_kernel_count(1, 8192, 8192, 128, "INT8_SYM") == 2
