@@ -46,7 +46,10 @@ int gemv_plan(GemvArgs& a, int fmt, int sms) {
     // row blocks per CTA (a.cta_rows = the most tiles a CTA gets) need no second pass; take them
     // when every compute warp has one tile at most (latency-bound shapes), or when no CTA gets more
     // tiles than under the stream-K split and the busiest CTA streams at most ~6 % more bytes than
-    // the average one.
+    // the average one, or when it gets at most 2 pairs of tiles more and all of x still fits in
+    // shared memory beside the ring (measured: the M = 2 sweep 2527 -> 2657 GB/s from its 4096 x
+    // 14336 down projection, W4A8 at M = 1 2036 -> 2101, INT2 g64 8192^2 at M = 1 1886 -> 2032,
+    // NF4 g64 1723 -> 1878; with x read through L1 instead, M = 8 lost 20 %).
     const int slots = sms;
     const long long KB2 = (a.KB + 1) / 2;
     const long long P2 = (long long)a.NB * KB2;                        // pairs of k tiles
@@ -59,7 +62,13 @@ int gemv_plan(GemvArgs& a, int fmt, int sms) {
         const long long rbs = (NBU + G - 1) / G;
         const long long tc = rbs * WU * 2 * KB2;
         const bool even = rbs * G * 100 <= (long long)NBU * 106;
-        if (tc <= MMA_TPC && (tc <= MMA_CW || (tc <= per_cta_split && even))) {
+        bool near = false;
+        if (tc <= MMA_TPC && tc > per_cta_split && tc <= per_cta_split + 4) {
+            const int sxg_rows = gemv_mma_sx_groups(fmt, a.group, a.NB, a.KB, G, (int)tc);
+            near = gemv_mma_smem(fmt, a.K, a.group, a.M, sxg_rows, (int)tc, MMA_X_WHOLE, a.a8 ? 1 : 2).S2 >=
+                   MMA_CW / 2 + 2;
+        }
+        if (tc <= MMA_TPC && (tc <= MMA_CW || (tc <= per_cta_split && even) || near)) {
             a.cta_rows = (int)tc;
             grid = G;
         }

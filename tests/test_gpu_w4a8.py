@@ -63,7 +63,10 @@ def test_w4a8_deterministic_and_kernel_count():
     y2 = uq.gemm_w4a8(device_x(x, DEV), wq, scales, zc, 1024, group, fmt)
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
     assert uq.gemm_w4a8_kernel_count(1, 14336, 4096, 128, "INT4_ASYM") == 2     # x codes + one GEMV launch
-    assert uq.gemm_w4a8_kernel_count(1, 4096, 14336, 128, "INT4_ASYM") == 3     # + the second pass
+    # 4096 x 14336: whole row blocks per CTA (x codes fit beside the ring), no second pass; at 8 rows
+    # the stream-K split and its second pass
+    assert uq.gemm_w4a8_kernel_count(1, 4096, 14336, 128, "INT4_ASYM") == 2
+    assert uq.gemm_w4a8_kernel_count(8, 4096, 14336, 128, "INT4_ASYM") == 3
     with pytest.raises(uq.UqError):
         uq.gemm_w4a8_kernel_count(1, 64, 256, 64, "NF4")
 
