@@ -24,14 +24,15 @@
 //    results are bit-reproducible, and a row's result is the same for either split and any M.
 //  * gemv_mma_kernel (every format at M = 1..8, except the case below): one CTA per SM, a copy
 //    warp feeding 12 compute warps through one ring of tile pairs (one 16 KB bulk copy per pair)
-//    in nearly all of shared memory; x whole in shared memory or read through L1; the sums of x
-//    over each scaling group in a table formed once per CTA.  INT8: the stored byte q + 128 =
+//    in nearly all of shared memory; x whole in shared memory (one row of it with the groups as
+//    columns) or read through L1; the sums of x over each scaling group in a table formed once
+//    per CTA.  INT8: the stored byte q + 128 =
 //    16 hi + lo, its two nibbles through the same bf16 magic, two mma chains per block, sum q x =
 //    16 D_hi + D_lo - 2304 sum x.  NF4: each codebook value c[q] as hi = bf16(c[q]) and lo =
 //    bf16(c[q] - hi) (16 significant bits) from a 16-entry shared table, two mma chains per block.
 //  * gemv_warp_kernel (INT4_SYM, INT4_ASYM at M = 1): the same per-tile arithmetic on per-warp
 //    rings of two stages (16-byte cp.async by each warp's own lanes) and double-buffered slices
-//    of x, two CTAs per SM.  Its launches are short, and two ~105 KB CTAs per SM let the next
+//    of x, two CTAs per SM.  Its launches are short, and two ~111 KB CTAs per SM let the next
 //    launch on the stream start streaming while the current one finishes; measured faster there.
 //    Both kernels form the sums of x in the same order, so they give the same rows.
 //    With launch overlap both request their first weights before waiting for the previous
@@ -302,8 +303,9 @@ __device__ __forceinline__ void row_meta_k4(const uint8_t* st, int r, int li, fl
 // of tiles, two consecutive k tiles of one row block (16 KB of codes, contiguous in the packed
 // plane, plus both tiles' metadata).  The copy warp requests the CTA's pairs in order: one 16 KB
 // bulk copy of the codes (lane 0) and the metadata by cp.async from all lanes, all counted on the
-// slot's "full" mbarrier.  Compute warp w takes tile w & 1 of the pairs w / 2, w / 2 + MMA_CW / 2,
-// ... and hands the slot back on its "empty" mbarrier (two arrivals per pair).  Bulk copies of
+// slot's "full" mbarrier.  Compute warp w takes tile w & 1 of the pairs w / 2, w / 2 + P, ... for
+// P tile-taking warp pairs (MMA_CW / 2, or fewer: gemv_mma_pairs) and hands the slot back on its
+// "empty" mbarrier (two arrivals per pair).  Bulk copies of
 // 16 KB keep an SM's share of HBM bandwidth streaming from a few copies in flight, where one warp
 // of 16-byte cp.async keeps about one tile in flight; the shared ring holds every tile in flight
 // once, so shared memory feeds 12 compute warps per SM instead of 8.
