@@ -186,8 +186,9 @@ __device__ __forceinline__ void issue_meta(const GemvArgs& a, const GemvSrc& w, 
         const int sv = GT / 8;                          // 16-byte vectors of scales per row
         const int zv = (FMT == UQ_INT4_ASYM) ? GT / 8 : ((FMT == UQ_INT2_ASYM) ? sv : 0);
         const int per = sv + zv;
+        const int perd = per > 0 ? per : 1;             // (no copies at all when per is 0)
         for (int e = lane; e < rows * per; e += 32) {
-            const int r = e / per, j = e % per;
+            const int r = e / perd, j = e % perd;
             const long long n = n0 + r;
             if (j < sv) {
                 cp_async16(md + r * F::MW + 4 * j, w.scales + (n * mc.G + (long long)kb * GT) * 2 + 16 * j);
@@ -466,7 +467,6 @@ __global__ void __launch_bounds__((MMA_CW + 1) * 32, 1) gemv_mma_kernel(const Ge
     constexpr int MB = MetaGeom<FMT, GPT>::META_BYTES;              // metadata bytes per tile
     constexpr int WPG = (FMT == UQ_INT2_ASYM) ? GB / 2 : (FMT == UQ_INT8_SYM ? 2 * GB : GB);   // code words per lane per group
     constexpr int BPCH = F::BPC;                                    // 16-k blocks per 512-byte chunk
-    constexpr int SPG = GS / 8;                                     // 8-k segments of x per group
     constexpr bool XS = XM != MMA_X_GLOBAL;                        // x in shared memory
     constexpr bool COL = XM == MMA_X_ROW1;                          // one row of x, groups as columns
     static_assert(!COL || (!A8 && !GATED), "the column scheme takes one plain row of x");
